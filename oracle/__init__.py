@@ -1,0 +1,191 @@
+"""fp64 CPU oracle for NCHW conv2d -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The product (``convolution_nchw_conv2d_gb300``)
+never imports it and shares no code with it.
+
+The arithmetic lives in ``conv2d_oracle.c`` (plain C, fp64, gather form,
+OpenMP over output elements).  This module only compiles it with gcc and
+marshals numpy arrays through ctypes.  Inputs of any float dtype are widened
+exactly to fp64 before the call.
+
+Citations (page titles): Apache SystemDS ``LibMatrixCuDNNConvolutionAlgorithm.java``
+(descriptor integers, NCHW / KCRS layouts, cross-correlation, dilation 1);
+Apache MXNet ``mkldnn_deconvolution.cc`` (deconvolution forward = convolution
+backward-data with the weight's in/out channel roles swapped); the C#
+``FilterDescriptor.SetFilter4dDescriptor`` examples (overwrite, alpha = 1,
+beta = 0).
+
+Parity status: all functions pinned by ``tests/test_oracle_pins.py``;
+NaN/Inf propagation is parity unpinned.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "conv2d_oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+_LIB = os.path.join(_BUILD, "liboracle_conv2d.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (-O2 -fopenmp) into ``oracle/_build``."""
+    os.makedirs(_BUILD, exist_ok=True)
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-std=c99",
+                               "-o", tmp, _SRC])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            i = ctypes.c_int
+            dp = ctypes.POINTER(ctypes.c_double)
+            ip = ctypes.POINTER(ctypes.c_int64)
+            i64 = ctypes.c_int64
+            lib.oracle_output_dim.argtypes = [i, i, i, i]
+            lib.oracle_output_dim.restype = i
+            for name in ("oracle_conv2d_fwd", "oracle_conv2d_bwd_data", "oracle_conv2d_bwd_filter"):
+                getattr(lib, name).argtypes = [dp, dp, dp] + [i] * 13
+                getattr(lib, name).restype = None
+            lib.oracle_deconv2d_fwd_scatter.argtypes = [dp, dp, dp] + [i] * 13
+            lib.oracle_deconv2d_fwd_scatter.restype = None
+            for name in ("oracle_conv2d_fwd_at", "oracle_conv2d_bwd_data_at",
+                         "oracle_conv2d_bwd_filter_at"):
+                getattr(lib, name).argtypes = [dp, dp] + [i] * 13 + [ip, i64, dp]
+                getattr(lib, name).restype = None
+            lib.oracle_num_threads.argtypes = []
+            lib.oracle_num_threads.restype = i
+            _lib = lib
+    return _lib
+
+
+def _f64(a) -> np.ndarray:
+    """Exact widening to a C-contiguous fp64 numpy array (torch tensors accepted)."""
+    if hasattr(a, "detach"):
+        a = a.detach().cpu().float().numpy() if str(a.dtype) == "torch.bfloat16" else a.detach().cpu().numpy()
+    return np.ascontiguousarray(np.asarray(a, dtype=np.float64))
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+
+
+def output_dim(inp: int, pad: int, k: int, stride: int) -> int:
+    """floor((inp + 2*pad - k)/stride) + 1, 0 if the window never fits, -1 on bad input."""
+    return _load().oracle_output_dim(inp, pad, k, stride)
+
+
+def _geom(x_shape, w_shape, pad, stride):
+    N, C, H, W = x_shape
+    K, C2, R, S = w_shape
+    assert C == C2, "channel mismatch between x and w"
+    ph, pw = pad
+    sh, sw = stride
+    P = output_dim(H, ph, R, sh)
+    Q = output_dim(W, pw, S, sw)
+    return N, C, H, W, K, R, S, ph, pw, sh, sw, P, Q
+
+
+def _pair(v):
+    return (v, v) if isinstance(v, int) else tuple(v)
+
+
+def conv2d_fwd(x, w, pad=0, stride=1) -> np.ndarray:
+    """y = cross-correlation of zero-padded x with w (NCHW, KCRS) in fp64."""
+    x, w = _f64(x), _f64(w)
+    g = _geom(x.shape, w.shape, _pair(pad), _pair(stride))
+    N, C, H, W, K, R, S, ph, pw, sh, sw, P, Q = g
+    y = np.empty((N, K, P, Q), dtype=np.float64)
+    _load().oracle_conv2d_fwd(_ptr(x), _ptr(w), _ptr(y), *g)
+    return y
+
+
+def conv2d_bwd_data(dy, w, x_hw, pad=0, stride=1) -> np.ndarray:
+    """dx (N,C,H,W) from dy (N,K,P,Q) and w (K,C,R,S); x_hw = (H, W) is explicit
+    because for stride > 1 several H give the same P."""
+    dy, w = _f64(dy), _f64(w)
+    N, K, P, Q = dy.shape
+    K2, C, R, S = w.shape
+    assert K == K2
+    H, W = x_hw
+    ph, pw = _pair(pad)
+    sh, sw = _pair(stride)
+    assert output_dim(H, ph, R, sh) == P and output_dim(W, pw, S, sw) == Q, "P/Q mismatch"
+    dx = np.empty((N, C, H, W), dtype=np.float64)
+    _load().oracle_conv2d_bwd_data(_ptr(dy), _ptr(w), _ptr(dx),
+                                   N, C, H, W, K, R, S, ph, pw, sh, sw, P, Q)
+    return dx
+
+
+def conv2d_bwd_filter(x, dy, rs, pad=0, stride=1) -> np.ndarray:
+    """dw (K,C,R,S) from x (N,C,H,W) and dy (N,K,P,Q); rs = (R, S)."""
+    x, dy = _f64(x), _f64(dy)
+    N, C, H, W = x.shape
+    N2, K, P, Q = dy.shape
+    assert N == N2
+    R, S = rs
+    ph, pw = _pair(pad)
+    sh, sw = _pair(stride)
+    assert output_dim(H, ph, R, sh) == P and output_dim(W, pw, S, sw) == Q, "P/Q mismatch"
+    dw = np.empty((K, C, R, S), dtype=np.float64)
+    _load().oracle_conv2d_bwd_filter(_ptr(x), _ptr(dy), _ptr(dw),
+                                     N, C, H, W, K, R, S, ph, pw, sh, sw, P, Q)
+    return dw
+
+
+def deconv2d_fwd_scatter(inp, wt, out_hw, pad=0, stride=1) -> np.ndarray:
+    """Transposed convolution by scatter: inp (N,Ci,Hi,Wi), wt (Ci,Co,R,S) -> (N,Co,Ho,Wo)."""
+    inp, wt = _f64(inp), _f64(wt)
+    N, Ci, Hi, Wi = inp.shape
+    Ci2, Co, R, S = wt.shape
+    assert Ci == Ci2
+    Ho, Wo = out_hw
+    ph, pw = _pair(pad)
+    sh, sw = _pair(stride)
+    out = np.empty((N, Co, Ho, Wo), dtype=np.float64)
+    _load().oracle_deconv2d_fwd_scatter(_ptr(inp), _ptr(wt), _ptr(out),
+                                        N, Ci, Hi, Wi, Co, R, S, ph, pw, sh, sw, Ho, Wo)
+    return out
+
+
+def _at(fn, a, b, dims, idx):
+    a, b = _f64(a), _f64(b)
+    idx = np.ascontiguousarray(np.asarray(idx, dtype=np.int64))
+    out = np.empty(idx.shape[0], dtype=np.float64)
+    fn(_ptr(a), _ptr(b), *dims,
+       idx.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), ctypes.c_int64(idx.shape[0]), _ptr(out))
+    return out
+
+
+def conv2d_fwd_at(x, w, dims, idx) -> np.ndarray:
+    """Forward outputs at flat (n,k,p,q) indices; dims = the 13 descriptor ints."""
+    return _at(_load().oracle_conv2d_fwd_at, x, w, dims, idx)
+
+
+def conv2d_bwd_data_at(dy, w, dims, idx) -> np.ndarray:
+    """Backward-data outputs at flat (n,c,h,w) indices."""
+    return _at(_load().oracle_conv2d_bwd_data_at, dy, w, dims, idx)
+
+
+def conv2d_bwd_filter_at(x, dy, dims, idx) -> np.ndarray:
+    """Backward-filter outputs at flat (k,c,r,s) indices."""
+    return _at(_load().oracle_conv2d_bwd_filter_at, x, dy, dims, idx)
+
+
+def num_threads() -> int:
+    """OpenMP threads the oracle's parallel loops use."""
+    return _load().oracle_num_threads()
