@@ -1,0 +1,218 @@
+"""GB300 (sm_103a) NCHW 2-D convolution: forward, backward-data, backward-filter.
+
+A thin ctypes binding over ``libconv2d_gb300.so`` (C ABI in
+``include/conv2d_gb300.h``).  The functions here only marshal torch tensors
+(device memory and the current CUDA stream) into the C calls; every step of
+the computation runs in the library's CUDA kernels.  If the library is missing
+or cannot be loaded, every call raises -- there is no fallback path.
+
+Names follow the descriptor of the Apache SystemDS cuDNN wrapper page
+(``LibMatrixCuDNNConvolutionAlgorithm.java``): N, C, H, W, K, R, S, pad_h, pad_w,
+stride_h, stride_w, P, Q.  ``deconv2d_fwd`` maps transposed convolution onto
+backward-data with the weight read as (deconv_in, deconv_out, R, S) (Apache MXNet
+``mkldnn_deconvolution.cc``, MKLDNNDeconvFwd::Execute comment).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+__all__ = [
+    "conv2d_fwd", "conv2d_bwd_data", "conv2d_bwd_filter", "deconv2d_fwd",
+    "conv2d_workspace_size", "conv2d_output_dim", "conv2d_device_status", "conv2d_strerror",
+    "Conv2dError", "lib_path", "load_library", "OP_FWD", "OP_BWD_DATA", "OP_BWD_FILTER",
+    "DTYPE_F32", "DTYPE_BF16",
+]
+
+OP_FWD, OP_BWD_DATA, OP_BWD_FILTER = 0, 1, 2
+DTYPE_F32, DTYPE_BF16 = 0, 1
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_PKG, "libconv2d_gb300.so")
+_lib = None
+_lock = threading.Lock()
+
+
+class Conv2dError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {conv2d_strerror(code)} (code {code})")
+
+
+def lib_path() -> str:
+    return _LIB_PATH
+
+
+EXPORTS = ("conv2d_output_dim", "conv2d_workspace_size", "conv2d_fwd", "conv2d_bwd_data",
+           "conv2d_bwd_filter", "conv2d_device_status", "conv2d_strerror")
+
+
+def load_library():
+    """Load the compiled library (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError(f"{_LIB_PATH} is missing: build it with "
+                               "`python -c 'import __graft_entry__ as g; g.build()'`")
+        lib = ctypes.CDLL(_LIB_PATH)
+        i, sz, vp = ctypes.c_int, ctypes.c_size_t, ctypes.c_void_p
+        lib.conv2d_output_dim.argtypes = [i, i, i, i, ctypes.POINTER(i)]
+        lib.conv2d_output_dim.restype = i
+        lib.conv2d_workspace_size.argtypes = [i] + [i] * 13 + [i, ctypes.POINTER(sz)]
+        lib.conv2d_workspace_size.restype = i
+        for name in ("conv2d_fwd", "conv2d_bwd_data", "conv2d_bwd_filter"):
+            f = getattr(lib, name)
+            f.argtypes = [i] * 13 + [i, vp, vp, vp, vp, sz, vp]
+            f.restype = i
+        lib.conv2d_device_status.argtypes = [vp]
+        lib.conv2d_device_status.restype = i
+        lib.conv2d_strerror.argtypes = [i]
+        lib.conv2d_strerror.restype = ctypes.c_char_p
+        _lib = lib
+        return lib
+
+
+def conv2d_strerror(code: int) -> str:
+    try:
+        return load_library().conv2d_strerror(code).decode()
+    except Exception:  # library missing: still describe the code
+        return f"error {code}"
+
+
+def conv2d_output_dim(inp: int, pad: int, k: int, stride: int) -> int:
+    out = ctypes.c_int(0)
+    rc = load_library().conv2d_output_dim(inp, pad, k, stride, ctypes.byref(out))
+    if rc:
+        raise Conv2dError(rc, "conv2d_output_dim")
+    return out.value
+
+
+def _pair(v):
+    return (int(v), int(v)) if isinstance(v, int) else (int(v[0]), int(v[1]))
+
+
+def _dtype_code(t) -> int:
+    import torch
+    if t.dtype == torch.float32:
+        return DTYPE_F32
+    if t.dtype == torch.bfloat16:
+        return DTYPE_BF16
+    raise TypeError(f"unsupported dtype {t.dtype}; expected float32 or bfloat16")
+
+
+def conv2d_workspace_size(op: int, dims, dtype_code: int) -> int:
+    """Workspace bytes for `op` and the 13 descriptor integers `dims`."""
+    out = ctypes.c_size_t(0)
+    rc = load_library().conv2d_workspace_size(op, *[int(v) for v in dims], dtype_code, ctypes.byref(out))
+    if rc:
+        raise Conv2dError(rc, "conv2d_workspace_size")
+    return out.value
+
+
+def _stream_ptr(stream):
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check_tensor(t, name):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous (dense NCHW / KCRS)")
+
+
+def _workspace(op, dims, dt, workspace, device):
+    import torch
+    need = conv2d_workspace_size(op, dims, dt)
+    if need == 0:
+        return None, 0
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=device)
+    if workspace.numel() * workspace.element_size() < need:
+        raise ValueError(f"workspace too small: need {need} bytes")
+    return workspace, workspace.numel() * workspace.element_size()
+
+
+def _call(name, dims, dt, a, b, out, workspace, op, stream):
+    ws, wsb = _workspace(op, dims, dt, workspace, out.device)
+    rc = getattr(load_library(), name)(*[int(v) for v in dims], dt,
+                                       ctypes.c_void_p(a.data_ptr()), ctypes.c_void_p(b.data_ptr()),
+                                       ctypes.c_void_p(out.data_ptr()),
+                                       ctypes.c_void_p(ws.data_ptr() if ws is not None else 0),
+                                       ctypes.c_size_t(wsb), _stream_ptr(stream))
+    if rc:
+        raise Conv2dError(rc, name)
+    return out
+
+
+def conv2d_fwd(x, w, pad=0, stride=1, out=None, workspace=None, stream=None):
+    """y = conv2d(x, w): x (N,C,H,W), w (K,C,R,S) -> y (N,K,P,Q), same dtype."""
+    import torch
+    _check_tensor(x, "x")
+    _check_tensor(w, "w")
+    N, C, H, W = x.shape
+    K, C2, R, S = w.shape
+    if C2 != C or w.dtype != x.dtype:
+        raise ValueError("x / w channel count or dtype mismatch")
+    ph, pw = _pair(pad)
+    sh, sw = _pair(stride)
+    P, Q = conv2d_output_dim(H, ph, R, sh), conv2d_output_dim(W, pw, S, sw)
+    if out is None:
+        out = torch.empty((N, K, P, Q), dtype=x.dtype, device=x.device)
+    dims = (N, C, H, W, K, R, S, ph, pw, sh, sw, P, Q)
+    return _call("conv2d_fwd", dims, _dtype_code(x), x, w, out, workspace, OP_FWD, stream)
+
+
+def conv2d_bwd_data(dy, w, x_hw, pad=0, stride=1, out=None, workspace=None, stream=None):
+    """dx (N,C,H,W) from dy (N,K,P,Q) and w (K,C,R,S); x_hw = (H, W)."""
+    import torch
+    _check_tensor(dy, "dy")
+    _check_tensor(w, "w")
+    N, K, P, Q = dy.shape
+    K2, C, R, S = w.shape
+    if K2 != K or w.dtype != dy.dtype:
+        raise ValueError("dy / w channel count or dtype mismatch")
+    H, W = x_hw
+    ph, pw = _pair(pad)
+    sh, sw = _pair(stride)
+    if out is None:
+        out = torch.empty((N, C, H, W), dtype=dy.dtype, device=dy.device)
+    dims = (N, C, H, W, K, R, S, ph, pw, sh, sw, P, Q)
+    return _call("conv2d_bwd_data", dims, _dtype_code(dy), dy, w, out, workspace, OP_BWD_DATA, stream)
+
+
+def conv2d_bwd_filter(x, dy, rs, pad=0, stride=1, out=None, workspace=None, stream=None):
+    """dw (K,C,R,S) from x (N,C,H,W) and dy (N,K,P,Q); rs = (R, S)."""
+    import torch
+    _check_tensor(x, "x")
+    _check_tensor(dy, "dy")
+    N, C, H, W = x.shape
+    N2, K, P, Q = dy.shape
+    if N2 != N or dy.dtype != x.dtype:
+        raise ValueError("x / dy batch or dtype mismatch")
+    R, S = rs
+    ph, pw = _pair(pad)
+    sh, sw = _pair(stride)
+    if out is None:
+        out = torch.empty((K, C, R, S), dtype=x.dtype, device=x.device)
+    dims = (N, C, H, W, K, R, S, ph, pw, sh, sw, P, Q)
+    return _call("conv2d_bwd_filter", dims, _dtype_code(x), x, dy, out, workspace, OP_BWD_FILTER, stream)
+
+
+def deconv2d_fwd(inp, wt, out_hw, pad=0, stride=1, out=None, workspace=None, stream=None):
+    """Transposed convolution: inp (N,Ci,Hi,Wi), wt (Ci,Co,R,S) -> (N,Co,Ho,Wo).
+
+    Runs conv2d_bwd_data with K = Ci (deconv input channels), C = Co, P = Hi, H = Ho."""
+    return conv2d_bwd_data(inp, wt, out_hw, pad, stride, out=out, workspace=workspace, stream=stream)
+
+
+def conv2d_device_status(stream=None) -> int:
+    """Synchronize the stream; raise if a kernel's bounded wait expired or the stream failed."""
+    rc = load_library().conv2d_device_status(_stream_ptr(stream))
+    if rc:
+        raise Conv2dError(rc, "conv2d_device_status")
+    return 0

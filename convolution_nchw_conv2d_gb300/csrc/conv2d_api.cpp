@@ -1,0 +1,637 @@
+// conv2d_api.cpp -- the C ABI (include/conv2d_gb300.h): descriptor validation,
+// planning of the implicit-GEMM launches, workspace sizing and launch on the
+// caller's stream.  No device memory is allocated here; nothing throws.
+#include "conv2d_gb300.h"
+
+#include <algorithm>
+#include <climits>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include <cuda_runtime.h>
+
+#include "conv_plan.h"
+
+namespace cg3 {
+cudaError_t launch_tap_gemm(const TapPlan& p, int dt, int grid, cudaStream_t st);
+cudaError_t launch_pack_filter(const PackPlan& pp, int dt, cudaStream_t st);
+size_t tap_gemm_smem_bytes(const TapPlan& p);
+cudaError_t launch_wgrad(const WgradPlan& p, int dt, int grid, cudaStream_t st);
+cudaError_t launch_wgrad_reduce(const ReducePlan& rp, int dt, int num_sms, cudaStream_t st);
+size_t wgrad_smem_bytes(const WgradPlan& p);
+int tap_gemm_take_error();
+int wgrad_take_error();
+}  // namespace cg3
+
+using namespace cg3;
+
+namespace {
+
+constexpr size_t kWorkspaceCap = 1000000000ull;  // 1e9 bytes
+constexpr int kDefaultSMs = 152;                  // used when no device can be queried
+constexpr size_t kDefaultSmemOptin = 232448;      // 227 KB
+
+struct Desc {
+  int N, C, H, W, K, R, S, ph, pw, sh, sw, P, Q, dt;
+};
+
+int floor_div(int a, int b) { return a >= 0 ? a / b : -((-a + b - 1) / b); }
+int ceil_div_i(int a, int b) { return -floor_div(-a, b); }
+int round_up(int a, int b) { return (a + b - 1) / b * b; }
+
+int out_dim(int in, int pad, int k, int stride) {
+  const int num = in + 2 * pad - k;
+  if (num < 0) return 0;
+  return num / stride + 1;
+}
+
+int validate(const Desc& d) {
+  if (d.N <= 0 || d.C <= 0 || d.H <= 0 || d.W <= 0 || d.K <= 0 || d.R <= 0 || d.S <= 0 || d.ph < 0 ||
+      d.pw < 0 || d.sh < 1 || d.sw < 1)
+    return CONV2D_ERR_BAD_DESC;
+  if (d.dt != CONV2D_DTYPE_F32 && d.dt != CONV2D_DTYPE_BF16) return CONV2D_ERR_DTYPE;
+  // Overflow-safe: the sums below are bounded by 2^31 + 2^31.
+  const long long P = out_dim(d.H, d.ph, d.R, d.sh), Q = out_dim(d.W, d.pw, d.S, d.sw);
+  if (P < 1 || Q < 1 || d.P != P || d.Q != Q) return CONV2D_ERR_SHAPE;
+  const long long lim = (1ll << 31);
+  if ((long long)d.N * d.C * d.H * d.W >= lim || (long long)d.N * d.K * d.P * d.Q >= lim ||
+      (long long)d.K * d.C * d.R * d.S >= lim)
+    return CONV2D_ERR_TOO_LARGE;
+  if (d.R * d.S > kMaxTaps || d.sh * d.sw > kMaxPlanes) return CONV2D_ERR_UNSUPPORTED;
+  return CONV2D_OK;
+}
+
+struct DevInfo {
+  int sms = kDefaultSMs;
+  size_t smem_optin = kDefaultSmemOptin;
+  bool ok = false;  // an sm_100-family device is current
+};
+
+std::mutex g_dev_mu;
+std::vector<DevInfo> g_dev_cache;
+std::vector<char> g_dev_known;
+
+DevInfo device_info() {
+  DevInfo di;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) {
+    cudaGetLastError();
+    return di;
+  }
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  if ((size_t)dev < g_dev_known.size() && g_dev_known[dev]) return g_dev_cache[dev];
+  int major = 0, sms = 0, smem = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) == cudaSuccess &&
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess &&
+      cudaDeviceGetAttribute(&smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) == cudaSuccess) {
+    di.sms = sms;
+    di.smem_optin = (size_t)smem;
+    di.ok = (major == 10);
+  } else {
+    cudaGetLastError();
+  }
+  if ((size_t)dev >= g_dev_known.size()) {
+    g_dev_known.resize(dev + 1, 0);
+    g_dev_cache.resize(dev + 1);
+  }
+  g_dev_cache[dev] = di;
+  g_dev_known[dev] = 1;
+  return di;
+}
+
+// ------------------------------------------------------------------ tap plans
+struct TapBuild {
+  TapPlan p;
+  PackPlan pp;
+  size_t pack_bytes;
+  int grid;
+};
+
+// Chooses MH, NT, CB, ACCB and the stage count for a TapPlan whose geometry (linear
+// space, planes, phases, taps) is already filled in.  Returns false if nothing fits.
+bool choose_tap_tiles(TapPlan& p, int max_off, int dt, const DevInfo& di, bool pair_taps) {
+  const int CHUNK = dt == 0 ? 4 : 8;
+  const size_t budget = di.smem_optin - 2048;
+  int nt_cands[2];
+  int nnt = 0;
+  if (p.Cd <= 256) {
+    nt_cands[nnt++] = round_up(p.Cd, 16);
+  } else {
+    nt_cands[nnt++] = 256;
+    nt_cands[nnt++] = 128;
+  }
+  int cb_cands[4];
+  int ncand = 0;
+  if (pair_taps) {
+    cb_cands[ncand++] = CHUNK;
+  } else {
+    const int cmax = round_up(p.Cs, 2 * CHUNK);
+    for (int cb : {16 * CHUNK, 8 * CHUNK, 4 * CHUNK, 2 * CHUNK})
+      if (cb <= cmax || cb == 2 * CHUNK) cb_cands[ncand++] = cb;
+  }
+  for (int ni = 0; ni < nnt; ++ni) {
+    const int NT = nt_cands[ni];
+    const int n_ntiles = (p.Cd + NT - 1) / NT;
+    for (int mh = 2; mh >= 1; --mh) {
+      const long long mtiles = (p.Mtot + 128ll * mh - 1) / (128ll * mh);
+      // Small problems: prefer more, smaller tiles so that every SM gets work.
+      if (mh == 2 && mtiles * n_ntiles * p.nph < di.sms) continue;
+      for (int ci = 0; ci < ncand; ++ci) {
+        const int CB = cb_cands[ci];
+        const int NCH = CB / CHUNK;
+        const int rows = round_up(128 * mh + max_off + (pair_taps ? 1 : 0), 8);
+        const long long a_bytes = (long long)p.npl * NCH * rows * 16;
+        const long long b_bytes = (long long)p.max_taps_ph * NCH * NT * 16;
+        const long long fixed = (long long)p.npl * rows * 4 + 8 * (3 * 4 + 5) + 16 + 1024;
+        const long long per = a_bytes + b_bytes;
+        long long stages = ((long long)budget - fixed) / per;
+        if (stages < 2) continue;
+        if (stages > 4) stages = 4;
+        if (b_bytes >= (1 << 20)) continue;  // mbarrier transaction-count limit
+        p.NT = NT;
+        p.n_ntiles = n_ntiles;
+        p.MH = mh;
+        p.CB = CB;
+        p.rows = rows;
+        p.a_stage_bytes = (int)a_bytes;
+        p.b_stage_bytes = (int)b_bytes;
+        p.stages = (int)stages;
+        p.ACCB = (2 * mh * NT <= 512) ? 2 : 1;
+        p.tmem_cols = 32;
+        while (p.tmem_cols < p.ACCB * mh * NT) p.tmem_cols <<= 1;
+        p.nkb = (p.Cs + CB - 1) / CB;
+        p.n_mtiles = (int)mtiles;
+        p.total_tiles = (long long)p.nph * p.n_mtiles * p.n_ntiles;
+        if (tap_gemm_smem_bytes(p) <= di.smem_optin) return true;
+      }
+    }
+  }
+  return false;
+}
+
+void fill_pack(TapBuild& b, const Desc& d, const void* w, void* wpack, int transpose,
+               const std::vector<int>& tr, const std::vector<int>& ts) {
+  PackPlan& pp = b.pp;
+  std::memset(&pp, 0, sizeof(pp));
+  pp.w = w;
+  pp.wpack = wpack;
+  pp.K = d.K;
+  pp.C = d.C;
+  pp.R = d.R;
+  pp.S = d.S;
+  pp.transpose = transpose;
+  pp.Cd = b.p.Cd;
+  pp.Cs = b.p.Cs;
+  pp.n_ntiles = b.p.n_ntiles;
+  pp.nkb = b.p.nkb;
+  pp.ntaps_total = b.p.ntaps_total;
+  pp.NT = b.p.NT;
+  pp.CB = b.p.CB;
+  for (int t = 0; t < b.p.ntaps_total; ++t) {
+    pp.tap_r[t] = tr[t];
+    pp.tap_s[t] = ts[t];
+  }
+  const int CHUNK = d.dt == 0 ? 4 : 8;
+  b.pack_bytes = (size_t)b.p.n_ntiles * b.p.nkb * b.p.ntaps_total * (b.p.CB / CHUNK) * b.p.NT * 16;
+}
+
+// Sort one phase's taps by staged address and, when taps are paired, pad to an even
+// count with a zero-weight tap (weight coordinates -1) placed at the last real tap.
+void order_phase_taps(std::vector<int>& pl, std::vector<int>& off, std::vector<int>& tr,
+                      std::vector<int>& ts, int begin, int rows_hint, bool pair) {
+  const int n = (int)pl.size() - begin;
+  std::vector<int> idx(n);
+  for (int i = 0; i < n; ++i) idx[i] = begin + i;
+  std::stable_sort(idx.begin(), idx.end(), [&](int a, int b) {
+    const long long ka = (long long)pl[a] * rows_hint + off[a];
+    const long long kb = (long long)pl[b] * rows_hint + off[b];
+    return ka < kb;
+  });
+  std::vector<int> npl(n), noff(n), ntr(n), nts(n);
+  for (int i = 0; i < n; ++i) {
+    npl[i] = pl[idx[i]];
+    noff[i] = off[idx[i]];
+    ntr[i] = tr[idx[i]];
+    nts[i] = ts[idx[i]];
+  }
+  for (int i = 0; i < n; ++i) {
+    pl[begin + i] = npl[i];
+    off[begin + i] = noff[i];
+    tr[begin + i] = ntr[i];
+    ts[begin + i] = nts[i];
+  }
+  if (pair && (n & 1)) {
+    pl.push_back(pl.back());
+    off.push_back(off.back());
+    tr.push_back(-1);
+    ts.push_back(-1);
+  }
+}
+
+int build_fwd(const Desc& d, const void* x, const void* w, void* y, void* ws, const DevInfo& di,
+              TapBuild& b) {
+  TapPlan& p = b.p;
+  std::memset(&p, 0, sizeof(p));
+  p.src = x;
+  p.dst = y;
+  p.N = d.N;
+  p.Cs = d.C;
+  p.Hs = d.H;
+  p.Ws = d.W;
+  p.Cd = d.K;
+  p.Hd = d.P;
+  p.Wd = d.Q;
+  const int mh = (d.R - 1) / d.sh, mw = (d.S - 1) / d.sw;
+  p.WL = d.Q + mw;
+  p.EL = d.P + mh;
+  p.Mtot = (long long)d.N * p.EL * p.WL;
+  p.npl = d.sh * d.sw;
+  p.pl_step_h = d.sh;
+  p.pl_step_w = d.sw;
+  for (int a = 0; a < d.sh; ++a)
+    for (int bb = 0; bb < d.sw; ++bb) {
+      p.pl_off_h[a * d.sw + bb] = a - d.ph;
+      p.pl_off_w[a * d.sw + bb] = bb - d.pw;
+    }
+  p.nph = 1;
+  p.ph_step_h = 1;
+  p.ph_step_w = 1;
+  const int CHUNK = d.dt == 0 ? 4 : 8;
+  const bool pair = d.C <= CHUNK;
+  std::vector<int> tpl, toff, tr, ts;
+  int max_off = 0;
+  for (int r = 0; r < d.R; ++r)
+    for (int s = 0; s < d.S; ++s) {
+      tpl.push_back((r % d.sh) * d.sw + (s % d.sw));
+      toff.push_back((r / d.sh) * p.WL + s / d.sw);
+      tr.push_back(r);
+      ts.push_back(s);
+      max_off = std::max(max_off, toff.back());
+    }
+  order_phase_taps(tpl, toff, tr, ts, 0, 1 << 20, pair);
+  p.ntaps_total = (int)tpl.size();
+  if (p.ntaps_total > kMaxTaps) return CONV2D_ERR_UNSUPPORTED;
+  p.ph_tap_begin[0] = 0;
+  p.ph_ntaps[0] = p.ntaps_total;
+  p.max_taps_ph = p.ntaps_total;
+  for (int t = 0; t < p.ntaps_total; ++t) {
+    p.tap_plane[t] = tpl[t];
+    p.tap_off[t] = toff[t];
+  }
+  if (!choose_tap_tiles(p, max_off, d.dt, di, pair)) return CONV2D_ERR_UNSUPPORTED;
+  p.wpack = ws;
+  fill_pack(b, d, w, ws, 0, tr, ts);
+  b.grid = (int)std::min<long long>(p.total_tiles, di.sms);
+  return CONV2D_OK;
+}
+
+int build_bwd_data(const Desc& d, const void* dy, const void* w, void* dx, void* ws, const DevInfo& di,
+                   TapBuild& b) {
+  TapPlan& p = b.p;
+  std::memset(&p, 0, sizeof(p));
+  p.src = dy;
+  p.dst = dx;
+  p.N = d.N;
+  p.Cs = d.K;
+  p.Hs = d.P;
+  p.Ws = d.Q;
+  p.Cd = d.C;
+  p.Hd = d.H;
+  p.Wd = d.W;
+  // Per output phase a (rows with (h + pad_h) mod stride_h == a): taps r = a + sh*t,
+  // output row h = sh*u + a - pad_h, dy row p = u - t.  Same for columns.
+  auto phase_dims = [](int H, int pad, int R, int st, std::vector<int>& T, std::vector<int>& ulo,
+                       std::vector<int>& U) {
+    T.assign(st, 0);
+    ulo.assign(st, 0);
+    U.assign(st, 0);
+    for (int a = 0; a < st; ++a) {
+      int cnt = 0;
+      for (int r = a; r < R; r += st) ++cnt;
+      T[a] = cnt;
+      ulo[a] = ceil_div_i(pad - a, st);
+      const int uhi = floor_div(H - 1 + pad - a, st);
+      U[a] = std::max(0, uhi - ulo[a] + 1);
+    }
+  };
+  std::vector<int> Th, uloh, Uh, Tw, ulow, Uw;
+  phase_dims(d.H, d.ph, d.R, d.sh, Th, uloh, Uh);
+  phase_dims(d.W, d.pw, d.S, d.sw, Tw, ulow, Uw);
+  int T0h = 0, T0w = 0;
+  for (int a = 0; a < d.sh; ++a)
+    if (Th[a] > 0) T0h = std::max(T0h, Th[a] - 1 - uloh[a]);
+  for (int c = 0; c < d.sw; ++c)
+    if (Tw[c] > 0) T0w = std::max(T0w, Tw[c] - 1 - ulow[c]);
+  int EL = 1, WL = 1;
+  for (int a = 0; a < d.sh; ++a) {
+    EL = std::max(EL, Uh[a]);
+    if (Th[a] > 0) EL = std::max(EL, Uh[a] + uloh[a] + T0h);
+  }
+  for (int c = 0; c < d.sw; ++c) {
+    WL = std::max(WL, Uw[c]);
+    if (Tw[c] > 0) WL = std::max(WL, Uw[c] + ulow[c] + T0w);
+  }
+  p.WL = WL;
+  p.EL = EL;
+  p.Mtot = (long long)d.N * EL * WL;
+  p.npl = 1;
+  p.pl_step_h = 1;
+  p.pl_step_w = 1;
+  p.pl_off_h[0] = -T0h;
+  p.pl_off_w[0] = -T0w;
+  p.nph = d.sh * d.sw;
+  p.ph_step_h = d.sh;
+  p.ph_step_w = d.sw;
+  const int CHUNK = d.dt == 0 ? 4 : 8;
+  const bool pair = d.K <= CHUNK;
+  std::vector<int> tpl, toff, tr, ts;
+  int max_off = 0, max_taps = 0;
+  for (int a = 0; a < d.sh; ++a)
+    for (int c = 0; c < d.sw; ++c) {
+      const int ph = a * d.sw + c;
+      p.ph_off_h[ph] = d.sh * uloh[a] + a - d.ph;
+      p.ph_off_w[ph] = d.sw * ulow[c] + c - d.pw;
+      const int begin = (int)tpl.size();
+      p.ph_tap_begin[ph] = begin;
+      for (int t = 0; t < Th[a]; ++t)
+        for (int t2 = 0; t2 < Tw[c]; ++t2) {
+          const int roff = uloh[a] - t + T0h;
+          const int coff = ulow[c] - t2 + T0w;
+          tpl.push_back(0);
+          toff.push_back(roff * WL + coff);
+          tr.push_back(a + d.sh * t);
+          ts.push_back(c + d.sw * t2);
+          max_off = std::max(max_off, toff.back());
+        }
+      if ((int)tpl.size() > begin) order_phase_taps(tpl, toff, tr, ts, begin, 1 << 20, pair);
+      p.ph_ntaps[ph] = (int)tpl.size() - begin;
+      max_taps = std::max(max_taps, p.ph_ntaps[ph]);
+    }
+  p.ntaps_total = (int)tpl.size();
+  if (p.ntaps_total > kMaxTaps) return CONV2D_ERR_UNSUPPORTED;
+  p.max_taps_ph = std::max(1, max_taps);
+  for (int t = 0; t < p.ntaps_total; ++t) {
+    p.tap_plane[t] = tpl[t];
+    p.tap_off[t] = toff[t];
+  }
+  if (!choose_tap_tiles(p, max_off, d.dt, di, pair)) return CONV2D_ERR_UNSUPPORTED;
+  p.wpack = ws;
+  fill_pack(b, d, w, ws, 1, tr, ts);
+  if (p.ntaps_total == 0) b.pack_bytes = 0;
+  b.grid = (int)std::min<long long>(p.total_tiles, di.sms);
+  return CONV2D_OK;
+}
+
+// ------------------------------------------------------------------ wgrad plan
+struct WgradBuild {
+  WgradPlan p;
+  ReducePlan rp;
+  size_t partial_bytes;
+  int grid;
+};
+
+int build_bwd_filter(const Desc& d, const void* x, const void* dy, void* dw, void* ws, const DevInfo& di,
+                     WgradBuild& b) {
+  WgradPlan& p = b.p;
+  std::memset(&p, 0, sizeof(p));
+  p.x = x;
+  p.dy = dy;
+  p.partial = static_cast<float*>(ws);
+  p.N = d.N;
+  p.C = d.C;
+  p.H = d.H;
+  p.W = d.W;
+  p.K = d.K;
+  p.P = d.P;
+  p.Q = d.Q;
+  const int mh = (d.R - 1) / d.sh, mw = (d.S - 1) / d.sw;
+  p.WL = d.Q + mw;
+  p.EL = d.P + mh;
+  p.Mtot = (long long)d.N * p.EL * p.WL;
+  p.npl = d.sh * d.sw;
+  p.pl_step_h = d.sh;
+  p.pl_step_w = d.sw;
+  for (int a = 0; a < d.sh; ++a)
+    for (int c = 0; c < d.sw; ++c) {
+      p.pl_off_h[a * d.sw + c] = a - d.ph;
+      p.pl_off_w[a * d.sw + c] = c - d.pw;
+    }
+  p.ntaps = d.R * d.S;
+  int max_off = 0;
+  for (int r = 0; r < d.R; ++r)
+    for (int s = 0; s < d.S; ++s) {
+      const int t = r * d.S + s;
+      p.tap_plane[t] = (r % d.sh) * d.sw + (s % d.sw);
+      p.tap_off[t] = (r / d.sh) * p.WL + s / d.sw;
+      max_off = std::max(max_off, p.tap_off[t]);
+    }
+  const int CHUNK = d.dt == 0 ? 4 : 8;
+  const int ESZ = d.dt == 0 ? 4 : 2;
+  const int abuf_cols = 32;
+  int NC = round_up(d.C, 16);
+  if (NC > 32) NC = (p.ntaps <= 15) ? 32 : 16;
+  p.NC = NC;
+  p.tap_group_size = std::min(p.ntaps, (512 - abuf_cols) / NC);
+  p.n_tgroups = (p.ntaps + p.tap_group_size - 1) / p.tap_group_size;
+  p.tmem_cols = 32;
+  while (p.tmem_cols < abuf_cols + p.tap_group_size * NC) p.tmem_cols <<= 1;
+  p.n_ktiles = (d.K + 127) / 128;
+  p.n_ctiles = (d.C + NC - 1) / NC;
+  p.k_pad = d.K;
+  p.c_pad = d.C;
+  const size_t budget = di.smem_optin - 2048;
+  bool fitted = false;
+  for (int KB : {128, 64, 32, 16}) {
+    if (KB % (2 * CHUNK)) continue;
+    const int rows = round_up(KB + max_off, 8);
+    const long long a_bytes = (long long)KB * 128 * ESZ;
+    const long long b_bytes = (long long)p.npl * (NC / CHUNK) * rows * 16;
+    const long long fixed = (long long)(KB + p.npl * rows) * 4 + 8 * (2 * 4 + 3) + 16 + 1024;
+    long long stages = ((long long)budget - fixed) / (a_bytes + b_bytes);
+    if (stages < 2) continue;
+    if (stages > 4) stages = 4;
+    p.KB = KB;
+    p.rows = rows;
+    p.a_stage_bytes = (int)a_bytes;
+    p.b_stage_bytes = (int)b_bytes;
+    p.stages = (int)stages;
+    fitted = wgrad_smem_bytes(p) <= di.smem_optin;
+    if (fitted) break;
+  }
+  if (!fitted) return CONV2D_ERR_UNSUPPORTED;
+  const long long base = (long long)p.n_ktiles * p.n_ctiles * p.n_tgroups;
+  long long want = std::max<long long>(1, (di.sms + base - 1) / base);
+  const long long stage_count = (p.Mtot + p.KB - 1) / p.KB;
+  want = std::min(want, stage_count);
+  const size_t per_split = (size_t)p.ntaps * p.c_pad * p.k_pad * sizeof(float);
+  while (want > 1 && per_split * (size_t)want > kWorkspaceCap) --want;
+  long long slen = (p.Mtot + want - 1) / want;
+  slen = (slen + p.KB - 1) / p.KB * p.KB;
+  p.split_len = slen;
+  p.nsplit = (int)((p.Mtot + slen - 1) / slen);
+  p.total_tiles = base * p.nsplit;
+  b.partial_bytes = per_split * (size_t)p.nsplit;
+  if (b.partial_bytes > kWorkspaceCap) return CONV2D_ERR_UNSUPPORTED;
+  ReducePlan& rp = b.rp;
+  rp.partial = p.partial;
+  rp.dw = dw;
+  rp.K = d.K;
+  rp.C = d.C;
+  rp.R = d.R;
+  rp.S = d.S;
+  rp.nsplit = p.nsplit;
+  rp.k_pad = p.k_pad;
+  rp.c_pad = p.c_pad;
+  b.grid = (int)std::min<long long>(p.total_tiles, di.sms);
+  return CONV2D_OK;
+}
+
+int check_ptrs(const void* a, const void* b, const void* c, int dt) {
+  if (!a || !b || !c) return CONV2D_ERR_NULLPTR;
+  const uintptr_t m = dt == CONV2D_DTYPE_F32 ? 3 : 1;
+  if (((uintptr_t)a & m) || ((uintptr_t)b & m) || ((uintptr_t)c & m)) return CONV2D_ERR_ALIGN;
+  return CONV2D_OK;
+}
+
+int check_ws(void* ws, size_t have, size_t need) {
+  if (need == 0) return CONV2D_OK;
+  if (!ws) return CONV2D_ERR_NULLPTR;
+  if ((uintptr_t)ws & 15) return CONV2D_ERR_ALIGN;
+  if (have < need) return CONV2D_ERR_WORKSPACE;
+  return CONV2D_OK;
+}
+
+int launch_err(cudaError_t e) {
+  if (e == cudaSuccess) return CONV2D_OK;
+  cudaGetLastError();
+  return CONV2D_ERR_LAUNCH;
+}
+
+}  // namespace
+
+extern "C" {
+
+int conv2d_output_dim(int in, int pad, int k, int stride, int* out) {
+  if (!out || in <= 0 || k <= 0 || pad < 0 || stride < 1) return CONV2D_ERR_BAD_DESC;
+  const int v = out_dim(in, pad, k, stride);
+  if (v < 1) return CONV2D_ERR_SHAPE;
+  *out = v;
+  return CONV2D_OK;
+}
+
+int conv2d_workspace_size(int op, int N, int C, int H, int W, int K, int R, int S, int pad_h, int pad_w,
+                          int stride_h, int stride_w, int P, int Q, int dtype, size_t* bytes) {
+  if (!bytes) return CONV2D_ERR_NULLPTR;
+  const Desc d{N, C, H, W, K, R, S, pad_h, pad_w, stride_h, stride_w, P, Q, dtype};
+  int rc = validate(d);
+  if (rc) return rc;
+  const DevInfo di = device_info();
+  if (op == CONV2D_OP_FWD || op == CONV2D_OP_BWD_DATA) {
+    TapBuild b;
+    rc = op == CONV2D_OP_FWD ? build_fwd(d, nullptr, nullptr, nullptr, nullptr, di, b)
+                             : build_bwd_data(d, nullptr, nullptr, nullptr, nullptr, di, b);
+    if (rc) return rc;
+    *bytes = b.pack_bytes;
+    return CONV2D_OK;
+  }
+  if (op == CONV2D_OP_BWD_FILTER) {
+    WgradBuild b;
+    rc = build_bwd_filter(d, nullptr, nullptr, nullptr, nullptr, di, b);
+    if (rc) return rc;
+    *bytes = b.partial_bytes;
+    return CONV2D_OK;
+  }
+  return CONV2D_ERR_BAD_OP;
+}
+
+static int run_tap(int op, const Desc& d, const void* src, const void* w, void* dst, void* ws, size_t wsb,
+                   void* stream) {
+  int rc = validate(d);
+  if (rc) return rc;
+  rc = check_ptrs(src, w, dst, d.dt);
+  if (rc) return rc;
+  const DevInfo di = device_info();
+  if (!di.ok) return CONV2D_ERR_DEVICE;
+  TapBuild b;
+  rc = op == CONV2D_OP_FWD ? build_fwd(d, src, w, dst, ws, di, b) : build_bwd_data(d, src, w, dst, ws, di, b);
+  if (rc) return rc;
+  rc = check_ws(ws, wsb, b.pack_bytes);
+  if (rc) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (b.pack_bytes) {
+    rc = launch_err(launch_pack_filter(b.pp, d.dt, st));
+    if (rc) return rc;
+  }
+  return launch_err(launch_tap_gemm(b.p, d.dt, b.grid, st));
+}
+
+int conv2d_fwd(int N, int C, int H, int W, int K, int R, int S, int pad_h, int pad_w, int stride_h,
+               int stride_w, int P, int Q, int dtype, const void* x, const void* w, void* y, void* workspace,
+               size_t workspace_bytes, void* stream) {
+  const Desc d{N, C, H, W, K, R, S, pad_h, pad_w, stride_h, stride_w, P, Q, dtype};
+  return run_tap(CONV2D_OP_FWD, d, x, w, y, workspace, workspace_bytes, stream);
+}
+
+int conv2d_bwd_data(int N, int C, int H, int W, int K, int R, int S, int pad_h, int pad_w, int stride_h,
+                    int stride_w, int P, int Q, int dtype, const void* dy, const void* w, void* dx,
+                    void* workspace, size_t workspace_bytes, void* stream) {
+  const Desc d{N, C, H, W, K, R, S, pad_h, pad_w, stride_h, stride_w, P, Q, dtype};
+  return run_tap(CONV2D_OP_BWD_DATA, d, dy, w, dx, workspace, workspace_bytes, stream);
+}
+
+int conv2d_bwd_filter(int N, int C, int H, int W, int K, int R, int S, int pad_h, int pad_w, int stride_h,
+                      int stride_w, int P, int Q, int dtype, const void* x, const void* dy, void* dw,
+                      void* workspace, size_t workspace_bytes, void* stream) {
+  const Desc d{N, C, H, W, K, R, S, pad_h, pad_w, stride_h, stride_w, P, Q, dtype};
+  int rc = validate(d);
+  if (rc) return rc;
+  rc = check_ptrs(x, dy, dw, d.dt);
+  if (rc) return rc;
+  const DevInfo di = device_info();
+  if (!di.ok) return CONV2D_ERR_DEVICE;
+  WgradBuild b;
+  rc = build_bwd_filter(d, x, dy, dw, workspace, di, b);
+  if (rc) return rc;
+  rc = check_ws(workspace, workspace_bytes, b.partial_bytes);
+  if (rc) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  rc = launch_err(launch_wgrad(b.p, d.dt, b.grid, st));
+  if (rc) return rc;
+  return launch_err(launch_wgrad_reduce(b.rp, d.dt, di.sms, st));
+}
+
+int conv2d_device_status(void* stream) {
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(st) != cudaSuccess) {
+    cudaGetLastError();
+    return CONV2D_ERR_LAUNCH;
+  }
+  const int a = tap_gemm_take_error();
+  const int b = wgrad_take_error();
+  if (a < 0 || b < 0) return CONV2D_ERR_LAUNCH;
+  if (a || b) return CONV2D_ERR_DEVICE_TIMEOUT;
+  return CONV2D_OK;
+}
+
+const char* conv2d_strerror(int code) {
+  switch (code) {
+    case CONV2D_OK: return "success";
+    case CONV2D_ERR_BAD_DESC: return "bad descriptor: a dimension <= 0, pad < 0 or stride < 1";
+    case CONV2D_ERR_SHAPE: return "P/Q differ from floor((H+2*pad-R)/stride)+1, or are < 1";
+    case CONV2D_ERR_NULLPTR: return "NULL tensor or workspace pointer";
+    case CONV2D_ERR_ALIGN: return "misaligned pointer";
+    case CONV2D_ERR_DTYPE: return "unknown dtype";
+    case CONV2D_ERR_WORKSPACE: return "workspace smaller than conv2d_workspace_size()";
+    case CONV2D_ERR_TOO_LARGE: return "a tensor has 2^31 or more elements";
+    case CONV2D_ERR_LAUNCH: return "CUDA launch or stream error";
+    case CONV2D_ERR_DEVICE: return "no sm_100-family CUDA device is current";
+    case CONV2D_ERR_DEVICE_TIMEOUT: return "a kernel's bounded pipeline wait expired";
+    case CONV2D_ERR_UNSUPPORTED: return "unsupported geometry (R*S > 64, stride_h*stride_w > 16, or no tile fits)";
+    case CONV2D_ERR_BAD_OP: return "unknown op";
+    default: return "unknown error code";
+  }
+}
+
+}  // extern "C"

@@ -1,0 +1,431 @@
+// conv_wgrad.cu -- backward-filter convolution on sm_103a tensor cores.
+//
+//   dw[k,c,r,s] = sum_{n,p,q} X(n, c, p*sh - ph + r, q*sw - pw + s) * dy[n,k,p,q]
+// (the filter gradient of the cuDNN backward-filter call in Apache SystemDS
+// LibMatrixCuDNNConvolutionAlgorithm.java; deconvolution's backward-weights in
+// Apache MXNet mkldnn_deconvolution.cc is the same product with the weight's roles
+// swapped).  The reduction runs over the forward linear position space L (see
+// conv_plan.h): dy is zero at positions with no output, and tap (r,s) reads the x
+// phase plane of (r mod sh, s mod sw) at L + tap_off.
+//
+// One CTA tile = 128 output channels k x NC input channels c x a group of taps x one
+// range of positions (split-K).  Per pipeline stage (KB positions):
+//   producers (warps 0-3) stage dy[k, L] K-major and x[c, L + off] in the
+//     core-matrix layout (read as MN-major: c along chunks, positions along rows);
+//   the MMA lane copies each 128 x 32-byte dy slice into TMEM with tcgen05.cp and
+//     issues one tcgen05.mma per tap with A from TMEM and B = x at the tap's row
+//     offset, so dy is read from shared memory once for all taps;
+//   epilogue warps (4-7) write each tap's 128 x NC fp32 partial sums.
+// A second kernel adds the split partials in a fixed order (deterministic) and
+// writes dw in KCRS, rounding to bf16 for bf16 tensors.
+#include "conv_plan.h"
+#include "sm103_ptx.cuh"
+
+namespace cg3 {
+
+__device__ int g_wgrad_err;
+
+namespace {
+constexpr int kThreads = 288;
+constexpr int kProdThreads = 128;
+constexpr int kAbufCols = 32;  // 4 TMEM staging buffers of 8 columns for dy slices
+
+__device__ __forceinline__ uint32_t bar_at(uint32_t base, int i) { return base + 8u * (uint32_t)i; }
+
+struct WTile {
+  int kt, ct, tg, sp;
+};
+__device__ __forceinline__ WTile decode_wtile(const WgradPlan& p, long long t) {
+  WTile w;
+  w.kt = (int)(t % p.n_ktiles);
+  long long r = t / p.n_ktiles;
+  w.ct = (int)(r % p.n_ctiles);
+  r /= p.n_ctiles;
+  w.tg = (int)(r % p.n_tgroups);
+  w.sp = (int)(r / p.n_tgroups);
+  return w;
+}
+}  // namespace
+
+template <int DT>
+__global__ void __launch_bounds__(kThreads, 1) wgrad_kernel(const __grid_constant__ WgradPlan p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  constexpr int ESZ = DT == 0 ? 4 : 2;
+  constexpr int CHUNK = 16 / ESZ;
+  constexpr int KIND = DT;
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const int S = p.stages;
+  const int rows = p.rows;
+  const int KB = p.KB;
+  const int NCA = KB / CHUNK;     // dy chunks per stage
+  const int NCB = p.NC / CHUNK;   // x chunks per plane per stage
+
+  uint8_t* ptr = smem_raw;
+  const uint32_t a0 = smem_u32(ptr);
+  ptr += (size_t)S * p.a_stage_bytes;
+  const uint32_t b0 = smem_u32(ptr);
+  ptr += (size_t)S * p.b_stage_bytes;
+  int* dytab = reinterpret_cast<int*>(ptr);
+  ptr += (size_t)KB * sizeof(int);
+  int* xtab = reinterpret_cast<int*>(ptr);
+  ptr += (size_t)p.npl * rows * sizeof(int);
+  ptr = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(ptr) + 15) & ~uintptr_t(15));
+  const uint32_t full = smem_u32(ptr);
+  const uint32_t empty = full + 8u * S;
+  const uint32_t accf = empty + 8u * S;
+  const uint32_t acce = accf + 8u;
+  const uint32_t drain = acce + 8u;
+  ptr += 8 * (2 * S + 3);
+  volatile uint32_t* tmem_holder = reinterpret_cast<volatile uint32_t*>(ptr);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(ptr + 4);
+
+  if (tid == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(bar_at(full, s), kProdThreads);
+      mbar_init(bar_at(empty, s), 1);
+    }
+    mbar_init(accf, 1);
+    mbar_init(acce, 4);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 8) {
+    tmem_alloc(smem_u32((const void*)tmem_holder), (uint32_t)p.tmem_cols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+
+  const long long img = (long long)p.EL * p.WL;
+  const long long HW = (long long)p.H * p.W;
+  const long long PQ = (long long)p.P * p.Q;
+
+  if (warp < 4) {
+    // =============================================================== producers
+    int stage = 0;
+    uint32_t ephase = 0;
+    int pending = -1;
+    bool ok = true;
+    for (long long t = blockIdx.x; t < p.total_tiles && ok; t += gridDim.x) {
+      const WTile wt = decode_wtile(p, t);
+      const long long lbeg = (long long)wt.sp * p.split_len;
+      long long lend = lbeg + p.split_len;
+      if (lend > p.Mtot) lend = p.Mtot;
+      const int kbase = wt.kt * 128;
+      const int cbase = wt.ct * p.NC;
+      for (long long l0 = lbeg; l0 < lend; l0 += KB) {
+        // Position tables for this stage.
+        named_bar_sync(1, kProdThreads);
+        for (int i = tid; i < KB + p.npl * rows; i += kProdThreads) {
+          if (i < KB) {
+            const long long L = l0 + i;
+            int off = -1;
+            if (L < lend) {
+              const int n = (int)(L / img);
+              const int rem = (int)(L - (long long)n * img);
+              const int e = rem / p.WL;
+              const int f = rem - e * p.WL;
+              if (e < p.P && f < p.Q) off = (int)((long long)n * p.K * PQ + (long long)e * p.Q + f);
+            }
+            dytab[i] = off;
+          } else {
+            const int j = i - KB;
+            const int pl = j / rows;
+            const int row = j - pl * rows;
+            const long long L = l0 + row;
+            int off = -1;
+            if (L < p.Mtot) {
+              const int n = (int)(L / img);
+              const int rem = (int)(L - (long long)n * img);
+              const int e = rem / p.WL;
+              const int f = rem - e * p.WL;
+              const int h = e * p.pl_step_h + p.pl_off_h[pl];
+              const int w = f * p.pl_step_w + p.pl_off_w[pl];
+              if (h >= 0 && h < p.H && w >= 0 && w < p.W)
+                off = (int)((long long)n * p.C * HW + (long long)h * p.W + w);
+            }
+            xtab[j] = off;
+          }
+        }
+        named_bar_sync(1, kProdThreads);
+        if (!mbar_wait(bar_at(empty, stage), ephase ^ 1u, abort_flag, &g_wgrad_err)) {
+          ok = false;
+          break;
+        }
+        const uint32_t a_st = a0 + (uint32_t)stage * p.a_stage_bytes;
+        const uint32_t b_st = b0 + (uint32_t)stage * p.b_stage_bytes;
+        if constexpr (DT == 0) {
+          const float* dy = static_cast<const float*>(p.dy);
+          const float* x = static_cast<const float*>(p.x);
+          const int e4 = lane & 3;
+          const int rsub = lane >> 2;
+          // dy: chunk j holds positions 4j..4j+3 of 128 k rows: [j][k][4 x fp32]
+          for (int j = 0; j < NCA; ++j) {
+            const int off = dytab[j * 4 + e4];
+            const uint32_t dbase = a_st + (uint32_t)(j * 128) * 16u + (uint32_t)e4 * 4u;
+#pragma unroll
+            for (int kg = warp; kg < 16; kg += 4) {
+              const int kr = kg * 8 + rsub;
+              const int k = kbase + kr;
+              const bool v = off >= 0 && k < p.K;
+              cp_async_4(dbase + (uint32_t)kr * 16u, v ? dy + off + (long long)k * PQ : dy, v);
+            }
+          }
+          // x: [plane][chunk][row][4 channels]
+          for (int pj = 0; pj < p.npl * NCB; ++pj) {
+            const int pl = pj / NCB;
+            const int j = pj - pl * NCB;
+            const int c = cbase + j * 4 + e4;
+            const bool cv = c < p.C;
+            const float* gc = x + (long long)(cv ? c : 0) * HW;
+            const uint32_t dbase = b_st + (uint32_t)(pj * rows) * 16u + (uint32_t)e4 * 4u;
+            const int* tab = xtab + pl * rows;
+#pragma unroll 4
+            for (int row = warp * 8 + rsub; row < rows; row += 32) {
+              const int off = tab[row];
+              const bool v = cv && off >= 0;
+              cp_async_4(dbase + (uint32_t)row * 16u, v ? gc + off : x, v);
+            }
+          }
+          cp_async_commit();
+          if (pending >= 0) {
+            cp_async_wait<1>();
+            fence_proxy_async();
+            mbar_arrive(bar_at(full, pending));
+          }
+          pending = stage;
+        } else {
+          const uint16_t* dy = static_cast<const uint16_t*>(p.dy);
+          const uint16_t* x = static_cast<const uint16_t*>(p.x);
+          // dy: thread -> (chunk j, k row); 8 positions of one k.
+          for (int i = tid; i < NCA * 128; i += kProdThreads) {
+            const int j = i >> 7;
+            const int kr = i & 127;
+            const int k = kbase + kr;
+            uint32_t wv[4] = {0u, 0u, 0u, 0u};
+            if (k < p.K) {
+              const uint16_t* gk = dy + (long long)k * PQ;
+#pragma unroll
+              for (int e = 0; e < 8; ++e) {
+                const int off = dytab[j * 8 + e];
+                if (off >= 0) wv[e >> 1] |= (uint32_t)__ldg(gk + off) << (16 * (e & 1));
+              }
+            }
+            asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(a_st + (uint32_t)i * 16u),
+                         "r"(wv[0]), "r"(wv[1]), "r"(wv[2]), "r"(wv[3])
+                         : "memory");
+          }
+          // x: thread -> (plane, chunk, row); 8 channels of one position.
+          for (int pj = 0; pj < p.npl * NCB; ++pj) {
+            const int pl = pj / NCB;
+            const int j = pj - pl * NCB;
+            const int c0 = cbase + j * 8;
+            const int nv = min(8, p.C - c0);
+            const uint16_t* gc = x + (long long)(nv > 0 ? c0 : 0) * HW;
+            const int* tab = xtab + pl * rows;
+            const uint32_t dbase = b_st + (uint32_t)(pj * rows) * 16u;
+#pragma unroll 2
+            for (int row = tid; row < rows; row += kProdThreads) {
+              const int off = tab[row];
+              uint32_t wv[4] = {0u, 0u, 0u, 0u};
+              if (off >= 0) {
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                  if (e < nv) wv[e >> 1] |= (uint32_t)__ldg(gc + off + (long long)e * HW) << (16 * (e & 1));
+              }
+              asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(dbase + (uint32_t)row * 16u),
+                           "r"(wv[0]), "r"(wv[1]), "r"(wv[2]), "r"(wv[3])
+                           : "memory");
+            }
+          }
+          fence_proxy_async();
+          mbar_arrive(bar_at(full, stage));
+        }
+        if (++stage == S) {
+          stage = 0;
+          ephase ^= 1u;
+        }
+      }
+    }
+    if constexpr (DT == 0) {
+      cp_async_wait<0>();
+      if (pending >= 0 && ok) {
+        fence_proxy_async();
+        mbar_arrive(bar_at(full, pending));
+      }
+    }
+  } else if (warp < 8) {
+    // =============================================================== epilogue
+    const int q = warp & 3;
+    uint32_t aphase = 0;
+    for (long long t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
+      const WTile wt = decode_wtile(p, t);
+      if (!mbar_wait(accf, aphase, abort_flag, &g_wgrad_err)) break;
+      tc_fence_after();
+      const int k = wt.kt * 128 + q * 32 + lane;
+      const int tap0 = wt.tg * p.tap_group_size;
+      const int ntg = min(p.tap_group_size, p.ntaps - tap0);
+      for (int ti = 0; ti < ntg; ++ti) {
+        float* dst = p.partial + ((long long)wt.sp * p.ntaps + tap0 + ti) * p.c_pad * (long long)p.k_pad;
+        for (int c0 = 0; c0 < p.NC; c0 += 16) {
+          uint32_t r[16];
+          tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(kAbufCols + ti * p.NC + c0), r);
+          tmem_ld_wait();
+          if (k < p.K) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const int c = wt.ct * p.NC + c0 + j;
+              if (c < p.C) dst[(long long)c * p.k_pad + k] = __uint_as_float(r[j]);
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acce);
+      aphase ^= 1u;
+    }
+  } else {
+    // =============================================================== MMA issuer
+    if (lane == 0) {
+      const uint32_t id = idesc(KIND, 128, p.NC, 0, 1);
+      int stage = 0;
+      uint32_t fphase = 0;
+      uint32_t aphase = 0;
+      int abuf = 0;
+      bool ok = true;
+      bool issued_any = false;
+      const int KSTEP = 2 * CHUNK;  // positions per MMA
+      for (long long t = blockIdx.x; t < p.total_tiles && ok; t += gridDim.x) {
+        const WTile wt = decode_wtile(p, t);
+        const long long lbeg = (long long)wt.sp * p.split_len;
+        long long lend = lbeg + p.split_len;
+        if (lend > p.Mtot) lend = p.Mtot;
+        const int tap0 = wt.tg * p.tap_group_size;
+        const int ntg = min(p.tap_group_size, p.ntaps - tap0);
+        if (!mbar_wait(acce, aphase ^ 1u, abort_flag, &g_wgrad_err)) break;
+        tc_fence_after();
+        bool first = true;
+        for (long long l0 = lbeg; l0 < lend; l0 += KB) {
+          if (!mbar_wait(bar_at(full, stage), fphase, abort_flag, &g_wgrad_err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          fence_proxy_async();
+          const uint32_t a_st = a0 + (uint32_t)stage * p.a_stage_bytes;
+          const uint32_t b_st = b0 + (uint32_t)stage * p.b_stage_bytes;
+          for (int ks = 0; ks < NCA / 2; ++ks) {
+            const uint32_t a_tm = tmem + (uint32_t)(abuf * 8);
+            tmem_cp_128x256b(a_tm, sdesc(a_st + (uint32_t)(2 * ks * 128) * 16u, 128u * 16u, 128u));
+            if (++abuf == kAbufCols / 8) abuf = 0;
+            for (int ti = 0; ti < ntg; ++ti) {
+              const int tap = tap0 + ti;
+              const uint32_t bst = b_st + (uint32_t)(p.tap_plane[tap] * NCB * rows) * 16u +
+                                   (uint32_t)(ks * KSTEP + p.tap_off[tap]) * 16u;
+              const uint64_t bd = sdesc(bst, 128u, (uint32_t)rows * 16u);
+              mma_ts<KIND>(tmem + (uint32_t)(kAbufCols + ti * p.NC), a_tm, bd, id, first ? 0u : 1u);
+            }
+            first = false;
+          }
+          tc_commit(bar_at(empty, stage));
+          issued_any = true;
+          if (++stage == S) {
+            stage = 0;
+            fphase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        tc_commit(accf);
+        aphase ^= 1u;
+      }
+      if (!ok && issued_any) {
+        tc_commit(drain);
+        mbar_wait_drain(drain, 0);
+      }
+    }
+    __syncwarp();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 8) {
+    tc_fence_after();
+    tmem_dealloc(tmem, (uint32_t)p.tmem_cols);
+  }
+}
+
+// Sum the split partials in split order and write dw (KCRS).  One thread per
+// (tap, c, k) with k fastest, so partial reads are coalesced.
+template <int DT>
+__global__ void wgrad_reduce_kernel(const __grid_constant__ ReducePlan rp) {
+  const int RS = rp.R * rp.S;
+  const long long total = (long long)RS * rp.C * rp.K;
+  const long long split_stride = (long long)RS * rp.c_pad * rp.k_pad;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
+       i += (long long)gridDim.x * blockDim.x) {
+    const int k = (int)(i % rp.K);
+    long long r = i / rp.K;
+    const int c = (int)(r % rp.C);
+    const int tap = (int)(r / rp.C);
+    const float* src = rp.partial + ((long long)tap * rp.c_pad + c) * rp.k_pad + k;
+    float acc = 0.f;
+    for (int s = 0; s < rp.nsplit; ++s) acc += src[s * split_stride];
+    const long long o = ((long long)k * rp.C + c) * RS + tap;
+    if constexpr (DT == 0)
+      static_cast<float*>(rp.dw)[o] = acc;
+    else
+      static_cast<__nv_bfloat16*>(rp.dw)[o] = __float2bfloat16_rn(acc);
+  }
+}
+
+size_t wgrad_smem_bytes(const WgradPlan& p) {
+  size_t b = (size_t)p.stages * (p.a_stage_bytes + p.b_stage_bytes);
+  b += (size_t)(p.KB + p.npl * p.rows) * sizeof(int);
+  b = (b + 15) & ~size_t(15);
+  b += 8 * (2 * p.stages + 3) + 16;
+  return b + 1024;
+}
+
+cudaError_t launch_wgrad(const WgradPlan& p, int dt, int grid, cudaStream_t st) {
+  const size_t smem = wgrad_smem_bytes(p);
+  cudaError_t e;
+  if (dt == 0) {
+    e = cudaFuncSetAttribute(wgrad_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    wgrad_kernel<0><<<grid, kThreads, smem, st>>>(p);
+  } else {
+    e = cudaFuncSetAttribute(wgrad_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    wgrad_kernel<1><<<grid, kThreads, smem, st>>>(p);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_wgrad_reduce(const ReducePlan& rp, int dt, int num_sms, cudaStream_t st) {
+  const long long total = (long long)rp.R * rp.S * rp.C * rp.K;
+  long long blocks = (total + 255) / 256;
+  const long long cap = (long long)num_sms * 8;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  if (dt == 0)
+    wgrad_reduce_kernel<0><<<(int)blocks, 256, 0, st>>>(rp);
+  else
+    wgrad_reduce_kernel<1><<<(int)blocks, 256, 0, st>>>(rp);
+  return cudaGetLastError();
+}
+
+int wgrad_take_error() {
+  int v = 0, zero = 0;
+  if (cudaMemcpyFromSymbol(&v, g_wgrad_err, sizeof(int)) != cudaSuccess) return -1;
+  if (v != 0) cudaMemcpyToSymbol(g_wgrad_err, &zero, sizeof(int));
+  return v;
+}
+
+}  // namespace cg3

@@ -1,0 +1,137 @@
+/*
+ * conv2d_gb300.h -- C ABI of the GB300 (sm_103a) NCHW 2-D convolution library.
+ *
+ * Three operations of dense 2-D cross-correlation with zero padding and stride,
+ * described by the thirteen integers N, C, H, W, K, R, S, pad_h, pad_w, stride_h,
+ * stride_w, P, Q in the order of the cuDNN wrapper factory methods of Apache
+ * SystemDS (page "LibMatrixCuDNNConvolutionAlgorithm.java",
+ * cudnnGetConvolutionForwardAlgorithm / ...BackwardFilterAlgorithm /
+ * ...BackwardDataAlgorithm parameter lists):
+ *
+ *   x  : N x C x H x W   (NCHW, dense, row-major)        "nchwTensorDesc"
+ *   w  : K x C x R x S   (KCRS, dense, row-major)        "filterDesc"
+ *   y  : N x K x P x Q   (dense, row-major)              "nkpqTensorDesc"
+ *   P  = floor((H + 2*pad_h - R) / stride_h) + 1,  Q likewise with W, pad_w, S, stride_w
+ *   X(n,c,h,w) = x[n,c,h,w] inside the image, 0 outside (zero padding)
+ *
+ *   forward          y[n,k,p,q]  = sum_{c,r,s} X(n,c,p*stride_h-pad_h+r,q*stride_w-pad_w+s) * w[k,c,r,s]
+ *   backward-data    dx[n,c,h,w] = sum over (k,r,s,p,q) with h = p*stride_h-pad_h+r and
+ *                                  w = q*stride_w-pad_w+s of dy[n,k,p,q] * w[k,c,r,s]
+ *   backward-filter  dw[k,c,r,s] = sum_{n,p,q} X(n,c,p*stride_h-pad_h+r,q*stride_w-pad_w+s) * dy[n,k,p,q]
+ *
+ * The mode is cross-correlation with dilation 1 (same page,
+ * allocateConvolutionDescriptor: CUDNN_CROSS_CORRELATION, dilation 1,1).  Outputs
+ * are overwritten, never accumulated: alpha = 1, beta = 0 as in the ConvolutionForward
+ * / ConvolutionBackwardData / ConvolutionBackwardFilter calls of the C# examples page
+ * ("FilterDescriptor.SetFilter4dDescriptor" examples: Conv2D, DoConvolutionGradient).
+ *
+ * Transposed convolution (deconvolution) forward is conv2d_bwd_data with the weight
+ * read as (deconv_in, deconv_out, R, S) = (K, C, R, S): deconv input = dy (N,K,P,Q),
+ * deconv output = dx (N,C,H,W).  Its backward-data is conv2d_fwd and its
+ * backward-weights is conv2d_bwd_filter with x = deconv output gradient and
+ * dy = deconv input (page "mkldnn_deconvolution.cc", MKLDNNDeconvFwd::Execute comment).
+ * H and W are explicit arguments because for stride > 1 several H give the same P.
+ *
+ * Data types (page "mkldnn_deconvolution.cc", SupportMKLDNNDeconv: float32 or bfloat16):
+ *   CONV2D_DTYPE_F32   fp32 tensors; products on TF32 tensor cores, fp32 accumulation.
+ *   CONV2D_DTYPE_BF16  bf16 tensors; bf16 products, fp32 accumulation, bf16 output
+ *                      rounded to nearest even.
+ *
+ * Memory, streams, ownership:
+ *   - All tensor pointers are DEVICE pointers owned by the caller, aligned to the
+ *     element size.  Inputs are read-only.  Outputs must not alias inputs.
+ *   - `workspace` is caller-owned device memory of at least the size reported by
+ *     conv2d_workspace_size() for the same op and descriptor, 16-byte aligned.  The
+ *     size never exceeds 1e9 bytes (the workspace cap of the SystemDS wrapper,
+ *     MAX_WORKSPACE_LIMIT_BYTES).  Forward and backward-data stage a repacked copy of
+ *     the filter there; backward-filter stages split partial sums.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls only enqueue
+ *     work on it and return; the library allocates no device memory, keeps no
+ *     pointer after returning and holds no per-call state.  Results are
+ *     deterministic run to run.
+ *
+ * Errors: every function returns CONV2D_OK (0) or a negative code; nothing throws or
+ * aborts.  Argument errors are detected on the host before anything is enqueued.
+ * A kernel whose internal pipeline wait exceeds its time limit (about one second)
+ * stops early and records CONV2D_ERR_DEVICE_TIMEOUT, which conv2d_device_status()
+ * reports.
+ */
+#ifndef CONV2D_GB300_H
+#define CONV2D_GB300_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum {
+    CONV2D_DTYPE_F32 = 0,
+    CONV2D_DTYPE_BF16 = 1
+};
+
+enum {
+    CONV2D_OP_FWD = 0,
+    CONV2D_OP_BWD_DATA = 1,
+    CONV2D_OP_BWD_FILTER = 2
+};
+
+enum {
+    CONV2D_OK = 0,
+    CONV2D_ERR_BAD_DESC = -1,       /* a dimension <= 0, pad < 0 or stride < 1 */
+    CONV2D_ERR_SHAPE = -2,          /* P or Q differs from the formula, or is < 1 */
+    CONV2D_ERR_NULLPTR = -3,        /* a tensor pointer (or a needed workspace) is NULL */
+    CONV2D_ERR_ALIGN = -4,          /* a pointer is not aligned as documented above */
+    CONV2D_ERR_DTYPE = -5,          /* unknown dtype */
+    CONV2D_ERR_WORKSPACE = -6,      /* workspace_bytes below conv2d_workspace_size() */
+    CONV2D_ERR_TOO_LARGE = -7,      /* a tensor has >= 2^31 elements */
+    CONV2D_ERR_LAUNCH = -8,         /* the CUDA runtime rejected a launch */
+    CONV2D_ERR_DEVICE = -9,         /* no usable sm_100-family device */
+    CONV2D_ERR_DEVICE_TIMEOUT = -10,/* a kernel's bounded internal wait expired */
+    CONV2D_ERR_UNSUPPORTED = -11,   /* R*S > 64 or stride_h*stride_w > 16 */
+    CONV2D_ERR_BAD_OP = -12         /* unknown op in conv2d_workspace_size() */
+};
+
+/* Output extent of one spatial dimension: *out = floor((in + 2*pad - k)/stride) + 1.
+ * Returns CONV2D_ERR_BAD_DESC for in, k <= 0, pad < 0, stride < 1 or a NULL out, and
+ * CONV2D_ERR_SHAPE when the padded input is shorter than the filter. */
+int conv2d_output_dim(int in, int pad, int k, int stride, int *out);
+
+/* Bytes of device workspace `op` needs for this descriptor and dtype (<= 1e9).
+ * Validates the descriptor exactly as the op itself does. */
+int conv2d_workspace_size(int op, int N, int C, int H, int W, int K, int R, int S,
+                          int pad_h, int pad_w, int stride_h, int stride_w, int P, int Q,
+                          int dtype, size_t *bytes);
+
+/* Forward: y (N,K,P,Q) = conv(x (N,C,H,W), w (K,C,R,S)). */
+int conv2d_fwd(int N, int C, int H, int W, int K, int R, int S,
+               int pad_h, int pad_w, int stride_h, int stride_w, int P, int Q, int dtype,
+               const void *x, const void *w, void *y,
+               void *workspace, size_t workspace_bytes, void *stream);
+
+/* Backward-data (= deconvolution forward): dx (N,C,H,W) from dy (N,K,P,Q) and w (K,C,R,S).
+ * Every element of dx is written; elements no output window reads are 0. */
+int conv2d_bwd_data(int N, int C, int H, int W, int K, int R, int S,
+                    int pad_h, int pad_w, int stride_h, int stride_w, int P, int Q, int dtype,
+                    const void *dy, const void *w, void *dx,
+                    void *workspace, size_t workspace_bytes, void *stream);
+
+/* Backward-filter: dw (K,C,R,S) from x (N,C,H,W) and dy (N,K,P,Q). */
+int conv2d_bwd_filter(int N, int C, int H, int W, int K, int R, int S,
+                      int pad_h, int pad_w, int stride_h, int stride_w, int P, int Q, int dtype,
+                      const void *x, const void *dy, void *dw,
+                      void *workspace, size_t workspace_bytes, void *stream);
+
+/* Synchronizes `stream`, then reports CONV2D_ERR_DEVICE_TIMEOUT if any kernel of this
+ * library hit its bounded-wait limit since the previous call (and clears the record),
+ * CONV2D_ERR_LAUNCH if the stream reports a CUDA error, else CONV2D_OK. */
+int conv2d_device_status(void *stream);
+
+/* Static description of an error code. */
+const char *conv2d_strerror(int code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CONV2D_GB300_H */

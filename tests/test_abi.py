@@ -1,0 +1,123 @@
+"""C-ABI checks that need no GPU: the library loads, exports every symbol the header
+declares, validates descriptors on the host, sizes workspaces, and links no vendor
+convolution/GEMM library."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import oracle
+from convolution_nchw_conv2d_gb300 import workloads as W
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "conv2d_gb300.h")
+
+
+@pytest.fixture(scope="module")
+def cg():
+    import __graft_entry__
+    __graft_entry__.build()
+    import convolution_nchw_conv2d_gb300 as m
+    return m
+
+
+def _declared():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^\s*(?:const\s+char\s*\*|int)\s*(conv2d_\w+)\s*\(", text, re.M)))
+
+
+def test_header_declares_the_abi():
+    names = _declared()
+    for n in ("conv2d_fwd", "conv2d_bwd_data", "conv2d_bwd_filter", "conv2d_workspace_size",
+              "conv2d_output_dim", "conv2d_strerror", "conv2d_device_status"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(cg):
+    lib = ctypes.CDLL(cg.lib_path())
+    for n in _declared():
+        assert hasattr(lib, n), n
+    out = subprocess.run(["nm", "-D", "--defined-only", cg.lib_path()], capture_output=True, text=True).stdout
+    for n in _declared():
+        assert re.search(rf"\bT {n}\b", out), n
+
+
+def test_no_vendor_conv_or_gemm_library_linked(cg):
+    out = subprocess.run(["nm", "-D", cg.lib_path()], capture_output=True, text=True).stdout.lower()
+    deps = subprocess.run(["ldd", cg.lib_path()], capture_output=True, text=True).stdout.lower()
+    for bad in ("cudnn", "cublas", "dnnl", "mkldnn"):
+        assert bad not in out and bad not in deps
+
+
+def test_output_dim_matches_oracle(cg):
+    for inp in range(1, 40):
+        for pad in range(0, 4):
+            for k in range(1, 8):
+                for st in range(1, 4):
+                    want = oracle.output_dim(inp, pad, k, st)
+                    if want >= 1:
+                        assert cg.conv2d_output_dim(inp, pad, k, st) == want
+                    else:
+                        with pytest.raises(cg.Conv2dError):
+                            cg.conv2d_output_dim(inp, pad, k, st)
+
+
+def _ws(cg, op, dims, dt=0):
+    lib = cg.load_library()
+    out = ctypes.c_size_t(0)
+    rc = lib.conv2d_workspace_size(op, *dims, dt, ctypes.byref(out))
+    return rc, out.value
+
+
+GOOD = (2, 3, 8, 8, 4, 3, 3, 1, 1, 1, 1, 8, 8)
+
+
+@pytest.mark.parametrize("bad,code", [
+    ((0, 3, 8, 8, 4, 3, 3, 1, 1, 1, 1, 8, 8), -1),    # N = 0
+    ((2, 3, 8, 8, 4, 3, 3, -1, 1, 1, 1, 8, 8), -1),   # negative pad
+    ((2, 3, 8, 8, 4, 3, 3, 1, 1, 0, 1, 8, 8), -1),    # stride 0
+    ((2, 3, 8, 8, 4, 3, 3, 1, 1, 1, 1, 7, 8), -2),    # P mismatch
+    ((2, 3, 2, 8, 4, 5, 3, 0, 1, 1, 1, 0, 8), -2),    # no output rows
+    ((65536, 256, 256, 256, 4, 3, 3, 1, 1, 1, 1, 256, 256), -7),  # too large
+    ((2, 3, 80, 80, 4, 9, 9, 1, 1, 1, 1, 74, 74), -11),  # R*S > 64
+])
+def test_descriptor_errors(cg, bad, code):
+    for op in (0, 1, 2):
+        rc, _ = _ws(cg, op, bad)
+        assert rc == code
+    lib = cg.load_library()
+    dummy = ctypes.c_void_p(0x1000)
+    for fn in (lib.conv2d_fwd, lib.conv2d_bwd_data, lib.conv2d_bwd_filter):
+        assert fn(*bad, 0, dummy, dummy, dummy, None, 0, None) == code
+
+
+def test_bad_dtype_and_op(cg):
+    assert _ws(cg, 0, GOOD, dt=7)[0] == -5
+    assert _ws(cg, 9, GOOD)[0] == -12
+    lib = cg.load_library()
+    assert lib.conv2d_workspace_size(0, *GOOD, 0, None) == -3
+
+
+def test_null_and_misaligned_pointers(cg):
+    lib = cg.load_library()
+    p = ctypes.c_void_p(0x10000)
+    odd = ctypes.c_void_p(0x10002)
+    for fn in (lib.conv2d_fwd, lib.conv2d_bwd_data, lib.conv2d_bwd_filter):
+        assert fn(*GOOD, 0, None, p, p, None, 0, None) == -3
+        assert fn(*GOOD, 0, odd, p, p, None, 0, None) == -4
+
+
+def test_workspace_sizes_are_bounded(cg):
+    for wl in W.WORKLOADS.values():
+        pb = wl.problem
+        dt = 0 if pb.dtype == "f32" else 1
+        for op in (0, 1, 2):
+            rc, n = _ws(cg, op, pb.dims(), dt)
+            assert rc == 0 and 0 < n <= 1_000_000_000 and n % 16 == 0
+
+
+def test_strerror_covers_codes(cg):
+    for c in range(0, -13, -1):
+        assert cg.conv2d_strerror(c) and "unknown error" not in cg.conv2d_strerror(c)

@@ -1,0 +1,196 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 CPU oracle.
+
+Tolerances (fixed by the workload definition):
+  fp32 tensors (TF32 tensor cores): max|err| <= 2e-3 * sqrt(L) * max|a| * max|b|, with
+      a, b the op's two inputs and L its reduction length: C*R*S (forward),
+      K*R*S (backward-data) and N*P*Q (backward-filter).  The literal C*R*S form is
+      reported but only enforced for the forward op.
+  bf16 tensors: ||err||_2 / ||ref||_2 <= 1e-2, the oracle run on the bf16 inputs.
+Every output is pre-filled with NaN, so an element the kernels fail to write fails
+the test; a second run must reproduce the first bit for bit.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from convolution_nchw_conv2d_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module")
+def cg():
+    import convolution_nchw_conv2d_gb300 as m
+    m.load_library()
+    return m
+
+
+def _poisoned(shape, dtype):
+    return torch.full(shape, float("nan"), dtype=dtype, device=DEV)
+
+
+def _run(cg, op, pb, x, w, dy):
+    pad, st = (pb.pad_h, pb.pad_w), (pb.stride_h, pb.stride_w)
+    if op == "fwd":
+        out = _poisoned(pb.y_shape, x.dtype)
+        cg.conv2d_fwd(x, w, pad, st, out=out)
+    elif op == "bwd_data":
+        out = _poisoned(pb.x_shape, x.dtype)
+        cg.conv2d_bwd_data(dy, w, (pb.H, pb.W), pad, st, out=out)
+    else:
+        out = _poisoned(pb.w_shape, x.dtype)
+        cg.conv2d_bwd_filter(x, dy, (pb.R, pb.S), pad, st, out=out)
+    cg.conv2d_device_status()
+    return out
+
+
+def _red_len(op, pb):
+    return {"fwd": pb.C * pb.R * pb.S, "bwd_data": pb.K * pb.R * pb.S, "bwd_filter": pb.N * pb.P * pb.Q}[op]
+
+
+def _operands(op, x, w, dy):
+    return {"fwd": (x, w), "bwd_data": (dy, w), "bwd_filter": (x, dy)}[op]
+
+
+def _oracle_full(op, pb, x, w, dy):
+    pad, st = (pb.pad_h, pb.pad_w), (pb.stride_h, pb.stride_w)
+    if op == "fwd":
+        return oracle.conv2d_fwd(x, w, pad, st)
+    if op == "bwd_data":
+        return oracle.conv2d_bwd_data(dy, w, (pb.H, pb.W), pad, st)
+    return oracle.conv2d_bwd_filter(x, dy, (pb.R, pb.S), pad, st)
+
+
+def _oracle_at(op, pb, x, w, dy, idx):
+    if op == "fwd":
+        return oracle.conv2d_fwd_at(x, w, pb.dims(), idx)
+    if op == "bwd_data":
+        return oracle.conv2d_bwd_data_at(dy, w, pb.dims(), idx)
+    return oracle.conv2d_bwd_filter_at(x, dy, pb.dims(), idx)
+
+
+def _check(op, pb, got, ref, a, b, what):
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    assert np.all(np.isfinite(got)), f"{what}: non-finite output (unwritten element?)"
+    err = np.abs(got - ref)
+    amax = float(a.abs().max()) if a.numel() else 0.0
+    bmax = float(b.abs().max()) if b.numel() else 0.0
+    if pb.dtype == "f32":
+        tol = 2e-3 * math.sqrt(_red_len(op, pb)) * amax * bmax
+        assert err.max(initial=0.0) <= tol, f"{what}: max|err| {err.max():.3e} > {tol:.3e}"
+        if op == "fwd":
+            lit = 2e-3 * math.sqrt(pb.C * pb.R * pb.S) * amax * bmax
+            assert err.max(initial=0.0) <= lit
+    else:
+        den = float(np.linalg.norm(ref))
+        rel = float(np.linalg.norm(got - ref)) / den if den > 0 else float(np.linalg.norm(got))
+        assert rel <= 1e-2, f"{what}: relative-to-norm error {rel:.3e} > 1e-2"
+
+
+def _sample_indices(n, rng, count, shape):
+    """Random flat indices plus the first/last elements along every axis edge."""
+    idx = set(rng.choice(n, size=min(count, n), replace=False).tolist())
+    strides = np.cumprod((1,) + tuple(reversed(shape[1:])))[::-1]
+    for corner in range(16):
+        pos = [(0 if (corner >> d) & 1 == 0 else shape[d] - 1) for d in range(min(4, len(shape)))]
+        idx.add(int(sum(p * s for p, s in zip(pos, strides))))
+    return np.array(sorted(idx), dtype=np.int64)
+
+
+# ------------------------------------------------------------------ the six workloads
+OPS = ["fwd", "bwd_data", "bwd_filter"]
+
+
+@pytest.mark.parametrize("name", list(W.WORKLOADS))
+@pytest.mark.parametrize("op", OPS)
+def test_workload_parity(cg, name, op):
+    wl = W.WORKLOADS[name]
+    pb = wl.problem
+    x, w, dy = W.make_inputs(wl)
+    xd, wd, dyd = x.to(DEV), w.to(DEV), dy.to(DEV)
+    out = _run(cg, op, pb, xd, wd, dyd)
+    assert not torch.isnan(out).any().item(), "unwritten output elements"
+    a, b = _operands(op, x, w, dy)
+    if name == "tiny":
+        ref = _oracle_full(op, pb, x, w, dy)
+        _check(op, pb, out.double().cpu().numpy(), ref, a, b, f"{name}/{op}")
+    else:
+        rng = np.random.default_rng(hash((name, op)) & 0xFFFF)
+        count = 600 if op == "bwd_filter" else 3000
+        idx = _sample_indices(out.numel(), rng, count, tuple(out.shape))
+        ref = _oracle_at(op, pb, x, w, dy, idx)
+        got = out.reshape(-1)[torch.from_numpy(idx).to(DEV)].double().cpu().numpy()
+        _check(op, pb, got, ref, a, b, f"{name}/{op}")
+    # bit-for-bit determinism
+    out2 = _run(cg, op, pb, xd, wd, dyd)
+    assert torch.equal(out.view(torch.int16 if out.dtype == torch.bfloat16 else torch.int32),
+                       out2.view(torch.int16 if out.dtype == torch.bfloat16 else torch.int32))
+
+
+# ------------------------------------------------------------------ ragged small shapes
+SMALL = [
+    # N, C, H, W, K, R, S, ph, pw, sh, sw
+    (1, 1, 5, 5, 1, 3, 3, 1, 1, 1, 1),
+    (2, 3, 7, 9, 5, 3, 2, 1, 0, 1, 1),       # R != S, H != W
+    (1, 5, 14, 7, 3, 3, 3, 1, 1, 2, 2),      # W*4 bytes not 16-byte aligned
+    (2, 4, 9, 11, 6, 5, 3, 2, 1, 3, 2),      # stride 3 x 2, trailing rows uncovered
+    (1, 2, 6, 13, 2, 6, 13, 0, 0, 1, 1),     # H == R, W == S
+    (3, 7, 10, 10, 9, 1, 1, 0, 0, 1, 1),     # 1x1
+    (1, 3, 12, 12, 16, 7, 7, 3, 3, 2, 2),    # stem-like
+    (2, 8, 8, 8, 4, 4, 4, 1, 1, 2, 2),       # deconvolution-like 4x4 / 2
+    (1, 33, 9, 9, 40, 3, 3, 1, 1, 1, 1),     # channel counts off every chunk size
+    (1, 17, 6, 6, 300, 3, 3, 1, 1, 1, 1),    # K > 256: several N tiles
+    (2, 70, 11, 5, 130, 2, 2, 0, 1, 1, 2),
+    (1, 1, 4, 4, 1, 1, 1, 0, 0, 3, 3),       # 1x1 stride 3: backward-data phases without taps
+    (4, 12, 20, 20, 24, 3, 3, 0, 0, 1, 1),   # no padding
+    (1, 9, 31, 17, 11, 5, 5, 2, 2, 1, 1),
+    (2, 300, 5, 5, 20, 3, 3, 1, 1, 1, 1),    # C > 256: several channel blocks
+]
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("case", SMALL)
+@pytest.mark.parametrize("op", OPS)
+def test_small_parity(cg, case, op, dtype):
+    N, C, H, Wd, K, R, S, ph, pw, sh, sw = case
+    pb = W.Conv2dProblem(N, C, H, Wd, K, R, S, ph, pw, sh, sw, dtype)
+    x, w, dy = W.random_problem_inputs(pb, 7000 + SMALL.index(case))
+    out = _run(cg, op, pb, x.to(DEV), w.to(DEV), dy.to(DEV))
+    assert not torch.isnan(out).any().item()
+    ref = _oracle_full(op, pb, x, w, dy)
+    a, b = _operands(op, x, w, dy)
+    _check(op, pb, out.double().cpu().numpy(), ref, a, b, f"{case}/{op}/{dtype}")
+
+
+def test_deconv_alias_matches_oracle_scatter(cg):
+    """deconv2d_fwd (= backward-data with the weight read as (in, out, R, S)) against
+    the oracle's independent scatter-form transposed convolution."""
+    g = torch.Generator().manual_seed(99)
+    inp = torch.randn(2, 12, 5, 5, generator=g)
+    wt = torch.randn(12, 7, 4, 4, generator=g)
+    out = cg.deconv2d_fwd(inp.to(DEV), wt.to(DEV), (10, 10), 1, 2)
+    cg.conv2d_device_status()
+    ref = oracle.deconv2d_fwd_scatter(inp, wt, (10, 10), 1, 2)
+    tol = 2e-3 * math.sqrt(12 * 16 / 4) * float(inp.abs().max()) * float(wt.abs().max())
+    assert float(np.abs(out.double().cpu().numpy() - ref).max()) <= tol
+
+
+def test_stream_argument_is_honoured(cg):
+    pb = W.WORKLOADS["tiny"].problem
+    x, w, dy = W.make_inputs(W.WORKLOADS["tiny"])
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        y = cg.conv2d_fwd(x.to(DEV), w.to(DEV), 1, 1, stream=s)
+    s.synchronize()
+    ref = oracle.conv2d_fwd(x, w, 1, 1)
+    assert float(np.abs(y.double().cpu().numpy() - ref).max()) <= 2e-3 * math.sqrt(27)
+
+
+def test_timeout_flag_clear_after_normal_runs(cg):
+    assert cg.conv2d_device_status() == 0
