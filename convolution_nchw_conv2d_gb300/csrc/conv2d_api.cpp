@@ -407,7 +407,8 @@ int build_bwd_filter(const Desc& d, const void* x, const void* dy, void* dw, voi
   p.P = d.P;
   p.Q = d.Q;
   const int mh = (d.R - 1) / d.sh, mw = (d.S - 1) / d.sw;
-  p.WL = d.Q + mw;
+  // fp32: WL a multiple of 4 so that a tap's offset mod 4 depends on its column only.
+  p.WL = d.dt == 0 ? round_up(d.Q + mw, 4) : d.Q + mw;
   p.EL = d.P + mh;
   p.Mtot = (long long)d.N * p.EL * p.WL;
   p.npl = d.sh * d.sw;
@@ -419,48 +420,119 @@ int build_bwd_filter(const Desc& d, const void* x, const void* dy, void* dw, voi
       p.pl_off_w[a * d.sw + c] = c - d.pw;
     }
   p.ntaps = d.R * d.S;
-  int max_off = 0;
-  for (int r = 0; r < d.R; ++r)
-    for (int s = 0; s < d.S; ++s) {
-      const int t = r * d.S + s;
-      p.tap_plane[t] = (r % d.sh) * d.sw + (s % d.sw);
-      p.tap_off[t] = (r / d.sh) * p.WL + s / d.sw;
-      max_off = std::max(max_off, p.tap_off[t]);
-    }
+  if (p.ntaps > kMaxTaps) return CONV2D_ERR_UNSUPPORTED;
   const int CHUNK = d.dt == 0 ? 4 : 8;
   const int ESZ = d.dt == 0 ? 4 : 2;
   const int abuf_cols = 32;
-  int NC = round_up(d.C, 16);
-  if (NC > 32) NC = (p.ntaps <= 15) ? 32 : 16;
-  p.NC = NC;
-  p.tap_group_size = std::min(p.ntaps, (512 - abuf_cols) / NC);
-  p.n_tgroups = (p.ntaps + p.tap_group_size - 1) / p.tap_group_size;
-  p.tmem_cols = 32;
-  while (p.tmem_cols < abuf_cols + p.tap_group_size * NC) p.tmem_cols <<= 1;
-  p.n_ktiles = (d.K + 127) / 128;
-  p.n_ctiles = (d.C + NC - 1) / NC;
-  p.k_pad = d.K;
-  p.c_pad = d.C;
+  // Raw tap groups: fp32 one per filter row offset r / stride_h (small halo per
+  // group), bf16 a single group (one staged tile per plane serves every tap).
+  std::vector<std::vector<int>> raw;  // filter tap ids r*S + s
+  if (d.dt == 0) {
+    for (int rho = 0; rho <= mh; ++rho) {
+      std::vector<int> g;
+      for (int r = rho * d.sh; r < std::min(d.R, (rho + 1) * d.sh); ++r)
+        for (int s = 0; s < d.S; ++s) g.push_back(r * d.S + s);
+      if (!g.empty()) raw.push_back(g);
+    }
+  } else {
+    std::vector<int> g;
+    for (int t = 0; t < p.ntaps; ++t) g.push_back(t);
+    raw.push_back(g);
+  }
+  auto tap_plane = [&](int id) { return ((id / d.S) % d.sh) * d.sw + ((id % d.S) % d.sw); };
+  auto tap_off = [&](int id) { return ((id / d.S) / d.sh) * p.WL + (id % d.S) / d.sw; };
+  int max_off = 0;
+  for (int t = 0; t < p.ntaps; ++t) max_off = std::max(max_off, tap_off(t));
   const size_t budget = di.smem_optin - 2048;
   bool fitted = false;
-  for (int KB : {128, 64, 32, 16}) {
-    if (KB % (2 * CHUNK)) continue;
-    const int rows = round_up(KB + max_off, 8);
-    const long long a_bytes = (long long)KB * 128 * ESZ;
-    const long long b_bytes = (long long)p.npl * (NC / CHUNK) * rows * 16;
-    const long long fixed = (long long)(KB + p.npl * rows) * 4 + 8 * (2 * 4 + 3) + 16 + 1024;
-    long long stages = ((long long)budget - fixed) / (a_bytes + b_bytes);
-    if (stages < 2) continue;
-    if (stages > 4) stages = 4;
-    p.KB = KB;
-    p.rows = rows;
-    p.a_stage_bytes = (int)a_bytes;
-    p.b_stage_bytes = (int)b_bytes;
-    p.stages = (int)stages;
-    fitted = wgrad_smem_bytes(p) <= di.smem_optin;
+  for (int NC : {256, 128, 64, 32, 16}) {
+    if (NC > round_up(d.C, 16) && NC != 16) continue;
+    const int maxg = (512 - abuf_cols) / NC;
+    // Split raw groups so each fits TMEM; build slots per group (fp32).
+    int ng = 0, nt = 0, nsl = 0, nsl_max = 0, qspan_max = 0;
+    bool ok = true;
+    for (const auto& g : raw) {
+      for (size_t i0 = 0; i0 < g.size(); i0 += maxg) {
+        const int cnt = (int)std::min<size_t>(maxg, g.size() - i0);
+        if (ng >= kMaxTaps) { ok = false; break; }
+        p.tg_begin[ng] = nt;
+        p.tg_count[ng] = cnt;
+        int qmin = INT_MAX, qmax = 0;
+        for (int i = 0; i < cnt; ++i) {
+          const int off = tap_off(g[i0 + i]);
+          qmin = std::min(qmin, off >> 2);
+          qmax = std::max(qmax, off >> 2);
+        }
+        p.tg_qmin[ng] = d.dt == 0 ? qmin : 0;
+        p.tg_slot_begin[ng] = nsl;
+        for (int i = 0; i < cnt; ++i) {
+          const int id = g[i0 + i];
+          const int t = nt + i;
+          p.tap_id[t] = id;
+          p.tap_plane[t] = tap_plane(id);
+          p.tap_off[t] = tap_off(id);
+          p.tap_q[t] = (p.tap_off[t] >> 2) - p.tg_qmin[ng];
+          const int res = p.tap_off[t] & 3;
+          int u = p.tg_slot_begin[ng];
+          while (u < nsl && !(p.slot_plane[u] == p.tap_plane[t] && p.slot_res[u] == res)) ++u;
+          if (u == nsl) {
+            if (nsl == kMaxSlots) { ok = false; break; }
+            p.slot_plane[u] = p.tap_plane[t];
+            p.slot_res[u] = res;
+            ++nsl;
+          }
+          p.tap_slot[t] = u;
+        }
+        if (!ok) break;
+        p.tg_nslots[ng] = nsl - p.tg_slot_begin[ng];
+        nsl_max = std::max(nsl_max, p.tg_nslots[ng]);
+        qspan_max = std::max(qspan_max, d.dt == 0 ? qmax - qmin : 0);
+        nt += cnt;
+        ++ng;
+      }
+      if (!ok) break;
+    }
+    if (!ok) continue;
+    p.n_tgroups = ng;
+    p.nslots = d.dt == 0 ? nsl : 0;
+    int gmax = 0;
+    for (int g = 0; g < ng; ++g) gmax = std::max(gmax, p.tg_count[g]);
+    for (int KB : {128, 64, 32, 16}) {
+      if (KB % (2 * CHUNK)) continue;
+      int rows;
+      long long b_bytes;
+      if (d.dt == 0) {
+        p.nchunks = KB / 4 + qspan_max;
+        rows = round_up(4 * p.nchunks + 3, 8);
+        b_bytes = (long long)nsl_max * p.nchunks * NC * 16;
+      } else {
+        p.nchunks = 0;
+        rows = round_up(KB + max_off, 8);
+        b_bytes = (long long)p.npl * (NC / CHUNK) * rows * 16;
+      }
+      const long long a_bytes = (long long)KB * 128 * ESZ;
+      const long long fixed = (long long)(KB + p.npl * rows) * 4 + 8 * (2 * 4 + 3) + 16 + 1024;
+      long long stages = ((long long)budget - fixed) / (a_bytes + b_bytes);
+      if (stages < 2) continue;
+      if (stages > 4) stages = 4;
+      p.NC = NC;
+      p.KB = KB;
+      p.rows = rows;
+      p.a_stage_bytes = (int)a_bytes;
+      p.b_stage_bytes = (int)b_bytes;
+      p.stages = (int)stages;
+      p.tmem_cols = 32;
+      while (p.tmem_cols < abuf_cols + gmax * NC) p.tmem_cols <<= 1;
+      fitted = wgrad_smem_bytes(p) <= di.smem_optin;
+      if (fitted) break;
+    }
     if (fitted) break;
   }
   if (!fitted) return CONV2D_ERR_UNSUPPORTED;
+  p.n_ktiles = (d.K + 127) / 128;
+  p.n_ctiles = (d.C + p.NC - 1) / p.NC;
+  p.k_pad = d.K;
+  p.c_pad = d.C;
   const long long base = (long long)p.n_ktiles * p.n_ctiles * p.n_tgroups;
   long long want = std::max<long long>(1, (di.sms + base - 1) / base);
   const long long stage_count = (p.Mtot + p.KB - 1) / p.KB;
@@ -628,7 +700,7 @@ const char* conv2d_strerror(int code) {
     case CONV2D_ERR_LAUNCH: return "CUDA launch or stream error";
     case CONV2D_ERR_DEVICE: return "no sm_100-family CUDA device is current";
     case CONV2D_ERR_DEVICE_TIMEOUT: return "a kernel's bounded pipeline wait expired";
-    case CONV2D_ERR_UNSUPPORTED: return "unsupported geometry (R*S > 64, stride_h*stride_w > 16, or no tile fits)";
+    case CONV2D_ERR_UNSUPPORTED: return "unsupported geometry (R*S > 256, stride_h*stride_w > 16, or no tile fits in shared memory)";
     case CONV2D_ERR_BAD_OP: return "unknown op";
     default: return "unknown error code";
   }

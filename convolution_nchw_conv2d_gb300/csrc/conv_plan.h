@@ -17,7 +17,8 @@ namespace cg3 {
 
 constexpr int kMaxPlanes = 16;   // stride_h * stride_w
 constexpr int kMaxPhases = 16;
-constexpr int kMaxTaps = 64;     // R * S
+constexpr int kMaxTaps = 256;    // R * S
+constexpr int kMaxSlots = 64;    // (plane, residue) x copies staged by fp32 backward-filter
 
 // Forward and backward-data: D[position, out_channel] = sum over taps and source
 // channels of S[channel, position + tap_off] * Wpacked[tap, out_channel, channel].
@@ -67,10 +68,19 @@ struct PackPlan {
 
 // Backward-filter: per tap t, D_t[k, c] = sum over positions L of
 // dy[k, L] * Xplane(t)[c, L + tap_off[t]], split over position ranges.
+// Taps are processed in groups (one group per CTA tile, the group's accumulators
+// side by side in TMEM); tap t of the plan is filter tap tap_id[t] = r*S + s.
+// bf16 stages x once per plane with positions along rows (an MN-major operand) and
+// reaches tap t by the row offset tap_off[t].  tf32 operands must be K-major, where
+// a 16-byte chunk holds 4 consecutive positions, so fp32 stages, per group, one copy
+// of x per (plane, offset mod 4) "slot", shifted by that residue and starting at
+// position 4*tg_qmin[g]; tap t is chunk offset tap_q[t] (relative to tg_qmin) of
+// slot tap_slot[t] (an index into slot_plane/slot_res).  WL is a multiple of 4 and
+// groups are formed per filter row offset, so a group's halo is a few positions.
 struct WgradPlan {
   const void* x;         // NCHW
   const void* dy;        // N K P Q
-  float* partial;        // [split][tap][c_pad][k_pad] fp32
+  float* partial;        // [split][R*S][c_pad][k_pad] fp32
   int N, C, H, W, K, P, Q;
   int WL, EL;
   long long Mtot;
@@ -78,12 +88,19 @@ struct WgradPlan {
   int pl_step_h, pl_step_w;
   int pl_off_h[kMaxPlanes], pl_off_w[kMaxPlanes];
   int ntaps;
-  int tap_plane[kMaxTaps], tap_off[kMaxTaps];
-  int tap_group_size, n_tgroups;   // taps handled per CTA tile
+  int tap_id[kMaxTaps];
+  int tap_plane[kMaxTaps], tap_off[kMaxTaps];   // bf16
+  int tap_slot[kMaxTaps], tap_q[kMaxTaps];      // fp32
+  int nslots;
+  int slot_plane[kMaxSlots], slot_res[kMaxSlots];
+  int n_tgroups;
+  int tg_begin[kMaxTaps], tg_count[kMaxTaps];
+  int tg_qmin[kMaxTaps], tg_slot_begin[kMaxTaps], tg_nslots[kMaxTaps];
+  int nchunks;           // fp32: position chunks staged per slot per stage
   int n_ktiles, n_ctiles, nsplit;
   long long split_len;   // positions per split (multiple of the stage length)
   int rows;              // staged x rows per plane per stage (multiple of 8)
-  int k_pad, c_pad;      // padded extents of the partial buffer
+  int k_pad, c_pad;      // extents of the partial buffer
   long long total_tiles; // n_ktiles * n_ctiles * n_tgroups * nsplit
   int stages;
   int NC;                // channels per tile (GEMM N per tap, multiple of 16)

@@ -10,8 +10,10 @@
 //
 // One CTA tile = 128 output channels k x NC input channels c x a group of taps x one
 // range of positions (split-K).  Per pipeline stage (KB positions):
-//   producers (warps 0-3) stage dy[k, L] K-major and x[c, L + off] in the
-//     core-matrix layout (read as MN-major: c along chunks, positions along rows);
+//   producers (warps 0-3) stage dy[k, L] K-major and x in the core-matrix layout:
+//     bf16 as an MN-major operand (channels along chunks, positions along rows, a
+//     tap is a row offset); fp32 as K-major copies per (plane, offset mod 4), since
+//     tf32 operands must be K-major (an MN-major tf32 B reads as zeros);
 //   the MMA lane copies each 128 x 32-byte dy slice into TMEM with tcgen05.cp and
 //     issues one tcgen05.mma per tap with A from TMEM and B = x at the tap's row
 //     offset, so dy is read from shared memory once for all taps;
@@ -119,6 +121,9 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_kernel(const __grid_constan
       if (lend > p.Mtot) lend = p.Mtot;
       const int kbase = wt.kt * 128;
       const int cbase = wt.ct * p.NC;
+      const long long xbase = DT == 0 ? 4ll * p.tg_qmin[wt.tg] : 0ll;
+      const int sl0 = p.tg_slot_begin[wt.tg];
+      const int nsl = p.tg_nslots[wt.tg];
       for (long long l0 = lbeg; l0 < lend; l0 += KB) {
         // Position tables for this stage.
         named_bar_sync(1, kProdThreads);
@@ -138,7 +143,7 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_kernel(const __grid_constan
             const int j = i - KB;
             const int pl = j / rows;
             const int row = j - pl * rows;
-            const long long L = l0 + row;
+            const long long L = l0 + xbase + row;
             int off = -1;
             if (L < p.Mtot) {
               const int n = (int)(L / img);
@@ -177,21 +182,23 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_kernel(const __grid_constan
               cp_async_4(dbase + (uint32_t)kr * 16u, v ? dy + off + (long long)k * PQ : dy, v);
             }
           }
-          // x: [plane][chunk][row][4 channels]
-          for (int pj = 0; pj < p.npl * NCB; ++pj) {
-            const int pl = pj / NCB;
-            const int j = pj - pl * NCB;
-            const int c = cbase + j * 4 + e4;
-            const bool cv = c < p.C;
-            const float* gc = x + (long long)(cv ? c : 0) * HW;
-            const uint32_t dbase = b_st + (uint32_t)(pj * rows) * 16u + (uint32_t)e4 * 4u;
-            const int* tab = xtab + pl * rows;
-#pragma unroll 4
-            for (int row = warp * 8 + rsub; row < rows; row += 32) {
-              const int off = tab[row];
-              const bool v = cv && off >= 0;
-              cp_async_4(dbase + (uint32_t)row * 16u, v ? gc + off : x, v);
-            }
+          // x, K-major per slot: [slot][position chunk j][channel row][4 positions];
+          // slot u holds positions i + slot_res[u] of plane slot_plane[u].
+          // lane = (channel within 8, position within chunk): 128 contiguous bytes.
+          const int ngrp = p.NC >> 3;
+          const int items = nsl * p.nchunks * ngrp;
+          for (int it = warp; it < items; it += 4) {
+            const int g = it % ngrp;
+            const int rest = it / ngrp;
+            const int j = rest % p.nchunks;
+            const int u = rest / p.nchunks;
+            const int cr = g * 8 + rsub;
+            const int c = cbase + cr;
+            const int off = xtab[p.slot_plane[sl0 + u] * rows + j * 4 + e4 + p.slot_res[sl0 + u]];
+            const bool v = off >= 0 && c < p.C;
+            const uint32_t dst =
+                b_st + (uint32_t)((u * p.nchunks + j) * p.NC + cr) * 16u + (uint32_t)e4 * 4u;
+            cp_async_4(dst, v ? x + off + (long long)c * HW : x, v);
           }
           cp_async_commit();
           if (pending >= 0) {
@@ -269,10 +276,10 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_kernel(const __grid_constan
       if (!mbar_wait(accf, aphase, abort_flag, &g_wgrad_err)) break;
       tc_fence_after();
       const int k = wt.kt * 128 + q * 32 + lane;
-      const int tap0 = wt.tg * p.tap_group_size;
-      const int ntg = min(p.tap_group_size, p.ntaps - tap0);
+      const int tap0 = p.tg_begin[wt.tg];
+      const int ntg = p.tg_count[wt.tg];
       for (int ti = 0; ti < ntg; ++ti) {
-        float* dst = p.partial + ((long long)wt.sp * p.ntaps + tap0 + ti) * p.c_pad * (long long)p.k_pad;
+        float* dst = p.partial + ((long long)wt.sp * p.ntaps + p.tap_id[tap0 + ti]) * p.c_pad * (long long)p.k_pad;
         for (int c0 = 0; c0 < p.NC; c0 += 16) {
           uint32_t r[16];
           tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(kAbufCols + ti * p.NC + c0), r);
@@ -294,7 +301,7 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_kernel(const __grid_constan
   } else {
     // =============================================================== MMA issuer
     if (lane == 0) {
-      const uint32_t id = idesc(KIND, 128, p.NC, 0, 1);
+      const uint32_t id = idesc(KIND, 128, p.NC, 0, DT == 0 ? 0 : 1);
       int stage = 0;
       uint32_t fphase = 0;
       uint32_t aphase = 0;
@@ -307,8 +314,9 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_kernel(const __grid_constan
         const long long lbeg = (long long)wt.sp * p.split_len;
         long long lend = lbeg + p.split_len;
         if (lend > p.Mtot) lend = p.Mtot;
-        const int tap0 = wt.tg * p.tap_group_size;
-        const int ntg = min(p.tap_group_size, p.ntaps - tap0);
+        const int tap0 = p.tg_begin[wt.tg];
+        const int ntg = p.tg_count[wt.tg];
+        const int sl0 = p.tg_slot_begin[wt.tg];
         if (!mbar_wait(acce, aphase ^ 1u, abort_flag, &g_wgrad_err)) break;
         tc_fence_after();
         bool first = true;
@@ -327,9 +335,17 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_kernel(const __grid_constan
             if (++abuf == kAbufCols / 8) abuf = 0;
             for (int ti = 0; ti < ntg; ++ti) {
               const int tap = tap0 + ti;
-              const uint32_t bst = b_st + (uint32_t)(p.tap_plane[tap] * NCB * rows) * 16u +
-                                   (uint32_t)(ks * KSTEP + p.tap_off[tap]) * 16u;
-              const uint64_t bd = sdesc(bst, 128u, (uint32_t)rows * 16u);
+              uint64_t bd;
+              if constexpr (DT == 0) {
+                // K-major x copy: chunk (2*ks + q) of the tap's slot.
+                const uint32_t bst = b_st + (uint32_t)(((p.tap_slot[tap] - sl0) * p.nchunks + 2 * ks + p.tap_q[tap]) *
+                                                       p.NC) * 16u;
+                bd = sdesc(bst, (uint32_t)p.NC * 16u, 128u);
+              } else {
+                const uint32_t bst = b_st + (uint32_t)(p.tap_plane[tap] * NCB * rows) * 16u +
+                                     (uint32_t)(ks * KSTEP + p.tap_off[tap]) * 16u;
+                bd = sdesc(bst, 128u, (uint32_t)rows * 16u);
+              }
               mma_ts<KIND>(tmem + (uint32_t)(kAbufCols + ti * p.NC), a_tm, bd, id, first ? 0u : 1u);
             }
             first = false;

@@ -88,7 +88,7 @@ enum {
     CONV2D_ERR_LAUNCH = -8,         /* the CUDA runtime rejected a launch */
     CONV2D_ERR_DEVICE = -9,         /* no usable sm_100-family device */
     CONV2D_ERR_DEVICE_TIMEOUT = -10,/* a kernel's bounded internal wait expired */
-    CONV2D_ERR_UNSUPPORTED = -11,   /* R*S > 64 or stride_h*stride_w > 16 */
+    CONV2D_ERR_UNSUPPORTED = -11,   /* R*S > 256, stride_h*stride_w > 16, or no tile fits */
     CONV2D_ERR_BAD_OP = -12         /* unknown op in conv2d_workspace_size() */
 };
 

@@ -81,7 +81,7 @@ GOOD = (2, 3, 8, 8, 4, 3, 3, 1, 1, 1, 1, 8, 8)
     ((2, 3, 8, 8, 4, 3, 3, 1, 1, 1, 1, 7, 8), -2),    # P mismatch
     ((2, 3, 2, 8, 4, 5, 3, 0, 1, 1, 1, 0, 8), -2),    # no output rows
     ((65536, 256, 256, 256, 4, 3, 3, 1, 1, 1, 1, 256, 256), -7),  # too large
-    ((2, 3, 80, 80, 4, 9, 9, 1, 1, 1, 1, 74, 74), -11),  # R*S > 64
+    ((2, 3, 80, 80, 4, 17, 17, 1, 1, 1, 1, 66, 66), -11),  # R*S > 256
 ])
 def test_descriptor_errors(cg, bad, code):
     for op in (0, 1, 2):
