@@ -1,0 +1,377 @@
+#!/usr/bin/env python3
+"""Benchmark: conv2d TFLOP/s per op (forward / backward-data / backward-filter) on GB300.
+
+One step = the whole hot path once: forward, backward-data and backward-filter of the
+workload (default: the ResNet-style 3x3 layer, fp32 tensors on TF32 tensor cores,
+N=32 C=K=64 H=W=56 pad 1 stride 1) on seeded synthetic inputs already resident in HBM.
+Each op is timed with CUDA events on the launching stream; L2 is flushed (a write of
+twice the L2 size) before every op, outside the events.  FLOP per op = 2*N*K*P*Q*C*R*S.
+
+Prints ONE JSON line (rank 0).  --impl reference times the fp64 CPU oracle on a bounded
+sample of the same workload instead (the reference arm of this build).
+Multi-GPU (torchrun, one rank per GPU): the path is run as independent replicas, one per
+rank, no collective on the data path; value = all ranks' FLOP / max rank time.
+"""
+from __future__ import annotations
+
+import argparse
+import datetime
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "conv2d TFLOP/s per op (fwd/dgrad/wgrad) and % of GB300 tensor-core peak"
+OPS = ("fwd", "bwd_data", "bwd_filter")
+KERNELS_PER_OP = 2  # forward/backward-data: filter pack + main; backward-filter: main + split reduce
+# Fallback peaks (used only if MEASURED_PEAKS.json is absent): one earlier GB300 measurement.
+FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+NOMINAL_TF32_OVER_BF16 = 1.1 / 2.25
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", default="resnet3x3")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    return ap.parse_args()
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            with open(path) as f:
+                d = json.load(f)
+            hbm = d.get("hbm_gbs") or d.get("hbm_GBps")
+            bf = d.get("bf16_tflops")
+            if hbm and bf:
+                return {"hbm_gbs": float(hbm), "bf16_tflops": float(bf),
+                        "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", bf)),
+                        "source": "measured"}
+        except Exception:
+            pass
+    return dict(FALLBACK, source="fallback")
+
+
+def src_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "convolution_nchw_conv2d_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(workload, op):
+    """DRAM bytes per launch from the committed ncu summary, if taken on this source."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        e = d.get(f"{workload}/{op}")
+        if e and e.get("source_sha") == src_hash():
+            return e.get("dram_bytes_per_launch")
+    except Exception:
+        pass
+    return None
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", str(gpu_index)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self, t0, t1):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        all_sm = []
+        for line in out.splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                clk = float(parts[2])
+                cmax = float(parts[3])
+            except ValueError:
+                continue
+            all_sm.append((ts, clk, cmax, parts[6:10]))
+        inside = [s for s in all_sm if t0 - 0.15 <= s[0] <= t1 + 0.15] or all_sm
+        for ts, clk, cmax, flags in inside:
+            sm.append(clk)
+            mx.append(cmax)
+            for n, v in zip(names, flags):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ our arm
+def run_ours(args, rank, world):
+    import torch
+    import convolution_nchw_conv2d_gb300 as cg
+    from convolution_nchw_conv2d_gb300 import workloads as W
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    wl = W.WORKLOADS[args.workload]
+    pb = wl.problem
+    x, w, dy = W.make_inputs(wl)
+    xd, wd, dyd = x.to(dev), w.to(dev), dy.to(dev)
+    pad, st = (pb.pad_h, pb.pad_w), (pb.stride_h, pb.stride_w)
+    y = torch.empty(pb.y_shape, dtype=x.dtype, device=dev)
+    dx = torch.empty(pb.x_shape, dtype=x.dtype, device=dev)
+    dw = torch.empty(pb.w_shape, dtype=x.dtype, device=dev)
+    dt = 0 if pb.dtype == "f32" else 1
+    wsz = max(cg.conv2d_workspace_size(op, pb.dims(), dt) for op in range(3))
+    ws = torch.empty(max(wsz, 16), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def op_call(op):
+        if op == "fwd":
+            cg.conv2d_fwd(xd, wd, pad, st, out=y, workspace=ws, stream=stream)
+        elif op == "bwd_data":
+            cg.conv2d_bwd_data(dyd, wd, (pb.H, pb.W), pad, st, out=dx, workspace=ws, stream=stream)
+        else:
+            cg.conv2d_bwd_filter(xd, dyd, (pb.R, pb.S), pad, st, out=dw, workspace=ws, stream=stream)
+
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
+
+    for _ in range(args.warmup):
+        for op in OPS:
+            flush.zero_()
+            op_call(op)
+    cg.conv2d_device_status(stream)
+
+    K = args.steps
+    evs = {op: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                for _ in range(K)] for op in OPS}
+    sampler = ClockSampler(local)
+    time.sleep(0.3)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    t0 = time.time()
+    for i in range(K):
+        for op in OPS:
+            flush.zero_()
+            a, b = evs[op][i]
+            a.record(stream)
+            op_call(op)
+            b.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    t1 = time.time()
+    clocks = sampler.stop(t0, t1)
+    cg.conv2d_device_status(stream)
+    op_ms = {op: sum(a.elapsed_time(b) for a, b in evs[op]) / K for op in OPS}
+    step_ms = sum(op_ms.values())
+    if world > 1:
+        tt = torch.tensor([step_ms], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        step_ms = float(tt.item())
+
+    # ---- end to end: pinned host inputs -> device -> three ops -> host results
+    xh, wh, dyh = x.pin_memory(), w.pin_memory(), dy.pin_memory()
+    yh = torch.empty(pb.y_shape, dtype=x.dtype).pin_memory()
+    dxh = torch.empty(pb.x_shape, dtype=x.dtype).pin_memory()
+    dwh = torch.empty(pb.w_shape, dtype=x.dtype).pin_memory()
+    E = max(1, args.e2e_steps)
+    e_evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(E)]
+    for i in range(E + 2):
+        flush.zero_()
+        if i >= 2:
+            e_evs[i - 2][0].record(stream)
+        xd.copy_(xh, non_blocking=True)
+        wd.copy_(wh, non_blocking=True)
+        dyd.copy_(dyh, non_blocking=True)
+        for op in OPS:
+            op_call(op)
+        yh.copy_(y, non_blocking=True)
+        dxh.copy_(dx, non_blocking=True)
+        dwh.copy_(dw, non_blocking=True)
+        if i >= 2:
+            e_evs[i - 2][1].record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = sum(a.elapsed_time(b) for a, b in e_evs) / E
+    esz = pb.elem_bytes()
+    nx, ny, nw = (math.prod(pb.x_shape), math.prod(pb.y_shape), math.prod(pb.w_shape))
+    flop = pb.flops()
+
+    peaks = load_peaks()
+    tc_peak = peaks["bf16_tflops"] * (NOMINAL_TF32_OVER_BF16 if pb.dtype == "f32" else 1.0)
+    per_op = {}
+    for op in OPS:
+        tf = flop / (op_ms[op] * 1e-3) / 1e12
+        gbs = pb.alg_bytes(op) / (op_ms[op] * 1e-3) / 1e9
+        per_op[op] = {"ms": round(op_ms[op], 5), "tflops": round(tf, 2),
+                      "frac_tc_peak": round(tf / tc_peak, 4), "alg_gbs": round(gbs, 1),
+                      "frac_hbm_peak": round(gbs / peaks["hbm_gbs"], 4)}
+    dom = max(OPS, key=lambda o: op_ms[o])
+    ai = flop / pb.alg_bytes(dom)
+    if ai * peaks["hbm_gbs"] * 1e9 < tc_peak * 1e12:
+        roof = {"bound": "hbm", "achieved": per_op[dom]["alg_gbs"], "peak": peaks["hbm_gbs"], "unit": "GB/s"}
+    else:
+        roof = {"bound": "tensor", "achieved": per_op[dom]["tflops"], "peak": round(tc_peak, 1), "unit": "TFLOP/s"}
+    roof["frac"] = round(roof["achieved"] / roof["peak"], 4)
+    roof["traffic"] = ncu_traffic(args.workload, dom)
+    roof["kernel"] = dom
+    roof["peak_source"] = peaks["source"] + (" (bf16 x nominal tf32/bf16 ratio)" if pb.dtype == "f32" else "")
+
+    value = world * 3 * flop / (step_ms * 1e-3) / 1e12
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": K, "warmup": args.warmup, "ms_per_step": round(step_ms, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "tf32" if pb.dtype == "f32" else "bf16", "data": "synthetic",
+        "config": {"workload": wl.name, "shape": wl.description,
+                   "N": pb.N, "C": pb.C, "H": pb.H, "W": pb.W, "K": pb.K, "R": pb.R, "S": pb.S,
+                   "pad": [pb.pad_h, pb.pad_w], "stride": [pb.stride_h, pb.stride_w],
+                   "step": "fwd + bwd_data + bwd_filter", "l2": "flushed before every op (2x L2 write)",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "per_op": per_op,
+        "roofline": roof,
+        "e2e": {"value": round(world * 3 * flop / (e2e_ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
+                "h2d_bytes_per_step": (nx + nw + ny) * esz, "d2h_bytes_per_step": (ny + nx + nw) * esz,
+                "ms_per_step": round(e2e_ms, 4)},
+        "gpu_launches": K * len(OPS) * KERNELS_PER_OP,
+        "clocks": clocks,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl, seconds=12.0)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return line
+
+
+# ------------------------------------------------------------------ oracle (CPU) arm
+def _oracle_sample(wl, budget_s, rng_seed=0):
+    """Time the fp64 oracle on random output elements of every op; returns (flop, seconds, desc)."""
+    import numpy as np
+
+    import oracle
+    from convolution_nchw_conv2d_gb300 import workloads as W
+    pb = wl.problem
+    x, w, dy = W.make_inputs(wl)
+    xs, ws_, dys = (oracle._f64(t) for t in (x, w, dy))
+    rng = np.random.default_rng(rng_seed)
+    red = {"fwd": pb.C * pb.R * pb.S, "bwd_data": pb.K * pb.R * pb.S, "bwd_filter": pb.N * pb.P * pb.Q}
+    sizes = {"fwd": math.prod(pb.y_shape), "bwd_data": math.prod(pb.x_shape), "bwd_filter": math.prod(pb.w_shape)}
+    fns = {"fwd": (oracle.conv2d_fwd_at, xs, ws_), "bwd_data": (oracle.conv2d_bwd_data_at, dys, ws_),
+           "bwd_filter": (oracle.conv2d_bwd_filter_at, xs, dys)}
+    # calibrate: equal multiply-add budget per op
+    macs_per_op = 2_000_000
+    flop = 0
+    t_all = 0.0
+    counts = {}
+    while True:
+        flop = 0
+        t0 = time.perf_counter()
+        for op in OPS:
+            n = max(1, min(sizes[op], macs_per_op // red[op]))
+            counts[op] = n
+            idx = rng.choice(sizes[op], size=n, replace=False)
+            fn, a, b = fns[op]
+            fn(a, b, pb.dims(), idx)
+            flop += 2 * n * red[op]
+        t_all = time.perf_counter() - t0
+        if t_all >= budget_s * 0.5 or macs_per_op > 10**12:
+            break
+        macs_per_op = int(macs_per_op * max(2.0, budget_s / max(t_all, 1e-3)))
+    desc = (f"{', '.join(f'{counts[o]} random {o} outputs' for o in OPS)} of the {wl.name} workload, "
+            f"each a full fp64 reduction (flop counted at 2*reduction length per output)")
+    return flop, t_all, desc
+
+
+def cpu_baseline(wl, seconds=12.0):
+    import oracle
+    flop, t, desc = _oracle_sample(wl, seconds)
+    return {"value": flop / t / 1e12, "unit": "TFLOP/s", "cores": oracle.num_threads(),
+            "kind": "oracle", "sample": desc, "seconds": round(t, 3)}
+
+
+def run_reference(args, rank, world):
+    import oracle
+    from convolution_nchw_conv2d_gb300 import workloads as W
+    wl = W.WORKLOADS[args.workload]
+    pb = wl.problem
+    per_step = 2.0
+    for _ in range(args.warmup):
+        _oracle_sample(wl, 0.2)
+    flops, secs = 0, 0.0
+    desc = ""
+    for _ in range(args.steps):
+        f, t, desc = _oracle_sample(wl, per_step)
+        flops += f
+        secs += t
+    v = flops / secs / 1e12
+    return {
+        "impl": "reference", "metric": METRIC, "value": v, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic",
+        "config": {"workload": wl.name, "shape": wl.description, "step": "fwd + bwd_data + bwd_filter (sampled)"},
+        "cpu_baseline": {"value": v, "unit": "TFLOP/s", "cores": oracle.num_threads(), "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+
+
+def main():
+    args = parse_args()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        line = run_reference(args, rank, world)
+    else:
+        line = run_ours(args, rank, world)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())
