@@ -19,7 +19,7 @@ import os
 import threading
 
 __all__ = [
-    "conv2d_fwd", "conv2d_bwd_data", "conv2d_bwd_filter", "deconv2d_fwd",
+    "conv2d_fwd", "conv2d_bwd_data", "conv2d_bwd_filter", "deconv2d_fwd", "conv2d_fwd_noalloc",
     "conv2d_workspace_size", "conv2d_output_dim", "conv2d_device_status", "conv2d_strerror",
     "Conv2dError", "lib_path", "load_library", "OP_FWD", "OP_BWD_DATA", "OP_BWD_FILTER",
     "DTYPE_F32", "DTYPE_BF16",
@@ -45,7 +45,7 @@ def lib_path() -> str:
 
 
 EXPORTS = ("conv2d_output_dim", "conv2d_workspace_size", "conv2d_fwd", "conv2d_bwd_data",
-           "conv2d_bwd_filter", "conv2d_device_status", "conv2d_strerror")
+           "conv2d_bwd_filter", "conv2d_fwd_noalloc", "conv2d_device_status", "conv2d_strerror")
 
 
 def load_library():
@@ -67,6 +67,8 @@ def load_library():
             f = getattr(lib, name)
             f.argtypes = [i] * 13 + [i, vp, vp, vp, vp, sz, vp]
             f.restype = i
+        lib.conv2d_fwd_noalloc.argtypes = [i] * 13 + [i, vp, vp, vp, vp]
+        lib.conv2d_fwd_noalloc.restype = i
         lib.conv2d_device_status.argtypes = [vp]
         lib.conv2d_device_status.restype = i
         lib.conv2d_strerror.argtypes = [i]
@@ -165,6 +167,31 @@ def conv2d_fwd(x, w, pad=0, stride=1, out=None, workspace=None, stream=None):
         out = torch.empty((N, K, P, Q), dtype=x.dtype, device=x.device)
     dims = (N, C, H, W, K, R, S, ph, pw, sh, sw, P, Q)
     return _call("conv2d_fwd", dims, _dtype_code(x), x, w, out, workspace, OP_FWD, stream)
+
+
+def conv2d_fwd_noalloc(x, w, pad=0, stride=1, out=None, stream=None):
+    """Forward with no workspace: the library stages the repacked filter in its own fixed
+    8 MiB device scratch, for callers that cannot allocate device memory.  Raises
+    Conv2dError (CONV2D_ERR_NOALLOC_LIMIT) if the filter does not fit.  Calls that overlap
+    on the GPU race on the shared scratch; keep them ordered on one stream."""
+    import torch
+    _check_tensor(x, "x")
+    _check_tensor(w, "w")
+    N, C, H, W = x.shape
+    K, C2, R, S = w.shape
+    if C2 != C or w.dtype != x.dtype:
+        raise ValueError("x / w channel count or dtype mismatch")
+    ph, pw = _pair(pad)
+    sh, sw = _pair(stride)
+    P, Q = conv2d_output_dim(H, ph, R, sh), conv2d_output_dim(W, pw, S, sw)
+    if out is None:
+        out = torch.empty((N, K, P, Q), dtype=x.dtype, device=x.device)
+    rc = load_library().conv2d_fwd_noalloc(N, C, H, W, K, R, S, ph, pw, sh, sw, P, Q, _dtype_code(x),
+                                           ctypes.c_void_p(x.data_ptr()), ctypes.c_void_p(w.data_ptr()),
+                                           ctypes.c_void_p(out.data_ptr()), _stream_ptr(stream))
+    if rc:
+        raise Conv2dError(rc, "conv2d_fwd_noalloc")
+    return out
 
 
 def conv2d_bwd_data(dy, w, x_hw, pad=0, stride=1, out=None, workspace=None, stream=None):

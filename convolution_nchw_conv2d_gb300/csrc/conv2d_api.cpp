@@ -23,6 +23,8 @@ cudaError_t launch_wgrad_reduce(const ReducePlan& rp, int dt, int num_sms, cudaS
 size_t wgrad_smem_bytes(const WgradPlan& p);
 int tap_gemm_take_error();
 int wgrad_take_error();
+size_t noalloc_scratch_capacity();
+cudaError_t noalloc_scratch_ptr(void** ptr);
 }  // namespace cg3
 
 using namespace cg3;
@@ -674,6 +676,33 @@ int conv2d_bwd_filter(int N, int C, int H, int W, int K, int R, int S, int pad_h
   return launch_err(launch_wgrad_reduce(b.rp, d.dt, di.sms, st));
 }
 
+int conv2d_fwd_noalloc(int N, int C, int H, int W, int K, int R, int S, int pad_h, int pad_w, int stride_h,
+                       int stride_w, int P, int Q, int dtype, const void* x, const void* w, void* y,
+                       void* stream) {
+  const Desc d{N, C, H, W, K, R, S, pad_h, pad_w, stride_h, stride_w, P, Q, dtype};
+  int rc = validate(d);
+  if (rc) return rc;
+  rc = check_ptrs(x, w, y, d.dt);
+  if (rc) return rc;
+  const DevInfo di = device_info();
+  if (!di.ok) return CONV2D_ERR_DEVICE;
+  TapBuild b;
+  rc = build_fwd(d, x, w, y, nullptr, di, b);  // sizes the packed filter
+  if (rc) return rc;
+  if (b.pack_bytes > noalloc_scratch_capacity()) return CONV2D_ERR_NOALLOC_LIMIT;
+  void* scratch = nullptr;
+  if (noalloc_scratch_ptr(&scratch) != cudaSuccess) {
+    cudaGetLastError();
+    return CONV2D_ERR_DEVICE;
+  }
+  b.p.wpack = scratch;
+  b.pp.wpack = scratch;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  rc = launch_err(launch_pack_filter(b.pp, d.dt, st));
+  if (rc) return rc;
+  return launch_err(launch_tap_gemm(b.p, d.dt, b.grid, st));
+}
+
 int conv2d_device_status(void* stream) {
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (cudaStreamSynchronize(st) != cudaSuccess) {
@@ -702,6 +731,8 @@ const char* conv2d_strerror(int code) {
     case CONV2D_ERR_DEVICE_TIMEOUT: return "a kernel's bounded pipeline wait expired";
     case CONV2D_ERR_UNSUPPORTED: return "unsupported geometry (R*S > 256, stride_h*stride_w > 16, or no tile fits in shared memory)";
     case CONV2D_ERR_BAD_OP: return "unknown op";
+    case CONV2D_ERR_NOALLOC_LIMIT:
+      return "conv2d_fwd_noalloc: the packed filter exceeds the library's fixed 8 MiB scratch";
     default: return "unknown error code";
   }
 }

@@ -19,6 +19,9 @@
 //              output positions; bf16 outputs rounded to nearest even.
 //   warp 8     TMEM allocation; lane 0 issues tcgen05.mma (kind::tf32 for fp32,
 //              kind::f16 with bf16 operands) accumulating in TMEM.
+#include <mutex>
+#include <vector>
+
 #include "conv_plan.h"
 #include "sm103_ptx.cuh"
 
@@ -490,6 +493,39 @@ cudaError_t launch_pack_filter(const PackPlan& pp, int dt, cudaStream_t st) {
   else
     pack_filter_kernel<1><<<(int)blocks, 256, 0, st>>>(pp);
   return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------- fixed scratch
+// Filter-pack scratch for conv2d_fwd_noalloc: a file-scope device array, so that callers
+// who cannot allocate device memory can still run the forward op.  Every GPU that loads
+// this library holds it until the process exits.  Host code must not pass the array's
+// name to a kernel (on the host it is only a stand-in); the device address is looked up
+// once per device with cudaGetSymbolAddress while that device is current.
+constexpr size_t kNoAllocScratchBytes = 8u << 20;  // 8 MiB
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
+
+size_t noalloc_scratch_capacity() { return kNoAllocScratchBytes; }
+
+// Device address of the scratch on the current device (looked up on first use per
+// device, then cached).  Returns cudaSuccess and sets *ptr, or the lookup's error.
+cudaError_t noalloc_scratch_ptr(void** ptr) {
+  static std::mutex mu;
+  static std::vector<void*> cache;
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lk(mu);
+  if ((size_t)dev < cache.size() && cache[dev] != nullptr) {
+    *ptr = cache[dev];
+    return cudaSuccess;
+  }
+  void* p = nullptr;
+  e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+  if (e != cudaSuccess) return e;
+  if ((size_t)dev >= cache.size()) cache.resize(dev + 1, nullptr);
+  cache[dev] = p;
+  *ptr = p;
+  return cudaSuccess;
 }
 
 int tap_gemm_take_error() {

@@ -89,7 +89,8 @@ enum {
     CONV2D_ERR_DEVICE = -9,         /* no usable sm_100-family device */
     CONV2D_ERR_DEVICE_TIMEOUT = -10,/* a kernel's bounded internal wait expired */
     CONV2D_ERR_UNSUPPORTED = -11,   /* R*S > 256, stride_h*stride_w > 16, or no tile fits */
-    CONV2D_ERR_BAD_OP = -12         /* unknown op in conv2d_workspace_size() */
+    CONV2D_ERR_BAD_OP = -12,        /* unknown op in conv2d_workspace_size() */
+    CONV2D_ERR_NOALLOC_LIMIT = -13  /* conv2d_fwd_noalloc: problem exceeds its fixed scratch */
 };
 
 /* Output extent of one spatial dimension: *out = floor((in + 2*pad - k)/stride) + 1.
@@ -121,6 +122,31 @@ int conv2d_bwd_filter(int N, int C, int H, int W, int K, int R, int S,
                       int pad_h, int pad_w, int stride_h, int stride_w, int P, int Q, int dtype,
                       const void *x, const void *dy, void *dw,
                       void *workspace, size_t workspace_bytes, void *stream);
+
+/* Forward without any workspace argument, for callers that cannot allocate device
+ * memory: for example code whose device memory is entirely owned by another runtime's
+ * pool, or a latency-critical path that must never call cudaMalloc (which can
+ * synchronize the device).  There is no counterpart of this entry point on the
+ * reference pages; it is an addition of this library.
+ *
+ * Same arguments, layouts, results and error codes as conv2d_fwd, except that the
+ * repacked filter is staged in a fixed 8 MiB scratch array compiled into the library
+ * instead of a caller workspace.  The function itself allocates nothing.
+ *   - Limit: returns CONV2D_ERR_NOALLOC_LIMIT (nothing enqueued) when the repacked
+ *     filter needs more than 8 MiB, which is about 2M fp32 or 4M bf16 filter values
+ *     (rounded up to whole tiles); conv2d_workspace_size(CONV2D_OP_FWD, ...) reports the
+ *     size needed.
+ *   - The scratch exists once per GPU that loaded the library and is held until the
+ *     process exits.  The first call on a device looks up the scratch's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call before
+ *     any stream capture.
+ *   - All calls share the scratch and it keeps the last call's contents (each call
+ *     rewrites the part it uses before reading it).  Calls whose execution overlaps on
+ *     the GPU (different streams, no ordering) race on it: order them on one stream or
+ *     with events. */
+int conv2d_fwd_noalloc(int N, int C, int H, int W, int K, int R, int S,
+                       int pad_h, int pad_w, int stride_h, int stride_w, int P, int Q, int dtype,
+                       const void *x, const void *w, void *y, void *stream);
 
 /* Synchronizes `stream`, then reports CONV2D_ERR_DEVICE_TIMEOUT if any kernel of this
  * library hit its bounded-wait limit since the previous call (and clears the record),
