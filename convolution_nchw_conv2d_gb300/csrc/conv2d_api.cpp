@@ -103,6 +103,18 @@ DevInfo device_info() {
   return di;
 }
 
+// A 1x1 filter with unit stride and no padding sees each image as one row of H*W
+// pixels; planning it that way makes every row of the linear space contiguous.
+Desc flatten_pointwise(Desc d) {
+  if (d.R == 1 && d.S == 1 && d.ph == 0 && d.pw == 0 && d.sh == 1 && d.sw == 1) {
+    d.W = d.H * d.W;
+    d.H = 1;
+    d.Q = d.W;
+    d.P = 1;
+  }
+  return d;
+}
+
 // ------------------------------------------------------------------ tap plans
 struct TapBuild {
   TapPlan p;
@@ -140,13 +152,16 @@ bool choose_tap_tiles(TapPlan& p, int max_off, int dt, const DevInfo& di, bool p
       const long long mtiles = (p.Mtot + 128ll * mh - 1) / (128ll * mh);
       // Small problems: prefer more, smaller tiles so that every SM gets work.
       if (mh == 2 && mtiles * n_ntiles * p.nph < di.sms) continue;
+      // Keep two accumulator buffers in TMEM (the epilogue of one tile overlaps the
+      // mainloop of the next): two 128-row halves only when 4*NT columns fit.
+      if (mh == 2 && 4 * NT > 512) continue;
       for (int ci = 0; ci < ncand; ++ci) {
         const int CB = cb_cands[ci];
         const int NCH = CB / CHUNK;
         const int rows = round_up(128 * mh + max_off + (pair_taps ? 1 : 0), 8);
         const long long a_bytes = (long long)p.npl * NCH * rows * 16;
         const long long b_bytes = (long long)p.max_taps_ph * NCH * NT * 16;
-        const long long fixed = (long long)p.npl * rows * 4 + 8 * (3 * 4 + 5) + 16 + 1024;
+        const long long fixed = (long long)p.npl * rows * 4 + 8ll * p.ntaps_total + 8 * (3 * 4 + 6) + 24 + 4 * 4 + 1024;
         const long long per = a_bytes + b_bytes;
         long long stages = ((long long)budget - fixed) / per;
         if (stages < 2) continue;
@@ -232,8 +247,9 @@ void order_phase_taps(std::vector<int>& pl, std::vector<int>& off, std::vector<i
   }
 }
 
-int build_fwd(const Desc& d, const void* x, const void* w, void* y, void* ws, const DevInfo& di,
+int build_fwd(const Desc& d0, const void* x, const void* w, void* y, void* ws, const DevInfo& di,
               TapBuild& b) {
+  const Desc d = flatten_pointwise(d0);
   TapPlan& p = b.p;
   std::memset(&p, 0, sizeof(p));
   p.src = x;
@@ -246,7 +262,11 @@ int build_fwd(const Desc& d, const void* x, const void* w, void* y, void* ws, co
   p.Hd = d.P;
   p.Wd = d.Q;
   const int mh = (d.R - 1) / d.sh, mw = (d.S - 1) / d.sw;
-  p.WL = d.Q + mw;
+  const int CHUNK = d.dt == 0 ? 4 : 8;
+  // 16-byte row loads need unit column stride, rows whose width is a multiple of a chunk,
+  // and a linear row width that keeps chunk alignment from row to row.
+  const bool vec_geom = d.sw == 1 && d.W % CHUNK == 0;
+  p.WL = vec_geom ? round_up(d.Q + mw, CHUNK) : d.Q + mw;
   p.EL = d.P + mh;
   p.Mtot = (long long)d.N * p.EL * p.WL;
   p.npl = d.sh * d.sw;
@@ -256,11 +276,12 @@ int build_fwd(const Desc& d, const void* x, const void* w, void* y, void* ws, co
     for (int bb = 0; bb < d.sw; ++bb) {
       p.pl_off_h[a * d.sw + bb] = a - d.ph;
       p.pl_off_w[a * d.sw + bb] = bb - d.pw;
+      p.vec_phase[a * d.sw + bb] = ((d.pw - bb) % CHUNK + CHUNK) % CHUNK;
     }
+  p.vec = vec_geom && ((uintptr_t)x & 15) == 0;
   p.nph = 1;
   p.ph_step_h = 1;
   p.ph_step_w = 1;
-  const int CHUNK = d.dt == 0 ? 4 : 8;
   const bool pair = d.C <= CHUNK;
   std::vector<int> tpl, toff, tr, ts;
   int max_off = 0;
@@ -289,8 +310,9 @@ int build_fwd(const Desc& d, const void* x, const void* w, void* y, void* ws, co
   return CONV2D_OK;
 }
 
-int build_bwd_data(const Desc& d, const void* dy, const void* w, void* dx, void* ws, const DevInfo& di,
+int build_bwd_data(const Desc& d0, const void* dy, const void* w, void* dx, void* ws, const DevInfo& di,
                    TapBuild& b) {
+  const Desc d = flatten_pointwise(d0);
   TapPlan& p = b.p;
   std::memset(&p, 0, sizeof(p));
   p.src = dy;
@@ -335,6 +357,9 @@ int build_bwd_data(const Desc& d, const void* dy, const void* w, void* dx, void*
     WL = std::max(WL, Uw[c]);
     if (Tw[c] > 0) WL = std::max(WL, Uw[c] + ulow[c] + T0w);
   }
+  const int CHUNK = d.dt == 0 ? 4 : 8;
+  const bool vec_geom = d.Q % CHUNK == 0;
+  if (vec_geom) WL = round_up(WL, CHUNK);
   p.WL = WL;
   p.EL = EL;
   p.Mtot = (long long)d.N * EL * WL;
@@ -343,10 +368,11 @@ int build_bwd_data(const Desc& d, const void* dy, const void* w, void* dx, void*
   p.pl_step_w = 1;
   p.pl_off_h[0] = -T0h;
   p.pl_off_w[0] = -T0w;
+  p.vec_phase[0] = T0w % CHUNK;
+  p.vec = vec_geom && ((uintptr_t)dy & 15) == 0;
   p.nph = d.sh * d.sw;
   p.ph_step_h = d.sh;
   p.ph_step_w = d.sw;
-  const int CHUNK = d.dt == 0 ? 4 : 8;
   const bool pair = d.K <= CHUNK;
   std::vector<int> tpl, toff, tr, ts;
   int max_off = 0, max_taps = 0;
@@ -394,8 +420,9 @@ struct WgradBuild {
   int grid;
 };
 
-int build_bwd_filter(const Desc& d, const void* x, const void* dy, void* dw, void* ws, const DevInfo& di,
+int build_bwd_filter(const Desc& d0, const void* x, const void* dy, void* dw, void* ws, const DevInfo& di,
                      WgradBuild& b) {
+  const Desc d = flatten_pointwise(d0);
   WgradPlan& p = b.p;
   std::memset(&p, 0, sizeof(p));
   p.x = x;
@@ -410,7 +437,18 @@ int build_bwd_filter(const Desc& d, const void* x, const void* dy, void* dw, voi
   p.Q = d.Q;
   const int mh = (d.R - 1) / d.sh, mw = (d.S - 1) / d.sw;
   // fp32: WL a multiple of 4 so that a tap's offset mod 4 depends on its column only.
-  p.WL = d.dt == 0 ? round_up(d.Q + mw, 4) : d.Q + mw;
+  // bf16: WL a multiple of 8 (16-byte dy chunks) when that wastes at most 1/8 of it.
+  if (d.dt == 0) {
+    p.WL = round_up(d.Q + mw, 4);
+  } else {
+    const int wl8 = round_up(d.Q + mw, 8);
+    p.WL = (8 * (wl8 - (d.Q + mw)) <= wl8) ? wl8 : d.Q + mw;
+  }
+  {
+    const int ch = d.dt == 0 ? 4 : 8;
+    p.vec_dy = d.Q % ch == 0 && p.WL % ch == 0 && ((uintptr_t)dy & 15) == 0;
+    p.vec_x = d.sw == 1 && d.W % ch == 0 && p.WL % ch == 0 && ((uintptr_t)x & 15) == 0;
+  }
   p.EL = d.P + mh;
   p.Mtot = (long long)d.N * p.EL * p.WL;
   p.npl = d.sh * d.sw;
@@ -420,6 +458,7 @@ int build_bwd_filter(const Desc& d, const void* x, const void* dy, void* dw, voi
     for (int c = 0; c < d.sw; ++c) {
       p.pl_off_h[a * d.sw + c] = a - d.ph;
       p.pl_off_w[a * d.sw + c] = c - d.pw;
+      p.vec_phase[a * d.sw + c] = ((d.pw - c) % 8 + 8) % 8;
     }
   p.ntaps = d.R * d.S;
   if (p.ntaps > kMaxTaps) return CONV2D_ERR_UNSUPPORTED;
@@ -443,6 +482,10 @@ int build_bwd_filter(const Desc& d, const void* x, const void* dy, void* dw, voi
   }
   auto tap_plane = [&](int id) { return ((id / d.S) % d.sh) * d.sw + ((id % d.S) % d.sw); };
   auto tap_off = [&](int id) { return ((id / d.S) / d.sh) * p.WL + (id % d.S) / d.sw; };
+  // fp32: x is staged from x_shift positions before the group's first chunk, chosen so
+  // that (for unit column stride) chunk starts fall on 16-byte aligned columns.
+  p.x_shift = (d.dt == 0 && d.sw == 1) ? (4 - d.pw % 4) % 4 : 0;
+  auto tap_soff = [&](int id) { return tap_off(id) + p.x_shift; };
   int max_off = 0;
   for (int t = 0; t < p.ntaps; ++t) max_off = std::max(max_off, tap_off(t));
   const size_t budget = di.smem_optin - 2048;
@@ -461,31 +504,48 @@ int build_bwd_filter(const Desc& d, const void* x, const void* dy, void* dw, voi
         p.tg_count[ng] = cnt;
         int qmin = INT_MAX, qmax = 0;
         for (int i = 0; i < cnt; ++i) {
-          const int off = tap_off(g[i0 + i]);
+          const int off = tap_soff(g[i0 + i]);
           qmin = std::min(qmin, off >> 2);
           qmax = std::max(qmax, off >> 2);
         }
         p.tg_qmin[ng] = d.dt == 0 ? qmin : 0;
         p.tg_slot_begin[ng] = nsl;
-        for (int i = 0; i < cnt; ++i) {
+        auto find_slot = [&](int plane, int res) {
+          int u = p.tg_slot_begin[ng];
+          while (u < nsl && !(p.slot_plane[u] == plane && p.slot_res[u] == res)) ++u;
+          if (u == nsl) {
+            if (nsl == kMaxSlots) return -1;
+            p.slot_plane[u] = plane;
+            p.slot_res[u] = res;
+            ++nsl;
+          }
+          return u;
+        };
+        for (int i = 0; i < cnt && ok; ++i) {
           const int id = g[i0 + i];
           const int t = nt + i;
           p.tap_id[t] = id;
           p.tap_plane[t] = tap_plane(id);
           p.tap_off[t] = tap_off(id);
-          p.tap_q[t] = (p.tap_off[t] >> 2) - p.tg_qmin[ng];
-          const int res = p.tap_off[t] & 3;
-          int u = p.tg_slot_begin[ng];
-          while (u < nsl && !(p.slot_plane[u] == p.tap_plane[t] && p.slot_res[u] == res)) ++u;
-          if (u == nsl) {
-            if (nsl == kMaxSlots) { ok = false; break; }
-            p.slot_plane[u] = p.tap_plane[t];
-            p.slot_res[u] = res;
-            ++nsl;
+          const int soff = tap_soff(id);
+          p.tap_q[t] = (soff >> 2) - p.tg_qmin[ng];
+          if (d.dt == 0) {
+            // every plane of the group has a residue-0 (base) slot the others derive from
+            if (find_slot(p.tap_plane[t], 0) < 0) { ok = false; break; }
+            const int u = find_slot(p.tap_plane[t], soff & 3);
+            if (u < 0) { ok = false; break; }
+            p.tap_slot[t] = u;
+          } else {
+            p.tap_slot[t] = 0;
           }
-          p.tap_slot[t] = u;
         }
         if (!ok) break;
+        if (d.dt == 0)
+          for (int u = p.tg_slot_begin[ng]; u < nsl; ++u) {
+            int b0 = p.tg_slot_begin[ng];
+            while (!(p.slot_plane[b0] == p.slot_plane[u] && p.slot_res[b0] == 0)) ++b0;
+            p.slot_base[u] = b0;
+          }
         p.tg_nslots[ng] = nsl - p.tg_slot_begin[ng];
         nsl_max = std::max(nsl_max, p.tg_nslots[ng]);
         qspan_max = std::max(qspan_max, d.dt == 0 ? qmax - qmin : 0);
@@ -505,15 +565,16 @@ int build_bwd_filter(const Desc& d, const void* x, const void* dy, void* dw, voi
       long long b_bytes;
       if (d.dt == 0) {
         p.nchunks = KB / 4 + qspan_max;
-        rows = round_up(4 * p.nchunks + 3, 8);
-        b_bytes = (long long)nsl_max * p.nchunks * NC * 16;
+        p.slot_chunks = p.nchunks + 1;
+        rows = round_up(4 * p.slot_chunks, 8);
+        b_bytes = (long long)nsl_max * p.slot_chunks * NC * 16;
       } else {
         p.nchunks = 0;
         rows = round_up(KB + max_off, 8);
         b_bytes = (long long)p.npl * (NC / CHUNK) * rows * 16;
       }
       const long long a_bytes = (long long)KB * 128 * ESZ;
-      const long long fixed = (long long)(KB + p.npl * rows) * 4 + 8 * (2 * 4 + 3) + 16 + 1024;
+      const long long fixed = 2ll * (KB + p.npl * rows) * 4 + 4ll * p.ntaps + 8 * (2 * 4 + 3) + 16 + 1024;
       long long stages = ((long long)budget - fixed) / (a_bytes + b_bytes);
       if (stages < 2) continue;
       if (stages > 4) stages = 4;

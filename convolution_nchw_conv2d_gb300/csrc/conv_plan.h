@@ -51,6 +51,8 @@ struct TapPlan {
   int ACCB;              // TMEM accumulator buffers (1 or 2)
   int a_stage_bytes, b_stage_bytes;
   int tmem_cols;
+  int vec;               // source rows may be read with 16-byte loads (see stage_pixel_rows)
+  int vec_phase[kMaxPlanes];
 };
 
 // Filter packing for TapPlan: one 16-byte chunk per (n_tile, k_block, tap, chunk, row).
@@ -93,6 +95,9 @@ struct WgradPlan {
   int tap_slot[kMaxTaps], tap_q[kMaxTaps];      // fp32
   int nslots;
   int slot_plane[kMaxSlots], slot_res[kMaxSlots];
+  int slot_base[kMaxSlots];        // fp32: residue-0 slot of the same plane and group
+  int slot_chunks;                 // fp32: chunks staged per slot (nchunks + 1)
+  int x_shift;                     // fp32: staged x origin offset (aligns chunk starts)
   int n_tgroups;
   int tg_begin[kMaxTaps], tg_count[kMaxTaps];
   int tg_qmin[kMaxTaps], tg_slot_begin[kMaxTaps], tg_nslots[kMaxTaps];
@@ -107,6 +112,9 @@ struct WgradPlan {
   int KB;                // positions per pipeline stage
   int a_stage_bytes, b_stage_bytes;
   int tmem_cols;
+  int vec_dy;            // dy chunks may be copied with 16-byte cp.async
+  int vec_x;             // x rows may be read with 16-byte loads
+  int vec_phase[kMaxPlanes];  // bf16 x: see stage_pixel_rows
 };
 
 struct ReducePlan {

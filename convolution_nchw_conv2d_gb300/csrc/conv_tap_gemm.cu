@@ -11,18 +11,20 @@
 // this is deconvolution forward with the weight's in/out roles swapped (Apache
 // MXNet mkldnn_deconvolution.cc, MKLDNNDeconvFwd::Execute comment).
 //
-// CTA roles (288 threads, persistent over tiles):
-//   warps 0-3  producers: stage source rows for CB channels into shared memory in
-//              the core-matrix interleaved layout (fp32: 4-byte cp.async with zero
-//              fill; bf16: register gather), and bulk-copy the packed filter slice.
-//   warps 4-7  epilogue: TMEM -> registers -> NCHW global stores, coalesced along
+// CTA roles (416 threads, persistent over tiles):
+//   warps 0-7  two producer groups taking pipeline stages in turn: stage source rows
+//              for CB channels into shared memory in the core-matrix interleaved layout
+//              (16-byte loads + register transpose where rows are contiguous, scalar
+//              loads elsewhere), and bulk-copy the packed filter slice.
+//   warps 8-11 epilogue: TMEM -> registers -> NCHW global stores, coalesced along
 //              output positions; bf16 outputs rounded to nearest even.
-//   warp 8     TMEM allocation; lane 0 issues tcgen05.mma (kind::tf32 for fp32,
-//              kind::f16 with bf16 operands) accumulating in TMEM.
+//   warps 12-13 TMEM allocation (warp 12); lane 0 of each issues tcgen05.mma (kind::tf32
+//              for fp32, kind::f16 with bf16 operands) for one 128-row accumulator half.
 #include <mutex>
 #include <vector>
 
 #include "conv_plan.h"
+#include "conv_stage.cuh"
 #include "sm103_ptx.cuh"
 
 namespace cg3 {
@@ -31,14 +33,14 @@ __device__ int g_tap_err;
 
 namespace {
 
-constexpr int kThreads = 288;
-constexpr int kProdThreads = 128;
-
-struct TapSmem {
-  uint32_t a0, b0;       // stage region bases (shared addresses)
-  int* rowtab;
-  uint32_t full, bfull, empty, accf, acce, drain;  // barrier arrays (shared addresses)
-};
+// CTA roles: warps 0-7 two producer groups (group g fills the stages with global stage
+// counter = g mod 2), warps 8-11 epilogue, warp 12 TMEM allocation + MMA issue for the
+// first 128-row half of a tile, warp 13 MMA issue for the second half (one issuing
+// thread per accumulator: a single thread can issue roughly one MMA per 50 cycles).
+constexpr int kThreads = 448;
+constexpr int kProdThreads = 128;  // per producer group
+constexpr int kEpiWarp0 = 8;
+constexpr int kMmaWarp = 12;
 
 __device__ __forceinline__ uint32_t bar_at(uint32_t base, int i) { return base + 8u * (uint32_t)i; }
 
@@ -82,43 +84,60 @@ __global__ void __launch_bounds__(kThreads, 1) tap_gemm_kernel(const __grid_cons
 
   // ---- shared memory carve-up
   uint8_t* ptr = smem_raw;
-  TapSmem sm;
-  sm.a0 = smem_u32(ptr);
+  const uint32_t a0 = smem_u32(ptr);
   ptr += (size_t)S * p.a_stage_bytes;
-  sm.b0 = smem_u32(ptr);
+  const uint32_t b0 = smem_u32(ptr);
   ptr += (size_t)S * p.b_stage_bytes;
-  sm.rowtab = reinterpret_cast<int*>(ptr);
+  int* rowtab = reinterpret_cast<int*>(ptr);
   ptr += (size_t)p.npl * rows * sizeof(int);
+  // Per tap: {A operand offset, B operand offset} relative to the stage bases, in 16-byte
+  // units (in tap-pair mode the A entry of a pair's first tap also carries the chunk
+  // stride to the second tap in bits 16..29, the descriptor's leading-byte-offset field).
+  uint2* tapo = reinterpret_cast<uint2*>(ptr);
+  ptr += (size_t)p.ntaps_total * sizeof(uint2);
   ptr = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(ptr) + 15) & ~uintptr_t(15));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(ptr);
-  sm.full = smem_u32(bars);
-  sm.bfull = sm.full + 8u * S;
-  sm.empty = sm.bfull + 8u * S;
-  sm.accf = sm.empty + 8u * S;
-  sm.acce = sm.accf + 16u;
-  sm.drain = sm.acce + 16u;
-  ptr += 8 * (3 * S + 5);
+  const uint32_t full = smem_u32(ptr);
+  const uint32_t empty = full + 8u * S;
+  const uint32_t accf = empty + 8u * S;
+  const uint32_t acce = accf + 16u;
+  const uint32_t drain = acce + 16u;  // two entries, one per issuer
+  ptr += 8 * (2 * S + 6);
   volatile uint32_t* tmem_holder = reinterpret_cast<volatile uint32_t*>(ptr);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(ptr + 4);
+  // Per stage slot: 0 = never used, else 1 + parity of the last bulk copy issued into it.
+  volatile int* last_copy = reinterpret_cast<volatile int*>(ptr + 8);
 
+  const int nissuers = p.MH;  // one MMA-issuing thread per 128-row accumulator half
   if (tid == 0) {
     for (int s = 0; s < S; ++s) {
-      mbar_init(bar_at(sm.full, s), kProdThreads);
-      mbar_init(bar_at(sm.bfull, s), 1);
-      mbar_init(bar_at(sm.empty, s), 1);
+      mbar_init(bar_at(full, s), kProdThreads);  // + the filter copy's transaction bytes
+      mbar_init(bar_at(empty, s), (uint32_t)nissuers);
     }
     for (int a = 0; a < 2; ++a) {
-      mbar_init(bar_at(sm.accf, a), 1);
-      mbar_init(bar_at(sm.acce, a), 4);
+      mbar_init(bar_at(accf, a), (uint32_t)nissuers);
+      mbar_init(bar_at(acce, a), 4);
     }
-    mbar_init(sm.drain, 1);
+    mbar_init(drain, 1);
+    mbar_init(drain + 8u, 1);
     *abort_flag = 0;
+    for (int s = 0; s < S; ++s) last_copy[s] = 0;
     fence_mbar_init();
   }
-  if (warp == 8) {
+  if (warp == kMmaWarp) {
     tmem_alloc(smem_u32((const void*)tmem_holder), (uint32_t)p.tmem_cols);
     tmem_relinquish();
   }
+  for (int ph = 0; ph < p.nph; ++ph)
+    for (int i = tid; i < p.ph_ntaps[ph]; i += kThreads) {
+      const int t = p.ph_tap_begin[ph] + i;
+      const uint32_t oa = (uint32_t)(p.tap_plane[t] * NCH * rows + p.tap_off[t]);
+      if (NCH >= 2) {
+        tapo[t] = make_uint2(oa, (uint32_t)(i * NCH * p.NT));
+      } else if ((i & 1) == 0) {
+        const uint32_t ob = (uint32_t)(p.tap_plane[t + 1] * rows + p.tap_off[t + 1]);
+        tapo[t] = make_uint2(oa | ((ob - oa) << 16), (uint32_t)(i * p.NT));
+      }
+    }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -130,23 +149,22 @@ __global__ void __launch_bounds__(kThreads, 1) tap_gemm_kernel(const __grid_cons
   const int MT = 128 * p.MH;
   const int b_tap_bytes = NCH * p.NT * 16;
 
-  if (warp < 4) {
+  if (warp < kEpiWarp0) {
     // =============================================================== producers
-    const int ptid = tid;
-    int stage = 0;
-    uint32_t ephase = 0;
-    int pending = -1;  // fp32: stage whose cp.async group is still in flight
+    const int grp = warp >> 2;           // producer group 0 or 1
+    const int gtid = tid & (kProdThreads - 1);
+    long long counter = 0;               // global stage counter (both groups count all stages)
     bool ok = true;
-    // Per stage slot: parity of the last bulk copy issued into it (for the exit drain).
-    uint32_t issued_mask = 0, issued_par = 0;
-    for (long long t = blockIdx.x; t < p.total_tiles && ok; t += gridDim.x) {
+    // Both groups meet at named barriers once per tile, so after an abort a group keeps
+    // walking the tiles (skipping all work) until the end instead of leaving early.
+    for (long long t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
       const TileCoord tc = decode_tile(p, t);
       const int ntaps = p.ph_ntaps[tc.ph];
       if (ntaps == 0) continue;
       const long long m0 = (long long)tc.mt * MT;
-      // Row table: source offset (channel 0) of every staged row of every plane.
-      named_bar_sync(1, kProdThreads);
-      for (int i = ptid; i < p.npl * rows; i += kProdThreads) {
+      // Row table (both groups): source offset of channel 0 for every staged row.
+      named_bar_sync(1, 2 * kProdThreads);
+      for (int i = tid; i < p.npl * rows; i += 2 * kProdThreads) {
         const int pl = i / rows;
         const int row = i - pl * rows;
         const long long L = m0 + row;
@@ -161,109 +179,47 @@ __global__ void __launch_bounds__(kThreads, 1) tap_gemm_kernel(const __grid_cons
           if (h >= 0 && h < p.Hs && w >= 0 && w < p.Ws)
             off = (int)((long long)n * p.Cs * HsWs + (long long)h * p.Ws + w);
         }
-        sm.rowtab[i] = off;
+        rowtab[i] = off;
       }
-      named_bar_sync(1, kProdThreads);
-      for (int kb = 0; kb < p.nkb; ++kb) {
-        if (!mbar_wait(bar_at(sm.empty, stage), ephase ^ 1u, abort_flag, &g_tap_err)) {
+      named_bar_sync(1, 2 * kProdThreads);
+      for (int kb = 0; kb < p.nkb; ++kb, ++counter) {
+        if ((int)(counter & 1) != grp || !ok) continue;
+        const int stage = (int)(counter % S);
+        const uint32_t ephase = (uint32_t)((counter / S) & 1);
+        if (!mbar_wait(bar_at(empty, stage), ephase ^ 1u, abort_flag, &g_tap_err)) {
           ok = false;
-          break;
+          continue;
         }
-        const uint32_t a_st = sm.a0 + (uint32_t)stage * p.a_stage_bytes;
-        const uint32_t b_st = sm.b0 + (uint32_t)stage * p.b_stage_bytes;
-        if (ptid == 0) {
+        const uint32_t a_st = a0 + (uint32_t)stage * p.a_stage_bytes;
+        const uint32_t b_st = b0 + (uint32_t)stage * p.b_stage_bytes;
+        if (gtid == 0) {
           const uint32_t bytes = (uint32_t)(ntaps * b_tap_bytes);
           const long long img_off =
               ((long long)(tc.nt * p.nkb + kb) * p.ntaps_total + p.ph_tap_begin[tc.ph]) * b_tap_bytes;
-          mbar_arrive_expect_tx(bar_at(sm.bfull, stage), bytes);
-          bulk_g2s(b_st, static_cast<const uint8_t*>(p.wpack) + img_off, bytes, bar_at(sm.bfull, stage));
-          issued_mask |= 1u << stage;
-          issued_par = (issued_par & ~(1u << stage)) | (ephase << stage);
+          // The copy completes on the stage's full barrier: its bytes are expected there
+          // before it is issued, and this thread arrives with the others after its fill.
+          mbar_expect_tx(bar_at(full, stage), bytes);
+          bulk_g2s(b_st, static_cast<const uint8_t*>(p.wpack) + img_off, bytes, bar_at(full, stage));
+          last_copy[stage] = 1 + (int)ephase;
         }
-        const int cbase = kb * p.CB;
-        if constexpr (DT == 0) {
-          // fp32: lane = (row within 8, channel within chunk); one warp instruction
-          // fills 8 rows x 16 bytes = 128 contiguous bytes.
-          const float* src = static_cast<const float*>(p.src);
-          const int c4 = lane & 3;
-          const int rsub = lane >> 2;
-          for (int pj = 0; pj < p.npl * NCH; ++pj) {
-            const int pl = pj / NCH;
-            const int j = pj - pl * NCH;
-            const int cs = cbase + j * 4 + c4;
-            const bool cv = cs < p.Cs;
-            const float* gc = src + (long long)(cv ? cs : 0) * HsWs;
-            const uint32_t dbase = a_st + (uint32_t)(pj * rows) * 16u + (uint32_t)c4 * 4u;
-            const int* tab = sm.rowtab + pl * rows;
-#pragma unroll 4
-            for (int row = warp * 8 + rsub; row < rows; row += 32) {
-              const int off = tab[row];
-              const bool v = cv && off >= 0;
-              cp_async_4(dbase + (uint32_t)row * 16u, v ? gc + off : src, v);
-            }
-          }
-          cp_async_commit();
-          if (pending >= 0) {
-            cp_async_wait<1>();
-            fence_proxy_async();
-            mbar_arrive(bar_at(sm.full, pending));
-          }
-          pending = stage;
-        } else {
-          // bf16: one thread gathers 8 channels of one row and writes one 16-byte chunk.
-          const uint16_t* src = static_cast<const uint16_t*>(p.src);
-          for (int pj = 0; pj < p.npl * NCH; ++pj) {
-            const int pl = pj / NCH;
-            const int j = pj - pl * NCH;
-            const int c0 = cbase + j * 8;
-            const int nv = min(8, p.Cs - c0);
-            const uint16_t* gc = src + (long long)(nv > 0 ? c0 : 0) * HsWs;
-            const int* tab = sm.rowtab + pl * rows;
-            const uint32_t dbase = a_st + (uint32_t)(pj * rows) * 16u;
-#pragma unroll 2
-            for (int row = ptid; row < rows; row += kProdThreads) {
-              const int off = tab[row];
-              uint32_t wv[4] = {0u, 0u, 0u, 0u};
-              if (off >= 0) {
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                  if (e < nv) {
-                    const uint32_t v = __ldg(gc + off + (long long)e * HsWs);
-                    wv[e >> 1] |= v << (16 * (e & 1));
-                  }
-                }
-              }
-              asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(dbase + (uint32_t)row * 16u),
-                           "r"(wv[0]), "r"(wv[1]), "r"(wv[2]), "r"(wv[3])
-                           : "memory");
-            }
-          }
-          fence_proxy_async();
-          mbar_arrive(bar_at(sm.full, stage));
-        }
-        if (++stage == S) {
-          stage = 0;
-          ephase ^= 1u;
-        }
-      }
-    }
-    if constexpr (DT == 0) {
-      cp_async_wait<0>();
-      if (pending >= 0 && ok) {
+        stage_pixel_rows<DT>(p.src, HsWs, p.Cs, rowtab, p.npl, rows, a_st, kb * p.CB, NCH, p.vec != 0,
+                             p.vec_phase, gtid);
         fence_proxy_async();
-        mbar_arrive(bar_at(sm.full, pending));
+        mbar_arrive(bar_at(full, stage));
       }
     }
-    // Drain: never leave a bulk copy in flight into shared memory that is about to be
-    // released.  In a normal run every one of these has long completed.
-    if (ptid == 0) {
-      for (int s = 0; s < S; ++s) {
-        if (issued_mask & (1u << s)) {
-          mbar_wait_drain(bar_at(sm.bfull, s), (issued_par >> s) & 1u);
-        }
-      }
+    // After an abort, never leave a bulk copy in flight into shared memory that is about
+    // to be released.  (In a normal run the MMA lane has waited on every copy.)  The copy
+    // completes on the stage's full barrier together with the producers' arrivals, so
+    // after an abort its phase may never complete: the bounded drain then gives up after
+    // its time limit.  Slots are shared by both groups, so the last copy per slot is known
+    // only after both groups are done issuing.
+    named_bar_sync(1, 2 * kProdThreads);
+    if (tid == 0 && *abort_flag) {
+      for (int s = 0; s < S; ++s)
+        if (last_copy[s]) mbar_wait_drain(bar_at(full, s), (uint32_t)(last_copy[s] - 1));
     }
-  } else if (warp < 8) {
+  } else if (warp < kMmaWarp) {
     // =============================================================== epilogue
     const int q = warp & 3;
     int acc = 0;
@@ -273,7 +229,7 @@ __global__ void __launch_bounds__(kThreads, 1) tap_gemm_kernel(const __grid_cons
       const int ntaps = p.ph_ntaps[tc.ph];
       const long long m0 = (long long)tc.mt * MT;
       if (ntaps != 0) {
-        if (!mbar_wait(bar_at(sm.accf, acc), aphase, abort_flag, &g_tap_err)) break;
+        if (!mbar_wait(bar_at(accf, acc), aphase, abort_flag, &g_tap_err)) break;
         tc_fence_after();
       }
       for (int h = 0; h < p.MH; ++h) {
@@ -291,28 +247,57 @@ __global__ void __launch_bounds__(kThreads, 1) tap_gemm_kernel(const __grid_cons
           valid = oh >= 0 && oh < p.Hd && ow >= 0 && ow < p.Wd;
           obase = (long long)n * p.Cd * HdWd + (long long)oh * p.Wd + ow;
         }
-        for (int c0 = 0; c0 < p.NT; c0 += 16) {
-          uint32_t r[16];
-          if (ntaps != 0) {
-            tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)((acc * p.MH + h) * p.NT + c0), r);
-            tmem_ld_wait();
-          } else {
+        const uint32_t tcol = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)((acc * p.MH + h) * p.NT);
+        const int nbase = tc.nt * p.NT;
+        const int nvalid = min(p.NT, p.Cd - nbase);  // output channels of this tile (NT is a multiple of 16)
+        // 16-column chunks; the TMEM load of chunk i+1 is in flight while chunk i is stored.
+        const int nchunk = (nvalid + 15) >> 4;
+        uint32_t ra[16], rb[16];
+        if (ntaps != 0) {
+          tmem_ld16(tcol, ra);
+          tmem_ld_wait();
+        } else {
 #pragma unroll
-            for (int j = 0; j < 16; ++j) r[j] = 0u;
-          }
+          for (int j = 0; j < 16; ++j) ra[j] = rb[j] = 0u;
+        }
+        const long long ostep = HdWd;
+        for (int ci = 0; ci < nchunk; ci += 2) {
+          const bool two = ci + 1 < nchunk;
+          if (ntaps != 0 && two) tmem_ld16(tcol + (uint32_t)(16 * (ci + 1)), rb);
           if (valid) {
+            const long long ob = obase + (long long)(nbase + 16 * ci) * ostep;
+            const int lim = nvalid - 16 * ci;
+            if (lim >= 16) {
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const int nn = tc.nt * p.NT + c0 + j;
-              if (nn < p.Cd) store_out<DT>(p.dst, obase + (long long)nn * HdWd, r[j]);
+              for (int j = 0; j < 16; ++j) store_out<DT>(p.dst, ob + j * ostep, ra[j]);
+            } else {
+#pragma unroll
+              for (int j = 0; j < 16; ++j)
+                if (j < lim) store_out<DT>(p.dst, ob + j * ostep, ra[j]);
             }
           }
+          if (ntaps != 0 && two) tmem_ld_wait();
+          if (!two) break;
+          if (ntaps != 0 && ci + 2 < nchunk) tmem_ld16(tcol + (uint32_t)(16 * (ci + 2)), ra);
+          if (valid) {
+            const long long ob = obase + (long long)(nbase + 16 * (ci + 1)) * ostep;
+            const int lim = nvalid - 16 * (ci + 1);
+            if (lim >= 16) {
+#pragma unroll
+              for (int j = 0; j < 16; ++j) store_out<DT>(p.dst, ob + j * ostep, rb[j]);
+            } else {
+#pragma unroll
+              for (int j = 0; j < 16; ++j)
+                if (j < lim) store_out<DT>(p.dst, ob + j * ostep, rb[j]);
+            }
+          }
+          if (ntaps != 0 && ci + 2 < nchunk) tmem_ld_wait();
         }
       }
       if (ntaps != 0) {
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar_at(sm.acce, acc));
+        if (lane == 0) mbar_arrive(bar_at(acce, acc));
         if (++acc == p.ACCB) {
           acc = 0;
           aphase ^= 1u;
@@ -320,11 +305,14 @@ __global__ void __launch_bounds__(kThreads, 1) tap_gemm_kernel(const __grid_cons
       }
     }
   } else {
-    // =============================================================== MMA issuer
-    if (lane == 0) {
+    // =============================================================== MMA issuers
+    const int issuer = warp - kMmaWarp;  // accumulator half this thread owns
+    if (lane == 0 && issuer < nissuers) {
       const uint32_t id = idesc(KIND, 128, p.NT, 0, 0);
-      int stage = 0;
-      uint32_t fphase = 0;
+      // Descriptor high halves (stride byte offset 128 B, version) are constant.
+      const uint32_t d_hi = (uint32_t)(sdesc(0u, 0u, 128u) >> 32);
+      const uint32_t a_ks = 2u * (uint32_t)rows, b_ks = 2u * (uint32_t)p.NT;
+      long long counter = 0;
       int acc = 0;
       uint32_t aphase = 0;
       bool ok = true;
@@ -334,34 +322,30 @@ __global__ void __launch_bounds__(kThreads, 1) tap_gemm_kernel(const __grid_cons
         const int ntaps = p.ph_ntaps[tc.ph];
         if (ntaps == 0) continue;
         const int tap0 = p.ph_tap_begin[tc.ph];
-        if (!mbar_wait(bar_at(sm.acce, acc), aphase ^ 1u, abort_flag, &g_tap_err)) break;
+        if (!mbar_wait(bar_at(acce, acc), aphase ^ 1u, abort_flag, &g_tap_err)) break;
         tc_fence_after();
-        const uint32_t dcol = tmem + (uint32_t)(acc * p.MH * p.NT);
-        for (int kb = 0; kb < p.nkb; ++kb) {
-          if (!mbar_wait(bar_at(sm.full, stage), fphase, abort_flag, &g_tap_err) ||
-              !mbar_wait(bar_at(sm.bfull, stage), fphase, abort_flag, &g_tap_err)) {
+        const uint32_t dcol = tmem + (uint32_t)((acc * p.MH + issuer) * p.NT);
+        for (int kb = 0; kb < p.nkb; ++kb, ++counter) {
+          const int stage = (int)(counter % S);
+          const uint32_t fphase = (uint32_t)((counter / S) & 1);
+          if (!mbar_wait(bar_at(full, stage), fphase, abort_flag, &g_tap_err)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          fence_proxy_async();
-          const uint32_t a_st = sm.a0 + (uint32_t)stage * p.a_stage_bytes;
-          const uint32_t b_st = sm.b0 + (uint32_t)stage * p.b_stage_bytes;
+          // Low descriptor halves of this stage's operands (this issuer's 128 rows of A).
+          const uint32_t a_st = a0 + (uint32_t)stage * p.a_stage_bytes + (uint32_t)issuer * 128u * 16u;
+          const uint32_t b_lo0 = (uint32_t)sdesc(b0 + (uint32_t)stage * p.b_stage_bytes, (uint32_t)p.NT * 16u, 0u);
           if (NCH >= 2) {
+            const uint32_t a_lo0 = (uint32_t)sdesc(a_st, (uint32_t)rows * 16u, 0u);
             for (int ti = 0; ti < ntaps; ++ti) {
-              const int tap = tap0 + ti;
-              const uint32_t a_pl = a_st + (uint32_t)(p.tap_plane[tap] * NCH * rows) * 16u +
-                                    (uint32_t)p.tap_off[tap] * 16u;
-              const uint32_t b_tp = b_st + (uint32_t)(ti * b_tap_bytes);
+              const uint2 o = tapo[tap0 + ti];
+              uint32_t alo = a_lo0 + o.x, blo = b_lo0 + o.y;
+              const uint32_t acc_in = (kb | ti) ? 1u : 0u;
               for (int ks = 0; ks < NCH / 2; ++ks) {
-                const uint64_t bd =
-                    sdesc(b_tp + (uint32_t)(2 * ks * p.NT) * 16u, (uint32_t)p.NT * 16u, 128u);
-                const uint32_t first = (kb == 0 && ti == 0 && ks == 0) ? 0u : 1u;
-                for (int h = 0; h < p.MH; ++h) {
-                  const uint64_t ad = sdesc(a_pl + (uint32_t)(2 * ks * rows) * 16u + (uint32_t)(h * 128) * 16u,
-                                            (uint32_t)rows * 16u, 128u);
-                  mma_ss<KIND>(dcol + (uint32_t)(h * p.NT), ad, bd, id, first);
-                }
+                mma_ss_lh<KIND>(dcol, alo, d_hi, blo, d_hi, id, acc_in | (uint32_t)ks);
+                alo += a_ks;
+                blo += b_ks;
               }
             }
           } else {
@@ -369,36 +353,26 @@ __global__ void __launch_bounds__(kThreads, 1) tap_gemm_kernel(const __grid_cons
             // K-chunk is the next tap's rows, reached through the descriptor's chunk
             // stride (taps are sorted by staged address; a padding tap with zero
             // weights repeats the last address).
+            const uint32_t a_lo0 = (uint32_t)sdesc(a_st, 0u, 0u);
             for (int ti = 0; ti < ntaps; ti += 2) {
-              const int t0 = tap0 + ti, t1 = t0 + 1;
-              const uint32_t a0 = a_st + (uint32_t)(p.tap_plane[t0] * rows + p.tap_off[t0]) * 16u;
-              const uint32_t a1 = a_st + (uint32_t)(p.tap_plane[t1] * rows + p.tap_off[t1]) * 16u;
-              const uint64_t bd = sdesc(b_st + (uint32_t)(ti * b_tap_bytes), (uint32_t)p.NT * 16u, 128u);
-              const uint32_t first = (kb == 0 && ti == 0) ? 0u : 1u;
-              for (int h = 0; h < p.MH; ++h) {
-                const uint64_t ad = sdesc(a0 + (uint32_t)(h * 128) * 16u, a1 - a0, 128u);
-                mma_ss<KIND>(dcol + (uint32_t)(h * p.NT), ad, bd, id, first);
-              }
+              const uint2 o = tapo[tap0 + ti];
+              mma_ss_lh<KIND>(dcol, a_lo0 + o.x, d_hi, b_lo0 + o.y, d_hi, id, (kb | ti) ? 1u : 0u);
             }
           }
-          tc_commit(bar_at(sm.empty, stage));
+          tc_commit(bar_at(empty, stage));
           issued_any = true;
-          if (++stage == S) {
-            stage = 0;
-            fphase ^= 1u;
-          }
         }
         if (!ok) break;
-        tc_commit(bar_at(sm.accf, acc));
+        tc_commit(bar_at(accf, acc));
         if (++acc == p.ACCB) {
           acc = 0;
           aphase ^= 1u;
         }
       }
       if (!ok && issued_any) {
-        // Wait (bounded) for every MMA already issued before TMEM is released.
-        tc_commit(sm.drain);
-        mbar_wait_drain(sm.drain, 0);
+        // Wait (bounded) for every MMA this thread issued before TMEM is released.
+        tc_commit(drain + 8u * (uint32_t)issuer);
+        mbar_wait_drain(drain + 8u * (uint32_t)issuer, 0);
       }
     }
     __syncwarp();
@@ -406,7 +380,7 @@ __global__ void __launch_bounds__(kThreads, 1) tap_gemm_kernel(const __grid_cons
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 8) {
+  if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, (uint32_t)p.tmem_cols);
   }
@@ -461,9 +435,9 @@ __global__ void pack_filter_kernel(const __grid_constant__ PackPlan pp) {
 // ---------------------------------------------------------------------------- launchers
 size_t tap_gemm_smem_bytes(const TapPlan& p) {
   size_t b = (size_t)p.stages * (p.a_stage_bytes + p.b_stage_bytes);
-  b += (size_t)p.npl * p.rows * sizeof(int);
+  b += (size_t)p.npl * p.rows * sizeof(int) + (size_t)p.ntaps_total * sizeof(uint2);
   b = (b + 15) & ~size_t(15);
-  b += 8 * (3 * p.stages + 5) + 16;
+  b += 8 * (2 * p.stages + 6) + 8 + 4 * p.stages + 16;
   return b + 1024;  // alignment slack for the dynamic base
 }
 

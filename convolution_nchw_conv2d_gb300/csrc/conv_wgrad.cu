@@ -10,17 +10,19 @@
 //
 // One CTA tile = 128 output channels k x NC input channels c x a group of taps x one
 // range of positions (split-K).  Per pipeline stage (KB positions):
-//   producers (warps 0-3) stage dy[k, L] K-major and x in the core-matrix layout:
+//   producers (warps 0-7, two groups taking stages in turn) stage dy[k, L] K-major and
+//     x in the core-matrix layout:
 //     bf16 as an MN-major operand (channels along chunks, positions along rows, a
 //     tap is a row offset); fp32 as K-major copies per (plane, offset mod 4), since
 //     tf32 operands must be K-major (an MN-major tf32 B reads as zeros);
 //   the MMA lane copies each 128 x 32-byte dy slice into TMEM with tcgen05.cp and
 //     issues one tcgen05.mma per tap with A from TMEM and B = x at the tap's row
 //     offset, so dy is read from shared memory once for all taps;
-//   epilogue warps (4-7) write each tap's 128 x NC fp32 partial sums.
+//   epilogue warps (8-11) write each tap's 128 x NC fp32 partial sums.
 // A second kernel adds the split partials in a fixed order (deterministic) and
 // writes dw in KCRS, rounding to bf16 for bf16 tensors.
 #include "conv_plan.h"
+#include "conv_stage.cuh"
 #include "sm103_ptx.cuh"
 
 namespace cg3 {
@@ -28,8 +30,12 @@ namespace cg3 {
 __device__ int g_wgrad_err;
 
 namespace {
-constexpr int kThreads = 288;
+// CTA roles: warps 0-7 two producer groups taking pipeline stages in turn, warps 8-11
+// epilogue, warp 12 TMEM allocation + tcgen05.cp / tcgen05.mma issue.
+constexpr int kThreads = 416;
 constexpr int kProdThreads = 128;
+constexpr int kEpiWarp0 = 8;
+constexpr int kMmaWarp = 12;
 constexpr int kAbufCols = 32;  // 4 TMEM staging buffers of 8 columns for dy slices
 
 __device__ __forceinline__ uint32_t bar_at(uint32_t base, int i) { return base + 8u * (uint32_t)i; }
@@ -63,17 +69,19 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_kernel(const __grid_constan
   const int rows = p.rows;
   const int KB = p.KB;
   const int NCA = KB / CHUNK;     // dy chunks per stage
-  const int NCB = p.NC / CHUNK;   // x chunks per plane per stage
+  const int NCB = p.NC / CHUNK;   // bf16: x chunks per plane per stage
 
   uint8_t* ptr = smem_raw;
   const uint32_t a0 = smem_u32(ptr);
   ptr += (size_t)S * p.a_stage_bytes;
   const uint32_t b0 = smem_u32(ptr);
   ptr += (size_t)S * p.b_stage_bytes;
-  int* dytab = reinterpret_cast<int*>(ptr);
-  ptr += (size_t)KB * sizeof(int);
-  int* xtab = reinterpret_cast<int*>(ptr);
-  ptr += (size_t)p.npl * rows * sizeof(int);
+  const int tab_ints = KB + p.npl * rows;
+  int* tabs = reinterpret_cast<int*>(ptr);  // one table set per producer group
+  ptr += (size_t)2 * tab_ints * sizeof(int);
+  // Per plan tap: start of its B operand relative to the stage base, in 16-byte units.
+  uint32_t* tapb = reinterpret_cast<uint32_t*>(ptr);
+  ptr += (size_t)p.ntaps * sizeof(uint32_t);
   ptr = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(ptr) + 15) & ~uintptr_t(15));
   const uint32_t full = smem_u32(ptr);
   const uint32_t empty = full + 8u * S;
@@ -95,10 +103,17 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_kernel(const __grid_constan
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 8) {
+  if (warp == kMmaWarp) {
     tmem_alloc(smem_u32((const void*)tmem_holder), (uint32_t)p.tmem_cols);
     tmem_relinquish();
   }
+  for (int g = 0; g < p.n_tgroups; ++g)
+    for (int t = p.tg_begin[g] + tid; t < p.tg_begin[g] + p.tg_count[g]; t += kThreads) {
+      if constexpr (DT == 0)
+        tapb[t] = (uint32_t)(((p.tap_slot[t] - p.tg_slot_begin[g]) * p.slot_chunks + p.tap_q[t]) * p.NC);
+      else
+        tapb[t] = (uint32_t)(p.tap_plane[t] * NCB * rows + p.tap_off[t]);
+    }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -108,26 +123,33 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_kernel(const __grid_constan
   const long long HW = (long long)p.H * p.W;
   const long long PQ = (long long)p.P * p.Q;
 
-  if (warp < 4) {
+  if (warp < kEpiWarp0) {
     // =============================================================== producers
-    int stage = 0;
-    uint32_t ephase = 0;
-    int pending = -1;
+    const int grp = warp >> 2;
+    const int gtid = tid & (kProdThreads - 1);
+    int* dytab = tabs + grp * tab_ints;
+    int* xtab = dytab + KB;
+    long long counter = 0;
     bool ok = true;
-    for (long long t = blockIdx.x; t < p.total_tiles && ok; t += gridDim.x) {
+    for (long long t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
       const WTile wt = decode_wtile(p, t);
       const long long lbeg = (long long)wt.sp * p.split_len;
       long long lend = lbeg + p.split_len;
       if (lend > p.Mtot) lend = p.Mtot;
       const int kbase = wt.kt * 128;
       const int cbase = wt.ct * p.NC;
-      const long long xbase = DT == 0 ? 4ll * p.tg_qmin[wt.tg] : 0ll;
+      const long long xbase = DT == 0 ? 4ll * p.tg_qmin[wt.tg] - p.x_shift : 0ll;
       const int sl0 = p.tg_slot_begin[wt.tg];
       const int nsl = p.tg_nslots[wt.tg];
-      for (long long l0 = lbeg; l0 < lend; l0 += KB) {
-        // Position tables for this stage.
-        named_bar_sync(1, kProdThreads);
-        for (int i = tid; i < KB + p.npl * rows; i += kProdThreads) {
+      for (long long l0 = lbeg; l0 < lend; l0 += KB, ++counter) {
+        // Stage ownership is a pure function of the counter, so all threads of a group
+        // pass the same named barriers even after an abort (which only skips work).
+        if ((int)(counter & 1) != grp) continue;
+        const int stage = (int)(counter % S);
+        const uint32_t ephase = (uint32_t)((counter / S) & 1);
+        // Position tables for this stage (this group's own copy).
+        named_bar_sync(1 + grp, kProdThreads);
+        for (int i = gtid; i < tab_ints; i += kProdThreads) {
           if (i < KB) {
             const long long L = l0 + i;
             int off = -1;
@@ -145,7 +167,7 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_kernel(const __grid_constan
             const int row = j - pl * rows;
             const long long L = l0 + xbase + row;
             int off = -1;
-            if (L < p.Mtot) {
+            if (L >= 0 && L < p.Mtot) {
               const int n = (int)(L / img);
               const int rem = (int)(L - (long long)n * img);
               const int e = rem / p.WL;
@@ -158,116 +180,44 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_kernel(const __grid_constan
             xtab[j] = off;
           }
         }
-        named_bar_sync(1, kProdThreads);
+        named_bar_sync(1 + grp, kProdThreads);
+        if (!ok) continue;
         if (!mbar_wait(bar_at(empty, stage), ephase ^ 1u, abort_flag, &g_wgrad_err)) {
           ok = false;
-          break;
+          continue;
         }
         const uint32_t a_st = a0 + (uint32_t)stage * p.a_stage_bytes;
         const uint32_t b_st = b0 + (uint32_t)stage * p.b_stage_bytes;
+        // dy: [chunk][k row][CHUNK positions], rows k >= K left as they are (never used).
+        stage_position_rows<DT>(p.dy, PQ, dytab, NCA, 128, p.K - kbase, a_st, kbase, p.vec_dy != 0, gtid);
         if constexpr (DT == 0) {
-          const float* dy = static_cast<const float*>(p.dy);
-          const float* x = static_cast<const float*>(p.x);
-          const int e4 = lane & 3;
-          const int rsub = lane >> 2;
-          // dy: chunk j holds positions 4j..4j+3 of 128 k rows: [j][k][4 x fp32]
-          for (int j = 0; j < NCA; ++j) {
-            const int off = dytab[j * 4 + e4];
-            const uint32_t dbase = a_st + (uint32_t)(j * 128) * 16u + (uint32_t)e4 * 4u;
-#pragma unroll
-            for (int kg = warp; kg < 16; kg += 4) {
-              const int kr = kg * 8 + rsub;
-              const int k = kbase + kr;
-              const bool v = off >= 0 && k < p.K;
-              cp_async_4(dbase + (uint32_t)kr * 16u, v ? dy + off + (long long)k * PQ : dy, v);
-            }
+          // Residue-0 copy of each plane asynchronously, then (once every thread's copies
+          // have landed) the shifted residue copies from it, in shared memory.
+          const uint32_t slot_bytes = (uint32_t)(p.slot_chunks * p.NC) * 16u;
+          for (int u = 0; u < nsl; ++u)
+            if (p.slot_res[sl0 + u] == 0)
+              stage_base_rows_async_f32(static_cast<const float*>(p.x), HW, p.C, xtab + p.slot_plane[sl0 + u] * rows,
+                                        p.slot_chunks, p.NC, b_st + (uint32_t)u * slot_bytes, cbase, p.vec_x != 0,
+                                        gtid);
+          cp_async_wait<0>();
+          named_bar_sync(1 + grp, kProdThreads);
+          for (int u = 0; u < nsl; ++u) {
+            const int r = p.slot_res[sl0 + u];
+            if (r != 0)
+              stage_shift_rows_f32(b_st + (uint32_t)(p.slot_base[sl0 + u] - sl0) * slot_bytes,
+                                   b_st + (uint32_t)u * slot_bytes, r, p.nchunks, p.NC, gtid);
           }
-          // x, K-major per slot: [slot][position chunk j][channel row][4 positions];
-          // slot u holds positions i + slot_res[u] of plane slot_plane[u].
-          // lane = (channel within 8, position within chunk): 128 contiguous bytes.
-          const int ngrp = p.NC >> 3;
-          const int items = nsl * p.nchunks * ngrp;
-          for (int it = warp; it < items; it += 4) {
-            const int g = it % ngrp;
-            const int rest = it / ngrp;
-            const int j = rest % p.nchunks;
-            const int u = rest / p.nchunks;
-            const int cr = g * 8 + rsub;
-            const int c = cbase + cr;
-            const int off = xtab[p.slot_plane[sl0 + u] * rows + j * 4 + e4 + p.slot_res[sl0 + u]];
-            const bool v = off >= 0 && c < p.C;
-            const uint32_t dst =
-                b_st + (uint32_t)((u * p.nchunks + j) * p.NC + cr) * 16u + (uint32_t)e4 * 4u;
-            cp_async_4(dst, v ? x + off + (long long)c * HW : x, v);
-          }
-          cp_async_commit();
-          if (pending >= 0) {
-            cp_async_wait<1>();
-            fence_proxy_async();
-            mbar_arrive(bar_at(full, pending));
-          }
-          pending = stage;
         } else {
-          const uint16_t* dy = static_cast<const uint16_t*>(p.dy);
-          const uint16_t* x = static_cast<const uint16_t*>(p.x);
-          // dy: thread -> (chunk j, k row); 8 positions of one k.
-          for (int i = tid; i < NCA * 128; i += kProdThreads) {
-            const int j = i >> 7;
-            const int kr = i & 127;
-            const int k = kbase + kr;
-            uint32_t wv[4] = {0u, 0u, 0u, 0u};
-            if (k < p.K) {
-              const uint16_t* gk = dy + (long long)k * PQ;
-#pragma unroll
-              for (int e = 0; e < 8; ++e) {
-                const int off = dytab[j * 8 + e];
-                if (off >= 0) wv[e >> 1] |= (uint32_t)__ldg(gk + off) << (16 * (e & 1));
-              }
-            }
-            asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(a_st + (uint32_t)i * 16u),
-                         "r"(wv[0]), "r"(wv[1]), "r"(wv[2]), "r"(wv[3])
-                         : "memory");
-          }
-          // x: thread -> (plane, chunk, row); 8 channels of one position.
-          for (int pj = 0; pj < p.npl * NCB; ++pj) {
-            const int pl = pj / NCB;
-            const int j = pj - pl * NCB;
-            const int c0 = cbase + j * 8;
-            const int nv = min(8, p.C - c0);
-            const uint16_t* gc = x + (long long)(nv > 0 ? c0 : 0) * HW;
-            const int* tab = xtab + pl * rows;
-            const uint32_t dbase = b_st + (uint32_t)(pj * rows) * 16u;
-#pragma unroll 2
-            for (int row = tid; row < rows; row += kProdThreads) {
-              const int off = tab[row];
-              uint32_t wv[4] = {0u, 0u, 0u, 0u};
-              if (off >= 0) {
-#pragma unroll
-                for (int e = 0; e < 8; ++e)
-                  if (e < nv) wv[e >> 1] |= (uint32_t)__ldg(gc + off + (long long)e * HW) << (16 * (e & 1));
-              }
-              asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(dbase + (uint32_t)row * 16u),
-                           "r"(wv[0]), "r"(wv[1]), "r"(wv[2]), "r"(wv[3])
-                           : "memory");
-            }
-          }
-          fence_proxy_async();
-          mbar_arrive(bar_at(full, stage));
+          stage_pixel_rows<DT>(p.x, HW, p.C, xtab, p.npl, rows, b_st, cbase, NCB, p.vec_x != 0, p.vec_phase,
+                               gtid);
+          cp_async_wait<0>();
         }
-        if (++stage == S) {
-          stage = 0;
-          ephase ^= 1u;
-        }
-      }
-    }
-    if constexpr (DT == 0) {
-      cp_async_wait<0>();
-      if (pending >= 0 && ok) {
         fence_proxy_async();
-        mbar_arrive(bar_at(full, pending));
+        mbar_arrive(bar_at(full, stage));
       }
     }
-  } else if (warp < 8) {
+    cp_async_wait<0>();
+  } else if (warp < kMmaWarp) {
     // =============================================================== epilogue
     const int q = warp & 3;
     uint32_t aphase = 0;
@@ -280,9 +230,10 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_kernel(const __grid_constan
       const int ntg = p.tg_count[wt.tg];
       for (int ti = 0; ti < ntg; ++ti) {
         float* dst = p.partial + ((long long)wt.sp * p.ntaps + p.tap_id[tap0 + ti]) * p.c_pad * (long long)p.k_pad;
+        const uint32_t tcol = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(kAbufCols + ti * p.NC);
         for (int c0 = 0; c0 < p.NC; c0 += 16) {
           uint32_t r[16];
-          tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(kAbufCols + ti * p.NC + c0), r);
+          tmem_ld16(tcol + (uint32_t)c0, r);
           tmem_ld_wait();
           if (k < p.K) {
 #pragma unroll
@@ -302,8 +253,7 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_kernel(const __grid_constan
     // =============================================================== MMA issuer
     if (lane == 0) {
       const uint32_t id = idesc(KIND, 128, p.NC, 0, DT == 0 ? 0 : 1);
-      int stage = 0;
-      uint32_t fphase = 0;
+      long long counter = 0;
       uint32_t aphase = 0;
       int abuf = 0;
       bool ok = true;
@@ -316,46 +266,41 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_kernel(const __grid_constan
         if (lend > p.Mtot) lend = p.Mtot;
         const int tap0 = p.tg_begin[wt.tg];
         const int ntg = p.tg_count[wt.tg];
-        const int sl0 = p.tg_slot_begin[wt.tg];
         if (!mbar_wait(acce, aphase ^ 1u, abort_flag, &g_wgrad_err)) break;
         tc_fence_after();
         bool first = true;
-        for (long long l0 = lbeg; l0 < lend; l0 += KB) {
+        for (long long l0 = lbeg; l0 < lend; l0 += KB, ++counter) {
+          const int stage = (int)(counter % S);
+          const uint32_t fphase = (uint32_t)((counter / S) & 1);
           if (!mbar_wait(bar_at(full, stage), fphase, abort_flag, &g_wgrad_err)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          fence_proxy_async();
           const uint32_t a_st = a0 + (uint32_t)stage * p.a_stage_bytes;
           const uint32_t b_st = b0 + (uint32_t)stage * p.b_stage_bytes;
+          // fp32: K-major x slot copies (chunk stride NC*16); bf16: MN-major x planes
+          // (positions along rows).  Per k-step the B start moves by 2 chunks / KSTEP rows.
+          const uint64_t bdesc0 = DT == 0 ? sdesc(b_st, (uint32_t)p.NC * 16u, 128u)
+                                          : sdesc(b_st, 128u, (uint32_t)rows * 16u);
+          const uint32_t b_lo0 = (uint32_t)bdesc0, b_hi = (uint32_t)(bdesc0 >> 32);
+          const uint32_t b_ks = DT == 0 ? 2u * (uint32_t)p.NC : (uint32_t)KSTEP;
+          const uint64_t cdesc0 = sdesc(a_st, 128u * 16u, 128u);
           for (int ks = 0; ks < NCA / 2; ++ks) {
             const uint32_t a_tm = tmem + (uint32_t)(abuf * 8);
-            tmem_cp_128x256b(a_tm, sdesc(a_st + (uint32_t)(2 * ks * 128) * 16u, 128u * 16u, 128u));
+            tmem_cp_128x256b(a_tm, cdesc0 + (uint32_t)(2 * ks * 128));
             if (++abuf == kAbufCols / 8) abuf = 0;
+            const uint32_t acc_in = first ? 0u : 1u;
+            const uint32_t blo = b_lo0 + (uint32_t)ks * b_ks;
+            uint32_t dcol = tmem + (uint32_t)kAbufCols;
             for (int ti = 0; ti < ntg; ++ti) {
-              const int tap = tap0 + ti;
-              uint64_t bd;
-              if constexpr (DT == 0) {
-                // K-major x copy: chunk (2*ks + q) of the tap's slot.
-                const uint32_t bst = b_st + (uint32_t)(((p.tap_slot[tap] - sl0) * p.nchunks + 2 * ks + p.tap_q[tap]) *
-                                                       p.NC) * 16u;
-                bd = sdesc(bst, (uint32_t)p.NC * 16u, 128u);
-              } else {
-                const uint32_t bst = b_st + (uint32_t)(p.tap_plane[tap] * NCB * rows) * 16u +
-                                     (uint32_t)(ks * KSTEP + p.tap_off[tap]) * 16u;
-                bd = sdesc(bst, 128u, (uint32_t)rows * 16u);
-              }
-              mma_ts<KIND>(tmem + (uint32_t)(kAbufCols + ti * p.NC), a_tm, bd, id, first ? 0u : 1u);
+              mma_ts_lh<KIND>(dcol, a_tm, blo + tapb[tap0 + ti], b_hi, id, acc_in);
+              dcol += (uint32_t)p.NC;
             }
             first = false;
           }
           tc_commit(bar_at(empty, stage));
           issued_any = true;
-          if (++stage == S) {
-            stage = 0;
-            fphase ^= 1u;
-          }
         }
         if (!ok) break;
         tc_commit(accf);
@@ -371,7 +316,7 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_kernel(const __grid_constan
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 8) {
+  if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, (uint32_t)p.tmem_cols);
   }
@@ -403,7 +348,7 @@ __global__ void wgrad_reduce_kernel(const __grid_constant__ ReducePlan rp) {
 
 size_t wgrad_smem_bytes(const WgradPlan& p) {
   size_t b = (size_t)p.stages * (p.a_stage_bytes + p.b_stage_bytes);
-  b += (size_t)(p.KB + p.npl * p.rows) * sizeof(int);
+  b += (size_t)2 * (p.KB + p.npl * p.rows) * sizeof(int) + (size_t)p.ntaps * sizeof(uint32_t);
   b = (b + 15) & ~size_t(15);
   b += 8 * (2 * p.stages + 3) + 16;
   return b + 1024;
