@@ -263,10 +263,7 @@ int build_fwd(const Desc& d0, const void* x, const void* w, void* y, void* ws, c
   p.Wd = d.Q;
   const int mh = (d.R - 1) / d.sh, mw = (d.S - 1) / d.sw;
   const int CHUNK = d.dt == 0 ? 4 : 8;
-  // 16-byte row loads need unit column stride, rows whose width is a multiple of a chunk,
-  // and a linear row width that keeps chunk alignment from row to row.
-  const bool vec_geom = d.sw == 1 && d.W % CHUNK == 0;
-  p.WL = vec_geom ? round_up(d.Q + mw, CHUNK) : d.Q + mw;
+  p.WL = d.Q + mw;
   p.EL = d.P + mh;
   p.Mtot = (long long)d.N * p.EL * p.WL;
   p.npl = d.sh * d.sw;
@@ -276,9 +273,7 @@ int build_fwd(const Desc& d0, const void* x, const void* w, void* y, void* ws, c
     for (int bb = 0; bb < d.sw; ++bb) {
       p.pl_off_h[a * d.sw + bb] = a - d.ph;
       p.pl_off_w[a * d.sw + bb] = bb - d.pw;
-      p.vec_phase[a * d.sw + bb] = ((d.pw - bb) % CHUNK + CHUNK) % CHUNK;
     }
-  p.vec = vec_geom && ((uintptr_t)x & 15) == 0;
   p.nph = 1;
   p.ph_step_h = 1;
   p.ph_step_w = 1;
@@ -358,8 +353,6 @@ int build_bwd_data(const Desc& d0, const void* dy, const void* w, void* dx, void
     if (Tw[c] > 0) WL = std::max(WL, Uw[c] + ulow[c] + T0w);
   }
   const int CHUNK = d.dt == 0 ? 4 : 8;
-  const bool vec_geom = d.Q % CHUNK == 0;
-  if (vec_geom) WL = round_up(WL, CHUNK);
   p.WL = WL;
   p.EL = EL;
   p.Mtot = (long long)d.N * EL * WL;
@@ -368,8 +361,6 @@ int build_bwd_data(const Desc& d0, const void* dy, const void* w, void* dx, void
   p.pl_step_w = 1;
   p.pl_off_h[0] = -T0h;
   p.pl_off_w[0] = -T0w;
-  p.vec_phase[0] = T0w % CHUNK;
-  p.vec = vec_geom && ((uintptr_t)dy & 15) == 0;
   p.nph = d.sh * d.sw;
   p.ph_step_h = d.sh;
   p.ph_step_w = d.sw;
@@ -435,19 +426,19 @@ int build_bwd_filter(const Desc& d0, const void* x, const void* dy, void* dw, vo
   p.K = d.K;
   p.P = d.P;
   p.Q = d.Q;
+  p.R = d.R;
+  p.S = d.S;
+  p.RS = d.R * d.S;
+  if (p.RS > kMaxTaps) return CONV2D_ERR_UNSUPPORTED;
+  const int CHUNK = d.dt == 0 ? 4 : 8;
+  const int ESZ = d.dt == 0 ? 4 : 2;
+  const int KSTEP = 2 * CHUNK;
   const int mh = (d.R - 1) / d.sh, mw = (d.S - 1) / d.sw;
-  // fp32: WL a multiple of 4 so that a tap's offset mod 4 depends on its column only.
-  // bf16: WL a multiple of 8 (16-byte dy chunks) when that wastes at most 1/8 of it.
-  if (d.dt == 0) {
-    p.WL = round_up(d.Q + mw, 4);
-  } else {
-    const int wl8 = round_up(d.Q + mw, 8);
-    p.WL = (8 * (wl8 - (d.Q + mw)) <= wl8) ? wl8 : d.Q + mw;
-  }
+  // Linear row width: a multiple of the chunk (16-byte dy copies) when that wastes at
+  // most 1/8 of it.
   {
-    const int ch = d.dt == 0 ? 4 : 8;
-    p.vec_dy = d.Q % ch == 0 && p.WL % ch == 0 && ((uintptr_t)dy & 15) == 0;
-    p.vec_x = d.sw == 1 && d.W % ch == 0 && p.WL % ch == 0 && ((uintptr_t)x & 15) == 0;
+    const int wl = round_up(d.Q + mw, CHUNK);
+    p.WL = (8 * (wl - (d.Q + mw)) <= wl) ? wl : d.Q + mw;
   }
   p.EL = d.P + mh;
   p.Mtot = (long long)d.N * p.EL * p.WL;
@@ -458,149 +449,53 @@ int build_bwd_filter(const Desc& d0, const void* x, const void* dy, void* dw, vo
     for (int c = 0; c < d.sw; ++c) {
       p.pl_off_h[a * d.sw + c] = a - d.ph;
       p.pl_off_w[a * d.sw + c] = c - d.pw;
-      p.vec_phase[a * d.sw + c] = ((d.pw - c) % 8 + 8) % 8;
     }
-  p.ntaps = d.R * d.S;
-  if (p.ntaps > kMaxTaps) return CONV2D_ERR_UNSUPPORTED;
-  const int CHUNK = d.dt == 0 ? 4 : 8;
-  const int ESZ = d.dt == 0 ? 4 : 2;
-  const int abuf_cols = 32;
-  // Raw tap groups: fp32 one per filter row offset r / stride_h (small halo per
-  // group), bf16 a single group (one staged tile per plane serves every tap).
-  std::vector<std::vector<int>> raw;  // filter tap ids r*S + s
-  if (d.dt == 0) {
-    for (int rho = 0; rho <= mh; ++rho) {
-      std::vector<int> g;
-      for (int r = rho * d.sh; r < std::min(d.R, (rho + 1) * d.sh); ++r)
-        for (int s = 0; s < d.S; ++s) g.push_back(r * d.S + s);
-      if (!g.empty()) raw.push_back(g);
-    }
-  } else {
-    std::vector<int> g;
-    for (int t = 0; t < p.ntaps; ++t) g.push_back(t);
-    raw.push_back(g);
-  }
-  auto tap_plane = [&](int id) { return ((id / d.S) % d.sh) * d.sw + ((id % d.S) % d.sw); };
-  auto tap_off = [&](int id) { return ((id / d.S) / d.sh) * p.WL + (id % d.S) / d.sw; };
-  // fp32: x is staged from x_shift positions before the group's first chunk, chosen so
-  // that (for unit column stride) chunk starts fall on 16-byte aligned columns.
-  p.x_shift = (d.dt == 0 && d.sw == 1) ? (4 - d.pw % 4) % 4 : 0;
-  auto tap_soff = [&](int id) { return tap_off(id) + p.x_shift; };
   int max_off = 0;
-  for (int t = 0; t < p.ntaps; ++t) max_off = std::max(max_off, tap_off(t));
+  for (int r = 0; r < d.R; ++r)
+    for (int s = 0; s < d.S; ++s) {
+      const int t = r * d.S + s;
+      p.tap_plane[t] = (r % d.sh) * d.sw + (s % d.sw);
+      p.tap_off[t] = (r / d.sh) * p.WL + s / d.sw;
+      max_off = std::max(max_off, p.tap_off[t]);
+    }
+  // Staged x rows start x_shift positions early so that (unit column stride) their
+  // 16-byte chunks fall on aligned columns of x.
+  p.x_shift = d.sw == 1 ? (CHUNK - d.pw % CHUNK) % CHUNK : 0;
+  p.vec_dy = d.Q % CHUNK == 0 && p.WL % CHUNK == 0 && ((uintptr_t)dy & 15) == 0;
+  p.vec_x = d.sw == 1 && d.W % CHUNK == 0 && p.WL % CHUNK == 0 && ((uintptr_t)x & 15) == 0;
+  p.M = d.C * p.RS;
+  p.n_mtiles = (p.M + 127) / 128;
+  p.NK = d.K <= 16 ? 16 : std::min(round_up(d.K, 32), 256);
+  p.n_ntiles = (d.K + p.NK - 1) / p.NK;
+  p.xch = std::min(d.C, (128 + p.RS - 1) / p.RS + 1);
+  p.tmem_cols = 32;
+  while (p.tmem_cols < 32 + p.NK + 16) p.tmem_cols <<= 1;
   const size_t budget = di.smem_optin - 2048;
   bool fitted = false;
-  for (int NC : {256, 128, 64, 32, 16}) {
-    if (NC > round_up(d.C, 16) && NC != 16) continue;
-    const int maxg = (512 - abuf_cols) / NC;
-    // Split raw groups so each fits TMEM; build slots per group (fp32).
-    int ng = 0, nt = 0, nsl = 0, nsl_max = 0, qspan_max = 0;
-    bool ok = true;
-    for (const auto& g : raw) {
-      for (size_t i0 = 0; i0 < g.size(); i0 += maxg) {
-        const int cnt = (int)std::min<size_t>(maxg, g.size() - i0);
-        if (ng >= kMaxTaps) { ok = false; break; }
-        p.tg_begin[ng] = nt;
-        p.tg_count[ng] = cnt;
-        int qmin = INT_MAX, qmax = 0;
-        for (int i = 0; i < cnt; ++i) {
-          const int off = tap_soff(g[i0 + i]);
-          qmin = std::min(qmin, off >> 2);
-          qmax = std::max(qmax, off >> 2);
-        }
-        p.tg_qmin[ng] = d.dt == 0 ? qmin : 0;
-        p.tg_slot_begin[ng] = nsl;
-        auto find_slot = [&](int plane, int res) {
-          int u = p.tg_slot_begin[ng];
-          while (u < nsl && !(p.slot_plane[u] == plane && p.slot_res[u] == res)) ++u;
-          if (u == nsl) {
-            if (nsl == kMaxSlots) return -1;
-            p.slot_plane[u] = plane;
-            p.slot_res[u] = res;
-            ++nsl;
-          }
-          return u;
-        };
-        for (int i = 0; i < cnt && ok; ++i) {
-          const int id = g[i0 + i];
-          const int t = nt + i;
-          p.tap_id[t] = id;
-          p.tap_plane[t] = tap_plane(id);
-          p.tap_off[t] = tap_off(id);
-          const int soff = tap_soff(id);
-          p.tap_q[t] = (soff >> 2) - p.tg_qmin[ng];
-          if (d.dt == 0) {
-            // every plane of the group has a residue-0 (base) slot the others derive from
-            if (find_slot(p.tap_plane[t], 0) < 0) { ok = false; break; }
-            const int u = find_slot(p.tap_plane[t], soff & 3);
-            if (u < 0) { ok = false; break; }
-            p.tap_slot[t] = u;
-          } else {
-            p.tap_slot[t] = 0;
-          }
-        }
-        if (!ok) break;
-        if (d.dt == 0)
-          for (int u = p.tg_slot_begin[ng]; u < nsl; ++u) {
-            int b0 = p.tg_slot_begin[ng];
-            while (!(p.slot_plane[b0] == p.slot_plane[u] && p.slot_res[b0] == 0)) ++b0;
-            p.slot_base[u] = b0;
-          }
-        p.tg_nslots[ng] = nsl - p.tg_slot_begin[ng];
-        nsl_max = std::max(nsl_max, p.tg_nslots[ng]);
-        qspan_max = std::max(qspan_max, d.dt == 0 ? qmax - qmin : 0);
-        nt += cnt;
-        ++ng;
-      }
-      if (!ok) break;
-    }
-    if (!ok) continue;
-    p.n_tgroups = ng;
-    p.nslots = d.dt == 0 ? nsl : 0;
-    int gmax = 0;
-    for (int g = 0; g < ng; ++g) gmax = std::max(gmax, p.tg_count[g]);
-    for (int KB : {128, 64, 32, 16}) {
-      if (KB % (2 * CHUNK)) continue;
-      int rows;
-      long long b_bytes;
-      if (d.dt == 0) {
-        p.nchunks = KB / 4 + qspan_max;
-        p.slot_chunks = p.nchunks + 1;
-        rows = round_up(4 * p.slot_chunks, 8);
-        b_bytes = (long long)nsl_max * p.slot_chunks * NC * 16;
-      } else {
-        p.nchunks = 0;
-        rows = round_up(KB + max_off, 8);
-        b_bytes = (long long)p.npl * (NC / CHUNK) * rows * 16;
-      }
-      const long long a_bytes = (long long)KB * 128 * ESZ;
-      const long long fixed = 2ll * (KB + p.npl * rows) * 4 + 4ll * p.ntaps + 8 * (2 * 4 + 3) + 16 + 1024;
-      long long stages = ((long long)budget - fixed) / (a_bytes + b_bytes);
-      if (stages < 2) continue;
-      if (stages > 4) stages = 4;
-      p.NC = NC;
-      p.KB = KB;
-      p.rows = rows;
-      p.a_stage_bytes = (int)a_bytes;
-      p.b_stage_bytes = (int)b_bytes;
-      p.stages = (int)stages;
-      p.tmem_cols = 32;
-      while (p.tmem_cols < abuf_cols + gmax * NC) p.tmem_cols <<= 1;
-      fitted = wgrad_smem_bytes(p) <= di.smem_optin;
-      if (fitted) break;
-    }
+  for (int KB : {128, 64, 32}) {
+    if (KB % (2 * KSTEP)) continue;
+    const int xchunks = (KB + max_off + p.x_shift + CHUNK - 1) / CHUNK;
+    const long long a_bytes = (long long)KB * p.NK * ESZ;
+    const long long b_bytes = (long long)p.npl * p.xch * xchunks * 16;
+    const long long fixed = 2ll * (KB + (long long)p.npl * xchunks * CHUNK) * 4 + 8 * (2 * 4 + 2 * 4 + 3) + 16 + 1024;
+    long long stages = ((long long)budget - fixed) / (a_bytes + b_bytes);
+    if (stages < 2) continue;
+    if (stages > 4) stages = 4;
+    p.KB = KB;
+    p.xchunks = xchunks;
+    p.xrow = xchunks * CHUNK;
+    p.a_stage_bytes = (int)a_bytes;
+    p.b_stage_bytes = (int)b_bytes;
+    p.stages = (int)stages;
+    fitted = wgrad_smem_bytes(p) <= di.smem_optin;
     if (fitted) break;
   }
   if (!fitted) return CONV2D_ERR_UNSUPPORTED;
-  p.n_ktiles = (d.K + 127) / 128;
-  p.n_ctiles = (d.C + p.NC - 1) / p.NC;
-  p.k_pad = d.K;
-  p.c_pad = d.C;
-  const long long base = (long long)p.n_ktiles * p.n_ctiles * p.n_tgroups;
+  const long long base = (long long)p.n_mtiles * p.n_ntiles;
   long long want = std::max<long long>(1, (di.sms + base - 1) / base);
   const long long stage_count = (p.Mtot + p.KB - 1) / p.KB;
   want = std::min(want, stage_count);
-  const size_t per_split = (size_t)p.ntaps * p.c_pad * p.k_pad * sizeof(float);
+  const size_t per_split = (size_t)p.RS * d.C * d.K * sizeof(float);
   while (want > 1 && per_split * (size_t)want > kWorkspaceCap) --want;
   long long slen = (p.Mtot + want - 1) / want;
   slen = (slen + p.KB - 1) / p.KB * p.KB;
@@ -617,8 +512,8 @@ int build_bwd_filter(const Desc& d0, const void* x, const void* dy, void* dw, vo
   rp.R = d.R;
   rp.S = d.S;
   rp.nsplit = p.nsplit;
-  rp.k_pad = p.k_pad;
-  rp.c_pad = p.c_pad;
+  rp.k_pad = d.K;
+  rp.c_pad = d.C;
   b.grid = (int)std::min<long long>(p.total_tiles, di.sms);
   return CONV2D_OK;
 }

@@ -18,7 +18,6 @@ namespace cg3 {
 constexpr int kMaxPlanes = 16;   // stride_h * stride_w
 constexpr int kMaxPhases = 16;
 constexpr int kMaxTaps = 256;    // R * S
-constexpr int kMaxSlots = 64;    // (plane, residue) x copies staged by fp32 backward-filter
 
 // Forward and backward-data: D[position, out_channel] = sum over taps and source
 // channels of S[channel, position + tap_off] * Wpacked[tap, out_channel, channel].
@@ -51,8 +50,6 @@ struct TapPlan {
   int ACCB;              // TMEM accumulator buffers (1 or 2)
   int a_stage_bytes, b_stage_bytes;
   int tmem_cols;
-  int vec;               // source rows may be read with 16-byte loads (see stage_pixel_rows)
-  int vec_phase[kMaxPlanes];
 };
 
 // Filter packing for TapPlan: one 16-byte chunk per (n_tile, k_block, tap, chunk, row).
@@ -68,53 +65,40 @@ struct PackPlan {
   int tap_r[kMaxTaps], tap_s[kMaxTaps];
 };
 
-// Backward-filter: per tap t, D_t[k, c] = sum over positions L of
-// dy[k, L] * Xplane(t)[c, L + tap_off[t]], split over position ranges.
-// Taps are processed in groups (one group per CTA tile, the group's accumulators
-// side by side in TMEM); tap t of the plan is filter tap tap_id[t] = r*S + s.
-// bf16 stages x once per plane with positions along rows (an MN-major operand) and
-// reaches tap t by the row offset tap_off[t].  tf32 operands must be K-major, where
-// a 16-byte chunk holds 4 consecutive positions, so fp32 stages, per group, one copy
-// of x per (plane, offset mod 4) "slot", shifted by that residue and starting at
-// position 4*tg_qmin[g]; tap t is chunk offset tap_q[t] (relative to tg_qmin) of
-// slot tap_slot[t] (an index into slot_plane/slot_res).  WL is a multiple of 4 and
-// groups are formed per filter row offset, so a group's halo is a few positions.
+// Backward-filter as one implicit GEMM per tile:
+//   D[m = c*RS + tap, k] = sum over positions L of X_plane(tap)[c, L + tap_off[tap]] * dy[k, L]
+// over the forward linear position space (dy is zero where a position has no output).
+// The A operand (the im2col of x for 128 rows (c, tap) and one k-step of positions) is
+// built directly in TMEM by builder warps from a staged x tile; B = dy[k, L] is K-major
+// (positions contiguous, as in NCHW).  Positions are split into ranges (split-K) whose
+// fp32 partials [split][tap][C][K] a second kernel adds in a fixed order.
 struct WgradPlan {
   const void* x;         // NCHW
   const void* dy;        // N K P Q
-  float* partial;        // [split][R*S][c_pad][k_pad] fp32
+  float* partial;        // [split][R*S][C][K] fp32
   int N, C, H, W, K, P, Q;
+  int R, S, RS;
   int WL, EL;
-  long long Mtot;
+  long long Mtot;        // positions
   int npl;
   int pl_step_h, pl_step_w;
   int pl_off_h[kMaxPlanes], pl_off_w[kMaxPlanes];
-  int ntaps;
-  int tap_id[kMaxTaps];
-  int tap_plane[kMaxTaps], tap_off[kMaxTaps];   // bf16
-  int tap_slot[kMaxTaps], tap_q[kMaxTaps];      // fp32
-  int nslots;
-  int slot_plane[kMaxSlots], slot_res[kMaxSlots];
-  int slot_base[kMaxSlots];        // fp32: residue-0 slot of the same plane and group
-  int slot_chunks;                 // fp32: chunks staged per slot (nchunks + 1)
-  int x_shift;                     // fp32: staged x origin offset (aligns chunk starts)
-  int n_tgroups;
-  int tg_begin[kMaxTaps], tg_count[kMaxTaps];
-  int tg_qmin[kMaxTaps], tg_slot_begin[kMaxTaps], tg_nslots[kMaxTaps];
-  int nchunks;           // fp32: position chunks staged per slot per stage
-  int n_ktiles, n_ctiles, nsplit;
-  long long split_len;   // positions per split (multiple of the stage length)
-  int rows;              // staged x rows per plane per stage (multiple of 8)
-  int k_pad, c_pad;      // extents of the partial buffer
-  long long total_tiles; // n_ktiles * n_ctiles * n_tgroups * nsplit
+  int tap_plane[kMaxTaps], tap_off[kMaxTaps];  // per filter tap r*S + s
+  int M;                 // C * RS
+  int n_mtiles, n_ntiles, nsplit;
+  long long split_len;   // positions per split (multiple of KB)
+  long long total_tiles; // n_mtiles * n_ntiles * nsplit
+  int NK;                // output channels k per tile (MMA N, multiple of 16, <= 256)
+  int KB;                // positions per pipeline stage (multiple of 2 k-steps)
+  int xch;               // x channels staged per tile
+  int xchunks;           // 16-byte chunks per staged x row
+  int xrow;              // staged x positions per row (xchunks * elements per chunk)
+  int x_shift;           // staged x row starts x_shift positions before the stage
+  int a_stage_bytes;     // dy tile bytes per stage
+  int b_stage_bytes;     // x tile bytes per stage
   int stages;
-  int NC;                // channels per tile (GEMM N per tap, multiple of 16)
-  int KB;                // positions per pipeline stage
-  int a_stage_bytes, b_stage_bytes;
   int tmem_cols;
-  int vec_dy;            // dy chunks may be copied with 16-byte cp.async
-  int vec_x;             // x rows may be read with 16-byte loads
-  int vec_phase[kMaxPlanes];  // bf16 x: see stage_pixel_rows
+  int vec_dy, vec_x;     // 16-byte copies allowed (alignment / contiguity of the tensors)
 };
 
 struct ReducePlan {

@@ -18,8 +18,9 @@
 //              loads elsewhere), and bulk-copy the packed filter slice.
 //   warps 8-11 epilogue: TMEM -> registers -> NCHW global stores, coalesced along
 //              output positions; bf16 outputs rounded to nearest even.
-//   warps 12-13 TMEM allocation (warp 12); lane 0 of each issues tcgen05.mma (kind::tf32
-//              for fp32, kind::f16 with bf16 operands) for one 128-row accumulator half.
+//   warps 12-13 TMEM allocation (warp 12); each warp issues tcgen05.mma (kind::tf32
+//              for fp32, kind::f16 with bf16 operands) for one 128-row accumulator half,
+//              through one elected lane.
 #include <mutex>
 #include <vector>
 
@@ -35,8 +36,7 @@ namespace {
 
 // CTA roles: warps 0-7 two producer groups (group g fills the stages with global stage
 // counter = g mod 2), warps 8-11 epilogue, warp 12 TMEM allocation + MMA issue for the
-// first 128-row half of a tile, warp 13 MMA issue for the second half (one issuing
-// thread per accumulator: a single thread can issue roughly one MMA per 50 cycles).
+// first 128-row half of a tile, warp 13 MMA issue for the second half.
 constexpr int kThreads = 448;
 constexpr int kProdThreads = 128;  // per producer group
 constexpr int kEpiWarp0 = 8;
@@ -63,6 +63,41 @@ __device__ __forceinline__ void store_out(void* dst, long long idx, uint32_t bit
     static_cast<float*>(dst)[idx] = __uint_as_float(bits);
   } else {
     static_cast<__nv_bfloat16*>(dst)[idx] = __float2bfloat16_rn(__uint_as_float(bits));
+  }
+}
+
+// Issues one pipeline stage's MMAs for one 128-row accumulator: for every tap of the
+// phase, KS MMAs (K = two 16-byte chunks each) over the stage's channel chunks; KS == 0
+// is tap-pair mode (one MMA covers two taps whose rows the A entry's chunk stride links).
+// The whole warp walks the taps; tap table entry j sits in lane j (blocks of 32) and is
+// broadcast by shuffles; only `leader` issues.  The inner sequence is unrolled: a single
+// issuing thread spends tens of cycles per tcgen05.mma, more with loop overhead.
+template <int KIND, int KS>
+__device__ __forceinline__ void issue_stage(const uint2* tapo, int tap0, int ntaps, uint2 tap_first, bool leader,
+                                            int lane, uint32_t dcol, uint32_t a_lo0, uint32_t b_lo0, uint32_t d_hi,
+                                            uint32_t id, uint32_t a_ks, uint32_t b_ks, bool first) {
+  constexpr int TSTEP = KS == 0 ? 2 : 1;
+  for (int tb = 0; tb < ntaps; tb += 32) {
+    const uint2 blk = tb == 0 ? tap_first : (tb + lane < ntaps ? tapo[tap0 + tb + lane] : make_uint2(0u, 0u));
+    const int nb = ntaps - tb < 32 ? ntaps - tb : 32;
+    for (int j = 0; j < nb; j += TSTEP) {
+      const uint32_t ox = __shfl_sync(0xffffffffu, blk.x, j);
+      const uint32_t oy = __shfl_sync(0xffffffffu, blk.y, j);
+      if (leader) {
+        const uint32_t acc_in = (first && tb == 0 && j == 0) ? 0u : 1u;
+        uint32_t alo = a_lo0 + ox, blo = b_lo0 + oy;
+        if constexpr (KS == 0) {
+          mma_ss_lh<KIND>(dcol, alo, d_hi, blo, d_hi, id, acc_in);
+        } else {
+#pragma unroll
+          for (int ks = 0; ks < KS; ++ks) {
+            mma_ss_lh<KIND>(dcol, alo, d_hi, blo, d_hi, id, ks ? 1u : acc_in);
+            alo += a_ks;
+            blo += b_ks;
+          }
+        }
+      }
+    }
   }
 }
 
@@ -202,8 +237,7 @@ __global__ void __launch_bounds__(kThreads, 1) tap_gemm_kernel(const __grid_cons
           bulk_g2s(b_st, static_cast<const uint8_t*>(p.wpack) + img_off, bytes, bar_at(full, stage));
           last_copy[stage] = 1 + (int)ephase;
         }
-        stage_pixel_rows<DT>(p.src, HsWs, p.Cs, rowtab, p.npl, rows, a_st, kb * p.CB, NCH, p.vec != 0,
-                             p.vec_phase, gtid);
+        stage_pixel_rows<DT>(p.src, HsWs, p.Cs, rowtab, p.npl, rows, a_st, kb * p.CB, NCH, gtid);
         fence_proxy_async();
         mbar_arrive(bar_at(full, stage));
       }
@@ -306,8 +340,13 @@ __global__ void __launch_bounds__(kThreads, 1) tap_gemm_kernel(const __grid_cons
     }
   } else {
     // =============================================================== MMA issuers
-    const int issuer = warp - kMmaWarp;  // accumulator half this thread owns
-    if (lane == 0 && issuer < nissuers) {
+    // The whole warp runs the loop (warp-uniform control flow and descriptor arithmetic);
+    // one elected lane issues the MMAs and commits.  The tap table is read into lane
+    // registers (entry j in lane j) and broadcast with shuffles: a shared-memory load that
+    // a descriptor depends on would wait behind the MMAs already issued by this thread.
+    const int issuer = warp - kMmaWarp;  // accumulator half this warp owns
+    if (issuer < nissuers) {
+      const bool leader = elect_one();
       const uint32_t id = idesc(KIND, 128, p.NT, 0, 0);
       // Descriptor high halves (stride byte offset 128 B, version) are constant.
       const uint32_t d_hi = (uint32_t)(sdesc(0u, 0u, 128u) >> 32);
@@ -322,6 +361,7 @@ __global__ void __launch_bounds__(kThreads, 1) tap_gemm_kernel(const __grid_cons
         const int ntaps = p.ph_ntaps[tc.ph];
         if (ntaps == 0) continue;
         const int tap0 = p.ph_tap_begin[tc.ph];
+        const uint2 tap_first = lane < ntaps ? tapo[tap0 + lane] : make_uint2(0u, 0u);
         if (!mbar_wait(bar_at(acce, acc), aphase ^ 1u, abort_flag, &g_tap_err)) break;
         tc_fence_after();
         const uint32_t dcol = tmem + (uint32_t)((acc * p.MH + issuer) * p.NT);
@@ -336,41 +376,39 @@ __global__ void __launch_bounds__(kThreads, 1) tap_gemm_kernel(const __grid_cons
           // Low descriptor halves of this stage's operands (this issuer's 128 rows of A).
           const uint32_t a_st = a0 + (uint32_t)stage * p.a_stage_bytes + (uint32_t)issuer * 128u * 16u;
           const uint32_t b_lo0 = (uint32_t)sdesc(b0 + (uint32_t)stage * p.b_stage_bytes, (uint32_t)p.NT * 16u, 0u);
-          if (NCH >= 2) {
-            const uint32_t a_lo0 = (uint32_t)sdesc(a_st, (uint32_t)rows * 16u, 0u);
-            for (int ti = 0; ti < ntaps; ++ti) {
-              const uint2 o = tapo[tap0 + ti];
-              uint32_t alo = a_lo0 + o.x, blo = b_lo0 + o.y;
-              const uint32_t acc_in = (kb | ti) ? 1u : 0u;
-              for (int ks = 0; ks < NCH / 2; ++ks) {
-                mma_ss_lh<KIND>(dcol, alo, d_hi, blo, d_hi, id, acc_in | (uint32_t)ks);
-                alo += a_ks;
-                blo += b_ks;
-              }
-            }
-          } else {
-            // One channel chunk per tap: one MMA K-step covers two taps.  Its second
-            // K-chunk is the next tap's rows, reached through the descriptor's chunk
-            // stride (taps are sorted by staged address; a padding tap with zero
-            // weights repeats the last address).
-            const uint32_t a_lo0 = (uint32_t)sdesc(a_st, 0u, 0u);
-            for (int ti = 0; ti < ntaps; ti += 2) {
-              const uint2 o = tapo[tap0 + ti];
-              mma_ss_lh<KIND>(dcol, a_lo0 + o.x, d_hi, b_lo0 + o.y, d_hi, id, (kb | ti) ? 1u : 0u);
-            }
+          // In tap-pair mode the A entry carries the chunk stride to the pair's second tap.
+          const uint32_t a_lo0 = (uint32_t)sdesc(a_st, NCH >= 2 ? (uint32_t)rows * 16u : 0u, 0u);
+          const bool first = kb == 0;
+          switch (NCH) {
+            case 1:
+              issue_stage<KIND, 0>(tapo, tap0, ntaps, tap_first, leader, lane, dcol, a_lo0, b_lo0, d_hi, id, a_ks, b_ks, first);
+              break;
+            case 2:
+              issue_stage<KIND, 1>(tapo, tap0, ntaps, tap_first, leader, lane, dcol, a_lo0, b_lo0, d_hi, id, a_ks, b_ks, first);
+              break;
+            case 4:
+              issue_stage<KIND, 2>(tapo, tap0, ntaps, tap_first, leader, lane, dcol, a_lo0, b_lo0, d_hi, id, a_ks, b_ks, first);
+              break;
+            case 8:
+              issue_stage<KIND, 4>(tapo, tap0, ntaps, tap_first, leader, lane, dcol, a_lo0, b_lo0, d_hi, id, a_ks, b_ks, first);
+              break;
+            default:
+              issue_stage<KIND, 8>(tapo, tap0, ntaps, tap_first, leader, lane, dcol, a_lo0, b_lo0, d_hi, id, a_ks, b_ks, first);
+              break;
           }
-          tc_commit(bar_at(empty, stage));
+          __syncwarp();
+          if (leader) tc_commit(bar_at(empty, stage));
           issued_any = true;
         }
         if (!ok) break;
-        tc_commit(bar_at(accf, acc));
+        if (leader) tc_commit(bar_at(accf, acc));
         if (++acc == p.ACCB) {
           acc = 0;
           aphase ^= 1u;
         }
       }
-      if (!ok && issued_any) {
-        // Wait (bounded) for every MMA this thread issued before TMEM is released.
+      if (!ok && issued_any && leader) {
+        // Wait (bounded) for every MMA this warp issued before TMEM is released.
         tc_commit(drain + 8u * (uint32_t)issuer);
         mbar_wait_drain(drain + 8u * (uint32_t)issuer, 0);
       }
