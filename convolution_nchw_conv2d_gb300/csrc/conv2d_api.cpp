@@ -161,7 +161,7 @@ bool choose_tap_tiles(TapPlan& p, int max_off, int dt, const DevInfo& di, bool p
         const int rows = round_up(128 * mh + max_off + (pair_taps ? 1 : 0), 8);
         const long long a_bytes = (long long)p.npl * NCH * rows * 16;
         const long long b_bytes = (long long)p.max_taps_ph * NCH * NT * 16;
-        const long long fixed = (long long)p.npl * rows * 4 + 8ll * p.ntaps_total + 8 * (3 * 4 + 6) + 24 + 4 * 4 + 1024;
+        const long long fixed = 8ll * p.ntaps_total + 8 * (3 * 4 + 6) + 24 + 4 * 4 + 1024;
         const long long per = a_bytes + b_bytes;
         long long stages = ((long long)budget - fixed) / per;
         if (stages < 2) continue;
@@ -266,6 +266,9 @@ int build_fwd(const Desc& d0, const void* x, const void* w, void* y, void* ws, c
   p.WL = d.Q + mw;
   p.EL = d.P + mh;
   p.Mtot = (long long)d.N * p.EL * p.WL;
+  if (p.Mtot >= (1ll << 31)) return CONV2D_ERR_TOO_LARGE;
+  p.fd_img = make_fastdiv((uint32_t)(p.EL * p.WL));
+  p.fd_WL = make_fastdiv((uint32_t)p.WL);
   p.npl = d.sh * d.sw;
   p.pl_step_h = d.sh;
   p.pl_step_w = d.sw;
@@ -356,6 +359,9 @@ int build_bwd_data(const Desc& d0, const void* dy, const void* w, void* dx, void
   p.WL = WL;
   p.EL = EL;
   p.Mtot = (long long)d.N * EL * WL;
+  if (p.Mtot >= (1ll << 31)) return CONV2D_ERR_TOO_LARGE;
+  p.fd_img = make_fastdiv((uint32_t)(EL * WL));
+  p.fd_WL = make_fastdiv((uint32_t)WL);
   p.npl = 1;
   p.pl_step_h = 1;
   p.pl_step_w = 1;
@@ -442,6 +448,9 @@ int build_bwd_filter(const Desc& d0, const void* x, const void* dy, void* dw, vo
   }
   p.EL = d.P + mh;
   p.Mtot = (long long)d.N * p.EL * p.WL;
+  if (p.Mtot >= (1ll << 31)) return CONV2D_ERR_TOO_LARGE;
+  p.fd_img = make_fastdiv((uint32_t)(p.EL * p.WL));
+  p.fd_WL = make_fastdiv((uint32_t)p.WL);
   p.npl = d.sh * d.sw;
   p.pl_step_h = d.sh;
   p.pl_step_w = d.sw;

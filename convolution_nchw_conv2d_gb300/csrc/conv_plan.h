@@ -15,6 +15,33 @@
 
 namespace cg3 {
 
+// Unsigned 32-bit division by a divisor fixed at planning time, as a multiply-high and
+// shifts (Granlund and Montgomery, "Division by Invariant Integers using
+// Multiplication", PLDI 1994, unsigned case): with l = ceil(log2 d) and
+// m = floor(2^32 (2^l - d) / d) + 1,  n / d = (t + ((n - t) >> min(l,1))) >> max(l-1,0)
+// where t = mulhi(m, n), exact for every n < 2^32.
+struct FastDiv {
+  uint32_t d, m, s1, s2;
+};
+
+inline FastDiv make_fastdiv(uint32_t d) {
+  FastDiv f;
+  uint32_t l = 0;
+  while (l < 32 && (1ull << l) < d) ++l;
+  f.d = d;
+  f.m = (uint32_t)((((1ull << 32) * ((1ull << l) - d)) / d) + 1);
+  f.s1 = l < 1 ? l : 1;
+  f.s2 = l > 1 ? l - 1 : 0;
+  return f;
+}
+
+#ifdef __CUDACC__
+__device__ __forceinline__ uint32_t fdiv(uint32_t n, const FastDiv& f) {
+  const uint32_t t = __umulhi(n, f.m);
+  return (t + ((n - t) >> f.s1)) >> f.s2;
+}
+#endif
+
 constexpr int kMaxPlanes = 16;   // stride_h * stride_w
 constexpr int kMaxPhases = 16;
 constexpr int kMaxTaps = 256;    // R * S
@@ -28,7 +55,8 @@ struct TapPlan {
   int N, Cs, Hs, Ws;     // source tensor
   int Cd, Hd, Wd;        // destination tensor
   int WL, EL;            // linear-space row width and rows per image
-  long long Mtot;        // N * EL * WL
+  long long Mtot;        // N * EL * WL (< 2^31)
+  FastDiv fd_img, fd_WL; // division by EL*WL and by WL
   int n_mtiles, n_ntiles, nkb;  // tiles along positions / out channels; channel blocks
   long long total_tiles;        // nph * n_mtiles * n_ntiles
   int rows;              // staged source rows per plane (multiple of 8)
@@ -79,7 +107,8 @@ struct WgradPlan {
   int N, C, H, W, K, P, Q;
   int R, S, RS;
   int WL, EL;
-  long long Mtot;        // positions
+  long long Mtot;        // positions (< 2^31)
+  FastDiv fd_img, fd_WL; // division by EL*WL and by WL
   int npl;
   int pl_step_h, pl_step_w;
   int pl_off_h[kMaxPlanes], pl_off_w[kMaxPlanes];

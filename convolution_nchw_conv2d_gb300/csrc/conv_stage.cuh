@@ -13,6 +13,7 @@
 #include <type_traits>
 #include <cuda_bf16.h>
 
+#include "conv_plan.h"
 #include "sm103_ptx.cuh"
 
 namespace cg3 {
@@ -29,69 +30,101 @@ __device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, int s
 }
 
 // ------------------------------------------------------------------ pixel rows
+// Source element offset of channel 0 of the pixel that plane `pl` of a TapPlan places at
+// linear position L (L = n*EL*WL + e*WL + f; plane pixel (e, f) is source pixel
+// (e*pl_step_h + pl_off_h, f*pl_step_w + pl_off_w)), or -1 outside the source tensor.
+__device__ __forceinline__ int tap_src_offset(const TapPlan& p, uint32_t L, int pl) {
+  if ((long long)L >= p.Mtot) return -1;
+  const uint32_t n = fdiv(L, p.fd_img);
+  const uint32_t rem = L - n * (uint32_t)p.fd_img.d;
+  const uint32_t e = fdiv(rem, p.fd_WL);
+  const int f = (int)(rem - e * (uint32_t)p.WL);
+  const int h = (int)e * p.pl_step_h + p.pl_off_h[pl];
+  const int w = f * p.pl_step_w + p.pl_off_w[pl];
+  if (h < 0 || h >= p.Hs || w < 0 || w >= p.Ws) return -1;
+  return (int)n * p.Cs * p.Hs * p.Ws + h * p.Ws + w;
+}
+
 // Layout [plane][chunk][row][16 bytes]: the 16 bytes of (plane, chunk j, row r) hold
-// CHUNK consecutive channels cbase + j*CHUNK + e of the source pixel tab[plane][r]
-// (the element offset of channel 0 of that pixel, -1 if outside the tensor).
+// CHUNK consecutive channels cbase + j*CHUNK + e of the source pixel at linear position
+// m0 + r of that plane (zero outside the tensor).
 //
-// One staged row per thread: CHUNK scalar loads, one per channel, and one 16-byte shared
-// store.  Lanes take consecutive rows, so each load instruction of a warp reads
-// consecutive pixels of one channel (coalesced wherever the rows are adjacent pixels) and
-// each store instruction writes 512 contiguous bytes (no bank conflicts); no register
-// transpose and no alignment condition on the rows.  Requires rows >= 128.
+// Work item = (row, plane, group of G chunks): G*CHUNK = 16 scalar loads, one per channel,
+// then G 16-byte shared stores.  Lanes take consecutive rows, so each load instruction
+// of a warp reads consecutive pixels of one channel (coalesced wherever the rows are
+// adjacent pixels) and each store instruction writes 512 contiguous bytes (no bank
+// conflicts); no register transpose and no alignment condition.  Loads of the next item
+// are issued before the stores of the current one.  Requires rows >= 128.
 template <int DT>
-__device__ __forceinline__ void stage_pixel_rows(const void* src_v, long long plane_stride, int Cs,
-                                                 const int* tab, int npl, int rows, uint32_t dst0,
-                                                 int cbase, int nch, int gtid) {
+__device__ __forceinline__ void stage_pixel_rows(const TapPlan& p, long long m0, uint32_t dst0, int cbase,
+                                                 int nch, int gtid) {
   constexpr int CHUNK = DT == 0 ? 4 : 8;
-  constexpr int U = DT == 0 ? 4 : 2;  // rows per batch: all loads of a batch precede its stores
+  constexpr int G = 16 / CHUNK;  // chunks per item
   using E = typename std::conditional<DT == 0, uint32_t, uint16_t>::type;
-  const E* src = static_cast<const E*>(src_v);
-  // Item (plane pl, chunk j, row r), walked in [pl][j][r] order with stride 128.
-  int pl = 0, j = 0, r = gtid;
-  while (pl < npl) {
-    uint32_t v[U][4];
-    uint32_t dst[U];
-    bool live[U];
+  const E* src = static_cast<const E*>(p.src);
+  const long long plane_stride = (long long)p.Hs * p.Ws;
+  const int rows = p.rows, npl = p.npl;
+  const int ngr = (nch + G - 1) / G;
+  struct Item {
+    int r, pl, jg;
+  };
+  auto load = [&](const Item& it, uint32_t (&v)[4 * G]) {
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      live[u] = pl < npl;
-      v[u][0] = v[u][1] = v[u][2] = v[u][3] = 0u;
-      dst[u] = dst0 + (uint32_t)(((pl * nch + j) * rows + r) * 16);
-      if (live[u]) {
-        const int off = tab[pl * rows + r];
-        const int c0 = cbase + j * CHUNK;
-        if (off >= 0) {
-          const E* s0 = src + (long long)c0 * plane_stride + off;
-          if (c0 + CHUNK <= Cs) {
+    for (int i = 0; i < 4 * G; ++i) v[i] = 0u;
+    const int off = tap_src_offset(p, (uint32_t)(m0 + it.r), it.pl);
+    if (off < 0) return;
+    const int c0 = cbase + it.jg * G * CHUNK;
+    const E* s0 = src + (long long)c0 * plane_stride + off;
+    if (c0 + G * CHUNK <= p.Cs) {
 #pragma unroll
-            for (int e = 0; e < CHUNK; ++e) {
-              const uint32_t x = (uint32_t)__ldg(s0 + e * plane_stride);
-              if constexpr (DT == 0) v[u][e] = x;
-              else v[u][e >> 1] |= x << (16 * (e & 1));
-            }
-          } else {
-#pragma unroll
-            for (int e = 0; e < CHUNK; ++e) {
-              if (c0 + e >= Cs) break;
-              const uint32_t x = (uint32_t)__ldg(s0 + e * plane_stride);
-              if constexpr (DT == 0) v[u][e] = x;
-              else v[u][e >> 1] |= x << (16 * (e & 1));
-            }
-          }
-        }
+      for (int e = 0; e < G * CHUNK; ++e) {
+        const uint32_t x = (uint32_t)__ldg(s0 + e * plane_stride);
+        if constexpr (DT == 0) v[e] = x;
+        else v[e >> 1] |= x << (16 * (e & 1));
       }
-      r += 128;
-      if (r >= rows) {
-        r -= rows;
-        if (++j == nch) {
-          j = 0;
-          ++pl;
-        }
+    } else {
+#pragma unroll
+      for (int e = 0; e < G * CHUNK; ++e) {
+        if (c0 + e >= p.Cs) break;
+        const uint32_t x = (uint32_t)__ldg(s0 + e * plane_stride);
+        if constexpr (DT == 0) v[e] = x;
+        else v[e >> 1] |= x << (16 * (e & 1));
       }
     }
+  };
+  auto store = [&](const Item& it, const uint32_t (&v)[4 * G]) {
 #pragma unroll
-    for (int u = 0; u < U; ++u)
-      if (live[u]) st_shared_v4(dst[u], v[u][0], v[u][1], v[u][2], v[u][3]);
+    for (int g = 0; g < G; ++g) {
+      const int j = it.jg * G + g;
+      if (j < nch)
+        st_shared_v4(dst0 + (uint32_t)(((it.pl * nch + j) * rows + it.r) * 16), v[4 * g], v[4 * g + 1],
+                     v[4 * g + 2], v[4 * g + 3]);
+    }
+  };
+  // Items in [jg][pl][r] order, stride 128 (rows >= 128: one wrap per step at most).
+  auto next = [&](Item& it) {
+    it.r += 128;
+    if (it.r >= rows) {
+      it.r -= rows;
+      if (++it.pl == npl) {
+        it.pl = 0;
+        ++it.jg;
+      }
+    }
+  };
+  Item a{gtid, 0, 0};
+  uint32_t va[4 * G], vb[4 * G];
+  if (a.jg < ngr) load(a, va);
+  while (a.jg < ngr) {
+    Item b = a;
+    next(b);
+    if (b.jg < ngr) load(b, vb);
+    store(a, va);
+    if (b.jg >= ngr) break;
+    a = b;
+    next(a);
+    if (a.jg < ngr) load(a, va);
+    store(b, vb);
   }
 }
 

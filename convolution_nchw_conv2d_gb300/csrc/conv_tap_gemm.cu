@@ -123,8 +123,6 @@ __global__ void __launch_bounds__(kThreads, 1) tap_gemm_kernel(const __grid_cons
   ptr += (size_t)S * p.a_stage_bytes;
   const uint32_t b0 = smem_u32(ptr);
   ptr += (size_t)S * p.b_stage_bytes;
-  int* rowtab = reinterpret_cast<int*>(ptr);
-  ptr += (size_t)p.npl * rows * sizeof(int);
   // Per tap: {A operand offset, B operand offset} relative to the stage bases, in 16-byte
   // units (in tap-pair mode the A entry of a pair's first tap also carries the chunk
   // stride to the second tap in bits 16..29, the descriptor's leading-byte-offset field).
@@ -178,8 +176,6 @@ __global__ void __launch_bounds__(kThreads, 1) tap_gemm_kernel(const __grid_cons
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
 
-  const long long img = (long long)p.EL * p.WL;
-  const long long HsWs = (long long)p.Hs * p.Ws;
   const long long HdWd = (long long)p.Hd * p.Wd;
   const int MT = 128 * p.MH;
   const int b_tap_bytes = NCH * p.NT * 16;
@@ -190,33 +186,13 @@ __global__ void __launch_bounds__(kThreads, 1) tap_gemm_kernel(const __grid_cons
     const int gtid = tid & (kProdThreads - 1);
     long long counter = 0;               // global stage counter (both groups count all stages)
     bool ok = true;
-    // Both groups meet at named barriers once per tile, so after an abort a group keeps
-    // walking the tiles (skipping all work) until the end instead of leaving early.
+    // After an abort a group keeps walking the tiles (skipping all work) to the final
+    // named barrier below instead of leaving early.
     for (long long t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
       const TileCoord tc = decode_tile(p, t);
       const int ntaps = p.ph_ntaps[tc.ph];
       if (ntaps == 0) continue;
       const long long m0 = (long long)tc.mt * MT;
-      // Row table (both groups): source offset of channel 0 for every staged row.
-      named_bar_sync(1, 2 * kProdThreads);
-      for (int i = tid; i < p.npl * rows; i += 2 * kProdThreads) {
-        const int pl = i / rows;
-        const int row = i - pl * rows;
-        const long long L = m0 + row;
-        int off = -1;
-        if (L < p.Mtot) {
-          const int n = (int)(L / img);
-          const int rem = (int)(L - (long long)n * img);
-          const int e = rem / p.WL;
-          const int f = rem - e * p.WL;
-          const int h = e * p.pl_step_h + p.pl_off_h[pl];
-          const int w = f * p.pl_step_w + p.pl_off_w[pl];
-          if (h >= 0 && h < p.Hs && w >= 0 && w < p.Ws)
-            off = (int)((long long)n * p.Cs * HsWs + (long long)h * p.Ws + w);
-        }
-        rowtab[i] = off;
-      }
-      named_bar_sync(1, 2 * kProdThreads);
       for (int kb = 0; kb < p.nkb; ++kb, ++counter) {
         if ((int)(counter & 1) != grp || !ok) continue;
         const int stage = (int)(counter % S);
@@ -237,7 +213,7 @@ __global__ void __launch_bounds__(kThreads, 1) tap_gemm_kernel(const __grid_cons
           bulk_g2s(b_st, static_cast<const uint8_t*>(p.wpack) + img_off, bytes, bar_at(full, stage));
           last_copy[stage] = 1 + (int)ephase;
         }
-        stage_pixel_rows<DT>(p.src, HsWs, p.Cs, rowtab, p.npl, rows, a_st, kb * p.CB, NCH, gtid);
+        stage_pixel_rows<DT>(p, m0, a_st, kb * p.CB, NCH, gtid);
         fence_proxy_async();
         mbar_arrive(bar_at(full, stage));
       }
@@ -272,10 +248,10 @@ __global__ void __launch_bounds__(kThreads, 1) tap_gemm_kernel(const __grid_cons
         bool valid = false;
         long long obase = 0;
         if (L < p.Mtot) {
-          const int n = (int)(L / img);
-          const int rem = (int)(L - (long long)n * img);
-          const int e = rem / p.WL;
-          const int f = rem - e * p.WL;
+          const uint32_t n = fdiv((uint32_t)L, p.fd_img);
+          const uint32_t rem = (uint32_t)L - n * p.fd_img.d;
+          const int e = (int)fdiv(rem, p.fd_WL);
+          const int f = (int)rem - e * p.WL;
           const int oh = e * p.ph_step_h + p.ph_off_h[tc.ph];
           const int ow = f * p.ph_step_w + p.ph_off_w[tc.ph];
           valid = oh >= 0 && oh < p.Hd && ow >= 0 && ow < p.Wd;
@@ -473,7 +449,7 @@ __global__ void pack_filter_kernel(const __grid_constant__ PackPlan pp) {
 // ---------------------------------------------------------------------------- launchers
 size_t tap_gemm_smem_bytes(const TapPlan& p) {
   size_t b = (size_t)p.stages * (p.a_stage_bytes + p.b_stage_bytes);
-  b += (size_t)p.npl * p.rows * sizeof(int) + (size_t)p.ntaps_total * sizeof(uint2);
+  b += (size_t)p.ntaps_total * sizeof(uint2);
   b = (b + 15) & ~size_t(15);
   b += 8 * (2 * p.stages + 6) + 8 + 4 * p.stages + 16;
   return b + 1024;  // alignment slack for the dynamic base

@@ -110,7 +110,6 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_kernel(const __grid_constan
   const uint32_t tmem = *tmem_holder;
   const uint32_t dcol0 = tmem + (uint32_t)(kNabuf * 8);  // accumulator columns
 
-  const long long img = (long long)p.EL * p.WL;
   const long long HW = (long long)p.H * p.W;
   const long long PQ = (long long)p.P * p.Q;
 
@@ -141,10 +140,10 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_kernel(const __grid_constan
             const long long L = l0 + i;
             int off = -1;
             if (L < lend) {
-              const int n = (int)(L / img);
-              const int rem = (int)(L - (long long)n * img);
-              const int e = rem / p.WL;
-              const int f = rem - e * p.WL;
+              const uint32_t n = fdiv((uint32_t)L, p.fd_img);
+              const uint32_t rem = (uint32_t)L - n * p.fd_img.d;
+              const int e = (int)fdiv(rem, p.fd_WL);
+              const int f = (int)rem - e * p.WL;
               if (e < p.P && f < p.Q) off = (int)((long long)n * p.K * PQ + (long long)e * p.Q + f);
             }
             dytab[i] = off;
@@ -155,10 +154,10 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_kernel(const __grid_constan
             const long long L = l0 - p.x_shift + xi;
             int off = -1;
             if (L >= 0 && L < p.Mtot) {
-              const int n = (int)(L / img);
-              const int rem = (int)(L - (long long)n * img);
-              const int e = rem / p.WL;
-              const int f = rem - e * p.WL;
+              const uint32_t n = fdiv((uint32_t)L, p.fd_img);
+              const uint32_t rem = (uint32_t)L - n * p.fd_img.d;
+              const int e = (int)fdiv(rem, p.fd_WL);
+              const int f = (int)rem - e * p.WL;
               const int h = e * p.pl_step_h + p.pl_off_h[pl];
               const int w = f * p.pl_step_w + p.pl_off_w[pl];
               if (h >= 0 && h < p.H && w >= 0 && w < p.W)
