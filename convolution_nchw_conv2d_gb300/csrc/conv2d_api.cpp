@@ -20,7 +20,7 @@ cudaError_t launch_pack_filter(const PackPlan& pp, int dt, cudaStream_t st);
 size_t tap_gemm_smem_bytes(const TapPlan& p);
 cudaError_t launch_wgrad(const WgradPlan& p, int dt, int grid, cudaStream_t st);
 cudaError_t launch_wgrad_reduce(const ReducePlan& rp, int dt, int num_sms, cudaStream_t st);
-size_t wgrad_smem_bytes(const WgradPlan& p);
+size_t wgrad_smem_bytes(const WgradPlan& p, int dt);
 int tap_gemm_take_error();
 int wgrad_take_error();
 size_t noalloc_scratch_capacity();
@@ -438,7 +438,7 @@ int build_bwd_filter(const Desc& d0, const void* x, const void* dy, void* dw, vo
   if (p.RS > kMaxTaps) return CONV2D_ERR_UNSUPPORTED;
   const int CHUNK = d.dt == 0 ? 4 : 8;
   const int ESZ = d.dt == 0 ? 4 : 2;
-  const int KSTEP = 2 * CHUNK;
+  const int BUFP = d.dt == 0 ? 32 : 64;  // positions per 32-column TMEM buffer
   const int mh = (d.R - 1) / d.sh, mw = (d.S - 1) / d.sw;
   // Linear row width: a multiple of the chunk (16-byte dy copies) when that wastes at
   // most 1/8 of it.
@@ -459,55 +459,120 @@ int build_bwd_filter(const Desc& d0, const void* x, const void* dy, void* dw, vo
       p.pl_off_h[a * d.sw + c] = a - d.ph;
       p.pl_off_w[a * d.sw + c] = c - d.pw;
     }
-  int max_off = 0;
+  p.max_off = 0;
   for (int r = 0; r < d.R; ++r)
     for (int s = 0; s < d.S; ++s) {
       const int t = r * d.S + s;
       p.tap_plane[t] = (r % d.sh) * d.sw + (s % d.sw);
       p.tap_off[t] = (r / d.sh) * p.WL + s / d.sw;
-      max_off = std::max(max_off, p.tap_off[t]);
+      p.max_off = std::max(p.max_off, p.tap_off[t]);
     }
-  // Staged x rows start x_shift positions early so that (unit column stride) their
-  // 16-byte chunks fall on aligned columns of x.
-  p.x_shift = d.sw == 1 ? (CHUNK - d.pw % CHUNK) % CHUNK : 0;
   p.vec_dy = d.Q % CHUNK == 0 && p.WL % CHUNK == 0 && ((uintptr_t)dy & 15) == 0;
-  p.vec_x = d.sw == 1 && d.W % CHUNK == 0 && p.WL % CHUNK == 0 && ((uintptr_t)x & 15) == 0;
-  p.M = d.C * p.RS;
-  p.n_mtiles = (p.M + 127) / 128;
+  // Row units of 32 TMEM lanes: 32 channels of one tap, or (C < 32) TPU taps x C channels.
+  p.Cg = d.C >= 32 ? 32 : d.C;
+  p.TPU = d.C >= 32 ? 1 : 32 / d.C;
+  p.upc = (p.RS + p.TPU - 1) / p.TPU;
+  const int ncg = (d.C + p.Cg - 1) / p.Cg;
+  p.nunits = ncg * p.upc;
+  p.n_mtiles = (p.nunits + 3) / 4;
+  p.xch = 0;
+  for (int mt = 0; mt < p.n_mtiles; ++mt) {
+    const int cg0 = (4 * mt) / p.upc, cg1 = std::min(p.nunits - 1, 4 * mt + 3) / p.upc;
+    p.xch = std::max(p.xch, std::min(d.C, (cg1 + 1) * p.Cg) - cg0 * p.Cg);
+  }
   p.NK = d.K <= 16 ? 16 : std::min(round_up(d.K, 32), 256);
   p.n_ntiles = (d.K + p.NK - 1) / p.NK;
-  p.xch = std::min(d.C, (128 + p.RS - 1) / p.RS + 1);
+  p.accb = (128 + 2 * p.NK <= 512) ? 2 : 1;
   p.tmem_cols = 32;
-  while (p.tmem_cols < 32 + p.NK + 16) p.tmem_cols <<= 1;
-  const size_t budget = di.smem_optin - 2048;
+  while (p.tmem_cols < 128 + p.accb * p.NK) p.tmem_cols <<= 1;
+  // 16-byte x loads: unit column stride, rows and planes of whole chunks, aligned base;
+  // sigma puts the start of every slot group on a chunk-aligned pixel.
+  p.vec_x = d.sw == 1 && p.WL % CHUNK == 0 && d.W % CHUNK == 0 && ((uintptr_t)x & 15) == 0;
+  p.sigma = p.vec_x ? (CHUNK - d.pw % CHUNK) % CHUNK : 0;
+  // Ring slot width: the channel span rounded to a chunk, plus the padding (in chunks) that
+  // minimises bank conflicts of the builders' reads when a unit mixes taps (C < 32).
+  {
+    const int base_xs = round_up(p.xch, CHUNK);
+    int best_xs = base_xs;
+    long long best_cost = -1;
+    for (int padc = 0; padc < (p.TPU > 1 ? 8 : 1); ++padc) {
+      const long long xs = base_xs + (long long)padc * CHUNK;
+      long long cost = 0;
+      for (int u = 0; u < p.nunits; ++u) {
+        int cnt[32] = {0};
+        const int c_lo = ((4 * (u / 4)) / p.upc) * p.Cg;
+        int worst = 0;
+        for (int l = 0; l < 32; ++l) {
+          const int cg = u / p.upc, tu = u % p.upc;
+          int c, tap;
+          bool v;
+          if (p.TPU == 1) {
+            c = cg * p.Cg + l;
+            tap = tu;
+            v = c < d.C;
+          } else {
+            const int tl = l / p.Cg;
+            c = l - tl * p.Cg;
+            tap = tu * p.TPU + tl;
+            v = tl < p.TPU && tap < p.RS;
+          }
+          if (!v) continue;
+          // word address (bank) at the first slot, 4-byte elements (2-byte: half a word)
+          const long long el = ((long long)p.tap_plane[tap] * 4096 + p.tap_off[tap]) * xs + (c - c_lo);
+          const long long word = d.dt == 0 ? el : el / 2;
+          worst = std::max(worst, ++cnt[word & 31]);
+        }
+        cost += worst;
+      }
+      if (best_cost < 0 || cost < best_cost) {
+        best_cost = cost;
+        best_xs = (int)xs;
+      }
+    }
+    p.xs = best_xs;
+  }
+  // Pipeline: the most positions in flight (stages x KB) that fit, then the larger KB.
   bool fitted = false;
-  for (int KB : {128, 64, 32}) {
-    if (KB % (2 * KSTEP)) continue;
-    const int xchunks = (KB + max_off + p.x_shift + CHUNK - 1) / CHUNK;
-    const long long a_bytes = (long long)KB * p.NK * ESZ;
-    const long long b_bytes = (long long)p.npl * p.xch * xchunks * 16;
-    const long long fixed = 2ll * (KB + (long long)p.npl * xchunks * CHUNK) * 4 + 8 * (2 * 4 + 2 * 4 + 3) + 16 + 1024;
-    long long stages = ((long long)budget - fixed) / (a_bytes + b_bytes);
-    if (stages < 2) continue;
-    if (stages > 4) stages = 4;
-    p.KB = KB;
-    p.xchunks = xchunks;
-    p.xrow = xchunks * CHUNK;
-    p.a_stage_bytes = (int)a_bytes;
-    p.b_stage_bytes = (int)b_bytes;
-    p.stages = (int)stages;
-    fitted = wgrad_smem_bytes(p) <= di.smem_optin;
-    if (fitted) break;
+  long long best = -1;
+  WgradPlan bestp = p;
+  for (int KB : {256, 192, 128, 96, 64, 32}) {
+    if (KB % BUFP) continue;
+    for (int S = 4; S >= 2; --S) {
+      WgradPlan q = p;
+      q.KB = KB;
+      q.stages = S;
+      // the ring holds S stages plus the halo, plus a slot group rewritten at each end
+      q.rlen = round_up(S * KB + p.max_off + 2 * CHUNK, 32);
+      q.a_stage_bytes = KB * p.NK * ESZ;
+      if (wgrad_smem_bytes(q, d.dt) > di.smem_optin) continue;
+      const long long score = (long long)S * KB * 4 + KB / 32;
+      if (score > best) {
+        best = score;
+        bestp = q;
+        fitted = true;
+      }
+    }
   }
   if (!fitted) return CONV2D_ERR_UNSUPPORTED;
+  p = bestp;
+  // Split the positions so that the tiles fill the SMs with the shortest makespan
+  // (tiles per CTA x positions per tile), preferring fewer splits.
   const long long base = (long long)p.n_mtiles * p.n_ntiles;
-  long long want = std::max<long long>(1, (di.sms + base - 1) / base);
   const long long stage_count = (p.Mtot + p.KB - 1) / p.KB;
-  want = std::min(want, stage_count);
   const size_t per_split = (size_t)p.RS * d.C * d.K * sizeof(float);
-  while (want > 1 && per_split * (size_t)want > kWorkspaceCap) --want;
-  long long slen = (p.Mtot + want - 1) / want;
-  slen = (slen + p.KB - 1) / p.KB * p.KB;
+  long long nsb = 1;
+  double best_t = -1.0;
+  for (long long ns = 1; ns <= std::min<long long>(stage_count, 4 * (long long)di.sms); ++ns) {
+    if (per_split * (size_t)ns > kWorkspaceCap) break;
+    const long long slen = (stage_count + ns - 1) / ns;  // stages per split
+    const long long waves = (base * ns + di.sms - 1) / di.sms;
+    const double tmake = (double)waves * (double)(slen * p.KB + p.max_off + 4 * p.KB);
+    if (best_t < 0 || tmake < best_t * 0.98) {
+      best_t = tmake;
+      nsb = ns;
+    }
+  }
+  long long slen = (stage_count + nsb - 1) / nsb * p.KB;
   p.split_len = slen;
   p.nsplit = (int)((p.Mtot + slen - 1) / slen);
   p.total_tiles = base * p.nsplit;

@@ -94,12 +94,22 @@ struct PackPlan {
 };
 
 // Backward-filter as one implicit GEMM per tile:
-//   D[m = c*RS + tap, k] = sum over positions L of X_plane(tap)[c, L + tap_off[tap]] * dy[k, L]
-// over the forward linear position space (dy is zero where a position has no output).
-// The A operand (the im2col of x for 128 rows (c, tap) and one k-step of positions) is
-// built directly in TMEM by builder warps from a staged x tile; B = dy[k, L] is K-major
-// (positions contiguous, as in NCHW).  Positions are split into ranges (split-K) whose
-// fp32 partials [split][tap][C][K] a second kernel adds in a fixed order.
+//   D[m, k] = sum over positions L of X_plane(tap)[c, L + tap_off[tap]] * dy[k, L]
+// over the forward linear position space (dy is zero where a position has no output),
+// with each row m standing for one (channel c, filter tap) pair.  Rows come in units of
+// 32 (one TMEM lane quarter): for C >= 32 a unit is 32 consecutive channels of one tap,
+// for C < 32 a unit is TPU taps x C channels (lane l: c = l mod C, tap = first + l / C).
+// Units are ordered channel group by channel group, taps within a group; a tile is 4
+// units (128 rows) x NK output channels x one range of positions (split-K).
+//
+// The A operand (the im2col of x for the tile's rows, 32 TMEM columns at a time) is
+// written into TMEM by builder warps from a ring of staged x; B = dy[k, L] is K-major
+// (positions contiguous, as in NCHW) in shared memory.  The ring is [plane][slot][xs]
+// with channels fastest: slot (q + sigma) mod rlen holds tile-relative position q of the
+// plane for the tile's channels (so the 32 lanes of a unit read 32 consecutive elements),
+// and every position is loaded once per tile.  sigma aligns slot groups of one 16-byte
+// chunk with aligned pixel groups, which are then loaded with 16-byte loads.  Split
+// partials [split][tap][C][K] (fp32) are added in a fixed order by a second kernel.
 struct WgradPlan {
   const void* x;         // NCHW
   const void* dy;        // N K P Q
@@ -113,21 +123,24 @@ struct WgradPlan {
   int pl_step_h, pl_step_w;
   int pl_off_h[kMaxPlanes], pl_off_w[kMaxPlanes];
   int tap_plane[kMaxTaps], tap_off[kMaxTaps];  // per filter tap r*S + s
-  int M;                 // C * RS
+  int max_off;           // largest tap_off
+  int Cg, TPU, upc;      // channels per unit, taps per unit, units per channel group
+  int nunits;            // units of 32 rows in all
   int n_mtiles, n_ntiles, nsplit;
   long long split_len;   // positions per split (multiple of KB)
   long long total_tiles; // n_mtiles * n_ntiles * nsplit
   int NK;                // output channels k per tile (MMA N, multiple of 16, <= 256)
-  int KB;                // positions per pipeline stage (multiple of 2 k-steps)
-  int xch;               // x channels staged per tile
-  int xchunks;           // 16-byte chunks per staged x row
-  int xrow;              // staged x positions per row (xchunks * elements per chunk)
-  int x_shift;           // staged x row starts x_shift positions before the stage
-  int a_stage_bytes;     // dy tile bytes per stage
-  int b_stage_bytes;     // x tile bytes per stage
+  int KB;                // positions per pipeline stage (multiple of 32 TMEM columns)
   int stages;
+  int xch;               // channels staged per tile (span of the widest tile)
+  int xs;                // elements per ring slot (>= xch, multiple of a 16-byte chunk)
+  int rlen;              // ring slots per plane (multiple of 32)
+  int sigma;             // slot of tile-relative position q is (q + sigma) mod rlen
+  int vec_x;             // 16-byte x loads allowed (unit column stride, aligned rows)
+  int a_stage_bytes;     // dy tile bytes per stage
+  int accb;              // TMEM accumulator buffers (1 or 2)
   int tmem_cols;
-  int vec_dy, vec_x;     // 16-byte copies allowed (alignment / contiguity of the tensors)
+  int vec_dy;            // 16-byte dy copies allowed (alignment / contiguity)
 };
 
 struct ReducePlan {

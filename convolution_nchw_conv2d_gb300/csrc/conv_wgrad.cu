@@ -5,16 +5,18 @@
 // LibMatrixCuDNNConvolutionAlgorithm.java; deconvolution's backward-weights in Apache
 // MXNet mkldnn_deconvolution.cc is the same product with the weight's roles swapped).
 //
-// One GEMM per tile (see WgradPlan in conv_plan.h): rows m = (c, tap) of the filter,
-// columns = output channels k, reduction over the forward linear position space L.
-// Per pipeline stage (KB positions) the producers stage dy[k, L] (K-major, positions
-// contiguous) and the few x channels the tile's rows need; builder warps then write the
-// im2col rows A[(c, tap), L] = X_plane(tap)[c, L + tap_off] straight into TMEM
-// (tcgen05.st), one k-step at a time, and one thread issues tcgen05.mma with A from TMEM
-// and B = dy from shared memory (kind::tf32 / kind::f16 with bf16), accumulating the
-// 128 x NK tile in TMEM.  The builders then store the tile's fp32 partial sums, with
-// 16-byte stores along k.  A second kernel adds the split partials in a fixed order
-// (deterministic) and writes dw in KCRS, rounding to bf16 for bf16 tensors.
+// One GEMM per tile (see WgradPlan in conv_plan.h): 128 rows (c, tap) x NK output
+// channels k, reduction over a range of the forward linear position space L.
+//   producers  stage dy[k, L] per pipeline stage (K-major: positions contiguous, as in
+//              NCHW) and append the stage's new x positions to a ring of x rows (one row
+//              per plane and channel), so every x position is read from memory once per tile.
+//   builders   write the im2col rows A[(c, tap), L] = X_plane(tap)[c, L + tap_off] into
+//              TMEM, 32 columns per buffer (tcgen05.st); the 32 lanes of a warp read 32
+//              ring rows whose starts fall in distinct shared-memory banks.
+//   MMA warp   issues tcgen05.mma with A from TMEM and B = dy from shared memory
+//              (kind::tf32 / kind::f16 with bf16), 4 per buffer, accumulating in TMEM.
+//   epilogue   stores each tile's fp32 sums as a split partial; a second kernel adds the
+//              partials in a fixed order (deterministic) and writes dw in KCRS.
 #include "conv_plan.h"
 #include "conv_stage.cuh"
 #include "sm103_ptx.cuh"
@@ -24,15 +26,16 @@ namespace cg3 {
 __device__ int g_wgrad_err;
 
 namespace {
-// CTA roles (544 threads): warps 0-7 two producer groups taking pipeline stages in turn
-// (cp.async of the dy tile and the x tile), warps 8-15 two builder sets (set h builds the
-// im2col A operand of every k-step with k-step mod 2 == h into TMEM, and runs half of the
-// epilogue), warp 16 TMEM allocation + MMA issue.
-constexpr int kThreads = 544;
+// CTA roles (672 threads): warps 0-7 two producer groups taking pipeline stages in turn,
+// warps 8-15 two builder sets (set h builds the A buffers with index mod 2 == h), warps
+// 16-19 epilogue, warp 20 TMEM allocation + MMA issue.
+constexpr int kThreads = 672;
 constexpr int kProdThreads = 128;
 constexpr int kBuildWarp0 = 8;
-constexpr int kMmaWarp = 16;
-constexpr int kNabuf = 4;  // TMEM A buffers (8 columns each)
+constexpr int kEpiWarp0 = 16;
+constexpr int kMmaWarp = 20;
+constexpr int kNabuf = 4;               // TMEM A buffers of 32 columns
+constexpr int kAcol = 32 * kNabuf;      // first accumulator column
 
 __device__ __forceinline__ uint32_t bar_at(uint32_t base, int i) { return base + 8u * (uint32_t)i; }
 
@@ -47,14 +50,150 @@ __device__ __forceinline__ WTile decode_wtile(const WgradPlan& p, long long t) {
   w.sp = (int)(r / p.n_ntiles);
   return w;
 }
+
+// (channel, tap) of lane `lane` of row unit `unit`; false for a padding row.
+__device__ __forceinline__ bool unit_row(const WgradPlan& p, int unit, int lane, int& c, int& tap) {
+  c = 0;
+  tap = 0;
+  if (unit >= p.nunits) return false;
+  const int cg = unit / p.upc;
+  const int tu = unit - cg * p.upc;
+  if (p.TPU == 1) {
+    c = cg * p.Cg + lane;
+    tap = tu;
+    return c < p.C;
+  }
+  const int tl = lane / p.Cg;
+  c = lane - tl * p.Cg;
+  tap = tu * p.TPU + tl;
+  return tl < p.TPU && tap < p.RS;
+}
+
+// First channel of the ring rows of m-tile mt.
+__device__ __forceinline__ int tile_c_lo(const WgradPlan& p, int mt) { return ((4 * mt) / p.upc) * p.Cg; }
+
+// Stages tile-relative x positions [q_begin, q_end) of every plane (the tile starts at
+// absolute position L0) into the ring for the tile's channels c_lo .. c_lo + xs - 1, in
+// whole slot groups of CHUNK slots (a group may also rewrite neighbouring positions with
+// their own values, which is harmless).  Item = (plane, slot group, CHUNK channels):
+// loaded as CHUNK 16-byte loads (one per channel, CHUNK consecutive pixels) when the
+// group's pixels are one aligned run, else element by element, then transposed in
+// registers and stored as CHUNK 16-byte shared stores (one per slot); lanes take
+// consecutive channel groups, so 8 lanes store 128 contiguous bytes.
+template <int DT>
+__device__ __forceinline__ void stage_ring(const WgradPlan& p, uint32_t ring, long long L0, int c_lo, int q_begin,
+                                           int q_end, int gtid) {
+  constexpr int CHUNK = DT == 0 ? 4 : 8;
+  constexpr int ESZ = DT == 0 ? 4 : 2;
+  constexpr int U = DT == 0 ? 2 : 1;  // items per batch: all loads of a batch precede its stores
+  using E = typename std::conditional<DT == 0, uint32_t, uint16_t>::type;
+  const E* xg = static_cast<const E*>(p.x);
+  const long long HW = (long long)p.H * p.W;
+  const int ncg = p.xs / CHUNK;
+  const int gbeg = (q_begin + p.sigma) / CHUNK;
+  const int ng = (q_end + p.sigma + CHUNK - 1) / CHUNK - gbeg;
+  const int ngr = p.rlen / CHUNK;
+  const int total = p.npl * ng * ncg;
+  for (int it0 = gtid; it0 < total; it0 += 128 * U) {
+    uint4 v[U][CHUNK];  // per item: one uint4 per channel holding CHUNK positions
+    uint32_t dst[U];
+    bool live[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int it = it0 + 128 * u;
+      live[u] = it < total;
+#pragma unroll
+      for (int i = 0; i < CHUNK; ++i) v[u][i] = make_uint4(0u, 0u, 0u, 0u);
+      dst[u] = 0u;
+      if (!live[u]) continue;
+      const int cgp = it % ncg;
+      const int rest = it / ncg;
+      const int gi = rest % ng;
+      const int pl = rest / ng;
+      const int g = gbeg + gi;
+      const long long La = L0 + (long long)g * CHUNK - p.sigma;  // absolute position of the first slot
+      dst[u] = ring + (uint32_t)((((long long)pl * p.rlen + (long long)(g % ngr) * CHUNK) * p.xs + cgp * CHUNK) * ESZ);
+      const int c0 = c_lo + cgp * CHUNK;
+      bool done = false;
+      if (p.vec_x && La >= 0 && La + CHUNK <= p.Mtot) {
+        const uint32_t n = fdiv((uint32_t)La, p.fd_img);
+        const uint32_t rem = (uint32_t)La - n * p.fd_img.d;
+        const int e = (int)fdiv(rem, p.fd_WL);
+        const int f = (int)rem - e * p.WL;
+        const int h = e * p.pl_step_h + p.pl_off_h[pl];
+        const int w = f + p.pl_off_w[pl];
+        if (f + CHUNK <= p.WL && (w & (CHUNK - 1)) == 0) {
+          done = true;  // one row, aligned: all valid, all outside, or (not here) mixed
+          if (h >= 0 && h < p.H && w >= 0 && w + CHUNK <= p.W) {
+            const E* s0 = xg + ((long long)n * p.C + c0) * HW + (long long)h * p.W + w;
+#pragma unroll
+            for (int i = 0; i < CHUNK; ++i)
+              if (c0 + i < p.C) v[u][i] = __ldg(reinterpret_cast<const uint4*>(s0 + i * HW));
+          } else if (!(w + CHUNK <= 0 || w >= p.W || h < 0 || h >= p.H)) {
+            done = false;  // partly inside: element by element
+          }
+        }
+      }
+      if (!done) {
+#pragma unroll
+        for (int j = 0; j < CHUNK; ++j) {
+          const long long L = La + j;
+          if (L < 0 || L >= p.Mtot) continue;
+          const uint32_t n = fdiv((uint32_t)L, p.fd_img);
+          const uint32_t rem = (uint32_t)L - n * p.fd_img.d;
+          const int e = (int)fdiv(rem, p.fd_WL);
+          const int f = (int)rem - e * p.WL;
+          const int h = e * p.pl_step_h + p.pl_off_h[pl];
+          const int w = f * p.pl_step_w + p.pl_off_w[pl];
+          if (h < 0 || h >= p.H || w < 0 || w >= p.W) continue;
+          const E* s0 = xg + ((long long)n * p.C + c0) * HW + (long long)h * p.W + w;
+#pragma unroll
+          for (int i = 0; i < CHUNK; ++i) {
+            if (c0 + i >= p.C) break;
+            const uint32_t x = (uint32_t)__ldg(s0 + i * HW);
+            uint32_t* wv = reinterpret_cast<uint32_t*>(&v[u][i]);
+            if constexpr (DT == 0) wv[j] = x;
+            else wv[j >> 1] |= x << (16 * (j & 1));
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      if (!live[u]) continue;
+#pragma unroll
+      for (int j = 0; j < CHUNK; ++j) {
+        const uint32_t d = dst[u] + (uint32_t)(j * p.xs * ESZ);
+        if constexpr (DT == 0) {
+          st_shared_v4(d, comp(v[u][0], j), comp(v[u][1], j), comp(v[u][2], j), comp(v[u][3], j));
+        } else {
+          const uint32_t sel = (j & 1) ? 0x7632u : 0x5410u;
+          const int k = j >> 1;
+          st_shared_v4(d, __byte_perm(comp(v[u][0], k), comp(v[u][1], k), sel),
+                       __byte_perm(comp(v[u][2], k), comp(v[u][3], k), sel),
+                       __byte_perm(comp(v[u][4], k), comp(v[u][5], k), sel),
+                       __byte_perm(comp(v[u][6], k), comp(v[u][7], k), sel));
+        }
+      }
+    }
+  }
+}
+
+// Position range [lbeg, lend) of split sp.
+__device__ __forceinline__ void split_range(const WgradPlan& p, int sp, long long& lbeg, long long& lend) {
+  lbeg = (long long)sp * p.split_len;
+  lend = lbeg + p.split_len;
+  if (lend > p.Mtot) lend = p.Mtot;
+}
 }  // namespace
 
 template <int DT>
 __global__ void __launch_bounds__(kThreads, 1) wgrad_kernel(const __grid_constant__ WgradPlan p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   constexpr int ESZ = DT == 0 ? 4 : 2;
-  constexpr int CHUNK = 16 / ESZ;
-  constexpr int KSTEP = 2 * CHUNK;  // positions per MMA
+  constexpr int CHUNK = 16 / ESZ;       // elements per 16-byte chunk
+  constexpr int PPC = DT == 0 ? 1 : 2;  // positions per TMEM column (and per ring slot)
+  constexpr int BUFP = 32 * PPC;        // positions per A buffer
   constexpr int KIND = DT;
 
   const int tid = threadIdx.x;
@@ -62,26 +201,26 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_kernel(const __grid_constan
   const int lane = tid & 31;
   const int S = p.stages;
   const int KB = p.KB;
-  const int nks = KB / KSTEP;  // k-steps per stage (even)
-  const int xrow = p.xrow;  // staged x positions per row
+  const int nbuf = KB / BUFP;  // A buffers per stage
+  const int rlen = p.rlen;
 
   uint8_t* ptr = smem_raw;
   const uint32_t a0 = smem_u32(ptr);  // dy tiles
   ptr += (size_t)S * p.a_stage_bytes;
-  const uint32_t b0 = smem_u32(ptr);  // x tiles
-  ptr += (size_t)S * p.b_stage_bytes;
-  const int tab_ints = KB + p.npl * xrow;
-  int* tabs = reinterpret_cast<int*>(ptr);  // one table set per producer group
-  ptr += (size_t)2 * tab_ints * sizeof(int);
+  const uint32_t ring = smem_u32(ptr);  // x ring, [plane][slot][xs channels]
+  ptr += ((size_t)p.npl * p.rlen * p.xs * ESZ + 15) & ~size_t(15);
+  int* tabs = reinterpret_cast<int*>(ptr);  // dy position table per producer group
+  ptr += (size_t)2 * KB * sizeof(int);
   ptr = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(ptr) + 15) & ~uintptr_t(15));
   const uint32_t full = smem_u32(ptr);
   const uint32_t empty = full + 8u * S;
   const uint32_t afull = empty + 8u * S;
   const uint32_t aempty = afull + 8u * kNabuf;
   const uint32_t accf = aempty + 8u * kNabuf;
-  const uint32_t acce = accf + 8u;
-  const uint32_t drain = acce + 8u;
-  ptr += 8 * (2 * S + 2 * kNabuf + 3);
+  const uint32_t acce = accf + 16u;
+  const uint32_t xfree = acce + 16u;
+  const uint32_t drain = xfree + 8u;
+  ptr += 8 * (2 * S + 2 * kNabuf + 6);
   volatile uint32_t* tmem_holder = reinterpret_cast<volatile uint32_t*>(ptr);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(ptr + 4);
 
@@ -94,8 +233,11 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_kernel(const __grid_constan
       mbar_init(bar_at(afull, b), 4);  // the 4 warps of the building set
       mbar_init(bar_at(aempty, b), 1);
     }
-    mbar_init(accf, 1);
-    mbar_init(acce, 8);
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(bar_at(accf, a), 1);
+      mbar_init(bar_at(acce, a), 4);
+    }
+    mbar_init(xfree, 8);
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -108,63 +250,42 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_kernel(const __grid_constan
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
-  const uint32_t dcol0 = tmem + (uint32_t)(kNabuf * 8);  // accumulator columns
 
-  const long long HW = (long long)p.H * p.W;
   const long long PQ = (long long)p.P * p.Q;
 
   if (warp < kBuildWarp0) {
     // =============================================================== producers
     const int grp = warp >> 2;
     const int gtid = tid & (kProdThreads - 1);
-    int* dytab = tabs + grp * tab_ints;
-    int* xtab = dytab + KB;
+    int* dytab = tabs + grp * KB;
     long long counter = 0;
+    int ti = 0;  // tiles of this CTA so far
     bool ok = true;
-    for (long long t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
+    for (long long t = blockIdx.x; t < p.total_tiles; t += gridDim.x, ++ti) {
       const WTile wt = decode_wtile(p, t);
-      const long long lbeg = (long long)wt.sp * p.split_len;
-      long long lend = lbeg + p.split_len;
-      if (lend > p.Mtot) lend = p.Mtot;
+      long long lbeg, lend;
+      split_range(p, wt.sp, lbeg, lend);
       const int kbase = wt.nt * p.NK;
-      const int cbase = (wt.mt * 128) / p.RS;
-      for (long long l0 = lbeg; l0 < lend; l0 += KB, ++counter) {
+      const int c_lo = tile_c_lo(p, wt.mt);
+      int s_local = 0;
+      for (long long l0 = lbeg; l0 < lend; l0 += KB, ++counter, ++s_local) {
         // Stage ownership is a pure function of the counter, so all threads of a group
         // pass the same named barriers even after an abort (which only skips work).
         if ((int)(counter & 1) != grp) continue;
         const int stage = (int)(counter % S);
         const uint32_t ephase = (uint32_t)((counter / S) & 1);
         named_bar_sync(1 + grp, kProdThreads);
-        for (int i = gtid; i < tab_ints; i += kProdThreads) {
-          if (i < KB) {
-            const long long L = l0 + i;
-            int off = -1;
-            if (L < lend) {
-              const uint32_t n = fdiv((uint32_t)L, p.fd_img);
-              const uint32_t rem = (uint32_t)L - n * p.fd_img.d;
-              const int e = (int)fdiv(rem, p.fd_WL);
-              const int f = (int)rem - e * p.WL;
-              if (e < p.P && f < p.Q) off = (int)((long long)n * p.K * PQ + (long long)e * p.Q + f);
-            }
-            dytab[i] = off;
-          } else {
-            const int j = i - KB;
-            const int pl = j / xrow;
-            const int xi = j - pl * xrow;
-            const long long L = l0 - p.x_shift + xi;
-            int off = -1;
-            if (L >= 0 && L < p.Mtot) {
-              const uint32_t n = fdiv((uint32_t)L, p.fd_img);
-              const uint32_t rem = (uint32_t)L - n * p.fd_img.d;
-              const int e = (int)fdiv(rem, p.fd_WL);
-              const int f = (int)rem - e * p.WL;
-              const int h = e * p.pl_step_h + p.pl_off_h[pl];
-              const int w = f * p.pl_step_w + p.pl_off_w[pl];
-              if (h >= 0 && h < p.H && w >= 0 && w < p.W)
-                off = (int)((long long)n * p.C * HW + (long long)h * p.W + w);
-            }
-            xtab[j] = off;
+        for (int i = gtid; i < KB; i += kProdThreads) {
+          const long long L = l0 + i;
+          int off = -1;
+          if (L < lend) {
+            const uint32_t n = fdiv((uint32_t)L, p.fd_img);
+            const uint32_t rem = (uint32_t)L - n * p.fd_img.d;
+            const int e = (int)fdiv(rem, p.fd_WL);
+            const int f = (int)rem - e * p.WL;
+            if (e < p.P && f < p.Q) off = (int)((long long)n * p.K * PQ + (long long)e * p.Q + f);
           }
+          dytab[i] = off;
         }
         named_bar_sync(1 + grp, kProdThreads);
         if (!ok) continue;
@@ -172,11 +293,20 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_kernel(const __grid_constan
           ok = false;
           continue;
         }
+        // The first stages of a tile overwrite ring slots the previous tile's builders
+        // may still be reading.
+        if (s_local < S && ti > 0 && !mbar_wait(xfree, (uint32_t)((ti - 1) & 1), abort_flag, &g_wgrad_err)) {
+          ok = false;
+          continue;
+        }
         const uint32_t a_st = a0 + (uint32_t)stage * p.a_stage_bytes;
-        const uint32_t b_st = b0 + (uint32_t)stage * p.b_stage_bytes;
-        // dy: [chunk][k row][CHUNK positions]; x: [plane][channel][positions]
+        // dy: [chunk][k row][CHUNK positions]
         stage_position_rows<DT>(p.dy, PQ, dytab, KB / CHUNK, p.NK, p.K - kbase, a_st, kbase, p.vec_dy != 0, gtid);
-        stage_channel_rows<DT>(p.x, HW, p.C, xtab, xrow, p.npl, p.xch, p.xchunks, b_st, cbase, p.vec_x != 0, gtid);
+        // x: this stage's new positions (stage 0 also loads the halo).
+        if (s_local == 0)
+          stage_ring<DT>(p, ring, lbeg, c_lo, 0, KB + p.max_off, gtid);
+        else
+          stage_ring<DT>(p, ring, lbeg, c_lo, s_local * KB + p.max_off, (s_local + 1) * KB + p.max_off, gtid);
         cp_async_commit();  // wait_group only covers committed groups
         cp_async_wait<0>();
         fence_proxy_async();
@@ -185,26 +315,24 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_kernel(const __grid_constan
     }
     cp_async_commit();
     cp_async_wait<0>();
-  } else if (warp < kMmaWarp) {
-    // =============================================================== builders + epilogue
-    const int set = (warp - kBuildWarp0) >> 2;  // builds k-steps with index mod 2 == set
+  } else if (warp < kEpiWarp0) {
+    // =============================================================== builders
+    const int set = (warp - kBuildWarp0) >> 2;  // builds A buffers with index mod 2 == set
     const int q = warp & 3;                      // TMEM lane quarter
     long long counter = 0, kglob = 0;
-    uint32_t aphase = 0;
     bool ok = true;
     for (long long t = blockIdx.x; t < p.total_tiles && ok; t += gridDim.x) {
       const WTile wt = decode_wtile(p, t);
-      const long long lbeg = (long long)wt.sp * p.split_len;
-      long long lend = lbeg + p.split_len;
-      if (lend > p.Mtot) lend = p.Mtot;
-      const int cbase = (wt.mt * 128) / p.RS;
-      const int m = wt.mt * 128 + q * 32 + lane;  // this thread's A row (c, tap)
-      const bool mvalid = m < p.M;
-      const int c = mvalid ? m / p.RS : 0;
-      const int tap = mvalid ? m - c * p.RS : 0;
-      // byte offset of this row's first needed x element inside a stage's x tile
-      const uint32_t xoff =
-          (uint32_t)(((p.tap_plane[tap] * p.xch + (c - cbase)) * xrow + p.tap_off[tap] + p.x_shift) * ESZ);
+      long long lbeg, lend;
+      split_range(p, wt.sp, lbeg, lend);
+      int c, tap;
+      const bool rv = unit_row(p, wt.mt * 4 + q, lane, c, tap);
+      const int c_lo = tile_c_lo(p, wt.mt);
+      // byte offset of this lane's (plane, channel) in ring slot 0; slot offset of its tap
+      const uint32_t rowb = rv ? (uint32_t)(((long long)p.tap_plane[tap] * p.rlen * p.xs + (c - c_lo)) * ESZ) : 0u;
+      const uint32_t sstr = (uint32_t)(p.xs * ESZ);  // bytes per slot
+      const int toff = (rv ? p.tap_off[tap] : 0) + p.sigma;
+      int sb = 0;  // tile-relative position of the stage's first position, mod rlen
       for (long long l0 = lbeg; l0 < lend && ok; l0 += KB, ++counter) {
         const int stage = (int)(counter % S);
         const uint32_t fphase = (uint32_t)((counter / S) & 1);
@@ -212,37 +340,41 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_kernel(const __grid_constan
           ok = false;
           break;
         }
-        const uint32_t xs = b0 + (uint32_t)stage * p.b_stage_bytes + xoff;
-        for (int ks = 0; ks < nks; ++ks, ++kglob) {
-          if ((ks & 1) != set) continue;
+        for (int b = 0; b < nbuf; ++b, ++kglob) {
+          if ((int)(kglob & 1) != set) continue;
           const int abuf = (int)(kglob % kNabuf);
           const uint32_t use = (uint32_t)((kglob / kNabuf) & 1);
           if (!mbar_wait(bar_at(aempty, abuf), use ^ 1u, abort_flag, &g_wgrad_err)) {
             ok = false;
             break;
           }
-          uint32_t v[8];
-          if (mvalid) {
-            const uint32_t a = xs + (uint32_t)(ks * KSTEP * ESZ);
-            if constexpr (DT == 0) {
+          uint32_t v[32];
+          int slot = sb + b * BUFP + toff;
+          if (slot >= rlen) slot -= rlen;
+          if (rv) {
 #pragma unroll
-              for (int e = 0; e < 8; ++e)
-                asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v[e]) : "r"(a + 4u * e));
-            } else {
-#pragma unroll
-              for (int e = 0; e < 8; ++e) {
+            for (int j = 0; j < 32; ++j) {
+              if constexpr (DT == 0) {
+                asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v[j]) : "r"(ring + rowb + (uint32_t)slot * sstr));
+                slot += 1;
+                if (slot >= rlen) slot -= rlen;
+              } else {
                 uint16_t lo, hi;
-                asm volatile("ld.shared.u16 %0, [%1];" : "=h"(lo) : "r"(a + 4u * e));
-                asm volatile("ld.shared.u16 %0, [%1];" : "=h"(hi) : "r"(a + 4u * e + 2u));
-                v[e] = (uint32_t)lo | ((uint32_t)hi << 16);
+                asm volatile("ld.shared.u16 %0, [%1];" : "=h"(lo) : "r"(ring + rowb + (uint32_t)slot * sstr));
+                slot += 1;
+                if (slot >= rlen) slot -= rlen;
+                asm volatile("ld.shared.u16 %0, [%1];" : "=h"(hi) : "r"(ring + rowb + (uint32_t)slot * sstr));
+                slot += 1;
+                if (slot >= rlen) slot -= rlen;
+                v[j] = (uint32_t)lo | ((uint32_t)hi << 16);
               }
             }
           } else {
 #pragma unroll
-            for (int e = 0; e < 8; ++e) v[e] = 0u;
+            for (int j = 0; j < 32; ++j) v[j] = 0u;
           }
           tc_fence_after();
-          tmem_st8(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(abuf * 8), v);
+          tmem_st32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(abuf * 32), v);
           tmem_st_wait();
           tc_fence_before();
           __syncwarp();
@@ -250,91 +382,117 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_kernel(const __grid_constan
         }
         if (!ok) break;
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar_at(empty, stage));  // done reading this stage's x tile
+        if (lane == 0) mbar_arrive(bar_at(empty, stage));  // done reading this stage's x
+        sb += KB;
+        if (sb >= rlen) sb -= rlen;
       }
       if (!ok) break;
-      // ---- epilogue: this set writes half of the accumulator columns
-      if (!mbar_wait(accf, aphase, abort_flag, &g_wgrad_err)) break;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(xfree);  // the ring may be refilled for the next tile
+    }
+  } else if (warp < kMmaWarp) {
+    // =============================================================== epilogue
+    const int q = warp & 3;
+    int acc = 0;
+    uint32_t aphase = 0;
+    for (long long t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
+      const WTile wt = decode_wtile(p, t);
+      if (!mbar_wait(bar_at(accf, acc), aphase, abort_flag, &g_wgrad_err)) break;
       tc_fence_after();
-      const int tapo = tap;  // filter tap index r*S + s
-      const int half = p.NK >> 1;
-      const int k0 = wt.nt * p.NK + set * half;
-      float* dst = p.partial + (((long long)wt.sp * p.RS + tapo) * p.C + c) * (long long)p.K;
-      for (int c0 = 0; c0 < half; c0 += 16) {
+      int c, tap;
+      const bool rv = unit_row(p, wt.mt * 4 + q, lane, c, tap);
+      const int k0 = wt.nt * p.NK;
+      float* dst = p.partial + (((long long)wt.sp * p.RS + tap) * p.C + c) * (long long)p.K + k0;
+      const uint32_t tcol = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(kAcol + acc * p.NK);
+      const bool vec = (p.K & 3) == 0;
+      for (int c0 = 0; c0 < p.NK; c0 += 16) {
         uint32_t r[16];
-        tmem_ld16(dcol0 + ((uint32_t)(q * 32) << 16) + (uint32_t)(set * half + c0), r);
+        tmem_ld16(tcol + (uint32_t)c0, r);
         tmem_ld_wait();
-        if (mvalid) {
+        if (rv) {
           const int kk = k0 + c0;
-          if (kk + 16 <= p.K && ((p.K & 3) == 0)) {
+          if (vec && kk + 16 <= p.K) {
 #pragma unroll
             for (int j = 0; j < 16; j += 4)
-              *reinterpret_cast<uint4*>(dst + kk + j) = make_uint4(r[j], r[j + 1], r[j + 2], r[j + 3]);
+              *reinterpret_cast<uint4*>(dst + c0 + j) = make_uint4(r[j], r[j + 1], r[j + 2], r[j + 3]);
           } else {
 #pragma unroll
             for (int j = 0; j < 16; ++j)
-              if (kk + j < p.K) dst[kk + j] = __uint_as_float(r[j]);
+              if (kk + j < p.K) dst[c0 + j] = __uint_as_float(r[j]);
           }
         }
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(acce);
-      aphase ^= 1u;
+      if (lane == 0) mbar_arrive(bar_at(acce, acc));
+      if (++acc == p.accb) {
+        acc = 0;
+        aphase ^= 1u;
+      }
     }
   } else {
     // =============================================================== MMA issuer
-    if (lane == 0) {
-      const uint32_t id = idesc(KIND, 128, p.NK, 0, 0);
-      const uint32_t b_hi = (uint32_t)(sdesc(0u, 0u, 128u) >> 32);
-      long long counter = 0, kglob = 0;
-      uint32_t aphase = 0;
-      bool ok = true;
-      bool issued_any = false;
-      for (long long t = blockIdx.x; t < p.total_tiles && ok; t += gridDim.x) {
-        const WTile wt = decode_wtile(p, t);
-        const long long lbeg = (long long)wt.sp * p.split_len;
-        long long lend = lbeg + p.split_len;
-        if (lend > p.Mtot) lend = p.Mtot;
-        if (!mbar_wait(acce, aphase ^ 1u, abort_flag, &g_wgrad_err)) break;
+    // The whole warp runs the loop; one elected lane issues and commits.
+    const bool leader = elect_one();
+    const uint32_t id = idesc(KIND, 128, p.NK, 0, 0);
+    const uint32_t b_hi = (uint32_t)(sdesc(0u, 0u, 128u) >> 32);
+    const uint32_t nk16 = (uint32_t)p.NK;  // one chunk of the dy tile, in descriptor units
+    long long counter = 0, kglob = 0;
+    int acc = 0;
+    uint32_t aphase = 0;
+    bool ok = true;
+    bool issued_any = false;
+    for (long long t = blockIdx.x; t < p.total_tiles && ok; t += gridDim.x) {
+      long long lbeg, lend;
+      split_range(p, decode_wtile(p, t).sp, lbeg, lend);
+      if (!mbar_wait(bar_at(acce, acc), aphase ^ 1u, abort_flag, &g_wgrad_err)) break;
+      tc_fence_after();
+      const uint32_t dcol = tmem + (uint32_t)(kAcol + acc * p.NK);
+      bool first = true;
+      for (long long l0 = lbeg; l0 < lend && ok; l0 += KB, ++counter) {
+        const int stage = (int)(counter % S);
+        const uint32_t fphase = (uint32_t)((counter / S) & 1);
+        if (!mbar_wait(bar_at(full, stage), fphase, abort_flag, &g_wgrad_err)) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
-        bool first = true;
-        for (long long l0 = lbeg; l0 < lend && ok; l0 += KB, ++counter) {
-          const int stage = (int)(counter % S);
-          const uint32_t fphase = (uint32_t)((counter / S) & 1);
-          if (!mbar_wait(bar_at(full, stage), fphase, abort_flag, &g_wgrad_err)) {
+        // B = dy tile, K-major [chunk][k row][16 B]; buffer b, MMA i uses chunks 8b+2i, 8b+2i+1.
+        const uint32_t blo0 = (uint32_t)sdesc(a0 + (uint32_t)stage * p.a_stage_bytes, (uint32_t)p.NK * 16u, 0u);
+        for (int b = 0; b < nbuf; ++b, ++kglob) {
+          const int abuf = (int)(kglob % kNabuf);
+          const uint32_t use = (uint32_t)((kglob / kNabuf) & 1);
+          if (!mbar_wait(bar_at(afull, abuf), use, abort_flag, &g_wgrad_err)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          // B = dy tile, K-major [chunk][k row][16 B]: k-step ks uses chunks 2ks, 2ks+1.
-          uint32_t blo = (uint32_t)sdesc(a0 + (uint32_t)stage * p.a_stage_bytes, (uint32_t)p.NK * 16u, 0u);
-          const uint32_t b_ks = 2u * (uint32_t)p.NK;
-          for (int ks = 0; ks < nks; ++ks, ++kglob) {
-            const int abuf = (int)(kglob % kNabuf);
-            const uint32_t use = (uint32_t)((kglob / kNabuf) & 1);
-            if (!mbar_wait(bar_at(afull, abuf), use, abort_flag, &g_wgrad_err)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            mma_ts_lh<KIND>(dcol0, tmem + (uint32_t)(abuf * 8), blo, b_hi, id, first ? 0u : 1u);
+          if (leader) {
+            const uint32_t blo = blo0 + (uint32_t)(8 * b) * nk16;
+            const uint32_t acol = tmem + (uint32_t)(abuf * 32);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              mma_ts_lh<KIND>(dcol, acol + (uint32_t)(8 * i), blo + (uint32_t)(2 * i) * nk16, b_hi, id,
+                              (first && i == 0) ? 0u : 1u);
             tc_commit(bar_at(aempty, abuf));
-            issued_any = true;
-            first = false;
-            blo += b_ks;
           }
-          if (!ok) break;
-          tc_commit(bar_at(empty, stage));
+          __syncwarp();
+          issued_any = true;
+          first = false;
         }
         if (!ok) break;
-        tc_commit(accf);
+        if (leader) tc_commit(bar_at(empty, stage));
+      }
+      if (!ok) break;
+      if (leader) tc_commit(bar_at(accf, acc));
+      if (++acc == p.accb) {
+        acc = 0;
         aphase ^= 1u;
       }
-      if (!ok && issued_any) {
-        tc_commit(drain);
-        mbar_wait_drain(drain, 0);
-      }
+    }
+    if (!ok && issued_any && leader) {
+      tc_commit(drain);
+      mbar_wait_drain(drain, 0);
     }
     __syncwarp();
   }
@@ -371,16 +529,17 @@ __global__ void wgrad_reduce_kernel(const __grid_constant__ ReducePlan rp) {
   }
 }
 
-size_t wgrad_smem_bytes(const WgradPlan& p) {
-  size_t b = (size_t)p.stages * (p.a_stage_bytes + p.b_stage_bytes);
-  b += (size_t)2 * (p.KB + p.npl * p.xrow) * sizeof(int);
+size_t wgrad_smem_bytes(const WgradPlan& p, int dt) {
+  size_t b = (size_t)p.stages * p.a_stage_bytes;
+  b += ((size_t)p.npl * p.rlen * p.xs * (dt == 0 ? 4 : 2) + 15) & ~size_t(15);
+  b += (size_t)2 * p.KB * sizeof(int);
   b = (b + 15) & ~size_t(15);
-  b += 8 * (2 * p.stages + 2 * 4 + 3) + 16;
+  b += 8 * (2 * p.stages + 2 * kNabuf + 6) + 16;
   return b + 1024;
 }
 
 cudaError_t launch_wgrad(const WgradPlan& p, int dt, int grid, cudaStream_t st) {
-  const size_t smem = wgrad_smem_bytes(p);
+  const size_t smem = wgrad_smem_bytes(p, dt);
   cudaError_t e;
   if (dt == 0) {
     e = cudaFuncSetAttribute(wgrad_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
