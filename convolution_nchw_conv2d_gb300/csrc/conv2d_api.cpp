@@ -409,6 +409,44 @@ int build_bwd_data(const Desc& d0, const void* dy, const void* w, void* dx, void
   return CONV2D_OK;
 }
 
+// ------------------------------------------------------------------ tensor maps
+// cuTensorMapEncodeTiled, looked up once through the runtime (no link-time dependency on
+// the driver library).
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess && f)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+    else
+      cudaGetLastError();
+  });
+  return fn;
+}
+
+// dy (N, K, P, Q) as the 4-D tensor (w = Q, k = K, e = P, n = N) with a box of one
+// 16-byte chunk of positions by NK output channels.  False if it cannot be encoded.
+bool encode_dy_map(CUtensorMap* m, const void* dy, int dt, int N, int K, int P, int Q, int NK) {
+  EncodeTiledFn fn = encode_tiled_fn();
+  if (!fn) return false;
+  const uint64_t esz = dt == 0 ? 4 : 2;
+  const cuuint64_t dims[4] = {(cuuint64_t)Q, (cuuint64_t)K, (cuuint64_t)P, (cuuint64_t)N};
+  const cuuint64_t strides[3] = {(cuuint64_t)P * Q * esz, (cuuint64_t)Q * esz, (cuuint64_t)K * P * Q * esz};
+  const cuuint32_t box[4] = {(cuuint32_t)(16 / esz), (cuuint32_t)NK, 1u, 1u};
+  const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+  const CUresult r = fn(m, dt == 0 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
+                        const_cast<void*>(dy), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // ------------------------------------------------------------------ wgrad plan
 struct WgradBuild {
   WgradPlan p;
@@ -475,62 +513,28 @@ int build_bwd_filter(const Desc& d0, const void* x, const void* dy, void* dw, vo
   const int ncg = (d.C + p.Cg - 1) / p.Cg;
   p.nunits = ncg * p.upc;
   p.n_mtiles = (p.nunits + 3) / 4;
-  p.xch = 0;
-  for (int mt = 0; mt < p.n_mtiles; ++mt) {
-    const int cg0 = (4 * mt) / p.upc, cg1 = std::min(p.nunits - 1, 4 * mt + 3) / p.upc;
-    p.xch = std::max(p.xch, std::min(d.C, (cg1 + 1) * p.Cg) - cg0 * p.Cg);
-  }
   p.NK = d.K <= 16 ? 16 : std::min(round_up(d.K, 32), 256);
   p.n_ntiles = (d.K + p.NK - 1) / p.NK;
-  p.accb = (128 + 2 * p.NK <= 512) ? 2 : 1;
+  // m-tiles per CTA tile: as many accumulators as TMEM holds next to the 4 A buffers, so
+  // x and dy are staged once for all of them; two accumulator sets when they fit.
+  p.G = std::max(1, std::min(p.n_mtiles, (512 - 128) / p.NK));
+  p.n_mgroups = (p.n_mtiles + p.G - 1) / p.G;
+  p.G = (p.n_mtiles + p.n_mgroups - 1) / p.n_mgroups;  // balance the groups
+  p.accb = (128 + 2 * p.G * p.NK <= 512) ? 2 : 1;
   p.tmem_cols = 32;
-  while (p.tmem_cols < 128 + p.accb * p.NK) p.tmem_cols <<= 1;
+  while (p.tmem_cols < 128 + p.accb * p.G * p.NK) p.tmem_cols <<= 1;
+  p.xch = 0;
+  for (int mg = 0; mg < p.n_mgroups; ++mg) {
+    const int u0 = 4 * p.G * mg, u1 = std::min(p.nunits, 4 * p.G * (mg + 1)) - 1;
+    const int cg0 = u0 / p.upc, cg1 = u1 / p.upc;
+    p.xch = std::max(p.xch, std::min(d.C, (cg1 + 1) * p.Cg) - cg0 * p.Cg);
+  }
   // 16-byte x loads: unit column stride, rows and planes of whole chunks, aligned base;
   // sigma puts the start of every slot group on a chunk-aligned pixel.
   p.vec_x = d.sw == 1 && p.WL % CHUNK == 0 && d.W % CHUNK == 0 && ((uintptr_t)x & 15) == 0;
   p.sigma = p.vec_x ? (CHUNK - d.pw % CHUNK) % CHUNK : 0;
-  // Ring slot width: the channel span rounded to a chunk, plus the padding (in chunks) that
-  // minimises bank conflicts of the builders' reads when a unit mixes taps (C < 32).
-  {
-    const int base_xs = round_up(p.xch, CHUNK);
-    int best_xs = base_xs;
-    long long best_cost = -1;
-    for (int padc = 0; padc < (p.TPU > 1 ? 8 : 1); ++padc) {
-      const long long xs = base_xs + (long long)padc * CHUNK;
-      long long cost = 0;
-      for (int u = 0; u < p.nunits; ++u) {
-        int cnt[32] = {0};
-        const int c_lo = ((4 * (u / 4)) / p.upc) * p.Cg;
-        int worst = 0;
-        for (int l = 0; l < 32; ++l) {
-          const int cg = u / p.upc, tu = u % p.upc;
-          int c, tap;
-          bool v;
-          if (p.TPU == 1) {
-            c = cg * p.Cg + l;
-            tap = tu;
-            v = c < d.C;
-          } else {
-            const int tl = l / p.Cg;
-            c = l - tl * p.Cg;
-            tap = tu * p.TPU + tl;
-            v = tl < p.TPU && tap < p.RS;
-          }
-          if (!v) continue;
-          // word address (bank) at the first slot, 4-byte elements (2-byte: half a word)
-          const long long el = ((long long)p.tap_plane[tap] * 4096 + p.tap_off[tap]) * xs + (c - c_lo);
-          const long long word = d.dt == 0 ? el : el / 2;
-          worst = std::max(worst, ++cnt[word & 31]);
-        }
-        cost += worst;
-      }
-      if (best_cost < 0 || cost < best_cost) {
-        best_cost = cost;
-        best_xs = (int)xs;
-      }
-    }
-    p.xs = best_xs;
-  }
+  // Copy-engine staging (unit column stride, chunk-aligned rows and tensors).
+  p.use_tma = p.vec_x && p.vec_dy && encode_dy_map(&p.tm_dy, dy, d.dt, d.N, d.K, d.P, d.Q, p.NK) ? 1 : 0;
   // Pipeline: the most positions in flight (stages x KB) that fit, then the larger KB.
   bool fitted = false;
   long long best = -1;
@@ -541,8 +545,11 @@ int build_bwd_filter(const Desc& d0, const void* x, const void* dy, void* dw, vo
       WgradPlan q = p;
       q.KB = KB;
       q.stages = S;
-      // the ring holds S stages plus the halo, plus a slot group rewritten at each end
+      // the ring holds S stages plus the halo, plus a slot group rewritten at each end;
+      // row stride: 16 bytes past a multiple of 128 (conflict-free 16-byte reads of 8 rows)
       q.rlen = round_up(S * KB + p.max_off + 2 * CHUNK, 32);
+      q.xs = q.rlen;
+      while ((q.xs * ESZ) % 128 != 16) q.xs += CHUNK;
       q.a_stage_bytes = KB * p.NK * ESZ;
       if (wgrad_smem_bytes(q, d.dt) > di.smem_optin) continue;
       const long long score = (long long)S * KB * 4 + KB / 32;
@@ -555,9 +562,11 @@ int build_bwd_filter(const Desc& d0, const void* x, const void* dy, void* dw, vo
   }
   if (!fitted) return CONV2D_ERR_UNSUPPORTED;
   p = bestp;
+  p.fd_EL = make_fastdiv((uint32_t)p.EL);
+  p.fd_rlen = make_fastdiv((uint32_t)p.rlen);
   // Split the positions so that the tiles fill the SMs with the shortest makespan
   // (tiles per CTA x positions per tile), preferring fewer splits.
-  const long long base = (long long)p.n_mtiles * p.n_ntiles;
+  const long long base = (long long)p.n_mgroups * p.n_ntiles;
   const long long stage_count = (p.Mtot + p.KB - 1) / p.KB;
   const size_t per_split = (size_t)p.RS * d.C * d.K * sizeof(float);
   long long nsb = 1;

@@ -13,6 +13,8 @@
 #pragma once
 #include <cstdint>
 
+#include <cuda.h>  // CUtensorMap (the plan only carries it; encoding is done by the host planner)
+
 namespace cg3 {
 
 // Unsigned 32-bit division by a divisor fixed at planning time, as a multiply-high and
@@ -104,13 +106,18 @@ struct PackPlan {
 //
 // The A operand (the im2col of x for the tile's rows, 32 TMEM columns at a time) is
 // written into TMEM by builder warps from a ring of staged x; B = dy[k, L] is K-major
-// (positions contiguous, as in NCHW) in shared memory.  The ring is [plane][slot][xs]
-// with channels fastest: slot (q + sigma) mod rlen holds tile-relative position q of the
-// plane for the tile's channels (so the 32 lanes of a unit read 32 consecutive elements),
-// and every position is loaded once per tile.  sigma aligns slot groups of one 16-byte
-// chunk with aligned pixel groups, which are then loaded with 16-byte loads.  Split
-// partials [split][tap][C][K] (fp32) are added in a fixed order by a second kernel.
+// (positions contiguous, as in NCHW) in shared memory.  The ring is [plane][channel][xs]:
+// slot (q + sigma) mod rlen of a row holds tile-relative position q of that plane and
+// channel, and every position is loaded once per tile.  sigma aligns 16-byte slot groups
+// with 16-byte pixel groups, which are copied with 16-byte cp.async; the row stride xs is
+// 16 bytes more than a multiple of 128, so the builders' 16-byte reads of 8 channel rows
+// at the same slot fall in distinct banks.  Split partials [split][tap][C][K] (fp32) are
+// added in a fixed order by a second kernel.
 struct WgradPlan {
+  // dy as a 4-D tensor (w, k, row e, image n) for copy-engine loads of one 16-byte chunk of
+  // positions for NK output channels ([k][CHUNK] in shared memory); valid when use_tma.
+  CUtensorMap tm_dy;
+  int use_tma;           // copy-engine staging: dy by tensor copies, x rows by bulk copies
   const void* x;         // NCHW
   const void* dy;        // N K P Q
   float* partial;        // [split][R*S][C][K] fp32
@@ -119,6 +126,7 @@ struct WgradPlan {
   int WL, EL;
   long long Mtot;        // positions (< 2^31)
   FastDiv fd_img, fd_WL; // division by EL*WL and by WL
+  FastDiv fd_EL, fd_rlen;  // division by EL and by rlen
   int npl;
   int pl_step_h, pl_step_w;
   int pl_off_h[kMaxPlanes], pl_off_w[kMaxPlanes];
@@ -127,18 +135,20 @@ struct WgradPlan {
   int Cg, TPU, upc;      // channels per unit, taps per unit, units per channel group
   int nunits;            // units of 32 rows in all
   int n_mtiles, n_ntiles, nsplit;
+  int G;                 // m-tiles per CTA tile (one TMEM accumulator each; x and dy staged once)
+  int n_mgroups;         // ceil(n_mtiles / G)
   long long split_len;   // positions per split (multiple of KB)
-  long long total_tiles; // n_mtiles * n_ntiles * nsplit
+  long long total_tiles; // n_mgroups * n_ntiles * nsplit
   int NK;                // output channels k per tile (MMA N, multiple of 16, <= 256)
   int KB;                // positions per pipeline stage (multiple of 32 TMEM columns)
   int stages;
   int xch;               // channels staged per tile (span of the widest tile)
-  int xs;                // elements per ring slot (>= xch, multiple of a 16-byte chunk)
-  int rlen;              // ring slots per plane (multiple of 32)
+  int xs;                // ring row stride in elements (>= rlen)
+  int rlen;              // ring slots per row (multiple of 32)
   int sigma;             // slot of tile-relative position q is (q + sigma) mod rlen
   int vec_x;             // 16-byte x loads allowed (unit column stride, aligned rows)
   int a_stage_bytes;     // dy tile bytes per stage
-  int accb;              // TMEM accumulator buffers (1 or 2)
+  int accb;              // TMEM accumulator sets of G tiles (1 or 2)
   int tmem_cols;
   int vec_dy;            // 16-byte dy copies allowed (alignment / contiguity)
 };

@@ -26,28 +26,31 @@ namespace cg3 {
 __device__ int g_wgrad_err;
 
 namespace {
-// CTA roles (672 threads): warps 0-7 two producer groups taking pipeline stages in turn,
-// warps 8-15 two builder sets (set h builds the A buffers with index mod 2 == h), warps
-// 16-19 epilogue, warp 20 TMEM allocation + MMA issue.
-constexpr int kThreads = 672;
+// CTA roles (544 threads): warps 0-3 producers (cp.async, two stages in flight), warps 4-11
+// two builder sets (set h builds the A buffers with index mod 2 == h), warps 12-15
+// epilogue, warp 16 TMEM allocation + MMA issue.
+constexpr int kThreads = 544;
 constexpr int kProdThreads = 128;
-constexpr int kBuildWarp0 = 8;
-constexpr int kEpiWarp0 = 16;
-constexpr int kMmaWarp = 20;
+constexpr int kBuildWarp0 = 4;
+constexpr int kEpiWarp0 = 12;
+constexpr int kMmaWarp = 16;
 constexpr int kNabuf = 4;               // TMEM A buffers of 32 columns
 constexpr int kAcol = 32 * kNabuf;      // first accumulator column
 
 __device__ __forceinline__ uint32_t bar_at(uint32_t base, int i) { return base + 8u * (uint32_t)i; }
 
 struct WTile {
-  int mt, nt, sp;
+  int mg, nt, sp;
+  int mt0, gcount;  // first m-tile of the group and the group's m-tiles
 };
 __device__ __forceinline__ WTile decode_wtile(const WgradPlan& p, long long t) {
   WTile w;
-  w.mt = (int)(t % p.n_mtiles);
-  long long r = t / p.n_mtiles;
+  w.mg = (int)(t % p.n_mgroups);
+  long long r = t / p.n_mgroups;
   w.nt = (int)(r % p.n_ntiles);
   w.sp = (int)(r / p.n_ntiles);
+  w.mt0 = w.mg * p.G;
+  w.gcount = p.n_mtiles - w.mt0 < p.G ? p.n_mtiles - w.mt0 : p.G;
   return w;
 }
 
@@ -69,111 +72,185 @@ __device__ __forceinline__ bool unit_row(const WgradPlan& p, int unit, int lane,
   return tl < p.TPU && tap < p.RS;
 }
 
-// First channel of the ring rows of m-tile mt.
-__device__ __forceinline__ int tile_c_lo(const WgradPlan& p, int mt) { return ((4 * mt) / p.upc) * p.Cg; }
+// First channel of the ring rows of a group whose first m-tile is mt0.
+__device__ __forceinline__ int tile_c_lo(const WgradPlan& p, int mt0) { return ((4 * mt0) / p.upc) * p.Cg; }
 
 // Stages tile-relative x positions [q_begin, q_end) of every plane (the tile starts at
-// absolute position L0) into the ring for the tile's channels c_lo .. c_lo + xs - 1, in
-// whole slot groups of CHUNK slots (a group may also rewrite neighbouring positions with
-// their own values, which is harmless).  Item = (plane, slot group, CHUNK channels):
-// loaded as CHUNK 16-byte loads (one per channel, CHUNK consecutive pixels) when the
-// group's pixels are one aligned run, else element by element, then transposed in
-// registers and stored as CHUNK 16-byte shared stores (one per slot); lanes take
-// consecutive channel groups, so 8 lanes store 128 contiguous bytes.
+// absolute position L0) into the ring rows of the tile's channels c_lo .. c_lo + xch - 1,
+// in whole slot groups of CHUNK slots (a group may also rewrite neighbouring positions
+// with their own values, which is harmless).  Lanes take consecutive slot groups and the
+// group's 4 warps split the rows, so each copy instruction of a warp moves 512 contiguous
+// bytes.  A group whose pixels are one aligned run (or lie wholly outside the tensor) is
+// one 16-byte cp.async (zero-filled outside); a mixed group is copied element by element.
 template <int DT>
 __device__ __forceinline__ void stage_ring(const WgradPlan& p, uint32_t ring, long long L0, int c_lo, int q_begin,
                                            int q_end, int gtid) {
   constexpr int CHUNK = DT == 0 ? 4 : 8;
   constexpr int ESZ = DT == 0 ? 4 : 2;
-  constexpr int U = DT == 0 ? 2 : 1;  // items per batch: all loads of a batch precede its stores
   using E = typename std::conditional<DT == 0, uint32_t, uint16_t>::type;
   const E* xg = static_cast<const E*>(p.x);
   const long long HW = (long long)p.H * p.W;
-  const int ncg = p.xs / CHUNK;
+  const int lane = gtid & 31, gw = gtid >> 5;
   const int gbeg = (q_begin + p.sigma) / CHUNK;
   const int ng = (q_end + p.sigma + CHUNK - 1) / CHUNK - gbeg;
   const int ngr = p.rlen / CHUNK;
-  const int total = p.npl * ng * ncg;
-  for (int it0 = gtid; it0 < total; it0 += 128 * U) {
-    uint4 v[U][CHUNK];  // per item: one uint4 per channel holding CHUNK positions
-    uint32_t dst[U];
-    bool live[U];
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int it = it0 + 128 * u;
-      live[u] = it < total;
-#pragma unroll
-      for (int i = 0; i < CHUNK; ++i) v[u][i] = make_uint4(0u, 0u, 0u, 0u);
-      dst[u] = 0u;
-      if (!live[u]) continue;
-      const int cgp = it % ncg;
-      const int rest = it / ncg;
-      const int gi = rest % ng;
-      const int pl = rest / ng;
-      const int g = gbeg + gi;
-      const long long La = L0 + (long long)g * CHUNK - p.sigma;  // absolute position of the first slot
-      dst[u] = ring + (uint32_t)((((long long)pl * p.rlen + (long long)(g % ngr) * CHUNK) * p.xs + cgp * CHUNK) * ESZ);
-      const int c0 = c_lo + cgp * CHUNK;
-      bool done = false;
-      if (p.vec_x && La >= 0 && La + CHUNK <= p.Mtot) {
-        const uint32_t n = fdiv((uint32_t)La, p.fd_img);
-        const uint32_t rem = (uint32_t)La - n * p.fd_img.d;
-        const int e = (int)fdiv(rem, p.fd_WL);
-        const int f = (int)rem - e * p.WL;
-        const int h = e * p.pl_step_h + p.pl_off_h[pl];
-        const int w = f + p.pl_off_w[pl];
-        if (f + CHUNK <= p.WL && (w & (CHUNK - 1)) == 0) {
-          done = true;  // one row, aligned: all valid, all outside, or (not here) mixed
-          if (h >= 0 && h < p.H && w >= 0 && w + CHUNK <= p.W) {
-            const E* s0 = xg + ((long long)n * p.C + c0) * HW + (long long)h * p.W + w;
-#pragma unroll
-            for (int i = 0; i < CHUNK; ++i)
-              if (c0 + i < p.C) v[u][i] = __ldg(reinterpret_cast<const uint4*>(s0 + i * HW));
-          } else if (!(w + CHUNK <= 0 || w >= p.W || h < 0 || h >= p.H)) {
-            done = false;  // partly inside: element by element
+  const uint32_t rowb = (uint32_t)(p.xs * ESZ);
+  for (int gi = lane; gi < ng + ((32 - ng % 32) % 32); gi += 32) {
+    const bool gv = gi < ng;
+    const int g = gbeg + gi;
+    const long long La = L0 + (long long)g * CHUNK - p.sigma;  // absolute position of the first slot
+    const uint32_t sdst = ring + (uint32_t)((g % ngr) * CHUNK * ESZ);
+    // the group's CHUNK positions: image n, linear row e, column f of the first
+    uint32_t n = 0;
+    int e = 0, f = 0;
+    bool one_row = false;
+    if (gv && La >= 0 && La + CHUNK <= p.Mtot) {
+      n = fdiv((uint32_t)La, p.fd_img);
+      const uint32_t rem = (uint32_t)La - n * p.fd_img.d;
+      e = (int)fdiv(rem, p.fd_WL);
+      f = (int)rem - e * p.WL;
+      one_row = f + CHUNK <= p.WL;
+    }
+    for (int pl = 0; pl < p.npl; ++pl) {
+      // 0: nothing to do, 1: 16-byte copy from src (valid run), 2: zero group, 3: mixed
+      int mode = 0;
+      long long soff = 0;
+      if (gv) {
+        mode = 3;
+        if (one_row) {
+          const int h = e * p.pl_step_h + p.pl_off_h[pl];
+          const int w = f * p.pl_step_w + p.pl_off_w[pl];
+          const int wl = (CHUNK - 1) * p.pl_step_w + w;  // last pixel's column
+          if (h < 0 || h >= p.H || wl < 0 || w >= p.W) {
+            mode = 2;
+          } else if (p.vec_x && (w & (CHUNK - 1)) == 0 && w >= 0 && wl < p.W) {
+            mode = 1;
+            soff = (long long)n * p.C * HW + (long long)h * p.W + w;
           }
         }
       }
-      if (!done) {
+      if (mode == 1 || mode == 2) {
+        for (int cr = gw; cr < p.xch; cr += 4) {
+          const int c = c_lo + cr;
+          const bool v = mode == 1 && c < p.C;
+          cp_async_16(sdst + (uint32_t)(pl * p.xch + cr) * rowb, v ? (const void*)(xg + soff + (long long)c * HW) : p.x,
+                      v ? 16 : 0);
+        }
+      } else if (mode == 3) {
+        // element offsets (channel 0) of the group's positions, -1 = zero
+        int offs[CHUNK];
 #pragma unroll
         for (int j = 0; j < CHUNK; ++j) {
+          offs[j] = -1;
           const long long L = La + j;
           if (L < 0 || L >= p.Mtot) continue;
-          const uint32_t n = fdiv((uint32_t)L, p.fd_img);
-          const uint32_t rem = (uint32_t)L - n * p.fd_img.d;
-          const int e = (int)fdiv(rem, p.fd_WL);
-          const int f = (int)rem - e * p.WL;
-          const int h = e * p.pl_step_h + p.pl_off_h[pl];
-          const int w = f * p.pl_step_w + p.pl_off_w[pl];
-          if (h < 0 || h >= p.H || w < 0 || w >= p.W) continue;
-          const E* s0 = xg + ((long long)n * p.C + c0) * HW + (long long)h * p.W + w;
+          const uint32_t nn = fdiv((uint32_t)L, p.fd_img);
+          const uint32_t rem = (uint32_t)L - nn * p.fd_img.d;
+          const int ee = (int)fdiv(rem, p.fd_WL);
+          const int ff = (int)rem - ee * p.WL;
+          const int h = ee * p.pl_step_h + p.pl_off_h[pl];
+          const int w = ff * p.pl_step_w + p.pl_off_w[pl];
+          if (h >= 0 && h < p.H && w >= 0 && w < p.W) offs[j] = (int)((long long)nn * p.C * HW + (long long)h * p.W + w);
+        }
+        // rows in batches of RB: all loads of a batch precede its stores
+        constexpr int RB = DT == 0 ? 4 : 2;
+        for (int cr0 = gw; cr0 < p.xch; cr0 += 4 * RB) {
+          uint32_t wv[RB][4];
 #pragma unroll
-          for (int i = 0; i < CHUNK; ++i) {
-            if (c0 + i >= p.C) break;
-            const uint32_t x = (uint32_t)__ldg(s0 + i * HW);
-            uint32_t* wv = reinterpret_cast<uint32_t*>(&v[u][i]);
-            if constexpr (DT == 0) wv[j] = x;
-            else wv[j >> 1] |= x << (16 * (j & 1));
+          for (int r = 0; r < RB; ++r) {
+            wv[r][0] = wv[r][1] = wv[r][2] = wv[r][3] = 0u;
+            const int c = c_lo + cr0 + 4 * r;
+            if (cr0 + 4 * r >= p.xch || c >= p.C) continue;
+            const E* sc = xg + (long long)c * HW;
+#pragma unroll
+            for (int j = 0; j < CHUNK; ++j) {
+              if (offs[j] < 0) continue;
+              const uint32_t x = (uint32_t)__ldg(sc + offs[j]);
+              if constexpr (DT == 0) wv[r][j] = x;
+              else wv[r][j >> 1] |= x << (16 * (j & 1));
+            }
           }
+#pragma unroll
+          for (int r = 0; r < RB; ++r)
+            if (cr0 + 4 * r < p.xch)
+              st_shared_v4(sdst + (uint32_t)(pl * p.xch + cr0 + 4 * r) * rowb, wv[r][0], wv[r][1], wv[r][2], wv[r][3]);
         }
       }
     }
+  }
+}
+
+// Stages the dy tile of positions [l0, l0 + KB) (zero at and past lend, and where a
+// position has no output) for output channels kbase .. kbase + NK - 1 as the B operand
+// [chunk j][k row][16 bytes].  Each warp takes whole chunks (the chunk's class is
+// warp-uniform): a chunk of CHUNK valid, contiguous, aligned positions is one 16-byte
+// cp.async per row, a chunk with no valid position is zeros, others element by element.
+// Rows at and past K - kbase are left untouched (they only reach discarded columns).
+template <int DT>
+__device__ __forceinline__ void stage_dy(const WgradPlan& p, uint32_t dst0, long long l0, long long lend, int kbase,
+                                         int gtid) {
+  constexpr int CHUNK = DT == 0 ? 4 : 8;
+  using E = typename std::conditional<DT == 0, uint32_t, uint16_t>::type;
+  const E* dg = static_cast<const E*>(p.dy);
+  const long long PQ = (long long)p.P * p.Q;
+  const int lane = gtid & 31, gw = gtid >> 5;
+  const int mrows = p.K - kbase < p.NK ? p.K - kbase : p.NK;
+  for (int j = gw; j < p.KB / CHUNK; j += 4) {
+    const long long La = l0 + (long long)CHUNK * j;
+    const uint32_t dbase = dst0 + (uint32_t)(j * p.NK) * 16u;
+    int mode = 2;  // 1: 16-byte copies, 2: zeros, 3: element by element
+    long long soff = 0;
+    if (La < lend) {
+      const uint32_t n = fdiv((uint32_t)La, p.fd_img);
+      const uint32_t rem = (uint32_t)La - n * p.fd_img.d;
+      const int e = (int)fdiv(rem, p.fd_WL);
+      const int f = (int)rem - e * p.WL;
+      if (p.vec_dy && La + CHUNK <= lend && e < p.P && f + CHUNK <= p.Q) {
+        mode = 1;
+        soff = (long long)n * p.K * PQ + (long long)e * p.Q + f;
+      } else if (!(p.vec_dy && (e >= p.P || f >= p.Q))) {
+        mode = 3;
+      }
+    }
+    if (mode == 1) {
+      for (int m = lane; m < mrows; m += 32)
+        cp_async_16(dbase + (uint32_t)m * 16u, dg + soff + (long long)(kbase + m) * PQ, 16);
+    } else if (mode == 2) {
+      for (int m = lane; m < mrows; m += 32) st_shared_v4(dbase + (uint32_t)m * 16u, 0u, 0u, 0u, 0u);
+    } else {
+      int offs[CHUNK];  // element offsets of the chunk's positions (channel 0), -1 = zero
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      if (!live[u]) continue;
+      for (int i = 0; i < CHUNK; ++i) {
+        const long long L = La + i;
+        offs[i] = -1;
+        if (L >= lend) continue;
+        const uint32_t n = fdiv((uint32_t)L, p.fd_img);
+        const uint32_t rem = (uint32_t)L - n * p.fd_img.d;
+        const int e = (int)fdiv(rem, p.fd_WL);
+        const int f = (int)rem - e * p.WL;
+        if (e < p.P && f < p.Q) offs[i] = (int)((long long)n * p.K * PQ + (long long)e * p.Q + f);
+      }
+      // rows in batches of RB: all loads of a batch precede its stores
+      constexpr int RB = DT == 0 ? 4 : 2;
+      for (int m0 = lane; m0 < mrows; m0 += 32 * RB) {
+        uint32_t wv[RB][4];
 #pragma unroll
-      for (int j = 0; j < CHUNK; ++j) {
-        const uint32_t d = dst[u] + (uint32_t)(j * p.xs * ESZ);
-        if constexpr (DT == 0) {
-          st_shared_v4(d, comp(v[u][0], j), comp(v[u][1], j), comp(v[u][2], j), comp(v[u][3], j));
-        } else {
-          const uint32_t sel = (j & 1) ? 0x7632u : 0x5410u;
-          const int k = j >> 1;
-          st_shared_v4(d, __byte_perm(comp(v[u][0], k), comp(v[u][1], k), sel),
-                       __byte_perm(comp(v[u][2], k), comp(v[u][3], k), sel),
-                       __byte_perm(comp(v[u][4], k), comp(v[u][5], k), sel),
-                       __byte_perm(comp(v[u][6], k), comp(v[u][7], k), sel));
+        for (int r = 0; r < RB; ++r) {
+          wv[r][0] = wv[r][1] = wv[r][2] = wv[r][3] = 0u;
+          const int m = m0 + 32 * r;
+          if (m >= mrows) continue;
+          const E* rowp = dg + (long long)(kbase + m) * PQ;
+#pragma unroll
+          for (int i = 0; i < CHUNK; ++i) {
+            if (offs[i] < 0) continue;
+            const uint32_t x = (uint32_t)__ldg(rowp + offs[i]);
+            if constexpr (DT == 0) wv[r][i] = x;
+            else wv[r][i >> 1] |= x << (16 * (i & 1));
+          }
         }
+#pragma unroll
+        for (int r = 0; r < RB; ++r)
+          if (m0 + 32 * r < mrows) st_shared_v4(dbase + (uint32_t)(m0 + 32 * r) * 16u, wv[r][0], wv[r][1], wv[r][2], wv[r][3]);
       }
     }
   }
@@ -186,6 +263,20 @@ __device__ __forceinline__ void split_range(const WgradPlan& p, int sp, long lon
   if (lend > p.Mtot) lend = p.Mtot;
 }
 }  // namespace
+
+// tcgen05.st of w[K .. K + 31] to 32 TMEM columns (K fixed, so w stays in registers).
+template <int K>
+__device__ __forceinline__ void tmem_st32_at(uint32_t taddr, const uint32_t (&w)[36]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(w[K + 0]), "r"(w[K + 1]), "r"(w[K + 2]), "r"(w[K + 3]), "r"(w[K + 4]), "r"(w[K + 5]), "r"(w[K + 6]),
+      "r"(w[K + 7]), "r"(w[K + 8]), "r"(w[K + 9]), "r"(w[K + 10]), "r"(w[K + 11]), "r"(w[K + 12]), "r"(w[K + 13]),
+      "r"(w[K + 14]), "r"(w[K + 15]), "r"(w[K + 16]), "r"(w[K + 17]), "r"(w[K + 18]), "r"(w[K + 19]),
+      "r"(w[K + 20]), "r"(w[K + 21]), "r"(w[K + 22]), "r"(w[K + 23]), "r"(w[K + 24]), "r"(w[K + 25]),
+      "r"(w[K + 26]), "r"(w[K + 27]), "r"(w[K + 28]), "r"(w[K + 29]), "r"(w[K + 30]), "r"(w[K + 31])
+      : "memory");
+}
 
 template <int DT>
 __global__ void __launch_bounds__(kThreads, 1) wgrad_kernel(const __grid_constant__ WgradPlan p) {
@@ -204,13 +295,12 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_kernel(const __grid_constan
   const int nbuf = KB / BUFP;  // A buffers per stage
   const int rlen = p.rlen;
 
-  uint8_t* ptr = smem_raw;
+  // 1024-byte aligned base (the size includes the slack): tensor-copy destinations
+  uint8_t* ptr = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t a0 = smem_u32(ptr);  // dy tiles
   ptr += (size_t)S * p.a_stage_bytes;
-  const uint32_t ring = smem_u32(ptr);  // x ring, [plane][slot][xs channels]
-  ptr += ((size_t)p.npl * p.rlen * p.xs * ESZ + 15) & ~size_t(15);
-  int* tabs = reinterpret_cast<int*>(ptr);  // dy position table per producer group
-  ptr += (size_t)2 * KB * sizeof(int);
+  const uint32_t ring = smem_u32(ptr);  // x ring, [plane][channel][xs]
+  ptr += ((size_t)p.npl * p.xch * p.xs * ESZ + 15) & ~size_t(15);
   ptr = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(ptr) + 15) & ~uintptr_t(15));
   const uint32_t full = smem_u32(ptr);
   const uint32_t empty = full + 8u * S;
@@ -251,70 +341,205 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_kernel(const __grid_constan
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
 
-  const long long PQ = (long long)p.P * p.Q;
-
   if (warp < kBuildWarp0) {
     // =============================================================== producers
-    const int grp = warp >> 2;
-    const int gtid = tid & (kProdThreads - 1);
-    int* dytab = tabs + grp * KB;
+    if (p.use_tma) {
+      // Copy-engine staging: per stage, one tensor copy per 16-byte chunk of positions
+      // (all NK output channels) for dy, and one bulk copy per (plane, linear row, channel)
+      // for the valid pixel run of x, plus shared stores of zeros for padding slots.  Every
+      // thread adds its own copies' bytes to the stage's full barrier before issuing them
+      // and then arrives without waiting, so the producers run ahead by up to S stages.
+      const int gtid = tid;
+      using E = typename std::conditional<DT == 0, uint32_t, uint16_t>::type;
+      const E* xg = static_cast<const E*>(p.x);
+      uint32_t last_phase[4] = {0u, 0u, 0u, 0u};  // 1 + parity of the last fill per slot (thread 0)
+      long long counter = 0;
+      int ti = 0;
+      bool ok = true;
+      for (long long t = blockIdx.x; t < p.total_tiles && ok; t += gridDim.x, ++ti) {
+        const WTile wt = decode_wtile(p, t);
+        long long lbeg, lend;
+        split_range(p, wt.sp, lbeg, lend);
+        const int kbase = wt.nt * p.NK;
+        const int c_lo = tile_c_lo(p, wt.mt0);
+        const int nch_x = p.C - c_lo < p.xch ? p.C - c_lo : p.xch;  // ring rows with real channels
+        int s_local = 0;
+        for (long long l0 = lbeg; l0 < lend; l0 += KB, ++counter, ++s_local) {
+          const int stage = (int)(counter % S);
+          const uint32_t ephase = (uint32_t)((counter / S) & 1);
+          if (!mbar_wait(bar_at(empty, stage), ephase ^ 1u, abort_flag, &g_wgrad_err)) {
+            ok = false;
+            break;
+          }
+          if (s_local < S && ti > 0 && !mbar_wait(xfree, (uint32_t)((ti - 1) & 1), abort_flag, &g_wgrad_err)) {
+            ok = false;
+            break;
+          }
+          // the slot's previous contents were read through the generic proxy (builder
+          // loads): order those reads before this stage's copy-engine writes
+          fence_proxy_async();
+          const uint32_t fb = bar_at(full, stage);
+          const uint32_t a_st = a0 + (uint32_t)stage * p.a_stage_bytes;
+          // dy: chunk j = positions l0 + CHUNK*j .. +CHUNK-1 (one linear row: WL % CHUNK == 0)
+          for (int j = gtid; j < KB / CHUNK; j += kProdThreads) {
+            const long long La = l0 + (long long)CHUNK * j;
+            int n = p.N, e = 0, f = 0;  // past the tensor: the copy reads zeros
+            if (La < p.Mtot) {
+              const uint32_t nn = fdiv((uint32_t)La, p.fd_img);
+              const uint32_t rem = (uint32_t)La - nn * p.fd_img.d;
+              n = (int)nn;
+              e = (int)fdiv(rem, p.fd_WL);
+              f = (int)rem - e * p.WL;
+            }
+            mbar_expect_tx(fb, (uint32_t)(p.NK * 16));
+            tma_load_4d(a_st + (uint32_t)(j * p.NK * 16), &p.tm_dy, f, kbase, e, n, fb);
+          }
+          // x: tile-relative positions [q0, q1) (stage 0 also loads the halo); 32-bit
+          // position arithmetic (positions < 2^31), divisions by multiply-high
+          const int q0 = s_local == 0 ? 0 : s_local * KB + p.max_off;
+          const int q1 = (s_local + 1) * KB + p.max_off;
+          const uint32_t Lx0 = (uint32_t)(lbeg + q0);
+          const uint32_t Lx1 = (uint32_t)(lbeg + q1 < p.Mtot ? lbeg + q1 : p.Mtot);
+          const uint32_t lb = (uint32_t)lbeg;
+          // slot of tile-relative position q >= -sigma (a copy widened to an aligned start
+          // may begin a few positions before the tile: those slots are dead at its start)
+          auto slot_of = [&](int q) {
+            const uint32_t v = (uint32_t)(q + p.sigma + rlen);
+            return (int)(v - fdiv(v, p.fd_rlen) * (uint32_t)rlen);
+          };
+          if (Lx0 < Lx1) {
+            const uint32_t row0 = fdiv(Lx0, p.fd_WL);
+            const int nseg = (int)(fdiv(Lx1 - 1u, p.fd_WL) - row0 + 1u);
+            const int items = p.npl * nseg * nch_x;
+            for (int it = gtid; it < items; it += kProdThreads) {
+              const int cr = it % nch_x;
+              const int rest = it / nch_x;
+              const int sg = rest % nseg;
+              const int pl = rest / nseg;
+              const uint32_t R = row0 + (uint32_t)sg;  // linear row (image n, row e)
+              const uint32_t Rs = R * (uint32_t)p.WL;  // its first position
+              const int f0 = (int)((Lx0 > Rs ? Lx0 : Rs) - Rs);
+              const int f1 = (int)((Lx1 < Rs + (uint32_t)p.WL ? Lx1 : Rs + (uint32_t)p.WL) - Rs);
+              const int n = (int)fdiv(R, p.fd_EL);
+              const int e = (int)R - n * p.EL;
+              const int h = e * p.pl_step_h + p.pl_off_h[pl];
+              const int ow = p.pl_off_w[pl];
+              const bool hv = h >= 0 && h < p.H;
+              const int rq = (int)(Rs - lb);             // tile-relative position of the row start
+              int lo = f0 + ow < 0 ? 0 : f0 + ow;        // valid pixel run [lo, hi)
+              int hi = f1 + ow > p.W ? p.W : f1 + ow;
+              const uint32_t rowbase = ring + (uint32_t)((pl * p.xch + cr) * p.xs) * ESZ;
+              if (hv && lo < hi) {
+                const int wa = lo & ~(CHUNK - 1);
+                const int wb = (hi + CHUNK - 1) & ~(CHUNK - 1);  // <= W (W % CHUNK == 0)
+                const int slot = slot_of(rq + (wa - ow));
+                const E* src = xg + (((long long)n * p.C + c_lo + cr) * p.H + h) * p.W + wa;
+                const int len = wb - wa;
+                const int part = rlen - slot < len ? rlen - slot : len;
+                mbar_expect_tx(fb, (uint32_t)(len * ESZ));
+                bulk_g2s(rowbase + (uint32_t)(slot * ESZ), src, (uint32_t)(part * ESZ), fb);
+                if (part < len) bulk_g2s(rowbase, src + part, (uint32_t)((len - part) * ESZ), fb);
+              } else {
+                lo = hi = f1 + ow;  // no valid pixel: every slot of the segment is zero
+              }
+              // zeros: the segment's positions before and after the valid run
+              auto zero_slots = [&](int fa, int fz) {
+                if (fa >= fz) return;
+                int sl = slot_of(rq + fa);
+                for (int ff = fa; ff < fz; ++ff) {
+                  if constexpr (DT == 0)
+                    asm volatile("st.shared.b32 [%0], %1;" ::"r"(rowbase + (uint32_t)sl * 4u), "r"(0u) : "memory");
+                  else
+                    asm volatile("st.shared.b16 [%0], %1;" ::"r"(rowbase + (uint32_t)sl * 2u), "h"((uint16_t)0) : "memory");
+                  if (++sl == rlen) sl = 0;
+                }
+              };
+              zero_slots(f0, lo - ow);
+              zero_slots(hi - ow, f1);
+            }
+          }
+          // positions past the last image: zeros (they only meet zero dy, but stale
+          // shared memory could hold non-finite values)
+          if ((long long)lbeg + q1 > p.Mtot) {
+            const int za = (int)((Lx0 > (uint32_t)p.Mtot ? (long long)Lx0 : p.Mtot) - lbeg);
+            const int nz = q1 - za;
+            const int rows = p.npl * p.xch;
+            for (int it = gtid; it < nz * rows; it += kProdThreads) {
+              const int row = it / nz;
+              const int q = za + it - row * nz;
+              const uint32_t a = ring + (uint32_t)(row * p.xs + slot_of(q)) * ESZ;
+              if constexpr (DT == 0)
+                asm volatile("st.shared.b32 [%0], %1;" ::"r"(a), "r"(0u) : "memory");
+              else
+                asm volatile("st.shared.b16 [%0], %1;" ::"r"(a), "h"((uint16_t)0) : "memory");
+            }
+          }
+          mbar_arrive(fb);
+          if (gtid == 0) last_phase[stage] = 1u + ephase;
+        }
+      }
+      // After an abort, wait (bounded) for copies still in flight into shared memory.
+      if (gtid == 0 && *abort_flag) {
+        for (int st = 0; st < S; ++st)
+          if (last_phase[st]) mbar_wait_drain(bar_at(full, st), last_phase[st] - 1u);
+      }
+    } else {
+    // Stage s's copies are issued, committed as one cp.async group, and its full barrier
+    // is arrived on once the next stage's copies are in flight too (wait_group 1), so two
+    // stages load at once.  Before any wait that needs the consumers to finish the pending
+    // stage (the ring refill at a tile start), the pending stage is completed first.
+    const int gtid = tid;
     long long counter = 0;
     int ti = 0;  // tiles of this CTA so far
+    int pending = -1;  // stage slot issued but not yet arrived on
     bool ok = true;
+    auto complete_pending = [&](bool all) {
+      if (pending < 0) return;
+      if (all) cp_async_wait<0>();
+      else cp_async_wait<1>();
+      fence_proxy_async();
+      mbar_arrive(bar_at(full, pending));
+      pending = -1;
+    };
     for (long long t = blockIdx.x; t < p.total_tiles; t += gridDim.x, ++ti) {
       const WTile wt = decode_wtile(p, t);
       long long lbeg, lend;
       split_range(p, wt.sp, lbeg, lend);
       const int kbase = wt.nt * p.NK;
-      const int c_lo = tile_c_lo(p, wt.mt);
+      const int c_lo = tile_c_lo(p, wt.mt0);
       int s_local = 0;
-      for (long long l0 = lbeg; l0 < lend; l0 += KB, ++counter, ++s_local) {
-        // Stage ownership is a pure function of the counter, so all threads of a group
-        // pass the same named barriers even after an abort (which only skips work).
-        if ((int)(counter & 1) != grp) continue;
+      for (long long l0 = lbeg; l0 < lend && ok; l0 += KB, ++counter, ++s_local) {
         const int stage = (int)(counter % S);
         const uint32_t ephase = (uint32_t)((counter / S) & 1);
-        named_bar_sync(1 + grp, kProdThreads);
-        for (int i = gtid; i < KB; i += kProdThreads) {
-          const long long L = l0 + i;
-          int off = -1;
-          if (L < lend) {
-            const uint32_t n = fdiv((uint32_t)L, p.fd_img);
-            const uint32_t rem = (uint32_t)L - n * p.fd_img.d;
-            const int e = (int)fdiv(rem, p.fd_WL);
-            const int f = (int)rem - e * p.WL;
-            if (e < p.P && f < p.Q) off = (int)((long long)n * p.K * PQ + (long long)e * p.Q + f);
-          }
-          dytab[i] = off;
-        }
-        named_bar_sync(1 + grp, kProdThreads);
-        if (!ok) continue;
         if (!mbar_wait(bar_at(empty, stage), ephase ^ 1u, abort_flag, &g_wgrad_err)) {
           ok = false;
-          continue;
+          break;
         }
-        // The first stages of a tile overwrite ring slots the previous tile's builders
-        // may still be reading.
-        if (s_local < S && ti > 0 && !mbar_wait(xfree, (uint32_t)((ti - 1) & 1), abort_flag, &g_wgrad_err)) {
-          ok = false;
-          continue;
+        // The first stages of a tile overwrite ring slots the previous tile's builders may
+        // still be reading.
+        if (s_local < S && ti > 0) {
+          complete_pending(true);
+          if (!mbar_wait(xfree, (uint32_t)((ti - 1) & 1), abort_flag, &g_wgrad_err)) {
+            ok = false;
+            break;
+          }
         }
         const uint32_t a_st = a0 + (uint32_t)stage * p.a_stage_bytes;
-        // dy: [chunk][k row][CHUNK positions]
-        stage_position_rows<DT>(p.dy, PQ, dytab, KB / CHUNK, p.NK, p.K - kbase, a_st, kbase, p.vec_dy != 0, gtid);
+        stage_dy<DT>(p, a_st, l0, lend, kbase, gtid);
         // x: this stage's new positions (stage 0 also loads the halo).
         if (s_local == 0)
           stage_ring<DT>(p, ring, lbeg, c_lo, 0, KB + p.max_off, gtid);
         else
           stage_ring<DT>(p, ring, lbeg, c_lo, s_local * KB + p.max_off, (s_local + 1) * KB + p.max_off, gtid);
-        cp_async_commit();  // wait_group only covers committed groups
-        cp_async_wait<0>();
-        fence_proxy_async();
-        mbar_arrive(bar_at(full, stage));
+        cp_async_commit();
+        complete_pending(false);
+        pending = stage;
       }
+      if (!ok) break;
     }
-    cp_async_commit();
+    complete_pending(true);
     cp_async_wait<0>();
+    }
   } else if (warp < kEpiWarp0) {
     // =============================================================== builders
     const int set = (warp - kBuildWarp0) >> 2;  // builds A buffers with index mod 2 == set
@@ -325,13 +550,8 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_kernel(const __grid_constan
       const WTile wt = decode_wtile(p, t);
       long long lbeg, lend;
       split_range(p, wt.sp, lbeg, lend);
-      int c, tap;
-      const bool rv = unit_row(p, wt.mt * 4 + q, lane, c, tap);
-      const int c_lo = tile_c_lo(p, wt.mt);
-      // byte offset of this lane's (plane, channel) in ring slot 0; slot offset of its tap
-      const uint32_t rowb = rv ? (uint32_t)(((long long)p.tap_plane[tap] * p.rlen * p.xs + (c - c_lo)) * ESZ) : 0u;
-      const uint32_t sstr = (uint32_t)(p.xs * ESZ);  // bytes per slot
-      const int toff = (rv ? p.tap_off[tap] : 0) + p.sigma;
+      const int c_lo = tile_c_lo(p, wt.mt0);
+      const int ngr = rlen / CHUNK;
       int sb = 0;  // tile-relative position of the stage's first position, mod rlen
       for (long long l0 = lbeg; l0 < lend && ok; l0 += KB, ++counter) {
         const int stage = (int)(counter % S);
@@ -340,41 +560,82 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_kernel(const __grid_constan
           ok = false;
           break;
         }
-        for (int b = 0; b < nbuf; ++b, ++kglob) {
+        for (int bg = 0; bg < nbuf * wt.gcount && ok; ++bg, ++kglob) {
           if ((int)(kglob & 1) != set) continue;
+          const int b = bg / wt.gcount;  // buffer of positions
+          const int g = bg - b * wt.gcount;  // m-tile within the group
           const int abuf = (int)(kglob % kNabuf);
           const uint32_t use = (uint32_t)((kglob / kNabuf) & 1);
           if (!mbar_wait(bar_at(aempty, abuf), use ^ 1u, abort_flag, &g_wgrad_err)) {
             ok = false;
             break;
           }
-          uint32_t v[32];
+          int c, tap;
+          const bool rv = unit_row(p, (wt.mt0 + g) * 4 + q, lane, c, tap);
+          // byte offset of this lane's ring row; slot offset of its tap
+          const uint32_t rowb = rv ? (uint32_t)((p.tap_plane[tap] * p.xch + (c - c_lo)) * p.xs * ESZ) : 0u;
+          // (with one tap per unit the tap, hence the slot, is the same in every lane)
+          const int toff = ((p.TPU == 1 || rv) ? p.tap_off[tap] : 0) + p.sigma;
+          // tcgen05.st is warp-collective: every lane must reach the same instruction, so the
+          // two read paths below branch on p.TPU (uniform), never on lane data.
+          uint32_t w[36];
           int slot = sb + b * BUFP + toff;
           if (slot >= rlen) slot -= rlen;
-          if (rv) {
+          const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(abuf * 32);
+          if (p.TPU == 1) {
+            // One tap per unit: the slot is the same in all lanes.  9 aligned 16-byte reads
+            // cover the 32 columns wherever they start in a group; column j is word k + j
+            // (fp32) or halfwords rho + 2j, rho + 2j + 1 (bf16, shifted down when rho is odd).
+            const int rho = slot & (CHUNK - 1);
+            const int k = DT == 0 ? rho : rho >> 1;
+            if (rv) {
+              int g = slot / CHUNK;
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              if constexpr (DT == 0) {
-                asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v[j]) : "r"(ring + rowb + (uint32_t)slot * sstr));
-                slot += 1;
-                if (slot >= rlen) slot -= rlen;
-              } else {
-                uint16_t lo, hi;
-                asm volatile("ld.shared.u16 %0, [%1];" : "=h"(lo) : "r"(ring + rowb + (uint32_t)slot * sstr));
-                slot += 1;
-                if (slot >= rlen) slot -= rlen;
-                asm volatile("ld.shared.u16 %0, [%1];" : "=h"(hi) : "r"(ring + rowb + (uint32_t)slot * sstr));
-                slot += 1;
-                if (slot >= rlen) slot -= rlen;
-                v[j] = (uint32_t)lo | ((uint32_t)hi << 16);
+              for (int i = 0; i < 9; ++i) {
+                asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+                             : "=r"(w[4 * i]), "=r"(w[4 * i + 1]), "=r"(w[4 * i + 2]), "=r"(w[4 * i + 3])
+                             : "r"(ring + rowb + (uint32_t)(g * 16)));
+                if (++g == ngr) g = 0;
               }
+              if (DT != 0 && (rho & 1)) {
+#pragma unroll
+                for (int j = 0; j < 35; ++j) w[j] = __byte_perm(w[j], w[j + 1], 0x5432);
+              }
+            } else {
+#pragma unroll
+              for (int j = 0; j < 36; ++j) w[j] = 0u;
+            }
+            tc_fence_after();
+            switch (k) {
+              case 0: tmem_st32_at<0>(ta, w); break;
+              case 1: tmem_st32_at<1>(ta, w); break;
+              case 2: tmem_st32_at<2>(ta, w); break;
+              default: tmem_st32_at<3>(ta, w); break;
             }
           } else {
+            // Several taps per unit: each lane reads its own slots element by element.
 #pragma unroll
-            for (int j = 0; j < 32; ++j) v[j] = 0u;
+            for (int j = 0; j < 36; ++j) w[j] = 0u;
+            if (rv) {
+              const uint32_t rb = ring + rowb;
+#pragma unroll
+              for (int j = 0; j < 32; ++j) {
+                if constexpr (DT == 0) {
+                  asm volatile("ld.shared.b32 %0, [%1];" : "=r"(w[j]) : "r"(rb + (uint32_t)slot * 4u));
+                  if (++slot == rlen) slot = 0;
+                } else {
+                  uint16_t lo, hi;
+                  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(lo) : "r"(rb + (uint32_t)slot * 2u));
+                  if (++slot == rlen) slot = 0;
+                  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(hi) : "r"(rb + (uint32_t)slot * 2u));
+                  if (++slot == rlen) slot = 0;
+                  w[j] = (uint32_t)lo | ((uint32_t)hi << 16);
+                }
+              }
+            }
+            tc_fence_after();
+            tmem_st32_at<0>(ta, w);
           }
-          tc_fence_after();
-          tmem_st32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(abuf * 32), v);
           tmem_st_wait();
           tc_fence_before();
           __syncwarp();
@@ -399,26 +660,28 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_kernel(const __grid_constan
       const WTile wt = decode_wtile(p, t);
       if (!mbar_wait(bar_at(accf, acc), aphase, abort_flag, &g_wgrad_err)) break;
       tc_fence_after();
-      int c, tap;
-      const bool rv = unit_row(p, wt.mt * 4 + q, lane, c, tap);
       const int k0 = wt.nt * p.NK;
-      float* dst = p.partial + (((long long)wt.sp * p.RS + tap) * p.C + c) * (long long)p.K + k0;
-      const uint32_t tcol = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(kAcol + acc * p.NK);
       const bool vec = (p.K & 3) == 0;
-      for (int c0 = 0; c0 < p.NK; c0 += 16) {
-        uint32_t r[16];
-        tmem_ld16(tcol + (uint32_t)c0, r);
-        tmem_ld_wait();
-        if (rv) {
-          const int kk = k0 + c0;
-          if (vec && kk + 16 <= p.K) {
+      for (int g = 0; g < wt.gcount; ++g) {
+        int c, tap;
+        const bool rv = unit_row(p, (wt.mt0 + g) * 4 + q, lane, c, tap);
+        float* dst = p.partial + (((long long)wt.sp * p.RS + tap) * p.C + c) * (long long)p.K + k0;
+        const uint32_t tcol = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(kAcol + (acc * p.G + g) * p.NK);
+        for (int c0 = 0; c0 < p.NK; c0 += 16) {
+          uint32_t r[16];
+          tmem_ld16(tcol + (uint32_t)c0, r);
+          tmem_ld_wait();
+          if (rv) {
+            const int kk = k0 + c0;
+            if (vec && kk + 16 <= p.K) {
 #pragma unroll
-            for (int j = 0; j < 16; j += 4)
-              *reinterpret_cast<uint4*>(dst + c0 + j) = make_uint4(r[j], r[j + 1], r[j + 2], r[j + 3]);
-          } else {
+              for (int j = 0; j < 16; j += 4)
+                *reinterpret_cast<uint4*>(dst + c0 + j) = make_uint4(r[j], r[j + 1], r[j + 2], r[j + 3]);
+            } else {
 #pragma unroll
-            for (int j = 0; j < 16; ++j)
-              if (kk + j < p.K) dst[c0 + j] = __uint_as_float(r[j]);
+              for (int j = 0; j < 16; ++j)
+                if (kk + j < p.K) dst[c0 + j] = __uint_as_float(r[j]);
+            }
           }
         }
       }
@@ -443,12 +706,13 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_kernel(const __grid_constan
     bool ok = true;
     bool issued_any = false;
     for (long long t = blockIdx.x; t < p.total_tiles && ok; t += gridDim.x) {
+      const WTile wt = decode_wtile(p, t);
       long long lbeg, lend;
-      split_range(p, decode_wtile(p, t).sp, lbeg, lend);
+      split_range(p, wt.sp, lbeg, lend);
       if (!mbar_wait(bar_at(acce, acc), aphase ^ 1u, abort_flag, &g_wgrad_err)) break;
       tc_fence_after();
-      const uint32_t dcol = tmem + (uint32_t)(kAcol + acc * p.NK);
-      bool first = true;
+      const uint32_t dcol0 = tmem + (uint32_t)(kAcol + acc * p.G * p.NK);
+      bool first_stage = true;
       for (long long l0 = lbeg; l0 < lend && ok; l0 += KB, ++counter) {
         const int stage = (int)(counter % S);
         const uint32_t fphase = (uint32_t)((counter / S) & 1);
@@ -459,7 +723,9 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_kernel(const __grid_constan
         tc_fence_after();
         // B = dy tile, K-major [chunk][k row][16 B]; buffer b, MMA i uses chunks 8b+2i, 8b+2i+1.
         const uint32_t blo0 = (uint32_t)sdesc(a0 + (uint32_t)stage * p.a_stage_bytes, (uint32_t)p.NK * 16u, 0u);
-        for (int b = 0; b < nbuf; ++b, ++kglob) {
+        for (int bg = 0; bg < nbuf * wt.gcount; ++bg, ++kglob) {
+          const int b = bg / wt.gcount;
+          const int g = bg - b * wt.gcount;
           const int abuf = (int)(kglob % kNabuf);
           const uint32_t use = (uint32_t)((kglob / kNabuf) & 1);
           if (!mbar_wait(bar_at(afull, abuf), use, abort_flag, &g_wgrad_err)) {
@@ -470,6 +736,8 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_kernel(const __grid_constan
           if (leader) {
             const uint32_t blo = blo0 + (uint32_t)(8 * b) * nk16;
             const uint32_t acol = tmem + (uint32_t)(abuf * 32);
+            const uint32_t dcol = dcol0 + (uint32_t)(g * p.NK);
+            const bool first = first_stage && b == 0;
 #pragma unroll
             for (int i = 0; i < 4; ++i)
               mma_ts_lh<KIND>(dcol, acol + (uint32_t)(8 * i), blo + (uint32_t)(2 * i) * nk16, b_hi, id,
@@ -478,8 +746,8 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_kernel(const __grid_constan
           }
           __syncwarp();
           issued_any = true;
-          first = false;
         }
+        first_stage = false;
         if (!ok) break;
         if (leader) tc_commit(bar_at(empty, stage));
       }
@@ -531,8 +799,7 @@ __global__ void wgrad_reduce_kernel(const __grid_constant__ ReducePlan rp) {
 
 size_t wgrad_smem_bytes(const WgradPlan& p, int dt) {
   size_t b = (size_t)p.stages * p.a_stage_bytes;
-  b += ((size_t)p.npl * p.rlen * p.xs * (dt == 0 ? 4 : 2) + 15) & ~size_t(15);
-  b += (size_t)2 * p.KB * sizeof(int);
+  b += ((size_t)p.npl * p.xch * p.xs * (dt == 0 ? 4 : 2) + 15) & ~size_t(15);
   b = (b + 15) & ~size_t(15);
   b += 8 * (2 * p.stages + 2 * kNabuf + 6) + 16;
   return b + 1024;
