@@ -510,6 +510,7 @@ int build_bwd_filter(const Desc& d0, const void* x, const void* dy, void* dw, vo
   p.Cg = d.C >= 32 ? 32 : d.C;
   p.TPU = d.C >= 32 ? 1 : 32 / d.C;
   p.upc = (p.RS + p.TPU - 1) / p.TPU;
+  p.fd_upc = make_fastdiv((uint32_t)p.upc);
   const int ncg = (d.C + p.Cg - 1) / p.Cg;
   p.nunits = ncg * p.upc;
   p.n_mtiles = (p.nunits + 3) / 4;

@@ -133,6 +133,7 @@ struct WgradPlan {
   int tap_plane[kMaxTaps], tap_off[kMaxTaps];  // per filter tap r*S + s
   int max_off;           // largest tap_off
   int Cg, TPU, upc;      // channels per unit, taps per unit, units per channel group
+  FastDiv fd_upc;        // division by upc
   int nunits;            // units of 32 rows in all
   int n_mtiles, n_ntiles, nsplit;
   int G;                 // m-tiles per CTA tile (one TMEM accumulator each; x and dy staged once)

@@ -59,7 +59,7 @@ __device__ __forceinline__ bool unit_row(const WgradPlan& p, int unit, int lane,
   c = 0;
   tap = 0;
   if (unit >= p.nunits) return false;
-  const int cg = unit / p.upc;
+  const int cg = (int)fdiv((uint32_t)unit, p.fd_upc);
   const int tu = unit - cg * p.upc;
   if (p.TPU == 1) {
     c = cg * p.Cg + lane;
@@ -78,104 +78,100 @@ __device__ __forceinline__ int tile_c_lo(const WgradPlan& p, int mt0) { return (
 // Stages tile-relative x positions [q_begin, q_end) of every plane (the tile starts at
 // absolute position L0) into the ring rows of the tile's channels c_lo .. c_lo + xch - 1,
 // in whole slot groups of CHUNK slots (a group may also rewrite neighbouring positions
-// with their own values, which is harmless).  Lanes take consecutive slot groups and the
-// group's 4 warps split the rows, so each copy instruction of a warp moves 512 contiguous
-// bytes.  A group whose pixels are one aligned run (or lie wholly outside the tensor) is
-// one 16-byte cp.async (zero-filled outside); a mixed group is copied element by element.
+// with their own values, which is harmless).  Work item = (plane, slot group, block of 8
+// rows), spread over all producer threads with the slot group fastest.  A group whose
+// pixels are one aligned run (or lie wholly outside the tensor) is one 16-byte cp.async per
+// row (zero-filled outside); a mixed group is loaded element by element, a block of rows
+// at a time (all loads before the stores).
 template <int DT>
 __device__ __forceinline__ void stage_ring(const WgradPlan& p, uint32_t ring, long long L0, int c_lo, int q_begin,
                                            int q_end, int gtid) {
   constexpr int CHUNK = DT == 0 ? 4 : 8;
   constexpr int ESZ = DT == 0 ? 4 : 2;
+  constexpr int RB = 8;  // rows per item
   using E = typename std::conditional<DT == 0, uint32_t, uint16_t>::type;
   const E* xg = static_cast<const E*>(p.x);
   const long long HW = (long long)p.H * p.W;
-  const int lane = gtid & 31, gw = gtid >> 5;
   const int gbeg = (q_begin + p.sigma) / CHUNK;
   const int ng = (q_end + p.sigma + CHUNK - 1) / CHUNK - gbeg;
   const int ngr = p.rlen / CHUNK;
-  const uint32_t rowb = (uint32_t)(p.xs * ESZ);
-  for (int gi = lane; gi < ng + ((32 - ng % 32) % 32); gi += 32) {
-    const bool gv = gi < ng;
+  const uint32_t rstride = (uint32_t)(p.xs * ESZ);
+  const int nrb = (p.xch + RB - 1) / RB;
+  const int total = p.npl * ng * nrb;
+  for (int it = gtid; it < total; it += 128) {
+    const int gi = it % ng;
+    const int rest = it / ng;
+    const int rb = rest % nrb;
+    const int pl = rest / nrb;
     const int g = gbeg + gi;
     const long long La = L0 + (long long)g * CHUNK - p.sigma;  // absolute position of the first slot
-    const uint32_t sdst = ring + (uint32_t)((g % ngr) * CHUNK * ESZ);
-    // the group's CHUNK positions: image n, linear row e, column f of the first
-    uint32_t n = 0;
-    int e = 0, f = 0;
-    bool one_row = false;
-    if (gv && La >= 0 && La + CHUNK <= p.Mtot) {
-      n = fdiv((uint32_t)La, p.fd_img);
+    const uint32_t sdst = ring + (uint32_t)((g % ngr) * CHUNK * ESZ) + (uint32_t)(pl * p.xch) * rstride;
+    const int cr0 = rb * RB;
+    const int cr1 = cr0 + RB < p.xch ? cr0 + RB : p.xch;
+    // classify the group: 1 = one aligned valid run, 2 = all outside, 3 = mixed
+    int mode = 3;
+    long long soff = 0;
+    if (La >= 0 && La + CHUNK <= p.Mtot) {
+      const uint32_t n = fdiv((uint32_t)La, p.fd_img);
       const uint32_t rem = (uint32_t)La - n * p.fd_img.d;
-      e = (int)fdiv(rem, p.fd_WL);
-      f = (int)rem - e * p.WL;
-      one_row = f + CHUNK <= p.WL;
-    }
-    for (int pl = 0; pl < p.npl; ++pl) {
-      // 0: nothing to do, 1: 16-byte copy from src (valid run), 2: zero group, 3: mixed
-      int mode = 0;
-      long long soff = 0;
-      if (gv) {
-        mode = 3;
-        if (one_row) {
-          const int h = e * p.pl_step_h + p.pl_off_h[pl];
-          const int w = f * p.pl_step_w + p.pl_off_w[pl];
-          const int wl = (CHUNK - 1) * p.pl_step_w + w;  // last pixel's column
-          if (h < 0 || h >= p.H || wl < 0 || w >= p.W) {
-            mode = 2;
-          } else if (p.vec_x && (w & (CHUNK - 1)) == 0 && w >= 0 && wl < p.W) {
-            mode = 1;
-            soff = (long long)n * p.C * HW + (long long)h * p.W + w;
-          }
+      const int e = (int)fdiv(rem, p.fd_WL);
+      const int f = (int)rem - e * p.WL;
+      if (f + CHUNK <= p.WL) {
+        const int h = e * p.pl_step_h + p.pl_off_h[pl];
+        const int w = f * p.pl_step_w + p.pl_off_w[pl];
+        const int wl = (CHUNK - 1) * p.pl_step_w + w;  // last pixel's column
+        if (h < 0 || h >= p.H || wl < 0 || w >= p.W) {
+          mode = 2;
+        } else if (p.vec_x && (w & (CHUNK - 1)) == 0 && w >= 0 && wl < p.W) {
+          mode = 1;
+          soff = (long long)n * p.C * HW + (long long)h * p.W + w;
         }
       }
-      if (mode == 1 || mode == 2) {
-        for (int cr = gw; cr < p.xch; cr += 4) {
-          const int c = c_lo + cr;
-          const bool v = mode == 1 && c < p.C;
-          cp_async_16(sdst + (uint32_t)(pl * p.xch + cr) * rowb, v ? (const void*)(xg + soff + (long long)c * HW) : p.x,
-                      v ? 16 : 0);
-        }
-      } else if (mode == 3) {
-        // element offsets (channel 0) of the group's positions, -1 = zero
-        int offs[CHUNK];
+    }
+    if (mode != 3) {
+      for (int cr = cr0; cr < cr1; ++cr) {
+        const int c = c_lo + cr;
+        const bool v = mode == 1 && c < p.C;
+        cp_async_16(sdst + (uint32_t)cr * rstride, v ? (const void*)(xg + soff + (long long)c * HW) : p.x, v ? 16 : 0);
+      }
+      continue;
+    }
+    // element offsets (channel 0) of the group's positions, -1 = zero
+    int offs[CHUNK];
+#pragma unroll
+    for (int j = 0; j < CHUNK; ++j) {
+      offs[j] = -1;
+      const long long L = La + j;
+      if (L < 0 || L >= p.Mtot) continue;
+      const uint32_t nn = fdiv((uint32_t)L, p.fd_img);
+      const uint32_t rem = (uint32_t)L - nn * p.fd_img.d;
+      const int ee = (int)fdiv(rem, p.fd_WL);
+      const int ff = (int)rem - ee * p.WL;
+      const int h = ee * p.pl_step_h + p.pl_off_h[pl];
+      const int w = ff * p.pl_step_w + p.pl_off_w[pl];
+      if (h >= 0 && h < p.H && w >= 0 && w < p.W) offs[j] = (int)((long long)nn * p.C * HW + (long long)h * p.W + w);
+    }
+    constexpr int RL = DT == 0 ? 4 : 2;  // rows per load batch
+    for (int c0r = cr0; c0r < cr1; c0r += RL) {
+      uint32_t wv[RL][4];
+#pragma unroll
+      for (int r = 0; r < RL; ++r) {
+        wv[r][0] = wv[r][1] = wv[r][2] = wv[r][3] = 0u;
+        const int c = c_lo + c0r + r;
+        if (c0r + r >= cr1 || c >= p.C) continue;
+        const E* sc = xg + (long long)c * HW;
 #pragma unroll
         for (int j = 0; j < CHUNK; ++j) {
-          offs[j] = -1;
-          const long long L = La + j;
-          if (L < 0 || L >= p.Mtot) continue;
-          const uint32_t nn = fdiv((uint32_t)L, p.fd_img);
-          const uint32_t rem = (uint32_t)L - nn * p.fd_img.d;
-          const int ee = (int)fdiv(rem, p.fd_WL);
-          const int ff = (int)rem - ee * p.WL;
-          const int h = ee * p.pl_step_h + p.pl_off_h[pl];
-          const int w = ff * p.pl_step_w + p.pl_off_w[pl];
-          if (h >= 0 && h < p.H && w >= 0 && w < p.W) offs[j] = (int)((long long)nn * p.C * HW + (long long)h * p.W + w);
-        }
-        // rows in batches of RB: all loads of a batch precede its stores
-        constexpr int RB = DT == 0 ? 4 : 2;
-        for (int cr0 = gw; cr0 < p.xch; cr0 += 4 * RB) {
-          uint32_t wv[RB][4];
-#pragma unroll
-          for (int r = 0; r < RB; ++r) {
-            wv[r][0] = wv[r][1] = wv[r][2] = wv[r][3] = 0u;
-            const int c = c_lo + cr0 + 4 * r;
-            if (cr0 + 4 * r >= p.xch || c >= p.C) continue;
-            const E* sc = xg + (long long)c * HW;
-#pragma unroll
-            for (int j = 0; j < CHUNK; ++j) {
-              if (offs[j] < 0) continue;
-              const uint32_t x = (uint32_t)__ldg(sc + offs[j]);
-              if constexpr (DT == 0) wv[r][j] = x;
-              else wv[r][j >> 1] |= x << (16 * (j & 1));
-            }
-          }
-#pragma unroll
-          for (int r = 0; r < RB; ++r)
-            if (cr0 + 4 * r < p.xch)
-              st_shared_v4(sdst + (uint32_t)(pl * p.xch + cr0 + 4 * r) * rowb, wv[r][0], wv[r][1], wv[r][2], wv[r][3]);
+          if (offs[j] < 0) continue;
+          const uint32_t x = (uint32_t)__ldg(sc + offs[j]);
+          if constexpr (DT == 0) wv[r][j] = x;
+          else wv[r][j >> 1] |= x << (16 * (j & 1));
         }
       }
+#pragma unroll
+      for (int r = 0; r < RL; ++r)
+        if (c0r + r < cr1)
+          st_shared_v4(sdst + (uint32_t)(c0r + r) * rstride, wv[r][0], wv[r][1], wv[r][2], wv[r][3]);
     }
   }
 }
@@ -560,10 +556,13 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_kernel(const __grid_constan
           ok = false;
           break;
         }
-        for (int bg = 0; bg < nbuf * wt.gcount && ok; ++bg, ++kglob) {
+        for (int bg = 0, b = 0, g = 0; bg < nbuf * wt.gcount && ok; ++bg, ++kglob) {
+          // b: buffer of positions, g: m-tile within the group (g fastest)
+          if (bg > 0 && ++g == wt.gcount) {
+            g = 0;
+            ++b;
+          }
           if ((int)(kglob & 1) != set) continue;
-          const int b = bg / wt.gcount;  // buffer of positions
-          const int g = bg - b * wt.gcount;  // m-tile within the group
           const int abuf = (int)(kglob % kNabuf);
           const uint32_t use = (uint32_t)((kglob / kNabuf) & 1);
           if (!mbar_wait(bar_at(aempty, abuf), use ^ 1u, abort_flag, &g_wgrad_err)) {
@@ -723,9 +722,11 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_kernel(const __grid_constan
         tc_fence_after();
         // B = dy tile, K-major [chunk][k row][16 B]; buffer b, MMA i uses chunks 8b+2i, 8b+2i+1.
         const uint32_t blo0 = (uint32_t)sdesc(a0 + (uint32_t)stage * p.a_stage_bytes, (uint32_t)p.NK * 16u, 0u);
-        for (int bg = 0; bg < nbuf * wt.gcount; ++bg, ++kglob) {
-          const int b = bg / wt.gcount;
-          const int g = bg - b * wt.gcount;
+        for (int bg = 0, b = 0, g = 0; bg < nbuf * wt.gcount; ++bg, ++kglob) {
+          if (bg > 0 && ++g == wt.gcount) {
+            g = 0;
+            ++b;
+          }
           const int abuf = (int)(kglob % kNabuf);
           const uint32_t use = (uint32_t)((kglob / kNabuf) & 1);
           if (!mbar_wait(bar_at(afull, abuf), use, abort_flag, &g_wgrad_err)) {

@@ -83,14 +83,15 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
 }
 
 // Wait for the phase with the given parity to complete, for at most kWaitLimitNs.
-// A short spin on the non-blocking test comes first (a phase that is already complete,
-// or completes within a few hundred cycles, is seen without suspending the thread).
+// A few non-blocking tests come first (a phase that is already complete is seen without
+// suspending the thread); then the thread suspends in try_wait, leaving issue slots to
+// the other warps.
 // On expiry the CTA-wide abort flag and the global error word are set and false is
 // returned; every role then leaves its loop, so the kernel always terminates.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                           int* err_word) {
 #pragma unroll 1
-  for (int i = 0; i < 32; ++i)
+  for (int i = 0; i < 4; ++i)
     if (mbar_test_wait(bar, parity)) return true;
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
