@@ -774,27 +774,43 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_kernel(const __grid_constan
   }
 }
 
-// Sum the split partials in split order and write dw (KCRS).  One thread per
-// (tap, c, k) with k fastest, so partial reads are coalesced.
+// Sum the split partials and write dw (KCRS), in a fixed order (deterministic).  A block
+// of 8 warps takes 32 consecutive outputs (tap, c, k) with k fastest, so every partial
+// read of a warp is one 128-byte line; warp w adds splits w, w + 8, w + 16, ... in order,
+// and the 8 warp sums are then added in warp order.
+constexpr int kReduceWarps = 8;
 template <int DT>
-__global__ void wgrad_reduce_kernel(const __grid_constant__ ReducePlan rp) {
+__global__ void __launch_bounds__(32 * kReduceWarps) wgrad_reduce_kernel(const __grid_constant__ ReducePlan rp) {
+  __shared__ float part[kReduceWarps][32];
   const int RS = rp.R * rp.S;
   const long long total = (long long)RS * rp.C * rp.K;
   const long long split_stride = (long long)RS * rp.c_pad * rp.k_pad;
-  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
-       i += (long long)gridDim.x * blockDim.x) {
-    const int k = (int)(i % rp.K);
-    long long r = i / rp.K;
-    const int c = (int)(r % rp.C);
-    const int tap = (int)(r / rp.C);
-    const float* src = rp.partial + ((long long)tap * rp.c_pad + c) * rp.k_pad + k;
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  for (long long o0 = (long long)blockIdx.x * 32; o0 < total; o0 += (long long)gridDim.x * 32) {
+    const long long i = o0 + lane;
+    int k = 0, c = 0, tap = 0;
     float acc = 0.f;
-    for (int s = 0; s < rp.nsplit; ++s) acc += src[s * split_stride];
-    const long long o = ((long long)k * rp.C + c) * RS + tap;
-    if constexpr (DT == 0)
-      static_cast<float*>(rp.dw)[o] = acc;
-    else
-      static_cast<__nv_bfloat16*>(rp.dw)[o] = __float2bfloat16_rn(acc);
+    if (i < total) {
+      k = (int)(i % rp.K);
+      const long long r = i / rp.K;
+      c = (int)(r % rp.C);
+      tap = (int)(r / rp.C);
+      const float* src = rp.partial + ((long long)tap * rp.c_pad + c) * rp.k_pad + k;
+      for (int sp = w; sp < rp.nsplit; sp += kReduceWarps) acc += __ldg(src + sp * split_stride);
+    }
+    part[w][lane] = acc;
+    __syncthreads();
+    if (w == 0 && i < total) {
+      float sum = part[0][lane];
+#pragma unroll
+      for (int j = 1; j < kReduceWarps; ++j) sum += part[j][lane];
+      const long long o = ((long long)k * rp.C + c) * RS + tap;
+      if constexpr (DT == 0)
+        static_cast<float*>(rp.dw)[o] = sum;
+      else
+        static_cast<__nv_bfloat16*>(rp.dw)[o] = __float2bfloat16_rn(sum);
+    }
+    __syncthreads();
   }
 }
 
@@ -823,14 +839,14 @@ cudaError_t launch_wgrad(const WgradPlan& p, int dt, int grid, cudaStream_t st) 
 
 cudaError_t launch_wgrad_reduce(const ReducePlan& rp, int dt, int num_sms, cudaStream_t st) {
   const long long total = (long long)rp.R * rp.S * rp.C * rp.K;
-  long long blocks = (total + 255) / 256;
-  const long long cap = (long long)num_sms * 8;
+  long long blocks = (total + 31) / 32;
+  const long long cap = (long long)num_sms * 16;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
   if (dt == 0)
-    wgrad_reduce_kernel<0><<<(int)blocks, 256, 0, st>>>(rp);
+    wgrad_reduce_kernel<0><<<(int)blocks, 32 * kReduceWarps, 0, st>>>(rp);
   else
-    wgrad_reduce_kernel<1><<<(int)blocks, 256, 0, st>>>(rp);
+    wgrad_reduce_kernel<1><<<(int)blocks, 32 * kReduceWarps, 0, st>>>(rp);
   return cudaGetLastError();
 }
 
