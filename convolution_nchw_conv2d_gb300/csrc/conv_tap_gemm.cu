@@ -184,6 +184,7 @@ __global__ void __launch_bounds__(kThreads, 1) tap_gemm_kernel(const __grid_cons
     // =============================================================== producers
     const int grp = warp >> 2;           // producer group 0 or 1
     const int gtid = tid & (kProdThreads - 1);
+    if (gtid == 0) griddep_wait();       // the packed filter is written by the previous grid
     long long counter = 0;               // global stage counter (both groups count all stages)
     bool ok = true;
     // After an abort a group keeps walking the tiles (skipping all work) to the final
@@ -410,6 +411,7 @@ __global__ void pack_filter_kernel(const __grid_constant__ PackPlan pp) {
   constexpr int ESZ = DT == 0 ? 4 : 2;
   constexpr int CHUNK = 16 / ESZ;
   const int NCH = pp.CB / CHUNK;
+  griddep_launch_dependents();  // the GEMM may start; it waits for this grid before reading wpack
   const long long total = (long long)pp.n_ntiles * pp.nkb * pp.ntaps_total * NCH * pp.NT;
   for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < total;
        idx += (long long)gridDim.x * blockDim.x) {
@@ -455,19 +457,31 @@ size_t tap_gemm_smem_bytes(const TapPlan& p) {
   return b + 1024;  // alignment slack for the dynamic base
 }
 
+// Launched with programmatic stream serialization: the kernel's set-up overlaps the filter
+// pack that precedes it in the stream (the producers wait for it before the first copy).
 cudaError_t launch_tap_gemm(const TapPlan& p, int dt, int grid, cudaStream_t st) {
   const size_t smem = tap_gemm_smem_bytes(p);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   cudaError_t e;
   if (dt == 0) {
     e = cudaFuncSetAttribute(tap_gemm_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    tap_gemm_kernel<0><<<grid, kThreads, smem, st>>>(p);
+    e = cudaLaunchKernelEx(&cfg, tap_gemm_kernel<0>, p);
   } else {
     e = cudaFuncSetAttribute(tap_gemm_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    tap_gemm_kernel<1><<<grid, kThreads, smem, st>>>(p);
+    e = cudaLaunchKernelEx(&cfg, tap_gemm_kernel<1>, p);
   }
-  return cudaGetLastError();
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t launch_pack_filter(const PackPlan& pp, int dt, cudaStream_t st) {

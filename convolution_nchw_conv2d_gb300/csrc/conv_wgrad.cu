@@ -289,6 +289,7 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_kernel(const __grid_constan
   const int S = p.stages;
   const int KB = p.KB;
   const int nbuf = KB / BUFP;  // A buffers per stage
+  griddep_launch_dependents();  // the reduce may be scheduled now; it waits for this grid
   const int rlen = p.rlen;
 
   // 1024-byte aligned base (the size includes the slack): tensor-copy destinations
@@ -786,6 +787,7 @@ __global__ void __launch_bounds__(32 * kReduceWarps) wgrad_reduce_kernel(const _
   const long long total = (long long)RS * rp.C * rp.K;
   const long long split_stride = (long long)RS * rp.c_pad * rp.k_pad;
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  griddep_wait();  // the partials are written by the previous grid
   for (long long o0 = (long long)blockIdx.x * 32; o0 < total; o0 += (long long)gridDim.x * 32) {
     const long long i = o0 + lane;
     int k = 0, c = 0, tap = 0;
@@ -843,11 +845,20 @@ cudaError_t launch_wgrad_reduce(const ReducePlan& rp, int dt, int num_sms, cudaS
   const long long cap = (long long)num_sms * 16;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
-  if (dt == 0)
-    wgrad_reduce_kernel<0><<<(int)blocks, 32 * kReduceWarps, 0, st>>>(rp);
-  else
-    wgrad_reduce_kernel<1><<<(int)blocks, 32 * kReduceWarps, 0, st>>>(rp);
-  return cudaGetLastError();
+  // programmatic stream serialization: launched while the GEMM runs, waits for it
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)blocks);
+  cfg.blockDim = dim3(32 * kReduceWarps);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = dt == 0 ? cudaLaunchKernelEx(&cfg, wgrad_reduce_kernel<0>, rp)
+                                : cudaLaunchKernelEx(&cfg, wgrad_reduce_kernel<1>, rp);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 int wgrad_take_error() {

@@ -133,6 +133,15 @@ __device__ __forceinline__ bool elect_one() {
   return r != 0;
 }
 
+// Programmatic dependent launch: a grid launched with programmatic stream serialization
+// may start while the previous grid in the stream is still running; it must execute
+// griddep_wait() before touching anything that grid writes.  The previous grid calls
+// griddep_launch_dependents() to let it start early.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Named barrier over a subset of warps (ids 1..15; 0 is __syncthreads).
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
