@@ -431,6 +431,22 @@ EncodeTiledFn encode_tiled_fn() {
   return fn;
 }
 
+// x (N, C, H, W) as the 4-D tensor (w = W, h = H, c = C, n = N) with a box of one image row
+// segment of WL pixels by 32 channels.  False if it cannot be encoded.
+bool encode_x_map(CUtensorMap* m, const void* x, int dt, int N, int C, int H, int W, int WL) {
+  EncodeTiledFn fn = encode_tiled_fn();
+  if (!fn) return false;
+  const uint64_t esz = dt == 0 ? 4 : 2;
+  const cuuint64_t dims[4] = {(cuuint64_t)W, (cuuint64_t)H, (cuuint64_t)C, (cuuint64_t)N};
+  const cuuint64_t strides[3] = {(cuuint64_t)W * esz, (cuuint64_t)H * W * esz, (cuuint64_t)C * H * W * esz};
+  const cuuint32_t box[4] = {(cuuint32_t)WL, 1u, 32u, 1u};
+  const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+  const CUresult r = fn(m, dt == 0 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
+                        const_cast<void*>(x), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // dy (N, K, P, Q) as the 4-D tensor (w = Q, k = K, e = P, n = N) with a box of one
 // 16-byte chunk of positions by NK output channels.  False if it cannot be encoded.
 bool encode_dy_map(CUtensorMap* m, const void* dy, int dt, int N, int K, int P, int Q, int NK) {
@@ -455,8 +471,8 @@ struct WgradBuild {
   int grid;
 };
 
-int build_bwd_filter(const Desc& d0, const void* x, const void* dy, void* dw, void* ws, const DevInfo& di,
-                     WgradBuild& b) {
+int build_bwd_filter_impl(const Desc& d0, const void* x, const void* dy, void* dw, void* ws, const DevInfo& di,
+                          WgradBuild& b, bool allow_tma) {
   const Desc d = flatten_pointwise(d0);
   WgradPlan& p = b.p;
   std::memset(&p, 0, sizeof(p));
@@ -478,9 +494,23 @@ int build_bwd_filter(const Desc& d0, const void* x, const void* dy, void* dw, vo
   const int ESZ = d.dt == 0 ? 4 : 2;
   const int BUFP = d.dt == 0 ? 32 : 64;  // positions per 32-column TMEM buffer
   const int mh = (d.R - 1) / d.sh, mw = (d.S - 1) / d.sw;
-  // Linear row width: a multiple of the chunk (16-byte dy copies) when that wastes at
-  // most 1/8 of it.
-  {
+  // Copy-engine staging: unit column stride, rows and planes of whole 16-byte chunks, aligned
+  // tensors.  Its linear row width WL covers the output columns plus the filter overhang and
+  // every pixel of an image row shifted by delta (the row copy starts at -align(pad_w)),
+  // and is CHUNK mod 2 CHUNK; at most 256 (one copy box).
+  bool tma = allow_tma && d.sw == 1 && d.W % CHUNK == 0 && d.Q % CHUNK == 0 && ((uintptr_t)x & 15) == 0 &&
+             ((uintptr_t)dy & 15) == 0 && encode_tiled_fn() != nullptr;
+  if (tma) {
+    p.delta = round_up(d.pw, CHUNK) - d.pw;
+    int wl = std::max(d.Q + mw, d.W + round_up(d.pw, CHUNK));
+    while (wl % (2 * CHUNK) != CHUNK) ++wl;
+    p.WL = wl;
+    tma = wl <= 256 && 8 * (wl - (d.Q + mw)) <= 2 * wl;  // at most a quarter of the work wasted
+  }
+  if (!tma) {
+    // Linear row width: a multiple of the chunk (16-byte dy copies) when that wastes at
+    // most 1/8 of it.
+    p.delta = 0;
     const int wl = round_up(d.Q + mw, CHUNK);
     p.WL = (8 * (wl - (d.Q + mw)) <= wl) ? wl : d.Q + mw;
   }
@@ -503,6 +533,7 @@ int build_bwd_filter(const Desc& d0, const void* x, const void* dy, void* dw, vo
       const int t = r * d.S + s;
       p.tap_plane[t] = (r % d.sh) * d.sw + (s % d.sw);
       p.tap_off[t] = (r / d.sh) * p.WL + s / d.sw;
+      p.tap_rc[t] = ((r / d.sh) << 16) | (s / d.sw);
       p.max_off = std::max(p.max_off, p.tap_off[t]);
     }
   p.vec_dy = d.Q % CHUNK == 0 && p.WL % CHUNK == 0 && ((uintptr_t)dy & 15) == 0;
@@ -518,7 +549,7 @@ int build_bwd_filter(const Desc& d0, const void* x, const void* dy, void* dw, vo
   p.n_ntiles = (d.K + p.NK - 1) / p.NK;
   // m-tiles per CTA tile: as many accumulators as TMEM holds next to the 4 A buffers, so
   // x and dy are staged once for all of them; two accumulator sets when they fit.
-  p.G = std::max(1, std::min(p.n_mtiles, (512 - 128) / p.NK));
+  p.G = std::max(1, std::min(std::min(p.n_mtiles, (512 - 128) / p.NK), 8));
   p.n_mgroups = (p.n_mtiles + p.G - 1) / p.G;
   p.G = (p.n_mtiles + p.n_mgroups - 1) / p.n_mgroups;  // balance the groups
   p.accb = (128 + 2 * p.G * p.NK <= 512) ? 2 : 1;
@@ -534,8 +565,8 @@ int build_bwd_filter(const Desc& d0, const void* x, const void* dy, void* dw, vo
   // sigma puts the start of every slot group on a chunk-aligned pixel.
   p.vec_x = d.sw == 1 && p.WL % CHUNK == 0 && d.W % CHUNK == 0 && ((uintptr_t)x & 15) == 0;
   p.sigma = p.vec_x ? (CHUNK - d.pw % CHUNK) % CHUNK : 0;
-  // Copy-engine staging (unit column stride, chunk-aligned rows and tensors).
-  p.use_tma = p.vec_x && p.vec_dy && encode_dy_map(&p.tm_dy, dy, d.dt, d.N, d.K, d.P, d.Q, p.NK) ? 1 : 0;
+  p.use_tma = tma ? 1 : 0;
+  p.xr = round_up(p.xch, 32);
   // Pipeline: the most positions in flight (stages x KB) that fit, then the larger KB.
   bool fitted = false;
   long long best = -1;
@@ -551,6 +582,8 @@ int build_bwd_filter(const Desc& d0, const void* x, const void* dy, void* dw, vo
       q.rlen = round_up(S * KB + p.max_off + 2 * CHUNK, 32);
       q.xs = q.rlen;
       while ((q.xs * ESZ) % 128 != 16) q.xs += CHUNK;
+      // row ring: S stages plus the halo, plus a row at each end
+      q.NR = (S * KB + p.max_off + p.delta + p.WL - 1) / p.WL + 2;
       q.a_stage_bytes = KB * p.NK * ESZ;
       if (wgrad_smem_bytes(q, d.dt) > di.smem_optin) continue;
       const long long score = (long long)S * KB * 4 + KB / 32;
@@ -565,6 +598,13 @@ int build_bwd_filter(const Desc& d0, const void* x, const void* dy, void* dw, vo
   p = bestp;
   p.fd_EL = make_fastdiv((uint32_t)p.EL);
   p.fd_rlen = make_fastdiv((uint32_t)p.rlen);
+  p.fd_NR = make_fastdiv((uint32_t)p.NR);
+  if (p.use_tma && !(encode_dy_map(&p.tm_dy, dy, d.dt, d.N, d.K, d.P, d.Q, p.NK) &&
+                     encode_x_map(&p.tm_x, x, d.dt, d.N, d.C, d.H, d.W, p.WL))) {
+    // The copy-engine path cannot be encoded: stage with cp.async instead (same linear space;
+    // its ring must then fit too).
+    return CONV2D_ERR_UNSUPPORTED;
+  }
   // Split the positions so that the tiles fill the SMs with the shortest makespan
   // (tiles per CTA x positions per tile), preferring fewer splits.
   const long long base = (long long)p.n_mgroups * p.n_ntiles;
@@ -600,6 +640,15 @@ int build_bwd_filter(const Desc& d0, const void* x, const void* dy, void* dw, vo
   rp.c_pad = d.C;
   b.grid = (int)std::min<long long>(p.total_tiles, di.sms);
   return CONV2D_OK;
+}
+
+// Backward-filter plan: copy-engine staging when the shape allows it and its row ring fits,
+// else the cp.async staging.
+int build_bwd_filter(const Desc& d, const void* x, const void* dy, void* dw, void* ws, const DevInfo& di,
+                     WgradBuild& b) {
+  const int rc = build_bwd_filter_impl(d, x, dy, dw, ws, di, b, true);
+  if (rc == CONV2D_OK || rc != CONV2D_ERR_UNSUPPORTED) return rc;
+  return build_bwd_filter_impl(d, x, dy, dw, ws, di, b, false);
 }
 
 int check_ptrs(const void* a, const void* b, const void* c, int dt) {

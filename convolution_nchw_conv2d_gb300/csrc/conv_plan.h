@@ -117,7 +117,18 @@ struct WgradPlan {
   // dy as a 4-D tensor (w, k, row e, image n) for copy-engine loads of one 16-byte chunk of
   // positions for NK output channels ([k][CHUNK] in shared memory); valid when use_tma.
   CUtensorMap tm_dy;
-  int use_tma;           // copy-engine staging: dy by tensor copies, x rows by bulk copies
+  // x as a 4-D tensor (w, h, c, n) with a box of one image row (WL pixels from column
+  // -align(pad_w)) by 32 channels; valid when use_tma.
+  CUtensorMap tm_x;
+  int use_tma;           // copy-engine staging (unit column stride, aligned tensors): dy by
+                         // tensor copies, x by tensor copies of whole rows into a row ring
+  // Row ring (use_tma): [NR row slots][plane][xr channel rows][WL].  Position L lives at
+  // slot s = L + delta: row slot (s / WL) mod NR, column s mod WL; the copy of linear row R
+  // holds pixels -align(pad_w) .. +WL-1 of its image row, so columns past the image and
+  // before it read as zeros.  WL = CHUNK mod 2 CHUNK keeps 16-byte reads of 8 consecutive
+  // channel rows in distinct banks.
+  int NR, xr, delta;
+  FastDiv fd_NR;
   const void* x;         // NCHW
   const void* dy;        // N K P Q
   float* partial;        // [split][R*S][C][K] fp32
@@ -131,6 +142,7 @@ struct WgradPlan {
   int pl_step_h, pl_step_w;
   int pl_off_h[kMaxPlanes], pl_off_w[kMaxPlanes];
   int tap_plane[kMaxTaps], tap_off[kMaxTaps];  // per filter tap r*S + s
+  int tap_rc[kMaxTaps];  // tap_off as (linear rows << 16) | columns
   int max_off;           // largest tap_off
   int Cg, TPU, upc;      // channels per unit, taps per unit, units per channel group
   FastDiv fd_upc;        // division by upc

@@ -260,6 +260,12 @@ __device__ __forceinline__ void split_range(const WgradPlan& p, int sp, long lon
 }
 }  // namespace
 
+// Bytes of the x ring.
+__host__ __device__ inline size_t wgrad_ring_bytes(const WgradPlan& p, int dt) {
+  const size_t esz = dt == 0 ? 4 : 2;
+  return p.use_tma ? (size_t)p.NR * p.npl * p.xr * p.WL * esz : (size_t)p.npl * p.xch * p.xs * esz;
+}
+
 // tcgen05.st of w[K .. K + 31] to 32 TMEM columns (K fixed, so w stays in registers).
 template <int K>
 __device__ __forceinline__ void tmem_st32_at(uint32_t taddr, const uint32_t (&w)[36]) {
@@ -296,8 +302,12 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_kernel(const __grid_constan
   uint8_t* ptr = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t a0 = smem_u32(ptr);  // dy tiles
   ptr += (size_t)S * p.a_stage_bytes;
-  const uint32_t ring = smem_u32(ptr);  // x ring, [plane][channel][xs]
-  ptr += ((size_t)p.npl * p.xch * p.xs * ESZ + 15) & ~size_t(15);
+  const uint32_t ring = smem_u32(ptr);  // x ring: [plane][channel][xs], or the row ring (use_tma)
+  ptr += (wgrad_ring_bytes(p, DT) + 15) & ~size_t(15);
+  // per builder warp, m-tile and lane: {ring offset of the lane's row (bit 31: padding row),
+  // tap offset} -- set once per tile
+  uint2* btab = reinterpret_cast<uint2*>(ptr);
+  ptr += (size_t)8 * p.G * 32 * sizeof(uint2);
   ptr = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(ptr) + 15) & ~uintptr_t(15));
   const uint32_t full = smem_u32(ptr);
   const uint32_t empty = full + 8u * S;
@@ -347,8 +357,6 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_kernel(const __grid_constan
       // thread adds its own copies' bytes to the stage's full barrier before issuing them
       // and then arrives without waiting, so the producers run ahead by up to S stages.
       const int gtid = tid;
-      using E = typename std::conditional<DT == 0, uint32_t, uint16_t>::type;
-      const E* xg = static_cast<const E*>(p.x);
       uint32_t last_phase[4] = {0u, 0u, 0u, 0u};  // 1 + parity of the last fill per slot (thread 0)
       long long counter = 0;
       int ti = 0;
@@ -359,7 +367,7 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_kernel(const __grid_constan
         split_range(p, wt.sp, lbeg, lend);
         const int kbase = wt.nt * p.NK;
         const int c_lo = tile_c_lo(p, wt.mt0);
-        const int nch_x = p.C - c_lo < p.xch ? p.C - c_lo : p.xch;  // ring rows with real channels
+        long long next_row = (lbeg + p.delta) / p.WL;  // first linear row not loaded for this tile
         int s_local = 0;
         for (long long l0 = lbeg; l0 < lend; l0 += KB, ++counter, ++s_local) {
           const int stage = (int)(counter % S);
@@ -378,7 +386,11 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_kernel(const __grid_constan
           const uint32_t fb = bar_at(full, stage);
           const uint32_t a_st = a0 + (uint32_t)stage * p.a_stage_bytes;
           // dy: chunk j = positions l0 + CHUNK*j .. +CHUNK-1 (one linear row: WL % CHUNK == 0)
-          for (int j = gtid; j < KB / CHUNK; j += kProdThreads) {
+          // chunk j is issued by lane j / 4 of warp j % 4 (the issue work is spread over the
+          // four schedulers)
+          for (int jb = 0; jb < KB / CHUNK; jb += kProdThreads) {
+            const int j = jb + 4 * (gtid & 31) + (gtid >> 5);
+            if (j >= KB / CHUNK) continue;
             const long long La = l0 + (long long)CHUNK * j;
             int n = p.N, e = 0, f = 0;  // past the tensor: the copy reads zeros
             if (La < p.Mtot) {
@@ -391,84 +403,29 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_kernel(const __grid_constan
             mbar_expect_tx(fb, (uint32_t)(p.NK * 16));
             tma_load_4d(a_st + (uint32_t)(j * p.NK * 16), &p.tm_dy, f, kbase, e, n, fb);
           }
-          // x: tile-relative positions [q0, q1) (stage 0 also loads the halo); 32-bit
-          // position arithmetic (positions < 2^31), divisions by multiply-high
-          const int q0 = s_local == 0 ? 0 : s_local * KB + p.max_off;
-          const int q1 = (s_local + 1) * KB + p.max_off;
-          const uint32_t Lx0 = (uint32_t)(lbeg + q0);
-          const uint32_t Lx1 = (uint32_t)(lbeg + q1 < p.Mtot ? lbeg + q1 : p.Mtot);
-          const uint32_t lb = (uint32_t)lbeg;
-          // slot of tile-relative position q >= -sigma (a copy widened to an aligned start
-          // may begin a few positions before the tile: those slots are dead at its start)
-          auto slot_of = [&](int q) {
-            const uint32_t v = (uint32_t)(q + p.sigma + rlen);
-            return (int)(v - fdiv(v, p.fd_rlen) * (uint32_t)rlen);
-          };
-          if (Lx0 < Lx1) {
-            const uint32_t row0 = fdiv(Lx0, p.fd_WL);
-            const int nseg = (int)(fdiv(Lx1 - 1u, p.fd_WL) - row0 + 1u);
-            const int items = p.npl * nseg * nch_x;
-            for (int it = gtid; it < items; it += kProdThreads) {
-              const int cr = it % nch_x;
-              const int rest = it / nch_x;
-              const int sg = rest % nseg;
-              const int pl = rest / nseg;
-              const uint32_t R = row0 + (uint32_t)sg;  // linear row (image n, row e)
-              const uint32_t Rs = R * (uint32_t)p.WL;  // its first position
-              const int f0 = (int)((Lx0 > Rs ? Lx0 : Rs) - Rs);
-              const int f1 = (int)((Lx1 < Rs + (uint32_t)p.WL ? Lx1 : Rs + (uint32_t)p.WL) - Rs);
-              const int n = (int)fdiv(R, p.fd_EL);
-              const int e = (int)R - n * p.EL;
-              const int h = e * p.pl_step_h + p.pl_off_h[pl];
-              const int ow = p.pl_off_w[pl];
-              const bool hv = h >= 0 && h < p.H;
-              const int rq = (int)(Rs - lb);             // tile-relative position of the row start
-              int lo = f0 + ow < 0 ? 0 : f0 + ow;        // valid pixel run [lo, hi)
-              int hi = f1 + ow > p.W ? p.W : f1 + ow;
-              const uint32_t rowbase = ring + (uint32_t)((pl * p.xch + cr) * p.xs) * ESZ;
-              if (hv && lo < hi) {
-                const int wa = lo & ~(CHUNK - 1);
-                const int wb = (hi + CHUNK - 1) & ~(CHUNK - 1);  // <= W (W % CHUNK == 0)
-                const int slot = slot_of(rq + (wa - ow));
-                const E* src = xg + (((long long)n * p.C + c_lo + cr) * p.H + h) * p.W + wa;
-                const int len = wb - wa;
-                const int part = rlen - slot < len ? rlen - slot : len;
-                mbar_expect_tx(fb, (uint32_t)(len * ESZ));
-                bulk_g2s(rowbase + (uint32_t)(slot * ESZ), src, (uint32_t)(part * ESZ), fb);
-                if (part < len) bulk_g2s(rowbase, src + part, (uint32_t)((len - part) * ESZ), fb);
-              } else {
-                lo = hi = f1 + ow;  // no valid pixel: every slot of the segment is zero
+          // x: the linear rows holding this stage's slots that are not loaded yet (one tensor
+          // copy per (row, plane, 32 channels)); rows past the tensor read as zeros.
+          {
+            const long long Llast = l0 + KB + p.max_off - 1;
+            const long long rB = (Llast + p.delta) / p.WL;
+            if (next_row <= rB) {
+              const int nrows = (int)(rB - next_row + 1);
+              const int ncg = p.xr / 32;
+              const int items = nrows * p.npl * ncg;
+              for (int it = gtid; it < items; it += kProdThreads) {
+                const int cg = it % ncg;
+                const int rest = it / ncg;
+                const int pl = rest % p.npl;
+                const long long R = next_row + rest / p.npl;
+                const int n = (int)(R / p.EL);
+                const int e = (int)(R - (long long)n * p.EL);
+                const int h = e * p.pl_step_h + p.pl_off_h[pl];
+                const int rs = (int)(R % p.NR);
+                const uint32_t dst = ring + (uint32_t)(((rs * p.npl + pl) * p.xr + 32 * cg) * p.WL * ESZ);
+                mbar_expect_tx(fb, (uint32_t)(32 * p.WL * ESZ));
+                tma_load_4d(dst, &p.tm_x, p.pl_off_w[pl] - p.delta, h, c_lo + 32 * cg, n, fb);
               }
-              // zeros: the segment's positions before and after the valid run
-              auto zero_slots = [&](int fa, int fz) {
-                if (fa >= fz) return;
-                int sl = slot_of(rq + fa);
-                for (int ff = fa; ff < fz; ++ff) {
-                  if constexpr (DT == 0)
-                    asm volatile("st.shared.b32 [%0], %1;" ::"r"(rowbase + (uint32_t)sl * 4u), "r"(0u) : "memory");
-                  else
-                    asm volatile("st.shared.b16 [%0], %1;" ::"r"(rowbase + (uint32_t)sl * 2u), "h"((uint16_t)0) : "memory");
-                  if (++sl == rlen) sl = 0;
-                }
-              };
-              zero_slots(f0, lo - ow);
-              zero_slots(hi - ow, f1);
-            }
-          }
-          // positions past the last image: zeros (they only meet zero dy, but stale
-          // shared memory could hold non-finite values)
-          if ((long long)lbeg + q1 > p.Mtot) {
-            const int za = (int)((Lx0 > (uint32_t)p.Mtot ? (long long)Lx0 : p.Mtot) - lbeg);
-            const int nz = q1 - za;
-            const int rows = p.npl * p.xch;
-            for (int it = gtid; it < nz * rows; it += kProdThreads) {
-              const int row = it / nz;
-              const int q = za + it - row * nz;
-              const uint32_t a = ring + (uint32_t)(row * p.xs + slot_of(q)) * ESZ;
-              if constexpr (DT == 0)
-                asm volatile("st.shared.b32 [%0], %1;" ::"r"(a), "r"(0u) : "memory");
-              else
-                asm volatile("st.shared.b16 [%0], %1;" ::"r"(a), "h"((uint16_t)0) : "memory");
+              next_row = rB + 1;
             }
           }
           mbar_arrive(fb);
@@ -541,6 +498,9 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_kernel(const __grid_constan
     // =============================================================== builders
     const int set = (warp - kBuildWarp0) >> 2;  // builds A buffers with index mod 2 == set
     const int q = warp & 3;                      // TMEM lane quarter
+    uint2* mytab = btab + (size_t)(warp - kBuildWarp0) * p.G * 32;
+    const uint32_t rslot = (uint32_t)(p.npl * p.xr * p.WL);  // row ring: elements per row slot
+    const int ngr = rlen / CHUNK;
     long long counter = 0, kglob = 0;
     bool ok = true;
     for (long long t = blockIdx.x; t < p.total_tiles && ok; t += gridDim.x) {
@@ -548,8 +508,24 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_kernel(const __grid_constan
       long long lbeg, lend;
       split_range(p, wt.sp, lbeg, lend);
       const int c_lo = tile_c_lo(p, wt.mt0);
-      const int ngr = rlen / CHUNK;
-      int sb = 0;  // tile-relative position of the stage's first position, mod rlen
+      // This lane's row of every m-tile of the group: where it lives in the ring and its tap
+      // offset (row ring: linear rows << 16 | columns; slot ring: slots).  With one tap per
+      // unit the tap, hence the offset, is the same in every lane, padding lanes included.
+      for (int g = 0; g < wt.gcount; ++g) {
+        int c, tap;
+        const bool rv = unit_row(p, (wt.mt0 + g) * 4 + q, lane, c, tap);
+        uint32_t off = 0x80000000u, toff = 0u;
+        if (p.use_tma) {
+          if (rv) off = (uint32_t)((p.tap_plane[tap] * p.xr + (c - c_lo)) * p.WL);
+          if (p.TPU == 1 || rv) toff = (uint32_t)p.tap_rc[tap];
+        } else {
+          if (rv) off = (uint32_t)((p.tap_plane[tap] * p.xch + (c - c_lo)) * p.xs * ESZ);
+          toff = (uint32_t)(((p.TPU == 1 || rv) ? p.tap_off[tap] : 0) + p.sigma);
+        }
+        mytab[g * 32 + lane] = make_uint2(off, toff);
+      }
+      __syncwarp();
+      int sb = 0;  // slot ring: tile-relative position of the stage's first position, mod rlen
       for (long long l0 = lbeg; l0 < lend && ok; l0 += KB, ++counter) {
         const int stage = (int)(counter % S);
         const uint32_t fphase = (uint32_t)((counter / S) & 1);
@@ -557,45 +533,84 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_kernel(const __grid_constan
           ok = false;
           break;
         }
+        // row ring: linear row slot and column of the stage's first slot
+        int rs0 = 0, c0 = 0;
+        if (p.use_tma) {
+          const uint32_t sg = (uint32_t)(l0 + p.delta);
+          const uint32_t r0 = fdiv(sg, p.fd_WL);
+          c0 = (int)(sg - r0 * (uint32_t)p.WL);
+          rs0 = (int)(r0 - fdiv(r0, p.fd_NR) * (uint32_t)p.NR);
+        }
+        int bs_rs = rs0, bs_c = c0;  // row ring position of buffer b's first column
         for (int bg = 0, b = 0, g = 0; bg < nbuf * wt.gcount && ok; ++bg, ++kglob) {
           // b: buffer of positions, g: m-tile within the group (g fastest)
           if (bg > 0 && ++g == wt.gcount) {
             g = 0;
             ++b;
+            bs_c += BUFP;
+            while (bs_c >= p.WL) {
+              bs_c -= p.WL;
+              if (++bs_rs == p.NR) bs_rs = 0;
+            }
           }
           if ((int)(kglob & 1) != set) continue;
-          const int abuf = (int)(kglob % kNabuf);
+          const int abuf = (int)(kglob & (kNabuf - 1));
           const uint32_t use = (uint32_t)((kglob / kNabuf) & 1);
           if (!mbar_wait(bar_at(aempty, abuf), use ^ 1u, abort_flag, &g_wgrad_err)) {
             ok = false;
             break;
           }
-          int c, tap;
-          const bool rv = unit_row(p, (wt.mt0 + g) * 4 + q, lane, c, tap);
-          // byte offset of this lane's ring row; slot offset of its tap
-          const uint32_t rowb = rv ? (uint32_t)((p.tap_plane[tap] * p.xch + (c - c_lo)) * p.xs * ESZ) : 0u;
-          // (with one tap per unit the tap, hence the slot, is the same in every lane)
-          const int toff = ((p.TPU == 1 || rv) ? p.tap_off[tap] : 0) + p.sigma;
-          // tcgen05.st is warp-collective: every lane must reach the same instruction, so the
-          // two read paths below branch on p.TPU (uniform), never on lane data.
+          const uint2 ent = mytab[g * 32 + lane];
+          const bool rv = (ent.x & 0x80000000u) == 0u;
+          // ring position of this buffer's first column for this lane's tap
+          int slot = 0, rs = 0, col = 0;
+          if (p.use_tma) {
+            col = bs_c + (int)(ent.y & 0xffffu);
+            rs = bs_rs + (int)(ent.y >> 16);
+            if (col >= p.WL) {
+              col -= p.WL;
+              ++rs;
+            }
+            if (rs >= p.NR) rs -= p.NR;
+          } else {
+            slot = sb + b * BUFP + (int)ent.y;
+            while (slot >= rlen) slot -= rlen;
+          }
           uint32_t w[36];
-          int slot = sb + b * BUFP + toff;
-          if (slot >= rlen) slot -= rlen;
           const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(abuf * 32);
+          // tcgen05.st is warp-collective: every lane must reach the same instruction, so the
+          // read paths below branch on plan values (uniform), never on lane data.
           if (p.TPU == 1) {
-            // One tap per unit: the slot is the same in all lanes.  9 aligned 16-byte reads
-            // cover the 32 columns wherever they start in a group; column j is word k + j
-            // (fp32) or halfwords rho + 2j, rho + 2j + 1 (bf16, shifted down when rho is odd).
-            const int rho = slot & (CHUNK - 1);
+            // One tap per unit: the position is the same in all lanes.  9 aligned 16-byte
+            // reads cover the 32 columns wherever they start in a group; column j is word
+            // k + j (fp32) or halfwords rho + 2j, rho + 2j + 1 (bf16, shifted down when rho is
+            // odd).  Groups never straddle ring rows (rlen and WL are chunk multiples).
+            const int rho = (p.use_tma ? col : slot) & (CHUNK - 1);
             const int k = DT == 0 ? rho : rho >> 1;
             if (rv) {
-              int g = slot / CHUNK;
+              if (p.use_tma) {
+                int cidx = col - rho;
 #pragma unroll
-              for (int i = 0; i < 9; ++i) {
-                asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
-                             : "=r"(w[4 * i]), "=r"(w[4 * i + 1]), "=r"(w[4 * i + 2]), "=r"(w[4 * i + 3])
-                             : "r"(ring + rowb + (uint32_t)(g * 16)));
-                if (++g == ngr) g = 0;
+                for (int i = 0; i < 9; ++i) {
+                  const uint32_t a = ring + ((uint32_t)rs * rslot + ent.x + (uint32_t)cidx) * ESZ;
+                  asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+                               : "=r"(w[4 * i]), "=r"(w[4 * i + 1]), "=r"(w[4 * i + 2]), "=r"(w[4 * i + 3])
+                               : "r"(a));
+                  cidx += CHUNK;
+                  if (cidx == p.WL) {
+                    cidx = 0;
+                    if (++rs == p.NR) rs = 0;
+                  }
+                }
+              } else {
+                int gq = slot / CHUNK;
+#pragma unroll
+                for (int i = 0; i < 9; ++i) {
+                  asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+                               : "=r"(w[4 * i]), "=r"(w[4 * i + 1]), "=r"(w[4 * i + 2]), "=r"(w[4 * i + 3])
+                               : "r"(ring + ent.x + (uint32_t)(gq * 16)));
+                  if (++gq == ngr) gq = 0;
+                }
               }
               if (DT != 0 && (rho & 1)) {
 #pragma unroll
@@ -613,23 +628,29 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_kernel(const __grid_constan
               default: tmem_st32_at<3>(ta, w); break;
             }
           } else {
-            // Several taps per unit: each lane reads its own slots element by element.
+            // Several taps per unit: each lane reads its own positions element by element.
 #pragma unroll
             for (int j = 0; j < 36; ++j) w[j] = 0u;
             if (rv) {
-              const uint32_t rb = ring + rowb;
 #pragma unroll
-              for (int j = 0; j < 32; ++j) {
-                if constexpr (DT == 0) {
-                  asm volatile("ld.shared.b32 %0, [%1];" : "=r"(w[j]) : "r"(rb + (uint32_t)slot * 4u));
-                  if (++slot == rlen) slot = 0;
+              for (int j = 0; j < 32 * PPC; ++j) {
+                uint32_t a;
+                if (p.use_tma) {
+                  a = ring + ((uint32_t)rs * rslot + ent.x + (uint32_t)col) * ESZ;
+                  if (++col == p.WL) {
+                    col = 0;
+                    if (++rs == p.NR) rs = 0;
+                  }
                 } else {
-                  uint16_t lo, hi;
-                  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(lo) : "r"(rb + (uint32_t)slot * 2u));
+                  a = ring + ent.x + (uint32_t)slot * ESZ;
                   if (++slot == rlen) slot = 0;
-                  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(hi) : "r"(rb + (uint32_t)slot * 2u));
-                  if (++slot == rlen) slot = 0;
-                  w[j] = (uint32_t)lo | ((uint32_t)hi << 16);
+                }
+                if constexpr (DT == 0) {
+                  asm volatile("ld.shared.b32 %0, [%1];" : "=r"(w[j]) : "r"(a));
+                } else {
+                  uint16_t h;
+                  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(h) : "r"(a));
+                  w[j >> 1] |= (uint32_t)h << (16 * (j & 1));
                 }
               }
             }
@@ -818,7 +839,8 @@ __global__ void __launch_bounds__(32 * kReduceWarps) wgrad_reduce_kernel(const _
 
 size_t wgrad_smem_bytes(const WgradPlan& p, int dt) {
   size_t b = (size_t)p.stages * p.a_stage_bytes;
-  b += ((size_t)p.npl * p.xch * p.xs * (dt == 0 ? 4 : 2) + 15) & ~size_t(15);
+  b += (wgrad_ring_bytes(p, dt) + 15) & ~size_t(15);
+  b += (size_t)8 * p.G * 32 * sizeof(uint2);
   b = (b + 15) & ~size_t(15);
   b += 8 * (2 * p.stages + 2 * kNabuf + 6) + 16;
   return b + 1024;
