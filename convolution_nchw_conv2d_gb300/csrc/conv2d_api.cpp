@@ -565,7 +565,8 @@ int build_bwd_filter_impl(const Desc& d0, const void* x, const void* dy, void* d
   // sigma puts the start of every slot group on a chunk-aligned pixel.
   p.vec_x = d.sw == 1 && p.WL % CHUNK == 0 && d.W % CHUNK == 0 && ((uintptr_t)x & 15) == 0;
   p.sigma = p.vec_x ? (CHUNK - d.pw % CHUNK) % CHUNK : 0;
-  p.use_tma = tma ? 1 : 0;
+  // x by whole-row tensor copies (1), else by bulk copies of pixel runs when 16-byte aligned (2)
+  p.use_tma = tma ? 1 : (p.vec_x && p.vec_dy ? 2 : 0);
   p.xr = round_up(p.xch, 32);
   // Pipeline: the most positions in flight (stages x KB) that fit, then the larger KB.
   bool fitted = false;
@@ -599,12 +600,13 @@ int build_bwd_filter_impl(const Desc& d0, const void* x, const void* dy, void* d
   p.fd_EL = make_fastdiv((uint32_t)p.EL);
   p.fd_rlen = make_fastdiv((uint32_t)p.rlen);
   p.fd_NR = make_fastdiv((uint32_t)p.NR);
-  if (p.use_tma && !(encode_dy_map(&p.tm_dy, dy, d.dt, d.N, d.K, d.P, d.Q, p.NK) &&
-                     encode_x_map(&p.tm_x, x, d.dt, d.N, d.C, d.H, d.W, p.WL))) {
-    // The copy-engine path cannot be encoded: stage with cp.async instead (same linear space;
-    // its ring must then fit too).
+  if (p.use_tma == 1 && !(encode_dy_map(&p.tm_dy, dy, d.dt, d.N, d.K, d.P, d.Q, p.NK) &&
+                          encode_x_map(&p.tm_x, x, d.dt, d.N, d.C, d.H, d.W, p.WL))) {
+    // The row ring cannot be encoded: plan the slot ring instead (another linear row width).
     return CONV2D_ERR_UNSUPPORTED;
   }
+  if (p.use_tma == 2 && !encode_dy_map(&p.tm_dy, dy, d.dt, d.N, d.K, d.P, d.Q, p.NK))
+    p.use_tma = 0;  // same ring, staged with cp.async
   // Split the positions so that the tiles fill the SMs with the shortest makespan
   // (tiles per CTA x positions per tile), preferring fewer splits.
   const long long base = (long long)p.n_mgroups * p.n_ntiles;

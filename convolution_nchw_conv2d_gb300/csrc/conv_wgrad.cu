@@ -263,7 +263,7 @@ __device__ __forceinline__ void split_range(const WgradPlan& p, int sp, long lon
 // Bytes of the x ring.
 __host__ __device__ inline size_t wgrad_ring_bytes(const WgradPlan& p, int dt) {
   const size_t esz = dt == 0 ? 4 : 2;
-  return p.use_tma ? (size_t)p.NR * p.npl * p.xr * p.WL * esz : (size_t)p.npl * p.xch * p.xs * esz;
+  return p.use_tma == 1 ? (size_t)p.NR * p.npl * p.xr * p.WL * esz : (size_t)p.npl * p.xch * p.xs * esz;
 }
 
 // tcgen05.st of w[K .. K + 31] to 32 TMEM columns (K fixed, so w stays in registers).
@@ -302,7 +302,7 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_kernel(const __grid_constan
   uint8_t* ptr = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t a0 = smem_u32(ptr);  // dy tiles
   ptr += (size_t)S * p.a_stage_bytes;
-  const uint32_t ring = smem_u32(ptr);  // x ring: [plane][channel][xs], or the row ring (use_tma)
+  const uint32_t ring = smem_u32(ptr);  // x: slot ring [plane][channel][xs], or the row ring (use_tma 1)
   ptr += (wgrad_ring_bytes(p, DT) + 15) & ~size_t(15);
   // per builder warp, m-tile and lane: {ring offset of the lane's row (bit 31: padding row),
   // tap offset} -- set once per tile
@@ -352,11 +352,15 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_kernel(const __grid_constan
     // =============================================================== producers
     if (p.use_tma) {
       // Copy-engine staging: per stage, one tensor copy per 16-byte chunk of positions
-      // (all NK output channels) for dy, and one bulk copy per (plane, linear row, channel)
-      // for the valid pixel run of x, plus shared stores of zeros for padding slots.  Every
-      // thread adds its own copies' bytes to the stage's full barrier before issuing them
-      // and then arrives without waiting, so the producers run ahead by up to S stages.
+      // (all NK output channels) for dy; for x either tensor copies of whole image rows
+      // into the row ring (use_tma 1) or, into the slot ring, one bulk copy per (plane,
+      // linear row, channel) for the valid pixel run plus shared stores of zeros for padding
+      // slots (use_tma 2).  Every thread adds its own copies' bytes to the stage's full
+      // barrier before issuing them and then arrives without waiting, so the producers run
+      // ahead by up to S stages.
       const int gtid = tid;
+      using E = typename std::conditional<DT == 0, uint32_t, uint16_t>::type;
+      const E* xg = static_cast<const E*>(p.x);
       uint32_t last_phase[4] = {0u, 0u, 0u, 0u};  // 1 + parity of the last fill per slot (thread 0)
       long long counter = 0;
       int ti = 0;
@@ -367,6 +371,7 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_kernel(const __grid_constan
         split_range(p, wt.sp, lbeg, lend);
         const int kbase = wt.nt * p.NK;
         const int c_lo = tile_c_lo(p, wt.mt0);
+        const int nch_x = p.C - c_lo < p.xch ? p.C - c_lo : p.xch;  // ring rows with real channels
         long long next_row = (lbeg + p.delta) / p.WL;  // first linear row not loaded for this tile
         int s_local = 0;
         for (long long l0 = lbeg; l0 < lend; l0 += KB, ++counter, ++s_local) {
@@ -403,29 +408,112 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_kernel(const __grid_constan
             mbar_expect_tx(fb, (uint32_t)(p.NK * 16));
             tma_load_4d(a_st + (uint32_t)(j * p.NK * 16), &p.tm_dy, f, kbase, e, n, fb);
           }
-          // x: the linear rows holding this stage's slots that are not loaded yet (one tensor
-          // copy per (row, plane, 32 channels)); rows past the tensor read as zeros.
-          {
-            const long long Llast = l0 + KB + p.max_off - 1;
-            const long long rB = (Llast + p.delta) / p.WL;
-            if (next_row <= rB) {
-              const int nrows = (int)(rB - next_row + 1);
-              const int ncg = p.xr / 32;
-              const int items = nrows * p.npl * ncg;
-              for (int it = gtid; it < items; it += kProdThreads) {
-                const int cg = it % ncg;
-                const int rest = it / ncg;
-                const int pl = rest % p.npl;
-                const long long R = next_row + rest / p.npl;
-                const int n = (int)(R / p.EL);
-                const int e = (int)(R - (long long)n * p.EL);
-                const int h = e * p.pl_step_h + p.pl_off_h[pl];
-                const int rs = (int)(R % p.NR);
-                const uint32_t dst = ring + (uint32_t)(((rs * p.npl + pl) * p.xr + 32 * cg) * p.WL * ESZ);
-                mbar_expect_tx(fb, (uint32_t)(32 * p.WL * ESZ));
-                tma_load_4d(dst, &p.tm_x, p.pl_off_w[pl] - p.delta, h, c_lo + 32 * cg, n, fb);
+          if (p.use_tma == 1) {
+            // x: the linear rows holding this stage's slots that are not loaded yet (one tensor
+            // copy per (row, plane, 32 channels)); rows past the tensor read as zeros.
+            {
+              const long long Llast = l0 + KB + p.max_off - 1;
+              const long long rB = (Llast + p.delta) / p.WL;
+              if (next_row <= rB) {
+                const int nrows = (int)(rB - next_row + 1);
+                const int ncg = p.xr / 32;
+                const int items = nrows * p.npl * ncg;
+                for (int it = gtid; it < items; it += kProdThreads) {
+                  const int cg = it % ncg;
+                  const int rest = it / ncg;
+                  const int pl = rest % p.npl;
+                  const long long R = next_row + rest / p.npl;
+                  const int n = (int)(R / p.EL);
+                  const int e = (int)(R - (long long)n * p.EL);
+                  const int h = e * p.pl_step_h + p.pl_off_h[pl];
+                  const int rs = (int)(R % p.NR);
+                  const uint32_t dst = ring + (uint32_t)(((rs * p.npl + pl) * p.xr + 32 * cg) * p.WL * ESZ);
+                  mbar_expect_tx(fb, (uint32_t)(32 * p.WL * ESZ));
+                  tma_load_4d(dst, &p.tm_x, p.pl_off_w[pl] - p.delta, h, c_lo + 32 * cg, n, fb);
+                }
+                next_row = rB + 1;
               }
-              next_row = rB + 1;
+            }
+          } else {
+            // x: tile-relative positions [q0, q1) (stage 0 also loads the halo); 32-bit
+            // position arithmetic (positions < 2^31), divisions by multiply-high
+            const int q0 = s_local == 0 ? 0 : s_local * KB + p.max_off;
+            const int q1 = (s_local + 1) * KB + p.max_off;
+            const uint32_t Lx0 = (uint32_t)(lbeg + q0);
+            const uint32_t Lx1 = (uint32_t)(lbeg + q1 < p.Mtot ? lbeg + q1 : p.Mtot);
+            const uint32_t lb = (uint32_t)lbeg;
+            // slot of tile-relative position q >= -sigma (a copy widened to an aligned start
+            // may begin a few positions before the tile: those slots are dead at its start)
+            auto slot_of = [&](int q) {
+              const uint32_t v = (uint32_t)(q + p.sigma + rlen);
+              return (int)(v - fdiv(v, p.fd_rlen) * (uint32_t)rlen);
+            };
+            if (Lx0 < Lx1) {
+              const uint32_t row0 = fdiv(Lx0, p.fd_WL);
+              const int nseg = (int)(fdiv(Lx1 - 1u, p.fd_WL) - row0 + 1u);
+              const int items = p.npl * nseg * nch_x;
+              for (int it = gtid; it < items; it += kProdThreads) {
+                const int cr = it % nch_x;
+                const int rest = it / nch_x;
+                const int sg = rest % nseg;
+                const int pl = rest / nseg;
+                const uint32_t R = row0 + (uint32_t)sg;  // linear row (image n, row e)
+                const uint32_t Rs = R * (uint32_t)p.WL;  // its first position
+                const int f0 = (int)((Lx0 > Rs ? Lx0 : Rs) - Rs);
+                const int f1 = (int)((Lx1 < Rs + (uint32_t)p.WL ? Lx1 : Rs + (uint32_t)p.WL) - Rs);
+                const int n = (int)fdiv(R, p.fd_EL);
+                const int e = (int)R - n * p.EL;
+                const int h = e * p.pl_step_h + p.pl_off_h[pl];
+                const int ow = p.pl_off_w[pl];
+                const bool hv = h >= 0 && h < p.H;
+                const int rq = (int)(Rs - lb);             // tile-relative position of the row start
+                int lo = f0 + ow < 0 ? 0 : f0 + ow;        // valid pixel run [lo, hi)
+                int hi = f1 + ow > p.W ? p.W : f1 + ow;
+                const uint32_t rowbase = ring + (uint32_t)((pl * p.xch + cr) * p.xs) * ESZ;
+                if (hv && lo < hi) {
+                  const int wa = lo & ~(CHUNK - 1);
+                  const int wb = (hi + CHUNK - 1) & ~(CHUNK - 1);  // <= W (W % CHUNK == 0)
+                  const int slot = slot_of(rq + (wa - ow));
+                  const E* src = xg + (((long long)n * p.C + c_lo + cr) * p.H + h) * p.W + wa;
+                  const int len = wb - wa;
+                  const int part = rlen - slot < len ? rlen - slot : len;
+                  mbar_expect_tx(fb, (uint32_t)(len * ESZ));
+                  bulk_g2s(rowbase + (uint32_t)(slot * ESZ), src, (uint32_t)(part * ESZ), fb);
+                  if (part < len) bulk_g2s(rowbase, src + part, (uint32_t)((len - part) * ESZ), fb);
+                } else {
+                  lo = hi = f1 + ow;  // no valid pixel: every slot of the segment is zero
+                }
+                // zeros: the segment's positions before and after the valid run
+                auto zero_slots = [&](int fa, int fz) {
+                  if (fa >= fz) return;
+                  int sl = slot_of(rq + fa);
+                  for (int ff = fa; ff < fz; ++ff) {
+                    if constexpr (DT == 0)
+                      asm volatile("st.shared.b32 [%0], %1;" ::"r"(rowbase + (uint32_t)sl * 4u), "r"(0u) : "memory");
+                    else
+                      asm volatile("st.shared.b16 [%0], %1;" ::"r"(rowbase + (uint32_t)sl * 2u), "h"((uint16_t)0) : "memory");
+                    if (++sl == rlen) sl = 0;
+                  }
+                };
+                zero_slots(f0, lo - ow);
+                zero_slots(hi - ow, f1);
+              }
+            }
+            // positions past the last image: zeros (they only meet zero dy, but stale
+            // shared memory could hold non-finite values)
+            if ((long long)lbeg + q1 > p.Mtot) {
+              const int za = (int)((Lx0 > (uint32_t)p.Mtot ? (long long)Lx0 : p.Mtot) - lbeg);
+              const int nz = q1 - za;
+              const int rows = p.npl * p.xch;
+              for (int it = gtid; it < nz * rows; it += kProdThreads) {
+                const int row = it / nz;
+                const int q = za + it - row * nz;
+                const uint32_t a = ring + (uint32_t)(row * p.xs + slot_of(q)) * ESZ;
+                if constexpr (DT == 0)
+                  asm volatile("st.shared.b32 [%0], %1;" ::"r"(a), "r"(0u) : "memory");
+                else
+                  asm volatile("st.shared.b16 [%0], %1;" ::"r"(a), "h"((uint16_t)0) : "memory");
+              }
             }
           }
           mbar_arrive(fb);
@@ -515,7 +603,7 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_kernel(const __grid_constan
         int c, tap;
         const bool rv = unit_row(p, (wt.mt0 + g) * 4 + q, lane, c, tap);
         uint32_t off = 0x80000000u, toff = 0u;
-        if (p.use_tma) {
+        if (p.use_tma == 1) {
           if (rv) off = (uint32_t)((p.tap_plane[tap] * p.xr + (c - c_lo)) * p.WL);
           if (p.TPU == 1 || rv) toff = (uint32_t)p.tap_rc[tap];
         } else {
@@ -535,7 +623,7 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_kernel(const __grid_constan
         }
         // row ring: linear row slot and column of the stage's first slot
         int rs0 = 0, c0 = 0;
-        if (p.use_tma) {
+        if (p.use_tma == 1) {
           const uint32_t sg = (uint32_t)(l0 + p.delta);
           const uint32_t r0 = fdiv(sg, p.fd_WL);
           c0 = (int)(sg - r0 * (uint32_t)p.WL);
@@ -564,7 +652,7 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_kernel(const __grid_constan
           const bool rv = (ent.x & 0x80000000u) == 0u;
           // ring position of this buffer's first column for this lane's tap
           int slot = 0, rs = 0, col = 0;
-          if (p.use_tma) {
+          if (p.use_tma == 1) {
             col = bs_c + (int)(ent.y & 0xffffu);
             rs = bs_rs + (int)(ent.y >> 16);
             if (col >= p.WL) {
@@ -585,10 +673,10 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_kernel(const __grid_constan
             // reads cover the 32 columns wherever they start in a group; column j is word
             // k + j (fp32) or halfwords rho + 2j, rho + 2j + 1 (bf16, shifted down when rho is
             // odd).  Groups never straddle ring rows (rlen and WL are chunk multiples).
-            const int rho = (p.use_tma ? col : slot) & (CHUNK - 1);
+            const int rho = (p.use_tma == 1 ? col : slot) & (CHUNK - 1);
             const int k = DT == 0 ? rho : rho >> 1;
             if (rv) {
-              if (p.use_tma) {
+              if (p.use_tma == 1) {
                 int cidx = col - rho;
 #pragma unroll
                 for (int i = 0; i < 9; ++i) {
@@ -635,7 +723,7 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_kernel(const __grid_constan
 #pragma unroll
               for (int j = 0; j < 32 * PPC; ++j) {
                 uint32_t a;
-                if (p.use_tma) {
+                if (p.use_tma == 1) {
                   a = ring + ((uint32_t)rs * rslot + ent.x + (uint32_t)col) * ESZ;
                   if (++col == p.WL) {
                     col = 0;
