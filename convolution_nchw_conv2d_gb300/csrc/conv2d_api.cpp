@@ -600,12 +600,15 @@ int build_bwd_filter_impl(const Desc& d0, const void* x, const void* dy, void* d
   p.fd_EL = make_fastdiv((uint32_t)p.EL);
   p.fd_rlen = make_fastdiv((uint32_t)p.rlen);
   p.fd_NR = make_fastdiv((uint32_t)p.NR);
-  if (p.use_tma == 1 && !(encode_dy_map(&p.tm_dy, dy, d.dt, d.N, d.K, d.P, d.Q, p.NK) &&
-                          encode_x_map(&p.tm_x, x, d.dt, d.N, d.C, d.H, d.W, p.WL))) {
+  // (sizing calls pass no tensors: their plan assumes the maps encode)
+  const bool sizing = x == nullptr && dy == nullptr;
+  if (p.use_tma == 1 && !sizing &&
+      !(encode_dy_map(&p.tm_dy, dy, d.dt, d.N, d.K, d.P, d.Q, p.NK) &&
+        encode_x_map(&p.tm_x, x, d.dt, d.N, d.C, d.H, d.W, p.WL))) {
     // The row ring cannot be encoded: plan the slot ring instead (another linear row width).
     return CONV2D_ERR_UNSUPPORTED;
   }
-  if (p.use_tma == 2 && !encode_dy_map(&p.tm_dy, dy, d.dt, d.N, d.K, d.P, d.Q, p.NK))
+  if (p.use_tma == 2 && !sizing && !encode_dy_map(&p.tm_dy, dy, d.dt, d.N, d.K, d.P, d.Q, p.NK))
     p.use_tma = 0;  // same ring, staged with cp.async
   // Split the positions so that the tiles fill the SMs with the shortest makespan
   // (tiles per CTA x positions per tile), preferring fewer splits.
@@ -674,6 +677,65 @@ int launch_err(cudaError_t e) {
   return CONV2D_ERR_LAUNCH;
 }
 
+// Plans of recent calls.  A plan depends only on the descriptor, the device and the tensor and
+// workspace addresses (the tensor maps and the launch parameters embed them), so a call that
+// repeats all of these reuses the plan instead of searching tile shapes and encoding tensor
+// maps again.  Small, fixed size, replaced round-robin; guarded by a mutex.
+struct PlanKey {
+  int op, dev;
+  Desc d;
+  const void* ptr[4];
+};
+
+bool same_key(const PlanKey& a, const PlanKey& b) {
+  return a.op == b.op && a.dev == b.dev && std::memcmp(&a.d, &b.d, sizeof(Desc)) == 0 && a.ptr[0] == b.ptr[0] &&
+         a.ptr[1] == b.ptr[1] && a.ptr[2] == b.ptr[2] && a.ptr[3] == b.ptr[3];
+}
+
+template <class Build>
+struct PlanCache {
+  static constexpr int kEntries = 16;
+  std::mutex mu;
+  PlanKey key[kEntries];
+  Build val[kEntries];
+  int used = 0, next = 0;
+  bool get(const PlanKey& k, Build& out) {
+    std::lock_guard<std::mutex> lk(mu);
+    for (int i = 0; i < used; ++i)
+      if (same_key(key[i], k)) {
+        out = val[i];
+        return true;
+      }
+    return false;
+  }
+  void put(const PlanKey& k, const Build& b) {
+    std::lock_guard<std::mutex> lk(mu);
+    key[next] = k;
+    val[next] = b;
+    next = (next + 1) % kEntries;
+    if (used < kEntries) ++used;
+  }
+};
+
+PlanCache<TapBuild> g_tap_plans;
+PlanCache<WgradBuild> g_wgrad_plans;
+PlanCache<size_t> g_ws_sizes;
+
+int workspace_size_uncached(int op, const Desc& d, size_t* bytes);
+
+PlanKey make_key(int op, const Desc& d, const void* a, const void* b, const void* c, const void* ws) {
+  PlanKey k;
+  std::memset(&k, 0, sizeof(k));
+  k.op = op;
+  cudaGetDevice(&k.dev);
+  k.d = d;
+  k.ptr[0] = a;
+  k.ptr[1] = b;
+  k.ptr[2] = c;
+  k.ptr[3] = ws;
+  return k;
+}
+
 }  // namespace
 
 extern "C" {
@@ -692,6 +754,18 @@ int conv2d_workspace_size(int op, int N, int C, int H, int W, int K, int R, int 
   const Desc d{N, C, H, W, K, R, S, pad_h, pad_w, stride_h, stride_w, P, Q, dtype};
   int rc = validate(d);
   if (rc) return rc;
+  const PlanKey key = make_key(op, d, nullptr, nullptr, nullptr, nullptr);
+  if (g_ws_sizes.get(key, *bytes)) return CONV2D_OK;
+  rc = workspace_size_uncached(op, d, bytes);
+  if (rc == CONV2D_OK) g_ws_sizes.put(key, *bytes);
+  return rc;
+}
+
+}  // extern "C"
+
+namespace {
+int workspace_size_uncached(int op, const Desc& d, size_t* bytes) {
+  int rc;
   const DevInfo di = device_info();
   if (op == CONV2D_OP_FWD || op == CONV2D_OP_BWD_DATA) {
     TapBuild b;
@@ -702,14 +776,23 @@ int conv2d_workspace_size(int op, int N, int C, int H, int W, int K, int R, int 
     return CONV2D_OK;
   }
   if (op == CONV2D_OP_BWD_FILTER) {
+    // The launch plans the copy-engine staging unless its tensor maps fail to encode for the
+    // actual tensors; size for whichever of the two plans it ends up with.
     WgradBuild b;
     rc = build_bwd_filter(d, nullptr, nullptr, nullptr, nullptr, di, b);
     if (rc) return rc;
-    *bytes = b.partial_bytes;
+    size_t need = b.partial_bytes;
+    WgradBuild b2;
+    if (build_bwd_filter_impl(d, nullptr, nullptr, nullptr, nullptr, di, b2, false) == CONV2D_OK)
+      need = std::max(need, b2.partial_bytes);
+    *bytes = need;
     return CONV2D_OK;
   }
   return CONV2D_ERR_BAD_OP;
 }
+}  // namespace
+
+extern "C" {
 
 static int run_tap(int op, const Desc& d, const void* src, const void* w, void* dst, void* ws, size_t wsb,
                    void* stream) {
@@ -720,8 +803,12 @@ static int run_tap(int op, const Desc& d, const void* src, const void* w, void* 
   const DevInfo di = device_info();
   if (!di.ok) return CONV2D_ERR_DEVICE;
   TapBuild b;
-  rc = op == CONV2D_OP_FWD ? build_fwd(d, src, w, dst, ws, di, b) : build_bwd_data(d, src, w, dst, ws, di, b);
-  if (rc) return rc;
+  const PlanKey key = make_key(op, d, src, w, dst, ws);
+  if (!g_tap_plans.get(key, b)) {
+    rc = op == CONV2D_OP_FWD ? build_fwd(d, src, w, dst, ws, di, b) : build_bwd_data(d, src, w, dst, ws, di, b);
+    if (rc) return rc;
+    g_tap_plans.put(key, b);
+  }
   rc = check_ws(ws, wsb, b.pack_bytes);
   if (rc) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -757,8 +844,12 @@ int conv2d_bwd_filter(int N, int C, int H, int W, int K, int R, int S, int pad_h
   const DevInfo di = device_info();
   if (!di.ok) return CONV2D_ERR_DEVICE;
   WgradBuild b;
-  rc = build_bwd_filter(d, x, dy, dw, workspace, di, b);
-  if (rc) return rc;
+  const PlanKey key = make_key(CONV2D_OP_BWD_FILTER, d, x, dy, dw, workspace);
+  if (!g_wgrad_plans.get(key, b)) {
+    rc = build_bwd_filter(d, x, dy, dw, workspace, di, b);
+    if (rc) return rc;
+    g_wgrad_plans.put(key, b);
+  }
   rc = check_ws(workspace, workspace_bytes, b.partial_bytes);
   if (rc) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);

@@ -27,6 +27,7 @@
 #include "conv_plan.h"
 #include "conv_stage.cuh"
 #include "sm103_ptx.cuh"
+#include "launch_util.cuh"
 
 namespace cg3 {
 
@@ -457,6 +458,8 @@ size_t tap_gemm_smem_bytes(const TapPlan& p) {
   return b + 1024;  // alignment slack for the dynamic base
 }
 
+static std::atomic<int> g_smem_set_0[kMaxDevices], g_smem_set_1[kMaxDevices];
+
 // Launched with programmatic stream serialization: the kernel's set-up overlaps the filter
 // pack that precedes it in the stream (the producers wait for it before the first copy).
 cudaError_t launch_tap_gemm(const TapPlan& p, int dt, int grid, cudaStream_t st) {
@@ -473,11 +476,11 @@ cudaError_t launch_tap_gemm(const TapPlan& p, int dt, int grid, cudaStream_t st)
   cfg.numAttrs = 1;
   cudaError_t e;
   if (dt == 0) {
-    e = cudaFuncSetAttribute(tap_gemm_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    e = ensure_dyn_smem(tap_gemm_kernel<0>, smem, g_smem_set_0);
     if (e != cudaSuccess) return e;
     e = cudaLaunchKernelEx(&cfg, tap_gemm_kernel<0>, p);
   } else {
-    e = cudaFuncSetAttribute(tap_gemm_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    e = ensure_dyn_smem(tap_gemm_kernel<1>, smem, g_smem_set_1);
     if (e != cudaSuccess) return e;
     e = cudaLaunchKernelEx(&cfg, tap_gemm_kernel<1>, p);
   }

@@ -20,6 +20,7 @@
 #include "conv_plan.h"
 #include "conv_stage.cuh"
 #include "sm103_ptx.cuh"
+#include "launch_util.cuh"
 
 namespace cg3 {
 
@@ -934,15 +935,17 @@ size_t wgrad_smem_bytes(const WgradPlan& p, int dt) {
   return b + 1024;
 }
 
+static std::atomic<int> g_smem_set_0[kMaxDevices], g_smem_set_1[kMaxDevices];
+
 cudaError_t launch_wgrad(const WgradPlan& p, int dt, int grid, cudaStream_t st) {
   const size_t smem = wgrad_smem_bytes(p, dt);
   cudaError_t e;
   if (dt == 0) {
-    e = cudaFuncSetAttribute(wgrad_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    e = ensure_dyn_smem(wgrad_kernel<0>, smem, g_smem_set_0);
     if (e != cudaSuccess) return e;
     wgrad_kernel<0><<<grid, kThreads, smem, st>>>(p);
   } else {
-    e = cudaFuncSetAttribute(wgrad_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    e = ensure_dyn_smem(wgrad_kernel<1>, smem, g_smem_set_1);
     if (e != cudaSuccess) return e;
     wgrad_kernel<1><<<grid, kThreads, smem, st>>>(p);
   }
