@@ -463,6 +463,25 @@ bool encode_dy_map(CUtensorMap* m, const void* dy, int dt, int N, int K, int P, 
   return r == CUDA_SUCCESS;
 }
 
+// dy (N, K, P, Q) as the 5-D tensor (w mod CHUNK, k, w / CHUNK, e, n) with a box of one
+// linear row of WL positions by NK output channels: shared-memory layout [chunk][k][CHUNK].
+// False if it cannot be encoded.
+bool encode_dy_row_map(CUtensorMap* m, const void* dy, int dt, int N, int K, int P, int Q, int NK, int WL) {
+  EncodeTiledFn fn = encode_tiled_fn();
+  if (!fn) return false;
+  const uint64_t esz = dt == 0 ? 4 : 2;
+  const uint64_t chunk = 16 / esz;
+  const cuuint64_t dims[5] = {(cuuint64_t)chunk, (cuuint64_t)K, (cuuint64_t)(Q / chunk), (cuuint64_t)P,
+                              (cuuint64_t)N};
+  const cuuint64_t strides[4] = {(cuuint64_t)P * Q * esz, 16u, (cuuint64_t)Q * esz, (cuuint64_t)K * P * Q * esz};
+  const cuuint32_t box[5] = {(cuuint32_t)chunk, (cuuint32_t)NK, (cuuint32_t)(WL / chunk), 1u, 1u};
+  const cuuint32_t estr[5] = {1u, 1u, 1u, 1u, 1u};
+  const CUresult r = fn(m, dt == 0 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5,
+                        const_cast<void*>(dy), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // ------------------------------------------------------------------ wgrad plan
 struct WgradBuild {
   WgradPlan p;
@@ -472,7 +491,7 @@ struct WgradBuild {
 };
 
 int build_bwd_filter_impl(const Desc& d0, const void* x, const void* dy, void* dw, void* ws, const DevInfo& di,
-                          WgradBuild& b, bool allow_tma) {
+                          WgradBuild& b, bool allow_tma, bool allow_rowshare) {
   const Desc d = flatten_pointwise(d0);
   WgradPlan& p = b.p;
   std::memset(&p, 0, sizeof(p));
@@ -494,29 +513,48 @@ int build_bwd_filter_impl(const Desc& d0, const void* x, const void* dy, void* d
   const int ESZ = d.dt == 0 ? 4 : 2;
   const int BUFP = d.dt == 0 ? 32 : 64;  // positions per 32-column TMEM buffer
   const int mh = (d.R - 1) / d.sh, mw = (d.S - 1) / d.sw;
+  p.NK = d.K <= 16 ? 16 : std::min(round_up(d.K, 32), 256);
+  p.n_ntiles = (d.K + p.NK - 1) / p.NK;
   // Copy-engine staging: unit column stride, rows and planes of whole 16-byte chunks, aligned
   // tensors.  Its linear row width WL covers the output columns plus the filter overhang and
-  // every pixel of an image row shifted by delta (the row copy starts at -align(pad_w)),
-  // and is CHUNK mod 2 CHUNK; at most 256 (one copy box).
+  // every pixel of an image row shifted by delta (the row copy starts at -align(pad_w)); at
+  // most 256 (one copy box).  Row-tap sharing (unit stride, 32 or more channels, two or more
+  // filter rows, room in TMEM for two row taps) takes WL a multiple of 2 CHUNK (an MMA's
+  // chunk pair never straddles a dy ring row) and pads the x ring rows to WL + CHUNK; without
+  // it WL itself is CHUNK mod 2 CHUNK.  Either way the x ring pitch is CHUNK mod 2 CHUNK, so
+  // 16-byte reads of 8 consecutive channel rows fall in distinct banks.
   bool tma = allow_tma && d.sw == 1 && d.W % CHUNK == 0 && d.Q % CHUNK == 0 && ((uintptr_t)x & 15) == 0 &&
              ((uintptr_t)dy & 15) == 0 && encode_tiled_fn() != nullptr;
+  p.TRU = 1;
+  if (tma && allow_rowshare && d.sh == 1 && d.C >= 32 && d.R > 1 && 2 * p.NK <= 384)
+    p.TRU = std::min(std::min(d.R, 4), 384 / p.NK);
+  if (allow_rowshare && p.TRU == 1) return CONV2D_ERR_UNSUPPORTED;  // the caller plans without sharing
   if (tma) {
     p.delta = round_up(d.pw, CHUNK) - d.pw;
     int wl = std::max(d.Q + mw, d.W + round_up(d.pw, CHUNK));
-    while (wl % (2 * CHUNK) != CHUNK) ++wl;
+    if (p.TRU > 1) {
+      wl = round_up(wl, 2 * CHUNK);
+      p.WLx = wl + CHUNK;
+    } else {
+      while (wl % (2 * CHUNK) != CHUNK) ++wl;
+      p.WLx = wl;
+    }
     p.WL = wl;
-    tma = wl <= 256 && 8 * (wl - (d.Q + mw)) <= 2 * wl;  // at most a quarter of the work wasted
+    tma = p.WLx <= 256 && 8 * (wl - (d.Q + mw)) <= 2 * wl;  // at most a quarter of the work wasted
   }
+  if (!tma && p.TRU > 1) return CONV2D_ERR_UNSUPPORTED;
   if (!tma) {
     // Linear row width: a multiple of the chunk (16-byte dy copies) when that wastes at
     // most 1/8 of it.
     p.delta = 0;
     const int wl = round_up(d.Q + mw, CHUNK);
     p.WL = (8 * (wl - (d.Q + mw)) <= wl) ? wl : d.Q + mw;
+    p.WLx = p.WL;
   }
   p.EL = d.P + mh;
   p.Mtot = (long long)d.N * p.EL * p.WL;
-  if (p.Mtot >= (1ll << 31)) return CONV2D_ERR_TOO_LARGE;
+  p.Mit = p.Mtot + (long long)(p.TRU - 1) * p.WL;
+  if (p.Mit >= (1ll << 31)) return CONV2D_ERR_TOO_LARGE;
   p.fd_img = make_fastdiv((uint32_t)(p.EL * p.WL));
   p.fd_WL = make_fastdiv((uint32_t)p.WL);
   p.npl = d.sh * d.sw;
@@ -527,34 +565,45 @@ int build_bwd_filter_impl(const Desc& d0, const void* x, const void* dy, void* d
       p.pl_off_h[a * d.sw + c] = a - d.ph;
       p.pl_off_w[a * d.sw + c] = c - d.pw;
     }
-  p.max_off = 0;
   for (int r = 0; r < d.R; ++r)
     for (int s = 0; s < d.S; ++s) {
       const int t = r * d.S + s;
       p.tap_plane[t] = (r % d.sh) * d.sw + (s % d.sw);
       p.tap_off[t] = (r / d.sh) * p.WL + s / d.sw;
       p.tap_rc[t] = ((r / d.sh) << 16) | (s / d.sw);
-      p.max_off = std::max(p.max_off, p.tap_off[t]);
     }
   p.vec_dy = d.Q % CHUNK == 0 && p.WL % CHUNK == 0 && ((uintptr_t)dy & 15) == 0;
   // Row units of 32 TMEM lanes: 32 channels of one tap, or (C < 32) TPU taps x C channels.
   p.Cg = d.C >= 32 ? 32 : d.C;
   p.TPU = d.C >= 32 ? 1 : 32 / d.C;
-  p.upc = (p.RS + p.TPU - 1) / p.TPU;
+  p.max_off = 0;
+  if (p.TPU == 1) {
+    // units of a channel group: (row block rb, column s), base tap (rb * TRU, s)
+    const int nrb = (d.R + p.TRU - 1) / p.TRU;
+    p.upc = nrb * d.S;
+    for (int rb = 0; rb < nrb; ++rb)
+      for (int s = 0; s < d.S; ++s) {
+        const int t = (rb * p.TRU) * d.S + s;
+        p.unit_tap[rb * d.S + s] = t;
+        p.max_off = std::max(p.max_off, p.tap_off[t]);
+      }
+  } else {
+    p.upc = (p.RS + p.TPU - 1) / p.TPU;
+    for (int t = 0; t < p.RS; ++t) p.max_off = std::max(p.max_off, p.tap_off[t]);
+  }
   p.fd_upc = make_fastdiv((uint32_t)p.upc);
   const int ncg = (d.C + p.Cg - 1) / p.Cg;
   p.nunits = ncg * p.upc;
   p.n_mtiles = (p.nunits + 3) / 4;
-  p.NK = d.K <= 16 ? 16 : std::min(round_up(d.K, 32), 256);
-  p.n_ntiles = (d.K + p.NK - 1) / p.NK;
-  // m-tiles per CTA tile: as many accumulators as TMEM holds next to the 4 A buffers, so
-  // x and dy are staged once for all of them; two accumulator sets when they fit.
-  p.G = std::max(1, std::min(std::min(p.n_mtiles, (512 - 128) / p.NK), 8));
+  // m-tiles per CTA tile: as many accumulators (TRU per m-tile) as TMEM holds next to the 4
+  // A buffers, so x and dy are staged once for all of them; two accumulator sets when they fit.
+  const int accw = p.TRU * p.NK;
+  p.G = std::max(1, std::min(std::min(p.n_mtiles, (512 - 128) / accw), 8));
   p.n_mgroups = (p.n_mtiles + p.G - 1) / p.G;
   p.G = (p.n_mtiles + p.n_mgroups - 1) / p.n_mgroups;  // balance the groups
-  p.accb = (128 + 2 * p.G * p.NK <= 512) ? 2 : 1;
+  p.accb = (128 + 2 * p.G * accw <= 512) ? 2 : 1;
   p.tmem_cols = 32;
-  while (p.tmem_cols < 128 + p.accb * p.G * p.NK) p.tmem_cols <<= 1;
+  while (p.tmem_cols < 128 + p.accb * p.G * accw) p.tmem_cols <<= 1;
   p.xch = 0;
   for (int mg = 0; mg < p.n_mgroups; ++mg) {
     const int u0 = 4 * p.G * mg, u1 = std::min(p.nunits, 4 * p.G * (mg + 1)) - 1;
@@ -585,7 +634,9 @@ int build_bwd_filter_impl(const Desc& d0, const void* x, const void* dy, void* d
       while ((q.xs * ESZ) % 128 != 16) q.xs += CHUNK;
       // row ring: S stages plus the halo, plus a row at each end
       q.NR = (S * KB + p.max_off + p.delta + p.WL - 1) / p.WL + 2;
-      q.a_stage_bytes = KB * p.NK * ESZ;
+      // dy row ring (row-tap sharing): the rows of S stages plus TRU - 1 rows before them
+      q.NRd = p.TRU > 1 ? (S * KB + (p.TRU - 1) * p.WL - 1) / p.WL + 2 : 0;
+      q.a_stage_bytes = p.TRU > 1 ? 0 : KB * p.NK * ESZ;
       if (wgrad_smem_bytes(q, d.dt) > di.smem_optin) continue;
       const long long score = (long long)S * KB * 4 + KB / 32;
       if (score > best) {
@@ -600,12 +651,15 @@ int build_bwd_filter_impl(const Desc& d0, const void* x, const void* dy, void* d
   p.fd_EL = make_fastdiv((uint32_t)p.EL);
   p.fd_rlen = make_fastdiv((uint32_t)p.rlen);
   p.fd_NR = make_fastdiv((uint32_t)p.NR);
+  p.fd_NRd = make_fastdiv((uint32_t)std::max(p.NRd, 1));
   // (sizing calls pass no tensors: their plan assumes the maps encode)
   const bool sizing = x == nullptr && dy == nullptr;
   if (p.use_tma == 1 && !sizing &&
-      !(encode_dy_map(&p.tm_dy, dy, d.dt, d.N, d.K, d.P, d.Q, p.NK) &&
-        encode_x_map(&p.tm_x, x, d.dt, d.N, d.C, d.H, d.W, p.WL))) {
-    // The row ring cannot be encoded: plan the slot ring instead (another linear row width).
+      !((p.TRU > 1 ? encode_dy_row_map(&p.tm_dyr, dy, d.dt, d.N, d.K, d.P, d.Q, p.NK, p.WL)
+                   : encode_dy_map(&p.tm_dy, dy, d.dt, d.N, d.K, d.P, d.Q, p.NK)) &&
+        encode_x_map(&p.tm_x, x, d.dt, d.N, d.C, d.H, d.W, p.WLx))) {
+    // The row ring cannot be encoded: plan without sharing, or the slot ring (another linear
+    // row width).
     return CONV2D_ERR_UNSUPPORTED;
   }
   if (p.use_tma == 2 && !sizing && !encode_dy_map(&p.tm_dy, dy, d.dt, d.N, d.K, d.P, d.Q, p.NK))
@@ -613,7 +667,7 @@ int build_bwd_filter_impl(const Desc& d0, const void* x, const void* dy, void* d
   // Split the positions so that the tiles fill the SMs with the shortest makespan
   // (tiles per CTA x positions per tile), preferring fewer splits.
   const long long base = (long long)p.n_mgroups * p.n_ntiles;
-  const long long stage_count = (p.Mtot + p.KB - 1) / p.KB;
+  const long long stage_count = (p.Mit + p.KB - 1) / p.KB;
   const size_t per_split = (size_t)p.RS * d.C * d.K * sizeof(float);
   long long nsb = 1;
   double best_t = -1.0;
@@ -629,7 +683,7 @@ int build_bwd_filter_impl(const Desc& d0, const void* x, const void* dy, void* d
   }
   long long slen = (stage_count + nsb - 1) / nsb * p.KB;
   p.split_len = slen;
-  p.nsplit = (int)((p.Mtot + slen - 1) / slen);
+  p.nsplit = (int)((p.Mit + slen - 1) / slen);
   p.total_tiles = base * p.nsplit;
   b.partial_bytes = per_split * (size_t)p.nsplit;
   if (b.partial_bytes > kWorkspaceCap) return CONV2D_ERR_UNSUPPORTED;
@@ -649,11 +703,18 @@ int build_bwd_filter_impl(const Desc& d0, const void* x, const void* dy, void* d
 
 // Backward-filter plan: copy-engine staging when the shape allows it and its row ring fits,
 // else the cp.async staging.
+// Staging variants of the backward-filter plan, most preferred first: copy-engine row ring
+// with row-tap sharing, copy-engine row ring, slot ring.
+constexpr bool kWgradVariants[3][2] = {{true, true}, {true, false}, {false, false}};
+
 int build_bwd_filter(const Desc& d, const void* x, const void* dy, void* dw, void* ws, const DevInfo& di,
                      WgradBuild& b) {
-  const int rc = build_bwd_filter_impl(d, x, dy, dw, ws, di, b, true);
-  if (rc == CONV2D_OK || rc != CONV2D_ERR_UNSUPPORTED) return rc;
-  return build_bwd_filter_impl(d, x, dy, dw, ws, di, b, false);
+  int rc = CONV2D_ERR_UNSUPPORTED;
+  for (const auto& v : kWgradVariants) {
+    rc = build_bwd_filter_impl(d, x, dy, dw, ws, di, b, v[0], v[1]);
+    if (rc != CONV2D_ERR_UNSUPPORTED) return rc;
+  }
+  return rc;
 }
 
 int check_ptrs(const void* a, const void* b, const void* c, int dt) {
@@ -782,9 +843,11 @@ int workspace_size_uncached(int op, const Desc& d, size_t* bytes) {
     rc = build_bwd_filter(d, nullptr, nullptr, nullptr, nullptr, di, b);
     if (rc) return rc;
     size_t need = b.partial_bytes;
-    WgradBuild b2;
-    if (build_bwd_filter_impl(d, nullptr, nullptr, nullptr, nullptr, di, b2, false) == CONV2D_OK)
-      need = std::max(need, b2.partial_bytes);
+    for (const auto& v : kWgradVariants) {
+      WgradBuild b2;
+      if (build_bwd_filter_impl(d, nullptr, nullptr, nullptr, nullptr, di, b2, v[0], v[1]) == CONV2D_OK)
+        need = std::max(need, b2.partial_bytes);
+    }
     *bytes = need;
     return CONV2D_OK;
   }

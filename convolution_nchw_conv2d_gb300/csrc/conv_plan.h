@@ -120,6 +120,10 @@ struct WgradPlan {
   // x as a 4-D tensor (w, h, c, n) with a box of one image row (WL pixels from column
   // -align(pad_w)) by 32 channels; valid when use_tma.
   CUtensorMap tm_x;
+  // dy as a 5-D tensor (w mod CHUNK, k, w / CHUNK, row e, image n) for copy-engine loads of
+  // one whole linear row of positions for NK output channels, [chunk][k][CHUNK] in shared
+  // memory; valid when TRU > 1.
+  CUtensorMap tm_dyr;
   int use_tma;           // copy-engine staging (unit column stride, aligned tensors): dy by
                          // tensor copies, x by tensor copies of whole rows into a row ring
   // Row ring (use_tma): [NR row slots][plane][xr channel rows][WL].  Position L lives at
@@ -129,6 +133,19 @@ struct WgradPlan {
   // channel rows in distinct banks.
   int NR, xr, delta;
   FastDiv fd_NR;
+  int WLx;               // row ring pitch of one channel row (elements, >= WL)
+  // Row-tap sharing (TRU > 1, row ring only): a unit is 32 channels x one base tap
+  // (r0, s) and stands for the TRU taps (r0 + j, s), j < TRU.  Since tap (r0 + j, s) reads
+  // x at L + j*WL + off(r0, s), the sum over positions L equals the sum over L' = L + j*WL of
+  // x[L' + off(r0, s)] * dy[L' - j*WL]: one A operand built from x at L' serves all TRU taps,
+  // each paired with dy shifted back by j linear rows.  dy is then staged as a ring of NRd
+  // whole linear rows, [row slot][chunk][k][CHUNK], and the positions L' run over
+  // [0, Mtot + (TRU-1)*WL) (dy reads as zero outside [0, Mtot)).
+  int TRU;               // row taps per unit (1: every unit is one tap)
+  int NRd;               // dy ring rows (TRU > 1)
+  FastDiv fd_NRd;
+  long long Mit;         // positions iterated (Mtot + (TRU - 1) * WL)
+  int unit_tap[kMaxTaps];  // base tap of the j-th unit of a channel group (TPU == 1)
   const void* x;         // NCHW
   const void* dy;        // N K P Q
   float* partial;        // [split][R*S][C][K] fp32

@@ -64,7 +64,7 @@ __device__ __forceinline__ bool unit_row(const WgradPlan& p, int unit, int lane,
   const int tu = unit - cg * p.upc;
   if (p.TPU == 1) {
     c = cg * p.Cg + lane;
-    tap = tu;
+    tap = p.unit_tap[tu];
     return c < p.C;
   }
   const int tl = lane / p.Cg;
@@ -257,14 +257,52 @@ __device__ __forceinline__ void stage_dy(const WgradPlan& p, uint32_t dst0, long
 __device__ __forceinline__ void split_range(const WgradPlan& p, int sp, long long& lbeg, long long& lend) {
   lbeg = (long long)sp * p.split_len;
   lend = lbeg + p.split_len;
-  if (lend > p.Mtot) lend = p.Mtot;
+  if (lend > p.Mit) lend = p.Mit;
 }
 }  // namespace
 
 // Bytes of the x ring.
 __host__ __device__ inline size_t wgrad_ring_bytes(const WgradPlan& p, int dt) {
   const size_t esz = dt == 0 ? 4 : 2;
-  return p.use_tma == 1 ? (size_t)p.NR * p.npl * p.xr * p.WL * esz : (size_t)p.npl * p.xch * p.xs * esz;
+  return p.use_tma == 1 ? (size_t)p.NR * p.npl * p.xr * p.WLx * esz : (size_t)p.npl * p.xch * p.xs * esz;
+}
+
+// Bytes of the dy row ring (row-tap sharing only).
+__host__ __device__ inline size_t wgrad_dyring_bytes(const WgradPlan& p, int dt) {
+  const size_t esz = dt == 0 ? 4 : 2;
+  return p.TRU > 1 ? (size_t)p.NRd * p.WL * p.NK * esz : 0;
+}
+
+// One A buffer's MMAs under row-tap sharing: for each row tap j, the 4 MMAs of the buffer
+// (8 * PPC positions each) into accumulator j, with B = dy at the buffer's positions moved
+// back by j linear rows, read from the dy row ring ([row slot][chunk][k][16 B]; an MMA's two
+// chunks never straddle a row since rows are whole pairs of chunks).  row0 / col0: ring row
+// slot and column of the buffer's first position.
+template <int KIND, int TRU>
+__device__ __forceinline__ void issue_row_taps(const WgradPlan& p, uint32_t dcol, uint32_t acol, uint32_t dyring,
+                                               int row0, int col0, uint32_t b_hi, uint32_t id, bool first) {
+  constexpr int CHUNK = KIND == 0 ? 4 : 8;
+  constexpr int KM = KIND == 0 ? 8 : 16;  // positions per MMA
+  const uint32_t cbytes = (uint32_t)p.NK * 16u;         // one chunk of NK rows
+  const uint32_t rbytes = (uint32_t)(p.WL / CHUNK) * cbytes;  // one ring row
+  const uint32_t lbo = ((cbytes >> 4) & 0x3FFFu) << 16;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    int col = col0 + KM * i, row = row0;
+    while (col >= p.WL) {  // (rows may be narrower than a buffer)
+      col -= p.WL;
+      if (++row == p.NRd) row = 0;
+    }
+    const uint32_t cofs = (uint32_t)(col / CHUNK) * cbytes;
+#pragma unroll
+    for (int j = 0; j < TRU; ++j) {
+      int sl = row - j;
+      if (sl < 0) sl += p.NRd;
+      const uint32_t addr = dyring + (uint32_t)sl * rbytes + cofs;
+      mma_ts_lh<KIND>(dcol + (uint32_t)(j * p.NK), acol + (uint32_t)(8 * i), ((addr & 0x3FFFFu) >> 4) | lbo, b_hi, id,
+                      (first && i == 0) ? 0u : 1u);
+    }
+  }
 }
 
 // tcgen05.st of w[K .. K + 31] to 32 TMEM columns (K fixed, so w stays in registers).
@@ -301,8 +339,8 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_kernel(const __grid_constan
 
   // 1024-byte aligned base (the size includes the slack): tensor-copy destinations
   uint8_t* ptr = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const uint32_t a0 = smem_u32(ptr);  // dy tiles
-  ptr += (size_t)S * p.a_stage_bytes;
+  const uint32_t a0 = smem_u32(ptr);  // dy tiles per stage, or the dy row ring (TRU > 1)
+  ptr += (size_t)S * p.a_stage_bytes + wgrad_dyring_bytes(p, DT);
   const uint32_t ring = smem_u32(ptr);  // x: slot ring [plane][channel][xs], or the row ring (use_tma 1)
   ptr += (wgrad_ring_bytes(p, DT) + 15) & ~size_t(15);
   // per builder warp, m-tile and lane: {ring offset of the lane's row (bit 31: padding row),
@@ -374,6 +412,7 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_kernel(const __grid_constan
         const int c_lo = tile_c_lo(p, wt.mt0);
         const int nch_x = p.C - c_lo < p.xch ? p.C - c_lo : p.xch;  // ring rows with real channels
         long long next_row = (lbeg + p.delta) / p.WL;  // first linear row not loaded for this tile
+        long long next_dy_row = lbeg / p.WL - (p.TRU - 1);  // first dy row not loaded (row ring)
         int s_local = 0;
         for (long long l0 = lbeg; l0 < lend; l0 += KB, ++counter, ++s_local) {
           const int stage = (int)(counter % S);
@@ -386,11 +425,41 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_kernel(const __grid_constan
             ok = false;
             break;
           }
+          // dy row ring: a new tile's rows may map to ring slots of the previous tile's last
+          // stages, so every earlier fill must be consumed first (fill c completes phase c / S
+          // of its slot's empty barrier; no later phase can have completed yet)
+          if (p.TRU > 1 && s_local == 0 && ti > 0) {
+            for (long long c = counter - S + 1 > 0 ? counter - S + 1 : 0; c < counter && ok; ++c)
+              if (!mbar_wait(bar_at(empty, (int)(c % S)), (uint32_t)((c / S) & 1), abort_flag, &g_wgrad_err))
+                ok = false;
+            if (!ok) break;
+          }
           // the slot's previous contents were read through the generic proxy (builder
           // loads): order those reads before this stage's copy-engine writes
           fence_proxy_async();
           const uint32_t fb = bar_at(full, stage);
           const uint32_t a_st = a0 + (uint32_t)stage * p.a_stage_bytes;
+          if (p.TRU > 1) {
+            // dy: the linear rows this stage reads that are not loaded yet, from (TRU - 1) rows
+            // before the stage to its last position; one tensor copy per row (NK channels,
+            // [chunk][k][CHUNK]); rows before the first image, past the last one, or past
+            // the output height read as zeros.
+            const long long rdB = (l0 + KB - 1) / p.WL;
+            const int nrows = next_dy_row <= rdB ? (int)(rdB - next_dy_row + 1) : 0;
+            const uint32_t rbytes = (uint32_t)(p.WL * p.NK * ESZ);
+            for (int it = gtid; it < nrows; it += kProdThreads) {
+              const long long R = next_dy_row + it;
+              int n = 0, e = (int)R;  // R < 0: a row before the tensor
+              if (R >= 0) {
+                n = (int)(R / p.EL);
+                e = (int)(R - (long long)n * p.EL);
+              }
+              const int slot = (int)(((R % p.NRd) + p.NRd) % p.NRd);
+              mbar_expect_tx(fb, rbytes);
+              tma_load_5d(a0 + (uint32_t)slot * rbytes, &p.tm_dyr, 0, kbase, 0, e, n, fb);
+            }
+            if (nrows > 0) next_dy_row = rdB + 1;
+          } else
           // dy: chunk j = positions l0 + CHUNK*j .. +CHUNK-1 (one linear row: WL % CHUNK == 0)
           // chunk j is issued by lane j / 4 of warp j % 4 (the issue work is spread over the
           // four schedulers)
@@ -428,8 +497,8 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_kernel(const __grid_constan
                   const int e = (int)(R - (long long)n * p.EL);
                   const int h = e * p.pl_step_h + p.pl_off_h[pl];
                   const int rs = (int)(R % p.NR);
-                  const uint32_t dst = ring + (uint32_t)(((rs * p.npl + pl) * p.xr + 32 * cg) * p.WL * ESZ);
-                  mbar_expect_tx(fb, (uint32_t)(32 * p.WL * ESZ));
+                  const uint32_t dst = ring + (uint32_t)(((rs * p.npl + pl) * p.xr + 32 * cg) * p.WLx * ESZ);
+                  mbar_expect_tx(fb, (uint32_t)(32 * p.WLx * ESZ));
                   tma_load_4d(dst, &p.tm_x, p.pl_off_w[pl] - p.delta, h, c_lo + 32 * cg, n, fb);
                 }
                 next_row = rB + 1;
@@ -588,7 +657,7 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_kernel(const __grid_constan
     const int set = (warp - kBuildWarp0) >> 2;  // builds A buffers with index mod 2 == set
     const int q = warp & 3;                      // TMEM lane quarter
     uint2* mytab = btab + (size_t)(warp - kBuildWarp0) * p.G * 32;
-    const uint32_t rslot = (uint32_t)(p.npl * p.xr * p.WL);  // row ring: elements per row slot
+    const uint32_t rslot = (uint32_t)(p.npl * p.xr * p.WLx);  // row ring: elements per row slot
     const int ngr = rlen / CHUNK;
     long long counter = 0, kglob = 0;
     bool ok = true;
@@ -605,7 +674,7 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_kernel(const __grid_constan
         const bool rv = unit_row(p, (wt.mt0 + g) * 4 + q, lane, c, tap);
         uint32_t off = 0x80000000u, toff = 0u;
         if (p.use_tma == 1) {
-          if (rv) off = (uint32_t)((p.tap_plane[tap] * p.xr + (c - c_lo)) * p.WL);
+          if (rv) off = (uint32_t)((p.tap_plane[tap] * p.xr + (c - c_lo)) * p.WLx);
           if (p.TPU == 1 || rv) toff = (uint32_t)p.tap_rc[tap];
         } else {
           if (rv) off = (uint32_t)((p.tap_plane[tap] * p.xch + (c - c_lo)) * p.xs * ESZ);
@@ -772,11 +841,18 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_kernel(const __grid_constan
       tc_fence_after();
       const int k0 = wt.nt * p.NK;
       const bool vec = (p.K & 3) == 0;
-      for (int g = 0; g < wt.gcount; ++g) {
+      for (int gj = 0; gj < wt.gcount * p.TRU; ++gj) {
+        // accumulator gj = (m-tile g, row tap j): taps (r0 + j, s) of the unit's base tap
+        const int g = gj / p.TRU, j = gj - g * p.TRU;
         int c, tap;
-        const bool rv = unit_row(p, (wt.mt0 + g) * 4 + q, lane, c, tap);
+        bool rv = unit_row(p, (wt.mt0 + g) * 4 + q, lane, c, tap);
+        if (j > 0) {
+          rv = rv && (p.tap_rc[tap] >> 16) + j < p.R;
+          tap += j * p.S;
+        }
         float* dst = p.partial + (((long long)wt.sp * p.RS + tap) * p.C + c) * (long long)p.K + k0;
-        const uint32_t tcol = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(kAcol + (acc * p.G + g) * p.NK);
+        const uint32_t tcol =
+            tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(kAcol + ((acc * p.G + g) * p.TRU + j) * p.NK);
         for (int c0 = 0; c0 < p.NK; c0 += 16) {
           uint32_t r[16];
           tmem_ld16(tcol + (uint32_t)c0, r);
@@ -821,7 +897,7 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_kernel(const __grid_constan
       split_range(p, wt.sp, lbeg, lend);
       if (!mbar_wait(bar_at(acce, acc), aphase ^ 1u, abort_flag, &g_wgrad_err)) break;
       tc_fence_after();
-      const uint32_t dcol0 = tmem + (uint32_t)(kAcol + acc * p.G * p.NK);
+      const uint32_t dcol0 = tmem + (uint32_t)(kAcol + acc * p.G * p.TRU * p.NK);
       bool first_stage = true;
       for (long long l0 = lbeg; l0 < lend && ok; l0 += KB, ++counter) {
         const int stage = (int)(counter % S);
@@ -846,14 +922,28 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_kernel(const __grid_constan
           }
           tc_fence_after();
           if (leader) {
-            const uint32_t blo = blo0 + (uint32_t)(8 * b) * nk16;
             const uint32_t acol = tmem + (uint32_t)(abuf * 32);
-            const uint32_t dcol = dcol0 + (uint32_t)(g * p.NK);
             const bool first = first_stage && b == 0;
+            if (p.TRU == 1) {
+              const uint32_t blo = blo0 + (uint32_t)(8 * b) * nk16;
+              const uint32_t dcol = dcol0 + (uint32_t)(g * p.NK);
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-              mma_ts_lh<KIND>(dcol, acol + (uint32_t)(8 * i), blo + (uint32_t)(2 * i) * nk16, b_hi, id,
-                              (first && i == 0) ? 0u : 1u);
+              for (int i = 0; i < 4; ++i)
+                mma_ts_lh<KIND>(dcol, acol + (uint32_t)(8 * i), blo + (uint32_t)(2 * i) * nk16, b_hi, id,
+                                (first && i == 0) ? 0u : 1u);
+            } else {
+              // ring row slot and column of the buffer's first position
+              const uint32_t P0 = (uint32_t)(l0 + (long long)b * BUFP);
+              const uint32_t R0 = fdiv(P0, p.fd_WL);
+              const int col0 = (int)(P0 - R0 * (uint32_t)p.WL);
+              const int row0 = (int)(R0 - fdiv(R0, p.fd_NRd) * (uint32_t)p.NRd);
+              const uint32_t dcol = dcol0 + (uint32_t)(g * p.TRU * p.NK);
+              switch (p.TRU) {
+                case 2: issue_row_taps<KIND, 2>(p, dcol, acol, a0, row0, col0, b_hi, id, first); break;
+                case 3: issue_row_taps<KIND, 3>(p, dcol, acol, a0, row0, col0, b_hi, id, first); break;
+                default: issue_row_taps<KIND, 4>(p, dcol, acol, a0, row0, col0, b_hi, id, first); break;
+              }
+            }
             tc_commit(bar_at(aempty, abuf));
           }
           __syncwarp();
@@ -927,7 +1017,7 @@ __global__ void __launch_bounds__(32 * kReduceWarps) wgrad_reduce_kernel(const _
 }
 
 size_t wgrad_smem_bytes(const WgradPlan& p, int dt) {
-  size_t b = (size_t)p.stages * p.a_stage_bytes;
+  size_t b = (size_t)p.stages * p.a_stage_bytes + wgrad_dyring_bytes(p, dt);
   b += (wgrad_ring_bytes(p, dt) + 15) & ~size_t(15);
   b += (size_t)8 * p.G * 32 * sizeof(uint2);
   b = (b + 15) & ~size_t(15);

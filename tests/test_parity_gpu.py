@@ -151,6 +151,12 @@ SMALL = [
     (4, 12, 20, 20, 24, 3, 3, 0, 0, 1, 1),   # no padding
     (1, 9, 31, 17, 11, 5, 5, 2, 2, 1, 1),
     (2, 300, 5, 5, 20, 3, 3, 1, 1, 1, 1),    # C > 256: several channel blocks
+    # backward-filter row-tap sharing (unit stride, C >= 32, aligned rows)
+    (2, 64, 16, 16, 64, 3, 3, 1, 1, 1, 1),   # 3 filter rows per unit
+    (1, 40, 16, 16, 48, 5, 3, 2, 1, 1, 1),   # row blocks of 4 + 1, a partial channel group
+    (1, 32, 16, 16, 150, 3, 3, 1, 1, 1, 1),  # wide k tile: row blocks of 2 + 1
+    (1, 32, 6, 48, 64, 3, 3, 1, 1, 1, 1),    # wide rows (bf16 shares rows too)
+    (2, 48, 10, 16, 20, 3, 5, 1, 2, 1, 1),
 ]
 
 
