@@ -27,14 +27,16 @@ namespace cg3 {
 __device__ int g_wgrad_err;
 
 namespace {
-// CTA roles (544 threads): warps 0-3 producers (cp.async, two stages in flight), warps 4-11
-// two builder sets (set h builds the A buffers with index mod 2 == h), warps 12-15
-// epilogue, warp 16 TMEM allocation + MMA issue.
-constexpr int kThreads = 544;
+// CTA roles: warps 0-3 producers, then kSets builder sets of 4 warps (set h builds the A
+// buffers whose running index is h mod kSets), then 4 epilogue warps, then one warp for TMEM
+// allocation + MMA issue.
+constexpr int kSets = 2;
 constexpr int kProdThreads = 128;
 constexpr int kBuildWarp0 = 4;
-constexpr int kEpiWarp0 = 12;
-constexpr int kMmaWarp = 16;
+constexpr int kBuildWarps = 4 * kSets;
+constexpr int kEpiWarp0 = kBuildWarp0 + kBuildWarps;
+constexpr int kMmaWarp = kEpiWarp0 + 4;
+constexpr int kThreads = 32 * (kMmaWarp + 1);
 constexpr int kNabuf = 4;               // TMEM A buffers of 32 columns
 constexpr int kAcol = 32 * kNabuf;      // first accumulator column
 
@@ -286,6 +288,25 @@ __device__ __forceinline__ void issue_row_taps(const WgradPlan& p, uint32_t dcol
   const uint32_t cbytes = (uint32_t)p.NK * 16u;         // one chunk of NK rows
   const uint32_t rbytes = (uint32_t)(p.WL / CHUNK) * cbytes;  // one ring row
   const uint32_t lbo = ((cbytes >> 4) & 0x3FFFu) << 16;
+  if (col0 + 3 * KM < p.WL) {
+    // the buffer's positions lie in one ring row: descriptors advance by one chunk pair per
+    // MMA from the row slot of each row tap (computed first, so the MMAs issue back to back)
+    uint32_t lo[TRU];
+#pragma unroll
+    for (int j = 0; j < TRU; ++j) {
+      int sl = row0 - j;
+      if (sl < 0) sl += p.NRd;
+      lo[j] = (((dyring + (uint32_t)sl * rbytes + (uint32_t)(col0 / CHUNK) * cbytes) & 0x3FFFFu) >> 4) | lbo;
+    }
+    const uint32_t step = (2u * cbytes) >> 4;
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int j = 0; j < TRU; ++j)
+        mma_ts_lh<KIND>(dcol + (uint32_t)(j * p.NK), acol + (uint32_t)(8 * i), lo[j] + (uint32_t)i * step, b_hi, id,
+                        (first && i == 0) ? 0u : 1u);
+    return;
+  }
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     int col = col0 + KM * i, row = row0;
@@ -346,7 +367,7 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_kernel(const __grid_constan
   // per builder warp, m-tile and lane: {ring offset of the lane's row (bit 31: padding row),
   // tap offset} -- set once per tile
   uint2* btab = reinterpret_cast<uint2*>(ptr);
-  ptr += (size_t)8 * p.G * 32 * sizeof(uint2);
+  ptr += (size_t)kBuildWarps * p.G * 32 * sizeof(uint2);
   ptr = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(ptr) + 15) & ~uintptr_t(15));
   const uint32_t full = smem_u32(ptr);
   const uint32_t empty = full + 8u * S;
@@ -363,7 +384,7 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_kernel(const __grid_constan
   if (tid == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(bar_at(full, s), kProdThreads);
-      mbar_init(bar_at(empty, s), 1 + 8);  // MMA commit + 8 builder warps
+      mbar_init(bar_at(empty, s), 1 + kBuildWarps);  // MMA commit + every builder warp
     }
     for (int b = 0; b < kNabuf; ++b) {
       mbar_init(bar_at(afull, b), 4);  // the 4 warps of the building set
@@ -373,7 +394,7 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_kernel(const __grid_constan
       mbar_init(bar_at(accf, a), 1);
       mbar_init(bar_at(acce, a), 4);
     }
-    mbar_init(xfree, 8);
+    mbar_init(xfree, kBuildWarps);
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -654,12 +675,13 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_kernel(const __grid_constan
     }
   } else if (warp < kEpiWarp0) {
     // =============================================================== builders
-    const int set = (warp - kBuildWarp0) >> 2;  // builds A buffers with index mod 2 == set
+    const int set = (warp - kBuildWarp0) >> 2;  // builds A buffers with running index mod kSets == set
     const int q = warp & 3;                      // TMEM lane quarter
     uint2* mytab = btab + (size_t)(warp - kBuildWarp0) * p.G * 32;
     const uint32_t rslot = (uint32_t)(p.npl * p.xr * p.WLx);  // row ring: elements per row slot
     const int ngr = rlen / CHUNK;
     long long counter = 0, kglob = 0;
+    int kset = 0;  // kglob mod kSets
     bool ok = true;
     for (long long t = blockIdx.x; t < p.total_tiles && ok; t += gridDim.x) {
       const WTile wt = decode_wtile(p, t);
@@ -700,7 +722,8 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_kernel(const __grid_constan
           rs0 = (int)(r0 - fdiv(r0, p.fd_NR) * (uint32_t)p.NR);
         }
         int bs_rs = rs0, bs_c = c0;  // row ring position of buffer b's first column
-        for (int bg = 0, b = 0, g = 0; bg < nbuf * wt.gcount && ok; ++bg, ++kglob) {
+        for (int bg = 0, b = 0, g = 0; bg < nbuf * wt.gcount && ok;
+             ++bg, ++kglob, kset = kset + 1 == kSets ? 0 : kset + 1) {
           // b: buffer of positions, g: m-tile within the group (g fastest)
           if (bg > 0 && ++g == wt.gcount) {
             g = 0;
@@ -711,7 +734,7 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_kernel(const __grid_constan
               if (++bs_rs == p.NR) bs_rs = 0;
             }
           }
-          if ((int)(kglob & 1) != set) continue;
+          if (kset != set) continue;
           const int abuf = (int)(kglob & (kNabuf - 1));
           const uint32_t use = (uint32_t)((kglob / kNabuf) & 1);
           if (!mbar_wait(bar_at(aempty, abuf), use ^ 1u, abort_flag, &g_wgrad_err)) {
@@ -1019,7 +1042,7 @@ __global__ void __launch_bounds__(32 * kReduceWarps) wgrad_reduce_kernel(const _
 size_t wgrad_smem_bytes(const WgradPlan& p, int dt) {
   size_t b = (size_t)p.stages * p.a_stage_bytes + wgrad_dyring_bytes(p, dt);
   b += (wgrad_ring_bytes(p, dt) + 15) & ~size_t(15);
-  b += (size_t)8 * p.G * 32 * sizeof(uint2);
+  b += (size_t)kBuildWarps * p.G * 32 * sizeof(uint2);
   b = (b + 15) & ~size_t(15);
   b += 8 * (2 * p.stages + 2 * kNabuf + 6) + 16;
   return b + 1024;
