@@ -999,41 +999,76 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_kernel(const __grid_constan
 }
 
 // Sum the split partials and write dw (KCRS), in a fixed order (deterministic).  A block
-// of 8 warps takes 32 consecutive outputs (tap, c, k) with k fastest, so every partial
-// read of a warp is one 128-byte line; warp w adds splits w, w + 8, w + 16, ... in order,
-// and the 8 warp sums are then added in warp order.
+// of 8 warps takes 32 * V consecutive outputs (tap, c, k) with k fastest (V = 4 when K is a
+// multiple of 4: one 16-byte read per lane, so a warp reads 512 contiguous bytes of a
+// split); warp w adds splits w, w + 8, w + 16, ... in order, with the reads of up to 8 of
+// its splits issued before their adds, and the 8 warp sums are then added in warp order.
 constexpr int kReduceWarps = 8;
-template <int DT>
+template <int DT, int V>
 __global__ void __launch_bounds__(32 * kReduceWarps) wgrad_reduce_kernel(const __grid_constant__ ReducePlan rp) {
-  __shared__ float part[kReduceWarps][32];
+  __shared__ float part[kReduceWarps][32 * V];
   const int RS = rp.R * rp.S;
   const long long total = (long long)RS * rp.C * rp.K;
   const long long split_stride = (long long)RS * rp.c_pad * rp.k_pad;
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   griddep_wait();  // the partials are written by the previous grid
-  for (long long o0 = (long long)blockIdx.x * 32; o0 < total; o0 += (long long)gridDim.x * 32) {
-    const long long i = o0 + lane;
-    int k = 0, c = 0, tap = 0;
-    float acc = 0.f;
-    if (i < total) {
-      k = (int)(i % rp.K);
-      const long long r = i / rp.K;
-      c = (int)(r % rp.C);
-      tap = (int)(r / rp.C);
-      const float* src = rp.partial + ((long long)tap * rp.c_pad + c) * rp.k_pad + k;
-      for (int sp = w; sp < rp.nsplit; sp += kReduceWarps) acc += __ldg(src + sp * split_stride);
-    }
-    part[w][lane] = acc;
-    __syncthreads();
-    if (w == 0 && i < total) {
-      float sum = part[0][lane];
+  for (long long o0 = (long long)blockIdx.x * 32 * V; o0 < total; o0 += (long long)gridDim.x * 32 * V) {
+    const long long i = o0 + (long long)lane * V;  // first of this lane's V outputs
+    float acc[V];
 #pragma unroll
-      for (int j = 1; j < kReduceWarps; ++j) sum += part[j][lane];
-      const long long o = ((long long)k * rp.C + c) * RS + tap;
-      if constexpr (DT == 0)
-        static_cast<float*>(rp.dw)[o] = sum;
-      else
-        static_cast<__nv_bfloat16*>(rp.dw)[o] = __float2bfloat16_rn(sum);
+    for (int v = 0; v < V; ++v) acc[v] = 0.f;
+    if (i < total) {
+      // partial index of output i: the partial layout [split][tap][c][k] equals the output
+      // order (tap, c, k) when c_pad == C and k_pad == K
+      const float* src = rp.partial + i;
+      int sp = w;
+      for (; sp + 7 * kReduceWarps < rp.nsplit; sp += 8 * kReduceWarps) {
+        float r[8][V];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const float* q = src + (long long)(sp + u * kReduceWarps) * split_stride;
+          if constexpr (V == 4) {
+            const float4 f = __ldg(reinterpret_cast<const float4*>(q));
+            r[u][0] = f.x, r[u][1] = f.y, r[u][2] = f.z, r[u][3] = f.w;
+          } else {
+            r[u][0] = __ldg(q);
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+#pragma unroll
+          for (int v = 0; v < V; ++v) acc[v] += r[u][v];
+      }
+      for (; sp < rp.nsplit; sp += kReduceWarps) {
+        const float* q = src + (long long)sp * split_stride;
+        if constexpr (V == 4) {
+          const float4 f = __ldg(reinterpret_cast<const float4*>(q));
+          acc[0] += f.x, acc[1] += f.y, acc[2] += f.z, acc[3] += f.w;
+        } else {
+          acc[0] += __ldg(q);
+        }
+      }
+    }
+#pragma unroll
+    for (int v = 0; v < V; ++v) part[w][lane * V + v] = acc[v];
+    __syncthreads();
+    // thread t finalises output o0 + t (t < 32 * V)
+    for (int t = threadIdx.x; t < 32 * V; t += 32 * kReduceWarps) {
+      const long long io = o0 + t;
+      if (io < total) {
+        float sum = part[0][t];
+#pragma unroll
+        for (int j = 1; j < kReduceWarps; ++j) sum += part[j][t];
+        const int k = (int)(io % rp.K);
+        const long long r = io / rp.K;
+        const int c = (int)(r % rp.C);
+        const int tap = (int)(r / rp.C);
+        const long long o = ((long long)k * rp.C + c) * RS + tap;
+        if constexpr (DT == 0)
+          static_cast<float*>(rp.dw)[o] = sum;
+        else
+          static_cast<__nv_bfloat16*>(rp.dw)[o] = __float2bfloat16_rn(sum);
+      }
     }
     __syncthreads();
   }
@@ -1067,7 +1102,11 @@ cudaError_t launch_wgrad(const WgradPlan& p, int dt, int grid, cudaStream_t st) 
 
 cudaError_t launch_wgrad_reduce(const ReducePlan& rp, int dt, int num_sms, cudaStream_t st) {
   const long long total = (long long)rp.R * rp.S * rp.C * rp.K;
-  long long blocks = (total + 31) / 32;
+  // 16-byte partial reads need every output group of 4 to start on a 16-byte boundary
+  const bool v4 = rp.K % 4 == 0 && rp.c_pad == rp.C && rp.k_pad == rp.K &&
+                  (reinterpret_cast<uintptr_t>(rp.partial) & 15) == 0;
+  const int per_block = 32 * (v4 ? 4 : 1);
+  long long blocks = (total + per_block - 1) / per_block;
   const long long cap = (long long)num_sms * 16;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
@@ -1082,8 +1121,13 @@ cudaError_t launch_wgrad_reduce(const ReducePlan& rp, int dt, int num_sms, cudaS
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  const cudaError_t e = dt == 0 ? cudaLaunchKernelEx(&cfg, wgrad_reduce_kernel<0>, rp)
-                                : cudaLaunchKernelEx(&cfg, wgrad_reduce_kernel<1>, rp);
+  cudaError_t e;
+  if (v4)
+    e = dt == 0 ? cudaLaunchKernelEx(&cfg, wgrad_reduce_kernel<0, 4>, rp)
+                : cudaLaunchKernelEx(&cfg, wgrad_reduce_kernel<1, 4>, rp);
+  else
+    e = dt == 0 ? cudaLaunchKernelEx(&cfg, wgrad_reduce_kernel<0, 1>, rp)
+                : cudaLaunchKernelEx(&cfg, wgrad_reduce_kernel<1, 1>, rp);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
