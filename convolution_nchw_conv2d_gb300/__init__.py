@@ -45,7 +45,8 @@ def lib_path() -> str:
 
 
 EXPORTS = ("conv2d_output_dim", "conv2d_workspace_size", "conv2d_fwd", "conv2d_bwd_data",
-           "conv2d_bwd_filter", "conv2d_fwd_noalloc", "conv2d_device_status", "conv2d_strerror")
+           "conv2d_bwd_filter", "conv2d_fwd_ex", "conv2d_bwd_data_ex", "conv2d_bwd_filter_ex",
+           "conv2d_fwd_noalloc", "conv2d_device_status", "conv2d_strerror")
 
 
 def load_library():
@@ -67,6 +68,13 @@ def load_library():
             f = getattr(lib, name)
             f.argtypes = [i] * 13 + [i, vp, vp, vp, vp, sz, vp]
             f.restype = i
+        fl = ctypes.c_float
+        for name in ("conv2d_fwd_ex", "conv2d_bwd_data_ex"):
+            f = getattr(lib, name)
+            f.argtypes = [i] * 13 + [i, vp, vp, vp, fl, vp, vp, sz, vp]
+            f.restype = i
+        lib.conv2d_bwd_filter_ex.argtypes = [i] * 13 + [i, vp, vp, fl, vp, vp, vp, vp, sz, vp]
+        lib.conv2d_bwd_filter_ex.restype = i
         lib.conv2d_fwd_noalloc.argtypes = [i] * 13 + [i, vp, vp, vp, vp]
         lib.conv2d_fwd_noalloc.restype = i
         lib.conv2d_device_status.argtypes = [vp]
@@ -139,20 +147,33 @@ def _workspace(op, dims, dt, workspace, device):
     return workspace, workspace.numel() * workspace.element_size()
 
 
-def _call(name, dims, dt, a, b, out, workspace, op, stream):
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr() if t is not None else 0)
+
+
+def _check_vec(v, n, like, name):
+    if v is None:
+        return
+    _check_tensor(v, name)
+    if v.dtype != like.dtype or v.numel() != n or v.device != like.device:
+        raise ValueError(f"{name} must be a vector of {n} {like.dtype} values on {like.device}")
+
+
+def _call(name, dims, dt, a, b, out, workspace, op, stream, bias=None, beta=0.0):
+    """Forward / backward-data through the fused-epilogue entry point (bias None and beta 0
+    are the plain op)."""
     ws, wsb = _workspace(op, dims, dt, workspace, out.device)
-    rc = getattr(load_library(), name)(*[int(v) for v in dims], dt,
-                                       ctypes.c_void_p(a.data_ptr()), ctypes.c_void_p(b.data_ptr()),
-                                       ctypes.c_void_p(out.data_ptr()),
-                                       ctypes.c_void_p(ws.data_ptr() if ws is not None else 0),
-                                       ctypes.c_size_t(wsb), _stream_ptr(stream))
+    rc = getattr(load_library(), name + "_ex")(*[int(v) for v in dims], dt, _ptr(a), _ptr(b), _ptr(bias),
+                                               ctypes.c_float(float(beta)), _ptr(out), _ptr(ws),
+                                               ctypes.c_size_t(wsb), _stream_ptr(stream))
     if rc:
         raise Conv2dError(rc, name)
     return out
 
 
-def conv2d_fwd(x, w, pad=0, stride=1, out=None, workspace=None, stream=None):
-    """y = conv2d(x, w): x (N,C,H,W), w (K,C,R,S) -> y (N,K,P,Q), same dtype."""
+def conv2d_fwd(x, w, pad=0, stride=1, out=None, workspace=None, stream=None, bias=None, beta=0.0):
+    """y = conv2d(x, w) (+ bias[k]) (+ beta * y): x (N,C,H,W), w (K,C,R,S) -> y (N,K,P,Q),
+    same dtype.  With beta != 0, `out` holds the values to accumulate onto."""
     import torch
     _check_tensor(x, "x")
     _check_tensor(w, "w")
@@ -164,9 +185,12 @@ def conv2d_fwd(x, w, pad=0, stride=1, out=None, workspace=None, stream=None):
     sh, sw = _pair(stride)
     P, Q = conv2d_output_dim(H, ph, R, sh), conv2d_output_dim(W, pw, S, sw)
     if out is None:
+        if beta != 0.0:
+            raise ValueError("beta != 0 accumulates onto `out`, which must then be given")
         out = torch.empty((N, K, P, Q), dtype=x.dtype, device=x.device)
+    _check_vec(bias, K, x, "bias")
     dims = (N, C, H, W, K, R, S, ph, pw, sh, sw, P, Q)
-    return _call("conv2d_fwd", dims, _dtype_code(x), x, w, out, workspace, OP_FWD, stream)
+    return _call("conv2d_fwd", dims, _dtype_code(x), x, w, out, workspace, OP_FWD, stream, bias, beta)
 
 
 def conv2d_fwd_noalloc(x, w, pad=0, stride=1, out=None, stream=None):
@@ -194,8 +218,9 @@ def conv2d_fwd_noalloc(x, w, pad=0, stride=1, out=None, stream=None):
     return out
 
 
-def conv2d_bwd_data(dy, w, x_hw, pad=0, stride=1, out=None, workspace=None, stream=None):
-    """dx (N,C,H,W) from dy (N,K,P,Q) and w (K,C,R,S); x_hw = (H, W)."""
+def conv2d_bwd_data(dy, w, x_hw, pad=0, stride=1, out=None, workspace=None, stream=None, bias=None, beta=0.0):
+    """dx (N,C,H,W) from dy (N,K,P,Q) and w (K,C,R,S); x_hw = (H, W).  Optional epilogue:
+    + bias[c] (the bias of a deconvolution) + beta * dx (`out` required when beta != 0)."""
     import torch
     _check_tensor(dy, "dy")
     _check_tensor(w, "w")
@@ -207,13 +232,23 @@ def conv2d_bwd_data(dy, w, x_hw, pad=0, stride=1, out=None, workspace=None, stre
     ph, pw = _pair(pad)
     sh, sw = _pair(stride)
     if out is None:
+        if beta != 0.0:
+            raise ValueError("beta != 0 accumulates onto `out`, which must then be given")
         out = torch.empty((N, C, H, W), dtype=dy.dtype, device=dy.device)
+    _check_vec(bias, C, dy, "bias")
     dims = (N, C, H, W, K, R, S, ph, pw, sh, sw, P, Q)
-    return _call("conv2d_bwd_data", dims, _dtype_code(dy), dy, w, out, workspace, OP_BWD_DATA, stream)
+    return _call("conv2d_bwd_data", dims, _dtype_code(dy), dy, w, out, workspace, OP_BWD_DATA, stream,
+                 bias, beta)
 
 
-def conv2d_bwd_filter(x, dy, rs, pad=0, stride=1, out=None, workspace=None, stream=None):
-    """dw (K,C,R,S) from x (N,C,H,W) and dy (N,K,P,Q); rs = (R, S)."""
+def conv2d_bwd_filter(x, dy, rs, pad=0, stride=1, out=None, workspace=None, stream=None, beta=0.0,
+                      db_k=None, db_c=None):
+    """dw (K,C,R,S) from x (N,C,H,W) and dy (N,K,P,Q); rs = (R, S).
+
+    Optional: beta accumulates onto `out` (dw) and onto the bias gradients; db_k (K values)
+    receives sum of dy over (n, p, q) -- the convolution bias gradient; db_c (C values)
+    receives sum of x over (n, h, w) -- the deconvolution bias gradient, x being the
+    deconvolution's output gradient."""
     import torch
     _check_tensor(x, "x")
     _check_tensor(dy, "dy")
@@ -225,16 +260,29 @@ def conv2d_bwd_filter(x, dy, rs, pad=0, stride=1, out=None, workspace=None, stre
     ph, pw = _pair(pad)
     sh, sw = _pair(stride)
     if out is None:
+        if beta != 0.0:
+            raise ValueError("beta != 0 accumulates onto `out`, which must then be given")
         out = torch.empty((K, C, R, S), dtype=x.dtype, device=x.device)
+    _check_vec(db_k, K, x, "db_k")
+    _check_vec(db_c, C, x, "db_c")
     dims = (N, C, H, W, K, R, S, ph, pw, sh, sw, P, Q)
-    return _call("conv2d_bwd_filter", dims, _dtype_code(x), x, dy, out, workspace, OP_BWD_FILTER, stream)
+    dt = _dtype_code(x)
+    ws, wsb = _workspace(OP_BWD_FILTER, dims, dt, workspace, out.device)
+    rc = load_library().conv2d_bwd_filter_ex(*[int(v) for v in dims], dt, _ptr(x), _ptr(dy),
+                                             ctypes.c_float(float(beta)), _ptr(out), _ptr(db_k), _ptr(db_c),
+                                             _ptr(ws), ctypes.c_size_t(wsb), _stream_ptr(stream))
+    if rc:
+        raise Conv2dError(rc, "conv2d_bwd_filter")
+    return out
 
 
-def deconv2d_fwd(inp, wt, out_hw, pad=0, stride=1, out=None, workspace=None, stream=None):
-    """Transposed convolution: inp (N,Ci,Hi,Wi), wt (Ci,Co,R,S) -> (N,Co,Ho,Wo).
+def deconv2d_fwd(inp, wt, out_hw, pad=0, stride=1, out=None, workspace=None, stream=None, bias=None, beta=0.0):
+    """Transposed convolution: inp (N,Ci,Hi,Wi), wt (Ci,Co,R,S) -> (N,Co,Ho,Wo), optionally
+    + bias[co] + beta * out.
 
     Runs conv2d_bwd_data with K = Ci (deconv input channels), C = Co, P = Hi, H = Ho."""
-    return conv2d_bwd_data(inp, wt, out_hw, pad, stride, out=out, workspace=workspace, stream=stream)
+    return conv2d_bwd_data(inp, wt, out_hw, pad, stride, out=out, workspace=workspace, stream=stream,
+                           bias=bias, beta=beta)
 
 
 def conv2d_device_status(stream=None) -> int:

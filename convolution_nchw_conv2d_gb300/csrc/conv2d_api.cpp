@@ -20,6 +20,7 @@ cudaError_t launch_pack_filter(const PackPlan& pp, int dt, cudaStream_t st);
 size_t tap_gemm_smem_bytes(const TapPlan& p);
 cudaError_t launch_wgrad(const WgradPlan& p, int dt, int grid, cudaStream_t st);
 cudaError_t launch_wgrad_reduce(const ReducePlan& rp, int dt, int num_sms, cudaStream_t st);
+cudaError_t launch_chan_sum(const ChanSumPlan& cp, int dt, cudaStream_t st);
 size_t wgrad_smem_bytes(const WgradPlan& p, int dt);
 int tap_gemm_take_error();
 int wgrad_take_error();
@@ -697,6 +698,7 @@ int build_bwd_filter_impl(const Desc& d0, const void* x, const void* dy, void* d
   rp.nsplit = p.nsplit;
   rp.k_pad = d.K;
   rp.c_pad = d.C;
+  rp.beta = 0.f;
   b.grid = (int)std::min<long long>(p.total_tiles, di.sms);
   return CONV2D_OK;
 }
@@ -722,6 +724,13 @@ int check_ptrs(const void* a, const void* b, const void* c, int dt) {
   const uintptr_t m = dt == CONV2D_DTYPE_F32 ? 3 : 1;
   if (((uintptr_t)a & m) || ((uintptr_t)b & m) || ((uintptr_t)c & m)) return CONV2D_ERR_ALIGN;
   return CONV2D_OK;
+}
+
+// Workspace of the bias-gradient sums of conv2d_bwd_filter_ex: fp32 partials per (channel,
+// image) for the K sums over dy and the C sums over x, each region 256-byte aligned.
+size_t align_ws(size_t b) { return (b + 255) & ~size_t(255); }
+size_t chan_sum_bytes(const Desc& d) {
+  return align_ws((size_t)d.K * d.N * sizeof(float)) + align_ws((size_t)d.C * d.N * sizeof(float));
 }
 
 int check_ws(void* ws, size_t have, size_t need) {
@@ -848,7 +857,7 @@ int workspace_size_uncached(int op, const Desc& d, size_t* bytes) {
       if (build_bwd_filter_impl(d, nullptr, nullptr, nullptr, nullptr, di, b2, v[0], v[1]) == CONV2D_OK)
         need = std::max(need, b2.partial_bytes);
     }
-    *bytes = need;
+    *bytes = align_ws(need) + chan_sum_bytes(d);
     return CONV2D_OK;
   }
   return CONV2D_ERR_BAD_OP;
@@ -857,8 +866,8 @@ int workspace_size_uncached(int op, const Desc& d, size_t* bytes) {
 
 extern "C" {
 
-static int run_tap(int op, const Desc& d, const void* src, const void* w, void* dst, void* ws, size_t wsb,
-                   void* stream) {
+static int run_tap(int op, const Desc& d, const void* src, const void* w, const void* bias, float beta, void* dst,
+                   void* ws, size_t wsb, void* stream) {
   int rc = validate(d);
   if (rc) return rc;
   rc = check_ptrs(src, w, dst, d.dt);
@@ -874,6 +883,9 @@ static int run_tap(int op, const Desc& d, const void* src, const void* w, void* 
   }
   rc = check_ws(ws, wsb, b.pack_bytes);
   if (rc) return rc;
+  if (bias != nullptr && ((uintptr_t)bias & (d.dt == CONV2D_DTYPE_F32 ? 3 : 1))) return CONV2D_ERR_ALIGN;
+  b.p.bias = bias;  // per-call epilogue inputs (not part of the cached plan)
+  b.p.beta = beta;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (b.pack_bytes) {
     rc = launch_err(launch_pack_filter(b.pp, d.dt, st));
@@ -886,19 +898,40 @@ int conv2d_fwd(int N, int C, int H, int W, int K, int R, int S, int pad_h, int p
                int stride_w, int P, int Q, int dtype, const void* x, const void* w, void* y, void* workspace,
                size_t workspace_bytes, void* stream) {
   const Desc d{N, C, H, W, K, R, S, pad_h, pad_w, stride_h, stride_w, P, Q, dtype};
-  return run_tap(CONV2D_OP_FWD, d, x, w, y, workspace, workspace_bytes, stream);
+  return run_tap(CONV2D_OP_FWD, d, x, w, nullptr, 0.f, y, workspace, workspace_bytes, stream);
+}
+
+int conv2d_fwd_ex(int N, int C, int H, int W, int K, int R, int S, int pad_h, int pad_w, int stride_h,
+                  int stride_w, int P, int Q, int dtype, const void* x, const void* w, const void* bias, float beta,
+                  void* y, void* workspace, size_t workspace_bytes, void* stream) {
+  const Desc d{N, C, H, W, K, R, S, pad_h, pad_w, stride_h, stride_w, P, Q, dtype};
+  return run_tap(CONV2D_OP_FWD, d, x, w, bias, beta, y, workspace, workspace_bytes, stream);
 }
 
 int conv2d_bwd_data(int N, int C, int H, int W, int K, int R, int S, int pad_h, int pad_w, int stride_h,
                     int stride_w, int P, int Q, int dtype, const void* dy, const void* w, void* dx,
                     void* workspace, size_t workspace_bytes, void* stream) {
   const Desc d{N, C, H, W, K, R, S, pad_h, pad_w, stride_h, stride_w, P, Q, dtype};
-  return run_tap(CONV2D_OP_BWD_DATA, d, dy, w, dx, workspace, workspace_bytes, stream);
+  return run_tap(CONV2D_OP_BWD_DATA, d, dy, w, nullptr, 0.f, dx, workspace, workspace_bytes, stream);
+}
+
+int conv2d_bwd_data_ex(int N, int C, int H, int W, int K, int R, int S, int pad_h, int pad_w, int stride_h,
+                       int stride_w, int P, int Q, int dtype, const void* dy, const void* w, const void* bias,
+                       float beta, void* dx, void* workspace, size_t workspace_bytes, void* stream) {
+  const Desc d{N, C, H, W, K, R, S, pad_h, pad_w, stride_h, stride_w, P, Q, dtype};
+  return run_tap(CONV2D_OP_BWD_DATA, d, dy, w, bias, beta, dx, workspace, workspace_bytes, stream);
 }
 
 int conv2d_bwd_filter(int N, int C, int H, int W, int K, int R, int S, int pad_h, int pad_w, int stride_h,
                       int stride_w, int P, int Q, int dtype, const void* x, const void* dy, void* dw,
                       void* workspace, size_t workspace_bytes, void* stream) {
+  return conv2d_bwd_filter_ex(N, C, H, W, K, R, S, pad_h, pad_w, stride_h, stride_w, P, Q, dtype, x, dy, 0.f, dw,
+                              nullptr, nullptr, workspace, workspace_bytes, stream);
+}
+
+int conv2d_bwd_filter_ex(int N, int C, int H, int W, int K, int R, int S, int pad_h, int pad_w, int stride_h,
+                         int stride_w, int P, int Q, int dtype, const void* x, const void* dy, float beta, void* dw,
+                         void* db_k, void* db_c, void* workspace, size_t workspace_bytes, void* stream) {
   const Desc d{N, C, H, W, K, R, S, pad_h, pad_w, stride_h, stride_w, P, Q, dtype};
   int rc = validate(d);
   if (rc) return rc;
@@ -913,12 +946,34 @@ int conv2d_bwd_filter(int N, int C, int H, int W, int K, int R, int S, int pad_h
     if (rc) return rc;
     g_wgrad_plans.put(key, b);
   }
-  rc = check_ws(workspace, workspace_bytes, b.partial_bytes);
+  const bool sums = db_k != nullptr || db_c != nullptr;
+  const size_t sum0 = align_ws(b.partial_bytes);
+  rc = check_ws(workspace, workspace_bytes, sums ? sum0 + chan_sum_bytes(d) : b.partial_bytes);
   if (rc) return rc;
+  const uintptr_t am = d.dt == CONV2D_DTYPE_F32 ? 3 : 1;
+  if (((uintptr_t)db_k & am) || ((uintptr_t)db_c & am)) return CONV2D_ERR_ALIGN;
+  b.rp.beta = beta;  // per-call (not part of the cached plan)
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   rc = launch_err(launch_wgrad(b.p, d.dt, b.grid, st));
   if (rc) return rc;
-  return launch_err(launch_wgrad_reduce(b.rp, d.dt, di.sms, st));
+  rc = launch_err(launch_wgrad_reduce(b.rp, d.dt, di.sms, st));
+  if (rc) return rc;
+  uint8_t* wsb = static_cast<uint8_t*>(workspace) + sum0;
+  if (db_k != nullptr) {
+    // conv bias gradient: sum of dy over images and output pixels, per output channel k
+    const ChanSumPlan cp{dy, db_k, reinterpret_cast<float*>(wsb), d.N, d.K, (long long)d.P * d.Q, beta};
+    rc = launch_err(launch_chan_sum(cp, d.dt, st));
+    if (rc) return rc;
+  }
+  if (db_c != nullptr) {
+    // deconvolution bias gradient: sum of x (the deconvolution's output gradient) over images
+    // and pixels, per channel c
+    const ChanSumPlan cp{x, db_c, reinterpret_cast<float*>(wsb + align_ws((size_t)d.K * d.N * sizeof(float))), d.N,
+                         d.C, (long long)d.H * d.W, beta};
+    rc = launch_err(launch_chan_sum(cp, d.dt, st));
+    if (rc) return rc;
+  }
+  return CONV2D_OK;
 }
 
 int conv2d_fwd_noalloc(int N, int C, int H, int W, int K, int R, int S, int pad_h, int pad_w, int stride_h,

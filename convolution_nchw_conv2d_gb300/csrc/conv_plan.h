@@ -53,6 +53,8 @@ constexpr int kMaxTaps = 256;    // R * S
 struct TapPlan {
   const void* src;       // x (forward) or dy (backward-data), NCHW
   void* dst;             // y or dx, NCHW
+  const void* bias;      // optional, one value per destination channel (NULL: none)
+  float beta;            // dst = D + bias + beta * dst (beta 0: dst is not read)
   const void* wpack;     // packed filter, see pack layout in conv_tap_gemm.cu
   int N, Cs, Hs, Ws;     // source tensor
   int Cd, Hd, Wd;        // destination tensor
@@ -188,6 +190,18 @@ struct ReducePlan {
   void* dw;              // KCRS, fp32 or bf16
   int K, C, R, S;
   int nsplit, k_pad, c_pad;
+  float beta;            // dw = sum + beta * dw (beta 0: dw is not read)
+};
+
+// Per-channel sum of an NCHW-like tensor t (N, Ch, HW): out[ch] = sum_{n, i} t[n, ch, i]
+// (+ beta * out[ch]), as fixed-order partials part[ch * N + n] and a final pass.
+struct ChanSumPlan {
+  const void* t;
+  void* out;
+  float* part;           // Ch * N fp32 (workspace)
+  int N, Ch;
+  long long HW;
+  float beta;
 };
 
 }  // namespace cg3

@@ -59,11 +59,24 @@ __device__ __forceinline__ TileCoord decode_tile(const TapPlan& p, long long t) 
 }
 
 template <int DT>
-__device__ __forceinline__ void store_out(void* dst, long long idx, uint32_t bits) {
+__device__ __forceinline__ float load_elem(const void* base, long long idx) {
+  if constexpr (DT == 0)
+    return static_cast<const float*>(base)[idx];
+  else
+    return __bfloat162float(static_cast<const __nv_bfloat16*>(base)[idx]);
+}
+
+// Epilogue of one output element: D (+ bias of its channel) (+ beta * the old value), in fp32,
+// then stored (bf16: rounded to nearest even).
+template <int DT>
+__device__ __forceinline__ void store_out(const TapPlan& p, long long idx, int ch, uint32_t bits) {
+  float v = __uint_as_float(bits);
+  if (p.bias != nullptr) v += load_elem<DT>(p.bias, ch);
+  if (p.beta != 0.f) v += p.beta * load_elem<DT>(p.dst, idx);
   if constexpr (DT == 0) {
-    static_cast<float*>(dst)[idx] = __uint_as_float(bits);
+    static_cast<float*>(p.dst)[idx] = v;
   } else {
-    static_cast<__nv_bfloat16*>(dst)[idx] = __float2bfloat16_rn(__uint_as_float(bits));
+    static_cast<__nv_bfloat16*>(p.dst)[idx] = __float2bfloat16_rn(v);
   }
 }
 
@@ -281,11 +294,11 @@ __global__ void __launch_bounds__(kThreads, 1) tap_gemm_kernel(const __grid_cons
             const int lim = nvalid - 16 * ci;
             if (lim >= 16) {
 #pragma unroll
-              for (int j = 0; j < 16; ++j) store_out<DT>(p.dst, ob + j * ostep, ra[j]);
+              for (int j = 0; j < 16; ++j) store_out<DT>(p, ob + j * ostep, nbase + 16 * ci + j, ra[j]);
             } else {
 #pragma unroll
               for (int j = 0; j < 16; ++j)
-                if (j < lim) store_out<DT>(p.dst, ob + j * ostep, ra[j]);
+                if (j < lim) store_out<DT>(p, ob + j * ostep, nbase + 16 * ci + j, ra[j]);
             }
           }
           if (ntaps != 0 && two) tmem_ld_wait();
@@ -296,11 +309,11 @@ __global__ void __launch_bounds__(kThreads, 1) tap_gemm_kernel(const __grid_cons
             const int lim = nvalid - 16 * (ci + 1);
             if (lim >= 16) {
 #pragma unroll
-              for (int j = 0; j < 16; ++j) store_out<DT>(p.dst, ob + j * ostep, rb[j]);
+              for (int j = 0; j < 16; ++j) store_out<DT>(p, ob + j * ostep, nbase + 16 * (ci + 1) + j, rb[j]);
             } else {
 #pragma unroll
               for (int j = 0; j < 16; ++j)
-                if (j < lim) store_out<DT>(p.dst, ob + j * ostep, rb[j]);
+                if (j < lim) store_out<DT>(p, ob + j * ostep, nbase + 16 * (ci + 1) + j, rb[j]);
             }
           }
           if (ntaps != 0 && ci + 2 < nchunk) tmem_ld_wait();

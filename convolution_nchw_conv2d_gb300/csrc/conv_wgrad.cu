@@ -1064,14 +1064,76 @@ __global__ void __launch_bounds__(32 * kReduceWarps) wgrad_reduce_kernel(const _
         const int c = (int)(r % rp.C);
         const int tap = (int)(r / rp.C);
         const long long o = ((long long)k * rp.C + c) * RS + tap;
-        if constexpr (DT == 0)
-          static_cast<float*>(rp.dw)[o] = sum;
-        else
-          static_cast<__nv_bfloat16*>(rp.dw)[o] = __float2bfloat16_rn(sum);
+        if constexpr (DT == 0) {
+          float* dwp = static_cast<float*>(rp.dw);
+          if (rp.beta != 0.f) sum += rp.beta * dwp[o];
+          dwp[o] = sum;
+        } else {
+          __nv_bfloat16* dwp = static_cast<__nv_bfloat16*>(rp.dw);
+          if (rp.beta != 0.f) sum += rp.beta * __bfloat162float(dwp[o]);
+          dwp[o] = __float2bfloat16_rn(sum);
+        }
       }
     }
     __syncthreads();
   }
+}
+
+// Per-channel sums (bias gradients).  Block (ch, n) adds t[n, ch, 0 .. HW) -- thread i takes
+// elements i, i + 256, ... in order, then the 256 thread sums are added by a fixed tree --
+// into part[ch * N + n]; the final pass adds the N partials of a channel in order.
+constexpr int kSumThreads = 256;
+template <int DT>
+__global__ void __launch_bounds__(kSumThreads) chan_sum_partial_kernel(const __grid_constant__ ChanSumPlan cp) {
+  __shared__ float red[kSumThreads];
+  const long long b = blockIdx.x;
+  const int n = (int)(b % cp.N);
+  const int ch = (int)(b / cp.N);
+  const long long base = ((long long)n * cp.Ch + ch) * cp.HW;
+  float acc = 0.f;
+  for (long long i = threadIdx.x; i < cp.HW; i += kSumThreads) {
+    if constexpr (DT == 0)
+      acc += static_cast<const float*>(cp.t)[base + i];
+    else
+      acc += __bfloat162float(static_cast<const __nv_bfloat16*>(cp.t)[base + i]);
+  }
+  red[threadIdx.x] = acc;
+  __syncthreads();
+  for (int h = kSumThreads / 2; h > 0; h >>= 1) {
+    if ((int)threadIdx.x < h) red[threadIdx.x] += red[threadIdx.x + h];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) cp.part[(long long)ch * cp.N + n] = red[0];
+}
+
+template <int DT>
+__global__ void __launch_bounds__(kSumThreads) chan_sum_final_kernel(const __grid_constant__ ChanSumPlan cp) {
+  const int ch = blockIdx.x * kSumThreads + threadIdx.x;
+  if (ch >= cp.Ch) return;
+  float sum = 0.f;
+  for (int n = 0; n < cp.N; ++n) sum += cp.part[(long long)ch * cp.N + n];
+  if constexpr (DT == 0) {
+    float* o = static_cast<float*>(cp.out);
+    if (cp.beta != 0.f) sum += cp.beta * o[ch];
+    o[ch] = sum;
+  } else {
+    __nv_bfloat16* o = static_cast<__nv_bfloat16*>(cp.out);
+    if (cp.beta != 0.f) sum += cp.beta * __bfloat162float(o[ch]);
+    o[ch] = __float2bfloat16_rn(sum);
+  }
+}
+
+cudaError_t launch_chan_sum(const ChanSumPlan& cp, int dt, cudaStream_t st) {
+  const unsigned blocks = (unsigned)((long long)cp.Ch * cp.N);
+  const unsigned fblocks = (unsigned)((cp.Ch + kSumThreads - 1) / kSumThreads);
+  if (dt == 0) {
+    chan_sum_partial_kernel<0><<<blocks, kSumThreads, 0, st>>>(cp);
+    chan_sum_final_kernel<0><<<fblocks, kSumThreads, 0, st>>>(cp);
+  } else {
+    chan_sum_partial_kernel<1><<<blocks, kSumThreads, 0, st>>>(cp);
+    chan_sum_final_kernel<1><<<fblocks, kSumThreads, 0, st>>>(cp);
+  }
+  return cudaGetLastError();
 }
 
 size_t wgrad_smem_bytes(const WgradPlan& p, int dt) {

@@ -123,6 +123,48 @@ int conv2d_bwd_filter(int N, int C, int H, int W, int K, int R, int S,
                       const void *x, const void *dy, void *dw,
                       void *workspace, size_t workspace_bytes, void *stream);
 
+/* Fused epilogues (page "mkldnn_deconvolution.cc": the deconvolution forward takes an
+ * optional bias and an output request that either writes or adds to the output
+ * (MKLDNNDeconvFwd::Execute, OutMem(req, ...)); its backward-weights pass also produces
+ * the bias gradient (ScheduleBwdWeights: bias_req, BiasGradMem).  cuDNN's alpha/beta
+ * scaling of the C# examples page is the same output rule with alpha = 1.)
+ *
+ * Each result element is computed in fp32 as  D + bias[channel] + beta * old  and then
+ * stored (bf16: rounded to nearest even), where D is the op's sum above, `old` the value
+ * the output held before the call (read only when beta != 0), and the bias term applies
+ * only where a bias pointer is given.  beta = 0 overwrites (the plain entry points);
+ * beta = 1 accumulates (MXNet kAddTo).  bias / db vectors have the tensor dtype, are
+ * device pointers aligned to the element size, and must not alias any other argument.
+ *
+ * conv2d_fwd_ex:       y = conv(x, w) + bias[k] + beta * y;            bias: K values or NULL.
+ * conv2d_bwd_data_ex:  dx = bwd_data(dy, w) + bias[c] + beta * dx;      bias: C values or NULL
+ *                      (the bias of a deconvolution, whose output is dx).
+ * conv2d_bwd_filter_ex: dw = bwd_filter(x, dy) + beta * dw, and optionally
+ *                      db_k[k] = sum_{n,p,q} dy[n,k,p,q] + beta * db_k[k]  (convolution bias
+ *                                gradient; K values), and
+ *                      db_c[c] = sum_{n,h,w} x[n,c,h,w] + beta * db_c[c]   (deconvolution bias
+ *                                gradient: x is the deconvolution's output gradient; C values).
+ *                      Either may be NULL.  Sums are in fixed order (deterministic).  When a
+ *                      bias gradient is requested the workspace must have the full size
+ *                      conv2d_workspace_size(CONV2D_OP_BWD_FILTER, ...) reports; otherwise the
+ *                      split partials alone suffice.
+ * Same descriptors, workspace rules and error codes as the plain entry points (which are
+ * these with bias = NULL, beta = 0, db_k = db_c = NULL). */
+int conv2d_fwd_ex(int N, int C, int H, int W, int K, int R, int S,
+                  int pad_h, int pad_w, int stride_h, int stride_w, int P, int Q, int dtype,
+                  const void *x, const void *w, const void *bias, float beta, void *y,
+                  void *workspace, size_t workspace_bytes, void *stream);
+
+int conv2d_bwd_data_ex(int N, int C, int H, int W, int K, int R, int S,
+                       int pad_h, int pad_w, int stride_h, int stride_w, int P, int Q, int dtype,
+                       const void *dy, const void *w, const void *bias, float beta, void *dx,
+                       void *workspace, size_t workspace_bytes, void *stream);
+
+int conv2d_bwd_filter_ex(int N, int C, int H, int W, int K, int R, int S,
+                         int pad_h, int pad_w, int stride_h, int stride_w, int P, int Q, int dtype,
+                         const void *x, const void *dy, float beta, void *dw, void *db_k, void *db_c,
+                         void *workspace, size_t workspace_bytes, void *stream);
+
 /* Forward without any workspace argument, for callers that cannot allocate device
  * memory: for example code whose device memory is entirely owned by another runtime's
  * pool, or a latency-critical path that must never call cudaMalloc (which can

@@ -4,10 +4,11 @@ Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
 ``bench.py`` may import this package.  The product (``convolution_nchw_conv2d_gb300``)
 never imports it and shares no code with it.
 
-The arithmetic lives in ``conv2d_oracle.c`` (plain C, fp64, gather form,
-OpenMP over output elements).  This module only compiles it with gcc and
-marshals numpy arrays through ctypes.  Inputs of any float dtype are widened
-exactly to fp64 before the call.
+The convolution arithmetic lives in ``conv2d_oracle.c`` (plain C, fp64, gather
+form, OpenMP over output elements); this module compiles it with gcc and marshals
+numpy arrays through ctypes.  The fused epilogues (bias, beta) and the per-channel
+bias-gradient sums are written here directly in fp64 numpy on top of those ops.
+Inputs of any float dtype are widened exactly to fp64 before the call.
 
 Citations (page titles): Apache SystemDS ``LibMatrixCuDNNConvolutionAlgorithm.java``
 (descriptor integers, NCHW / KCRS layouts, cross-correlation, dilation 1);
@@ -159,6 +160,52 @@ def deconv2d_fwd_scatter(inp, wt, out_hw, pad=0, stride=1) -> np.ndarray:
     out = np.empty((N, Co, Ho, Wo), dtype=np.float64)
     _load().oracle_deconv2d_fwd_scatter(_ptr(inp), _ptr(wt), _ptr(out),
                                         N, Ci, Hi, Wi, Co, R, S, ph, pw, sh, sw, Ho, Wo)
+    return out
+
+
+# ------------------------------------------------------------------ fused epilogues
+# Page "mkldnn_deconvolution.cc": the deconvolution forward adds an optional bias per output
+# channel and either writes or adds to its output (MKLDNNDeconvFwd::Execute, OutMem(req));
+# its backward-weights pass also yields the bias gradient (ScheduleBwdWeights, BiasGradMem).
+# The rule for every output element is  D + bias[channel] + beta * old  (beta 0 writes,
+# beta 1 adds), written out below on top of the plain ops, in fp64.
+
+def _epilogue(d, bias, beta, old, channel_axis):
+    out = np.array(d, dtype=np.float64, copy=True)
+    if bias is not None:
+        b = _f64(bias).reshape(-1)
+        shape = [1] * out.ndim
+        shape[channel_axis] = b.shape[0]
+        out = out + b.reshape(shape)
+    if beta != 0.0:
+        out = out + float(beta) * _f64(old)
+    return out
+
+
+def conv2d_fwd_ex(x, w, bias=None, beta=0.0, y_old=None, pad=0, stride=1) -> np.ndarray:
+    """y = conv(x, w) + bias[k] + beta * y_old (bias per output channel k, axis 1 of y)."""
+    return _epilogue(conv2d_fwd(x, w, pad, stride), bias, beta, y_old, 1)
+
+
+def conv2d_bwd_data_ex(dy, w, x_hw, bias=None, beta=0.0, dx_old=None, pad=0, stride=1) -> np.ndarray:
+    """dx = bwd_data(dy, w) + bias[c] + beta * dx_old (bias per channel c of dx: the bias of
+    the deconvolution whose output dx is)."""
+    return _epilogue(conv2d_bwd_data(dy, w, x_hw, pad, stride), bias, beta, dx_old, 1)
+
+
+def conv2d_bwd_filter_ex(x, dy, rs, beta=0.0, dw_old=None, pad=0, stride=1) -> np.ndarray:
+    """dw = bwd_filter(x, dy) + beta * dw_old."""
+    return _epilogue(conv2d_bwd_filter(x, dy, rs, pad, stride), None, beta, dw_old, 0)
+
+
+def channel_sum(t, beta=0.0, old=None) -> np.ndarray:
+    """out[ch] = sum over images and pixels of t[n, ch, :, :] (+ beta * old[ch]) in fp64: the
+    convolution bias gradient for t = dy, the deconvolution bias gradient for t = its output
+    gradient."""
+    t = _f64(t)
+    out = t.sum(axis=(0, 2, 3))
+    if beta != 0.0:
+        out = out + float(beta) * _f64(old)
     return out
 
 

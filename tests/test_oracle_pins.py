@@ -315,3 +315,116 @@ def test_pins_catch_planted_fwd_mistake(mistake):
 @pytest.mark.parametrize("mistake", ["swap_rs", "stride_ignored"])
 def test_pins_catch_planted_bwd_data_mistake(mistake):
     assert not _pins_pass(_py_fwd, lambda *a: _py_bwd_data(*a, mistake=mistake))
+
+
+# --------------------------------------------------------------------------- fused epilogues
+# Page "mkldnn_deconvolution.cc": optional bias on the deconvolution output, output request
+# write / add-to, bias gradient in the backward-weights pass.  Pinned by closed forms (zero
+# operands), by the derivative identity linking a bias to its gradient, and by PyTorch CPU
+# fp64 (conv2d / conv_transpose2d with bias).
+EPI = (2, 3, 5, 7, 4, 3, 2, 1, 0, 2, 1)  # N C H W K R S ph pw sh sw: no two sizes equal
+
+
+def _epi_shapes():
+    N, C, H, W, K, R, S, ph, pw, sh, sw = EPI
+    return N, C, H, W, K, R, S, ph, pw, sh, sw, oracle.output_dim(H, ph, R, sh), oracle.output_dim(W, pw, S, sw)
+
+
+def test_epilogue_closed_forms_with_zero_operands():
+    N, C, H, W, K, R, S, ph, pw, sh, sw, P, Q = _epi_shapes()
+    x = RNG.standard_normal((N, C, H, W))
+    dy = RNG.standard_normal((N, K, P, Q))
+    bk, bc = RNG.standard_normal(K), RNG.standard_normal(C)
+    y0, dx0 = RNG.standard_normal((N, K, P, Q)), RNG.standard_normal((N, C, H, W))
+    dw0 = RNG.standard_normal((K, C, R, S))
+    wz = np.zeros((K, C, R, S))
+    y = oracle.conv2d_fwd_ex(x, wz, bk, 0.5, y0, (ph, pw), (sh, sw))
+    for n, k, p, q in itertools.product(range(N), range(K), range(P), range(Q)):
+        assert y[n, k, p, q] == bk[k] + 0.5 * y0[n, k, p, q]
+    dx = oracle.conv2d_bwd_data_ex(dy, wz, (H, W), bc, 1.0, dx0, (ph, pw), (sh, sw))
+    for n, c, h, w in itertools.product(range(N), range(C), range(H), range(W)):
+        assert dx[n, c, h, w] == bc[c] + dx0[n, c, h, w]
+    dw = oracle.conv2d_bwd_filter_ex(x, np.zeros((N, K, P, Q)), (R, S), 2.0, dw0, (ph, pw), (sh, sw))
+    assert np.array_equal(dw, 2.0 * dw0)
+    # beta = 0 never reads the old value (NaN there must not leak)
+    nan_old = np.full((N, K, P, Q), np.nan)
+    assert np.all(np.isfinite(oracle.conv2d_fwd_ex(x, wz, bk, 0.0, nan_old, (ph, pw), (sh, sw))))
+
+
+def _chan_sum_pins(chan_sum):
+    """Closed forms for a per-channel sum over (n, h, w); True if all hold."""
+    ok = True
+    N, Ch, Hh, Ww = 3, 4, 2, 5
+    HW = Hh * Ww
+    t = np.arange(N * Ch * HW, dtype=np.float64).reshape(N, Ch, Hh, Ww)
+    # t[n, ch, i] = (n*Ch + ch)*HW + i, so the sum over n < N, i < HW is
+    # HW^2 * (Ch*N*(N-1)/2 + ch*N) + N*HW*(HW-1)/2
+    want = np.array([HW * HW * (Ch * N * (N - 1) / 2 + ch * N) + N * HW * (HW - 1) / 2 for ch in range(Ch)])
+    got = chan_sum(t)
+    ok &= got.shape == (Ch,) and bool(np.array_equal(got, want))
+    ok &= bool(np.array_equal(chan_sum(np.full((N, Ch, Hh, Ww), 0.25)), np.full(Ch, 0.25 * N * HW)))
+    return ok
+
+
+def test_channel_sum_closed_forms():
+    assert _chan_sum_pins(oracle.channel_sum)
+    old = RNG.standard_normal(4)
+    t = RNG.standard_normal((2, 4, 3, 3))
+    assert np.allclose(oracle.channel_sum(t, 1.0, old), t.sum(axis=(0, 2, 3)) + old, rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("mistake", ["drop_batch", "wrong_axis", "drop_last_row"])
+def test_channel_sum_pins_catch_planted_mistakes(mistake):
+    def bad(t):
+        if mistake == "drop_batch":
+            return t[0].sum(axis=(1, 2))
+        if mistake == "wrong_axis":
+            return t.sum(axis=(1, 2, 3))
+        return t[:, :, :-1, :].sum(axis=(0, 2, 3))
+    assert not _chan_sum_pins(bad)
+
+
+def test_bias_gradient_is_derivative_of_bias():
+    """<conv_ex(x, w, b), dy> is affine in b with slope channel_sum(dy) (convolution bias), and
+    <bwd_data_ex(dy, w, b), g> has slope channel_sum(g) (deconvolution bias, g = its output
+    gradient): finite differences of size 1 are exact in fp64 up to rounding."""
+    N, C, H, W, K, R, S, ph, pw, sh, sw, P, Q = _epi_shapes()
+    x = RNG.standard_normal((N, C, H, W))
+    w = RNG.standard_normal((K, C, R, S))
+    dy = RNG.standard_normal((N, K, P, Q))
+    g = RNG.standard_normal((N, C, H, W))
+    bk, bc = RNG.standard_normal(K), RNG.standard_normal(C)
+    base = np.vdot(oracle.conv2d_fwd_ex(x, w, bk, 0.0, None, (ph, pw), (sh, sw)), dy)
+    db = oracle.channel_sum(dy)
+    for k in range(K):
+        e = bk.copy()
+        e[k] += 1.0
+        slope = np.vdot(oracle.conv2d_fwd_ex(x, w, e, 0.0, None, (ph, pw), (sh, sw)), dy) - base
+        assert abs(slope - db[k]) <= 1e-9 * max(1.0, abs(db[k]))
+    base = np.vdot(oracle.conv2d_bwd_data_ex(dy, w, (H, W), bc, 0.0, None, (ph, pw), (sh, sw)), g)
+    dbc = oracle.channel_sum(g)
+    for c in range(C):
+        e = bc.copy()
+        e[c] += 1.0
+        slope = np.vdot(oracle.conv2d_bwd_data_ex(dy, w, (H, W), e, 0.0, None, (ph, pw), (sh, sw)), g) - base
+        assert abs(slope - dbc[c]) <= 1e-9 * max(1.0, abs(dbc[c]))
+
+
+def test_epilogue_torch_cpu_fp64_witness():
+    torch = pytest.importorskip("torch")
+    import torch.nn.functional as F
+    N, C, H, W, K, R, S, ph, pw, sh, sw, P, Q = _epi_shapes()
+    x = RNG.standard_normal((N, C, H, W))
+    w = RNG.standard_normal((K, C, R, S))
+    dy = RNG.standard_normal((N, K, P, Q))
+    bk, bc = RNG.standard_normal(K), RNG.standard_normal(C)
+    y_ref = F.conv2d(torch.from_numpy(x), torch.from_numpy(w), torch.from_numpy(bk), stride=(sh, sw),
+                     padding=(ph, pw)).numpy()
+    y = oracle.conv2d_fwd_ex(x, w, bk, 0.0, None, (ph, pw), (sh, sw))
+    assert np.max(np.abs(y - y_ref)) <= 1e-12 * max(1.0, np.max(np.abs(y_ref)))
+    # deconvolution with bias: conv_transpose2d(dy, w as (in=K, out=C), bias over C)
+    outpad = (H - ((P - 1) * sh - 2 * ph + R), W - ((Q - 1) * sw - 2 * pw + S))
+    d_ref = F.conv_transpose2d(torch.from_numpy(dy), torch.from_numpy(w), torch.from_numpy(bc),
+                               stride=(sh, sw), padding=(ph, pw), output_padding=outpad).numpy()
+    d = oracle.conv2d_bwd_data_ex(dy, w, (H, W), bc, 0.0, None, (ph, pw), (sh, sw))
+    assert np.max(np.abs(d - d_ref)) <= 1e-12 * max(1.0, np.max(np.abs(d_ref)))

@@ -200,3 +200,84 @@ def test_stream_argument_is_honoured(cg):
 
 def test_timeout_flag_clear_after_normal_runs(cg):
     assert cg.conv2d_device_status() == 0
+
+
+# ------------------------------------------------------------------ fused epilogues
+# bias + beta * old on every output, bias gradients over dy (per k) and x (per c).
+EPI_CASES = [
+    (2, 3, 7, 9, 5, 3, 2, 1, 0, 1, 1),
+    (1, 33, 9, 9, 40, 3, 3, 1, 1, 1, 1),
+    (2, 64, 16, 16, 64, 3, 3, 1, 1, 1, 1),   # backward-filter row-tap sharing
+    (2, 8, 8, 8, 4, 4, 4, 1, 1, 2, 2),
+]
+
+
+def _check_plain(pb, got, ref, scale, length, what):
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    assert np.all(np.isfinite(got)), f"{what}: non-finite output"
+    if pb.dtype == "f32":
+        tol = 2e-3 * math.sqrt(length) * scale
+        err = float(np.abs(got - ref).max(initial=0.0))
+        assert err <= tol, f"{what}: max|err| {err:.3e} > {tol:.3e}"
+    else:
+        den = float(np.linalg.norm(ref))
+        rel = float(np.linalg.norm(got - ref)) / den if den > 0 else float(np.linalg.norm(got))
+        assert rel <= 1e-2, f"{what}: relative-to-norm error {rel:.3e} > 1e-2"
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("case", EPI_CASES)
+def test_fused_epilogue_parity(cg, case, dtype):
+    N, C, H, Wd, K, R, S, ph, pw, sh, sw = case
+    pb = W.Conv2dProblem(N, C, H, Wd, K, R, S, ph, pw, sh, sw, dtype)
+    x, w, dy = W.random_problem_inputs(pb, 9100 + EPI_CASES.index(case))
+    tdt = x.dtype
+    g = torch.Generator().manual_seed(9200 + EPI_CASES.index(case))
+    bk = torch.randn(K, generator=g).to(tdt)
+    bc = torch.randn(C, generator=g).to(tdt)
+    y0 = torch.randn(pb.y_shape, generator=g).to(tdt)
+    dx0 = torch.randn(pb.x_shape, generator=g).to(tdt)
+    dw0 = torch.randn(pb.w_shape, generator=g).to(tdt)
+    dbk0 = torch.randn(K, generator=g).to(tdt)
+    dbc0 = torch.randn(C, generator=g).to(tdt)
+    pad, st = (ph, pw), (sh, sw)
+    xd, wd, dyd = x.to(DEV), w.to(DEV), dy.to(DEV)
+    amax = lambda t: float(t.abs().max())
+
+    y = y0.to(DEV)
+    cg.conv2d_fwd(xd, wd, pad, st, out=y, bias=bk.to(DEV), beta=1.0)
+    dx = dx0.to(DEV)
+    cg.conv2d_bwd_data(dyd, wd, (H, Wd), pad, st, out=dx, bias=bc.to(DEV), beta=0.5)
+    dw, dbk, dbc = dw0.to(DEV), dbk0.to(DEV), dbc0.to(DEV)
+    cg.conv2d_bwd_filter(xd, dyd, (R, S), pad, st, out=dw, beta=1.0, db_k=dbk, db_c=dbc)
+    cg.conv2d_device_status()
+
+    _check_plain(pb, y.double().cpu().numpy(), oracle.conv2d_fwd_ex(x, w, bk, 1.0, y0, pad, st),
+                 amax(x) * amax(w), C * R * S, f"{case}/fwd_ex/{dtype}")
+    _check_plain(pb, dx.double().cpu().numpy(), oracle.conv2d_bwd_data_ex(dy, w, (H, Wd), bc, 0.5, dx0, pad, st),
+                 amax(dy) * amax(w), K * R * S, f"{case}/bwd_data_ex/{dtype}")
+    _check_plain(pb, dw.double().cpu().numpy(), oracle.conv2d_bwd_filter_ex(x, dy, (R, S), 1.0, dw0, pad, st),
+                 amax(x) * amax(dy), N * pb.P * pb.Q, f"{case}/bwd_filter_ex/{dtype}")
+    _check_plain(pb, dbk.double().cpu().numpy(), oracle.channel_sum(dy, 1.0, dbk0),
+                 amax(dy), N * pb.P * pb.Q, f"{case}/db_k/{dtype}")
+    _check_plain(pb, dbc.double().cpu().numpy(), oracle.channel_sum(x, 1.0, dbc0),
+                 amax(x), N * H * Wd, f"{case}/db_c/{dtype}")
+
+
+def test_bias_gradient_resnet_workload(cg):
+    """Bias gradients at the full ResNet 3x3 size (every channel, exact fp64 reference)."""
+    wl = W.WORKLOADS["resnet3x3"]
+    pb = wl.problem
+    x, w, dy = W.make_inputs(wl)
+    K, C = pb.K, pb.C
+    dbk = _poisoned((K,), x.dtype)
+    dbc = _poisoned((C,), x.dtype)
+    dw = _poisoned(pb.w_shape, x.dtype)
+    cg.conv2d_bwd_filter(x.to(DEV), dy.to(DEV), (pb.R, pb.S), (pb.pad_h, pb.pad_w), (pb.stride_h, pb.stride_w),
+                         out=dw, db_k=dbk, db_c=dbc)
+    cg.conv2d_device_status()
+    for got, t, length in ((dbk, dy, pb.N * pb.P * pb.Q), (dbc, x, pb.N * pb.H * pb.W)):
+        ref = oracle.channel_sum(t)
+        err = float(np.abs(got.double().cpu().numpy() - ref).max())
+        assert err <= 2e-3 * math.sqrt(length) * float(t.abs().max())
