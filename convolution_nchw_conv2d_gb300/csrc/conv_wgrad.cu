@@ -432,8 +432,10 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_kernel(const __grid_constan
         const int kbase = wt.nt * p.NK;
         const int c_lo = tile_c_lo(p, wt.mt0);
         const int nch_x = p.C - c_lo < p.xch ? p.C - c_lo : p.xch;  // ring rows with real channels
-        long long next_row = (lbeg + p.delta) / p.WL;  // first linear row not loaded for this tile
-        long long next_dy_row = lbeg / p.WL - (p.TRU - 1);  // first dy row not loaded (row ring)
+        // Row bookkeeping in 32 bits with multiply-high divisions (positions and rows < 2^31):
+        // the producers' issue time is on the pipeline's critical path.
+        int next_row = (int)fdiv((uint32_t)(lbeg + p.delta), p.fd_WL);  // first x row not loaded
+        int next_dy_row = (int)fdiv((uint32_t)lbeg, p.fd_WL) - (p.TRU - 1);  // first dy row not loaded
         int s_local = 0;
         for (long long l0 = lbeg; l0 < lend; l0 += KB, ++counter, ++s_local) {
           const int stage = (int)(counter % S);
@@ -465,17 +467,17 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_kernel(const __grid_constan
             // before the stage to its last position; one tensor copy per row (NK channels,
             // [chunk][k][CHUNK]); rows before the first image, past the last one, or past
             // the output height read as zeros.
-            const long long rdB = (l0 + KB - 1) / p.WL;
-            const int nrows = next_dy_row <= rdB ? (int)(rdB - next_dy_row + 1) : 0;
+            const int rdB = (int)fdiv((uint32_t)(l0 + KB - 1), p.fd_WL);
+            const int nrows = next_dy_row <= rdB ? rdB - next_dy_row + 1 : 0;
             const uint32_t rbytes = (uint32_t)(p.WL * p.NK * ESZ);
             for (int it = gtid; it < nrows; it += kProdThreads) {
-              const long long R = next_dy_row + it;
-              int n = 0, e = (int)R;  // R < 0: a row before the tensor
+              const int R = next_dy_row + it;
+              int n = 0, e = R, slot = R + p.NRd;  // R < 0: a row before the tensor (R > -NRd)
               if (R >= 0) {
-                n = (int)(R / p.EL);
-                e = (int)(R - (long long)n * p.EL);
+                n = (int)fdiv((uint32_t)R, p.fd_EL);
+                e = R - n * p.EL;
+                slot = R - (int)fdiv((uint32_t)R, p.fd_NRd) * p.NRd;
               }
-              const int slot = (int)(((R % p.NRd) + p.NRd) % p.NRd);
               mbar_expect_tx(fb, rbytes);
               tma_load_5d(a0 + (uint32_t)slot * rbytes, &p.tm_dyr, 0, kbase, 0, e, n, fb);
             }
@@ -503,21 +505,20 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_kernel(const __grid_constan
             // x: the linear rows holding this stage's slots that are not loaded yet (one tensor
             // copy per (row, plane, 32 channels)); rows past the tensor read as zeros.
             {
-              const long long Llast = l0 + KB + p.max_off - 1;
-              const long long rB = (Llast + p.delta) / p.WL;
+              const int rB = (int)fdiv((uint32_t)(l0 + KB + p.max_off - 1 + p.delta), p.fd_WL);
               if (next_row <= rB) {
-                const int nrows = (int)(rB - next_row + 1);
+                const int nrows = rB - next_row + 1;
                 const int ncg = p.xr / 32;
                 const int items = nrows * p.npl * ncg;
                 for (int it = gtid; it < items; it += kProdThreads) {
                   const int cg = it % ncg;
                   const int rest = it / ncg;
                   const int pl = rest % p.npl;
-                  const long long R = next_row + rest / p.npl;
-                  const int n = (int)(R / p.EL);
-                  const int e = (int)(R - (long long)n * p.EL);
+                  const int R = next_row + rest / p.npl;
+                  const int n = (int)fdiv((uint32_t)R, p.fd_EL);
+                  const int e = R - n * p.EL;
                   const int h = e * p.pl_step_h + p.pl_off_h[pl];
-                  const int rs = (int)(R % p.NR);
+                  const int rs = R - (int)fdiv((uint32_t)R, p.fd_NR) * p.NR;
                   const uint32_t dst = ring + (uint32_t)(((rs * p.npl + pl) * p.xr + 32 * cg) * p.WLx * ESZ);
                   mbar_expect_tx(fb, (uint32_t)(32 * p.WLx * ESZ));
                   tma_load_4d(dst, &p.tm_x, p.pl_off_w[pl] - p.delta, h, c_lo + 32 * cg, n, fb);
