@@ -211,6 +211,47 @@ def run_ours(args, rank, world):
         torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
         step_ms = float(tt.item())
 
+    # ---- fused epilogues (bias + add-to on forward, bias gradients on backward-filter),
+    # timed like the step's ops but outside it
+    bias_k = torch.randn(pb.K, generator=torch.Generator().manual_seed(5)).to(x.dtype).to(dev)
+    dbk = torch.empty(pb.K, dtype=x.dtype, device=dev)
+    dbc = torch.empty(pb.C, dtype=x.dtype, device=dev)
+    wsz_f = cg.conv2d_workspace_size(2, pb.dims(), dt)
+    ws_f = torch.empty(max(wsz_f, 16), dtype=torch.uint8, device=dev) if wsz_f > ws.numel() else ws
+
+    def ex_call(which):
+        if which == "fwd_bias_addto":
+            cg.conv2d_fwd(xd, wd, pad, st, out=y, workspace=ws, stream=stream, bias=bias_k, beta=1.0)
+        else:
+            cg.conv2d_bwd_filter(xd, dyd, (pb.R, pb.S), pad, st, out=dw, workspace=ws_f, stream=stream,
+                                 db_k=dbk, db_c=dbc)
+
+    ex_ms = {}
+    for which in ("fwd_bias_addto", "bwd_filter_with_bias_grads"):
+        for _ in range(args.warmup):
+            flush.zero_()
+            ex_call(which)
+        pairs = []
+        for _ in range(min(K, 50)):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            ex_call(which)
+            b.record(stream)
+            pairs.append((a, b))
+        torch.cuda.synchronize()
+        ex_ms[which] = sum(a.elapsed_time(b) for a, b in pairs) / len(pairs)
+    cg.conv2d_device_status(stream)
+    extra_ms = ex_ms["bwd_filter_with_bias_grads"] - op_ms["bwd_filter"]
+    sum_bytes = (math.prod(pb.y_shape) + math.prod(pb.x_shape)) * pb.elem_bytes()  # dy and x read once
+    fused = {"fwd_bias_addto_ms": round(ex_ms["fwd_bias_addto"], 5),
+             "fwd_ms": round(op_ms["fwd"], 5),
+             "bwd_filter_with_bias_grads_ms": round(ex_ms["bwd_filter_with_bias_grads"], 5),
+             "bwd_filter_ms": round(op_ms["bwd_filter"], 5),
+             "bias_grads_extra_ms": round(extra_ms, 5),
+             "bias_grads_alg_gbs": round(sum_bytes / (extra_ms * 1e-3) / 1e9, 1) if extra_ms > 0 else None,
+             "note": "bias gradients = channel sums of dy (per k) and x (per c); alg bytes = |dy| + |x|"}
+
     # ---- end to end: pinned host inputs -> device -> three ops -> host results
     xh, wh, dyh = x.pin_memory(), w.pin_memory(), dy.pin_memory()
     yh = torch.empty(pb.y_shape, dtype=x.dtype).pin_memory()
@@ -275,6 +316,7 @@ def run_ours(args, rank, world):
                 "h2d_bytes_per_step": (nx + nw + ny) * esz, "d2h_bytes_per_step": (ny + nx + nw) * esz,
                 "ms_per_step": round(e2e_ms, 4)},
         "gpu_launches": K * len(OPS) * KERNELS_PER_OP,
+        "fused_epilogue": fused,
         "clocks": clocks,
     }
     if rank == 0 and not args.no_cpu_baseline:

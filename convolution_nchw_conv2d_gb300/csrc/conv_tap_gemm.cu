@@ -66,17 +66,46 @@ __device__ __forceinline__ float load_elem(const void* base, long long idx) {
     return __bfloat162float(static_cast<const __nv_bfloat16*>(base)[idx]);
 }
 
-// Epilogue of one output element: D (+ bias of its channel) (+ beta * the old value), in fp32,
-// then stored (bf16: rounded to nearest even).
-template <int DT>
-__device__ __forceinline__ void store_out(const TapPlan& p, long long idx, int ch, uint32_t bits) {
-  float v = __uint_as_float(bits);
-  if (p.bias != nullptr) v += load_elem<DT>(p.bias, ch);
-  if (p.beta != 0.f) v += p.beta * load_elem<DT>(p.dst, idx);
-  if constexpr (DT == 0) {
-    static_cast<float*>(p.dst)[idx] = v;
-  } else {
-    static_cast<__nv_bfloat16*>(p.dst)[idx] = __float2bfloat16_rn(v);
+// Epilogue of 16 output channels ch0 .. ch0 + 15 (the first `lim` of them exist) at one output
+// position: D (+ bias of the channel) (+ beta * the old value), in fp32, then stored (bf16:
+// rounded to nearest even).  The old values are all read before the first store, so their
+// reads overlap instead of each waiting behind the previous store.
+template <int DT, bool EPI>
+__device__ __forceinline__ void store16(const TapPlan& p, long long ob, long long ostep, int ch0, int lim,
+                                        const uint32_t (&r)[16]) {
+  if constexpr (!EPI) {
+    auto st1 = [&](int j) {
+      if constexpr (DT == 0)
+        static_cast<float*>(p.dst)[ob + j * ostep] = __uint_as_float(r[j]);
+      else
+        static_cast<__nv_bfloat16*>(p.dst)[ob + j * ostep] = __float2bfloat16_rn(__uint_as_float(r[j]));
+    };
+    if (lim >= 16) {
+#pragma unroll
+      for (int j = 0; j < 16; ++j) st1(j);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 16; ++j)
+        if (j < lim) st1(j);
+    }
+    return;
+  }
+  float old[16];
+  if (p.beta != 0.f) {
+#pragma unroll
+    for (int j = 0; j < 16; ++j) old[j] = j < lim ? load_elem<DT>(p.dst, ob + j * ostep) : 0.f;
+  }
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    if (j < lim) {
+      float v = __uint_as_float(r[j]);
+      if (p.bias != nullptr) v += load_elem<DT>(p.bias, ch0 + j);
+      if (p.beta != 0.f) v += p.beta * old[j];
+      if constexpr (DT == 0)
+        static_cast<float*>(p.dst)[ob + j * ostep] = v;
+      else
+        static_cast<__nv_bfloat16*>(p.dst)[ob + j * ostep] = __float2bfloat16_rn(v);
+    }
   }
 }
 
@@ -117,7 +146,8 @@ __device__ __forceinline__ void issue_stage(const uint2* tapo, int tap0, int nta
 
 }  // namespace
 
-template <int DT>
+// EPI: the launch has a bias or beta != 0 (fused epilogue); the plain kernel stores D only.
+template <int DT, bool EPI>
 __global__ void __launch_bounds__(kThreads, 1) tap_gemm_kernel(const __grid_constant__ TapPlan p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   constexpr int ESZ = DT == 0 ? 4 : 2;
@@ -292,14 +322,7 @@ __global__ void __launch_bounds__(kThreads, 1) tap_gemm_kernel(const __grid_cons
           if (valid) {
             const long long ob = obase + (long long)(nbase + 16 * ci) * ostep;
             const int lim = nvalid - 16 * ci;
-            if (lim >= 16) {
-#pragma unroll
-              for (int j = 0; j < 16; ++j) store_out<DT>(p, ob + j * ostep, nbase + 16 * ci + j, ra[j]);
-            } else {
-#pragma unroll
-              for (int j = 0; j < 16; ++j)
-                if (j < lim) store_out<DT>(p, ob + j * ostep, nbase + 16 * ci + j, ra[j]);
-            }
+            store16<DT, EPI>(p, ob, ostep, nbase + 16 * ci, lim < 16 ? lim : 16, ra);
           }
           if (ntaps != 0 && two) tmem_ld_wait();
           if (!two) break;
@@ -307,14 +330,7 @@ __global__ void __launch_bounds__(kThreads, 1) tap_gemm_kernel(const __grid_cons
           if (valid) {
             const long long ob = obase + (long long)(nbase + 16 * (ci + 1)) * ostep;
             const int lim = nvalid - 16 * (ci + 1);
-            if (lim >= 16) {
-#pragma unroll
-              for (int j = 0; j < 16; ++j) store_out<DT>(p, ob + j * ostep, nbase + 16 * (ci + 1) + j, rb[j]);
-            } else {
-#pragma unroll
-              for (int j = 0; j < 16; ++j)
-                if (j < lim) store_out<DT>(p, ob + j * ostep, nbase + 16 * (ci + 1) + j, rb[j]);
-            }
+            store16<DT, EPI>(p, ob, ostep, nbase + 16 * (ci + 1), lim < 16 ? lim : 16, rb);
           }
           if (ntaps != 0 && ci + 2 < nchunk) tmem_ld_wait();
         }
@@ -471,7 +487,14 @@ size_t tap_gemm_smem_bytes(const TapPlan& p) {
   return b + 1024;  // alignment slack for the dynamic base
 }
 
-static std::atomic<int> g_smem_set_0[kMaxDevices], g_smem_set_1[kMaxDevices];
+static std::atomic<int> g_smem_set[2][2][kMaxDevices];
+
+template <int DT, bool EPI>
+cudaError_t launch_tap_gemm_t(const cudaLaunchConfig_t& cfg, const TapPlan& p, size_t smem) {
+  const cudaError_t e = ensure_dyn_smem(tap_gemm_kernel<DT, EPI>, smem, g_smem_set[DT][EPI ? 1 : 0]);
+  if (e != cudaSuccess) return e;
+  return cudaLaunchKernelEx(&cfg, tap_gemm_kernel<DT, EPI>, p);
+}
 
 // Launched with programmatic stream serialization: the kernel's set-up overlaps the filter
 // pack that precedes it in the stream (the producers wait for it before the first copy).
@@ -487,16 +510,12 @@ cudaError_t launch_tap_gemm(const TapPlan& p, int dt, int grid, cudaStream_t st)
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  const bool epi = p.bias != nullptr || p.beta != 0.f;
   cudaError_t e;
-  if (dt == 0) {
-    e = ensure_dyn_smem(tap_gemm_kernel<0>, smem, g_smem_set_0);
-    if (e != cudaSuccess) return e;
-    e = cudaLaunchKernelEx(&cfg, tap_gemm_kernel<0>, p);
-  } else {
-    e = ensure_dyn_smem(tap_gemm_kernel<1>, smem, g_smem_set_1);
-    if (e != cudaSuccess) return e;
-    e = cudaLaunchKernelEx(&cfg, tap_gemm_kernel<1>, p);
-  }
+  if (dt == 0)
+    e = epi ? launch_tap_gemm_t<0, true>(cfg, p, smem) : launch_tap_gemm_t<0, false>(cfg, p, smem);
+  else
+    e = epi ? launch_tap_gemm_t<1, true>(cfg, p, smem) : launch_tap_gemm_t<1, false>(cfg, p, smem);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 

@@ -1081,8 +1081,10 @@ __global__ void __launch_bounds__(32 * kReduceWarps) wgrad_reduce_kernel(const _
 }
 
 // Per-channel sums (bias gradients).  Block (ch, n) adds t[n, ch, 0 .. HW) -- thread i takes
-// elements i, i + 256, ... in order, then the 256 thread sums are added by a fixed tree --
-// into part[ch * N + n]; the final pass adds the N partials of a channel in order.
+// 16-byte groups i, i + 256, ... in order (elements i, i + 256, ... when HW is not a multiple
+// of a group), then the 256 thread sums are added by a fixed tree -- into part[ch * N + n];
+// the final pass adds the N partials of a channel in order.  (A bf16 value is the high half
+// of the fp32 with the same bits.)
 constexpr int kSumThreads = 256;
 template <int DT>
 __global__ void __launch_bounds__(kSumThreads) chan_sum_partial_kernel(const __grid_constant__ ChanSumPlan cp) {
@@ -1092,11 +1094,32 @@ __global__ void __launch_bounds__(kSumThreads) chan_sum_partial_kernel(const __g
   const int ch = (int)(b / cp.N);
   const long long base = ((long long)n * cp.Ch + ch) * cp.HW;
   float acc = 0.f;
-  for (long long i = threadIdx.x; i < cp.HW; i += kSumThreads) {
-    if constexpr (DT == 0)
-      acc += static_cast<const float*>(cp.t)[base + i];
-    else
-      acc += __bfloat162float(static_cast<const __nv_bfloat16*>(cp.t)[base + i]);
+  constexpr int VE = DT == 0 ? 4 : 8;  // elements per 16-byte read
+  const bool vec = (cp.HW % VE) == 0 && (reinterpret_cast<uintptr_t>(cp.t) & 15) == 0;
+  if (vec) {
+    // 16-byte reads: thread i adds groups i, i + 256, ... (each group's elements in order)
+    const uint4* src = reinterpret_cast<const uint4*>(static_cast<const char*>(cp.t) + base * (16 / VE));
+    const long long ng = cp.HW / VE;
+    for (long long gi = threadIdx.x; gi < ng; gi += kSumThreads) {
+      const uint4 u = __ldg(src + gi);
+      const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        if constexpr (DT == 0) {
+          acc += __uint_as_float(wv[e]);
+        } else {
+          acc += __uint_as_float(wv[e] << 16);
+          acc += __uint_as_float(wv[e] & 0xffff0000u);
+        }
+      }
+    }
+  } else {
+    for (long long i = threadIdx.x; i < cp.HW; i += kSumThreads) {
+      if constexpr (DT == 0)
+        acc += static_cast<const float*>(cp.t)[base + i];
+      else
+        acc += __bfloat162float(static_cast<const __nv_bfloat16*>(cp.t)[base + i]);
+    }
   }
   red[threadIdx.x] = acc;
   __syncthreads();
