@@ -20,12 +20,14 @@ import threading
 
 __all__ = [
     "conv2d_fwd", "conv2d_bwd_data", "conv2d_bwd_filter", "deconv2d_fwd", "conv2d_fwd_noalloc",
+    "conv1d_fwd", "conv1d_bwd_data", "conv1d_bwd_filter", "MODE_CROSS_CORRELATION", "MODE_CONVOLUTION",
     "conv2d_workspace_size", "conv2d_output_dim", "conv2d_device_status", "conv2d_strerror",
     "Conv2dError", "lib_path", "load_library", "OP_FWD", "OP_BWD_DATA", "OP_BWD_FILTER",
     "DTYPE_F32", "DTYPE_BF16",
 ]
 
 OP_FWD, OP_BWD_DATA, OP_BWD_FILTER = 0, 1, 2
+MODE_CROSS_CORRELATION, MODE_CONVOLUTION = 0, 1
 DTYPE_F32, DTYPE_BF16 = 0, 1
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -71,9 +73,9 @@ def load_library():
         fl = ctypes.c_float
         for name in ("conv2d_fwd_ex", "conv2d_bwd_data_ex"):
             f = getattr(lib, name)
-            f.argtypes = [i] * 13 + [i, vp, vp, vp, fl, vp, vp, sz, vp]
+            f.argtypes = [i] * 13 + [i, i, vp, vp, vp, fl, vp, vp, sz, vp]
             f.restype = i
-        lib.conv2d_bwd_filter_ex.argtypes = [i] * 13 + [i, vp, vp, fl, vp, vp, vp, vp, sz, vp]
+        lib.conv2d_bwd_filter_ex.argtypes = [i] * 13 + [i, i, vp, vp, fl, vp, vp, vp, vp, sz, vp]
         lib.conv2d_bwd_filter_ex.restype = i
         lib.conv2d_fwd_noalloc.argtypes = [i] * 13 + [i, vp, vp, vp, vp]
         lib.conv2d_fwd_noalloc.restype = i
@@ -159,11 +161,15 @@ def _check_vec(v, n, like, name):
         raise ValueError(f"{name} must be a vector of {n} {like.dtype} values on {like.device}")
 
 
-def _call(name, dims, dt, a, b, out, workspace, op, stream, bias=None, beta=0.0):
-    """Forward / backward-data through the fused-epilogue entry point (bias None and beta 0
-    are the plain op)."""
+def _mode(flip):
+    return MODE_CONVOLUTION if flip else MODE_CROSS_CORRELATION
+
+
+def _call(name, dims, dt, a, b, out, workspace, op, stream, bias=None, beta=0.0, flip=False):
+    """Forward / backward-data through the fused-epilogue entry point (bias None, beta 0 and
+    flip False are the plain op)."""
     ws, wsb = _workspace(op, dims, dt, workspace, out.device)
-    rc = getattr(load_library(), name + "_ex")(*[int(v) for v in dims], dt, _ptr(a), _ptr(b), _ptr(bias),
+    rc = getattr(load_library(), name + "_ex")(*[int(v) for v in dims], dt, _mode(flip), _ptr(a), _ptr(b), _ptr(bias),
                                                ctypes.c_float(float(beta)), _ptr(out), _ptr(ws),
                                                ctypes.c_size_t(wsb), _stream_ptr(stream))
     if rc:
@@ -171,9 +177,10 @@ def _call(name, dims, dt, a, b, out, workspace, op, stream, bias=None, beta=0.0)
     return out
 
 
-def conv2d_fwd(x, w, pad=0, stride=1, out=None, workspace=None, stream=None, bias=None, beta=0.0):
+def conv2d_fwd(x, w, pad=0, stride=1, out=None, workspace=None, stream=None, bias=None, beta=0.0, flip=False):
     """y = conv2d(x, w) (+ bias[k]) (+ beta * y): x (N,C,H,W), w (K,C,R,S) -> y (N,K,P,Q),
-    same dtype.  With beta != 0, `out` holds the values to accumulate onto."""
+    same dtype.  With beta != 0, `out` holds the values to accumulate onto.  flip=True is
+    convolution mode (the filter rotated by 180 degrees); the default is cross-correlation."""
     import torch
     _check_tensor(x, "x")
     _check_tensor(w, "w")
@@ -190,7 +197,7 @@ def conv2d_fwd(x, w, pad=0, stride=1, out=None, workspace=None, stream=None, bia
         out = torch.empty((N, K, P, Q), dtype=x.dtype, device=x.device)
     _check_vec(bias, K, x, "bias")
     dims = (N, C, H, W, K, R, S, ph, pw, sh, sw, P, Q)
-    return _call("conv2d_fwd", dims, _dtype_code(x), x, w, out, workspace, OP_FWD, stream, bias, beta)
+    return _call("conv2d_fwd", dims, _dtype_code(x), x, w, out, workspace, OP_FWD, stream, bias, beta, flip)
 
 
 def conv2d_fwd_noalloc(x, w, pad=0, stride=1, out=None, stream=None):
@@ -218,7 +225,8 @@ def conv2d_fwd_noalloc(x, w, pad=0, stride=1, out=None, stream=None):
     return out
 
 
-def conv2d_bwd_data(dy, w, x_hw, pad=0, stride=1, out=None, workspace=None, stream=None, bias=None, beta=0.0):
+def conv2d_bwd_data(dy, w, x_hw, pad=0, stride=1, out=None, workspace=None, stream=None, bias=None, beta=0.0,
+                    flip=False):
     """dx (N,C,H,W) from dy (N,K,P,Q) and w (K,C,R,S); x_hw = (H, W).  Optional epilogue:
     + bias[c] (the bias of a deconvolution) + beta * dx (`out` required when beta != 0)."""
     import torch
@@ -238,11 +246,11 @@ def conv2d_bwd_data(dy, w, x_hw, pad=0, stride=1, out=None, workspace=None, stre
     _check_vec(bias, C, dy, "bias")
     dims = (N, C, H, W, K, R, S, ph, pw, sh, sw, P, Q)
     return _call("conv2d_bwd_data", dims, _dtype_code(dy), dy, w, out, workspace, OP_BWD_DATA, stream,
-                 bias, beta)
+                 bias, beta, flip)
 
 
 def conv2d_bwd_filter(x, dy, rs, pad=0, stride=1, out=None, workspace=None, stream=None, beta=0.0,
-                      db_k=None, db_c=None):
+                      db_k=None, db_c=None, flip=False):
     """dw (K,C,R,S) from x (N,C,H,W) and dy (N,K,P,Q); rs = (R, S).
 
     Optional: beta accumulates onto `out` (dw) and onto the bias gradients; db_k (K values)
@@ -268,7 +276,7 @@ def conv2d_bwd_filter(x, dy, rs, pad=0, stride=1, out=None, workspace=None, stre
     dims = (N, C, H, W, K, R, S, ph, pw, sh, sw, P, Q)
     dt = _dtype_code(x)
     ws, wsb = _workspace(OP_BWD_FILTER, dims, dt, workspace, out.device)
-    rc = load_library().conv2d_bwd_filter_ex(*[int(v) for v in dims], dt, _ptr(x), _ptr(dy),
+    rc = load_library().conv2d_bwd_filter_ex(*[int(v) for v in dims], dt, _mode(flip), _ptr(x), _ptr(dy),
                                              ctypes.c_float(float(beta)), _ptr(out), _ptr(db_k), _ptr(db_c),
                                              _ptr(ws), ctypes.c_size_t(wsb), _stream_ptr(stream))
     if rc:
@@ -276,13 +284,48 @@ def conv2d_bwd_filter(x, dy, rs, pad=0, stride=1, out=None, workspace=None, stre
     return out
 
 
-def deconv2d_fwd(inp, wt, out_hw, pad=0, stride=1, out=None, workspace=None, stream=None, bias=None, beta=0.0):
+def deconv2d_fwd(inp, wt, out_hw, pad=0, stride=1, out=None, workspace=None, stream=None, bias=None, beta=0.0,
+                 flip=False):
     """Transposed convolution: inp (N,Ci,Hi,Wi), wt (Ci,Co,R,S) -> (N,Co,Ho,Wo), optionally
     + bias[co] + beta * out.
 
     Runs conv2d_bwd_data with K = Ci (deconv input channels), C = Co, P = Hi, H = Ho."""
     return conv2d_bwd_data(inp, wt, out_hw, pad, stride, out=out, workspace=workspace, stream=stream,
-                           bias=bias, beta=beta)
+                           bias=bias, beta=beta, flip=flip)
+
+
+# ------------------------------------------------------------------ 1-D
+# A 1-D convolution over (N, C, W) is the 2-D one with H = R = 1 (pad and stride along W
+# only); these wrappers only reshape views and call the 2-D entry points.
+
+def _one(v):
+    return int(v if isinstance(v, int) else v[0])
+
+
+def conv1d_fwd(x, w, pad=0, stride=1, out=None, workspace=None, stream=None, bias=None, beta=0.0, flip=False):
+    """y (N,K,Q) = conv1d(x (N,C,W), w (K,C,S))."""
+    o4 = out.unsqueeze(2) if out is not None else None
+    y = conv2d_fwd(x.unsqueeze(2), w.unsqueeze(2), (0, _one(pad)), (1, _one(stride)), out=o4,
+                   workspace=workspace, stream=stream, bias=bias, beta=beta, flip=flip)
+    return y.squeeze(2) if out is None else out
+
+
+def conv1d_bwd_data(dy, w, x_w, pad=0, stride=1, out=None, workspace=None, stream=None, bias=None, beta=0.0,
+                    flip=False):
+    """dx (N,C,W) from dy (N,K,Q) and w (K,C,S); x_w = W."""
+    o4 = out.unsqueeze(2) if out is not None else None
+    dx = conv2d_bwd_data(dy.unsqueeze(2), w.unsqueeze(2), (1, int(x_w)), (0, _one(pad)), (1, _one(stride)), out=o4,
+                         workspace=workspace, stream=stream, bias=bias, beta=beta, flip=flip)
+    return dx.squeeze(2) if out is None else out
+
+
+def conv1d_bwd_filter(x, dy, s, pad=0, stride=1, out=None, workspace=None, stream=None, beta=0.0, db_k=None,
+                      db_c=None, flip=False):
+    """dw (K,C,S) from x (N,C,W) and dy (N,K,Q); s = S."""
+    o4 = out.unsqueeze(2) if out is not None else None
+    dw = conv2d_bwd_filter(x.unsqueeze(2), dy.unsqueeze(2), (1, int(s)), (0, _one(pad)), (1, _one(stride)), out=o4,
+                           workspace=workspace, stream=stream, beta=beta, db_k=db_k, db_c=db_c, flip=flip)
+    return dw.squeeze(2) if out is None else out
 
 
 def conv2d_device_status(stream=None) -> int:

@@ -699,6 +699,7 @@ int build_bwd_filter_impl(const Desc& d0, const void* x, const void* dy, void* d
   rp.k_pad = d.K;
   rp.c_pad = d.C;
   rp.beta = 0.f;
+  rp.flip = 0;
   b.grid = (int)std::min<long long>(p.total_tiles, di.sms);
   return CONV2D_OK;
 }
@@ -866,8 +867,9 @@ int workspace_size_uncached(int op, const Desc& d, size_t* bytes) {
 
 extern "C" {
 
-static int run_tap(int op, const Desc& d, const void* src, const void* w, const void* bias, float beta, void* dst,
-                   void* ws, size_t wsb, void* stream) {
+static int run_tap(int op, const Desc& d, const void* src, const void* w, const void* bias, float beta, int mode,
+                   void* dst, void* ws, size_t wsb, void* stream) {
+  if (mode != CONV2D_MODE_CROSS_CORRELATION && mode != CONV2D_MODE_CONVOLUTION) return CONV2D_ERR_BAD_DESC;
   int rc = validate(d);
   if (rc) return rc;
   rc = check_ptrs(src, w, dst, d.dt);
@@ -884,8 +886,9 @@ static int run_tap(int op, const Desc& d, const void* src, const void* w, const 
   rc = check_ws(ws, wsb, b.pack_bytes);
   if (rc) return rc;
   if (bias != nullptr && ((uintptr_t)bias & (d.dt == CONV2D_DTYPE_F32 ? 3 : 1))) return CONV2D_ERR_ALIGN;
-  b.p.bias = bias;  // per-call epilogue inputs (not part of the cached plan)
+  b.p.bias = bias;  // per-call epilogue inputs and mode (not part of the cached plan)
   b.p.beta = beta;
+  b.pp.flip = mode == CONV2D_MODE_CONVOLUTION ? 1 : 0;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (b.pack_bytes) {
     rc = launch_err(launch_pack_filter(b.pp, d.dt, st));
@@ -898,41 +901,45 @@ int conv2d_fwd(int N, int C, int H, int W, int K, int R, int S, int pad_h, int p
                int stride_w, int P, int Q, int dtype, const void* x, const void* w, void* y, void* workspace,
                size_t workspace_bytes, void* stream) {
   const Desc d{N, C, H, W, K, R, S, pad_h, pad_w, stride_h, stride_w, P, Q, dtype};
-  return run_tap(CONV2D_OP_FWD, d, x, w, nullptr, 0.f, y, workspace, workspace_bytes, stream);
+  return run_tap(CONV2D_OP_FWD, d, x, w, nullptr, 0.f, CONV2D_MODE_CROSS_CORRELATION, y, workspace, workspace_bytes,
+                 stream);
 }
 
 int conv2d_fwd_ex(int N, int C, int H, int W, int K, int R, int S, int pad_h, int pad_w, int stride_h,
-                  int stride_w, int P, int Q, int dtype, const void* x, const void* w, const void* bias, float beta,
-                  void* y, void* workspace, size_t workspace_bytes, void* stream) {
+                  int stride_w, int P, int Q, int dtype, int mode, const void* x, const void* w, const void* bias,
+                  float beta, void* y, void* workspace, size_t workspace_bytes, void* stream) {
   const Desc d{N, C, H, W, K, R, S, pad_h, pad_w, stride_h, stride_w, P, Q, dtype};
-  return run_tap(CONV2D_OP_FWD, d, x, w, bias, beta, y, workspace, workspace_bytes, stream);
+  return run_tap(CONV2D_OP_FWD, d, x, w, bias, beta, mode, y, workspace, workspace_bytes, stream);
 }
 
 int conv2d_bwd_data(int N, int C, int H, int W, int K, int R, int S, int pad_h, int pad_w, int stride_h,
                     int stride_w, int P, int Q, int dtype, const void* dy, const void* w, void* dx,
                     void* workspace, size_t workspace_bytes, void* stream) {
   const Desc d{N, C, H, W, K, R, S, pad_h, pad_w, stride_h, stride_w, P, Q, dtype};
-  return run_tap(CONV2D_OP_BWD_DATA, d, dy, w, nullptr, 0.f, dx, workspace, workspace_bytes, stream);
+  return run_tap(CONV2D_OP_BWD_DATA, d, dy, w, nullptr, 0.f, CONV2D_MODE_CROSS_CORRELATION, dx, workspace,
+                 workspace_bytes, stream);
 }
 
 int conv2d_bwd_data_ex(int N, int C, int H, int W, int K, int R, int S, int pad_h, int pad_w, int stride_h,
-                       int stride_w, int P, int Q, int dtype, const void* dy, const void* w, const void* bias,
-                       float beta, void* dx, void* workspace, size_t workspace_bytes, void* stream) {
+                       int stride_w, int P, int Q, int dtype, int mode, const void* dy, const void* w,
+                       const void* bias, float beta, void* dx, void* workspace, size_t workspace_bytes, void* stream) {
   const Desc d{N, C, H, W, K, R, S, pad_h, pad_w, stride_h, stride_w, P, Q, dtype};
-  return run_tap(CONV2D_OP_BWD_DATA, d, dy, w, bias, beta, dx, workspace, workspace_bytes, stream);
+  return run_tap(CONV2D_OP_BWD_DATA, d, dy, w, bias, beta, mode, dx, workspace, workspace_bytes, stream);
 }
 
 int conv2d_bwd_filter(int N, int C, int H, int W, int K, int R, int S, int pad_h, int pad_w, int stride_h,
                       int stride_w, int P, int Q, int dtype, const void* x, const void* dy, void* dw,
                       void* workspace, size_t workspace_bytes, void* stream) {
-  return conv2d_bwd_filter_ex(N, C, H, W, K, R, S, pad_h, pad_w, stride_h, stride_w, P, Q, dtype, x, dy, 0.f, dw,
-                              nullptr, nullptr, workspace, workspace_bytes, stream);
+  return conv2d_bwd_filter_ex(N, C, H, W, K, R, S, pad_h, pad_w, stride_h, stride_w, P, Q, dtype,
+                              CONV2D_MODE_CROSS_CORRELATION, x, dy, 0.f, dw, nullptr, nullptr, workspace,
+                              workspace_bytes, stream);
 }
 
 int conv2d_bwd_filter_ex(int N, int C, int H, int W, int K, int R, int S, int pad_h, int pad_w, int stride_h,
-                         int stride_w, int P, int Q, int dtype, const void* x, const void* dy, float beta, void* dw,
-                         void* db_k, void* db_c, void* workspace, size_t workspace_bytes, void* stream) {
+                         int stride_w, int P, int Q, int dtype, int mode, const void* x, const void* dy, float beta,
+                         void* dw, void* db_k, void* db_c, void* workspace, size_t workspace_bytes, void* stream) {
   const Desc d{N, C, H, W, K, R, S, pad_h, pad_w, stride_h, stride_w, P, Q, dtype};
+  if (mode != CONV2D_MODE_CROSS_CORRELATION && mode != CONV2D_MODE_CONVOLUTION) return CONV2D_ERR_BAD_DESC;
   int rc = validate(d);
   if (rc) return rc;
   rc = check_ptrs(x, dy, dw, d.dt);
@@ -953,6 +960,7 @@ int conv2d_bwd_filter_ex(int N, int C, int H, int W, int K, int R, int S, int pa
   const uintptr_t am = d.dt == CONV2D_DTYPE_F32 ? 3 : 1;
   if (((uintptr_t)db_k & am) || ((uintptr_t)db_c & am)) return CONV2D_ERR_ALIGN;
   b.rp.beta = beta;  // per-call (not part of the cached plan)
+  b.rp.flip = mode == CONV2D_MODE_CONVOLUTION ? 1 : 0;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   rc = launch_err(launch_wgrad(b.p, d.dt, b.grid, st));
   if (rc) return rc;

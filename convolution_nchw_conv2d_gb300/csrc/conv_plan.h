@@ -95,6 +95,7 @@ struct PackPlan {
   int n_ntiles, nkb, ntaps_total;
   int NT, CB;
   int tap_r[kMaxTaps], tap_s[kMaxTaps];
+  int flip;               // convolution mode: tap (r, s) reads w[.., R-1-r, S-1-s]
 };
 
 // Backward-filter as one implicit GEMM per tile:
@@ -191,6 +192,7 @@ struct ReducePlan {
   int K, C, R, S;
   int nsplit, k_pad, c_pad;
   float beta;            // dw = sum + beta * dw (beta 0: dw is not read)
+  int flip;              // convolution mode: partial tap (r, s) is dw[.., R-1-r, S-1-s]
 };
 
 // Per-channel sum of an NCHW-like tensor t (N, Ch, HW): out[ch] = sum_{n, i} t[n, ch, i]

@@ -455,7 +455,11 @@ __global__ void pack_filter_kernel(const __grid_constant__ PackPlan pp) {
     const int kb = (int)(rest % pp.nkb);
     const int nt = (int)(rest / pp.nkb);
     const int nn = nt * pp.NT + n;
-    const int r = pp.tap_r[t], s = pp.tap_s[t];
+    int r = pp.tap_r[t], s = pp.tap_s[t];
+    if (pp.flip && r >= 0) {  // convolution mode: the filter rotated by 180 degrees
+      r = pp.R - 1 - r;
+      s = pp.S - 1 - s;
+    }
     uint32_t out[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
     for (int e = 0; e < CHUNK; ++e) {

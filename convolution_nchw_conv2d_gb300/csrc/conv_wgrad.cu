@@ -1064,7 +1064,7 @@ __global__ void __launch_bounds__(32 * kReduceWarps) wgrad_reduce_kernel(const _
         const long long r = io / rp.K;
         const int c = (int)(r % rp.C);
         const int tap = (int)(r / rp.C);
-        const long long o = ((long long)k * rp.C + c) * RS + tap;
+        const long long o = ((long long)k * rp.C + c) * RS + (rp.flip ? RS - 1 - tap : tap);
         if constexpr (DT == 0) {
           float* dwp = static_cast<float*>(rp.dw);
           if (rp.beta != 0.f) sum += rp.beta * dwp[o];

@@ -70,6 +70,17 @@ enum {
     CONV2D_DTYPE_BF16 = 1
 };
 
+/* Convolution mode (cuDNN's cudnnConvolutionMode_t, which the SystemDS page sets to
+ * CUDNN_CROSS_CORRELATION in allocateConvolutionDescriptor): cross-correlation (the
+ * formulas above), or convolution, the same with the filter rotated by 180 degrees --
+ * tap (r, s) multiplies w[k,c,R-1-r,S-1-s]; its backward-filter returns the gradient of that
+ * filter, dw[k,c,R-1-r,S-1-s] = the cross-correlation dw[k,c,r,s].  Only the _ex entry points
+ * take a mode; the plain ones are cross-correlation. */
+enum {
+    CONV2D_MODE_CROSS_CORRELATION = 0,
+    CONV2D_MODE_CONVOLUTION = 1
+};
+
 enum {
     CONV2D_OP_FWD = 0,
     CONV2D_OP_BWD_DATA = 1,
@@ -148,20 +159,22 @@ int conv2d_bwd_filter(int N, int C, int H, int W, int K, int R, int S,
  *                      bias gradient is requested the workspace must have the full size
  *                      conv2d_workspace_size(CONV2D_OP_BWD_FILTER, ...) reports; otherwise the
  *                      split partials alone suffice.
- * Same descriptors, workspace rules and error codes as the plain entry points (which are
- * these with bias = NULL, beta = 0, db_k = db_c = NULL). */
+ * `mode` is CONV2D_MODE_CROSS_CORRELATION or CONV2D_MODE_CONVOLUTION (any other value:
+ * CONV2D_ERR_BAD_DESC).  Same descriptors, workspace rules and error codes as the plain
+ * entry points (which are these with cross-correlation, bias = NULL, beta = 0,
+ * db_k = db_c = NULL). */
 int conv2d_fwd_ex(int N, int C, int H, int W, int K, int R, int S,
-                  int pad_h, int pad_w, int stride_h, int stride_w, int P, int Q, int dtype,
+                  int pad_h, int pad_w, int stride_h, int stride_w, int P, int Q, int dtype, int mode,
                   const void *x, const void *w, const void *bias, float beta, void *y,
                   void *workspace, size_t workspace_bytes, void *stream);
 
 int conv2d_bwd_data_ex(int N, int C, int H, int W, int K, int R, int S,
-                       int pad_h, int pad_w, int stride_h, int stride_w, int P, int Q, int dtype,
+                       int pad_h, int pad_w, int stride_h, int stride_w, int P, int Q, int dtype, int mode,
                        const void *dy, const void *w, const void *bias, float beta, void *dx,
                        void *workspace, size_t workspace_bytes, void *stream);
 
 int conv2d_bwd_filter_ex(int N, int C, int H, int W, int K, int R, int S,
-                         int pad_h, int pad_w, int stride_h, int stride_w, int P, int Q, int dtype,
+                         int pad_h, int pad_w, int stride_h, int stride_w, int P, int Q, int dtype, int mode,
                          const void *x, const void *dy, float beta, void *dw, void *db_k, void *db_c,
                          void *workspace, size_t workspace_bytes, void *stream);
 

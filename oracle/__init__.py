@@ -182,20 +182,30 @@ def _epilogue(d, bias, beta, old, channel_axis):
     return out
 
 
-def conv2d_fwd_ex(x, w, bias=None, beta=0.0, y_old=None, pad=0, stride=1) -> np.ndarray:
-    """y = conv(x, w) + bias[k] + beta * y_old (bias per output channel k, axis 1 of y)."""
-    return _epilogue(conv2d_fwd(x, w, pad, stride), bias, beta, y_old, 1)
+# Convolution mode (cuDNN's CUDNN_CONVOLUTION, the alternative to the CUDNN_CROSS_CORRELATION
+# the SystemDS page selects): the filter enters rotated by 180 degrees, w[k,c,R-1-r,S-1-s]; the
+# filter gradient of that op is the cross-correlation gradient rotated back.
+
+def _rot180(w):
+    return np.ascontiguousarray(_f64(w)[:, :, ::-1, ::-1])
 
 
-def conv2d_bwd_data_ex(dy, w, x_hw, bias=None, beta=0.0, dx_old=None, pad=0, stride=1) -> np.ndarray:
+def conv2d_fwd_ex(x, w, bias=None, beta=0.0, y_old=None, pad=0, stride=1, flip=False) -> np.ndarray:
+    """y = conv(x, w) + bias[k] + beta * y_old (bias per output channel k, axis 1 of y); flip:
+    convolution mode."""
+    return _epilogue(conv2d_fwd(x, _rot180(w) if flip else w, pad, stride), bias, beta, y_old, 1)
+
+
+def conv2d_bwd_data_ex(dy, w, x_hw, bias=None, beta=0.0, dx_old=None, pad=0, stride=1, flip=False) -> np.ndarray:
     """dx = bwd_data(dy, w) + bias[c] + beta * dx_old (bias per channel c of dx: the bias of
-    the deconvolution whose output dx is)."""
-    return _epilogue(conv2d_bwd_data(dy, w, x_hw, pad, stride), bias, beta, dx_old, 1)
+    the deconvolution whose output dx is); flip: convolution mode."""
+    return _epilogue(conv2d_bwd_data(dy, _rot180(w) if flip else w, x_hw, pad, stride), bias, beta, dx_old, 1)
 
 
-def conv2d_bwd_filter_ex(x, dy, rs, beta=0.0, dw_old=None, pad=0, stride=1) -> np.ndarray:
-    """dw = bwd_filter(x, dy) + beta * dw_old."""
-    return _epilogue(conv2d_bwd_filter(x, dy, rs, pad, stride), None, beta, dw_old, 0)
+def conv2d_bwd_filter_ex(x, dy, rs, beta=0.0, dw_old=None, pad=0, stride=1, flip=False) -> np.ndarray:
+    """dw = bwd_filter(x, dy) + beta * dw_old; flip: the gradient of the rotated filter."""
+    dw = conv2d_bwd_filter(x, dy, rs, pad, stride)
+    return _epilogue(_rot180(dw) if flip else dw, None, beta, dw_old, 0)
 
 
 def channel_sum(t, beta=0.0, old=None) -> np.ndarray:

@@ -428,3 +428,41 @@ def test_epilogue_torch_cpu_fp64_witness():
                                stride=(sh, sw), padding=(ph, pw), output_padding=outpad).numpy()
     d = oracle.conv2d_bwd_data_ex(dy, w, (H, W), bc, 0.0, None, (ph, pw), (sh, sw))
     assert np.max(np.abs(d - d_ref)) <= 1e-12 * max(1.0, np.max(np.abs(d_ref)))
+
+
+# --------------------------------------------------------------------------- convolution mode
+# cuDNN's convolution mode (the SystemDS page picks CUDNN_CROSS_CORRELATION, the other value
+# of the same descriptor field): the filter enters rotated by 180 degrees.
+
+def test_convolution_mode_torch_witness():
+    torch = pytest.importorskip("torch")
+    import torch.nn.functional as F
+    N, C, H, W, K, R, S, ph, pw, sh, sw, P, Q = _epi_shapes()
+    x = RNG.standard_normal((N, C, H, W))
+    w = RNG.standard_normal((K, C, R, S))
+    ref = F.conv2d(torch.from_numpy(x), torch.from_numpy(w).flip(2, 3), stride=(sh, sw), padding=(ph, pw)).numpy()
+    got = oracle.conv2d_fwd_ex(x, w, None, 0.0, None, (ph, pw), (sh, sw), flip=True)
+    assert np.max(np.abs(got - ref)) <= 1e-12 * max(1.0, np.max(np.abs(ref)))
+    # a half flip (rows only) is not the same op: the witness separates them
+    half = oracle.conv2d_fwd(x, np.ascontiguousarray(w[:, :, ::-1, :]), (ph, pw), (sh, sw))
+    assert np.max(np.abs(half - ref)) > 1e-6
+
+
+def test_convolution_mode_adjoint_identities():
+    """<fwd(x, w), dy> = <x, bwd_data(dy, w)> = <w, bwd_filter(x, dy)> in convolution mode
+    too: ties the three flipped ops together (a flip missing or misplaced in one of them
+    breaks an equality)."""
+    for case in ADJ_CASES[:3]:
+        N, C, H, W, K, R, S, ph, pw, sh, sw = case
+        P, Q = oracle.output_dim(H, ph, R, sh), oracle.output_dim(W, pw, S, sw)
+        x = RNG.standard_normal((N, C, H, W))
+        w = RNG.standard_normal((K, C, R, S))
+        dy = RNG.standard_normal((N, K, P, Q))
+        a = np.vdot(oracle.conv2d_fwd_ex(x, w, None, 0.0, None, (ph, pw), (sh, sw), flip=True), dy)
+        b = np.vdot(x, oracle.conv2d_bwd_data_ex(dy, w, (H, W), None, 0.0, None, (ph, pw), (sh, sw), flip=True))
+        c = np.vdot(w, oracle.conv2d_bwd_filter_ex(x, dy, (R, S), 0.0, None, (ph, pw), (sh, sw), flip=True))
+        assert abs(a - b) <= 1e-10 * max(1.0, abs(a)) and abs(a - c) <= 1e-10 * max(1.0, abs(a))
+        if R * S > 1:
+            # the unflipped filter gradient does not satisfy the flipped identity
+            c0 = np.vdot(w, oracle.conv2d_bwd_filter(x, dy, (R, S), (ph, pw), (sh, sw)))
+            assert abs(a - c0) > 1e-8 * max(1.0, abs(a))

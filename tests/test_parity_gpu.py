@@ -281,3 +281,60 @@ def test_bias_gradient_resnet_workload(cg):
         ref = oracle.channel_sum(t)
         err = float(np.abs(got.double().cpu().numpy() - ref).max())
         assert err <= 2e-3 * math.sqrt(length) * float(t.abs().max())
+
+
+# ------------------------------------------------------------------ convolution mode, 1-D
+FLIP_CASES = [
+    (2, 3, 7, 9, 5, 3, 2, 1, 0, 1, 1),
+    (1, 5, 14, 7, 3, 3, 3, 1, 1, 2, 2),
+    (2, 64, 16, 16, 64, 3, 3, 1, 1, 1, 1),   # backward-filter row-tap sharing
+    (2, 40, 23, 19, 24, 3, 3, 1, 1, 3, 2),
+]
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("case", FLIP_CASES)
+def test_convolution_mode_parity(cg, case, dtype):
+    N, C, H, Wd, K, R, S, ph, pw, sh, sw = case
+    pb = W.Conv2dProblem(N, C, H, Wd, K, R, S, ph, pw, sh, sw, dtype)
+    x, w, dy = W.random_problem_inputs(pb, 9300 + FLIP_CASES.index(case))
+    pad, st = (ph, pw), (sh, sw)
+    xd, wd, dyd = x.to(DEV), w.to(DEV), dy.to(DEV)
+    y = _poisoned(pb.y_shape, x.dtype)
+    cg.conv2d_fwd(xd, wd, pad, st, out=y, flip=True)
+    dx = _poisoned(pb.x_shape, x.dtype)
+    cg.conv2d_bwd_data(dyd, wd, (H, Wd), pad, st, out=dx, flip=True)
+    dw = _poisoned(pb.w_shape, x.dtype)
+    cg.conv2d_bwd_filter(xd, dyd, (R, S), pad, st, out=dw, flip=True)
+    cg.conv2d_device_status()
+    for op, got, ref in (("fwd", y, oracle.conv2d_fwd_ex(x, w, None, 0.0, None, pad, st, flip=True)),
+                         ("bwd_data", dx, oracle.conv2d_bwd_data_ex(dy, w, (H, Wd), None, 0.0, None, pad, st, flip=True)),
+                         ("bwd_filter", dw, oracle.conv2d_bwd_filter_ex(x, dy, (R, S), 0.0, None, pad, st, flip=True))):
+        a, b = _operands(op, x, w, dy)
+        _check(op, pb, got.double().cpu().numpy(), ref, a, b, f"{case}/{op}/flip/{dtype}")
+
+
+@pytest.mark.parametrize("flip", [False, True])
+def test_conv1d_wrappers(cg, flip):
+    """conv1d_* = the 2-D ops with H = R = 1, checked against the oracle on (N, C, 1, W)."""
+    g = torch.Generator().manual_seed(9400 + int(flip))
+    N, C, Wd, K, S, pad, stride = 3, 6, 29, 5, 4, 2, 2
+    Q = (Wd + 2 * pad - S) // stride + 1
+    x = torch.randn(N, C, Wd, generator=g)
+    w = torch.randn(K, C, S, generator=g)
+    dy = torch.randn(N, K, Q, generator=g)
+    y = cg.conv1d_fwd(x.to(DEV), w.to(DEV), pad, stride, flip=flip)
+    dx = cg.conv1d_bwd_data(dy.to(DEV), w.to(DEV), Wd, pad, stride, flip=flip)
+    dw = cg.conv1d_bwd_filter(x.to(DEV), dy.to(DEV), S, pad, stride, flip=flip)
+    cg.conv2d_device_status()
+    x4, w4, dy4 = x.unsqueeze(2), w.unsqueeze(2), dy.unsqueeze(2)
+    refs = (oracle.conv2d_fwd_ex(x4, w4, None, 0.0, None, (0, pad), (1, stride), flip=flip)[:, :, 0],
+            oracle.conv2d_bwd_data_ex(dy4, w4, (1, Wd), None, 0.0, None, (0, pad), (1, stride), flip=flip)[:, :, 0],
+            oracle.conv2d_bwd_filter_ex(x4, dy4, (1, S), 0.0, None, (0, pad), (1, stride), flip=flip)[:, :, 0])
+    lens = (C * S, K * S, N * Q)
+    amax = [float(t.abs().max()) for t in (x, w, dy)]
+    scales = (amax[0] * amax[1], amax[2] * amax[1], amax[0] * amax[2])
+    for got, ref, L, sc in zip((y, dx, dw), refs, lens, scales):
+        assert tuple(got.shape) == ref.shape
+        err = float(np.abs(got.double().cpu().numpy() - ref).max())
+        assert err <= 2e-3 * math.sqrt(L) * sc
