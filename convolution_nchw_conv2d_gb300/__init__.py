@@ -46,7 +46,7 @@ def lib_path() -> str:
     return _LIB_PATH
 
 
-EXPORTS = ("conv2d_output_dim", "conv2d_workspace_size", "conv2d_fwd", "conv2d_bwd_data",
+EXPORTS = ("conv2d_output_dim", "conv2d_workspace_size", "conv2d_workspace_size_ex", "conv2d_fwd", "conv2d_bwd_data",
            "conv2d_bwd_filter", "conv2d_fwd_ex", "conv2d_bwd_data_ex", "conv2d_bwd_filter_ex",
            "conv2d_fwd_noalloc", "conv2d_device_status", "conv2d_strerror")
 
@@ -73,9 +73,11 @@ def load_library():
         fl = ctypes.c_float
         for name in ("conv2d_fwd_ex", "conv2d_bwd_data_ex"):
             f = getattr(lib, name)
-            f.argtypes = [i] * 13 + [i, i, vp, vp, vp, fl, vp, vp, sz, vp]
+            f.argtypes = [i] * 15 + [i, i, vp, vp, vp, fl, vp, vp, sz, vp]
             f.restype = i
-        lib.conv2d_bwd_filter_ex.argtypes = [i] * 13 + [i, i, vp, vp, fl, vp, vp, vp, vp, sz, vp]
+        lib.conv2d_bwd_filter_ex.argtypes = [i] * 15 + [i, i, vp, vp, fl, vp, vp, vp, vp, sz, vp]
+        lib.conv2d_workspace_size_ex.argtypes = [i] + [i] * 15 + [i, ctypes.POINTER(sz)]
+        lib.conv2d_workspace_size_ex.restype = i
         lib.conv2d_bwd_filter_ex.restype = i
         lib.conv2d_fwd_noalloc.argtypes = [i] * 13 + [i, vp, vp, vp, vp]
         lib.conv2d_fwd_noalloc.restype = i
@@ -115,10 +117,11 @@ def _dtype_code(t) -> int:
     raise TypeError(f"unsupported dtype {t.dtype}; expected float32 or bfloat16")
 
 
-def conv2d_workspace_size(op: int, dims, dtype_code: int) -> int:
-    """Workspace bytes for `op` and the 13 descriptor integers `dims`."""
+def conv2d_workspace_size(op: int, dims, dtype_code: int, dilation=(1, 1)) -> int:
+    """Workspace bytes for `op`, the 13 descriptor integers `dims` and the dilation."""
     out = ctypes.c_size_t(0)
-    rc = load_library().conv2d_workspace_size(op, *[int(v) for v in dims], dtype_code, ctypes.byref(out))
+    dh, dw = _pair(dilation)
+    rc = load_library().conv2d_workspace_size_ex(op, *[int(v) for v in dims], dh, dw, dtype_code, ctypes.byref(out))
     if rc:
         raise Conv2dError(rc, "conv2d_workspace_size")
     return out.value
@@ -137,9 +140,9 @@ def _check_tensor(t, name):
         raise ValueError(f"{name} must be contiguous (dense NCHW / KCRS)")
 
 
-def _workspace(op, dims, dt, workspace, device):
+def _workspace(op, dims, dt, workspace, device, dilation=(1, 1)):
     import torch
-    need = conv2d_workspace_size(op, dims, dt)
+    need = conv2d_workspace_size(op, dims, dt, dilation)
     if need == 0:
         return None, 0
     if workspace is None:
@@ -165,11 +168,13 @@ def _mode(flip):
     return MODE_CONVOLUTION if flip else MODE_CROSS_CORRELATION
 
 
-def _call(name, dims, dt, a, b, out, workspace, op, stream, bias=None, beta=0.0, flip=False):
-    """Forward / backward-data through the fused-epilogue entry point (bias None, beta 0 and
-    flip False are the plain op)."""
-    ws, wsb = _workspace(op, dims, dt, workspace, out.device)
-    rc = getattr(load_library(), name + "_ex")(*[int(v) for v in dims], dt, _mode(flip), _ptr(a), _ptr(b), _ptr(bias),
+def _call(name, dims, dt, a, b, out, workspace, op, stream, bias=None, beta=0.0, flip=False, dilation=(1, 1)):
+    """Forward / backward-data through the fused-epilogue entry point (bias None, beta 0,
+    flip False and dilation 1 are the plain op)."""
+    ws, wsb = _workspace(op, dims, dt, workspace, out.device, dilation)
+    dh, dw = _pair(dilation)
+    rc = getattr(load_library(), name + "_ex")(*[int(v) for v in dims], dh, dw, dt, _mode(flip), _ptr(a), _ptr(b),
+                                               _ptr(bias),
                                                ctypes.c_float(float(beta)), _ptr(out), _ptr(ws),
                                                ctypes.c_size_t(wsb), _stream_ptr(stream))
     if rc:
@@ -177,10 +182,16 @@ def _call(name, dims, dt, a, b, out, workspace, op, stream, bias=None, beta=0.0,
     return out
 
 
-def conv2d_fwd(x, w, pad=0, stride=1, out=None, workspace=None, stream=None, bias=None, beta=0.0, flip=False):
+def _eff(k, d):
+    return d * (k - 1) + 1  # extent of a dilated filter
+
+
+def conv2d_fwd(x, w, pad=0, stride=1, out=None, workspace=None, stream=None, bias=None, beta=0.0, flip=False,
+               dilation=1):
     """y = conv2d(x, w) (+ bias[k]) (+ beta * y): x (N,C,H,W), w (K,C,R,S) -> y (N,K,P,Q),
     same dtype.  With beta != 0, `out` holds the values to accumulate onto.  flip=True is
-    convolution mode (the filter rotated by 180 degrees); the default is cross-correlation."""
+    convolution mode (the filter rotated by 180 degrees); the default is cross-correlation.
+    dilation (int or pair): filter tap (r, s) reads input offset (r*dil_h, s*dil_w)."""
     import torch
     _check_tensor(x, "x")
     _check_tensor(w, "w")
@@ -190,14 +201,16 @@ def conv2d_fwd(x, w, pad=0, stride=1, out=None, workspace=None, stream=None, bia
         raise ValueError("x / w channel count or dtype mismatch")
     ph, pw = _pair(pad)
     sh, sw = _pair(stride)
-    P, Q = conv2d_output_dim(H, ph, R, sh), conv2d_output_dim(W, pw, S, sw)
+    dh, dw = _pair(dilation)
+    P, Q = conv2d_output_dim(H, ph, _eff(R, dh), sh), conv2d_output_dim(W, pw, _eff(S, dw), sw)
     if out is None:
         if beta != 0.0:
             raise ValueError("beta != 0 accumulates onto `out`, which must then be given")
         out = torch.empty((N, K, P, Q), dtype=x.dtype, device=x.device)
     _check_vec(bias, K, x, "bias")
     dims = (N, C, H, W, K, R, S, ph, pw, sh, sw, P, Q)
-    return _call("conv2d_fwd", dims, _dtype_code(x), x, w, out, workspace, OP_FWD, stream, bias, beta, flip)
+    return _call("conv2d_fwd", dims, _dtype_code(x), x, w, out, workspace, OP_FWD, stream, bias, beta, flip,
+                 (dh, dw))
 
 
 def conv2d_fwd_noalloc(x, w, pad=0, stride=1, out=None, stream=None):
@@ -226,7 +239,7 @@ def conv2d_fwd_noalloc(x, w, pad=0, stride=1, out=None, stream=None):
 
 
 def conv2d_bwd_data(dy, w, x_hw, pad=0, stride=1, out=None, workspace=None, stream=None, bias=None, beta=0.0,
-                    flip=False):
+                    flip=False, dilation=1):
     """dx (N,C,H,W) from dy (N,K,P,Q) and w (K,C,R,S); x_hw = (H, W).  Optional epilogue:
     + bias[c] (the bias of a deconvolution) + beta * dx (`out` required when beta != 0)."""
     import torch
@@ -246,11 +259,11 @@ def conv2d_bwd_data(dy, w, x_hw, pad=0, stride=1, out=None, workspace=None, stre
     _check_vec(bias, C, dy, "bias")
     dims = (N, C, H, W, K, R, S, ph, pw, sh, sw, P, Q)
     return _call("conv2d_bwd_data", dims, _dtype_code(dy), dy, w, out, workspace, OP_BWD_DATA, stream,
-                 bias, beta, flip)
+                 bias, beta, flip, _pair(dilation))
 
 
 def conv2d_bwd_filter(x, dy, rs, pad=0, stride=1, out=None, workspace=None, stream=None, beta=0.0,
-                      db_k=None, db_c=None, flip=False):
+                      db_k=None, db_c=None, flip=False, dilation=1):
     """dw (K,C,R,S) from x (N,C,H,W) and dy (N,K,P,Q); rs = (R, S).
 
     Optional: beta accumulates onto `out` (dw) and onto the bias gradients; db_k (K values)
@@ -275,8 +288,9 @@ def conv2d_bwd_filter(x, dy, rs, pad=0, stride=1, out=None, workspace=None, stre
     _check_vec(db_c, C, x, "db_c")
     dims = (N, C, H, W, K, R, S, ph, pw, sh, sw, P, Q)
     dt = _dtype_code(x)
-    ws, wsb = _workspace(OP_BWD_FILTER, dims, dt, workspace, out.device)
-    rc = load_library().conv2d_bwd_filter_ex(*[int(v) for v in dims], dt, _mode(flip), _ptr(x), _ptr(dy),
+    dh, dw = _pair(dilation)
+    ws, wsb = _workspace(OP_BWD_FILTER, dims, dt, workspace, out.device, (dh, dw))
+    rc = load_library().conv2d_bwd_filter_ex(*[int(v) for v in dims], dh, dw, dt, _mode(flip), _ptr(x), _ptr(dy),
                                              ctypes.c_float(float(beta)), _ptr(out), _ptr(db_k), _ptr(db_c),
                                              _ptr(ws), ctypes.c_size_t(wsb), _stream_ptr(stream))
     if rc:
@@ -285,13 +299,13 @@ def conv2d_bwd_filter(x, dy, rs, pad=0, stride=1, out=None, workspace=None, stre
 
 
 def deconv2d_fwd(inp, wt, out_hw, pad=0, stride=1, out=None, workspace=None, stream=None, bias=None, beta=0.0,
-                 flip=False):
+                 flip=False, dilation=1):
     """Transposed convolution: inp (N,Ci,Hi,Wi), wt (Ci,Co,R,S) -> (N,Co,Ho,Wo), optionally
     + bias[co] + beta * out.
 
     Runs conv2d_bwd_data with K = Ci (deconv input channels), C = Co, P = Hi, H = Ho."""
     return conv2d_bwd_data(inp, wt, out_hw, pad, stride, out=out, workspace=workspace, stream=stream,
-                           bias=bias, beta=beta, flip=flip)
+                           bias=bias, beta=beta, flip=flip, dilation=dilation)
 
 
 # ------------------------------------------------------------------ 1-D
@@ -302,29 +316,32 @@ def _one(v):
     return int(v if isinstance(v, int) else v[0])
 
 
-def conv1d_fwd(x, w, pad=0, stride=1, out=None, workspace=None, stream=None, bias=None, beta=0.0, flip=False):
+def conv1d_fwd(x, w, pad=0, stride=1, out=None, workspace=None, stream=None, bias=None, beta=0.0, flip=False,
+               dilation=1):
     """y (N,K,Q) = conv1d(x (N,C,W), w (K,C,S))."""
     o4 = out.unsqueeze(2) if out is not None else None
     y = conv2d_fwd(x.unsqueeze(2), w.unsqueeze(2), (0, _one(pad)), (1, _one(stride)), out=o4,
-                   workspace=workspace, stream=stream, bias=bias, beta=beta, flip=flip)
+                   workspace=workspace, stream=stream, bias=bias, beta=beta, flip=flip, dilation=(1, _one(dilation)))
     return y.squeeze(2) if out is None else out
 
 
 def conv1d_bwd_data(dy, w, x_w, pad=0, stride=1, out=None, workspace=None, stream=None, bias=None, beta=0.0,
-                    flip=False):
+                    flip=False, dilation=1):
     """dx (N,C,W) from dy (N,K,Q) and w (K,C,S); x_w = W."""
     o4 = out.unsqueeze(2) if out is not None else None
     dx = conv2d_bwd_data(dy.unsqueeze(2), w.unsqueeze(2), (1, int(x_w)), (0, _one(pad)), (1, _one(stride)), out=o4,
-                         workspace=workspace, stream=stream, bias=bias, beta=beta, flip=flip)
+                         workspace=workspace, stream=stream, bias=bias, beta=beta, flip=flip,
+                         dilation=(1, _one(dilation)))
     return dx.squeeze(2) if out is None else out
 
 
 def conv1d_bwd_filter(x, dy, s, pad=0, stride=1, out=None, workspace=None, stream=None, beta=0.0, db_k=None,
-                      db_c=None, flip=False):
+                      db_c=None, flip=False, dilation=1):
     """dw (K,C,S) from x (N,C,W) and dy (N,K,Q); s = S."""
     o4 = out.unsqueeze(2) if out is not None else None
     dw = conv2d_bwd_filter(x.unsqueeze(2), dy.unsqueeze(2), (1, int(s)), (0, _one(pad)), (1, _one(stride)), out=o4,
-                           workspace=workspace, stream=stream, beta=beta, db_k=db_k, db_c=db_c, flip=flip)
+                           workspace=workspace, stream=stream, beta=beta, db_k=db_k, db_c=db_c, flip=flip,
+                           dilation=(1, _one(dilation)))
     return dw.squeeze(2) if out is None else out
 
 

@@ -38,6 +38,7 @@ constexpr size_t kDefaultSmemOptin = 232448;      // 227 KB
 
 struct Desc {
   int N, C, H, W, K, R, S, ph, pw, sh, sw, P, Q, dt;
+  int dh = 1, dw = 1;  // dilation: filter tap (r, s) sits at (r*dh, s*dw) in the window
 };
 
 int floor_div(int a, int b) { return a >= 0 ? a / b : -((-a + b - 1) / b); }
@@ -56,7 +57,11 @@ int validate(const Desc& d) {
     return CONV2D_ERR_BAD_DESC;
   if (d.dt != CONV2D_DTYPE_F32 && d.dt != CONV2D_DTYPE_BF16) return CONV2D_ERR_DTYPE;
   // Overflow-safe: the sums below are bounded by 2^31 + 2^31.
-  const long long P = out_dim(d.H, d.ph, d.R, d.sh), Q = out_dim(d.W, d.pw, d.S, d.sw);
+  if (d.dh < 1 || d.dw < 1) return CONV2D_ERR_BAD_DESC;
+  // extent of the dilated filter (overflow-safe: R, S, dh, dw are positive ints)
+  const long long Re = (long long)d.dh * (d.R - 1) + 1, Se = (long long)d.dw * (d.S - 1) + 1;
+  if (Re > INT_MAX || Se > INT_MAX) return CONV2D_ERR_BAD_DESC;
+  const long long P = out_dim(d.H, d.ph, (int)Re, d.sh), Q = out_dim(d.W, d.pw, (int)Se, d.sw);
   if (P < 1 || Q < 1 || d.P != P || d.Q != Q) return CONV2D_ERR_SHAPE;
   const long long lim = (1ll << 31);
   if ((long long)d.N * d.C * d.H * d.W >= lim || (long long)d.N * d.K * d.P * d.Q >= lim ||
@@ -262,7 +267,7 @@ int build_fwd(const Desc& d0, const void* x, const void* w, void* y, void* ws, c
   p.Cd = d.K;
   p.Hd = d.P;
   p.Wd = d.Q;
-  const int mh = (d.R - 1) / d.sh, mw = (d.S - 1) / d.sw;
+  const int mh = (d.dh * (d.R - 1)) / d.sh, mw = (d.dw * (d.S - 1)) / d.sw;
   const int CHUNK = d.dt == 0 ? 4 : 8;
   p.WL = d.Q + mw;
   p.EL = d.P + mh;
@@ -286,8 +291,9 @@ int build_fwd(const Desc& d0, const void* x, const void* w, void* y, void* ws, c
   int max_off = 0;
   for (int r = 0; r < d.R; ++r)
     for (int s = 0; s < d.S; ++s) {
-      tpl.push_back((r % d.sh) * d.sw + (s % d.sw));
-      toff.push_back((r / d.sh) * p.WL + s / d.sw);
+      const int re = r * d.dh, se = s * d.dw;  // the tap's place in the dilated window
+      tpl.push_back((re % d.sh) * d.sw + (se % d.sw));
+      toff.push_back((re / d.sh) * p.WL + se / d.sw);
       tr.push_back(r);
       ts.push_back(s);
       max_off = std::max(max_off, toff.back());
@@ -323,25 +329,31 @@ int build_bwd_data(const Desc& d0, const void* dy, const void* w, void* dx, void
   p.Cd = d.C;
   p.Hd = d.H;
   p.Wd = d.W;
-  // Per output phase a (rows with (h + pad_h) mod stride_h == a): taps r = a + sh*t,
-  // output row h = sh*u + a - pad_h, dy row p = u - t.  Same for columns.
-  auto phase_dims = [](int H, int pad, int R, int st, std::vector<int>& T, std::vector<int>& ulo,
-                       std::vector<int>& U) {
+  // Per output phase a (rows with (h + pad_h) mod stride_h == a): the taps r with
+  // r*dh = a (mod stride_h), at t_r = (r*dh - a) / stride_h; output row h = sh*u + a - pad_h
+  // reads dy row p = u - t_r.  Th[a] = 1 + the largest t_r (0: no tap reaches the phase).
+  // Same for columns.
+  auto phase_dims = [](int H, int pad, int R, int dil, int st, std::vector<int>& T, std::vector<int>& ulo,
+                       std::vector<int>& U, std::vector<std::vector<int>>& taps) {
     T.assign(st, 0);
     ulo.assign(st, 0);
     U.assign(st, 0);
+    taps.assign(st, {});
     for (int a = 0; a < st; ++a) {
-      int cnt = 0;
-      for (int r = a; r < R; r += st) ++cnt;
-      T[a] = cnt;
+      for (int r = 0; r < R; ++r)
+        if ((r * dil) % st == a) {
+          taps[a].push_back(r);
+          T[a] = std::max(T[a], (r * dil - a) / st + 1);
+        }
       ulo[a] = ceil_div_i(pad - a, st);
       const int uhi = floor_div(H - 1 + pad - a, st);
       U[a] = std::max(0, uhi - ulo[a] + 1);
     }
   };
   std::vector<int> Th, uloh, Uh, Tw, ulow, Uw;
-  phase_dims(d.H, d.ph, d.R, d.sh, Th, uloh, Uh);
-  phase_dims(d.W, d.pw, d.S, d.sw, Tw, ulow, Uw);
+  std::vector<std::vector<int>> tapsh, tapsw;
+  phase_dims(d.H, d.ph, d.R, d.dh, d.sh, Th, uloh, Uh, tapsh);
+  phase_dims(d.W, d.pw, d.S, d.dw, d.sw, Tw, ulow, Uw, tapsw);
   int T0h = 0, T0w = 0;
   for (int a = 0; a < d.sh; ++a)
     if (Th[a] > 0) T0h = std::max(T0h, Th[a] - 1 - uloh[a]);
@@ -381,14 +393,15 @@ int build_bwd_data(const Desc& d0, const void* dy, const void* w, void* dx, void
       p.ph_off_w[ph] = d.sw * ulow[c] + c - d.pw;
       const int begin = (int)tpl.size();
       p.ph_tap_begin[ph] = begin;
-      for (int t = 0; t < Th[a]; ++t)
-        for (int t2 = 0; t2 < Tw[c]; ++t2) {
+      for (const int r : tapsh[a])
+        for (const int s2 : tapsw[c]) {
+          const int t = (r * d.dh - a) / d.sh, t2 = (s2 * d.dw - c) / d.sw;
           const int roff = uloh[a] - t + T0h;
           const int coff = ulow[c] - t2 + T0w;
           tpl.push_back(0);
           toff.push_back(roff * WL + coff);
-          tr.push_back(a + d.sh * t);
-          ts.push_back(c + d.sw * t2);
+          tr.push_back(r);
+          ts.push_back(s2);
           max_off = std::max(max_off, toff.back());
         }
       if ((int)tpl.size() > begin) order_phase_taps(tpl, toff, tr, ts, begin, 1 << 20, pair);
@@ -513,7 +526,7 @@ int build_bwd_filter_impl(const Desc& d0, const void* x, const void* dy, void* d
   const int CHUNK = d.dt == 0 ? 4 : 8;
   const int ESZ = d.dt == 0 ? 4 : 2;
   const int BUFP = d.dt == 0 ? 32 : 64;  // positions per 32-column TMEM buffer
-  const int mh = (d.R - 1) / d.sh, mw = (d.S - 1) / d.sw;
+  const int mh = (d.dh * (d.R - 1)) / d.sh, mw = (d.dw * (d.S - 1)) / d.sw;
   p.NK = d.K <= 16 ? 16 : std::min(round_up(d.K, 32), 256);
   p.n_ntiles = (d.K + p.NK - 1) / p.NK;
   // Copy-engine staging: unit column stride, rows and planes of whole 16-byte chunks, aligned
@@ -527,7 +540,7 @@ int build_bwd_filter_impl(const Desc& d0, const void* x, const void* dy, void* d
   bool tma = allow_tma && d.sw == 1 && d.W % CHUNK == 0 && d.Q % CHUNK == 0 && ((uintptr_t)x & 15) == 0 &&
              ((uintptr_t)dy & 15) == 0 && encode_tiled_fn() != nullptr;
   p.TRU = 1;
-  if (tma && allow_rowshare && d.sh == 1 && d.C >= 32 && d.R > 1 && 2 * p.NK <= 384)
+  if (tma && allow_rowshare && d.sh == 1 && d.dh == 1 && d.C >= 32 && d.R > 1 && 2 * p.NK <= 384)
     p.TRU = std::min(std::min(d.R, 4), 384 / p.NK);
   if (allow_rowshare && p.TRU == 1) return CONV2D_ERR_UNSUPPORTED;  // the caller plans without sharing
   if (tma) {
@@ -569,9 +582,10 @@ int build_bwd_filter_impl(const Desc& d0, const void* x, const void* dy, void* d
   for (int r = 0; r < d.R; ++r)
     for (int s = 0; s < d.S; ++s) {
       const int t = r * d.S + s;
-      p.tap_plane[t] = (r % d.sh) * d.sw + (s % d.sw);
-      p.tap_off[t] = (r / d.sh) * p.WL + s / d.sw;
-      p.tap_rc[t] = ((r / d.sh) << 16) | (s / d.sw);
+      const int re = r * d.dh, se = s * d.dw;  // the tap's place in the dilated window
+      p.tap_plane[t] = (re % d.sh) * d.sw + (se % d.sw);
+      p.tap_off[t] = (re / d.sh) * p.WL + se / d.sw;
+      p.tap_rc[t] = ((re / d.sh) << 16) | (se / d.sw);
     }
   p.vec_dy = d.Q % CHUNK == 0 && p.WL % CHUNK == 0 && ((uintptr_t)dy & 15) == 0;
   // Row units of 32 TMEM lanes: 32 channels of one tap, or (C < 32) TPU taps x C channels.
@@ -821,8 +835,15 @@ int conv2d_output_dim(int in, int pad, int k, int stride, int* out) {
 
 int conv2d_workspace_size(int op, int N, int C, int H, int W, int K, int R, int S, int pad_h, int pad_w,
                           int stride_h, int stride_w, int P, int Q, int dtype, size_t* bytes) {
+  return conv2d_workspace_size_ex(op, N, C, H, W, K, R, S, pad_h, pad_w, stride_h, stride_w, P, Q, 1, 1, dtype,
+                                  bytes);
+}
+
+int conv2d_workspace_size_ex(int op, int N, int C, int H, int W, int K, int R, int S, int pad_h, int pad_w,
+                             int stride_h, int stride_w, int P, int Q, int dil_h, int dil_w, int dtype,
+                             size_t* bytes) {
   if (!bytes) return CONV2D_ERR_NULLPTR;
-  const Desc d{N, C, H, W, K, R, S, pad_h, pad_w, stride_h, stride_w, P, Q, dtype};
+  const Desc d{N, C, H, W, K, R, S, pad_h, pad_w, stride_h, stride_w, P, Q, dtype, dil_h, dil_w};
   int rc = validate(d);
   if (rc) return rc;
   const PlanKey key = make_key(op, d, nullptr, nullptr, nullptr, nullptr);
@@ -906,9 +927,9 @@ int conv2d_fwd(int N, int C, int H, int W, int K, int R, int S, int pad_h, int p
 }
 
 int conv2d_fwd_ex(int N, int C, int H, int W, int K, int R, int S, int pad_h, int pad_w, int stride_h,
-                  int stride_w, int P, int Q, int dtype, int mode, const void* x, const void* w, const void* bias,
-                  float beta, void* y, void* workspace, size_t workspace_bytes, void* stream) {
-  const Desc d{N, C, H, W, K, R, S, pad_h, pad_w, stride_h, stride_w, P, Q, dtype};
+                  int stride_w, int P, int Q, int dil_h, int dil_w, int dtype, int mode, const void* x, const void* w,
+                  const void* bias, float beta, void* y, void* workspace, size_t workspace_bytes, void* stream) {
+  const Desc d{N, C, H, W, K, R, S, pad_h, pad_w, stride_h, stride_w, P, Q, dtype, dil_h, dil_w};
   return run_tap(CONV2D_OP_FWD, d, x, w, bias, beta, mode, y, workspace, workspace_bytes, stream);
 }
 
@@ -921,24 +942,26 @@ int conv2d_bwd_data(int N, int C, int H, int W, int K, int R, int S, int pad_h, 
 }
 
 int conv2d_bwd_data_ex(int N, int C, int H, int W, int K, int R, int S, int pad_h, int pad_w, int stride_h,
-                       int stride_w, int P, int Q, int dtype, int mode, const void* dy, const void* w,
-                       const void* bias, float beta, void* dx, void* workspace, size_t workspace_bytes, void* stream) {
-  const Desc d{N, C, H, W, K, R, S, pad_h, pad_w, stride_h, stride_w, P, Q, dtype};
+                       int stride_w, int P, int Q, int dil_h, int dil_w, int dtype, int mode, const void* dy,
+                       const void* w, const void* bias, float beta, void* dx, void* workspace, size_t workspace_bytes,
+                       void* stream) {
+  const Desc d{N, C, H, W, K, R, S, pad_h, pad_w, stride_h, stride_w, P, Q, dtype, dil_h, dil_w};
   return run_tap(CONV2D_OP_BWD_DATA, d, dy, w, bias, beta, mode, dx, workspace, workspace_bytes, stream);
 }
 
 int conv2d_bwd_filter(int N, int C, int H, int W, int K, int R, int S, int pad_h, int pad_w, int stride_h,
                       int stride_w, int P, int Q, int dtype, const void* x, const void* dy, void* dw,
                       void* workspace, size_t workspace_bytes, void* stream) {
-  return conv2d_bwd_filter_ex(N, C, H, W, K, R, S, pad_h, pad_w, stride_h, stride_w, P, Q, dtype,
+  return conv2d_bwd_filter_ex(N, C, H, W, K, R, S, pad_h, pad_w, stride_h, stride_w, P, Q, 1, 1, dtype,
                               CONV2D_MODE_CROSS_CORRELATION, x, dy, 0.f, dw, nullptr, nullptr, workspace,
                               workspace_bytes, stream);
 }
 
 int conv2d_bwd_filter_ex(int N, int C, int H, int W, int K, int R, int S, int pad_h, int pad_w, int stride_h,
-                         int stride_w, int P, int Q, int dtype, int mode, const void* x, const void* dy, float beta,
-                         void* dw, void* db_k, void* db_c, void* workspace, size_t workspace_bytes, void* stream) {
-  const Desc d{N, C, H, W, K, R, S, pad_h, pad_w, stride_h, stride_w, P, Q, dtype};
+                         int stride_w, int P, int Q, int dil_h, int dil_w, int dtype, int mode, const void* x,
+                         const void* dy, float beta, void* dw, void* db_k, void* db_c, void* workspace,
+                         size_t workspace_bytes, void* stream) {
+  const Desc d{N, C, H, W, K, R, S, pad_h, pad_w, stride_h, stride_w, P, Q, dtype, dil_h, dil_w};
   if (mode != CONV2D_MODE_CROSS_CORRELATION && mode != CONV2D_MODE_CONVOLUTION) return CONV2D_ERR_BAD_DESC;
   int rc = validate(d);
   if (rc) return rc;

@@ -190,21 +190,42 @@ def _rot180(w):
     return np.ascontiguousarray(_f64(w)[:, :, ::-1, ::-1])
 
 
-def conv2d_fwd_ex(x, w, bias=None, beta=0.0, y_old=None, pad=0, stride=1, flip=False) -> np.ndarray:
+# Dilation (cuDNN's convolution-descriptor dilation, which the SystemDS page sets to 1, 1):
+# tap (r, s) reads the input at offset (r*dh, s*dw) of the window.  That is the undilated op
+# with the zero-inserted filter of extent (dh*(R-1)+1, dw*(S-1)+1) holding w[r, s] at
+# (r*dh, s*dw); the filter gradient is that op's gradient read back at those places.
+
+def dilate_filter(w, dilation) -> np.ndarray:
+    dh, dw = _pair(dilation)
+    w = _f64(w)
+    K, C, R, S = w.shape
+    out = np.zeros((K, C, dh * (R - 1) + 1, dw * (S - 1) + 1))
+    out[:, :, ::dh, ::dw] = w
+    return out
+
+
+def conv2d_fwd_ex(x, w, bias=None, beta=0.0, y_old=None, pad=0, stride=1, flip=False, dilation=1) -> np.ndarray:
     """y = conv(x, w) + bias[k] + beta * y_old (bias per output channel k, axis 1 of y); flip:
-    convolution mode."""
-    return _epilogue(conv2d_fwd(x, _rot180(w) if flip else w, pad, stride), bias, beta, y_old, 1)
+    convolution mode; dilation: see above."""
+    wf = dilate_filter(_rot180(w) if flip else w, dilation)
+    return _epilogue(conv2d_fwd(x, wf, pad, stride), bias, beta, y_old, 1)
 
 
-def conv2d_bwd_data_ex(dy, w, x_hw, bias=None, beta=0.0, dx_old=None, pad=0, stride=1, flip=False) -> np.ndarray:
+def conv2d_bwd_data_ex(dy, w, x_hw, bias=None, beta=0.0, dx_old=None, pad=0, stride=1, flip=False,
+                       dilation=1) -> np.ndarray:
     """dx = bwd_data(dy, w) + bias[c] + beta * dx_old (bias per channel c of dx: the bias of
-    the deconvolution whose output dx is); flip: convolution mode."""
-    return _epilogue(conv2d_bwd_data(dy, _rot180(w) if flip else w, x_hw, pad, stride), bias, beta, dx_old, 1)
+    the deconvolution whose output dx is); flip: convolution mode; dilation: see above."""
+    wf = dilate_filter(_rot180(w) if flip else w, dilation)
+    return _epilogue(conv2d_bwd_data(dy, wf, x_hw, pad, stride), bias, beta, dx_old, 1)
 
 
-def conv2d_bwd_filter_ex(x, dy, rs, beta=0.0, dw_old=None, pad=0, stride=1, flip=False) -> np.ndarray:
-    """dw = bwd_filter(x, dy) + beta * dw_old; flip: the gradient of the rotated filter."""
-    dw = conv2d_bwd_filter(x, dy, rs, pad, stride)
+def conv2d_bwd_filter_ex(x, dy, rs, beta=0.0, dw_old=None, pad=0, stride=1, flip=False, dilation=1) -> np.ndarray:
+    """dw = bwd_filter(x, dy) + beta * dw_old; flip: the gradient of the rotated filter;
+    dilation: see above."""
+    dh, dwl = _pair(dilation)
+    R, S = rs
+    big = conv2d_bwd_filter(x, dy, (dh * (R - 1) + 1, dwl * (S - 1) + 1), pad, stride)
+    dw = np.ascontiguousarray(big[:, :, ::dh, ::dwl])
     return _epilogue(_rot180(dw) if flip else dw, None, beta, dw_old, 0)
 
 

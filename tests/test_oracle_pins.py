@@ -466,3 +466,55 @@ def test_convolution_mode_adjoint_identities():
             # the unflipped filter gradient does not satisfy the flipped identity
             c0 = np.vdot(w, oracle.conv2d_bwd_filter(x, dy, (R, S), (ph, pw), (sh, sw)))
             assert abs(a - c0) > 1e-8 * max(1.0, abs(a))
+
+
+# --------------------------------------------------------------------------- dilation
+# cuDNN's convolution-descriptor dilation (set to 1, 1 on the SystemDS page): tap (r, s) reads
+# the window at (r*dh, s*dw).  Pinned by PyTorch CPU fp64 for all three ops and by the adjoint
+# identities.
+DIL_CASES = [
+    ((2, 3, 12, 13, 4, 3, 3, 2, 2, 1, 1), (2, 2)),
+    ((1, 2, 17, 15, 3, 3, 2, 2, 1, 2, 1), (2, 3)),
+    ((2, 4, 11, 16, 5, 2, 3, 1, 2, 1, 2), (3, 2)),
+]
+
+
+def _dil_out(H, W, R, S, ph, pw, sh, sw, dil):
+    dh, dw = dil
+    return oracle.output_dim(H, ph, dh * (R - 1) + 1, sh), oracle.output_dim(W, pw, dw * (S - 1) + 1, sw)
+
+
+@pytest.mark.parametrize("case,dil", DIL_CASES)
+def test_dilation_torch_witness(case, dil):
+    torch = pytest.importorskip("torch")
+    import torch.nn.functional as F
+    N, C, H, W, K, R, S, ph, pw, sh, sw = case
+    P, Q = _dil_out(H, W, R, S, ph, pw, sh, sw, dil)
+    x = RNG.standard_normal((N, C, H, W))
+    w = RNG.standard_normal((K, C, R, S))
+    dy = RNG.standard_normal((N, K, P, Q))
+    tx, tw, tdy = (torch.from_numpy(a) for a in (x, w, dy))
+    kw = dict(stride=(sh, sw), padding=(ph, pw), dilation=dil)
+    refs = (F.conv2d(tx, tw, **kw).numpy(),
+            torch.nn.grad.conv2d_input((N, C, H, W), tw, tdy, **kw).numpy(),
+            torch.nn.grad.conv2d_weight(tx, (K, C, R, S), tdy, **kw).numpy())
+    gots = (oracle.conv2d_fwd_ex(x, w, None, 0.0, None, (ph, pw), (sh, sw), dilation=dil),
+            oracle.conv2d_bwd_data_ex(dy, w, (H, W), None, 0.0, None, (ph, pw), (sh, sw), dilation=dil),
+            oracle.conv2d_bwd_filter_ex(x, dy, (R, S), 0.0, None, (ph, pw), (sh, sw), dilation=dil))
+    for got, ref in zip(gots, refs):
+        assert got.shape == ref.shape
+        assert np.max(np.abs(got - ref)) <= 1e-12 * max(1.0, np.max(np.abs(ref)))
+
+
+@pytest.mark.parametrize("case,dil", DIL_CASES)
+def test_dilation_adjoint_identities(case, dil):
+    N, C, H, W, K, R, S, ph, pw, sh, sw = case
+    P, Q = _dil_out(H, W, R, S, ph, pw, sh, sw, dil)
+    x = RNG.standard_normal((N, C, H, W))
+    w = RNG.standard_normal((K, C, R, S))
+    dy = RNG.standard_normal((N, K, P, Q))
+    for flip in (False, True):
+        a = np.vdot(oracle.conv2d_fwd_ex(x, w, None, 0.0, None, (ph, pw), (sh, sw), flip, dil), dy)
+        b = np.vdot(x, oracle.conv2d_bwd_data_ex(dy, w, (H, W), None, 0.0, None, (ph, pw), (sh, sw), flip, dil))
+        c = np.vdot(w, oracle.conv2d_bwd_filter_ex(x, dy, (R, S), 0.0, None, (ph, pw), (sh, sw), flip, dil))
+        assert abs(a - b) <= 1e-10 * max(1.0, abs(a)) and abs(a - c) <= 1e-10 * max(1.0, abs(a))

@@ -338,3 +338,53 @@ def test_conv1d_wrappers(cg, flip):
         assert tuple(got.shape) == ref.shape
         err = float(np.abs(got.double().cpu().numpy() - ref).max())
         assert err <= 2e-3 * math.sqrt(L) * sc
+
+
+# ------------------------------------------------------------------ dilation
+DIL_GPU_CASES = [
+    ((2, 8, 12, 13, 6, 3, 3, 2, 2, 1, 1), (2, 2)),
+    ((1, 5, 20, 17, 7, 3, 2, 2, 1, 2, 1), (2, 3)),
+    ((2, 64, 16, 16, 64, 3, 3, 2, 2, 1, 1), (2, 2)),    # copy-engine staging, no row-tap sharing
+    ((1, 33, 15, 16, 40, 2, 3, 1, 2, 1, 2), (3, 2)),
+    ((2, 3, 21, 21, 16, 3, 3, 3, 3, 2, 2), (3, 3)),     # few channels, stride 2
+]
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("case,dil", DIL_GPU_CASES)
+def test_dilation_parity(cg, case, dil, dtype):
+    N, C, H, Wd, K, R, S, ph, pw, sh, sw = case
+    dh, dw_ = dil
+    P = (H + 2 * ph - dh * (R - 1) - 1) // sh + 1
+    Q = (Wd + 2 * pw - dw_ * (S - 1) - 1) // sw + 1
+    g = torch.Generator().manual_seed(9500 + DIL_GPU_CASES.index((case, dil)))
+    tdt = torch.float32 if dtype == "f32" else torch.bfloat16
+    x = torch.randn(N, C, H, Wd, generator=g).to(tdt)
+    w = torch.randn(K, C, R, S, generator=g).to(tdt)
+    dy = torch.randn(N, K, P, Q, generator=g).to(tdt)
+    pad, st = (ph, pw), (sh, sw)
+    flip = DIL_GPU_CASES.index((case, dil)) % 2 == 1
+    xd, wd, dyd = x.to(DEV), w.to(DEV), dy.to(DEV)
+    y = _poisoned((N, K, P, Q), tdt)
+    cg.conv2d_fwd(xd, wd, pad, st, out=y, dilation=dil, flip=flip)
+    dx = _poisoned((N, C, H, Wd), tdt)
+    cg.conv2d_bwd_data(dyd, wd, (H, Wd), pad, st, out=dx, dilation=dil, flip=flip)
+    dwt = _poisoned((K, C, R, S), tdt)
+    cg.conv2d_bwd_filter(xd, dyd, (R, S), pad, st, out=dwt, dilation=dil, flip=flip)
+    cg.conv2d_device_status()
+    amax = lambda t: float(t.abs().max())
+    checks = (("fwd", y, oracle.conv2d_fwd_ex(x, w, None, 0.0, None, pad, st, flip, dil), amax(x) * amax(w), C * R * S),
+              ("bwd_data", dx, oracle.conv2d_bwd_data_ex(dy, w, (H, Wd), None, 0.0, None, pad, st, flip, dil),
+               amax(dy) * amax(w), K * R * S),
+              ("bwd_filter", dwt, oracle.conv2d_bwd_filter_ex(x, dy, (R, S), 0.0, None, pad, st, flip, dil),
+               amax(x) * amax(dy), N * P * Q))
+    for op, got, ref, scale, L in checks:
+        got = got.double().cpu().numpy()
+        assert np.all(np.isfinite(got)), f"{case}/{dil}/{op}: unwritten element"
+        if dtype == "f32":
+            err = float(np.abs(got - ref).max())
+            assert err <= 2e-3 * math.sqrt(L) * scale, f"{case}/{dil}/{op}: {err:.3e}"
+        else:
+            den = float(np.linalg.norm(ref))
+            rel = float(np.linalg.norm(got - ref)) / den if den > 0 else float(np.linalg.norm(got))
+            assert rel <= 1e-2, f"{case}/{dil}/{op}: {rel:.3e}"
