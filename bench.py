@@ -217,6 +217,9 @@ def run_ours(args, rank, world):
     dbk = torch.empty(pb.K, dtype=x.dtype, device=dev)
     dbc = torch.empty(pb.C, dtype=x.dtype, device=dev)
     wsz_f = cg.conv2d_workspace_size(2, pb.dims(), dt)
+    wsz_d = cg.conv2d_workspace_size(2, (pb.N, pb.C, pb.H, pb.W, pb.K, pb.R, pb.S, 2 * pb.pad_h, 2 * pb.pad_w,
+                                         pb.stride_h, pb.stride_w, pb.P, pb.Q), dt, (2, 2))
+    ws_d = torch.empty(max(wsz_d, 16), dtype=torch.uint8, device=dev)
     ws_f = torch.empty(max(wsz_f, 16), dtype=torch.uint8, device=dev) if wsz_f > ws.numel() else ws
 
     def ex_call(which):
@@ -242,6 +245,36 @@ def run_ours(args, rank, world):
         torch.cuda.synchronize()
         ex_ms[which] = sum(a.elapsed_time(b) for a, b in pairs) / len(pairs)
     cg.conv2d_device_status(stream)
+    # dilation 2 on the same layer (pad 2 keeps P = H, Q = W): the three ops, timed alike
+    dil_ms = {}
+    for op in OPS:
+        def dcall():
+            if op == "fwd":
+                cg.conv2d_fwd(xd, wd, (2 * pb.pad_h, 2 * pb.pad_w), st, out=y, workspace=ws, stream=stream,
+                              dilation=2)
+            elif op == "bwd_data":
+                cg.conv2d_bwd_data(dyd, wd, (pb.H, pb.W), (2 * pb.pad_h, 2 * pb.pad_w), st, out=dx, workspace=ws,
+                                   stream=stream, dilation=2)
+            else:
+                cg.conv2d_bwd_filter(xd, dyd, (pb.R, pb.S), (2 * pb.pad_h, 2 * pb.pad_w), st, out=dw,
+                                     workspace=ws_d, stream=stream, dilation=2)
+        for _ in range(args.warmup):
+            flush.zero_()
+            dcall()
+        pairs = []
+        for _ in range(min(K, 50)):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            dcall()
+            b.record(stream)
+            pairs.append((a, b))
+        torch.cuda.synchronize()
+        dil_ms[op] = sum(a.elapsed_time(b) for a, b in pairs) / len(pairs)
+    cg.conv2d_device_status(stream)
+    dilated = {op: {"ms": round(dil_ms[op], 5), "tflops": round(flop / (dil_ms[op] * 1e-3) / 1e12, 2)} for op in OPS}
+    dilated["note"] = "same layer with dilation 2 and pad 2 (P, Q unchanged, same FLOP)"
+
     extra_ms = ex_ms["bwd_filter_with_bias_grads"] - op_ms["bwd_filter"]
     sum_bytes = (math.prod(pb.y_shape) + math.prod(pb.x_shape)) * pb.elem_bytes()  # dy and x read once
     fused = {"fwd_bias_addto_ms": round(ex_ms["fwd_bias_addto"], 5),
@@ -317,6 +350,7 @@ def run_ours(args, rank, world):
                 "ms_per_step": round(e2e_ms, 4)},
         "gpu_launches": K * len(OPS) * KERNELS_PER_OP,
         "fused_epilogue": fused,
+        "dilation_2": dilated,
         "clocks": clocks,
     }
     if rank == 0 and not args.no_cpu_baseline:
