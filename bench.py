@@ -272,7 +272,8 @@ def run_ours(args, rank, world):
         torch.cuda.synchronize()
         dil_ms[op] = sum(a.elapsed_time(b) for a, b in pairs) / len(pairs)
     cg.conv2d_device_status(stream)
-    dilated = {op: {"ms": round(dil_ms[op], 5), "tflops": round(flop / (dil_ms[op] * 1e-3) / 1e12, 2)} for op in OPS}
+    dilated = {op: {"ms": round(dil_ms[op], 5), "tflops": round(pb.flops() / (dil_ms[op] * 1e-3) / 1e12, 2)}
+               for op in OPS}
     dilated["note"] = "same layer with dilation 2 and pad 2 (P, Q unchanged, same FLOP)"
 
     extra_ms = ex_ms["bwd_filter_with_bias_grads"] - op_ms["bwd_filter"]
