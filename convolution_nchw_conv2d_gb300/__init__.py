@@ -73,10 +73,10 @@ def load_library():
         fl = ctypes.c_float
         for name in ("conv2d_fwd_ex", "conv2d_bwd_data_ex"):
             f = getattr(lib, name)
-            f.argtypes = [i] * 15 + [i, i, vp, vp, vp, fl, vp, vp, sz, vp]
+            f.argtypes = [i] * 16 + [i, i, vp, vp, vp, fl, vp, vp, sz, vp]
             f.restype = i
-        lib.conv2d_bwd_filter_ex.argtypes = [i] * 15 + [i, i, vp, vp, fl, vp, vp, vp, vp, sz, vp]
-        lib.conv2d_workspace_size_ex.argtypes = [i] + [i] * 15 + [i, ctypes.POINTER(sz)]
+        lib.conv2d_bwd_filter_ex.argtypes = [i] * 16 + [i, i, vp, vp, fl, vp, vp, vp, vp, sz, vp]
+        lib.conv2d_workspace_size_ex.argtypes = [i] + [i] * 16 + [i, ctypes.POINTER(sz)]
         lib.conv2d_workspace_size_ex.restype = i
         lib.conv2d_bwd_filter_ex.restype = i
         lib.conv2d_fwd_noalloc.argtypes = [i] * 13 + [i, vp, vp, vp, vp]
@@ -117,11 +117,12 @@ def _dtype_code(t) -> int:
     raise TypeError(f"unsupported dtype {t.dtype}; expected float32 or bfloat16")
 
 
-def conv2d_workspace_size(op: int, dims, dtype_code: int, dilation=(1, 1)) -> int:
-    """Workspace bytes for `op`, the 13 descriptor integers `dims` and the dilation."""
+def conv2d_workspace_size(op: int, dims, dtype_code: int, dilation=(1, 1), groups: int = 1) -> int:
+    """Workspace bytes for `op`, the 13 descriptor integers `dims`, the dilation and groups."""
     out = ctypes.c_size_t(0)
     dh, dw = _pair(dilation)
-    rc = load_library().conv2d_workspace_size_ex(op, *[int(v) for v in dims], dh, dw, dtype_code, ctypes.byref(out))
+    rc = load_library().conv2d_workspace_size_ex(op, *[int(v) for v in dims], dh, dw, int(groups), dtype_code,
+                                                 ctypes.byref(out))
     if rc:
         raise Conv2dError(rc, "conv2d_workspace_size")
     return out.value
@@ -140,9 +141,9 @@ def _check_tensor(t, name):
         raise ValueError(f"{name} must be contiguous (dense NCHW / KCRS)")
 
 
-def _workspace(op, dims, dt, workspace, device, dilation=(1, 1)):
+def _workspace(op, dims, dt, workspace, device, dilation=(1, 1), groups=1):
     import torch
-    need = conv2d_workspace_size(op, dims, dt, dilation)
+    need = conv2d_workspace_size(op, dims, dt, dilation, groups)
     if need == 0:
         return None, 0
     if workspace is None:
@@ -168,12 +169,14 @@ def _mode(flip):
     return MODE_CONVOLUTION if flip else MODE_CROSS_CORRELATION
 
 
-def _call(name, dims, dt, a, b, out, workspace, op, stream, bias=None, beta=0.0, flip=False, dilation=(1, 1)):
+def _call(name, dims, dt, a, b, out, workspace, op, stream, bias=None, beta=0.0, flip=False, dilation=(1, 1),
+          groups=1):
     """Forward / backward-data through the fused-epilogue entry point (bias None, beta 0,
-    flip False and dilation 1 are the plain op)."""
-    ws, wsb = _workspace(op, dims, dt, workspace, out.device, dilation)
+    flip False, dilation 1 and groups 1 are the plain op)."""
+    ws, wsb = _workspace(op, dims, dt, workspace, out.device, dilation, groups)
     dh, dw = _pair(dilation)
-    rc = getattr(load_library(), name + "_ex")(*[int(v) for v in dims], dh, dw, dt, _mode(flip), _ptr(a), _ptr(b),
+    rc = getattr(load_library(), name + "_ex")(*[int(v) for v in dims], dh, dw, int(groups), dt, _mode(flip), _ptr(a),
+                                               _ptr(b),
                                                _ptr(bias),
                                                ctypes.c_float(float(beta)), _ptr(out), _ptr(ws),
                                                ctypes.c_size_t(wsb), _stream_ptr(stream))
@@ -187,18 +190,19 @@ def _eff(k, d):
 
 
 def conv2d_fwd(x, w, pad=0, stride=1, out=None, workspace=None, stream=None, bias=None, beta=0.0, flip=False,
-               dilation=1):
+               dilation=1, groups=1):
     """y = conv2d(x, w) (+ bias[k]) (+ beta * y): x (N,C,H,W), w (K,C,R,S) -> y (N,K,P,Q),
     same dtype.  With beta != 0, `out` holds the values to accumulate onto.  flip=True is
     convolution mode (the filter rotated by 180 degrees); the default is cross-correlation.
-    dilation (int or pair): filter tap (r, s) reads input offset (r*dil_h, s*dil_w)."""
+    dilation (int or pair): filter tap (r, s) reads input offset (r*dil_h, s*dil_w).  groups:
+    the channels split into independent convolutions; w is (K, C/groups, R, S)."""
     import torch
     _check_tensor(x, "x")
     _check_tensor(w, "w")
     N, C, H, W = x.shape
     K, C2, R, S = w.shape
-    if C2 != C or w.dtype != x.dtype:
-        raise ValueError("x / w channel count or dtype mismatch")
+    if C2 * groups != C or K % groups != 0 or w.dtype != x.dtype:
+        raise ValueError("x / w channel count, groups or dtype mismatch")
     ph, pw = _pair(pad)
     sh, sw = _pair(stride)
     dh, dw = _pair(dilation)
@@ -210,7 +214,7 @@ def conv2d_fwd(x, w, pad=0, stride=1, out=None, workspace=None, stream=None, bia
     _check_vec(bias, K, x, "bias")
     dims = (N, C, H, W, K, R, S, ph, pw, sh, sw, P, Q)
     return _call("conv2d_fwd", dims, _dtype_code(x), x, w, out, workspace, OP_FWD, stream, bias, beta, flip,
-                 (dh, dw))
+                 (dh, dw), groups)
 
 
 def conv2d_fwd_noalloc(x, w, pad=0, stride=1, out=None, stream=None):
@@ -239,16 +243,17 @@ def conv2d_fwd_noalloc(x, w, pad=0, stride=1, out=None, stream=None):
 
 
 def conv2d_bwd_data(dy, w, x_hw, pad=0, stride=1, out=None, workspace=None, stream=None, bias=None, beta=0.0,
-                    flip=False, dilation=1):
+                    flip=False, dilation=1, groups=1):
     """dx (N,C,H,W) from dy (N,K,P,Q) and w (K,C,R,S); x_hw = (H, W).  Optional epilogue:
     + bias[c] (the bias of a deconvolution) + beta * dx (`out` required when beta != 0)."""
     import torch
     _check_tensor(dy, "dy")
     _check_tensor(w, "w")
     N, K, P, Q = dy.shape
-    K2, C, R, S = w.shape
-    if K2 != K or w.dtype != dy.dtype:
-        raise ValueError("dy / w channel count or dtype mismatch")
+    K2, Cg, R, S = w.shape
+    C = Cg * groups
+    if K2 != K or K % groups != 0 or w.dtype != dy.dtype:
+        raise ValueError("dy / w channel count, groups or dtype mismatch")
     H, W = x_hw
     ph, pw = _pair(pad)
     sh, sw = _pair(stride)
@@ -259,11 +264,11 @@ def conv2d_bwd_data(dy, w, x_hw, pad=0, stride=1, out=None, workspace=None, stre
     _check_vec(bias, C, dy, "bias")
     dims = (N, C, H, W, K, R, S, ph, pw, sh, sw, P, Q)
     return _call("conv2d_bwd_data", dims, _dtype_code(dy), dy, w, out, workspace, OP_BWD_DATA, stream,
-                 bias, beta, flip, _pair(dilation))
+                 bias, beta, flip, _pair(dilation), groups)
 
 
 def conv2d_bwd_filter(x, dy, rs, pad=0, stride=1, out=None, workspace=None, stream=None, beta=0.0,
-                      db_k=None, db_c=None, flip=False, dilation=1):
+                      db_k=None, db_c=None, flip=False, dilation=1, groups=1):
     """dw (K,C,R,S) from x (N,C,H,W) and dy (N,K,P,Q); rs = (R, S).
 
     Optional: beta accumulates onto `out` (dw) and onto the bias gradients; db_k (K values)
@@ -283,14 +288,17 @@ def conv2d_bwd_filter(x, dy, rs, pad=0, stride=1, out=None, workspace=None, stre
     if out is None:
         if beta != 0.0:
             raise ValueError("beta != 0 accumulates onto `out`, which must then be given")
-        out = torch.empty((K, C, R, S), dtype=x.dtype, device=x.device)
+        out = torch.empty((K, C // groups, R, S), dtype=x.dtype, device=x.device)
+    if C % groups != 0 or K % groups != 0:
+        raise ValueError("groups must divide C and K")
     _check_vec(db_k, K, x, "db_k")
     _check_vec(db_c, C, x, "db_c")
     dims = (N, C, H, W, K, R, S, ph, pw, sh, sw, P, Q)
     dt = _dtype_code(x)
     dh, dw = _pair(dilation)
-    ws, wsb = _workspace(OP_BWD_FILTER, dims, dt, workspace, out.device, (dh, dw))
-    rc = load_library().conv2d_bwd_filter_ex(*[int(v) for v in dims], dh, dw, dt, _mode(flip), _ptr(x), _ptr(dy),
+    ws, wsb = _workspace(OP_BWD_FILTER, dims, dt, workspace, out.device, (dh, dw), groups)
+    rc = load_library().conv2d_bwd_filter_ex(*[int(v) for v in dims], dh, dw, int(groups), dt, _mode(flip), _ptr(x),
+                                             _ptr(dy),
                                              ctypes.c_float(float(beta)), _ptr(out), _ptr(db_k), _ptr(db_c),
                                              _ptr(ws), ctypes.c_size_t(wsb), _stream_ptr(stream))
     if rc:
@@ -299,13 +307,13 @@ def conv2d_bwd_filter(x, dy, rs, pad=0, stride=1, out=None, workspace=None, stre
 
 
 def deconv2d_fwd(inp, wt, out_hw, pad=0, stride=1, out=None, workspace=None, stream=None, bias=None, beta=0.0,
-                 flip=False, dilation=1):
+                 flip=False, dilation=1, groups=1):
     """Transposed convolution: inp (N,Ci,Hi,Wi), wt (Ci,Co,R,S) -> (N,Co,Ho,Wo), optionally
     + bias[co] + beta * out.
 
     Runs conv2d_bwd_data with K = Ci (deconv input channels), C = Co, P = Hi, H = Ho."""
     return conv2d_bwd_data(inp, wt, out_hw, pad, stride, out=out, workspace=workspace, stream=stream,
-                           bias=bias, beta=beta, flip=flip, dilation=dilation)
+                           bias=bias, beta=beta, flip=flip, dilation=dilation, groups=groups)
 
 
 # ------------------------------------------------------------------ 1-D

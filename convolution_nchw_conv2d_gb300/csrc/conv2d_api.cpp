@@ -39,6 +39,8 @@ constexpr size_t kDefaultSmemOptin = 232448;      // 227 KB
 struct Desc {
   int N, C, H, W, K, R, S, ph, pw, sh, sw, P, Q, dt;
   int dh = 1, dw = 1;  // dilation: filter tap (r, s) sits at (r*dh, s*dw) in the window
+  int g = 1;           // groups this per-group descriptor belongs to: the tensors hold g*C
+                       // input and g*K output channels (image strides), the filter K x C
 };
 
 int floor_div(int a, int b) { return a >= 0 ? a / b : -((-a + b - 1) / b); }
@@ -70,6 +72,19 @@ int validate(const Desc& d) {
   if (d.R * d.S > kMaxTaps || d.sh * d.sw > kMaxPlanes) return CONV2D_ERR_UNSUPPORTED;
   return CONV2D_OK;
 }
+
+// Per-group descriptor of a grouped problem (C and K are the totals; the filter is
+// K x C/groups x R x S): C/groups input and K/groups output channels per group.
+int group_desc(const Desc& d, int groups, Desc& dg) {
+  if (groups < 1 || d.C % groups != 0 || d.K % groups != 0) return CONV2D_ERR_BAD_DESC;
+  dg = d;
+  dg.C = d.C / groups;
+  dg.K = d.K / groups;
+  dg.g = groups;
+  return CONV2D_OK;
+}
+
+const uint8_t* byte_ptr(const void* p) { return static_cast<const uint8_t*>(p); }
 
 struct DevInfo {
   int sms = kDefaultSMs;
@@ -267,6 +282,8 @@ int build_fwd(const Desc& d0, const void* x, const void* w, void* y, void* ws, c
   p.Cd = d.K;
   p.Hd = d.P;
   p.Wd = d.Q;
+  p.src_nstride = (long long)d.g * d.C * d.H * d.W;
+  p.dst_nstride = (long long)d.g * d.K * d.P * d.Q;
   const int mh = (d.dh * (d.R - 1)) / d.sh, mw = (d.dw * (d.S - 1)) / d.sw;
   const int CHUNK = d.dt == 0 ? 4 : 8;
   p.WL = d.Q + mw;
@@ -329,6 +346,8 @@ int build_bwd_data(const Desc& d0, const void* dy, const void* w, void* dx, void
   p.Cd = d.C;
   p.Hd = d.H;
   p.Wd = d.W;
+  p.src_nstride = (long long)d.g * d.K * d.P * d.Q;
+  p.dst_nstride = (long long)d.g * d.C * d.H * d.W;
   // Per output phase a (rows with (h + pad_h) mod stride_h == a): the taps r with
   // r*dh = a (mod stride_h), at t_r = (r*dh - a) / stride_h; output row h = sh*u + a - pad_h
   // reads dy row p = u - t_r.  Th[a] = 1 + the largest t_r (0: no tap reaches the phase).
@@ -447,12 +466,12 @@ EncodeTiledFn encode_tiled_fn() {
 
 // x (N, C, H, W) as the 4-D tensor (w = W, h = H, c = C, n = N) with a box of one image row
 // segment of WL pixels by 32 channels.  False if it cannot be encoded.
-bool encode_x_map(CUtensorMap* m, const void* x, int dt, int N, int C, int H, int W, int WL) {
+bool encode_x_map(CUtensorMap* m, const void* x, int dt, int N, int C, int H, int W, int WL, long long nstride) {
   EncodeTiledFn fn = encode_tiled_fn();
   if (!fn) return false;
   const uint64_t esz = dt == 0 ? 4 : 2;
   const cuuint64_t dims[4] = {(cuuint64_t)W, (cuuint64_t)H, (cuuint64_t)C, (cuuint64_t)N};
-  const cuuint64_t strides[3] = {(cuuint64_t)W * esz, (cuuint64_t)H * W * esz, (cuuint64_t)C * H * W * esz};
+  const cuuint64_t strides[3] = {(cuuint64_t)W * esz, (cuuint64_t)H * W * esz, (cuuint64_t)nstride * esz};
   const cuuint32_t box[4] = {(cuuint32_t)WL, 1u, 32u, 1u};
   const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
   const CUresult r = fn(m, dt == 0 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
@@ -463,12 +482,12 @@ bool encode_x_map(CUtensorMap* m, const void* x, int dt, int N, int C, int H, in
 
 // dy (N, K, P, Q) as the 4-D tensor (w = Q, k = K, e = P, n = N) with a box of one
 // 16-byte chunk of positions by NK output channels.  False if it cannot be encoded.
-bool encode_dy_map(CUtensorMap* m, const void* dy, int dt, int N, int K, int P, int Q, int NK) {
+bool encode_dy_map(CUtensorMap* m, const void* dy, int dt, int N, int K, int P, int Q, int NK, long long nstride) {
   EncodeTiledFn fn = encode_tiled_fn();
   if (!fn) return false;
   const uint64_t esz = dt == 0 ? 4 : 2;
   const cuuint64_t dims[4] = {(cuuint64_t)Q, (cuuint64_t)K, (cuuint64_t)P, (cuuint64_t)N};
-  const cuuint64_t strides[3] = {(cuuint64_t)P * Q * esz, (cuuint64_t)Q * esz, (cuuint64_t)K * P * Q * esz};
+  const cuuint64_t strides[3] = {(cuuint64_t)P * Q * esz, (cuuint64_t)Q * esz, (cuuint64_t)nstride * esz};
   const cuuint32_t box[4] = {(cuuint32_t)(16 / esz), (cuuint32_t)NK, 1u, 1u};
   const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
   const CUresult r = fn(m, dt == 0 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
@@ -480,14 +499,15 @@ bool encode_dy_map(CUtensorMap* m, const void* dy, int dt, int N, int K, int P, 
 // dy (N, K, P, Q) as the 5-D tensor (w mod CHUNK, k, w / CHUNK, e, n) with a box of one
 // linear row of WL positions by NK output channels: shared-memory layout [chunk][k][CHUNK].
 // False if it cannot be encoded.
-bool encode_dy_row_map(CUtensorMap* m, const void* dy, int dt, int N, int K, int P, int Q, int NK, int WL) {
+bool encode_dy_row_map(CUtensorMap* m, const void* dy, int dt, int N, int K, int P, int Q, int NK, int WL,
+                       long long nstride) {
   EncodeTiledFn fn = encode_tiled_fn();
   if (!fn) return false;
   const uint64_t esz = dt == 0 ? 4 : 2;
   const uint64_t chunk = 16 / esz;
   const cuuint64_t dims[5] = {(cuuint64_t)chunk, (cuuint64_t)K, (cuuint64_t)(Q / chunk), (cuuint64_t)P,
                               (cuuint64_t)N};
-  const cuuint64_t strides[4] = {(cuuint64_t)P * Q * esz, 16u, (cuuint64_t)Q * esz, (cuuint64_t)K * P * Q * esz};
+  const cuuint64_t strides[4] = {(cuuint64_t)P * Q * esz, 16u, (cuuint64_t)Q * esz, (cuuint64_t)nstride * esz};
   const cuuint32_t box[5] = {(cuuint32_t)chunk, (cuuint32_t)NK, (cuuint32_t)(WL / chunk), 1u, 1u};
   const cuuint32_t estr[5] = {1u, 1u, 1u, 1u, 1u};
   const CUresult r = fn(m, dt == 0 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5,
@@ -511,6 +531,8 @@ int build_bwd_filter_impl(const Desc& d0, const void* x, const void* dy, void* d
   std::memset(&p, 0, sizeof(p));
   p.x = x;
   p.dy = dy;
+  p.x_nstride = (long long)d.g * d.C * d.H * d.W;
+  p.dy_nstride = (long long)d.g * d.K * d.P * d.Q;
   p.partial = static_cast<float*>(ws);
   p.N = d.N;
   p.C = d.C;
@@ -670,14 +692,14 @@ int build_bwd_filter_impl(const Desc& d0, const void* x, const void* dy, void* d
   // (sizing calls pass no tensors: their plan assumes the maps encode)
   const bool sizing = x == nullptr && dy == nullptr;
   if (p.use_tma == 1 && !sizing &&
-      !((p.TRU > 1 ? encode_dy_row_map(&p.tm_dyr, dy, d.dt, d.N, d.K, d.P, d.Q, p.NK, p.WL)
-                   : encode_dy_map(&p.tm_dy, dy, d.dt, d.N, d.K, d.P, d.Q, p.NK)) &&
-        encode_x_map(&p.tm_x, x, d.dt, d.N, d.C, d.H, d.W, p.WLx))) {
+      !((p.TRU > 1 ? encode_dy_row_map(&p.tm_dyr, dy, d.dt, d.N, d.K, d.P, d.Q, p.NK, p.WL, p.dy_nstride)
+                   : encode_dy_map(&p.tm_dy, dy, d.dt, d.N, d.K, d.P, d.Q, p.NK, p.dy_nstride)) &&
+        encode_x_map(&p.tm_x, x, d.dt, d.N, d.C, d.H, d.W, p.WLx, p.x_nstride))) {
     // The row ring cannot be encoded: plan without sharing, or the slot ring (another linear
     // row width).
     return CONV2D_ERR_UNSUPPORTED;
   }
-  if (p.use_tma == 2 && !sizing && !encode_dy_map(&p.tm_dy, dy, d.dt, d.N, d.K, d.P, d.Q, p.NK))
+  if (p.use_tma == 2 && !sizing && !encode_dy_map(&p.tm_dy, dy, d.dt, d.N, d.K, d.P, d.Q, p.NK, p.dy_nstride))
     p.use_tma = 0;  // same ring, staged with cp.async
   // Split the positions so that the tiles fill the SMs with the shortest makespan
   // (tiles per CTA x positions per tile), preferring fewer splits.
@@ -744,8 +766,8 @@ int check_ptrs(const void* a, const void* b, const void* c, int dt) {
 // Workspace of the bias-gradient sums of conv2d_bwd_filter_ex: fp32 partials per (channel,
 // image) for the K sums over dy and the C sums over x, each region 256-byte aligned.
 size_t align_ws(size_t b) { return (b + 255) & ~size_t(255); }
-size_t chan_sum_bytes(const Desc& d) {
-  return align_ws((size_t)d.K * d.N * sizeof(float)) + align_ws((size_t)d.C * d.N * sizeof(float));
+size_t chan_sum_bytes(const Desc& d) {  // the sums cover all d.g groups' channels
+  return align_ws((size_t)d.g * d.K * d.N * sizeof(float)) + align_ws((size_t)d.g * d.C * d.N * sizeof(float));
 }
 
 int check_ws(void* ws, size_t have, size_t need) {
@@ -835,16 +857,19 @@ int conv2d_output_dim(int in, int pad, int k, int stride, int* out) {
 
 int conv2d_workspace_size(int op, int N, int C, int H, int W, int K, int R, int S, int pad_h, int pad_w,
                           int stride_h, int stride_w, int P, int Q, int dtype, size_t* bytes) {
-  return conv2d_workspace_size_ex(op, N, C, H, W, K, R, S, pad_h, pad_w, stride_h, stride_w, P, Q, 1, 1, dtype,
+  return conv2d_workspace_size_ex(op, N, C, H, W, K, R, S, pad_h, pad_w, stride_h, stride_w, P, Q, 1, 1, 1, dtype,
                                   bytes);
 }
 
 int conv2d_workspace_size_ex(int op, int N, int C, int H, int W, int K, int R, int S, int pad_h, int pad_w,
-                             int stride_h, int stride_w, int P, int Q, int dil_h, int dil_w, int dtype,
+                             int stride_h, int stride_w, int P, int Q, int dil_h, int dil_w, int groups, int dtype,
                              size_t* bytes) {
   if (!bytes) return CONV2D_ERR_NULLPTR;
-  const Desc d{N, C, H, W, K, R, S, pad_h, pad_w, stride_h, stride_w, P, Q, dtype, dil_h, dil_w};
-  int rc = validate(d);
+  const Desc dt{N, C, H, W, K, R, S, pad_h, pad_w, stride_h, stride_w, P, Q, dtype, dil_h, dil_w};
+  int rc = validate(dt);
+  if (rc) return rc;
+  Desc d;
+  rc = group_desc(dt, groups, d);  // per-group plans; the bias sums cover the whole tensors
   if (rc) return rc;
   const PlanKey key = make_key(op, d, nullptr, nullptr, nullptr, nullptr);
   if (g_ws_sizes.get(key, *bytes)) return CONV2D_OK;
@@ -888,107 +913,143 @@ int workspace_size_uncached(int op, const Desc& d, size_t* bytes) {
 
 extern "C" {
 
-static int run_tap(int op, const Desc& d, const void* src, const void* w, const void* bias, float beta, int mode,
-                   void* dst, void* ws, size_t wsb, void* stream) {
+
+// Forward / backward-data: the plan is made once per descriptor (cached with the group-0
+// addresses) and each group runs it with its own tensor slices: source, destination and
+// bias channels of the group, the group's filter rows; the repacked filter reuses the
+// workspace group after group (stream order).
+static int run_tap(int op, const Desc& d, int groups, const void* src, const void* w, const void* bias, float beta,
+                   int mode, void* dst, void* ws, size_t wsb, void* stream) {
   if (mode != CONV2D_MODE_CROSS_CORRELATION && mode != CONV2D_MODE_CONVOLUTION) return CONV2D_ERR_BAD_DESC;
   int rc = validate(d);
+  if (rc) return rc;
+  Desc dg;
+  rc = group_desc(d, groups, dg);
   if (rc) return rc;
   rc = check_ptrs(src, w, dst, d.dt);
   if (rc) return rc;
   const DevInfo di = device_info();
   if (!di.ok) return CONV2D_ERR_DEVICE;
   TapBuild b;
-  const PlanKey key = make_key(op, d, src, w, dst, ws);
+  const PlanKey key = make_key(op, dg, src, w, dst, ws);
   if (!g_tap_plans.get(key, b)) {
-    rc = op == CONV2D_OP_FWD ? build_fwd(d, src, w, dst, ws, di, b) : build_bwd_data(d, src, w, dst, ws, di, b);
+    rc = op == CONV2D_OP_FWD ? build_fwd(dg, src, w, dst, ws, di, b) : build_bwd_data(dg, src, w, dst, ws, di, b);
     if (rc) return rc;
     g_tap_plans.put(key, b);
   }
   rc = check_ws(ws, wsb, b.pack_bytes);
   if (rc) return rc;
   if (bias != nullptr && ((uintptr_t)bias & (d.dt == CONV2D_DTYPE_F32 ? 3 : 1))) return CONV2D_ERR_ALIGN;
-  b.p.bias = bias;  // per-call epilogue inputs and mode (not part of the cached plan)
-  b.p.beta = beta;
+  b.p.beta = beta;  // per-call epilogue inputs and mode (not part of the cached plan)
   b.pp.flip = mode == CONV2D_MODE_CONVOLUTION ? 1 : 0;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (b.pack_bytes) {
-    rc = launch_err(launch_pack_filter(b.pp, d.dt, st));
+  const size_t esz = d.dt == CONV2D_DTYPE_F32 ? 4 : 2;
+  const bool fwd = op == CONV2D_OP_FWD;
+  // per-group element offsets of the source, destination, filter and bias slices
+  const size_t src_g = fwd ? (size_t)dg.C * dg.H * dg.W : (size_t)dg.K * dg.P * dg.Q;
+  const size_t dst_g = fwd ? (size_t)dg.K * dg.P * dg.Q : (size_t)dg.C * dg.H * dg.W;
+  const size_t w_g = (size_t)dg.K * dg.C * dg.R * dg.S;
+  const size_t bias_g = fwd ? (size_t)dg.K : (size_t)dg.C;
+  for (int gi = 0; gi < groups; ++gi) {
+    b.p.src = byte_ptr(src) + gi * src_g * esz;
+    b.p.dst = const_cast<uint8_t*>(byte_ptr(dst)) + gi * dst_g * esz;
+    b.pp.w = byte_ptr(w) + gi * w_g * esz;
+    b.p.bias = bias != nullptr ? byte_ptr(bias) + gi * bias_g * esz : nullptr;
+    if (b.pack_bytes) {
+      rc = launch_err(launch_pack_filter(b.pp, d.dt, st));
+      if (rc) return rc;
+    }
+    rc = launch_err(launch_tap_gemm(b.p, d.dt, b.grid, st));
     if (rc) return rc;
   }
-  return launch_err(launch_tap_gemm(b.p, d.dt, b.grid, st));
+  return CONV2D_OK;
 }
 
 int conv2d_fwd(int N, int C, int H, int W, int K, int R, int S, int pad_h, int pad_w, int stride_h,
                int stride_w, int P, int Q, int dtype, const void* x, const void* w, void* y, void* workspace,
                size_t workspace_bytes, void* stream) {
   const Desc d{N, C, H, W, K, R, S, pad_h, pad_w, stride_h, stride_w, P, Q, dtype};
-  return run_tap(CONV2D_OP_FWD, d, x, w, nullptr, 0.f, CONV2D_MODE_CROSS_CORRELATION, y, workspace, workspace_bytes,
-                 stream);
+  return run_tap(CONV2D_OP_FWD, d, 1, x, w, nullptr, 0.f, CONV2D_MODE_CROSS_CORRELATION, y, workspace,
+                 workspace_bytes, stream);
 }
 
 int conv2d_fwd_ex(int N, int C, int H, int W, int K, int R, int S, int pad_h, int pad_w, int stride_h,
-                  int stride_w, int P, int Q, int dil_h, int dil_w, int dtype, int mode, const void* x, const void* w,
-                  const void* bias, float beta, void* y, void* workspace, size_t workspace_bytes, void* stream) {
+                  int stride_w, int P, int Q, int dil_h, int dil_w, int groups, int dtype, int mode, const void* x,
+                  const void* w, const void* bias, float beta, void* y, void* workspace, size_t workspace_bytes,
+                  void* stream) {
   const Desc d{N, C, H, W, K, R, S, pad_h, pad_w, stride_h, stride_w, P, Q, dtype, dil_h, dil_w};
-  return run_tap(CONV2D_OP_FWD, d, x, w, bias, beta, mode, y, workspace, workspace_bytes, stream);
+  return run_tap(CONV2D_OP_FWD, d, groups, x, w, bias, beta, mode, y, workspace, workspace_bytes, stream);
 }
 
 int conv2d_bwd_data(int N, int C, int H, int W, int K, int R, int S, int pad_h, int pad_w, int stride_h,
                     int stride_w, int P, int Q, int dtype, const void* dy, const void* w, void* dx,
                     void* workspace, size_t workspace_bytes, void* stream) {
   const Desc d{N, C, H, W, K, R, S, pad_h, pad_w, stride_h, stride_w, P, Q, dtype};
-  return run_tap(CONV2D_OP_BWD_DATA, d, dy, w, nullptr, 0.f, CONV2D_MODE_CROSS_CORRELATION, dx, workspace,
+  return run_tap(CONV2D_OP_BWD_DATA, d, 1, dy, w, nullptr, 0.f, CONV2D_MODE_CROSS_CORRELATION, dx, workspace,
                  workspace_bytes, stream);
 }
 
 int conv2d_bwd_data_ex(int N, int C, int H, int W, int K, int R, int S, int pad_h, int pad_w, int stride_h,
-                       int stride_w, int P, int Q, int dil_h, int dil_w, int dtype, int mode, const void* dy,
-                       const void* w, const void* bias, float beta, void* dx, void* workspace, size_t workspace_bytes,
-                       void* stream) {
+                       int stride_w, int P, int Q, int dil_h, int dil_w, int groups, int dtype, int mode,
+                       const void* dy, const void* w, const void* bias, float beta, void* dx, void* workspace,
+                       size_t workspace_bytes, void* stream) {
   const Desc d{N, C, H, W, K, R, S, pad_h, pad_w, stride_h, stride_w, P, Q, dtype, dil_h, dil_w};
-  return run_tap(CONV2D_OP_BWD_DATA, d, dy, w, bias, beta, mode, dx, workspace, workspace_bytes, stream);
+  return run_tap(CONV2D_OP_BWD_DATA, d, groups, dy, w, bias, beta, mode, dx, workspace, workspace_bytes, stream);
 }
 
 int conv2d_bwd_filter(int N, int C, int H, int W, int K, int R, int S, int pad_h, int pad_w, int stride_h,
                       int stride_w, int P, int Q, int dtype, const void* x, const void* dy, void* dw,
                       void* workspace, size_t workspace_bytes, void* stream) {
-  return conv2d_bwd_filter_ex(N, C, H, W, K, R, S, pad_h, pad_w, stride_h, stride_w, P, Q, 1, 1, dtype,
+  return conv2d_bwd_filter_ex(N, C, H, W, K, R, S, pad_h, pad_w, stride_h, stride_w, P, Q, 1, 1, 1, dtype,
                               CONV2D_MODE_CROSS_CORRELATION, x, dy, 0.f, dw, nullptr, nullptr, workspace,
                               workspace_bytes, stream);
 }
 
 int conv2d_bwd_filter_ex(int N, int C, int H, int W, int K, int R, int S, int pad_h, int pad_w, int stride_h,
-                         int stride_w, int P, int Q, int dil_h, int dil_w, int dtype, int mode, const void* x,
-                         const void* dy, float beta, void* dw, void* db_k, void* db_c, void* workspace,
+                         int stride_w, int P, int Q, int dil_h, int dil_w, int groups, int dtype, int mode,
+                         const void* x, const void* dy, float beta, void* dw, void* db_k, void* db_c, void* workspace,
                          size_t workspace_bytes, void* stream) {
   const Desc d{N, C, H, W, K, R, S, pad_h, pad_w, stride_h, stride_w, P, Q, dtype, dil_h, dil_w};
   if (mode != CONV2D_MODE_CROSS_CORRELATION && mode != CONV2D_MODE_CONVOLUTION) return CONV2D_ERR_BAD_DESC;
   int rc = validate(d);
   if (rc) return rc;
-  rc = check_ptrs(x, dy, dw, d.dt);
+  Desc dg;
+  rc = group_desc(d, groups, dg);
   if (rc) return rc;
-  const DevInfo di = device_info();
-  if (!di.ok) return CONV2D_ERR_DEVICE;
-  WgradBuild b;
-  const PlanKey key = make_key(CONV2D_OP_BWD_FILTER, d, x, dy, dw, workspace);
-  if (!g_wgrad_plans.get(key, b)) {
-    rc = build_bwd_filter(d, x, dy, dw, workspace, di, b);
-    if (rc) return rc;
-    g_wgrad_plans.put(key, b);
-  }
-  const bool sums = db_k != nullptr || db_c != nullptr;
-  const size_t sum0 = align_ws(b.partial_bytes);
-  rc = check_ws(workspace, workspace_bytes, sums ? sum0 + chan_sum_bytes(d) : b.partial_bytes);
+  rc = check_ptrs(x, dy, dw, d.dt);
   if (rc) return rc;
   const uintptr_t am = d.dt == CONV2D_DTYPE_F32 ? 3 : 1;
   if (((uintptr_t)db_k & am) || ((uintptr_t)db_c & am)) return CONV2D_ERR_ALIGN;
-  b.rp.beta = beta;  // per-call (not part of the cached plan)
-  b.rp.flip = mode == CONV2D_MODE_CONVOLUTION ? 1 : 0;
+  const DevInfo di = device_info();
+  if (!di.ok) return CONV2D_ERR_DEVICE;
+  const bool sums = db_k != nullptr || db_c != nullptr;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  rc = launch_err(launch_wgrad(b.p, d.dt, b.grid, st));
-  if (rc) return rc;
-  rc = launch_err(launch_wgrad_reduce(b.rp, d.dt, di.sms, st));
-  if (rc) return rc;
+  const size_t esz = d.dt == CONV2D_DTYPE_F32 ? 4 : 2;
+  size_t sum0 = 0;
+  // One split-K pass per group on the group's slices (x channels, dy channels, dw rows);
+  // the split partials reuse the workspace group after group (stream order).  The plans
+  // embed the slices' addresses (tensor maps), so each group has its own cached plan.
+  for (int gi = 0; gi < groups; ++gi) {
+    const void* xg = byte_ptr(x) + gi * (size_t)dg.C * dg.H * dg.W * esz;
+    const void* dyg = byte_ptr(dy) + gi * (size_t)dg.K * dg.P * dg.Q * esz;
+    void* dwg = const_cast<uint8_t*>(byte_ptr(dw)) + gi * (size_t)dg.K * dg.C * dg.R * dg.S * esz;
+    WgradBuild b;
+    const PlanKey key = make_key(CONV2D_OP_BWD_FILTER, dg, xg, dyg, dwg, workspace);
+    if (!g_wgrad_plans.get(key, b)) {
+      rc = build_bwd_filter(dg, xg, dyg, dwg, workspace, di, b);
+      if (rc) return rc;
+      g_wgrad_plans.put(key, b);
+    }
+    sum0 = std::max(sum0, align_ws(b.partial_bytes));
+    rc = check_ws(workspace, workspace_bytes, sums ? align_ws(b.partial_bytes) + chan_sum_bytes(d) : b.partial_bytes);
+    if (rc) return rc;
+    b.rp.beta = beta;  // per-call (not part of the cached plan)
+    b.rp.flip = mode == CONV2D_MODE_CONVOLUTION ? 1 : 0;
+    rc = launch_err(launch_wgrad(b.p, d.dt, b.grid, st));
+    if (rc) return rc;
+    rc = launch_err(launch_wgrad_reduce(b.rp, d.dt, di.sms, st));
+    if (rc) return rc;
+  }
   uint8_t* wsb = static_cast<uint8_t*>(workspace) + sum0;
   if (db_k != nullptr) {
     // conv bias gradient: sum of dy over images and output pixels, per output channel k

@@ -54,6 +54,8 @@ struct TapPlan {
   const void* src;       // x (forward) or dy (backward-data), NCHW
   void* dst;             // y or dx, NCHW
   const void* bias;      // optional, one value per destination channel (NULL: none)
+  long long src_nstride, dst_nstride;  // elements from one image to the next (C*H*W unless
+                                       // the tensors hold several groups)
   float beta;            // dst = D + bias + beta * dst (beta 0: dst is not read)
   const void* wpack;     // packed filter, see pack layout in conv_tap_gemm.cu
   int N, Cs, Hs, Ws;     // source tensor
@@ -151,6 +153,8 @@ struct WgradPlan {
   int unit_tap[kMaxTaps];  // base tap of the j-th unit of a channel group (TPU == 1)
   const void* x;         // NCHW
   const void* dy;        // N K P Q
+  long long x_nstride, dy_nstride;  // elements from one image to the next (C*H*W and K*P*Q
+                                    // unless the tensors hold several groups)
   float* partial;        // [split][R*S][C][K] fp32
   int N, C, H, W, K, P, Q;
   int R, S, RS;

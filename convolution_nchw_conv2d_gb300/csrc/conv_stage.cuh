@@ -46,7 +46,7 @@ __device__ __forceinline__ int tap_src_offset(const TapPlan& p, uint32_t L, int 
   const int h = (int)e * p.pl_step_h + p.pl_off_h[pl];
   const int w = f * p.pl_step_w + p.pl_off_w[pl];
   if (h < 0 || h >= p.Hs || w < 0 || w >= p.Ws) return -1;
-  return (int)n * p.Cs * p.Hs * p.Ws + h * p.Ws + w;
+  return (int)((long long)n * p.src_nstride + (long long)h * p.Ws + w);
 }
 
 // Layout [plane][chunk][row][16 bytes]: the 16 bytes of (plane, chunk j, row r) hold

@@ -300,7 +300,7 @@ __global__ void __launch_bounds__(kThreads, 1) tap_gemm_kernel(const __grid_cons
           const int oh = e * p.ph_step_h + p.ph_off_h[tc.ph];
           const int ow = f * p.ph_step_w + p.ph_off_w[tc.ph];
           valid = oh >= 0 && oh < p.Hd && ow >= 0 && ow < p.Wd;
-          obase = (long long)n * p.Cd * HdWd + (long long)oh * p.Wd + ow;
+          obase = (long long)n * p.dst_nstride + (long long)oh * p.Wd + ow;
         }
         const uint32_t tcol = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)((acc * p.MH + h) * p.NT);
         const int nbase = tc.nt * p.NT;

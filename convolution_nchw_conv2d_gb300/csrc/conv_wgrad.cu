@@ -127,7 +127,7 @@ __device__ __forceinline__ void stage_ring(const WgradPlan& p, uint32_t ring, lo
           mode = 2;
         } else if (p.vec_x && (w & (CHUNK - 1)) == 0 && w >= 0 && wl < p.W) {
           mode = 1;
-          soff = (long long)n * p.C * HW + (long long)h * p.W + w;
+          soff = (long long)n * p.x_nstride + (long long)h * p.W + w;
         }
       }
     }
@@ -152,7 +152,7 @@ __device__ __forceinline__ void stage_ring(const WgradPlan& p, uint32_t ring, lo
       const int ff = (int)rem - ee * p.WL;
       const int h = ee * p.pl_step_h + p.pl_off_h[pl];
       const int w = ff * p.pl_step_w + p.pl_off_w[pl];
-      if (h >= 0 && h < p.H && w >= 0 && w < p.W) offs[j] = (int)((long long)nn * p.C * HW + (long long)h * p.W + w);
+      if (h >= 0 && h < p.H && w >= 0 && w < p.W) offs[j] = (int)((long long)nn * p.x_nstride + (long long)h * p.W + w);
     }
     constexpr int RL = DT == 0 ? 4 : 2;  // rows per load batch
     for (int c0r = cr0; c0r < cr1; c0r += RL) {
@@ -206,7 +206,7 @@ __device__ __forceinline__ void stage_dy(const WgradPlan& p, uint32_t dst0, long
       const int f = (int)rem - e * p.WL;
       if (p.vec_dy && La + CHUNK <= lend && e < p.P && f + CHUNK <= p.Q) {
         mode = 1;
-        soff = (long long)n * p.K * PQ + (long long)e * p.Q + f;
+        soff = (long long)n * p.dy_nstride + (long long)e * p.Q + f;
       } else if (!(p.vec_dy && (e >= p.P || f >= p.Q))) {
         mode = 3;
       }
@@ -227,7 +227,7 @@ __device__ __forceinline__ void stage_dy(const WgradPlan& p, uint32_t dst0, long
         const uint32_t rem = (uint32_t)L - n * p.fd_img.d;
         const int e = (int)fdiv(rem, p.fd_WL);
         const int f = (int)rem - e * p.WL;
-        if (e < p.P && f < p.Q) offs[i] = (int)((long long)n * p.K * PQ + (long long)e * p.Q + f);
+        if (e < p.P && f < p.Q) offs[i] = (int)((long long)n * p.dy_nstride + (long long)e * p.Q + f);
       }
       // rows in batches of RB: all loads of a batch precede its stores
       constexpr int RB = DT == 0 ? 4 : 2;
@@ -566,7 +566,7 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_kernel(const __grid_constan
                   const int wa = lo & ~(CHUNK - 1);
                   const int wb = (hi + CHUNK - 1) & ~(CHUNK - 1);  // <= W (W % CHUNK == 0)
                   const int slot = slot_of(rq + (wa - ow));
-                  const E* src = xg + (((long long)n * p.C + c_lo + cr) * p.H + h) * p.W + wa;
+                  const E* src = xg + (long long)n * p.x_nstride + ((long long)(c_lo + cr) * p.H + h) * p.W + wa;
                   const int len = wb - wa;
                   const int part = rlen - slot < len ? rlen - slot : len;
                   mbar_expect_tx(fb, (uint32_t)(len * ESZ));

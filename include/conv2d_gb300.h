@@ -115,10 +115,11 @@ int conv2d_workspace_size(int op, int N, int C, int H, int W, int K, int R, int 
                           int pad_h, int pad_w, int stride_h, int stride_w, int P, int Q,
                           int dtype, size_t *bytes);
 
-/* conv2d_workspace_size for a dilated descriptor (dil_h = dil_w = 1: the same value). */
+/* conv2d_workspace_size for a dilated and/or grouped descriptor (dil_h = dil_w = groups = 1:
+ * the same value). */
 int conv2d_workspace_size_ex(int op, int N, int C, int H, int W, int K, int R, int S,
                              int pad_h, int pad_w, int stride_h, int stride_w, int P, int Q,
-                             int dil_h, int dil_w, int dtype, size_t *bytes);
+                             int dil_h, int dil_w, int groups, int dtype, size_t *bytes);
 
 /* Forward: y (N,K,P,Q) = conv(x (N,C,H,W), w (K,C,R,S)). */
 int conv2d_fwd(int N, int C, int H, int W, int K, int R, int S,
@@ -169,24 +170,27 @@ int conv2d_bwd_filter(int N, int C, int H, int W, int K, int R, int S,
  * convolution descriptor, which the SystemDS page sets to 1, 1): filter tap (r, s) reads
  * X(n, c, p*stride_h - pad_h + r*dil_h, q*stride_w - pad_w + s*dil_w), and
  * P = floor((H + 2*pad_h - dil_h*(R-1) - 1) / stride_h) + 1, Q likewise; the workspace of a
- * dilated problem is sized by conv2d_workspace_size_ex.  Same descriptors, workspace rules and error codes as the plain
+ * dilated problem is sized by conv2d_workspace_size_ex.  groups >= 1 divides C and K: the
+ * channels split into `groups` independent convolutions (input channels g*C/groups .. and output
+ * channels g*K/groups .. of group g), and the filter is K x C/groups x R x S (cuDNN's
+ * group count of the convolution descriptor); C and K stay the tensors' channel counts.  Same descriptors, workspace rules and error codes as the plain
  * entry points (which are these with cross-correlation, bias = NULL, beta = 0,
  * db_k = db_c = NULL). */
 int conv2d_fwd_ex(int N, int C, int H, int W, int K, int R, int S,
                   int pad_h, int pad_w, int stride_h, int stride_w, int P, int Q,
-                  int dil_h, int dil_w, int dtype, int mode,
+                  int dil_h, int dil_w, int groups, int dtype, int mode,
                   const void *x, const void *w, const void *bias, float beta, void *y,
                   void *workspace, size_t workspace_bytes, void *stream);
 
 int conv2d_bwd_data_ex(int N, int C, int H, int W, int K, int R, int S,
                        int pad_h, int pad_w, int stride_h, int stride_w, int P, int Q,
-                       int dil_h, int dil_w, int dtype, int mode,
+                       int dil_h, int dil_w, int groups, int dtype, int mode,
                        const void *dy, const void *w, const void *bias, float beta, void *dx,
                        void *workspace, size_t workspace_bytes, void *stream);
 
 int conv2d_bwd_filter_ex(int N, int C, int H, int W, int K, int R, int S,
                          int pad_h, int pad_w, int stride_h, int stride_w, int P, int Q,
-                         int dil_h, int dil_w, int dtype, int mode,
+                         int dil_h, int dil_w, int groups, int dtype, int mode,
                          const void *x, const void *dy, float beta, void *dw, void *db_k, void *db_c,
                          void *workspace, size_t workspace_bytes, void *stream);
 

@@ -204,27 +204,46 @@ def dilate_filter(w, dilation) -> np.ndarray:
     return out
 
 
-def conv2d_fwd_ex(x, w, bias=None, beta=0.0, y_old=None, pad=0, stride=1, flip=False, dilation=1) -> np.ndarray:
+# Groups (cuDNN's group count of the convolution descriptor): the C input and K output
+# channels split into `groups` independent convolutions, group g taking input channels
+# g*C/groups .. and output channels g*K/groups .. with filter rows g*K/groups .. of a
+# K x C/groups x R x S filter.  Written out as one plain op per group on channel slices.
+
+def conv2d_fwd_ex(x, w, bias=None, beta=0.0, y_old=None, pad=0, stride=1, flip=False, dilation=1,
+                  groups=1) -> np.ndarray:
     """y = conv(x, w) + bias[k] + beta * y_old (bias per output channel k, axis 1 of y); flip:
-    convolution mode; dilation: see above."""
+    convolution mode; dilation, groups: see above."""
+    x = _f64(x)
     wf = dilate_filter(_rot180(w) if flip else w, dilation)
-    return _epilogue(conv2d_fwd(x, wf, pad, stride), bias, beta, y_old, 1)
+    Cg, Kg = x.shape[1] // groups, wf.shape[0] // groups
+    y = np.concatenate([conv2d_fwd(x[:, g * Cg:(g + 1) * Cg], wf[g * Kg:(g + 1) * Kg], pad, stride)
+                        for g in range(groups)], axis=1)
+    return _epilogue(y, bias, beta, y_old, 1)
 
 
 def conv2d_bwd_data_ex(dy, w, x_hw, bias=None, beta=0.0, dx_old=None, pad=0, stride=1, flip=False,
-                       dilation=1) -> np.ndarray:
+                       dilation=1, groups=1) -> np.ndarray:
     """dx = bwd_data(dy, w) + bias[c] + beta * dx_old (bias per channel c of dx: the bias of
-    the deconvolution whose output dx is); flip: convolution mode; dilation: see above."""
+    the deconvolution whose output dx is); flip: convolution mode; dilation, groups: see above."""
+    dy = _f64(dy)
     wf = dilate_filter(_rot180(w) if flip else w, dilation)
-    return _epilogue(conv2d_bwd_data(dy, wf, x_hw, pad, stride), bias, beta, dx_old, 1)
+    Kg = dy.shape[1] // groups
+    dx = np.concatenate([conv2d_bwd_data(dy[:, g * Kg:(g + 1) * Kg], wf[g * Kg:(g + 1) * Kg], x_hw, pad, stride)
+                         for g in range(groups)], axis=1)
+    return _epilogue(dx, bias, beta, dx_old, 1)
 
 
-def conv2d_bwd_filter_ex(x, dy, rs, beta=0.0, dw_old=None, pad=0, stride=1, flip=False, dilation=1) -> np.ndarray:
-    """dw = bwd_filter(x, dy) + beta * dw_old; flip: the gradient of the rotated filter;
-    dilation: see above."""
+def conv2d_bwd_filter_ex(x, dy, rs, beta=0.0, dw_old=None, pad=0, stride=1, flip=False, dilation=1,
+                         groups=1) -> np.ndarray:
+    """dw (K, C/groups, R, S) = bwd_filter(x, dy) + beta * dw_old; flip: the gradient of the
+    rotated filter; dilation, groups: see above."""
+    x, dy = _f64(x), _f64(dy)
     dh, dwl = _pair(dilation)
     R, S = rs
-    big = conv2d_bwd_filter(x, dy, (dh * (R - 1) + 1, dwl * (S - 1) + 1), pad, stride)
+    Cg, Kg = x.shape[1] // groups, dy.shape[1] // groups
+    big = np.concatenate([conv2d_bwd_filter(x[:, g * Cg:(g + 1) * Cg], dy[:, g * Kg:(g + 1) * Kg],
+                                            (dh * (R - 1) + 1, dwl * (S - 1) + 1), pad, stride)
+                          for g in range(groups)], axis=0)
     dw = np.ascontiguousarray(big[:, :, ::dh, ::dwl])
     return _epilogue(_rot180(dw) if flip else dw, None, beta, dw_old, 0)
 

@@ -518,3 +518,50 @@ def test_dilation_adjoint_identities(case, dil):
         b = np.vdot(x, oracle.conv2d_bwd_data_ex(dy, w, (H, W), None, 0.0, None, (ph, pw), (sh, sw), flip, dil))
         c = np.vdot(w, oracle.conv2d_bwd_filter_ex(x, dy, (R, S), 0.0, None, (ph, pw), (sh, sw), flip, dil))
         assert abs(a - b) <= 1e-10 * max(1.0, abs(a)) and abs(a - c) <= 1e-10 * max(1.0, abs(a))
+
+
+# --------------------------------------------------------------------------- groups
+# cuDNN's group count of the convolution descriptor: `groups` independent convolutions on
+# channel slices, filter K x C/groups x R x S.  Pinned by PyTorch CPU fp64 (groups=) for the
+# three ops, with dilation and convolution mode mixed in, and by the adjoint identities.
+GROUP_CASES = [
+    ((2, 6, 9, 10, 9, 3, 3, 1, 1, 1, 1), 3, (1, 1)),
+    ((1, 8, 11, 12, 8, 3, 2, 1, 0, 2, 1), 8, (1, 1)),    # depthwise
+    ((2, 4, 13, 11, 6, 3, 3, 2, 2, 1, 2), 2, (2, 1)),
+]
+
+
+@pytest.mark.parametrize("case,groups,dil", GROUP_CASES)
+def test_groups_torch_witness(case, groups, dil):
+    torch = pytest.importorskip("torch")
+    import torch.nn.functional as F
+    N, C, H, W, K, R, S, ph, pw, sh, sw = case
+    P, Q = _dil_out(H, W, R, S, ph, pw, sh, sw, dil)
+    x = RNG.standard_normal((N, C, H, W))
+    w = RNG.standard_normal((K, C // groups, R, S))
+    dy = RNG.standard_normal((N, K, P, Q))
+    tx, tw, tdy = (torch.from_numpy(a) for a in (x, w, dy))
+    kw = dict(stride=(sh, sw), padding=(ph, pw), dilation=dil, groups=groups)
+    refs = (F.conv2d(tx, tw, **kw).numpy(),
+            torch.nn.grad.conv2d_input((N, C, H, W), tw, tdy, **kw).numpy(),
+            torch.nn.grad.conv2d_weight(tx, (K, C // groups, R, S), tdy, **kw).numpy())
+    gots = (oracle.conv2d_fwd_ex(x, w, None, 0.0, None, (ph, pw), (sh, sw), dilation=dil, groups=groups),
+            oracle.conv2d_bwd_data_ex(dy, w, (H, W), None, 0.0, None, (ph, pw), (sh, sw), dilation=dil, groups=groups),
+            oracle.conv2d_bwd_filter_ex(x, dy, (R, S), 0.0, None, (ph, pw), (sh, sw), dilation=dil, groups=groups))
+    for got, ref in zip(gots, refs):
+        assert got.shape == ref.shape
+        assert np.max(np.abs(got - ref)) <= 1e-12 * max(1.0, np.max(np.abs(ref)))
+
+
+@pytest.mark.parametrize("case,groups,dil", GROUP_CASES)
+def test_groups_adjoint_identities(case, groups, dil):
+    N, C, H, W, K, R, S, ph, pw, sh, sw = case
+    P, Q = _dil_out(H, W, R, S, ph, pw, sh, sw, dil)
+    x = RNG.standard_normal((N, C, H, W))
+    w = RNG.standard_normal((K, C // groups, R, S))
+    dy = RNG.standard_normal((N, K, P, Q))
+    for flip in (False, True):
+        a = np.vdot(oracle.conv2d_fwd_ex(x, w, None, 0.0, None, (ph, pw), (sh, sw), flip, dil, groups), dy)
+        b = np.vdot(x, oracle.conv2d_bwd_data_ex(dy, w, (H, W), None, 0.0, None, (ph, pw), (sh, sw), flip, dil, groups))
+        c = np.vdot(w, oracle.conv2d_bwd_filter_ex(x, dy, (R, S), 0.0, None, (ph, pw), (sh, sw), flip, dil, groups))
+        assert abs(a - b) <= 1e-10 * max(1.0, abs(a)) and abs(a - c) <= 1e-10 * max(1.0, abs(a))

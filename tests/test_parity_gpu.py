@@ -388,3 +388,57 @@ def test_dilation_parity(cg, case, dil, dtype):
             den = float(np.linalg.norm(ref))
             rel = float(np.linalg.norm(got - ref)) / den if den > 0 else float(np.linalg.norm(got))
             assert rel <= 1e-2, f"{case}/{dil}/{op}: {rel:.3e}"
+
+
+# ------------------------------------------------------------------ groups
+GROUP_GPU_CASES = [
+    ((2, 6, 9, 10, 9, 3, 3, 1, 1, 1, 1), 3, (1, 1), False),
+    ((1, 16, 12, 12, 16, 3, 3, 1, 1, 1, 1), 16, (1, 1), True),    # depthwise
+    ((2, 64, 16, 16, 64, 3, 3, 1, 1, 1, 1), 2, (1, 1), False),    # copy-engine staging per group
+    ((2, 8, 13, 11, 6, 3, 3, 2, 2, 1, 2), 2, (2, 1), True),
+]
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("case,groups,dil,flip", GROUP_GPU_CASES)
+def test_groups_parity(cg, case, groups, dil, flip, dtype):
+    N, C, H, Wd, K, R, S, ph, pw, sh, sw = case
+    dh, dw_ = dil
+    P = (H + 2 * ph - dh * (R - 1) - 1) // sh + 1
+    Q = (Wd + 2 * pw - dw_ * (S - 1) - 1) // sw + 1
+    idx = [c[0] for c in GROUP_GPU_CASES].index(case)
+    g = torch.Generator().manual_seed(9600 + idx)
+    tdt = torch.float32 if dtype == "f32" else torch.bfloat16
+    x = torch.randn(N, C, H, Wd, generator=g).to(tdt)
+    w = torch.randn(K, C // groups, R, S, generator=g).to(tdt)
+    dy = torch.randn(N, K, P, Q, generator=g).to(tdt)
+    bk = torch.randn(K, generator=g).to(tdt)
+    y0 = torch.randn(N, K, P, Q, generator=g).to(tdt)
+    pad, st = (ph, pw), (sh, sw)
+    xd, wd, dyd = x.to(DEV), w.to(DEV), dy.to(DEV)
+    y = y0.to(DEV)
+    cg.conv2d_fwd(xd, wd, pad, st, out=y, bias=bk.to(DEV), beta=1.0, dilation=dil, groups=groups, flip=flip)
+    dx = _poisoned((N, C, H, Wd), tdt)
+    cg.conv2d_bwd_data(dyd, wd, (H, Wd), pad, st, out=dx, dilation=dil, groups=groups, flip=flip)
+    dwt = _poisoned((K, C // groups, R, S), tdt)
+    dbk = _poisoned((K,), tdt)
+    cg.conv2d_bwd_filter(xd, dyd, (R, S), pad, st, out=dwt, dilation=dil, groups=groups, flip=flip, db_k=dbk)
+    cg.conv2d_device_status()
+    amax = lambda t: float(t.abs().max())
+    checks = (("fwd", y, oracle.conv2d_fwd_ex(x, w, bk, 1.0, y0, pad, st, flip, dil, groups), amax(x) * amax(w),
+               (C // groups) * R * S),
+              ("bwd_data", dx, oracle.conv2d_bwd_data_ex(dy, w, (H, Wd), None, 0.0, None, pad, st, flip, dil, groups),
+               amax(dy) * amax(w), (K // groups) * R * S),
+              ("bwd_filter", dwt, oracle.conv2d_bwd_filter_ex(x, dy, (R, S), 0.0, None, pad, st, flip, dil, groups),
+               amax(x) * amax(dy), N * P * Q),
+              ("db_k", dbk, oracle.channel_sum(dy), amax(dy), N * P * Q))
+    for op, got, ref, scale, L in checks:
+        got = got.double().cpu().numpy()
+        assert np.all(np.isfinite(got)), f"{case}/g{groups}/{op}: unwritten element"
+        if dtype == "f32":
+            err = float(np.abs(got - ref).max())
+            assert err <= 2e-3 * math.sqrt(L) * scale, f"{case}/g{groups}/{op}: {err:.3e}"
+        else:
+            den = float(np.linalg.norm(ref))
+            rel = float(np.linalg.norm(got - ref)) / den if den > 0 else float(np.linalg.norm(got))
+            assert rel <= 1e-2, f"{case}/g{groups}/{op}: {rel:.3e}"
