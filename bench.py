@@ -276,6 +276,38 @@ def run_ours(args, rank, world):
                for op in OPS}
     dilated["note"] = "same layer with dilation 2 and pad 2 (P, Q unchanged, same FLOP)"
 
+    # groups 2 on the same layer (two independent 32 -> 32 channel convolutions: half the FLOP)
+    wg2 = wd[:, : pb.C // 2].contiguous()
+    wsz_g = max(cg.conv2d_workspace_size(op, pb.dims(), dt, (1, 1), 2) for op in range(3))
+    ws_g = torch.empty(max(wsz_g, 16), dtype=torch.uint8, device=dev)
+    dwg = torch.empty_like(wg2)
+    grp_ms = {}
+    for op in OPS:
+        def gcall():
+            if op == "fwd":
+                cg.conv2d_fwd(xd, wg2, pad, st, out=y, workspace=ws_g, stream=stream, groups=2)
+            elif op == "bwd_data":
+                cg.conv2d_bwd_data(dyd, wg2, (pb.H, pb.W), pad, st, out=dx, workspace=ws_g, stream=stream, groups=2)
+            else:
+                cg.conv2d_bwd_filter(xd, dyd, (pb.R, pb.S), pad, st, out=dwg, workspace=ws_g, stream=stream, groups=2)
+        for _ in range(args.warmup):
+            flush.zero_()
+            gcall()
+        pairs = []
+        for _ in range(min(K, 50)):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            gcall()
+            b.record(stream)
+            pairs.append((a, b))
+        torch.cuda.synchronize()
+        grp_ms[op] = sum(a.elapsed_time(b) for a, b in pairs) / len(pairs)
+    cg.conv2d_device_status(stream)
+    grouped = {op: {"ms": round(grp_ms[op], 5), "tflops": round(pb.flops() / 2 / (grp_ms[op] * 1e-3) / 1e12, 2)}
+               for op in OPS}
+    grouped["note"] = "same layer with groups 2 (C/2 -> K/2 per group, half the FLOP)"
+
     extra_ms = ex_ms["bwd_filter_with_bias_grads"] - op_ms["bwd_filter"]
     sum_bytes = (math.prod(pb.y_shape) + math.prod(pb.x_shape)) * pb.elem_bytes()  # dy and x read once
     fused = {"fwd_bias_addto_ms": round(ex_ms["fwd_bias_addto"], 5),
@@ -352,6 +384,7 @@ def run_ours(args, rank, world):
         "gpu_launches": K * len(OPS) * KERNELS_PER_OP,
         "fused_epilogue": fused,
         "dilation_2": dilated,
+        "groups_2": grouped,
         "clocks": clocks,
     }
     if rank == 0 and not args.no_cpu_baseline:
