@@ -121,3 +121,43 @@ def test_workspace_sizes_are_bounded(cg):
 def test_strerror_covers_codes(cg):
     for c in range(0, -13, -1):
         assert cg.conv2d_strerror(c) and "unknown error" not in cg.conv2d_strerror(c)
+
+
+# ------------------------------------------------------------------ extended entry points
+def _ws_ex(cg, op, dims, dil=(1, 1), groups=1, dt=0):
+    lib = cg.load_library()
+    out = ctypes.c_size_t(0)
+    rc = lib.conv2d_workspace_size_ex(op, *dims, dil[0], dil[1], groups, dt, ctypes.byref(out))
+    return rc, out.value
+
+
+def test_ex_entry_points_validate_on_the_host(cg):
+    """Mode, dilation and groups are checked before anything is planned or launched."""
+    lib = cg.load_library()
+    d = ctypes.c_void_p(0x10000)
+    grp = (2, 6, 8, 8, 9, 3, 3, 1, 1, 1, 1, 8, 8)
+    # unknown mode
+    assert lib.conv2d_fwd_ex(*GOOD, 1, 1, 1, 0, 2, d, d, None, ctypes.c_float(0), d, None, 0, None) == -1
+    assert lib.conv2d_bwd_data_ex(*GOOD, 1, 1, 1, 0, 5, d, d, None, ctypes.c_float(0), d, None, 0, None) == -1
+    assert lib.conv2d_bwd_filter_ex(*GOOD, 1, 1, 1, 0, -1, d, d, ctypes.c_float(0), d, None, None, None, 0,
+                                    None) == -1
+    # dilation < 1
+    assert _ws_ex(cg, 0, GOOD, dil=(0, 1))[0] == -1
+    # P, Q must follow the dilated filter extent: R = 3, dilation 2 -> extent 5
+    assert _ws_ex(cg, 0, GOOD, dil=(2, 2))[0] == -2
+    assert _ws_ex(cg, 0, (2, 3, 8, 8, 4, 3, 3, 2, 2, 1, 1, 8, 8), dil=(2, 2))[0] == 0
+    # groups must divide C and K
+    assert _ws_ex(cg, 0, grp, groups=3)[0] == 0
+    assert _ws_ex(cg, 0, grp, groups=2)[0] == -1      # K = 9
+    assert _ws_ex(cg, 2, grp, groups=0)[0] == -1
+    for op in (0, 1, 2):
+        assert _ws_ex(cg, op, GOOD)[1] == _ws(cg, op, GOOD)[1]   # defaults = the plain sizing
+
+
+def test_grouped_and_dilated_workspace_bounded(cg):
+    for dims, dil, groups in [((32, 64, 56, 56, 64, 3, 3, 1, 1, 1, 1, 56, 56), (1, 1), 2),
+                              ((32, 64, 56, 56, 64, 3, 3, 2, 2, 1, 1, 56, 56), (2, 2), 1),
+                              ((8, 32, 28, 28, 32, 3, 3, 1, 1, 1, 1, 28, 28), (1, 1), 32)]:
+        for op in (0, 1, 2):
+            rc, n = _ws_ex(cg, op, dims, dil, groups)
+            assert rc == 0 and 0 < n <= 1_000_000_000 and n % 16 == 0
