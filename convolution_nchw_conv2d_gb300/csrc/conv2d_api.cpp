@@ -562,7 +562,7 @@ int build_bwd_filter_impl(const Desc& d0, const void* x, const void* dy, void* d
   bool tma = allow_tma && d.sw == 1 && d.W % CHUNK == 0 && d.Q % CHUNK == 0 && ((uintptr_t)x & 15) == 0 &&
              ((uintptr_t)dy & 15) == 0 && encode_tiled_fn() != nullptr;
   p.TRU = 1;
-  if (tma && allow_rowshare && d.sh == 1 && d.dh == 1 && d.C >= 32 && d.R > 1 && 2 * p.NK <= 384)
+  if (tma && allow_rowshare && d.sh == 1 && d.C >= 32 && d.R > 1 && 2 * p.NK <= 384)
     p.TRU = std::min(std::min(d.R, 4), 384 / p.NK);
   if (allow_rowshare && p.TRU == 1) return CONV2D_ERR_UNSUPPORTED;  // the caller plans without sharing
   if (tma) {
@@ -589,7 +589,8 @@ int build_bwd_filter_impl(const Desc& d0, const void* x, const void* dy, void* d
   }
   p.EL = d.P + mh;
   p.Mtot = (long long)d.N * p.EL * p.WL;
-  p.Mit = p.Mtot + (long long)(p.TRU - 1) * p.WL;
+  p.tru_step = d.dh;  // (unit row stride only: sh == 1 whenever TRU > 1)
+  p.Mit = p.Mtot + (long long)(p.TRU - 1) * p.tru_step * p.WL;
   if (p.Mit >= (1ll << 31)) return CONV2D_ERR_TOO_LARGE;
   p.fd_img = make_fastdiv((uint32_t)(p.EL * p.WL));
   p.fd_WL = make_fastdiv((uint32_t)p.WL);
@@ -671,8 +672,8 @@ int build_bwd_filter_impl(const Desc& d0, const void* x, const void* dy, void* d
       while ((q.xs * ESZ) % 128 != 16) q.xs += CHUNK;
       // row ring: S stages plus the halo, plus a row at each end
       q.NR = (S * KB + p.max_off + p.delta + p.WL - 1) / p.WL + 2;
-      // dy row ring (row-tap sharing): the rows of S stages plus TRU - 1 rows before them
-      q.NRd = p.TRU > 1 ? (S * KB + (p.TRU - 1) * p.WL - 1) / p.WL + 2 : 0;
+      // dy row ring (row-tap sharing): the rows of S stages plus (TRU - 1) * tru_step rows before
+      q.NRd = p.TRU > 1 ? (S * KB + (p.TRU - 1) * p.tru_step * p.WL - 1) / p.WL + 2 : 0;
       q.a_stage_bytes = p.TRU > 1 ? 0 : KB * p.NK * ESZ;
       if (wgrad_smem_bytes(q, d.dt) > di.smem_optin) continue;
       const long long score = (long long)S * KB * 4 + KB / 32;

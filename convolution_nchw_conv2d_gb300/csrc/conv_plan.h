@@ -143,13 +143,15 @@ struct WgradPlan {
   // (r0, s) and stands for the TRU taps (r0 + j, s), j < TRU.  Since tap (r0 + j, s) reads
   // x at L + j*WL + off(r0, s), the sum over positions L equals the sum over L' = L + j*WL of
   // x[L' + off(r0, s)] * dy[L' - j*WL]: one A operand built from x at L' serves all TRU taps,
-  // each paired with dy shifted back by j linear rows.  dy is then staged as a ring of NRd
-  // whole linear rows, [row slot][chunk][k][CHUNK], and the positions L' run over
-  // [0, Mtot + (TRU-1)*WL) (dy reads as zero outside [0, Mtot)).
+  // each paired with dy shifted back by j linear rows (j*dil_h rows with row dilation: the
+  // shift is j*tru_step).  dy is then staged as a ring of NRd whole linear rows,
+  // [row slot][chunk][k][CHUNK], and the positions L' run over [0, Mtot + (TRU-1)*tru_step*WL)
+  // (dy reads as zero outside [0, Mtot)).
   int TRU;               // row taps per unit (1: every unit is one tap)
+  int tru_step;          // linear rows between consecutive row taps (the row dilation)
   int NRd;               // dy ring rows (TRU > 1)
   FastDiv fd_NRd;
-  long long Mit;         // positions iterated (Mtot + (TRU - 1) * WL)
+  long long Mit;         // positions iterated (Mtot + (TRU - 1) * tru_step * WL)
   int unit_tap[kMaxTaps];  // base tap of the j-th unit of a channel group (TPU == 1)
   const void* x;         // NCHW
   const void* dy;        // N K P Q

@@ -294,7 +294,7 @@ __device__ __forceinline__ void issue_row_taps(const WgradPlan& p, uint32_t dcol
     uint32_t lo[TRU];
 #pragma unroll
     for (int j = 0; j < TRU; ++j) {
-      int sl = row0 - j;
+      int sl = row0 - j * p.tru_step;
       if (sl < 0) sl += p.NRd;
       lo[j] = (((dyring + (uint32_t)sl * rbytes + (uint32_t)(col0 / CHUNK) * cbytes) & 0x3FFFFu) >> 4) | lbo;
     }
@@ -317,7 +317,7 @@ __device__ __forceinline__ void issue_row_taps(const WgradPlan& p, uint32_t dcol
     const uint32_t cofs = (uint32_t)(col / CHUNK) * cbytes;
 #pragma unroll
     for (int j = 0; j < TRU; ++j) {
-      int sl = row - j;
+      int sl = row - j * p.tru_step;
       if (sl < 0) sl += p.NRd;
       const uint32_t addr = dyring + (uint32_t)sl * rbytes + cofs;
       mma_ts_lh<KIND>(dcol + (uint32_t)(j * p.NK), acol + (uint32_t)(8 * i), ((addr & 0x3FFFFu) >> 4) | lbo, b_hi, id,
@@ -435,7 +435,7 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_kernel(const __grid_constan
         // Row bookkeeping in 32 bits with multiply-high divisions (positions and rows < 2^31):
         // the producers' issue time is on the pipeline's critical path.
         int next_row = (int)fdiv((uint32_t)(lbeg + p.delta), p.fd_WL);  // first x row not loaded
-        int next_dy_row = (int)fdiv((uint32_t)lbeg, p.fd_WL) - (p.TRU - 1);  // first dy row not loaded
+        int next_dy_row = (int)fdiv((uint32_t)lbeg, p.fd_WL) - (p.TRU - 1) * p.tru_step;  // first dy row not loaded
         int s_local = 0;
         for (long long l0 = lbeg; l0 < lend; l0 += KB, ++counter, ++s_local) {
           const int stage = (int)(counter % S);
@@ -463,7 +463,7 @@ __global__ void __launch_bounds__(kThreads, 1) wgrad_kernel(const __grid_constan
           const uint32_t fb = bar_at(full, stage);
           const uint32_t a_st = a0 + (uint32_t)stage * p.a_stage_bytes;
           if (p.TRU > 1) {
-            // dy: the linear rows this stage reads that are not loaded yet, from (TRU - 1) rows
+            // dy: the linear rows this stage reads that are not loaded yet, from (TRU - 1) * tru_step rows
             // before the stage to its last position; one tensor copy per row (NK channels,
             // [chunk][k][CHUNK]); rows before the first image, past the last one, or past
             // the output height read as zeros.
