@@ -11,13 +11,14 @@
 // this is deconvolution forward with the weight's in/out roles swapped (Apache
 // MXNet mkldnn_deconvolution.cc, MKLDNNDeconvFwd::Execute comment).
 //
-// CTA roles (416 threads, persistent over tiles):
+// CTA roles (448 threads, persistent over tiles):
 //   warps 0-7  two producer groups taking pipeline stages in turn: stage source rows
 //              for CB channels into shared memory in the core-matrix interleaved layout
-//              (16-byte loads + register transpose where rows are contiguous, scalar
-//              loads elsewhere), and bulk-copy the packed filter slice.
+//              (one load per channel of each staged row, 16-byte shared stores), and
+//              bulk-copy the packed filter slice.
 //   warps 8-11 epilogue: TMEM -> registers -> NCHW global stores, coalesced along
-//              output positions; bf16 outputs rounded to nearest even.
+//              output positions, with the optional bias and add-to (beta) of the fused
+//              epilogue; bf16 outputs rounded to nearest even.
 //   warps 12-13 TMEM allocation (warp 12); each warp issues tcgen05.mma (kind::tf32
 //              for fp32, kind::f16 with bf16 operands) for one 128-row accumulator half,
 //              through one elected lane.

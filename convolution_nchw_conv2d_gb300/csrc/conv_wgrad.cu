@@ -5,16 +5,19 @@
 // LibMatrixCuDNNConvolutionAlgorithm.java; deconvolution's backward-weights in Apache
 // MXNet mkldnn_deconvolution.cc is the same product with the weight's roles swapped).
 //
-// One GEMM per tile (see WgradPlan in conv_plan.h): 128 rows (c, tap) x NK output
-// channels k, reduction over a range of the forward linear position space L.
-//   producers  stage dy[k, L] per pipeline stage (K-major: positions contiguous, as in
-//              NCHW) and append the stage's new x positions to a ring of x rows (one row
-//              per plane and channel), so every x position is read from memory once per tile.
+// One GEMM per tile (see WgradPlan in conv_plan.h): G m-tiles of 128 rows (c, tap) x NK
+// output channels k, reduction over a range of the forward linear position space L.
+//   producers  stage dy[k, L] (K-major: positions contiguous, as in NCHW) per pipeline stage,
+//              or as a ring of whole linear rows (row-tap sharing), and x either as a ring of
+//              whole image rows loaded by tensor copies or as a ring of slots (one row per
+//              plane and channel) appended stage by stage, so every x position is read from
+//              memory once per tile.
 //   builders   write the im2col rows A[(c, tap), L] = X_plane(tap)[c, L + tap_off] into
 //              TMEM, 32 columns per buffer (tcgen05.st); the 32 lanes of a warp read 32
 //              ring rows whose starts fall in distinct shared-memory banks.
 //   MMA warp   issues tcgen05.mma with A from TMEM and B = dy from shared memory
-//              (kind::tf32 / kind::f16 with bf16), 4 per buffer, accumulating in TMEM.
+//              (kind::tf32 / kind::f16 with bf16), 4 per buffer -- 4 per filter row sharing
+//              the buffer under row-tap sharing -- accumulating in TMEM.
 //   epilogue   stores each tile's fp32 sums as a split partial; a second kernel adds the
 //              partials in a fixed order (deterministic) and writes dw in KCRS.
 #include "conv_plan.h"
