@@ -141,6 +141,22 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------ our arm
+def slowest_rank_ms(ms, world, device):
+    """Replicas only: every rank runs the whole step on its own GPU; the job's step time is the
+    slowest rank's (MAX over ranks through the process group; no data-path collective)."""
+    if world <= 1:
+        return ms
+    import torch
+    t = torch.tensor([float(ms)], device=device, dtype=torch.float64)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(flop_per_op, n_ops, world, step_ms):
+    """Whole-job throughput: all ranks' FLOP over the slowest rank's step time (weak scaling)."""
+    return world * n_ops * flop_per_op / (step_ms * 1e-3) / 1e12
+
+
 def run_ours(args, rank, world):
     import torch
     import convolution_nchw_conv2d_gb300 as cg
@@ -206,10 +222,7 @@ def run_ours(args, rank, world):
     cg.conv2d_device_status(stream)
     op_ms = {op: sum(a.elapsed_time(b) for a, b in evs[op]) / K for op in OPS}
     step_ms = sum(op_ms.values())
-    if world > 1:
-        tt = torch.tensor([step_ms], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        step_ms = float(tt.item())
+    step_ms = slowest_rank_ms(step_ms, world, dev)
 
     # ---- fused epilogues (bias + add-to on forward, bias gradients on backward-filter),
     # timed like the step's ops but outside it
@@ -397,7 +410,7 @@ def run_ours(args, rank, world):
     roof["kernel"] = dom
     roof["peak_source"] = peaks["source"] + (" (bf16 x nominal tf32/bf16 ratio)" if pb.dtype == "f32" else "")
 
-    value = world * 3 * flop / (step_ms * 1e-3) / 1e12
+    value = job_tflops(flop, len(OPS), world, step_ms)
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world,
         "steps": K, "warmup": args.warmup, "ms_per_step": round(step_ms, 5),
