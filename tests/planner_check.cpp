@@ -1,0 +1,207 @@
+// Host-only check of the launch planner (no GPU): plans the three ops for a list of shapes
+// and verifies the invariants the kernels rely on -- shared-memory and TMEM budgets, staged
+// rows covering every tap offset, ring sizes covering the positions in flight, bank-spread
+// ring pitches, and that every (channel, tap) of the filter gradient is produced exactly once.
+// Tensor maps are not encoded (a stand-in encoder accepts every map), so the copy-engine
+// plans are checked as they would be planned for aligned tensors.  Prints one line per
+// violation and exits with the number of violations (capped at 100).
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+static CUresult accept_map(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*, const cuuint64_t*,
+                           const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                           CUtensorMapL2promotion, CUtensorMapFloatOOBfill) {
+  return CUDA_SUCCESS;
+}
+static cudaError_t entry_point_stand_in(const char*, void** f, unsigned int, unsigned long long,
+                                        cudaDriverEntryPointQueryResult* q) {
+  *f = (void*)&accept_map;
+  *q = cudaDriverEntryPointSuccess;
+  return cudaSuccess;
+}
+#define cudaGetDriverEntryPointByVersion entry_point_stand_in
+#include "conv2d_api.cpp"
+
+#include <cstdio>
+#include <vector>
+
+namespace {
+
+int g_fail = 0;
+
+void fail(const char* nm, const char* op, const char* what) {
+  ++g_fail;
+  std::printf("FAIL %s %s: %s\n", nm, op, what);
+}
+
+struct Shape {
+  const char* nm;
+  int N, C, H, W, K, R, S, ph, pw, sh, sw, dt;
+  int dh, dw, g;
+  int refused;  // bit 0 forward, bit 1 backward-data: expected CONV2D_ERR_UNSUPPORTED
+};
+
+void check_tap(const char* nm, const char* op, const TapBuild& b, const DevInfo& di) {
+  const TapPlan& p = b.p;
+  if (tap_gemm_smem_bytes(p) > di.smem_optin) fail(nm, op, "shared memory over budget");
+  if (p.tmem_cols > 512 || p.ACCB * p.MH * p.NT > p.tmem_cols) fail(nm, op, "TMEM over budget");
+  if (p.rows < 128 * p.MH) fail(nm, op, "staged rows below the tile height");
+  for (int ph = 0; ph < p.nph; ++ph)
+    for (int t = p.ph_tap_begin[ph]; t < p.ph_tap_begin[ph] + p.ph_ntaps[ph]; ++t)
+      if (p.tap_off[t] < 0 || p.tap_off[t] + 128 * p.MH > p.rows) fail(nm, op, "tap offset beyond the staged rows");
+  if (p.NT % 16 || p.NT > 256 || (p.MH != 1 && p.MH != 2)) fail(nm, op, "tile shape");
+  if (p.Mtot >= (1ll << 31)) fail(nm, op, "position space too large");
+}
+
+void check_wgrad(const char* nm, const Desc& d, const WgradBuild& b, const DevInfo& di) {
+  const char* op = "bwd_filter";
+  const WgradPlan& p = b.p;
+  if (wgrad_smem_bytes(p, d.dt) > di.smem_optin) fail(nm, op, "shared memory over budget");
+  if (128 + p.accb * p.G * p.TRU * p.NK > p.tmem_cols || p.tmem_cols > 512) fail(nm, op, "TMEM over budget");
+  if (p.use_tma != 1 && p.rlen < p.stages * p.KB + p.max_off + 4) fail(nm, op, "slot ring shorter than the positions in flight");
+  if (p.use_tma == 1) {
+    // rows touched by the stages in flight: at most floor((S*KB + max_off - 1) / WL) + 2
+    if ((long long)(p.NR - 2) * p.WL < (long long)p.stages * p.KB + p.max_off - 1) fail(nm, op, "x row ring too small");
+    if (d.dt == 0 && p.WLx % 8 != 4) fail(nm, op, "x row pitch not 16 bytes past a multiple of 32");
+    if (d.dt == 1 && p.WLx % 16 != 8) fail(nm, op, "x row pitch not 16 bytes past a multiple of 32");
+  }
+  if (p.TRU > 1) {
+    if ((long long)(p.NRd - 1 - (p.TRU - 1) * p.tru_step) * p.WL <= (long long)p.stages * p.KB - 1)
+      fail(nm, op, "dy row ring too small");
+    if (p.WL % (d.dt == 0 ? 8 : 16)) fail(nm, op, "row width splits an MMA's chunk pair");
+    if (p.use_tma != 1 || p.TPU != 1) fail(nm, op, "row-tap sharing outside the row ring");
+  }
+  if (p.KB % (d.dt == 0 ? 32 : 64)) fail(nm, op, "stage not a whole number of A buffers");
+  // every row of every m-tile lies in the staged channels of its group, and every
+  // (channel, tap) is produced exactly once
+  std::vector<int> seen((size_t)d.C * p.RS, 0);
+  for (int mg = 0; mg < p.n_mgroups; ++mg) {
+    const int mt0 = mg * p.G;
+    const int c_lo = ((4 * mt0) / p.upc) * p.Cg;
+    for (int mt = mt0; mt < std::min(p.n_mtiles, mt0 + p.G); ++mt)
+      for (int q = 0; q < 4; ++q)
+        for (int l = 0; l < 32; ++l) {
+          const int u = 4 * mt + q;
+          if (u >= p.nunits) continue;
+          const int cg = u / p.upc, tu = u % p.upc;
+          int c, tap;
+          bool v;
+          if (p.TPU == 1) {
+            c = cg * p.Cg + l;
+            tap = p.unit_tap[tu];
+            v = c < d.C;
+          } else {
+            const int tl = l / p.Cg;
+            c = l - tl * p.Cg;
+            tap = tu * p.TPU + tl;
+            v = tl < p.TPU && tap < p.RS;
+          }
+          if (!v) continue;
+          if (c - c_lo < 0 || c - c_lo >= p.xch) fail(nm, op, "row outside the group's staged channels");
+          if (p.use_tma == 1 && c - c_lo >= p.xr) fail(nm, op, "row outside the row ring's channels");
+          for (int j = 0; j < p.TRU; ++j) {
+            if (tap / d.S + j >= d.R) break;
+            ++seen[(size_t)c * p.RS + tap + j * d.S];
+          }
+        }
+  }
+  for (size_t i = 0; i < seen.size(); ++i)
+    if (seen[i] != 1) {
+      fail(nm, op, "a (channel, tap) of the filter gradient is not produced exactly once");
+      break;
+    }
+}
+
+}  // namespace
+
+int main() {
+  using namespace cg3;
+  // The last field marks the refusals the planner is expected to make.  The tap GEMM stages
+  // the filter slices of every tap of a phase for each k-block; with a stride-1 15x15 filter
+  // and more than 4 fp32 (8 bf16) source channels that is 225 taps x 2 chunks x 16 columns
+  // x 16 bytes = 115 KB a stage, so two stages do not fit in shared memory and the call
+  // returns CONV2D_ERR_UNSUPPORTED.  With at most 4 (8) source channels two taps share one
+  // MMA and the slices halve.  The source channels are C forward and K backward-data.
+  std::vector<Shape> shapes = {
+      {"tiny", 2, 3, 8, 8, 4, 3, 3, 1, 1, 1, 1, 0, 1, 1, 1, 0},
+      {"resnet3x3", 32, 64, 56, 56, 64, 3, 3, 1, 1, 1, 1, 0, 1, 1, 1, 0},
+      {"resnet3x3_bf16", 32, 64, 56, 56, 64, 3, 3, 1, 1, 1, 1, 1, 1, 1, 1, 0},
+      {"strided", 64, 128, 56, 56, 256, 3, 3, 1, 1, 2, 2, 0, 1, 1, 1, 0},
+      {"pointwise", 128, 256, 14, 14, 1024, 1, 1, 0, 0, 1, 1, 0, 1, 1, 1, 0},
+      {"stem7x7", 64, 3, 224, 224, 64, 7, 7, 3, 3, 2, 2, 0, 1, 1, 1, 0},
+      {"deconv", 32, 256, 32, 32, 512, 4, 4, 1, 1, 2, 2, 1, 1, 1, 1, 0},
+      {"c33", 3, 33, 9, 11, 40, 3, 3, 1, 1, 1, 1, 0, 1, 1, 1, 0},
+      {"k300", 1, 17, 6, 6, 300, 3, 3, 1, 1, 1, 1, 0, 1, 1, 1, 0},
+      {"c300", 2, 300, 5, 5, 20, 3, 3, 1, 1, 1, 1, 1, 1, 1, 1, 0},
+      {"c5k300", 2, 5, 17, 13, 300, 5, 3, 2, 1, 2, 1, 1, 1, 1, 1, 0},
+      {"r15", 1, 4, 40, 40, 8, 15, 15, 7, 7, 1, 1, 0, 1, 1, 1, 2},
+      {"r15_k4", 1, 8, 40, 40, 4, 15, 15, 7, 7, 1, 1, 0, 1, 1, 1, 1},
+      {"s32", 2, 40, 23, 19, 24, 3, 3, 1, 1, 3, 2, 1, 1, 1, 1, 0},
+      {"hr", 1, 2, 6, 13, 2, 6, 13, 0, 0, 1, 1, 0, 1, 1, 1, 0},
+      {"rows5", 1, 40, 16, 16, 48, 5, 3, 2, 1, 1, 1, 0, 1, 1, 1, 0},
+      {"rows5_bf16", 1, 40, 16, 16, 48, 5, 3, 2, 1, 1, 1, 1, 1, 1, 1, 0},
+      {"wide_k", 1, 32, 8, 8, 150, 3, 3, 1, 1, 1, 1, 0, 1, 1, 1, 0},
+      {"wide_k_bf16", 1, 32, 8, 8, 150, 3, 3, 1, 1, 1, 1, 1, 1, 1, 1, 0},
+      {"rect", 2, 48, 10, 16, 20, 3, 5, 1, 2, 1, 1, 0, 1, 1, 1, 0},
+      {"big7", 8, 64, 32, 32, 64, 7, 7, 3, 3, 1, 1, 0, 1, 1, 1, 0},
+      {"dil2", 2, 64, 16, 16, 64, 3, 3, 2, 2, 1, 1, 0, 2, 2, 1, 0},
+      {"dil2_bf16", 2, 64, 16, 16, 64, 3, 3, 2, 2, 1, 1, 1, 2, 2, 1, 0},
+      {"dil23", 1, 5, 20, 17, 7, 3, 2, 2, 1, 2, 1, 1, 2, 3, 1, 0},
+      {"dil32", 1, 33, 15, 16, 40, 2, 3, 1, 2, 1, 2, 0, 3, 2, 1, 0},
+      {"dil3_s2", 2, 3, 21, 21, 16, 3, 3, 3, 3, 2, 2, 1, 3, 3, 1, 0},
+      {"grp3", 2, 6, 9, 10, 9, 3, 3, 1, 1, 1, 1, 0, 1, 1, 3, 0},
+      {"grp2", 2, 64, 16, 16, 64, 3, 3, 1, 1, 1, 1, 0, 1, 1, 2, 0},
+      {"depthwise", 1, 16, 12, 12, 16, 3, 3, 1, 1, 1, 1, 1, 1, 1, 16, 0},
+      {"grp_dil", 2, 8, 13, 11, 6, 3, 3, 2, 2, 1, 2, 0, 2, 1, 2, 0},
+  };
+  DevInfo di;
+  di.sms = 152;
+  di.smem_optin = 232448;
+  di.ok = true;
+  int plans = 0;
+  for (const Shape& s : shapes) {
+    Desc t{};
+    t.N = s.N; t.C = s.C; t.H = s.H; t.W = s.W; t.K = s.K; t.R = s.R; t.S = s.S;
+    t.ph = s.ph; t.pw = s.pw; t.sh = s.sh; t.sw = s.sw; t.dt = s.dt; t.dh = s.dh; t.dw = s.dw;
+    t.P = out_dim(t.H, t.ph, t.dh * (t.R - 1) + 1, t.sh);
+    t.Q = out_dim(t.W, t.pw, t.dw * (t.S - 1) + 1, t.sw);
+    if (validate(t) != CONV2D_OK) { fail(s.nm, "desc", "descriptor rejected"); continue; }
+    Desc d;
+    if (group_desc(t, s.g, d) != CONV2D_OK) { fail(s.nm, "desc", "groups rejected"); continue; }
+    void* px = (void*)0x100000;  // 16-byte aligned stand-in addresses
+    void* pw = (void*)0x200000;
+    void* py = (void*)0x300000;
+    void* ws = (void*)0x400000;
+    TapBuild bf, bd;
+    const int rcf = build_fwd(d, px, pw, py, ws, di, bf);
+    if (s.refused & 1) {
+      if (rcf != CONV2D_ERR_UNSUPPORTED) fail(s.nm, "fwd", "expected the documented refusal");
+    } else if (rcf != CONV2D_OK) {
+      fail(s.nm, "fwd", "no plan");
+    } else {
+      check_tap(s.nm, "fwd", bf, di);
+      ++plans;
+    }
+    const int rcd = build_bwd_data(d, py, pw, px, ws, di, bd);
+    if (s.refused & 2) {
+      if (rcd != CONV2D_ERR_UNSUPPORTED) fail(s.nm, "bwd_data", "expected the documented refusal");
+    } else if (rcd != CONV2D_OK) {
+      fail(s.nm, "bwd_data", "no plan");
+    } else {
+      check_tap(s.nm, "bwd_data", bd, di);
+      ++plans;
+    }
+    for (const auto& v : kWgradVariants) {  // every staging variant the planner may fall back to
+      WgradBuild bw;
+      const int rc = build_bwd_filter_impl(d, px, py, pw, ws, di, bw, v[0], v[1]);
+      if (rc == CONV2D_ERR_UNSUPPORTED) continue;
+      if (rc != CONV2D_OK) { fail(s.nm, "bwd_filter", "planner error"); continue; }
+      check_wgrad(s.nm, d, bw, di);
+      ++plans;
+    }
+    WgradBuild bw;
+    if (build_bwd_filter(d, px, py, pw, ws, di, bw) != CONV2D_OK) fail(s.nm, "bwd_filter", "no plan");
+  }
+  std::printf("checked %d plans, %d violations\n", plans, g_fail);
+  return g_fail > 100 ? 100 : g_fail;
+}
