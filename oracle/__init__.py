@@ -1,12 +1,12 @@
-"""fp64 CPU oracle for NCHW conv2d -- TEST INFRASTRUCTURE ONLY.
+"""fp64 CPU oracle for NCHW conv2d (and NCDHW conv3d) -- TEST INFRASTRUCTURE ONLY.
 
 Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
 ``bench.py`` may import this package.  The product (``convolution_nchw_conv2d_gb300``)
 never imports it and shares no code with it.
 
-The convolution arithmetic lives in ``conv2d_oracle.c`` (plain C, fp64, gather
-form, OpenMP over output elements); this module compiles it with gcc and marshals
-numpy arrays through ctypes.  The fused epilogues (bias, beta) and the per-channel
+The convolution arithmetic lives in ``conv2d_oracle.c`` and ``conv3d_oracle.c``
+(plain C, fp64, gather form, OpenMP over output elements); this module compiles
+them with gcc into one library and marshals numpy arrays through ctypes.  The fused epilogues (bias, beta) and the per-channel
 bias-gradient sums are written here directly in fp64 numpy on top of those ops.
 Inputs of any float dtype are widened exactly to fp64 before the call.
 
@@ -17,8 +17,8 @@ backward-data with the weight's in/out channel roles swapped); the C#
 ``FilterDescriptor.SetFilter4dDescriptor`` examples (overwrite, alpha = 1,
 beta = 0).
 
-Parity status: all functions pinned by ``tests/test_oracle_pins.py``;
-NaN/Inf propagation is parity unpinned.
+Parity status: all functions pinned by ``tests/test_oracle_pins.py`` (2-D) and
+``tests/test_oracle_pins_3d.py`` (3-D); NaN/Inf propagation is parity unpinned.
 """
 from __future__ import annotations
 
@@ -30,7 +30,7 @@ import threading
 import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-_SRC = os.path.join(_HERE, "conv2d_oracle.c")
+_SRCS = [os.path.join(_HERE, "conv2d_oracle.c"), os.path.join(_HERE, "conv3d_oracle.c")]
 _BUILD = os.path.join(_HERE, "_build")
 _LIB = os.path.join(_BUILD, "liboracle_conv2d.so")
 _lock = threading.Lock()
@@ -40,37 +40,45 @@ _lib = None
 def build(force: bool = False) -> str:
     """Compile the oracle with gcc (-O2 -fopenmp) into ``oracle/_build``."""
     os.makedirs(_BUILD, exist_ok=True)
-    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < max(map(os.path.getmtime, _SRCS)):
         tmp = _LIB + f".tmp{os.getpid()}"
         subprocess.check_call(["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-std=c99",
-                               "-o", tmp, _SRC])
+                               "-o", tmp] + _SRCS)
         os.replace(tmp, _LIB)
     return _LIB
+
+
+def _bind(lib):
+    """Set the ctypes signatures of the oracle library's entry points; returns lib."""
+    i = ctypes.c_int
+    dp = ctypes.POINTER(ctypes.c_double)
+    ip = ctypes.POINTER(ctypes.c_int64)
+    i64 = ctypes.c_int64
+    lib.oracle_output_dim.argtypes = [i, i, i, i]
+    lib.oracle_output_dim.restype = i
+    for name in ("oracle_conv2d_fwd", "oracle_conv2d_bwd_data", "oracle_conv2d_bwd_filter"):
+        getattr(lib, name).argtypes = [dp, dp, dp] + [i] * 13
+        getattr(lib, name).restype = None
+    lib.oracle_deconv2d_fwd_scatter.argtypes = [dp, dp, dp] + [i] * 13
+    lib.oracle_deconv2d_fwd_scatter.restype = None
+    for name in ("oracle_conv2d_fwd_at", "oracle_conv2d_bwd_data_at",
+                 "oracle_conv2d_bwd_filter_at"):
+        getattr(lib, name).argtypes = [dp, dp] + [i] * 13 + [ip, i64, dp]
+        getattr(lib, name).restype = None
+    ivp = ctypes.POINTER(ctypes.c_int)
+    for name in ("oracle_conv3d_fwd", "oracle_conv3d_bwd_data", "oracle_conv3d_bwd_filter"):
+        getattr(lib, name).argtypes = [dp, dp, dp, ivp]
+        getattr(lib, name).restype = None
+    lib.oracle_num_threads.argtypes = []
+    lib.oracle_num_threads.restype = i
+    return lib
 
 
 def _load():
     global _lib
     with _lock:
         if _lib is None:
-            lib = ctypes.CDLL(build())
-            i = ctypes.c_int
-            dp = ctypes.POINTER(ctypes.c_double)
-            ip = ctypes.POINTER(ctypes.c_int64)
-            i64 = ctypes.c_int64
-            lib.oracle_output_dim.argtypes = [i, i, i, i]
-            lib.oracle_output_dim.restype = i
-            for name in ("oracle_conv2d_fwd", "oracle_conv2d_bwd_data", "oracle_conv2d_bwd_filter"):
-                getattr(lib, name).argtypes = [dp, dp, dp] + [i] * 13
-                getattr(lib, name).restype = None
-            lib.oracle_deconv2d_fwd_scatter.argtypes = [dp, dp, dp] + [i] * 13
-            lib.oracle_deconv2d_fwd_scatter.restype = None
-            for name in ("oracle_conv2d_fwd_at", "oracle_conv2d_bwd_data_at",
-                         "oracle_conv2d_bwd_filter_at"):
-                getattr(lib, name).argtypes = [dp, dp] + [i] * 13 + [ip, i64, dp]
-                getattr(lib, name).restype = None
-            lib.oracle_num_threads.argtypes = []
-            lib.oracle_num_threads.restype = i
-            _lib = lib
+            _lib = _bind(ctypes.CDLL(build()))
     return _lib
 
 
@@ -281,6 +289,88 @@ def conv2d_bwd_data_at(dy, w, dims, idx) -> np.ndarray:
 def conv2d_bwd_filter_at(x, dy, dims, idx) -> np.ndarray:
     """Backward-filter outputs at flat (k,c,r,s) indices."""
     return _at(_load().oracle_conv2d_bwd_filter_at, x, dy, dims, idx)
+
+
+# ------------------------------------------------------------------ 3-D (NCDHW)
+# Page "mkldnn_convolution.cc" (Apache MXNet): kernels of one to three spatial dims, input
+# with two more dims, one stride / pad / dilation per spatial dim.  The 3-D ops below take
+# x (N,C,D,H,W), w (K,C/groups,T,R,S), y / dy (N,K,Z,P,Q); groups split the channels as in
+# the 2-D ops.  The per-element definitions are in conv3d_oracle.c.
+
+def _triple(v):
+    return (v, v, v) if isinstance(v, int) else tuple(v)
+
+
+def output_dim_dilated(inp: int, pad: int, k: int, stride: int, dil: int) -> int:
+    """Output extent along one dim for a filter of k taps dilated by dil (extent dil*(k-1)+1)."""
+    return output_dim(inp, pad, dil * (k - 1) + 1, stride)
+
+
+def _dims3(N, C, DHW, K, TRS, pad, stride, dilation):
+    pads, strides, dils = _triple(pad), _triple(stride), _triple(dilation)
+    out = [output_dim_dilated(i, p_, k, s_, d_) for i, p_, k, s_, d_ in zip(DHW, pads, TRS, strides, dils)]
+    dims = [N, C, *DHW, K, *TRS, *pads, *strides, *dils, *out]
+    return np.ascontiguousarray(np.asarray(dims, dtype=np.int32)), tuple(out)
+
+
+def _iptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_int))
+
+
+def conv3d_fwd(x, w, pad=0, stride=1, dilation=1, groups=1) -> np.ndarray:
+    """y (N,K,Z,P,Q) = cross-correlation of zero-padded x (N,C,D,H,W) with w (K,C/groups,T,R,S)."""
+    x, w = _f64(x), _f64(w)
+    N, C = x.shape[:2]
+    K, Cg = w.shape[:2]
+    assert C == Cg * groups and K % groups == 0, "channel / group mismatch"
+    Kg = K // groups
+    parts = []
+    for g in range(groups):
+        xs = np.ascontiguousarray(x[:, g * Cg:(g + 1) * Cg])
+        ws = np.ascontiguousarray(w[g * Kg:(g + 1) * Kg])
+        dims, (Z, P, Q) = _dims3(N, Cg, x.shape[2:], Kg, w.shape[2:], pad, stride, dilation)
+        y = np.empty((N, Kg, Z, P, Q), dtype=np.float64)
+        _load().oracle_conv3d_fwd(_ptr(xs), _ptr(ws), _ptr(y), _iptr(dims))
+        parts.append(y)
+    return np.concatenate(parts, axis=1)
+
+
+def conv3d_bwd_data(dy, w, x_dhw, pad=0, stride=1, dilation=1, groups=1) -> np.ndarray:
+    """dx (N,C,D,H,W) from dy (N,K,Z,P,Q) and w (K,C/groups,T,R,S); x_dhw = (D, H, W)."""
+    dy, w = _f64(dy), _f64(w)
+    N, K = dy.shape[:2]
+    K2, Cg = w.shape[:2]
+    assert K == K2 and K % groups == 0
+    Kg = K // groups
+    parts = []
+    for g in range(groups):
+        dys = np.ascontiguousarray(dy[:, g * Kg:(g + 1) * Kg])
+        ws = np.ascontiguousarray(w[g * Kg:(g + 1) * Kg])
+        dims, out = _dims3(N, Cg, tuple(x_dhw), Kg, w.shape[2:], pad, stride, dilation)
+        assert out == tuple(dy.shape[2:]), "Z/P/Q mismatch"
+        dx = np.empty((N, Cg, *x_dhw), dtype=np.float64)
+        _load().oracle_conv3d_bwd_data(_ptr(dys), _ptr(ws), _ptr(dx), _iptr(dims))
+        parts.append(dx)
+    return np.concatenate(parts, axis=1)
+
+
+def conv3d_bwd_filter(x, dy, trs, pad=0, stride=1, dilation=1, groups=1) -> np.ndarray:
+    """dw (K,C/groups,T,R,S) from x (N,C,D,H,W) and dy (N,K,Z,P,Q); trs = (T, R, S)."""
+    x, dy = _f64(x), _f64(dy)
+    N, C = x.shape[:2]
+    N2, K = dy.shape[:2]
+    assert N == N2 and C % groups == 0 and K % groups == 0
+    Cg, Kg = C // groups, K // groups
+    parts = []
+    for g in range(groups):
+        xs = np.ascontiguousarray(x[:, g * Cg:(g + 1) * Cg])
+        dys = np.ascontiguousarray(dy[:, g * Kg:(g + 1) * Kg])
+        dims, out = _dims3(N, Cg, x.shape[2:], Kg, tuple(trs), pad, stride, dilation)
+        assert out == tuple(dy.shape[2:]), "Z/P/Q mismatch"
+        dw = np.empty((Kg, Cg, *trs), dtype=np.float64)
+        _load().oracle_conv3d_bwd_filter(_ptr(xs), _ptr(dys), _ptr(dw), _iptr(dims))
+        parts.append(dw)
+    return np.concatenate(parts, axis=0)
 
 
 def num_threads() -> int:
