@@ -8,7 +8,7 @@ Each op is timed with CUDA events on the launching stream; L2 is flushed (a writ
 twice the L2 size) before every op, outside the events.  FLOP per op = 2*N*K*P*Q*C*R*S.
 
 Prints ONE JSON line (rank 0).  --impl reference times the fp64 CPU oracle on a bounded
-sample of the same workload instead (the reference arm of this build).
+sample of the same workload instead (the slow, plainly correct reference arm).
 Multi-GPU (torchrun, one rank per GPU): the path is run as independent replicas, one per
 rank, no collective on the data path; value = all ranks' FLOP / max rank time.
 """
