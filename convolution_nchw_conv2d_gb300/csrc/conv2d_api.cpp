@@ -268,8 +268,11 @@ void order_phase_taps(std::vector<int>& pl, std::vector<int>& off, std::vector<i
   }
 }
 
+// Taps u = r*S + s in [u_lo, u_hi) only (the whole filter by default).  A partial tap set
+// moves the staged window down by its smallest tap row (plane offsets up, tap offsets
+// down by the same rows), so that the window holds no rows that none of its taps reads.
 int build_fwd(const Desc& d0, const void* x, const void* w, void* y, void* ws, const DevInfo& di,
-              TapBuild& b) {
+              TapBuild& b, int u_lo = 0, int u_hi = 1 << 30) {
   const Desc d = flatten_pointwise(d0);
   TapPlan& p = b.p;
   std::memset(&p, 0, sizeof(p));
@@ -305,16 +308,24 @@ int build_fwd(const Desc& d0, const void* x, const void* w, void* y, void* ws, c
   p.ph_step_w = 1;
   const bool pair = d.C <= CHUNK;
   std::vector<int> tpl, toff, tr, ts;
-  int max_off = 0;
+  int min_row = 1 << 30;
   for (int r = 0; r < d.R; ++r)
     for (int s = 0; s < d.S; ++s) {
+      if (r * d.S + s < u_lo || r * d.S + s >= u_hi) continue;
       const int re = r * d.dh, se = s * d.dw;  // the tap's place in the dilated window
       tpl.push_back((re % d.sh) * d.sw + (se % d.sw));
       toff.push_back((re / d.sh) * p.WL + se / d.sw);
       tr.push_back(r);
       ts.push_back(s);
-      max_off = std::max(max_off, toff.back());
+      min_row = std::min(min_row, re / d.sh);
     }
+  if (tpl.empty()) return CONV2D_ERR_BAD_DESC;
+  int max_off = 0;
+  for (int& o : toff) {
+    o -= min_row * p.WL;
+    max_off = std::max(max_off, o);
+  }
+  for (int pl = 0; pl < p.npl; ++pl) p.pl_off_h[pl] += min_row * d.sh;
   order_phase_taps(tpl, toff, tr, ts, 0, 1 << 20, pair);
   p.ntaps_total = (int)tpl.size();
   if (p.ntaps_total > kMaxTaps) return CONV2D_ERR_UNSUPPORTED;
@@ -332,8 +343,10 @@ int build_fwd(const Desc& d0, const void* x, const void* w, void* y, void* ws, c
   return CONV2D_OK;
 }
 
+// Taps u = r*S + s in [u_lo, u_hi) only, with the staged window moved down by the
+// smallest tap row as in build_fwd.
 int build_bwd_data(const Desc& d0, const void* dy, const void* w, void* dx, void* ws, const DevInfo& di,
-                   TapBuild& b) {
+                   TapBuild& b, int u_lo = 0, int u_hi = 1 << 30) {
   const Desc d = flatten_pointwise(d0);
   TapPlan& p = b.p;
   std::memset(&p, 0, sizeof(p));
@@ -404,7 +417,20 @@ int build_bwd_data(const Desc& d0, const void* dy, const void* w, void* dx, void
   p.ph_step_w = d.sw;
   const bool pair = d.K <= CHUNK;
   std::vector<int> tpl, toff, tr, ts;
-  int max_off = 0, max_taps = 0;
+  int max_taps = 0, min_row = 1 << 30, n_real = 0;
+  for (int a = 0; a < d.sh; ++a)
+    for (int c = 0; c < d.sw; ++c)
+      for (const int r : tapsh[a])
+        for (const int s2 : tapsw[c])
+          if (r * d.S + s2 >= u_lo && r * d.S + s2 < u_hi) {
+            min_row = std::min(min_row, uloh[a] - (r * d.dh - a) / d.sh + T0h);
+            ++n_real;
+          }
+  if (n_real == 0) {
+    if (u_lo > 0 || u_hi < d.R * d.S) return CONV2D_ERR_BAD_DESC;
+    min_row = 0;  // no tap reaches any output: the plan writes zeros
+  }
+  p.pl_off_h[0] += min_row;
   for (int a = 0; a < d.sh; ++a)
     for (int c = 0; c < d.sw; ++c) {
       const int ph = a * d.sw + c;
@@ -414,19 +440,21 @@ int build_bwd_data(const Desc& d0, const void* dy, const void* w, void* dx, void
       p.ph_tap_begin[ph] = begin;
       for (const int r : tapsh[a])
         for (const int s2 : tapsw[c]) {
+          if (r * d.S + s2 < u_lo || r * d.S + s2 >= u_hi) continue;
           const int t = (r * d.dh - a) / d.sh, t2 = (s2 * d.dw - c) / d.sw;
-          const int roff = uloh[a] - t + T0h;
+          const int roff = uloh[a] - t + T0h - min_row;
           const int coff = ulow[c] - t2 + T0w;
           tpl.push_back(0);
           toff.push_back(roff * WL + coff);
           tr.push_back(r);
           ts.push_back(s2);
-          max_off = std::max(max_off, toff.back());
         }
       if ((int)tpl.size() > begin) order_phase_taps(tpl, toff, tr, ts, begin, 1 << 20, pair);
       p.ph_ntaps[ph] = (int)tpl.size() - begin;
       max_taps = std::max(max_taps, p.ph_ntaps[ph]);
     }
+  int max_off = 0;
+  for (const int o : toff) max_off = std::max(max_off, o);
   p.ntaps_total = (int)tpl.size();
   if (p.ntaps_total > kMaxTaps) return CONV2D_ERR_UNSUPPORTED;
   p.max_taps_ph = std::max(1, max_taps);
@@ -800,6 +828,45 @@ bool same_key(const PlanKey& a, const PlanKey& b) {
          a.ptr[1] == b.ptr[1] && a.ptr[2] == b.ptr[2] && a.ptr[3] == b.ptr[3];
 }
 
+// Forward / backward-data as one or more tap-GEMM passes.  The tap GEMM stages, per k-block,
+// the filter slices of every tap of a phase; when that does not fit twice in shared memory
+// (large filters over many source channels) the taps u = r*S + s are split into contiguous
+// ranges, one pass each: the first pass applies the caller's bias and beta, the later ones
+// add onto the output (beta = 1).  Each pass has its own repacked filter in the workspace.
+constexpr int kMaxTapPasses = 16;
+
+struct TapSet {
+  std::vector<TapBuild> pass;
+  size_t pack_bytes = 0;  // workspace for all passes' repacked filters
+};
+
+int build_tap_set(int op, const Desc& d, const void* src, const void* w, void* dst, void* ws, const DevInfo& di,
+                  TapSet& out) {
+  const int RS = d.R * d.S;
+  for (int n = 1; n <= std::min(RS, kMaxTapPasses); ++n) {
+    TapSet set;
+    size_t off = 0;
+    int rc = CONV2D_OK;
+    for (int i = 0; i < n; ++i) {
+      const int lo = (int)((long long)RS * i / n), hi = (int)((long long)RS * (i + 1) / n);
+      void* wsi = ws != nullptr ? static_cast<void*>(static_cast<uint8_t*>(ws) + off) : nullptr;
+      TapBuild b;
+      rc = op == CONV2D_OP_FWD ? build_fwd(d, src, w, dst, wsi, di, b, n == 1 ? 0 : lo, n == 1 ? 1 << 30 : hi)
+                               : build_bwd_data(d, src, w, dst, wsi, di, b, n == 1 ? 0 : lo, n == 1 ? 1 << 30 : hi);
+      if (rc != CONV2D_OK) break;
+      off += i + 1 < n ? align_ws(b.pack_bytes) : b.pack_bytes;
+      set.pass.push_back(b);
+    }
+    if (rc == CONV2D_OK) {
+      set.pack_bytes = off;
+      out = std::move(set);
+      return CONV2D_OK;
+    }
+    if (rc != CONV2D_ERR_UNSUPPORTED) return rc;
+  }
+  return CONV2D_ERR_UNSUPPORTED;
+}
+
 template <class Build>
 struct PlanCache {
   static constexpr int kEntries = 16;
@@ -825,7 +892,7 @@ struct PlanCache {
   }
 };
 
-PlanCache<TapBuild> g_tap_plans;
+PlanCache<TapSet> g_tap_plans;
 PlanCache<WgradBuild> g_wgrad_plans;
 PlanCache<size_t> g_ws_sizes;
 
@@ -886,11 +953,10 @@ int workspace_size_uncached(int op, const Desc& d, size_t* bytes) {
   int rc;
   const DevInfo di = device_info();
   if (op == CONV2D_OP_FWD || op == CONV2D_OP_BWD_DATA) {
-    TapBuild b;
-    rc = op == CONV2D_OP_FWD ? build_fwd(d, nullptr, nullptr, nullptr, nullptr, di, b)
-                             : build_bwd_data(d, nullptr, nullptr, nullptr, nullptr, di, b);
+    TapSet set;
+    rc = build_tap_set(op, d, nullptr, nullptr, nullptr, nullptr, di, set);
     if (rc) return rc;
-    *bytes = b.pack_bytes;
+    *bytes = set.pack_bytes;
     return CONV2D_OK;
   }
   if (op == CONV2D_OP_BWD_FILTER) {
@@ -915,10 +981,10 @@ int workspace_size_uncached(int op, const Desc& d, size_t* bytes) {
 extern "C" {
 
 
-// Forward / backward-data: the plan is made once per descriptor (cached with the group-0
-// addresses) and each group runs it with its own tensor slices: source, destination and
-// bias channels of the group, the group's filter rows; the repacked filter reuses the
-// workspace group after group (stream order).
+// Forward / backward-data: the plan (one or more tap passes) is made once per descriptor
+// (cached with the group-0 addresses) and each group runs it with its own tensor slices:
+// source, destination and bias channels of the group, the group's filter rows; the
+// repacked filters reuse the workspace group after group (stream order).
 static int run_tap(int op, const Desc& d, int groups, const void* src, const void* w, const void* bias, float beta,
                    int mode, void* dst, void* ws, size_t wsb, void* stream) {
   if (mode != CONV2D_MODE_CROSS_CORRELATION && mode != CONV2D_MODE_CONVOLUTION) return CONV2D_ERR_BAD_DESC;
@@ -931,18 +997,16 @@ static int run_tap(int op, const Desc& d, int groups, const void* src, const voi
   if (rc) return rc;
   const DevInfo di = device_info();
   if (!di.ok) return CONV2D_ERR_DEVICE;
-  TapBuild b;
+  TapSet set;
   const PlanKey key = make_key(op, dg, src, w, dst, ws);
-  if (!g_tap_plans.get(key, b)) {
-    rc = op == CONV2D_OP_FWD ? build_fwd(dg, src, w, dst, ws, di, b) : build_bwd_data(dg, src, w, dst, ws, di, b);
+  if (!g_tap_plans.get(key, set)) {
+    rc = build_tap_set(op, dg, src, w, dst, ws, di, set);
     if (rc) return rc;
-    g_tap_plans.put(key, b);
+    g_tap_plans.put(key, set);
   }
-  rc = check_ws(ws, wsb, b.pack_bytes);
+  rc = check_ws(ws, wsb, set.pack_bytes);
   if (rc) return rc;
   if (bias != nullptr && ((uintptr_t)bias & (d.dt == CONV2D_DTYPE_F32 ? 3 : 1))) return CONV2D_ERR_ALIGN;
-  b.p.beta = beta;  // per-call epilogue inputs and mode (not part of the cached plan)
-  b.pp.flip = mode == CONV2D_MODE_CONVOLUTION ? 1 : 0;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const size_t esz = d.dt == CONV2D_DTYPE_F32 ? 4 : 2;
   const bool fwd = op == CONV2D_OP_FWD;
@@ -951,18 +1015,23 @@ static int run_tap(int op, const Desc& d, int groups, const void* src, const voi
   const size_t dst_g = fwd ? (size_t)dg.K * dg.P * dg.Q : (size_t)dg.C * dg.H * dg.W;
   const size_t w_g = (size_t)dg.K * dg.C * dg.R * dg.S;
   const size_t bias_g = fwd ? (size_t)dg.K : (size_t)dg.C;
-  for (int gi = 0; gi < groups; ++gi) {
-    b.p.src = byte_ptr(src) + gi * src_g * esz;
-    b.p.dst = const_cast<uint8_t*>(byte_ptr(dst)) + gi * dst_g * esz;
-    b.pp.w = byte_ptr(w) + gi * w_g * esz;
-    b.p.bias = bias != nullptr ? byte_ptr(bias) + gi * bias_g * esz : nullptr;
-    if (b.pack_bytes) {
-      rc = launch_err(launch_pack_filter(b.pp, d.dt, st));
+  for (int gi = 0; gi < groups; ++gi)
+    for (size_t pi = 0; pi < set.pass.size(); ++pi) {
+      TapBuild& b = set.pass[pi];
+      // per-call epilogue inputs and mode (not part of the cached plan); later passes add on
+      b.p.beta = pi == 0 ? beta : 1.f;
+      b.pp.flip = mode == CONV2D_MODE_CONVOLUTION ? 1 : 0;
+      b.p.src = byte_ptr(src) + gi * src_g * esz;
+      b.p.dst = const_cast<uint8_t*>(byte_ptr(dst)) + gi * dst_g * esz;
+      b.pp.w = byte_ptr(w) + gi * w_g * esz;
+      b.p.bias = bias != nullptr && pi == 0 ? byte_ptr(bias) + gi * bias_g * esz : nullptr;
+      if (b.pack_bytes) {
+        rc = launch_err(launch_pack_filter(b.pp, d.dt, st));
+        if (rc) return rc;
+      }
+      rc = launch_err(launch_tap_gemm(b.p, d.dt, b.grid, st));
       if (rc) return rc;
     }
-    rc = launch_err(launch_tap_gemm(b.p, d.dt, b.grid, st));
-    if (rc) return rc;
-  }
   return CONV2D_OK;
 }
 

@@ -45,6 +45,10 @@
  *     size never exceeds 1e9 bytes (the workspace cap of the SystemDS wrapper,
  *     MAX_WORKSPACE_LIMIT_BYTES).  Forward and backward-data stage a repacked copy of
  *     the filter there; backward-filter stages split partial sums.
+ *   - Forward and backward-data with large filters over many source channels (about
+ *     13 x 13 taps and more) run as several passes over contiguous ranges of the taps
+ *     r*S + s, each adding onto the output the previous one wrote; with bf16 tensors
+ *     the output is then rounded to bf16 once per pass.
  *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls only enqueue
  *     work on it and return; the library allocates no device memory, keeps no
  *     pointer after returning and holds no per-call state.  Results are
@@ -99,7 +103,8 @@ enum {
     CONV2D_ERR_LAUNCH = -8,         /* the CUDA runtime rejected a launch */
     CONV2D_ERR_DEVICE = -9,         /* no usable sm_100-family device */
     CONV2D_ERR_DEVICE_TIMEOUT = -10,/* a kernel's bounded internal wait expired */
-    CONV2D_ERR_UNSUPPORTED = -11,   /* R*S > 256, stride_h*stride_w > 16, or no tile fits */
+    CONV2D_ERR_UNSUPPORTED = -11,   /* R*S > 256, stride_h*stride_w > 16, or no tile fits
+                                       even with the taps split over 16 passes */
     CONV2D_ERR_BAD_OP = -12,        /* unknown op in conv2d_workspace_size() */
     CONV2D_ERR_NOALLOC_LIMIT = -13  /* conv2d_fwd_noalloc: problem exceeds its fixed scratch */
 };

@@ -1,7 +1,9 @@
 // Host-only check of the launch planner (no GPU): plans the three ops for a list of shapes
 // and verifies the invariants the kernels rely on -- shared-memory and TMEM budgets, staged
-// rows covering every tap offset, ring sizes covering the positions in flight, bank-spread
-// ring pitches, and that every (channel, tap) of the filter gradient is produced exactly once.
+// rows covering every tap offset, every forward / backward-data tap reading the pixel the
+// definition names (also across the passes of large filters), ring sizes covering the
+// positions in flight, bank-spread ring pitches, and that every (channel, tap) of the
+// filter gradient is produced exactly once.
 // Tensor maps are not encoded (a stand-in encoder accepts every map), so the copy-engine
 // plans are checked as they would be planned for aligned tensors.  Prints one line per
 // violation and exits with the number of violations (capped at 100).
@@ -38,7 +40,7 @@ struct Shape {
   const char* nm;
   int N, C, H, W, K, R, S, ph, pw, sh, sw, dt;
   int dh, dw, g;
-  int refused;  // bit 0 forward, bit 1 backward-data: expected CONV2D_ERR_UNSUPPORTED
+  int passes[2];  // tap passes expected for forward and backward-data
 };
 
 void check_tap(const char* nm, const char* op, const TapBuild& b, const DevInfo& di) {
@@ -51,6 +53,41 @@ void check_tap(const char* nm, const char* op, const TapBuild& b, const DevInfo&
       if (p.tap_off[t] < 0 || p.tap_off[t] + 128 * p.MH > p.rows) fail(nm, op, "tap offset beyond the staged rows");
   if (p.NT % 16 || p.NT > 256 || (p.MH != 1 && p.MH != 2)) fail(nm, op, "tile shape");
   if (p.Mtot >= (1ll << 31)) fail(nm, op, "position space too large");
+}
+
+// Every real tap of every pass reads, for each output, the source pixel the definition
+// names: forward row (p*sh - ph + r*dh), column (q*sw - pw + s*dw); backward-data dy row
+// (h + ph - r*dh) / sh, column (w + pw - s*dw) / sw.  In the plan an output at linear
+// (e, f) reads linear (e + roff, f + coff) of its plane, roff / coff being the tap offset
+// split by the row width; planes and phases add their own offsets.  Every (r, s) must be
+// a real tap of exactly one pass.
+void check_tap_semantics(const char* nm, const char* op, const Desc& d, const TapSet& set, bool fwd) {
+  std::vector<int> seen((size_t)d.R * d.S, 0);
+  for (const TapBuild& b : set.pass) {
+    const TapPlan& p = b.p;
+    for (int ph = 0; ph < p.nph; ++ph)
+      for (int t = p.ph_tap_begin[ph]; t < p.ph_tap_begin[ph] + p.ph_ntaps[ph]; ++t) {
+        const int r = b.pp.tap_r[t], s = b.pp.tap_s[t];
+        if (r < 0) continue;  // zero-weight tap that pads a phase to an even count
+        ++seen[(size_t)r * d.S + s];
+        const int roff = p.tap_off[t] / p.WL, coff = p.tap_off[t] % p.WL;
+        if (fwd) {
+          const int pl = p.tap_plane[t];
+          if (roff * d.sh + p.pl_off_h[pl] != r * d.dh - d.ph || coff * d.sw + p.pl_off_w[pl] != s * d.dw - d.pw)
+            fail(nm, op, "a tap reads the wrong source pixel");
+        } else {
+          const int nh = p.ph_off_h[ph] + d.ph - r * d.dh, nw = p.ph_off_w[ph] + d.pw - s * d.dw;
+          if (nh % d.sh != 0 || nw % d.sw != 0 || roff + p.pl_off_h[0] != nh / d.sh ||
+              coff + p.pl_off_w[0] != nw / d.sw)
+            fail(nm, op, "a tap reads the wrong dy pixel");
+        }
+      }
+  }
+  for (size_t i = 0; i < seen.size(); ++i)
+    if (seen[i] != 1) {
+      fail(nm, op, "a filter tap is not in exactly one pass");
+      break;
+    }
 }
 
 void check_wgrad(const char* nm, const Desc& d, const WgradBuild& b, const DevInfo& di) {
@@ -116,43 +153,46 @@ void check_wgrad(const char* nm, const Desc& d, const WgradBuild& b, const DevIn
 
 int main() {
   using namespace cg3;
-  // The last field marks the refusals the planner is expected to make.  The tap GEMM stages
-  // the filter slices of every tap of a phase for each k-block; with a stride-1 15x15 filter
-  // and more than 4 fp32 (8 bf16) source channels that is 225 taps x 2 chunks x 16 columns
-  // x 16 bytes = 115 KB a stage, so two stages do not fit in shared memory and the call
-  // returns CONV2D_ERR_UNSUPPORTED.  With at most 4 (8) source channels two taps share one
-  // MMA and the slices halve.  The source channels are C forward and K backward-data.
+  // The last field gives the tap passes expected for forward and backward-data.  The tap GEMM
+  // stages the filter slices of every tap of a phase for each k-block; with a stride-1 15x15
+  // filter and more than 4 fp32 (8 bf16) source channels that is 225 taps x 2 chunks x 16
+  // columns x 16 bytes = 115 KB a stage, so two stages do not fit in shared memory and the
+  // taps are split over passes.  With at most 4 (8) source channels two taps share one MMA
+  // and the slices halve.  The source channels are C forward and K backward-data.
   std::vector<Shape> shapes = {
-      {"tiny", 2, 3, 8, 8, 4, 3, 3, 1, 1, 1, 1, 0, 1, 1, 1, 0},
-      {"resnet3x3", 32, 64, 56, 56, 64, 3, 3, 1, 1, 1, 1, 0, 1, 1, 1, 0},
-      {"resnet3x3_bf16", 32, 64, 56, 56, 64, 3, 3, 1, 1, 1, 1, 1, 1, 1, 1, 0},
-      {"strided", 64, 128, 56, 56, 256, 3, 3, 1, 1, 2, 2, 0, 1, 1, 1, 0},
-      {"pointwise", 128, 256, 14, 14, 1024, 1, 1, 0, 0, 1, 1, 0, 1, 1, 1, 0},
-      {"stem7x7", 64, 3, 224, 224, 64, 7, 7, 3, 3, 2, 2, 0, 1, 1, 1, 0},
-      {"deconv", 32, 256, 32, 32, 512, 4, 4, 1, 1, 2, 2, 1, 1, 1, 1, 0},
-      {"c33", 3, 33, 9, 11, 40, 3, 3, 1, 1, 1, 1, 0, 1, 1, 1, 0},
-      {"k300", 1, 17, 6, 6, 300, 3, 3, 1, 1, 1, 1, 0, 1, 1, 1, 0},
-      {"c300", 2, 300, 5, 5, 20, 3, 3, 1, 1, 1, 1, 1, 1, 1, 1, 0},
-      {"c5k300", 2, 5, 17, 13, 300, 5, 3, 2, 1, 2, 1, 1, 1, 1, 1, 0},
-      {"r15", 1, 4, 40, 40, 8, 15, 15, 7, 7, 1, 1, 0, 1, 1, 1, 2},
-      {"r15_k4", 1, 8, 40, 40, 4, 15, 15, 7, 7, 1, 1, 0, 1, 1, 1, 1},
-      {"s32", 2, 40, 23, 19, 24, 3, 3, 1, 1, 3, 2, 1, 1, 1, 1, 0},
-      {"hr", 1, 2, 6, 13, 2, 6, 13, 0, 0, 1, 1, 0, 1, 1, 1, 0},
-      {"rows5", 1, 40, 16, 16, 48, 5, 3, 2, 1, 1, 1, 0, 1, 1, 1, 0},
-      {"rows5_bf16", 1, 40, 16, 16, 48, 5, 3, 2, 1, 1, 1, 1, 1, 1, 1, 0},
-      {"wide_k", 1, 32, 8, 8, 150, 3, 3, 1, 1, 1, 1, 0, 1, 1, 1, 0},
-      {"wide_k_bf16", 1, 32, 8, 8, 150, 3, 3, 1, 1, 1, 1, 1, 1, 1, 1, 0},
-      {"rect", 2, 48, 10, 16, 20, 3, 5, 1, 2, 1, 1, 0, 1, 1, 1, 0},
-      {"big7", 8, 64, 32, 32, 64, 7, 7, 3, 3, 1, 1, 0, 1, 1, 1, 0},
-      {"dil2", 2, 64, 16, 16, 64, 3, 3, 2, 2, 1, 1, 0, 2, 2, 1, 0},
-      {"dil2_bf16", 2, 64, 16, 16, 64, 3, 3, 2, 2, 1, 1, 1, 2, 2, 1, 0},
-      {"dil23", 1, 5, 20, 17, 7, 3, 2, 2, 1, 2, 1, 1, 2, 3, 1, 0},
-      {"dil32", 1, 33, 15, 16, 40, 2, 3, 1, 2, 1, 2, 0, 3, 2, 1, 0},
-      {"dil3_s2", 2, 3, 21, 21, 16, 3, 3, 3, 3, 2, 2, 1, 3, 3, 1, 0},
-      {"grp3", 2, 6, 9, 10, 9, 3, 3, 1, 1, 1, 1, 0, 1, 1, 3, 0},
-      {"grp2", 2, 64, 16, 16, 64, 3, 3, 1, 1, 1, 1, 0, 1, 1, 2, 0},
-      {"depthwise", 1, 16, 12, 12, 16, 3, 3, 1, 1, 1, 1, 1, 1, 1, 16, 0},
-      {"grp_dil", 2, 8, 13, 11, 6, 3, 3, 2, 2, 1, 2, 0, 2, 1, 2, 0},
+      {"tiny", 2, 3, 8, 8, 4, 3, 3, 1, 1, 1, 1, 0, 1, 1, 1, {1, 1}},
+      {"resnet3x3", 32, 64, 56, 56, 64, 3, 3, 1, 1, 1, 1, 0, 1, 1, 1, {1, 1}},
+      {"resnet3x3_bf16", 32, 64, 56, 56, 64, 3, 3, 1, 1, 1, 1, 1, 1, 1, 1, {1, 1}},
+      {"strided", 64, 128, 56, 56, 256, 3, 3, 1, 1, 2, 2, 0, 1, 1, 1, {1, 1}},
+      {"pointwise", 128, 256, 14, 14, 1024, 1, 1, 0, 0, 1, 1, 0, 1, 1, 1, {1, 1}},
+      {"stem7x7", 64, 3, 224, 224, 64, 7, 7, 3, 3, 2, 2, 0, 1, 1, 1, {1, 1}},
+      {"deconv", 32, 256, 32, 32, 512, 4, 4, 1, 1, 2, 2, 1, 1, 1, 1, {1, 1}},
+      {"c33", 3, 33, 9, 11, 40, 3, 3, 1, 1, 1, 1, 0, 1, 1, 1, {1, 1}},
+      {"k300", 1, 17, 6, 6, 300, 3, 3, 1, 1, 1, 1, 0, 1, 1, 1, {1, 1}},
+      {"c300", 2, 300, 5, 5, 20, 3, 3, 1, 1, 1, 1, 1, 1, 1, 1, {1, 1}},
+      {"c5k300", 2, 5, 17, 13, 300, 5, 3, 2, 1, 2, 1, 1, 1, 1, 1, {1, 1}},
+      {"r15", 1, 4, 40, 40, 8, 15, 15, 7, 7, 1, 1, 0, 1, 1, 1, {1, 2}},
+      {"r15_k4", 1, 8, 40, 40, 4, 15, 15, 7, 7, 1, 1, 0, 1, 1, 1, {2, 1}},
+      {"r16_c16", 1, 16, 40, 40, 16, 16, 16, 7, 7, 1, 1, 0, 1, 1, 1, {2, 2}},
+      {"r16_s2_bf16", 2, 24, 40, 40, 20, 16, 16, 7, 7, 2, 2, 1, 1, 1, 1, {4, 1}},
+      {"r1_s256", 1, 16, 4, 300, 16, 1, 256, 0, 3, 1, 1, 0, 1, 1, 1, {2, 2}},
+      {"s32", 2, 40, 23, 19, 24, 3, 3, 1, 1, 3, 2, 1, 1, 1, 1, {1, 1}},
+      {"hr", 1, 2, 6, 13, 2, 6, 13, 0, 0, 1, 1, 0, 1, 1, 1, {1, 1}},
+      {"rows5", 1, 40, 16, 16, 48, 5, 3, 2, 1, 1, 1, 0, 1, 1, 1, {1, 1}},
+      {"rows5_bf16", 1, 40, 16, 16, 48, 5, 3, 2, 1, 1, 1, 1, 1, 1, 1, {1, 1}},
+      {"wide_k", 1, 32, 8, 8, 150, 3, 3, 1, 1, 1, 1, 0, 1, 1, 1, {1, 1}},
+      {"wide_k_bf16", 1, 32, 8, 8, 150, 3, 3, 1, 1, 1, 1, 1, 1, 1, 1, {1, 1}},
+      {"rect", 2, 48, 10, 16, 20, 3, 5, 1, 2, 1, 1, 0, 1, 1, 1, {1, 1}},
+      {"big7", 8, 64, 32, 32, 64, 7, 7, 3, 3, 1, 1, 0, 1, 1, 1, {1, 1}},
+      {"dil2", 2, 64, 16, 16, 64, 3, 3, 2, 2, 1, 1, 0, 2, 2, 1, {1, 1}},
+      {"dil2_bf16", 2, 64, 16, 16, 64, 3, 3, 2, 2, 1, 1, 1, 2, 2, 1, {1, 1}},
+      {"dil23", 1, 5, 20, 17, 7, 3, 2, 2, 1, 2, 1, 1, 2, 3, 1, {1, 1}},
+      {"dil32", 1, 33, 15, 16, 40, 2, 3, 1, 2, 1, 2, 0, 3, 2, 1, {1, 1}},
+      {"dil3_s2", 2, 3, 21, 21, 16, 3, 3, 3, 3, 2, 2, 1, 3, 3, 1, {1, 1}},
+      {"grp3", 2, 6, 9, 10, 9, 3, 3, 1, 1, 1, 1, 0, 1, 1, 3, {1, 1}},
+      {"grp2", 2, 64, 16, 16, 64, 3, 3, 1, 1, 1, 1, 0, 1, 1, 2, {1, 1}},
+      {"depthwise", 1, 16, 12, 12, 16, 3, 3, 1, 1, 1, 1, 1, 1, 1, 16, {1, 1}},
+      {"grp_dil", 2, 8, 13, 11, 6, 3, 3, 2, 2, 1, 2, 0, 2, 1, 2, {1, 1}},
   };
   DevInfo di;
   di.sms = 152;
@@ -172,24 +212,24 @@ int main() {
     void* pw = (void*)0x200000;
     void* py = (void*)0x300000;
     void* ws = (void*)0x400000;
-    TapBuild bf, bd;
-    const int rcf = build_fwd(d, px, pw, py, ws, di, bf);
-    if (s.refused & 1) {
-      if (rcf != CONV2D_ERR_UNSUPPORTED) fail(s.nm, "fwd", "expected the documented refusal");
-    } else if (rcf != CONV2D_OK) {
-      fail(s.nm, "fwd", "no plan");
-    } else {
-      check_tap(s.nm, "fwd", bf, di);
-      ++plans;
-    }
-    const int rcd = build_bwd_data(d, py, pw, px, ws, di, bd);
-    if (s.refused & 2) {
-      if (rcd != CONV2D_ERR_UNSUPPORTED) fail(s.nm, "bwd_data", "expected the documented refusal");
-    } else if (rcd != CONV2D_OK) {
-      fail(s.nm, "bwd_data", "no plan");
-    } else {
-      check_tap(s.nm, "bwd_data", bd, di);
-      ++plans;
+    for (int op = 0; op < 2; ++op) {
+      const char* opn = op == 0 ? "fwd" : "bwd_data";
+      TapSet set;
+      const int rc = op == 0 ? build_tap_set(CONV2D_OP_FWD, d, px, pw, py, ws, di, set)
+                             : build_tap_set(CONV2D_OP_BWD_DATA, d, py, pw, px, ws, di, set);
+      if (rc != CONV2D_OK) {
+        fail(s.nm, opn, "no plan");
+        continue;
+      }
+      if ((int)set.pass.size() != s.passes[op]) {
+        std::printf("  %s %s: %d passes\n", s.nm, opn, (int)set.pass.size());
+        fail(s.nm, opn, "unexpected number of tap passes");
+      }
+      for (const TapBuild& b : set.pass) {
+        check_tap(s.nm, opn, b, di);
+        ++plans;
+      }
+      check_tap_semantics(s.nm, opn, d, set, op == 0);
     }
     for (const auto& v : kWgradVariants) {  // every staging variant the planner may fall back to
       WgradBuild bw;

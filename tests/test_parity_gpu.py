@@ -442,3 +442,43 @@ def test_groups_parity(cg, case, groups, dil, flip, dtype):
             den = float(np.linalg.norm(ref))
             rel = float(np.linalg.norm(got - ref)) / den if den > 0 else float(np.linalg.norm(got))
             assert rel <= 1e-2, f"{case}/g{groups}/{op}: {rel:.3e}"
+
+
+# Large filters whose filter slices do not fit the tap GEMM's shared memory in one pass: the
+# taps run in contiguous ranges, the first pass with the caller's bias and beta, the later
+# ones adding on.  The comment gives the passes the planner makes (forward, backward-data).
+PASS_CASES = [
+    ((1, 4, 40, 40, 8, 15, 15, 7, 7, 1, 1), "f32"),     # 1, 2
+    ((1, 8, 40, 40, 4, 15, 15, 7, 7, 1, 1), "f32"),     # 2, 1
+    ((1, 16, 40, 40, 16, 16, 16, 7, 7, 1, 1), "f32"),   # 2, 2
+    ((2, 24, 40, 40, 20, 16, 16, 7, 7, 2, 2), "bf16"),  # 4, 1
+    ((1, 16, 4, 300, 16, 1, 256, 0, 3, 1, 1), "f32"),   # 2, 2
+]
+
+
+@pytest.mark.parametrize("epi", [False, True])
+@pytest.mark.parametrize("case,dtype", PASS_CASES)
+def test_tap_passes_parity(cg, case, dtype, epi):
+    N, C, H, Wd, K, R, S, ph, pw, sh, sw = case
+    pb = W.Conv2dProblem(N, C, H, Wd, K, R, S, ph, pw, sh, sw, dtype)
+    seed = 9500 + 2 * PASS_CASES.index((case, dtype)) + int(epi)
+    x, w, dy = W.random_problem_inputs(pb, seed)
+    tdt = x.dtype
+    g = torch.Generator().manual_seed(seed)
+    bk = torch.randn(K, generator=g).to(tdt) if epi else None
+    bc = torch.randn(C, generator=g).to(tdt) if epi else None
+    y0 = torch.randn(pb.y_shape, generator=g).to(tdt)
+    dx0 = torch.randn(pb.x_shape, generator=g).to(tdt)
+    beta_f, beta_d = (1.0, 0.5) if epi else (0.0, 0.0)
+    pad, st = (ph, pw), (sh, sw)
+    xd, wd, dyd = x.to(DEV), w.to(DEV), dy.to(DEV)
+    amax = lambda t: float(t.abs().max())
+    y = y0.to(DEV) if epi else _poisoned(pb.y_shape, tdt)
+    cg.conv2d_fwd(xd, wd, pad, st, out=y, bias=bk.to(DEV) if epi else None, beta=beta_f)
+    dx = dx0.to(DEV) if epi else _poisoned(pb.x_shape, tdt)
+    cg.conv2d_bwd_data(dyd, wd, (H, Wd), pad, st, out=dx, bias=bc.to(DEV) if epi else None, beta=beta_d)
+    cg.conv2d_device_status()
+    _check_plain(pb, y.double().cpu().numpy(), oracle.conv2d_fwd_ex(x, w, bk, beta_f, y0, pad, st),
+                 amax(x) * amax(w), C * R * S, f"{case}/fwd/{dtype}/epi={epi}")
+    _check_plain(pb, dx.double().cpu().numpy(), oracle.conv2d_bwd_data_ex(dy, w, (H, Wd), bc, beta_d, dx0, pad, st),
+                 amax(dy) * amax(w), K * R * S, f"{case}/bwd_data/{dtype}/epi={epi}")

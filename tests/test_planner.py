@@ -1,8 +1,9 @@
 """Planner invariants on the host (no GPU): compiles tests/planner_check.cpp against the
 library's planner source and its built kernel objects (for the shared-memory size functions)
 and runs it; it plans the three ops for workloads, test shapes, dilated and grouped problems
-and checks the budgets, ring sizes, tap coverage and the exactly-once production of every
-(channel, tap) of the filter gradient."""
+and checks the budgets, ring sizes, tap coverage, that every tap of every forward and
+backward-data pass reads the source pixel the definition names, the pass counts of large
+filters, and the exactly-once production of every (channel, tap) of the filter gradient."""
 import os
 import shutil
 import subprocess
