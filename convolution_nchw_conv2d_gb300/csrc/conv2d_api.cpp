@@ -608,11 +608,14 @@ int build_bwd_filter_impl(const Desc& d0, const void* x, const void* dy, void* d
   }
   if (!tma && p.TRU > 1) return CONV2D_ERR_UNSUPPORTED;
   if (!tma) {
-    // Linear row width: a multiple of the chunk (16-byte dy copies) when that wastes at
-    // most 1/8 of it.
+    // Linear row width: a multiple of the chunk when that wastes at most 1/8 of it, or at
+    // most half of it when the output rows are whole chunks, since then it turns the dy
+    // staging from one copy per element into 16-byte copies, and the element copies, not
+    // the MMAs, pace these plans.
     p.delta = 0;
     const int wl = round_up(d.Q + mw, CHUNK);
-    p.WL = (8 * (wl - (d.Q + mw)) <= wl) ? wl : d.Q + mw;
+    const int waste = wl - (d.Q + mw);
+    p.WL = (8 * waste <= wl || (d.Q % CHUNK == 0 && 2 * waste <= wl)) ? wl : d.Q + mw;
     p.WLx = p.WL;
   }
   p.EL = d.P + mh;
