@@ -21,6 +21,7 @@ size_t tap_gemm_smem_bytes(const TapPlan& p);
 cudaError_t launch_wgrad(const WgradPlan& p, int dt, int grid, cudaStream_t st);
 cudaError_t launch_wgrad_reduce(const ReducePlan& rp, int dt, int num_sms, cudaStream_t st);
 cudaError_t launch_chan_sum(const ChanSumPlan& cp, int dt, cudaStream_t st);
+cudaError_t launch_space_to_depth(const S2dPlan& sp, int dt, cudaStream_t st);
 size_t wgrad_smem_bytes(const WgradPlan& p, int dt);
 int tap_gemm_take_error();
 int wgrad_take_error();
@@ -41,6 +42,7 @@ struct Desc {
   int dh = 1, dw = 1;  // dilation: filter tap (r, s) sits at (r*dh, s*dw) in the window
   int g = 1;           // groups this per-group descriptor belongs to: the tensors hold g*C
                        // input and g*K output channels (image strides), the filter K x C
+  int xg = 0;          // x image stride in units of C*H*W when not g (stride-phase planes)
 };
 
 int floor_div(int a, int b) { return a >= 0 ? a / b : -((-a + b - 1) / b); }
@@ -559,7 +561,7 @@ int build_bwd_filter_impl(const Desc& d0, const void* x, const void* dy, void* d
   std::memset(&p, 0, sizeof(p));
   p.x = x;
   p.dy = dy;
-  p.x_nstride = (long long)d.g * d.C * d.H * d.W;
+  p.x_nstride = (long long)(d.xg ? d.xg : d.g) * d.C * d.H * d.W;
   p.dy_nstride = (long long)d.g * d.K * d.P * d.Q;
   p.partial = static_cast<float*>(ws);
   p.N = d.N;
@@ -768,6 +770,10 @@ int build_bwd_filter_impl(const Desc& d0, const void* x, const void* dy, void* d
   rp.c_pad = d.C;
   rp.beta = 0.f;
   rp.flip = 0;
+  rp.R_out = d.R;
+  rp.S_out = d.S;
+  rp.r0 = rp.s0 = 0;
+  rp.rstep = rp.sstep = 1;
   b.grid = (int)std::min<long long>(p.total_tiles, di.sms);
   return CONV2D_OK;
 }
@@ -787,6 +793,86 @@ int build_bwd_filter(const Desc& d, const void* x, const void* dy, void* dw, voi
   }
   return rc;
 }
+
+// ---------------------------------------------------------------- strided backward-filter
+// With stride st > 1 the filter rows split by the residue rho of the input row they read:
+// row p*st - pad + r = st*(p + alpha) + rho.  Phase rho holds the taps r = r0 + st*r'
+// (r' < n) with (r - pad - rho) divisible by st; on the plane of input rows congruent to rho
+// they read plane row p - pad' + r', pad' = -(r0 - pad - rho) / st >= 0 (r0 < st).  Columns
+// likewise.  Every phase is a stride-1 problem over unit-stride planes, so x is copied once
+// into the planes (space to depth) and each phase runs the stride-1 backward-filter, whose
+// reduce places tap (r', s') at (r0 + sh*r', s0 + sw*s').  Every tap is in one phase, so the
+// phases' FLOP add up to the original.  Dilation 1 only.
+struct StridePhase {
+  int rho, r0, n, pad;
+};
+
+std::vector<StridePhase> stride_phases(int R, int pad, int st) {
+  std::vector<StridePhase> v;
+  for (int rho = 0; rho < st; ++rho) {
+    StridePhase f{rho, -1, 0, 0};
+    for (int r = 0; r < R; ++r)
+      if (((r - pad - rho) % st + st) % st == 0) {
+        if (f.n++ == 0) f.r0 = r;
+      }
+    if (f.n > 0) {
+      f.pad = -floor_div(f.r0 - pad - rho, st);
+      v.push_back(f);
+    }
+  }
+  return v;
+}
+
+size_t align_ws(size_t b);
+
+struct PhaseLayout {
+  bool on = false;
+  int Hp = 0, Wp = 0;    // plane extent (Wp a whole number of 16-byte chunks)
+  size_t xs_bytes = 0;   // planes of all channels (aligned)
+  std::vector<StridePhase> rows, cols;
+};
+
+// dg: the per-group descriptor; the planes hold all dg.g * dg.C channels.
+PhaseLayout phase_layout(const Desc& dg) {
+  PhaseLayout L;
+  if ((dg.sh == 1 && dg.sw == 1) || dg.dh != 1 || dg.dw != 1) return L;
+  const int CHUNK = dg.dt == 0 ? 4 : 8;
+  const size_t esz = dg.dt == 0 ? 4 : 2;
+  L.on = true;
+  L.Hp = ceil_div_i(dg.H, dg.sh);
+  L.Wp = round_up(ceil_div_i(dg.W, dg.sw), CHUNK);
+  L.xs_bytes = align_ws((size_t)dg.N * dg.sh * dg.sw * dg.g * dg.C * L.Hp * L.Wp * esz);
+  L.rows = stride_phases(dg.R, dg.ph, dg.sh);
+  L.cols = stride_phases(dg.S, dg.pw, dg.sw);
+  return L;
+}
+
+// The stride-1 descriptor of phase (a, b): planes as the input, the phase's taps and pads,
+// the caller's output extent (P, Q stay; they need not follow from the plane size).
+Desc phase_desc(const Desc& dg, const PhaseLayout& L, const StridePhase& a, const StridePhase& b) {
+  Desc q = dg;
+  q.H = L.Hp;
+  q.W = L.Wp;
+  q.R = a.n;
+  q.S = b.n;
+  q.ph = a.pad;
+  q.pw = b.pad;
+  q.sh = q.sw = 1;
+  q.xg = dg.g * dg.sh * dg.sw;
+  return q;
+}
+
+// Address of the plane of phase (a, b) for group gi within the planes buffer.
+const void* phase_plane(const void* xs, const Desc& dg, const PhaseLayout& L, const StridePhase& a,
+                        const StridePhase& b, int gi) {
+  const size_t esz = dg.dt == 0 ? 4 : 2;
+  const size_t pl = (size_t)a.rho * dg.sw + b.rho;
+  return byte_ptr(xs) + ((pl * dg.g + gi) * dg.C) * (size_t)L.Hp * L.Wp * esz;
+}
+
+// Plans every phase of group gi (cached); false if one of them has no plan.
+int plan_phases(const Desc& dg, const PhaseLayout& L, const void* xs, const void* dyg, void* dwg, void* partial_ws,
+                int gi, const DevInfo& di, std::vector<WgradBuild>& out);
 
 int check_ptrs(const void* a, const void* b, const void* c, int dt) {
   if (!a || !b || !c) return CONV2D_ERR_NULLPTR;
@@ -914,6 +1000,52 @@ PlanKey make_key(int op, const Desc& d, const void* a, const void* b, const void
   return k;
 }
 
+int plan_phases(const Desc& dg, const PhaseLayout& L, const void* xs, const void* dyg, void* dwg, void* partial_ws,
+                int gi, const DevInfo& di, std::vector<WgradBuild>& out) {
+  out.clear();
+  for (const StridePhase& a : L.rows)
+    for (const StridePhase& b : L.cols) {
+      const Desc q = phase_desc(dg, L, a, b);
+      const void* xq = xs != nullptr ? phase_plane(xs, dg, L, a, b, gi) : nullptr;
+      WgradBuild wb;
+      const PlanKey key = make_key(CONV2D_OP_BWD_FILTER, q, xq, dyg, dwg, partial_ws);
+      if (xs == nullptr || !g_wgrad_plans.get(key, wb)) {
+        const int rc = build_bwd_filter(q, xq, dyg, dwg, partial_ws, di, wb);
+        if (rc) return rc;
+        if (xs != nullptr) g_wgrad_plans.put(key, wb);
+      }
+      // the phase's taps in the caller's filter
+      wb.rp.R_out = dg.R;
+      wb.rp.S_out = dg.S;
+      wb.rp.r0 = a.r0;
+      wb.rp.s0 = b.r0;
+      wb.rp.rstep = dg.sh;
+      wb.rp.sstep = dg.sw;
+      out.push_back(wb);
+    }
+  return CONV2D_OK;
+}
+
+// Workspace of the phase path: the planes, then the largest phase's partials (the phases
+// reuse them in stream order), for whichever staging variant a phase ends up with.
+int phase_workspace(const Desc& dg, const PhaseLayout& L, const DevInfo& di, size_t& partial) {
+  partial = 0;
+  for (const StridePhase& a : L.rows)
+    for (const StridePhase& b : L.cols) {
+      const Desc q = phase_desc(dg, L, a, b);
+      WgradBuild wb;
+      const int rc = build_bwd_filter(q, nullptr, nullptr, nullptr, nullptr, di, wb);
+      if (rc) return rc;
+      partial = std::max(partial, wb.partial_bytes);
+      for (const auto& v : kWgradVariants) {
+        WgradBuild b2;
+        if (build_bwd_filter_impl(q, nullptr, nullptr, nullptr, nullptr, di, b2, v[0], v[1]) == CONV2D_OK)
+          partial = std::max(partial, b2.partial_bytes);
+      }
+    }
+  return CONV2D_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -963,18 +1095,25 @@ int workspace_size_uncached(int op, const Desc& d, size_t* bytes) {
     return CONV2D_OK;
   }
   if (op == CONV2D_OP_BWD_FILTER) {
+    // Strided filters run as stride phases when every phase plans (else as one problem);
+    // size for either.
+    size_t phased = 0;
+    const PhaseLayout L = phase_layout(d);
+    size_t partial = 0;
+    if (L.on && phase_workspace(d, L, di, partial) == CONV2D_OK)
+      phased = L.xs_bytes + align_ws(partial) + chan_sum_bytes(d);
     // The launch plans the copy-engine staging unless its tensor maps fail to encode for the
     // actual tensors; size for whichever of the two plans it ends up with.
     WgradBuild b;
     rc = build_bwd_filter(d, nullptr, nullptr, nullptr, nullptr, di, b);
-    if (rc) return rc;
+    if (rc) return phased ? (*bytes = phased, CONV2D_OK) : rc;
     size_t need = b.partial_bytes;
     for (const auto& v : kWgradVariants) {
       WgradBuild b2;
       if (build_bwd_filter_impl(d, nullptr, nullptr, nullptr, nullptr, di, b2, v[0], v[1]) == CONV2D_OK)
         need = std::max(need, b2.partial_bytes);
     }
-    *bytes = align_ws(need) + chan_sum_bytes(d);
+    *bytes = std::max(phased, align_ws(need) + chan_sum_bytes(d));
     return CONV2D_OK;
   }
   return CONV2D_ERR_BAD_OP;
@@ -1099,10 +1238,47 @@ int conv2d_bwd_filter_ex(int N, int C, int H, int W, int K, int R, int S, int pa
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const size_t esz = d.dt == CONV2D_DTYPE_F32 ? 4 : 2;
   size_t sum0 = 0;
+  bool phases_run = false;
+  // Strided filters: x into stride-phase planes once, then one stride-1 pass per phase and
+  // group (all planned before anything is enqueued; one problem if a phase has no plan).
+  const PhaseLayout L = phase_layout(dg);
+  if (L.on && workspace != nullptr) {
+    uint8_t* wsp = static_cast<uint8_t*>(workspace);
+    std::vector<std::vector<WgradBuild>> gp((size_t)groups);
+    size_t partial = 0;
+    bool phased = true;
+    for (int gi = 0; gi < groups && phased; ++gi) {
+      const void* dyg = byte_ptr(dy) + gi * (size_t)dg.K * dg.P * dg.Q * esz;
+      void* dwg = const_cast<uint8_t*>(byte_ptr(dw)) + gi * (size_t)dg.K * dg.C * dg.R * dg.S * esz;
+      rc = plan_phases(dg, L, wsp, dyg, dwg, wsp + L.xs_bytes, gi, di, gp[(size_t)gi]);
+      if (rc == CONV2D_ERR_UNSUPPORTED) phased = false;
+      else if (rc) return rc;
+      for (const WgradBuild& wb : gp[(size_t)gi]) partial = std::max(partial, wb.partial_bytes);
+    }
+    if (phased) {
+      rc = check_ws(workspace, workspace_bytes,
+                    L.xs_bytes + (sums ? align_ws(partial) + chan_sum_bytes(d) : partial));
+      if (rc) return rc;
+      const S2dPlan sp{x, wsp, d.N, d.C, d.H, d.W, d.sh, d.sw, L.Hp, L.Wp};
+      rc = launch_err(launch_space_to_depth(sp, d.dt, st));
+      if (rc) return rc;
+      for (auto& phases : gp)
+        for (WgradBuild& wb : phases) {
+          wb.rp.beta = beta;  // per-call (not part of the cached plan)
+          wb.rp.flip = mode == CONV2D_MODE_CONVOLUTION ? 1 : 0;
+          rc = launch_err(launch_wgrad(wb.p, d.dt, wb.grid, st));
+          if (rc) return rc;
+          rc = launch_err(launch_wgrad_reduce(wb.rp, d.dt, di.sms, st));
+          if (rc) return rc;
+        }
+      sum0 = L.xs_bytes + align_ws(partial);
+      phases_run = true;
+    }
+  }
   // One split-K pass per group on the group's slices (x channels, dy channels, dw rows);
   // the split partials reuse the workspace group after group (stream order).  The plans
   // embed the slices' addresses (tensor maps), so each group has its own cached plan.
-  for (int gi = 0; gi < groups; ++gi) {
+  for (int gi = 0; gi < groups && !phases_run; ++gi) {
     const void* xg = byte_ptr(x) + gi * (size_t)dg.C * dg.H * dg.W * esz;
     const void* dyg = byte_ptr(dy) + gi * (size_t)dg.K * dg.P * dg.Q * esz;
     void* dwg = const_cast<uint8_t*>(byte_ptr(dw)) + gi * (size_t)dg.K * dg.C * dg.R * dg.S * esz;

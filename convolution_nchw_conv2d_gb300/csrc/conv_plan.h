@@ -194,11 +194,22 @@ struct WgradPlan {
 
 struct ReducePlan {
   const float* partial;
-  void* dw;              // KCRS, fp32 or bf16
-  int K, C, R, S;
+  void* dw;              // K x C x R_out x S_out, fp32 or bf16
+  int K, C, R, S;        // the partials' filter: R x S taps
   int nsplit, k_pad, c_pad;
   float beta;            // dw = sum + beta * dw (beta 0: dw is not read)
-  int flip;              // convolution mode: partial tap (r, s) is dw[.., R-1-r, S-1-s]
+  int flip;              // convolution mode: the placed tap (r, s) is dw[.., R_out-1-r, S_out-1-s]
+  // Placement of partial tap (r', s') in dw: (r0 + rstep * r', s0 + sstep * s') of an
+  // R_out x S_out filter (one stride phase of a strided filter; the identity otherwise).
+  int R_out, S_out, r0, s0, rstep, sstep;
+};
+
+// Space-to-depth of x for strided backward-filter: xs[n][a*sw + b][c][i][j] =
+// x[n][c][i*sh + a][j*sw + b] (zero where that lies outside x), i < Hp, j < Wp.
+struct S2dPlan {
+  const void* x;
+  void* xs;
+  int N, C, H, W, sh, sw, Hp, Wp;
 };
 
 // Per-channel sum of an NCHW-like tensor t (N, Ch, HW): out[ch] = sum_{n, i} t[n, ch, i]

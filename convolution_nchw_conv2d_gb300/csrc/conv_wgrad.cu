@@ -1067,7 +1067,12 @@ __global__ void __launch_bounds__(32 * kReduceWarps) wgrad_reduce_kernel(const _
         const long long r = io / rp.K;
         const int c = (int)(r % rp.C);
         const int tap = (int)(r / rp.C);
-        const long long o = ((long long)k * rp.C + c) * RS + (rp.flip ? RS - 1 - tap : tap);
+        int rr = rp.r0 + rp.rstep * (tap / rp.S), ss = rp.s0 + rp.sstep * (tap % rp.S);
+        if (rp.flip) {
+          rr = rp.R_out - 1 - rr;
+          ss = rp.S_out - 1 - ss;
+        }
+        const long long o = (((long long)k * rp.C + c) * rp.R_out + rr) * rp.S_out + ss;
         if constexpr (DT == 0) {
           float* dwp = static_cast<float*>(rp.dw);
           if (rp.beta != 0.f) sum += rp.beta * dwp[o];
@@ -1160,6 +1165,45 @@ cudaError_t launch_chan_sum(const ChanSumPlan& cp, int dt, cudaStream_t st) {
     chan_sum_partial_kernel<1><<<blocks, kSumThreads, 0, st>>>(cp);
     chan_sum_final_kernel<1><<<fblocks, kSumThreads, 0, st>>>(cp);
   }
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------- space to depth
+// xs[n][a*sw + b][c][i][j] = x[n][c][i*sh + a][j*sw + b], zero outside x.  One (image, plane,
+// channel) slab per block row; threads take consecutive j, so stores are contiguous and a
+// warp's loads touch sw times its width of one input row.
+template <int DT>
+__global__ void __launch_bounds__(256) space_to_depth_kernel(const __grid_constant__ S2dPlan sp) {
+  using E = typename std::conditional<DT == 0, uint32_t, uint16_t>::type;
+  const E* x = static_cast<const E*>(sp.x);
+  E* xs = static_cast<E*>(sp.xs);
+  const int npl = sp.sh * sp.sw;
+  const long long slabs = (long long)sp.N * npl * sp.C;
+  const int plane = sp.Hp * sp.Wp;
+  for (long long sl = blockIdx.y; sl < slabs; sl += gridDim.y) {
+    const int c = (int)(sl % sp.C);
+    const long long t = sl / sp.C;  // n * npl + plane index
+    const int pl = (int)(t % npl);
+    const long long n = t / npl;
+    const int a = pl / sp.sw, b = pl - (pl / sp.sw) * sp.sw;
+    const E* src = x + (n * sp.C + c) * (long long)sp.H * sp.W;
+    E* dst = xs + sl * (long long)plane;
+    for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < plane; e += gridDim.x * blockDim.x) {
+      const int i = e / sp.Wp, j = e - (e / sp.Wp) * sp.Wp;
+      const int h = i * sp.sh + a, w = j * sp.sw + b;
+      dst[e] = (h < sp.H && w < sp.W) ? src[(long long)h * sp.W + w] : E(0);
+    }
+  }
+}
+
+cudaError_t launch_space_to_depth(const S2dPlan& sp, int dt, cudaStream_t st) {
+  const long long plane = (long long)sp.Hp * sp.Wp;
+  const long long slabs = (long long)sp.N * sp.sh * sp.sw * sp.C;
+  const dim3 grid((unsigned)std::min<long long>((plane + 255) / 256, 64), (unsigned)std::min<long long>(slabs, 65535));
+  if (dt == 0)
+    space_to_depth_kernel<0><<<grid, 256, 0, st>>>(sp);
+  else
+    space_to_depth_kernel<1><<<grid, 256, 0, st>>>(sp);
   return cudaGetLastError();
 }
 

@@ -44,7 +44,8 @@
  *     conv2d_workspace_size() for the same op and descriptor, 16-byte aligned.  The
  *     size never exceeds 1e9 bytes (the workspace cap of the SystemDS wrapper,
  *     MAX_WORKSPACE_LIMIT_BYTES).  Forward and backward-data stage a repacked copy of
- *     the filter there; backward-filter stages split partial sums.
+ *     the filter there; backward-filter stages split partial sums, and with a stride
+ *     above 1 (dilation 1) also a copy of x rearranged into its stride phases.
  *   - Forward and backward-data with large filters over many source channels (about
  *     13 x 13 taps and more) run as several passes over contiguous ranges of the taps
  *     r*S + s, each adding onto the output the previous one wrote; with bf16 tensors

@@ -149,6 +149,48 @@ void check_wgrad(const char* nm, const Desc& d, const WgradBuild& b, const DevIn
     }
 }
 
+// Strided backward-filter as stride phases: each phase plans and meets the invariants
+// above; each of its taps reads, through the planes, the input pixel the definition names
+// for every output; the placed taps cover the filter once.
+void check_phases(const char* nm, const Desc& dg, const DevInfo& di, int& plans) {
+  const PhaseLayout L = phase_layout(dg);
+  if (!L.on) return;
+  std::vector<WgradBuild> ph;
+  void* xs = (void*)0x500000;
+  if (plan_phases(dg, L, xs, (void*)0x300000, (void*)0x200000, (void*)0x600000, 0, di, ph) != CONV2D_OK) {
+    fail(nm, "bwd_filter", "a stride phase has no plan");
+    return;
+  }
+  std::vector<int> seen((size_t)dg.R * dg.S, 0);
+  size_t i = 0;
+  for (const StridePhase& a : L.rows)
+    for (const StridePhase& b : L.cols) {
+      const Desc q = phase_desc(dg, L, a, b);
+      const WgradBuild& wb = ph[i++];
+      check_wgrad(nm, q, wb, di);
+      ++plans;
+      for (int r2 = 0; r2 < q.R; ++r2)
+        for (int s2 = 0; s2 < q.S; ++s2) {
+          const int r = wb.rp.r0 + wb.rp.rstep * r2, s = wb.rp.s0 + wb.rp.sstep * s2;
+          if (r < 0 || r >= dg.R || s < 0 || s >= dg.S) {
+            fail(nm, "bwd_filter", "a phase tap lies outside the filter");
+            continue;
+          }
+          ++seen[(size_t)r * dg.S + s];
+          for (int p = 0; p < dg.P; ++p)
+            if (dg.sh * (p - q.ph + r2) + a.rho != p * dg.sh - dg.ph + r) fail(nm, "bwd_filter", "phase row");
+          for (int qq = 0; qq < dg.Q; ++qq)
+            if (dg.sw * (qq - q.pw + s2) + b.rho != qq * dg.sw - dg.pw + s) fail(nm, "bwd_filter", "phase column");
+        }
+      if (q.ph < 0 || q.pw < 0) fail(nm, "bwd_filter", "negative phase pad");
+    }
+  for (size_t t = 0; t < seen.size(); ++t)
+    if (seen[t] != 1) {
+      fail(nm, "bwd_filter", "a filter tap is not in exactly one stride phase");
+      break;
+    }
+}
+
 }  // namespace
 
 int main() {
@@ -193,6 +235,9 @@ int main() {
       {"grp2", 2, 64, 16, 16, 64, 3, 3, 1, 1, 1, 1, 0, 1, 1, 2, {1, 1}},
       {"depthwise", 1, 16, 12, 12, 16, 3, 3, 1, 1, 1, 1, 1, 1, 1, 16, {1, 1}},
       {"grp_dil", 2, 8, 13, 11, 6, 3, 3, 2, 2, 1, 2, 0, 2, 1, 2, {1, 1}},
+      {"s3_r2", 1, 1, 7, 7, 1, 2, 2, 0, 0, 3, 3, 0, 1, 1, 1, {1, 1}},
+      {"s2_grp", 2, 8, 14, 13, 6, 3, 3, 1, 1, 2, 2, 1, 1, 1, 2, {1, 1}},
+      {"s32_r5", 1, 40, 20, 19, 24, 5, 3, 2, 0, 2, 3, 0, 1, 1, 1, {1, 1}},
   };
   DevInfo di;
   di.sms = 152;
@@ -241,6 +286,7 @@ int main() {
     }
     WgradBuild bw;
     if (build_bwd_filter(d, px, py, pw, ws, di, bw) != CONV2D_OK) fail(s.nm, "bwd_filter", "no plan");
+    check_phases(s.nm, d, di, plans);
   }
   std::printf("checked %d plans, %d violations\n", plans, g_fail);
   return g_fail > 100 ? 100 : g_fail;

@@ -482,3 +482,41 @@ def test_tap_passes_parity(cg, case, dtype, epi):
                  amax(x) * amax(w), C * R * S, f"{case}/fwd/{dtype}/epi={epi}")
     _check_plain(pb, dx.double().cpu().numpy(), oracle.conv2d_bwd_data_ex(dy, w, (H, Wd), bc, beta_d, dx0, pad, st),
                  amax(dy) * amax(w), K * R * S, f"{case}/bwd_data/{dtype}/epi={epi}")
+
+
+# Strided backward-filter (dilation 1) runs as stride phases: x copied once into unit-stride
+# planes, one stride-1 pass per phase whose reduce places its taps in the filter.  Cases:
+# odd and even extents, stride 3 (a phase without taps when R < stride), unequal strides,
+# groups, convolution mode, beta and the bias gradients, both dtypes.
+PHASE_CASES = [
+    ((2, 3, 9, 9, 4, 3, 3, 1, 1, 2, 2), 1),
+    ((2, 8, 14, 13, 6, 4, 4, 1, 1, 2, 2), 2),
+    ((1, 2, 11, 10, 5, 2, 2, 0, 0, 3, 3), 1),
+    ((2, 40, 20, 19, 24, 5, 3, 2, 0, 2, 3), 1),
+    ((2, 64, 17, 16, 64, 3, 3, 1, 1, 2, 1), 2),
+]
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("flip", [False, True])
+@pytest.mark.parametrize("case,groups", PHASE_CASES)
+def test_stride_phase_bwd_filter_parity(cg, case, groups, flip, dtype):
+    N, C, H, Wd, K, R, S, ph, pw, sh, sw = case
+    pb = W.Conv2dProblem(N, C, H, Wd, K, R, S, ph, pw, sh, sw, dtype)
+    seed = 9700 + 4 * PHASE_CASES.index((case, groups)) + 2 * int(flip) + int(dtype == "bf16")
+    x, _, dy = W.random_problem_inputs(pb, seed)
+    tdt = x.dtype
+    g = torch.Generator().manual_seed(seed)
+    dw0 = torch.randn((K, C // groups, R, S), generator=g).to(tdt)
+    dbk0 = torch.randn(K, generator=g).to(tdt)
+    pad, st = (ph, pw), (sh, sw)
+    dw, dbk = dw0.to(DEV), dbk0.to(DEV)
+    cg.conv2d_bwd_filter(x.to(DEV), dy.to(DEV), (R, S), pad, st, out=dw, beta=0.5, db_k=dbk, flip=flip,
+                         groups=groups)
+    cg.conv2d_device_status()
+    amax = lambda t: float(t.abs().max())
+    ref = oracle.conv2d_bwd_filter_ex(x, dy, (R, S), 0.5, dw0, pad, st, flip=flip, groups=groups)
+    _check_plain(pb, dw.double().cpu().numpy(), ref, amax(x) * amax(dy), N * pb.P * pb.Q,
+                 f"{case}/g{groups}/flip={flip}/{dtype}")
+    _check_plain(pb, dbk.double().cpu().numpy(), oracle.channel_sum(dy, 0.5, dbk0), amax(dy), N * pb.P * pb.Q,
+                 f"{case}/db_k/{dtype}")
