@@ -129,7 +129,9 @@ DevInfo device_info() {
 // A 1x1 filter with unit stride and no padding sees each image as one row of H*W
 // pixels; planning it that way makes every row of the linear space contiguous.
 Desc flatten_pointwise(Desc d) {
-  if (d.R == 1 && d.S == 1 && d.ph == 0 && d.pw == 0 && d.sh == 1 && d.sw == 1) {
+  // (P == H and Q == W for every caller descriptor of such a filter; a stride-phase problem
+  // may carry a smaller output and is left as it is)
+  if (d.R == 1 && d.S == 1 && d.ph == 0 && d.pw == 0 && d.sh == 1 && d.sw == 1 && d.P == d.H && d.Q == d.W) {
     d.W = d.H * d.W;
     d.H = 1;
     d.Q = d.W;

@@ -169,6 +169,11 @@ void check_phases(const char* nm, const Desc& dg, const DevInfo& di, int& plans)
       const WgradBuild& wb = ph[i++];
       check_wgrad(nm, q, wb, di);
       ++plans;
+      // the plan addresses the caller's dy and the planes buffer with their real image strides
+      if (wb.p.dy_nstride != (long long)dg.g * dg.K * dg.P * dg.Q)
+        fail(nm, "bwd_filter", "phase plan's dy image stride differs from the dy tensor's");
+      if (wb.p.x_nstride != (long long)dg.sh * dg.sw * dg.g * dg.C * L.Hp * L.Wp)
+        fail(nm, "bwd_filter", "phase plan's x image stride differs from the planes buffer's");
       for (int r2 = 0; r2 < q.R; ++r2)
         for (int s2 = 0; s2 < q.S; ++s2) {
           const int r = wb.rp.r0 + wb.rp.rstep * r2, s = wb.rp.s0 + wb.rp.sstep * s2;
@@ -236,6 +241,7 @@ int main() {
       {"depthwise", 1, 16, 12, 12, 16, 3, 3, 1, 1, 1, 1, 1, 1, 1, 16, {1, 1}},
       {"grp_dil", 2, 8, 13, 11, 6, 3, 3, 2, 2, 1, 2, 0, 2, 1, 2, {1, 1}},
       {"s3_r2", 1, 1, 7, 7, 1, 2, 2, 0, 0, 3, 3, 0, 1, 1, 1, {1, 1}},
+      {"s2_9x9", 2, 3, 9, 9, 4, 3, 3, 1, 1, 2, 2, 0, 1, 1, 1, {1, 1}},
       {"s2_grp", 2, 8, 14, 13, 6, 3, 3, 1, 1, 2, 2, 1, 1, 1, 2, {1, 1}},
       {"s32_r5", 1, 40, 20, 19, 24, 5, 3, 2, 0, 2, 3, 0, 1, 1, 1, {1, 1}},
   };
