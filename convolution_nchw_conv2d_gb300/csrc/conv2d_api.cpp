@@ -872,6 +872,26 @@ const void* phase_plane(const void* xs, const Desc& dg, const PhaseLayout& L, co
   return byte_ptr(xs) + ((pl * dg.g + gi) * dg.C) * (size_t)L.Hp * L.Wp * esz;
 }
 
+// Staging work of a backward-filter plan, in copies: for every (m-group, n-tile) pass over
+// the positions, each position stages the x channels of every plane and the dy rows of the
+// n tile; a 16-byte (or whole-row tensor) copy counts once, an element copy once per element.
+// The stride phases trade element copies of x for one more pass over dy per phase, which
+// pays only where x staging dominates (many channels) -- not on a 3-channel stem.
+double staging_copies(const WgradPlan& p, int dt) {
+  const int CHUNK = dt == 0 ? 4 : 8;
+  const double xc = (double)p.xch * p.npl / ((p.vec_x || p.use_tma == 1) ? CHUNK : 1);
+  const double dc = (double)p.NK / ((p.vec_dy || p.use_tma == 1) ? CHUNK : 1);
+  return (double)p.n_mgroups * p.n_ntiles * (xc + dc) * (double)p.Mit;
+}
+
+// True when the phases stage less than the problem as a whole (or it has no plan).
+bool phases_stage_less(const std::vector<WgradBuild>& phases, const WgradPlan* whole, int dt) {
+  if (whole == nullptr) return true;
+  double cp = 0.0;
+  for (const WgradBuild& wb : phases) cp += staging_copies(wb.p, dt);
+  return cp < staging_copies(*whole, dt);
+}
+
 // Plans every phase of group gi (cached); false if one of them has no plan.
 int plan_phases(const Desc& dg, const PhaseLayout& L, const void* xs, const void* dyg, void* dwg, void* partial_ws,
                 int gi, const DevInfo& di, std::vector<WgradBuild>& out);
@@ -1256,6 +1276,18 @@ int conv2d_bwd_filter_ex(int N, int C, int H, int W, int K, int R, int S, int pa
       if (rc == CONV2D_ERR_UNSUPPORTED) phased = false;
       else if (rc) return rc;
       for (const WgradBuild& wb : gp[(size_t)gi]) partial = std::max(partial, wb.partial_bytes);
+    }
+    if (phased) {
+      // the phases must stage less than the problem as a whole
+      const void* dy0 = dy;
+      WgradBuild whole;
+      const PlanKey key = make_key(CONV2D_OP_BWD_FILTER, dg, x, dy0, dw, workspace);
+      bool have_whole = g_wgrad_plans.get(key, whole);
+      if (!have_whole && build_bwd_filter(dg, x, dy0, dw, workspace, di, whole) == CONV2D_OK) {
+        g_wgrad_plans.put(key, whole);
+        have_whole = true;
+      }
+      phased = phases_stage_less(gp[0], have_whole ? &whole.p : nullptr, d.dt);
     }
     if (phased) {
       rc = check_ws(workspace, workspace_bytes,

@@ -196,6 +196,38 @@ void check_phases(const char* nm, const Desc& dg, const DevInfo& di, int& plans)
     }
 }
 
+// The stride-phase choice on the strided workloads: the phases pay where x staging dominates
+// (128 and 256 channels), not on the 3-channel stem, as measured.
+void check_phase_choice(int& plans) {
+  struct W { const char* nm; int v[12]; bool phases; } ws[] = {
+      {"strided", {64, 128, 56, 56, 256, 3, 3, 1, 1, 2, 2, 0}, true},
+      {"stem7x7", {64, 3, 224, 224, 64, 7, 7, 3, 3, 2, 2, 0}, false},
+      {"deconv", {32, 256, 32, 32, 512, 4, 4, 1, 1, 2, 2, 1}, true},
+  };
+  DevInfo di;
+  di.sms = 152;
+  di.smem_optin = 232448;
+  di.ok = true;
+  for (const W& w : ws) {
+    Desc d{};
+    const int* v = w.v;
+    d.N = v[0]; d.C = v[1]; d.H = v[2]; d.W = v[3]; d.K = v[4]; d.R = v[5]; d.S = v[6];
+    d.ph = v[7]; d.pw = v[8]; d.sh = v[9]; d.sw = v[10]; d.dt = v[11];
+    d.P = out_dim(d.H, d.ph, d.R, d.sh);
+    d.Q = out_dim(d.W, d.pw, d.S, d.sw);
+    const PhaseLayout L = phase_layout(d);
+    std::vector<WgradBuild> ph;
+    WgradBuild whole;
+    if (plan_phases(d, L, (void*)0x500000, (void*)0x300000, (void*)0x200000, (void*)0x600000, 0, di, ph) != CONV2D_OK ||
+        build_bwd_filter(d, (void*)0x100000, (void*)0x300000, (void*)0x200000, (void*)0x600000, di, whole) != CONV2D_OK) {
+      fail(w.nm, "bwd_filter", "no plan");
+      continue;
+    }
+    plans += 1 + (int)ph.size();
+    if (phases_stage_less(ph, &whole.p, d.dt) != w.phases) fail(w.nm, "bwd_filter", "unexpected stride-phase choice");
+  }
+}
+
 }  // namespace
 
 int main() {
@@ -294,6 +326,7 @@ int main() {
     if (build_bwd_filter(d, px, py, pw, ws, di, bw) != CONV2D_OK) fail(s.nm, "bwd_filter", "no plan");
     check_phases(s.nm, d, di, plans);
   }
+  check_phase_choice(plans);
   std::printf("checked %d plans, %d violations\n", plans, g_fail);
   return g_fail > 100 ? 100 : g_fail;
 }

@@ -484,16 +484,19 @@ def test_tap_passes_parity(cg, case, dtype, epi):
                  amax(dy) * amax(w), K * R * S, f"{case}/bwd_data/{dtype}/epi={epi}")
 
 
-# Strided backward-filter (dilation 1) runs as stride phases: x copied once into unit-stride
-# planes, one stride-1 pass per phase whose reduce places its taps in the filter.  Cases:
-# odd and even extents, stride 3 (a phase without taps when R < stride), unequal strides,
-# groups, convolution mode, beta and the bias gradients, both dtypes.
+# Strided backward-filter (dilation 1) runs as stride phases where that stages less than the
+# problem as a whole: x copied once into unit-stride planes, one stride-1 pass per phase whose
+# reduce places its taps in the filter.  Every case below takes the phases in both dtypes:
+# groups, 4x4 stride 2, stride 3 with 2x2 taps (phases without taps), unequal strides, odd
+# extents; each with convolution mode, beta and the bias gradient.
 PHASE_CASES = [
-    ((2, 3, 9, 9, 4, 3, 3, 1, 1, 2, 2), 1),
-    ((2, 8, 14, 13, 6, 4, 4, 1, 1, 2, 2), 2),
-    ((1, 2, 11, 10, 5, 2, 2, 0, 0, 3, 3), 1),
-    ((2, 40, 20, 19, 24, 5, 3, 2, 0, 2, 3), 1),
-    ((2, 64, 17, 16, 64, 3, 3, 1, 1, 2, 1), 2),
+    ((2, 256, 14, 14, 128, 3, 3, 1, 1, 2, 2), 2),
+    ((1, 192, 20, 16, 160, 4, 4, 1, 1, 2, 2), 2),
+    ((1, 128, 24, 24, 64, 2, 2, 0, 0, 3, 3), 1),
+    ((1, 128, 23, 22, 96, 2, 3, 0, 1, 3, 2), 1),
+    ((2, 128, 15, 14, 64, 3, 3, 1, 1, 2, 2), 1),
+    ((1, 96, 25, 23, 64, 3, 3, 1, 1, 3, 3), 1),
+    ((1, 64, 22, 21, 32, 5, 3, 2, 1, 2, 3), 1),
 ]
 
 
