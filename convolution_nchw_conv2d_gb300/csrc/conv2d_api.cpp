@@ -1068,6 +1068,26 @@ int phase_workspace(const Desc& dg, const PhaseLayout& L, const DevInfo& di, siz
   return CONV2D_OK;
 }
 
+// Workspace the stride phases of dg need (planes, largest partials, bias sums), or 0 when
+// they do not apply, do not plan, or would pass the workspace cap (the problem then runs as a
+// whole).  The size query and the call both decide from this value.  Cached per descriptor.
+constexpr int kPhaseNeedKey = 16;  // cache key tag (not an op code)
+
+size_t phase_need(const Desc& dg, const DevInfo& di) {
+  const PhaseLayout L = phase_layout(dg);
+  if (!L.on) return 0;
+  const PlanKey key = make_key(kPhaseNeedKey, dg, nullptr, nullptr, nullptr, nullptr);
+  size_t v = 0;
+  if (g_ws_sizes.get(key, v)) return v;
+  size_t partial = 0;
+  if (phase_workspace(dg, L, di, partial) == CONV2D_OK) {
+    v = L.xs_bytes + align_ws(partial) + chan_sum_bytes(dg);
+    if (v > kWorkspaceCap) v = 0;
+  }
+  g_ws_sizes.put(key, v);
+  return v;
+}
+
 }  // namespace
 
 extern "C" {
@@ -1119,11 +1139,7 @@ int workspace_size_uncached(int op, const Desc& d, size_t* bytes) {
   if (op == CONV2D_OP_BWD_FILTER) {
     // Strided filters run as stride phases when every phase plans (else as one problem);
     // size for either.
-    size_t phased = 0;
-    const PhaseLayout L = phase_layout(d);
-    size_t partial = 0;
-    if (L.on && phase_workspace(d, L, di, partial) == CONV2D_OK)
-      phased = L.xs_bytes + align_ws(partial) + chan_sum_bytes(d);
+    const size_t phased = phase_need(d, di);
     // The launch plans the copy-engine staging unless its tensor maps fail to encode for the
     // actual tensors; size for whichever of the two plans it ends up with.
     WgradBuild b;
@@ -1264,7 +1280,7 @@ int conv2d_bwd_filter_ex(int N, int C, int H, int W, int K, int R, int S, int pa
   // Strided filters: x into stride-phase planes once, then one stride-1 pass per phase and
   // group (all planned before anything is enqueued; one problem if a phase has no plan).
   const PhaseLayout L = phase_layout(dg);
-  if (L.on && workspace != nullptr) {
+  if (L.on && workspace != nullptr && phase_need(dg, di) != 0) {
     uint8_t* wsp = static_cast<uint8_t*>(workspace);
     std::vector<std::vector<WgradBuild>> gp((size_t)groups);
     size_t partial = 0;

@@ -225,7 +225,14 @@ void check_phase_choice(int& plans) {
     }
     plans += 1 + (int)ph.size();
     if (phases_stage_less(ph, &whole.p, d.dt) != w.phases) fail(w.nm, "bwd_filter", "unexpected stride-phase choice");
+    const size_t need = phase_need(d, di);
+    if (need == 0 || need > kWorkspaceCap || need < L.xs_bytes) fail(w.nm, "bwd_filter", "stride-phase workspace");
   }
+  // a layer whose x alone passes the workspace cap runs as a whole
+  Desc big{};
+  big.N = 112; big.C = 256; big.H = 96; big.W = 96; big.K = 256; big.R = 3; big.S = 3;
+  big.ph = 1; big.pw = 1; big.sh = 2; big.sw = 2; big.dt = 0; big.P = 48; big.Q = 48;
+  if (phase_need(big, di) != 0) fail("x_over_cap", "bwd_filter", "stride phases past the workspace cap");
 }
 
 }  // namespace

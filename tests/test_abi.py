@@ -118,6 +118,17 @@ def test_workspace_sizes_are_bounded(cg):
             assert rc == 0 and 0 < n <= 1_000_000_000 and n % 16 == 0
 
 
+def test_strided_filter_gradient_workspace_stays_under_the_cap(cg):
+    """Strided backward-filter may stage a copy of x in the workspace (stride phases); a layer
+    whose x alone passes the 1e9-byte cap runs without it, so the size stays under the cap."""
+    x_over_cap = (112, 256, 96, 96, 256, 3, 3, 1, 1, 2, 2, 48, 48)  # x: 1.06e9 bytes in fp32
+    rc, n = _ws(cg, 2, x_over_cap, 0)
+    assert rc == 0 and 0 < n <= 1_000_000_000
+    strided = W.WORKLOADS["strided"].problem  # takes the phases: x (102.8 MB) is in the size
+    rc, n = _ws(cg, 2, strided.dims(), 0)
+    assert rc == 0 and n > strided.N * strided.C * strided.H * strided.W * 4
+
+
 def test_strerror_covers_codes(cg):
     for c in range(0, -13, -1):
         assert cg.conv2d_strerror(c) and "unknown error" not in cg.conv2d_strerror(c)
