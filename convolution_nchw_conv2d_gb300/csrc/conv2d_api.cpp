@@ -1294,12 +1294,12 @@ int conv2d_bwd_filter_ex(int N, int C, int H, int W, int K, int R, int S, int pa
       for (const WgradBuild& wb : gp[(size_t)gi]) partial = std::max(partial, wb.partial_bytes);
     }
     if (phased) {
-      // the phases must stage less than the problem as a whole
-      const void* dy0 = dy;
+      // the phases must stage less than the problem as a whole (group 0's plan, cached under
+      // the key the per-group loop below uses)
       WgradBuild whole;
-      const PlanKey key = make_key(CONV2D_OP_BWD_FILTER, dg, x, dy0, dw, workspace);
+      const PlanKey key = make_key(CONV2D_OP_BWD_FILTER, dg, x, dy, dw, workspace);
       bool have_whole = g_wgrad_plans.get(key, whole);
-      if (!have_whole && build_bwd_filter(dg, x, dy0, dw, workspace, di, whole) == CONV2D_OK) {
+      if (!have_whole && build_bwd_filter(dg, x, dy, dw, workspace, di, whole) == CONV2D_OK) {
         g_wgrad_plans.put(key, whole);
         have_whole = true;
       }
