@@ -1011,7 +1011,7 @@ int workspace_size_uncached(int op, const Desc& d, size_t* bytes);
 
 PlanKey make_key(int op, const Desc& d, const void* a, const void* b, const void* c, const void* ws) {
   PlanKey k;
-  std::memset(&k, 0, sizeof(k));
+  std::memset(static_cast<void*>(&k), 0, sizeof(k));  // padding too: keys compare by memcmp
   k.op = op;
   cudaGetDevice(&k.dev);
   k.d = d;
