@@ -69,6 +69,9 @@ def _bind(lib):
     for name in ("oracle_conv3d_fwd", "oracle_conv3d_bwd_data", "oracle_conv3d_bwd_filter"):
         getattr(lib, name).argtypes = [dp, dp, dp, ivp]
         getattr(lib, name).restype = None
+    for name in ("oracle_conv3d_fwd_at", "oracle_conv3d_bwd_data_at", "oracle_conv3d_bwd_filter_at"):
+        getattr(lib, name).argtypes = [dp, dp, ivp, ip, i64, dp]
+        getattr(lib, name).restype = None
     lib.oracle_num_threads.argtypes = []
     lib.oracle_num_threads.restype = i
     return lib
@@ -371,6 +374,38 @@ def conv3d_bwd_filter(x, dy, trs, pad=0, stride=1, dilation=1, groups=1) -> np.n
         _load().oracle_conv3d_bwd_filter(_ptr(xs), _ptr(dys), _ptr(dw), _iptr(dims))
         parts.append(dw)
     return np.concatenate(parts, axis=0)
+
+
+def _at3(fn, a, b, dims, idx):
+    a, b = _f64(a), _f64(b)
+    dims = np.ascontiguousarray(np.asarray(dims, dtype=np.int32))
+    idx = np.ascontiguousarray(np.asarray(idx, dtype=np.int64))
+    out = np.empty(idx.shape[0], dtype=np.float64)
+    fn(_ptr(a), _ptr(b), _iptr(dims), idx.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)),
+       ctypes.c_int64(idx.shape[0]), _ptr(out))
+    return out
+
+
+def conv3d_dims(x_shape, w_shape, pad=0, stride=1, dilation=1):
+    """The 21 descriptor ints of the C 3-D ops for x (N,C,D,H,W) and w (K,C,T,R,S), one group."""
+    dims, _ = _dims3(x_shape[0], x_shape[1], tuple(x_shape[2:]), w_shape[0], tuple(w_shape[2:]), pad, stride,
+                     dilation)
+    return dims
+
+
+def conv3d_fwd_at(x, w, dims, idx) -> np.ndarray:
+    """Forward outputs at flat (n,k,z,p,q) indices; dims from conv3d_dims (one group)."""
+    return _at3(_load().oracle_conv3d_fwd_at, x, w, dims, idx)
+
+
+def conv3d_bwd_data_at(dy, w, dims, idx) -> np.ndarray:
+    """Backward-data outputs at flat (n,c,z,h,w) indices."""
+    return _at3(_load().oracle_conv3d_bwd_data_at, dy, w, dims, idx)
+
+
+def conv3d_bwd_filter_at(x, dy, dims, idx) -> np.ndarray:
+    """Backward-filter outputs at flat (k,c,t,r,s) indices."""
+    return _at3(_load().oracle_conv3d_bwd_filter_at, x, dy, dims, idx)
 
 
 def num_threads() -> int:

@@ -163,3 +163,50 @@ void oracle_conv3d_bwd_filter(const double *x, const double *dy, double *dw, con
                     for (int s = 0; s < g.S; ++s)
                         dw[IDX5(k, c, t, r, s, g.C, g.T, g.R, g.S)] = bwd_filter3_one(x, dy, &g, k, c, t, r, s);
 }
+
+/* Sampled evaluation: the same per-element definitions at the flat output indices
+ * idx[0..count) (y / dx / dw in their NCDHW / KCTRS order), for parity at full sizes. */
+void oracle_conv3d_fwd_at(const double *x, const double *w, const int *dims, const int64_t *idx, int64_t count,
+                          double *out)
+{
+    const geom3 g = make_geom(dims);
+#pragma omp parallel for schedule(dynamic, 16)
+    for (int64_t i = 0; i < count; ++i) {
+        int64_t f = idx[i];
+        const int q = (int)(f % g.Q); f /= g.Q;
+        const int p = (int)(f % g.P); f /= g.P;
+        const int z = (int)(f % g.Z); f /= g.Z;
+        const int k = (int)(f % g.K); f /= g.K;
+        out[i] = fwd3_one(x, w, &g, (int)f, k, z, p, q);
+    }
+}
+
+void oracle_conv3d_bwd_data_at(const double *dy, const double *w, const int *dims, const int64_t *idx,
+                               int64_t count, double *out)
+{
+    const geom3 g = make_geom(dims);
+#pragma omp parallel for schedule(dynamic, 16)
+    for (int64_t i = 0; i < count; ++i) {
+        int64_t f = idx[i];
+        const int ww = (int)(f % g.W); f /= g.W;
+        const int h = (int)(f % g.H); f /= g.H;
+        const int z = (int)(f % g.D); f /= g.D;
+        const int c = (int)(f % g.C); f /= g.C;
+        out[i] = bwd_data3_one(dy, w, &g, (int)f, c, z, h, ww);
+    }
+}
+
+void oracle_conv3d_bwd_filter_at(const double *x, const double *dy, const int *dims, const int64_t *idx,
+                                 int64_t count, double *out)
+{
+    const geom3 g = make_geom(dims);
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t i = 0; i < count; ++i) {
+        int64_t f = idx[i];
+        const int s = (int)(f % g.S); f /= g.S;
+        const int r = (int)(f % g.R); f /= g.R;
+        const int t = (int)(f % g.T); f /= g.T;
+        const int c = (int)(f % g.C); f /= g.C;
+        out[i] = bwd_filter3_one(x, dy, &g, (int)f, c, t, r, s);
+    }
+}

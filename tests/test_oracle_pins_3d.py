@@ -217,6 +217,18 @@ def test_torch_cpu_fp64_witness_3d(case):
     assert _close(_bwd_filter(x, dy, case), wt.grad.numpy(), 1e-11)
 
 
+@pytest.mark.parametrize("case", [c for c in CASES if c[12] == 1])
+def test_sampled_equals_full_3d(case):
+    """The sampled evaluators (full-size parity) agree bit for bit with the full ops."""
+    x, w, dy = _tensors(case, RNG)
+    dims = oracle.conv3d_dims(x.shape, w.shape, case[9], case[10], case[11])
+    y, dx, dw = _fwd(x, w, case), _bwd_data(dy, w, case), _bwd_filter(x, dy, case)
+    for full, fn, a, b in ((y, oracle.conv3d_fwd_at, x, w), (dx, oracle.conv3d_bwd_data_at, dy, w),
+                           (dw, oracle.conv3d_bwd_filter_at, x, dy)):
+        idx = RNG.choice(full.size, size=min(40, full.size), replace=False)
+        assert np.array_equal(fn(a, b, dims, idx), full.reshape(-1)[idx])
+
+
 # --------------------------------------------------------------------------- planted mistakes
 # Each entry: (function in conv3d_oracle.c, text there, replacement).  Every replacement keeps
 # all reads in bounds (reads go through the zero-padding helper or the reader test).
