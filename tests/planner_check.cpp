@@ -55,32 +55,56 @@ void check_tap(const char* nm, const char* op, const TapBuild& b, const DevInfo&
   if (p.Mtot >= (1ll << 31)) fail(nm, op, "position space too large");
 }
 
-// Every real tap of every pass reads, for each output, the source pixel the definition
-// names: forward row (p*sh - ph + r*dh), column (q*sw - pw + s*dw); backward-data dy row
-// (h + ph - r*dh) / sh, column (w + pw - s*dw) / sw.  In the plan an output at linear
-// (e, f) reads linear (e + roff, f + coff) of its plane, roff / coff being the tap offset
-// split by the row width; planes and phases add their own offsets.  Every (r, s) must be
-// a real tap of exactly one pass.
+// Every real tap of every pass reads, for every output the plan writes, the source pixel the
+// definition names: forward (p*sh - ph + r*dh, q*sw - pw + s*dw) of x; backward-data
+// ((h + ph - r*dh) / sh, (w + pw - s*dw) / sw) of dy.  The kernel's read follows the linear
+// space: the output at linear (e, f) reads linear position e*WL + f + tap offset of the tap's
+// plane, whose pixel is (row * step + plane offset) in each dim; outputs outside the
+// destination are not written, so their reads do not matter.  Every (r, s) must be a real
+// tap of exactly one pass.
 void check_tap_semantics(const char* nm, const char* op, const Desc& d, const TapSet& set, bool fwd) {
   std::vector<int> seen((size_t)d.R * d.S, 0);
+  bool bad = false;
   for (const TapBuild& b : set.pass) {
     const TapPlan& p = b.p;
-    for (int ph = 0; ph < p.nph; ++ph)
-      for (int t = p.ph_tap_begin[ph]; t < p.ph_tap_begin[ph] + p.ph_ntaps[ph]; ++t) {
+    for (int ph = 0; ph < p.nph && !bad; ++ph)
+      for (int t = p.ph_tap_begin[ph]; t < p.ph_tap_begin[ph] + p.ph_ntaps[ph] && !bad; ++t) {
         const int r = b.pp.tap_r[t], s = b.pp.tap_s[t];
         if (r < 0) continue;  // zero-weight tap that pads a phase to an even count
         ++seen[(size_t)r * d.S + s];
-        const int roff = p.tap_off[t] / p.WL, coff = p.tap_off[t] % p.WL;
-        if (fwd) {
-          const int pl = p.tap_plane[t];
-          if (roff * d.sh + p.pl_off_h[pl] != r * d.dh - d.ph || coff * d.sw + p.pl_off_w[pl] != s * d.dw - d.pw)
-            fail(nm, op, "a tap reads the wrong source pixel");
-        } else {
-          const int nh = p.ph_off_h[ph] + d.ph - r * d.dh, nw = p.ph_off_w[ph] + d.pw - s * d.dw;
-          if (nh % d.sh != 0 || nw % d.sw != 0 || roff + p.pl_off_h[0] != nh / d.sh ||
-              coff + p.pl_off_w[0] != nw / d.sw)
-            fail(nm, op, "a tap reads the wrong dy pixel");
-        }
+        const int pl = p.tap_plane[t];
+        for (int e = 0; e < p.EL && !bad; ++e)
+          for (int f = 0; f < p.WL; ++f) {
+            const int oh = e * p.ph_step_h + p.ph_off_h[ph], ow = f * p.ph_step_w + p.ph_off_w[ph];
+            if (oh < 0 || oh >= p.Hd || ow < 0 || ow >= p.Wd) continue;  // not an output
+            const long long L = (long long)e * p.WL + f + p.tap_off[t];
+            const long long es = L / p.WL, fs = L % p.WL;
+            if (es >= p.EL) {  // the kernel would read the next image's rows
+              fail(nm, op, "a tap reads past its image in the linear space");
+              bad = true;
+              break;
+            }
+            const long long kh = es * p.pl_step_h + p.pl_off_h[pl], kw = fs * p.pl_step_w + p.pl_off_w[pl];
+            long long dh, dwc;
+            if (fwd) {
+              dh = (long long)oh * d.sh - d.ph + r * d.dh;
+              dwc = (long long)ow * d.sw - d.pw + s * d.dw;
+            } else {
+              const int nh = oh + d.ph - r * d.dh, nw = ow + d.pw - s * d.dw;
+              if (((nh % d.sh) + d.sh) % d.sh != 0 || ((nw % d.sw) + d.sw) % d.sw != 0) {
+                fail(nm, op, "a tap sits in a phase whose outputs it does not reach");
+                bad = true;
+                break;
+              }
+              dh = floor_div(nh, d.sh);
+              dwc = floor_div(nw, d.sw);
+            }
+            if (kh != dh || kw != dwc) {
+              fail(nm, op, fwd ? "a tap reads the wrong source pixel" : "a tap reads the wrong dy pixel");
+              bad = true;
+              break;
+            }
+          }
       }
   }
   for (size_t i = 0; i < seen.size(); ++i)
@@ -334,6 +358,74 @@ int main() {
     check_phases(s.nm, d, di, plans);
   }
   check_phase_choice(plans);
+  // seeded random descriptors: every op plans (or is refused as documented) and meets the
+  // same invariants and definition checks
+  {
+    unsigned long long st = 0x9E3779B97F4A7C15ull;
+    auto rnd = [&](int lo, int hi) {  // inclusive, splitmix64
+      st += 0x9E3779B97F4A7C15ull;
+      unsigned long long z = st;
+      z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+      z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+      z ^= z >> 31;
+      return lo + (int)(z % (unsigned long long)(hi - lo + 1));
+    };
+    int drawn = 0;
+    while (drawn < 400) {
+      Desc t{};
+      t.N = rnd(1, 8);
+      t.R = rnd(1, 7);
+      t.S = rnd(1, 7);
+      t.dh = rnd(1, 3) == 3 ? rnd(2, 3) : 1;
+      t.dw = rnd(1, 3) == 3 ? rnd(2, 3) : 1;
+      t.sh = rnd(1, 3);
+      t.sw = rnd(1, 3);
+      t.ph = rnd(0, t.R / 2 + 1);
+      t.pw = rnd(0, t.S / 2 + 1);
+      t.H = rnd(t.dh * (t.R - 1) + 1, 40);
+      t.W = rnd(t.dw * (t.S - 1) + 1, 40);
+      const int g = rnd(1, 4) == 4 ? rnd(2, 4) : 1;
+      t.C = g * rnd(1, 48);
+      t.K = g * rnd(1, 64);
+      t.dt = rnd(0, 1);
+      t.P = out_dim(t.H, t.ph, t.dh * (t.R - 1) + 1, t.sh);
+      t.Q = out_dim(t.W, t.pw, t.dw * (t.S - 1) + 1, t.sw);
+      if (t.P < 1 || t.Q < 1 || validate(t) != CONV2D_OK) continue;
+      Desc d;
+      if (group_desc(t, g, d) != CONV2D_OK) continue;
+      ++drawn;
+      char nm[96];
+      std::snprintf(nm, sizeof nm, "rand%d[%d,%d,%dx%d,%d,%dx%d,p%d%d,s%d%d,d%d%d,g%d,%s]", drawn, t.N, t.C, t.H, t.W,
+                    t.K, t.R, t.S, t.ph, t.pw, t.sh, t.sw, t.dh, t.dw, g, t.dt ? "bf16" : "f32");
+      void* px = (void*)0x100000;
+      void* pw = (void*)0x200000;
+      void* py = (void*)0x300000;
+      void* ws = (void*)0x400000;
+      for (int op = 0; op < 2; ++op) {
+        TapSet set;
+        const int rc = op == 0 ? build_tap_set(CONV2D_OP_FWD, d, px, pw, py, ws, di, set)
+                               : build_tap_set(CONV2D_OP_BWD_DATA, d, py, pw, px, ws, di, set);
+        if (rc != CONV2D_OK) {
+          fail(nm, op == 0 ? "fwd" : "bwd_data", "no plan");
+          continue;
+        }
+        for (const TapBuild& b : set.pass) {
+          check_tap(nm, op == 0 ? "fwd" : "bwd_data", b, di);
+          ++plans;
+        }
+        check_tap_semantics(nm, op == 0 ? "fwd" : "bwd_data", d, set, op == 0);
+      }
+      WgradBuild bw;
+      const int rcw = build_bwd_filter(d, px, py, pw, ws, di, bw);
+      if (rcw != CONV2D_OK) {
+        fail(nm, "bwd_filter", "no plan");
+      } else {
+        check_wgrad(nm, d, bw, di);
+        ++plans;
+      }
+      check_phases(nm, d, di, plans);
+    }
+  }
   std::printf("checked %d plans, %d violations\n", plans, g_fail);
   return g_fail > 100 ? 100 : g_fail;
 }
