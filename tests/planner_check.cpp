@@ -117,6 +117,30 @@ void check_tap_semantics(const char* nm, const char* op, const Desc& d, const Ta
 void check_wgrad(const char* nm, const Desc& d, const WgradBuild& b, const DevInfo& di) {
   const char* op = "bwd_filter";
   const WgradPlan& p = b.p;
+  // Every tap pairs dy at each output (e, f) with the x pixel the definition names
+  // (e*sh - ph + r*dh, f*sw - pw + s*dw): x is read at linear e*WL + f + tap offset of the
+  // tap's plane, without leaving the image; row-tap sharing shifts dy by j * tru_step rows
+  // for filter row r0 + j, which needs offset(r0 + j) - offset(r0) = j * tru_step * WL.
+  // (1x1 problems are planned on their flattened descriptor, one row of H*W pixels.)
+  const Desc dd = flatten_pointwise(d);
+  for (int r = 0; r < d.R; ++r)
+    for (int s2 = 0; s2 < d.S; ++s2) {
+      const int t = r * d.S + s2, pl = p.tap_plane[t];
+      bool bad = false;
+      for (int e = 0; e < dd.P && !bad; ++e)
+        for (int f = 0; f < dd.Q; ++f) {
+          const long long L = (long long)e * p.WL + f + p.tap_off[t];
+          const long long es = L / p.WL, fs = L % p.WL;
+          if (es >= p.EL || es * p.pl_step_h + p.pl_off_h[pl] != (long long)e * dd.sh - dd.ph + r * dd.dh ||
+              fs * p.pl_step_w + p.pl_off_w[pl] != (long long)f * dd.sw - dd.pw + s2 * dd.dw) {
+            fail(nm, op, "a tap pairs dy with the wrong x pixel");
+            bad = true;
+            break;
+          }
+        }
+      if (p.TRU > 1 && r > 0 && p.tap_off[t] - p.tap_off[t - d.S] != p.tru_step * p.WL)
+        fail(nm, op, "row-tap sharing: consecutive filter rows are not tru_step linear rows apart");
+    }
   if (wgrad_smem_bytes(p, d.dt) > di.smem_optin) fail(nm, op, "shared memory over budget");
   if (128 + p.accb * p.G * p.TRU * p.NK > p.tmem_cols || p.tmem_cols > 512) fail(nm, op, "TMEM over budget");
   if (p.use_tma != 1 && p.rlen < p.stages * p.KB + p.max_off + 4) fail(nm, op, "slot ring shorter than the positions in flight");
