@@ -2,8 +2,10 @@
 """Benchmark: conv2d TFLOP/s per op (forward / backward-data / backward-filter) on GB300.
 
 One step = the whole hot path once: forward, backward-data and backward-filter of the
-workload (default: the ResNet-style 3x3 layer, fp32 tensors on TF32 tensor cores,
-N=32 C=K=64 H=W=56 pad 1 stride 1) on seeded synthetic inputs already resident in HBM.
+workload (default: the largest of the five by FLOP, the bf16 deconvolution layer: deconv
+input [32,512,16,16] -> output [32,256,32,32], weight [512,256,4,4], stride 2, pad 1) on
+seeded synthetic inputs already resident in HBM.  Every workload's three ops are also
+timed alone (the per_config block).
 Each op is timed with CUDA events on the launching stream; L2 is flushed (a write of
 twice the L2 size) before every op, outside the events.  FLOP per op = 2*N*K*P*Q*C*R*S.
 
@@ -30,7 +32,9 @@ sys.path.insert(0, ROOT)
 
 METRIC = "conv2d TFLOP/s per op (fwd/dgrad/wgrad) and % of GB300 tensor-core peak"
 OPS = ("fwd", "bwd_data", "bwd_filter")
-KERNELS_PER_OP = 2  # forward/backward-data: filter pack + main; backward-filter: main + split reduce
+# The headline workload: the largest of the five by FLOP per op (the bf16 deconvolution layer,
+# 3.44e10); every workload is timed in the line's per_config block.
+DEFAULT_WORKLOAD = "deconv"
 # Fallback peaks (used only if MEASURED_PEAKS.json is absent): one earlier GB300 measurement.
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 NOMINAL_TF32_OVER_BF16 = 1.1 / 2.25
@@ -42,7 +46,8 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--workload", default="resnet3x3")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--config-reps", type=int, default=30)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=20)
     return ap.parse_args()
@@ -157,203 +162,169 @@ def job_tflops(flop_per_op, n_ops, world, step_ms):
     return world * n_ops * flop_per_op / (step_ms * 1e-3) / 1e12
 
 
-def run_ours(args, rank, world):
+def _device_case(wl, dev):
+    """Seeded inputs of a workload on the device, its outputs and one workspace for all three ops."""
     import torch
     import convolution_nchw_conv2d_gb300 as cg
     from convolution_nchw_conv2d_gb300 import workloads as W
-
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=dev)
-    wl = W.WORKLOADS[args.workload]
     pb = wl.problem
     x, w, dy = W.make_inputs(wl)
-    xd, wd, dyd = x.to(dev), w.to(dev), dy.to(dev)
-    pad, st = (pb.pad_h, pb.pad_w), (pb.stride_h, pb.stride_w)
-    y = torch.empty(pb.y_shape, dtype=x.dtype, device=dev)
-    dx = torch.empty(pb.x_shape, dtype=x.dtype, device=dev)
-    dw = torch.empty(pb.w_shape, dtype=x.dtype, device=dev)
+    c = {"pb": pb, "host": (x, w, dy), "x": x.to(dev), "w": w.to(dev), "dy": dy.to(dev),
+         "y": torch.empty(pb.y_shape, dtype=x.dtype, device=dev),
+         "dx": torch.empty(pb.x_shape, dtype=x.dtype, device=dev),
+         "dw": torch.empty(pb.w_shape, dtype=x.dtype, device=dev)}
     dt = 0 if pb.dtype == "f32" else 1
     wsz = max(cg.conv2d_workspace_size(op, pb.dims(), dt) for op in range(3))
-    ws = torch.empty(max(wsz, 16), dtype=torch.uint8, device=dev)
-    stream = torch.cuda.current_stream()
+    c["ws"] = torch.empty(max(wsz, 16), dtype=torch.uint8, device=dev)
+    return c
 
-    def op_call(op):
-        if op == "fwd":
-            cg.conv2d_fwd(xd, wd, pad, st, out=y, workspace=ws, stream=stream)
-        elif op == "bwd_data":
-            cg.conv2d_bwd_data(dyd, wd, (pb.H, pb.W), pad, st, out=dx, workspace=ws, stream=stream)
-        else:
-            cg.conv2d_bwd_filter(xd, dyd, (pb.R, pb.S), pad, st, out=dw, workspace=ws, stream=stream)
 
-    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    flush = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
+def _op_call(c, op, stream):
+    import convolution_nchw_conv2d_gb300 as cg
+    pb = c["pb"]
+    pad, st = (pb.pad_h, pb.pad_w), (pb.stride_h, pb.stride_w)
+    if op == "fwd":
+        cg.conv2d_fwd(c["x"], c["w"], pad, st, out=c["y"], workspace=c["ws"], stream=stream)
+    elif op == "bwd_data":
+        cg.conv2d_bwd_data(c["dy"], c["w"], (pb.H, pb.W), pad, st, out=c["dx"], workspace=c["ws"], stream=stream)
+    else:
+        cg.conv2d_bwd_filter(c["x"], c["dy"], (pb.R, pb.S), pad, st, out=c["dw"], workspace=c["ws"], stream=stream)
 
-    for _ in range(args.warmup):
-        for op in OPS:
-            flush.zero_()
-            op_call(op)
-    cg.conv2d_device_status(stream)
 
-    K = args.steps
-    evs = {op: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                for _ in range(K)] for op in OPS}
-    sampler = ClockSampler(local)
-    time.sleep(0.3)
+def _time_call(fn, flush, stream, reps, warmup):
+    """Mean device time (ms) of fn over `reps` calls, CUDA events on `stream` around each call;
+    L2 flushed (a write of twice its size) before every call, outside the events."""
+    import torch
+    for _ in range(warmup):
+        flush.zero_()
+        fn()
+    pairs = []
+    for _ in range(reps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        pairs.append((a, b))
     torch.cuda.synchronize()
-    if world > 1:
-        torch.distributed.barrier()
-    t0 = time.time()
-    for i in range(K):
-        for op in OPS:
-            flush.zero_()
-            a, b = evs[op][i]
-            a.record(stream)
-            op_call(op)
-            b.record(stream)
-    torch.cuda.synchronize()
-    if world > 1:
-        torch.distributed.barrier()
-    t1 = time.time()
-    clocks = sampler.stop(t0, t1)
-    cg.conv2d_device_status(stream)
-    op_ms = {op: sum(a.elapsed_time(b) for a, b in evs[op]) / K for op in OPS}
-    step_ms = sum(op_ms.values())
-    step_ms = slowest_rank_ms(step_ms, world, dev)
+    return sum(a.elapsed_time(b) for a, b in pairs) / len(pairs)
 
-    # ---- fused epilogues (bias + add-to on forward, bias gradients on backward-filter),
-    # timed like the step's ops but outside it
+
+def _roofline_of(pb, op_ms, peaks):
+    """Per-op throughput and fractions of the tensor and HBM peaks; the dominant (slowest) op
+    against whichever roof bounds it (tensor when its arithmetic intensity is past the ridge)."""
+    tc_peak = peaks["bf16_tflops"] * (NOMINAL_TF32_OVER_BF16 if pb.dtype == "f32" else 1.0)
+    flop = pb.flops()
+    per_op = {}
+    for op in OPS:
+        tf = flop / (op_ms[op] * 1e-3) / 1e12
+        gbs = pb.alg_bytes(op) / (op_ms[op] * 1e-3) / 1e9
+        per_op[op] = {"ms": round(op_ms[op], 5), "tflops": round(tf, 2),
+                      "frac_tc_peak": round(tf / tc_peak, 4), "alg_gbs": round(gbs, 1),
+                      "frac_hbm_peak": round(gbs / peaks["hbm_gbs"], 4)}
+    dom = max(OPS, key=lambda o: op_ms[o])
+    ai = flop / pb.alg_bytes(dom)
+    if ai * peaks["hbm_gbs"] * 1e9 < tc_peak * 1e12:
+        roof = {"bound": "hbm", "achieved": per_op[dom]["alg_gbs"], "peak": peaks["hbm_gbs"], "unit": "GB/s"}
+    else:
+        roof = {"bound": "tensor", "achieved": per_op[dom]["tflops"], "peak": round(tc_peak, 1), "unit": "TFLOP/s"}
+    roof["frac"] = round(roof["achieved"] / roof["peak"], 4)
+    roof["kernel"] = dom
+    return per_op, roof
+
+
+def _extras_resnet(c, flush, stream, reps, warmup, op_ms):
+    """Timings of the extended entry points on the ResNet 3x3 layer: the fused epilogues (bias +
+    add-to on the forward op, both bias gradients on backward-filter), dilation 2, groups 2."""
+    import torch
+    import convolution_nchw_conv2d_gb300 as cg
+    pb = c["pb"]
+    dev = c["x"].device
+    pad, st = (pb.pad_h, pb.pad_w), (pb.stride_h, pb.stride_w)
+    dt = 0 if pb.dtype == "f32" else 1
+    x, w, dy, y, dx, dw, ws = c["x"], c["w"], c["dy"], c["y"], c["dx"], c["dw"], c["ws"]
     bias_k = torch.randn(pb.K, generator=torch.Generator().manual_seed(5)).to(x.dtype).to(dev)
     dbk = torch.empty(pb.K, dtype=x.dtype, device=dev)
     dbc = torch.empty(pb.C, dtype=x.dtype, device=dev)
     wsz_f = cg.conv2d_workspace_size(2, pb.dims(), dt)
-    wsz_d = cg.conv2d_workspace_size(2, (pb.N, pb.C, pb.H, pb.W, pb.K, pb.R, pb.S, 2 * pb.pad_h, 2 * pb.pad_w,
+    ws_f = torch.empty(max(wsz_f, 16), dtype=torch.uint8, device=dev) if wsz_f > ws.numel() else ws
+    ex_ms = {
+        "fwd_bias_addto": _time_call(lambda: cg.conv2d_fwd(x, w, pad, st, out=y, workspace=ws, stream=stream,
+                                                           bias=bias_k, beta=1.0), flush, stream, reps, warmup),
+        "bwd_filter_with_bias_grads": _time_call(
+            lambda: cg.conv2d_bwd_filter(x, dy, (pb.R, pb.S), pad, st, out=dw, workspace=ws_f, stream=stream,
+                                         db_k=dbk, db_c=dbc), flush, stream, reps, warmup)}
+    extra_ms = ex_ms["bwd_filter_with_bias_grads"] - op_ms["bwd_filter"]
+    sum_bytes = (math.prod(pb.y_shape) + math.prod(pb.x_shape)) * pb.elem_bytes()  # dy and x read once
+    fused = {"fwd_bias_addto_ms": round(ex_ms["fwd_bias_addto"], 5), "fwd_ms": round(op_ms["fwd"], 5),
+             "bwd_filter_with_bias_grads_ms": round(ex_ms["bwd_filter_with_bias_grads"], 5),
+             "bwd_filter_ms": round(op_ms["bwd_filter"], 5), "bias_grads_extra_ms": round(extra_ms, 5),
+             "bias_grads_alg_gbs": round(sum_bytes / (extra_ms * 1e-3) / 1e9, 1) if extra_ms > 0 else None,
+             "note": "bias gradients = channel sums of dy (per k) and x (per c); alg bytes = |dy| + |x|"}
+    # dilation 2 on the same layer (pad 2 keeps P = H, Q = W, same FLOP)
+    pad2 = (2 * pb.pad_h, 2 * pb.pad_w)
+    wsz_d = cg.conv2d_workspace_size(2, (pb.N, pb.C, pb.H, pb.W, pb.K, pb.R, pb.S, pad2[0], pad2[1],
                                          pb.stride_h, pb.stride_w, pb.P, pb.Q), dt, (2, 2))
     ws_d = torch.empty(max(wsz_d, 16), dtype=torch.uint8, device=dev)
-    ws_f = torch.empty(max(wsz_f, 16), dtype=torch.uint8, device=dev) if wsz_f > ws.numel() else ws
-
-    def ex_call(which):
-        if which == "fwd_bias_addto":
-            cg.conv2d_fwd(xd, wd, pad, st, out=y, workspace=ws, stream=stream, bias=bias_k, beta=1.0)
-        else:
-            cg.conv2d_bwd_filter(xd, dyd, (pb.R, pb.S), pad, st, out=dw, workspace=ws_f, stream=stream,
-                                 db_k=dbk, db_c=dbc)
-
-    ex_ms = {}
-    for which in ("fwd_bias_addto", "bwd_filter_with_bias_grads"):
-        for _ in range(args.warmup):
-            flush.zero_()
-            ex_call(which)
-        pairs = []
-        for _ in range(min(K, 50)):
-            flush.zero_()
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record(stream)
-            ex_call(which)
-            b.record(stream)
-            pairs.append((a, b))
-        torch.cuda.synchronize()
-        ex_ms[which] = sum(a.elapsed_time(b) for a, b in pairs) / len(pairs)
-    cg.conv2d_device_status(stream)
-    # dilation 2 on the same layer (pad 2 keeps P = H, Q = W): the three ops, timed alike
-    dil_ms = {}
+    dcalls = {"fwd": lambda: cg.conv2d_fwd(x, w, pad2, st, out=y, workspace=ws, stream=stream, dilation=2),
+              "bwd_data": lambda: cg.conv2d_bwd_data(dy, w, (pb.H, pb.W), pad2, st, out=dx, workspace=ws,
+                                                     stream=stream, dilation=2),
+              "bwd_filter": lambda: cg.conv2d_bwd_filter(x, dy, (pb.R, pb.S), pad2, st, out=dw, workspace=ws_d,
+                                                         stream=stream, dilation=2)}
+    dilated = {}
     for op in OPS:
-        def dcall():
-            if op == "fwd":
-                cg.conv2d_fwd(xd, wd, (2 * pb.pad_h, 2 * pb.pad_w), st, out=y, workspace=ws, stream=stream,
-                              dilation=2)
-            elif op == "bwd_data":
-                cg.conv2d_bwd_data(dyd, wd, (pb.H, pb.W), (2 * pb.pad_h, 2 * pb.pad_w), st, out=dx, workspace=ws,
-                                   stream=stream, dilation=2)
-            else:
-                cg.conv2d_bwd_filter(xd, dyd, (pb.R, pb.S), (2 * pb.pad_h, 2 * pb.pad_w), st, out=dw,
-                                     workspace=ws_d, stream=stream, dilation=2)
-        for _ in range(args.warmup):
-            flush.zero_()
-            dcall()
-        pairs = []
-        for _ in range(min(K, 50)):
-            flush.zero_()
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record(stream)
-            dcall()
-            b.record(stream)
-            pairs.append((a, b))
-        torch.cuda.synchronize()
-        dil_ms[op] = sum(a.elapsed_time(b) for a, b in pairs) / len(pairs)
-    cg.conv2d_device_status(stream)
-    dilated = {op: {"ms": round(dil_ms[op], 5), "tflops": round(pb.flops() / (dil_ms[op] * 1e-3) / 1e12, 2)}
-               for op in OPS}
+        ms = _time_call(dcalls[op], flush, stream, reps, warmup)
+        dilated[op] = {"ms": round(ms, 5), "tflops": round(pb.flops() / (ms * 1e-3) / 1e12, 2)}
     dilated["note"] = "same layer with dilation 2 and pad 2 (P, Q unchanged, same FLOP)"
-
     # groups 2 on the same layer (two independent 32 -> 32 channel convolutions: half the FLOP)
-    wg2 = wd[:, : pb.C // 2].contiguous()
+    wg2 = w[:, : pb.C // 2].contiguous()
     wsz_g = max(cg.conv2d_workspace_size(op, pb.dims(), dt, (1, 1), 2) for op in range(3))
     ws_g = torch.empty(max(wsz_g, 16), dtype=torch.uint8, device=dev)
     dwg = torch.empty_like(wg2)
-    grp_ms = {}
+    gcalls = {"fwd": lambda: cg.conv2d_fwd(x, wg2, pad, st, out=y, workspace=ws_g, stream=stream, groups=2),
+              "bwd_data": lambda: cg.conv2d_bwd_data(dy, wg2, (pb.H, pb.W), pad, st, out=dx, workspace=ws_g,
+                                                     stream=stream, groups=2),
+              "bwd_filter": lambda: cg.conv2d_bwd_filter(x, dy, (pb.R, pb.S), pad, st, out=dwg, workspace=ws_g,
+                                                         stream=stream, groups=2)}
+    grouped = {}
     for op in OPS:
-        def gcall():
-            if op == "fwd":
-                cg.conv2d_fwd(xd, wg2, pad, st, out=y, workspace=ws_g, stream=stream, groups=2)
-            elif op == "bwd_data":
-                cg.conv2d_bwd_data(dyd, wg2, (pb.H, pb.W), pad, st, out=dx, workspace=ws_g, stream=stream, groups=2)
-            else:
-                cg.conv2d_bwd_filter(xd, dyd, (pb.R, pb.S), pad, st, out=dwg, workspace=ws_g, stream=stream, groups=2)
-        for _ in range(args.warmup):
-            flush.zero_()
-            gcall()
-        pairs = []
-        for _ in range(min(K, 50)):
-            flush.zero_()
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record(stream)
-            gcall()
-            b.record(stream)
-            pairs.append((a, b))
-        torch.cuda.synchronize()
-        grp_ms[op] = sum(a.elapsed_time(b) for a, b in pairs) / len(pairs)
-    cg.conv2d_device_status(stream)
-    grouped = {op: {"ms": round(grp_ms[op], 5), "tflops": round(pb.flops() / 2 / (grp_ms[op] * 1e-3) / 1e12, 2)}
-               for op in OPS}
+        ms = _time_call(gcalls[op], flush, stream, reps, warmup)
+        grouped[op] = {"ms": round(ms, 5), "tflops": round(pb.flops() / 2 / (ms * 1e-3) / 1e12, 2)}
     grouped["note"] = "same layer with groups 2 (C/2 -> K/2 per group, half the FLOP)"
+    cg.conv2d_device_status(stream)
+    return fused, dilated, grouped
 
-    extra_ms = ex_ms["bwd_filter_with_bias_grads"] - op_ms["bwd_filter"]
-    sum_bytes = (math.prod(pb.y_shape) + math.prod(pb.x_shape)) * pb.elem_bytes()  # dy and x read once
-    fused = {"fwd_bias_addto_ms": round(ex_ms["fwd_bias_addto"], 5),
-             "fwd_ms": round(op_ms["fwd"], 5),
-             "bwd_filter_with_bias_grads_ms": round(ex_ms["bwd_filter_with_bias_grads"], 5),
-             "bwd_filter_ms": round(op_ms["bwd_filter"], 5),
-             "bias_grads_extra_ms": round(extra_ms, 5),
-             "bias_grads_alg_gbs": round(sum_bytes / (extra_ms * 1e-3) / 1e9, 1) if extra_ms > 0 else None,
-             "note": "bias gradients = channel sums of dy (per k) and x (per c); alg bytes = |dy| + |x|"}
 
-    # ---- end to end: pinned host inputs -> device -> three ops -> host results, every step.
-    # Steps are pipelined over three streams with two device buffer sets: step i's input
-    # copies (stream s_in) overlap step i-1's ops (the compute stream) and step i-2's result
-    # copies (stream s_out); events order each buffer's reuse.  The timed region spans the
-    # first input copy to the last result copy; e2e = whole-run throughput.
+def _e2e(c, flush, stream, nsteps):
+    """End to end through the public API: pinned host inputs -> device -> three ops -> host
+    results, every step.  Steps are pipelined over three streams with two device buffer sets:
+    step i's input copies (stream s_in) overlap step i-1's ops (the compute stream) and step
+    i-2's result copies (stream s_out); events order each buffer's reuse.  The timed region
+    spans the first input copy to the last result copy.  Returns ms per step."""
+    import torch
+    import convolution_nchw_conv2d_gb300 as cg
+    pb = c["pb"]
+    dev = c["x"].device
+    pad, st = (pb.pad_h, pb.pad_w), (pb.stride_h, pb.stride_w)
+    x, w, dy = c["host"]
     xh, wh, dyh = x.pin_memory(), w.pin_memory(), dy.pin_memory()
-    E = max(1, args.e2e_steps)
+    ws = c["ws"]
     s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
     bufs = []
     for _ in range(2):
-        bufs.append({"x": torch.empty_like(xd), "w": torch.empty_like(wd), "dy": torch.empty_like(dyd),
-                     "y": torch.empty_like(y), "dx": torch.empty_like(dx), "dw": torch.empty_like(dw),
+        bufs.append({"x": torch.empty_like(c["x"]), "w": torch.empty_like(c["w"]), "dy": torch.empty_like(c["dy"]),
+                     "y": torch.empty_like(c["y"]), "dx": torch.empty_like(c["dx"]), "dw": torch.empty_like(c["dw"]),
                      "yh": torch.empty(pb.y_shape, dtype=x.dtype).pin_memory(),
                      "dxh": torch.empty(pb.x_shape, dtype=x.dtype).pin_memory(),
                      "dwh": torch.empty(pb.w_shape, dtype=x.dtype).pin_memory()})
 
-    def e2e_run(nsteps):
-        ev_cmp = [torch.cuda.Event() for _ in range(nsteps)]
-        ev_in = [torch.cuda.Event() for _ in range(nsteps)]
-        ev_out = [torch.cuda.Event() for _ in range(nsteps)]
+    def run(n):
+        ev_cmp = [torch.cuda.Event() for _ in range(n)]
+        ev_in = [torch.cuda.Event() for _ in range(n)]
+        ev_out = [torch.cuda.Event() for _ in range(n)]
         t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         t0.record(s_in)
-        for i in range(nsteps):
+        for i in range(n):
             bb = bufs[i % 2]
             with torch.cuda.stream(s_in):
                 if i >= 2:
@@ -379,37 +350,102 @@ def run_ours(args, rank, world):
                 bb["dxh"].copy_(bb["dx"], non_blocking=True)
                 bb["dwh"].copy_(bb["dw"], non_blocking=True)
                 ev_out[i].record(s_out)
-        s_out.wait_event(ev_out[nsteps - 1])
+        s_out.wait_event(ev_out[n - 1])
         t1.record(s_out)
         torch.cuda.synchronize()
         return t0.elapsed_time(t1)
 
-    e2e_run(2)  # warm-up of the streams and buffers
-    e2e_ms = e2e_run(E) / E
+    run(2)  # warm-up of the streams and buffers
+    return run(nsteps) / nsteps
+
+
+def run_ours(args, rank, world):
+    import torch
+    import convolution_nchw_conv2d_gb300 as cg
+    from convolution_nchw_conv2d_gb300 import workloads as W
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    peaks = load_peaks()
+    stream = torch.cuda.current_stream()
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
+
+    wl = W.WORKLOADS[args.workload]
+    pb = wl.problem
+    head = _device_case(wl, dev)
+    for _ in range(args.warmup):
+        for op in OPS:
+            flush.zero_()
+            _op_call(head, op, stream)
+    cg.conv2d_device_status(stream)
+
+    # ---- the timed steps: fwd + bwd_data + bwd_filter of the headline workload, L2 flushed
+    # before every op outside its events
+    K = args.steps
+    evs = {op: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                for _ in range(K)] for op in OPS}
+    sampler = ClockSampler(local)
+    time.sleep(0.3)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    launches0 = cg.conv2d_kernel_launches()
+    t0 = time.time()
+    for i in range(K):
+        for op in OPS:
+            flush.zero_()
+            a, b = evs[op][i]
+            a.record(stream)
+            _op_call(head, op, stream)
+            b.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    t1 = time.time()
+    launches = cg.conv2d_kernel_launches() - launches0
+    clocks = sampler.stop(t0, t1)
+    cg.conv2d_device_status(stream)
+    op_ms = {op: sum(a.elapsed_time(b) for a, b in evs[op]) / K for op in OPS}
+    step_ms = slowest_rank_ms(sum(op_ms.values()), world, dev)
+    per_op, roof = _roofline_of(pb, op_ms, peaks)
+    roof["traffic"] = ncu_traffic(wl.name, roof["kernel"])
+    roof["peak_source"] = peaks["source"] + (" (bf16 x nominal tf32/bf16 ratio)" if pb.dtype == "f32" else "")
+
+    # ---- every workload, each op timed alone the same way (the headline one included again)
+    reps = max(1, min(args.config_reps, K))
+    per_config = {}
+    for name, wlc in W.WORKLOADS.items():
+        c = head if name == wl.name else _device_case(wlc, dev)
+        ms = {op: _time_call(lambda: _op_call(c, op, stream), flush, stream, reps, args.warmup) for op in OPS}
+        cg.conv2d_device_status(stream)
+        po, rf = _roofline_of(wlc.problem, ms, peaks)
+        per_config[name] = {"shape": wlc.description, "dtype": "tf32" if wlc.problem.dtype == "f32" else "bf16",
+                            "flop_per_op": wlc.problem.flops(), "alg_bytes_per_op": wlc.problem.alg_bytes("fwd"),
+                            "per_op": po, "dominant": rf,
+                            "step_tflops": round(3 * wlc.problem.flops() / (sum(ms.values()) * 1e-3) / 1e12, 2)}
+        if c is not head:
+            del c
+    per_config["note"] = (f"each op timed alone ({reps} calls after {args.warmup} warm-up calls, L2 flushed before "
+                          "every call); tensor peak TF32 for fp32 workloads, BF16 for bf16; the dominant op against "
+                          "its roof (tensor or HBM by arithmetic intensity)")
+
+    extras = {}
+    if "resnet3x3" in W.WORKLOADS:
+        rc = head if wl.name == "resnet3x3" else _device_case(W.WORKLOADS["resnet3x3"], dev)
+        rms = per_config["resnet3x3"]["per_op"]
+        fused, dilated, grouped = _extras_resnet(rc, flush, stream, reps, args.warmup,
+                                                 {op: rms[op]["ms"] for op in OPS})
+        extras = {"fused_epilogue": fused, "dilation_2": dilated, "groups_2": grouped}
+
+    e2e_ms = _e2e(head, flush, stream, max(1, args.e2e_steps))
     esz = pb.elem_bytes()
     nx, ny, nw = (math.prod(pb.x_shape), math.prod(pb.y_shape), math.prod(pb.w_shape))
     flop = pb.flops()
-
-    peaks = load_peaks()
-    tc_peak = peaks["bf16_tflops"] * (NOMINAL_TF32_OVER_BF16 if pb.dtype == "f32" else 1.0)
-    per_op = {}
-    for op in OPS:
-        tf = flop / (op_ms[op] * 1e-3) / 1e12
-        gbs = pb.alg_bytes(op) / (op_ms[op] * 1e-3) / 1e9
-        per_op[op] = {"ms": round(op_ms[op], 5), "tflops": round(tf, 2),
-                      "frac_tc_peak": round(tf / tc_peak, 4), "alg_gbs": round(gbs, 1),
-                      "frac_hbm_peak": round(gbs / peaks["hbm_gbs"], 4)}
-    dom = max(OPS, key=lambda o: op_ms[o])
-    ai = flop / pb.alg_bytes(dom)
-    if ai * peaks["hbm_gbs"] * 1e9 < tc_peak * 1e12:
-        roof = {"bound": "hbm", "achieved": per_op[dom]["alg_gbs"], "peak": peaks["hbm_gbs"], "unit": "GB/s"}
-    else:
-        roof = {"bound": "tensor", "achieved": per_op[dom]["tflops"], "peak": round(tc_peak, 1), "unit": "TFLOP/s"}
-    roof["frac"] = round(roof["achieved"] / roof["peak"], 4)
-    roof["traffic"] = ncu_traffic(args.workload, dom)
-    roof["kernel"] = dom
-    roof["peak_source"] = peaks["source"] + (" (bf16 x nominal tf32/bf16 ratio)" if pb.dtype == "f32" else "")
-
     value = job_tflops(flop, len(OPS), world, step_ms)
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world,
@@ -428,12 +464,11 @@ def run_ours(args, rank, world):
                 "ms_per_step": round(e2e_ms, 4),
                 "pipelined": "input copies, ops and result copies of consecutive steps overlap "
                              "on three streams (two device buffer sets)"},
-        "gpu_launches": K * len(OPS) * KERNELS_PER_OP,
-        "fused_epilogue": fused,
-        "dilation_2": dilated,
-        "groups_2": grouped,
+        "gpu_launches": launches,
+        "per_config": per_config,
         "clocks": clocks,
     }
+    line.update(extras)
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, seconds=12.0)
     if world > 1:

@@ -22,6 +22,7 @@ __all__ = [
     "conv2d_fwd", "conv2d_bwd_data", "conv2d_bwd_filter", "deconv2d_fwd", "conv2d_fwd_noalloc",
     "conv1d_fwd", "conv1d_bwd_data", "conv1d_bwd_filter", "MODE_CROSS_CORRELATION", "MODE_CONVOLUTION",
     "conv2d_workspace_size", "conv2d_output_dim", "conv2d_device_status", "conv2d_strerror",
+    "conv2d_kernel_launches",
     "Conv2dError", "lib_path", "load_library", "OP_FWD", "OP_BWD_DATA", "OP_BWD_FILTER",
     "DTYPE_F32", "DTYPE_BF16",
 ]
@@ -48,7 +49,7 @@ def lib_path() -> str:
 
 EXPORTS = ("conv2d_output_dim", "conv2d_workspace_size", "conv2d_workspace_size_ex", "conv2d_fwd", "conv2d_bwd_data",
            "conv2d_bwd_filter", "conv2d_fwd_ex", "conv2d_bwd_data_ex", "conv2d_bwd_filter_ex",
-           "conv2d_fwd_noalloc", "conv2d_device_status", "conv2d_strerror")
+           "conv2d_fwd_noalloc", "conv2d_device_status", "conv2d_strerror", "conv2d_kernel_launches")
 
 
 def load_library():
@@ -83,6 +84,8 @@ def load_library():
         lib.conv2d_fwd_noalloc.restype = i
         lib.conv2d_device_status.argtypes = [vp]
         lib.conv2d_device_status.restype = i
+        lib.conv2d_kernel_launches.argtypes = []
+        lib.conv2d_kernel_launches.restype = ctypes.c_ulonglong
         lib.conv2d_strerror.argtypes = [i]
         lib.conv2d_strerror.restype = ctypes.c_char_p
         _lib = lib
@@ -351,6 +354,11 @@ def conv1d_bwd_filter(x, dy, s, pad=0, stride=1, out=None, workspace=None, strea
                            workspace=workspace, stream=stream, beta=beta, db_k=db_k, db_c=db_c, flip=flip,
                            dilation=(1, _one(dilation)))
     return dw.squeeze(2) if out is None else out
+
+
+def conv2d_kernel_launches() -> int:
+    """Kernels the library has enqueued in this process so far (diagnostic counter)."""
+    return int(load_library().conv2d_kernel_launches())
 
 
 def conv2d_device_status(stream=None) -> int:

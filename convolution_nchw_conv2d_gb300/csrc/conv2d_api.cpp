@@ -4,6 +4,7 @@
 #include "conv2d_gb300.h"
 
 #include <algorithm>
+#include <atomic>
 #include <climits>
 #include <cstdint>
 #include <cstring>
@@ -918,8 +919,15 @@ int check_ws(void* ws, size_t have, size_t need) {
   return CONV2D_OK;
 }
 
-int launch_err(cudaError_t e) {
-  if (e == cudaSuccess) return CONV2D_OK;
+// Kernels this library has enqueued since the process started (conv2d_kernel_launches).
+std::atomic<unsigned long long> g_launches{0};
+
+// Status of a launch helper that enqueued `kernels` kernels when it returned cudaSuccess.
+int launch_err(cudaError_t e, int kernels = 1) {
+  if (e == cudaSuccess) {
+    g_launches.fetch_add((unsigned long long)kernels, std::memory_order_relaxed);
+    return CONV2D_OK;
+  }
   cudaGetLastError();
   return CONV2D_ERR_LAUNCH;
 }
@@ -1353,7 +1361,7 @@ int conv2d_bwd_filter_ex(int N, int C, int H, int W, int K, int R, int S, int pa
   if (db_k != nullptr) {
     // conv bias gradient: sum of dy over images and output pixels, per output channel k
     const ChanSumPlan cp{dy, db_k, reinterpret_cast<float*>(wsb), d.N, d.K, (long long)d.P * d.Q, beta};
-    rc = launch_err(launch_chan_sum(cp, d.dt, st));
+    rc = launch_err(launch_chan_sum(cp, d.dt, st), 2);
     if (rc) return rc;
   }
   if (db_c != nullptr) {
@@ -1361,7 +1369,7 @@ int conv2d_bwd_filter_ex(int N, int C, int H, int W, int K, int R, int S, int pa
     // and pixels, per channel c
     const ChanSumPlan cp{x, db_c, reinterpret_cast<float*>(wsb + align_ws((size_t)d.K * d.N * sizeof(float))), d.N,
                          d.C, (long long)d.H * d.W, beta};
-    rc = launch_err(launch_chan_sum(cp, d.dt, st));
+    rc = launch_err(launch_chan_sum(cp, d.dt, st), 2);
     if (rc) return rc;
   }
   return CONV2D_OK;
@@ -1377,22 +1385,37 @@ int conv2d_fwd_noalloc(int N, int C, int H, int W, int K, int R, int S, int pad_
   if (rc) return rc;
   const DevInfo di = device_info();
   if (!di.ok) return CONV2D_ERR_DEVICE;
-  TapBuild b;
-  rc = build_fwd(d, x, w, y, nullptr, di, b);  // sizes the packed filter
-  if (rc) return rc;
-  if (b.pack_bytes > noalloc_scratch_capacity()) return CONV2D_ERR_NOALLOC_LIMIT;
   void* scratch = nullptr;
   if (noalloc_scratch_ptr(&scratch) != cudaSuccess) {
     cudaGetLastError();
     return CONV2D_ERR_DEVICE;
   }
-  b.p.wpack = scratch;
-  b.pp.wpack = scratch;
+  // The plan conv2d_fwd makes (one or more tap passes), with the scratch as its workspace.
+  TapSet set;
+  const PlanKey key = make_key(CONV2D_OP_FWD, d, x, w, y, scratch);
+  if (!g_tap_plans.get(key, set)) {
+    rc = build_tap_set(CONV2D_OP_FWD, d, x, w, y, scratch, di, set);
+    if (rc) return rc;
+    g_tap_plans.put(key, set);
+  }
+  if (set.pack_bytes > noalloc_scratch_capacity()) return CONV2D_ERR_NOALLOC_LIMIT;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  rc = launch_err(launch_pack_filter(b.pp, d.dt, st));
-  if (rc) return rc;
-  return launch_err(launch_tap_gemm(b.p, d.dt, b.grid, st));
+  for (size_t pi = 0; pi < set.pass.size(); ++pi) {
+    TapBuild& b = set.pass[pi];
+    b.p.beta = pi == 0 ? 0.f : 1.f;  // later passes add onto the output the first one wrote
+    b.p.bias = nullptr;
+    b.pp.flip = 0;
+    if (b.pack_bytes) {
+      rc = launch_err(launch_pack_filter(b.pp, d.dt, st));
+      if (rc) return rc;
+    }
+    rc = launch_err(launch_tap_gemm(b.p, d.dt, b.grid, st));
+    if (rc) return rc;
+  }
+  return CONV2D_OK;
 }
+
+unsigned long long conv2d_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
 
 int conv2d_device_status(void* stream) {
   cudaStream_t st = static_cast<cudaStream_t>(stream);

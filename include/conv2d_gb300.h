@@ -208,13 +208,14 @@ int conv2d_bwd_filter_ex(int N, int C, int H, int W, int K, int R, int S,
  * synchronize the device).  There is no counterpart of this entry point on the
  * reference pages; it is an addition of this library.
  *
- * Same arguments, layouts, results and error codes as conv2d_fwd, except that the
+ * Same arguments, layouts, results and error codes as conv2d_fwd (the same plan, large
+ * filters included: their tap passes each stage a repacked filter slice), except that the
  * repacked filter is staged in a fixed 8 MiB scratch array compiled into the library
  * instead of a caller workspace.  The function itself allocates nothing.
  *   - Limit: returns CONV2D_ERR_NOALLOC_LIMIT (nothing enqueued) when the repacked
  *     filter needs more than 8 MiB, which is about 2M fp32 or 4M bf16 filter values
  *     (rounded up to whole tiles); conv2d_workspace_size(CONV2D_OP_FWD, ...) reports the
- *     size needed.
+ *     size needed, and every size up to and including 8 MiB is accepted.
  *   - The scratch exists once per GPU that loaded the library and is held until the
  *     process exits.  The first call on a device looks up the scratch's device address
  *     (cudaGetSymbolAddress) with that device current; make that first call before
@@ -231,6 +232,11 @@ int conv2d_fwd_noalloc(int N, int C, int H, int W, int K, int R, int S,
  * library hit its bounded-wait limit since the previous call (and clears the record),
  * CONV2D_ERR_LAUNCH if the stream reports a CUDA error, else CONV2D_OK. */
 int conv2d_device_status(void *stream);
+
+/* Number of kernels the library has enqueued in this process so far, on any stream and
+ * device (a diagnostic: the difference across a region counts the kernels the region's
+ * calls launched).  Thread-safe. */
+unsigned long long conv2d_kernel_launches(void);
 
 /* Static description of an error code. */
 const char *conv2d_strerror(int code);

@@ -295,8 +295,9 @@ def conv2d_bwd_filter_at(x, dy, dims, idx) -> np.ndarray:
 
 
 # ------------------------------------------------------------------ 3-D (NCDHW)
-# Page "mkldnn_convolution.cc" (Apache MXNet): kernels of one to three spatial dims, input
-# with two more dims, one stride / pad / dilation per spatial dim.  The 3-D ops below take
+# Page "mkldnn_deconvolution.cc" (Apache MXNet): SupportMKLDNNDeconv accepts kernels of one to
+# three spatial dims on an input with two more dims, and DeconvDescCreator takes one stride /
+# pad / dilation per spatial dim (equal counts, 1 to 3).  The 3-D ops below take
 # x (N,C,D,H,W), w (K,C/groups,T,R,S), y / dy (N,K,Z,P,Q); groups split the channels as in
 # the 2-D ops.  The per-element definitions are in conv3d_oracle.c.
 

@@ -7,8 +7,8 @@
  * never links or calls it; only the tests, the smoke check and the bench's
  * CPU leg load this library.
  *
- * Source: Apache MXNet, mkldnn_convolution.cc / mkldnn_deconvolution.cc --
- * the support test accepts kernels of one to three spatial dims with an input
+ * Source: Apache MXNet, mkldnn_deconvolution.cc -- SupportMKLDNNDeconv
+ * accepts kernels of one to three spatial dims with an input
  * of two more dims (batch, channel), and the primitive setup takes one
  * stride, pad and dilation per spatial dim (CHECK_EQ of their counts, 1..3).
  * Notation extends the 2-D one by a depth dim in front: N images, C

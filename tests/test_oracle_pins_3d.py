@@ -1,7 +1,8 @@
 """Pins for the fp64 CPU oracle's 3-D (NCDHW) ops (CPU only).
 
-Semantics (page title): Apache MXNet mkldnn_convolution.cc -- kernels of one to three
-spatial dims, an input of two more dims, one stride, pad and dilation per spatial dim.
+Semantics (page title): Apache MXNet mkldnn_deconvolution.cc -- SupportMKLDNNDeconv: kernels
+of one to three spatial dims on an input of two more dims; DeconvDescCreator: one stride, pad
+and dilation per spatial dim.
 
 The 3-D oracle is trusted only after it agrees with things other than itself:
 hand-counted all-ones values (tests/golden/box_ones_3d.txt); depth-1 problems equal the
