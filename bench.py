@@ -50,7 +50,26 @@ def parse_args():
     ap.add_argument("--config-reps", type=int, default=30)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--profile", choices=OPS, default=None,
+                    help="run only this op of the workload (warmup + steps calls) for a profiler; prints its mean ms")
     return ap.parse_args()
+
+
+def run_profile(args):
+    """One op of one workload, `warmup` + `steps` calls back to back (L2 flushed before each), for
+    capturing its kernels under a profiler; prints the mean device time of the last `steps` calls."""
+    import torch
+    import convolution_nchw_conv2d_gb300 as cg
+    from convolution_nchw_conv2d_gb300 import workloads as W
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(2 * torch.cuda.get_device_properties(dev).L2_cache_size, dtype=torch.uint8, device=dev)
+    c = _device_case(W.WORKLOADS[args.workload], dev)
+    ms = _time_call(lambda: _op_call(c, args.profile, stream), flush, stream, max(1, args.steps), args.warmup)
+    cg.conv2d_device_status(stream)
+    print(json.dumps({"profile": args.profile, "workload": args.workload, "ms": round(ms, 5)}), flush=True)
+    return 0
 
 
 def load_peaks():
@@ -568,6 +587,8 @@ def main():
     args = parse_args()
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
+    if args.profile is not None:
+        return run_profile(args)
     if args.impl == "reference":
         if rank != 0:
             return 0

@@ -24,8 +24,13 @@ cudaError_t launch_wgrad_reduce(const ReducePlan& rp, int dt, int num_sms, cudaS
 cudaError_t launch_chan_sum(const ChanSumPlan& cp, int dt, cudaStream_t st);
 cudaError_t launch_space_to_depth(const S2dPlan& sp, int dt, cudaStream_t st);
 size_t wgrad_smem_bytes(const WgradPlan& p, int dt);
+cudaError_t launch_wgrad_mn(const WgradMnPlan& p, int grid, cudaStream_t st);
+cudaError_t launch_nhwc_pack(const NhwcPackPlan& a, const NhwcPackPlan& b, int dt, int num_sms, cudaStream_t st);
+cudaError_t launch_wgrad_reduce_t(const ReduceTPlan& rp, int dt, int num_sms, cudaStream_t st);
+size_t wgrad_mn_smem_bytes(const WgradMnPlan& p);
 int tap_gemm_take_error();
 int wgrad_take_error();
+int wgrad_mn_take_error();
 size_t noalloc_scratch_capacity();
 cudaError_t noalloc_scratch_ptr(void** ptr);
 }  // namespace cg3
@@ -897,6 +902,305 @@ bool phases_stage_less(const std::vector<WgradBuild>& phases, const WgradPlan* w
 int plan_phases(const Desc& dg, const PhaseLayout& L, const void* xs, const void* dyg, void* dwg, void* partial_ws,
                 int gi, const DevInfo& di, std::vector<WgradBuild>& out);
 
+// ------------------------------------------------------------------ bf16 channel-chunked wgrad
+// Backward-filter of bf16 tensors on channel-chunked planes (WgradMnPlan): x is packed once per
+// stride phase plane and dy once into zero-padded planes of the position space
+// L = n*EX*WL + e*WL + f, where every filter tap is an offset; the GEMM then stages both operands
+// with tensor copies.  Applies to bf16 tensors with unit stride (any dilation) or dilation 1
+// (stride phases).  Workspace: the packed x planes, the packed dy, the split partials.
+struct MnBuild {
+  WgradMnPlan p;
+  NhwcPackPlan px, pd;
+  ReduceTPlan rp;
+  size_t xq_bytes = 0, dyq_bytes = 0, partial_bytes = 0;
+  int grid = 0;
+};
+
+// One filter dimension split into phases: the taps of a phase read padded plane row e + off of
+// a plane whose row e is source row step*e + xoff.  Unit stride: one phase, offsets r*dil,
+// xoff = -pad.  Stride st > 1 (dilation 1): the stride phases, offsets r'.
+struct MnPhase {
+  int xoff;
+  std::vector<int> tap, off;  // filter index and its offset
+};
+
+std::vector<MnPhase> mn_phases(int R, int pad, int st, int dil) {
+  std::vector<MnPhase> v;
+  if (st == 1) {
+    MnPhase p;
+    p.xoff = -pad;
+    for (int r = 0; r < R; ++r) {
+      p.tap.push_back(r);
+      p.off.push_back(r * dil);
+    }
+    v.push_back(p);
+    return v;
+  }
+  for (const StridePhase& f : stride_phases(R, pad, st)) {
+    MnPhase p;
+    p.xoff = f.rho - st * f.pad;
+    for (int i = 0; i < f.n; ++i) {
+      p.tap.push_back(f.r0 + st * i);
+      p.off.push_back(i);
+    }
+    v.push_back(p);
+  }
+  return v;
+}
+
+// Packed planes as tensors of 8-byte elements, two per position: dims[0] = 2 * positions
+// (contiguous), then chunks (and planes); the box's first dim is a run of positions.
+bool encode_mn_map(CUtensorMap* m, const void* base, int rank, const uint64_t* dims, const uint32_t* box) {
+  EncodeTiledFn fn = encode_tiled_fn();
+  if (!fn) return false;
+  cuuint64_t gd[3], gs[2];
+  cuuint32_t bx[3], es[3] = {1u, 1u, 1u};
+  uint64_t stride = 8;  // bytes per element
+  for (int i = 0; i < rank; ++i) {
+    gd[i] = dims[i];
+    bx[i] = box[i];
+    if (i > 0) gs[i - 1] = stride;
+    stride *= dims[i];
+  }
+  const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT64, (cuuint32_t)rank, const_cast<void*>(base), gd, gs, bx, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// Copy-engine variant of a pack (NhwcPackPlan::use_tma): the source tensor (all Ctot channels,
+// whole rows) as a 4-D map with a box of W columns x ER plane rows (row traversal stride
+// step_h) x one chunk of channels.  Needs rows of whole 16-byte groups, W <= 256 and an
+// aligned base; false (plain pack) otherwise.  Sizing calls (no tensor) plan it as possible.
+bool setup_pack_tma(NhwcPackPlan& q, const void* base, int /*unused*/, int Ctot, int N, int H, int W, int esz) {
+  q.use_tma = 0;
+  const int CHUNK = 16 / esz;
+  if ((W * esz) % 16 != 0 || W > 256 || ((uintptr_t)base & 15) != 0) return false;
+  // rows per copy: at most 16 KB of source per buffer, then split the slab's rows evenly
+  int ER = std::max(1, std::min(q.EX, 20480 / (CHUNK * W * esz)));
+  while (ER > 1 && ER * q.step_h > 256) --ER;
+  if (ER * q.step_h > 256) return false;
+  const int ngrp = (q.EX + ER - 1) / ER;
+  ER = (q.EX + ngrp - 1) / ngrp;
+  if (base != nullptr) {
+    EncodeTiledFn fn = encode_tiled_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[4] = {(cuuint64_t)W, (cuuint64_t)H, (cuuint64_t)Ctot, (cuuint64_t)N};
+    const cuuint64_t strides[3] = {(cuuint64_t)W * esz, (cuuint64_t)H * W * esz, (cuuint64_t)q.src_nstride * esz};
+    const cuuint32_t box[4] = {(cuuint32_t)W, (cuuint32_t)(ER * q.step_h), (cuuint32_t)CHUNK, 1u};
+    const cuuint32_t estr[4] = {1u, (cuuint32_t)q.step_h, 1u, 1u};
+    const CUresult r = fn(&q.tm_src, esz == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
+                          const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return false;
+  }
+  const long long gps = (q.EX + ER - 1) / ER;
+  const long long units = gps * q.npl * q.nchunk * N;
+  if (units >= (1ll << 31)) return false;
+  q.use_tma = 1;
+  q.ER = ER;
+  q.c_base = 0;
+  q.tma_units = (unsigned)units;
+  q.fd_gps = make_fastdiv((uint32_t)gps);
+  return true;
+}
+
+int build_wgrad_mn(const Desc& d, const void* x, const void* dy, void* dw, void* ws, const DevInfo& di, MnBuild& b) {
+  if (d.dt != CONV2D_DTYPE_BF16) return CONV2D_ERR_UNSUPPORTED;
+  if ((d.sh > 1 || d.sw > 1) && (d.dh != 1 || d.dw != 1)) return CONV2D_ERR_UNSUPPORTED;
+  if (d.K % 4 != 0) return CONV2D_ERR_UNSUPPORTED;  // the reduce reads 4 output channels at a time
+  const std::vector<MnPhase> rows = mn_phases(d.R, d.ph, d.sh, d.dh), cols = mn_phases(d.S, d.pw, d.sw, d.dw);
+  int mo_r = 0, mo_c = 0;
+  for (const MnPhase& a : rows)
+    for (int o : a.off) mo_r = std::max(mo_r, o);
+  for (const MnPhase& c : cols)
+    for (int o : c.off) mo_c = std::max(mo_c, o);
+  const int EX = d.P + mo_r, WL = d.Q + mo_c;
+  const long long Mtot = (long long)d.N * EX * WL;
+  if (Mtot >= (1ll << 31)) return CONV2D_ERR_TOO_LARGE;
+  const int npl = (int)(rows.size() * cols.size());
+  if (npl > kMaxPlanes) return CONV2D_ERR_UNSUPPORTED;
+  WgradMnPlan& p = b.p;
+  std::memset(&p, 0, sizeof(p));
+  p.C = d.C;
+  p.K = d.K;
+  p.RS = d.R * d.S;
+  p.Mtot = Mtot;
+  p.NK = d.K >= 256 ? 256 : std::max(16, round_up(d.K, 16));
+  p.n_ktiles = (d.K + p.NK - 1) / p.NK;
+  p.n_ctiles = (d.C + 127) / 128;
+  // taps of every plane, sorted by offset
+  struct Tap {
+    int off, out;
+  };
+  std::vector<std::vector<Tap>> ptaps((size_t)npl);
+  int maxtaps = 1;
+  for (size_t a = 0; a < rows.size(); ++a)
+    for (size_t c = 0; c < cols.size(); ++c) {
+      std::vector<Tap>& v = ptaps[a * cols.size() + c];
+      for (size_t i = 0; i < rows[a].tap.size(); ++i)
+        for (size_t j = 0; j < cols[c].tap.size(); ++j)
+          v.push_back({rows[a].off[i] * WL + cols[c].off[j], rows[a].tap[i] * d.S + cols[c].tap[j]});
+      std::stable_sort(v.begin(), v.end(), [](const Tap& u, const Tap& w) { return u.off < w.off; });
+      maxtaps = std::max(maxtaps, (int)v.size());
+    }
+  p.T = std::max(1, std::min(maxtaps, 512 / p.NK));
+  p.tmem_cols = 32;
+  while (p.tmem_cols < p.T * p.NK) p.tmem_cols <<= 1;
+  const size_t budget = di.smem_optin - 2048;
+  // Candidate stage lengths; each groups every plane's taps greedily (at most T taps whose
+  // offsets fit one copy box with the stage).  Preferred: the fewest groups (every group stages
+  // dy and x again), then at least 3 pipeline stages, then the longer stage.
+  bool fitted = false;
+  WgradMnPlan best = p;
+  long long best_score = -1;
+  for (int KB : {128, 64, 32}) {
+    WgradMnPlan q = p;
+    int ng = 0, nt = 0, span = 0;
+    bool ok = true;
+    for (int pl = 0; pl < npl && ok; ++pl) {
+      const std::vector<Tap>& v = ptaps[(size_t)pl];
+      for (size_t i = 0; i < v.size();) {
+        if (ng >= kMaxTaps) {
+          ok = false;
+          break;
+        }
+        size_t j = i + 1;
+        while (j < v.size() && (int)(j - i) < q.T && v[j].off - v[i].off + KB <= 128) ++j;
+        q.grp_plane[ng] = pl;
+        q.grp_tap0[ng] = nt;
+        q.grp_ntaps[ng] = (int)(j - i);
+        q.grp_off0[ng] = v[i].off;
+        for (size_t u = i; u < j; ++u, ++nt) {
+          q.tap_delta[nt] = v[u].off - v[i].off;
+          q.tap_out[nt] = v[u].out;
+        }
+        span = std::max(span, v[j - 1].off - v[i].off);
+        ++ng;
+        i = j;
+      }
+    }
+    if (!ok || KB + span > 128) continue;  // a copy box row is at most 128 positions (256 elements)
+    const int KBX = KB + span;
+    const int a_box = 16 * KBX * 16, b_box = (q.NK / 8) * KB * 16;
+    const int a_st = round_up(a_box, 1024), b_st = round_up(b_box, 1024);
+    const size_t fixed = 8 * (2 * 8 + 3) + 16 + 1024 + 8 * 32 * 80;  // barriers, epilogue staging
+    long long st = ((long long)budget - (long long)fixed) / (a_st + b_st);
+    if (st > 4) st = 4;
+    if (st < 2) continue;
+    q.ngroups = ng;
+    q.KB = KB;
+    q.KBX = KBX;
+    q.stages = (int)st;
+    q.a_stage_bytes = a_st;
+    q.b_stage_bytes = b_st;
+    q.tx_bytes = a_box + b_box;
+    if (wgrad_mn_smem_bytes(q) > di.smem_optin) continue;
+    const long long score = (long long)(kMaxTaps + 1 - ng) * 1000000 + (st >= 3 ? 1000 : 0) + KB;
+    if (score > best_score) {
+      best_score = score;
+      best = q;
+      fitted = true;
+    }
+  }
+  if (fitted) p = best;
+  if (!fitted) return CONV2D_ERR_UNSUPPORTED;
+  // splits: one wave of tiles when there are fewer tile shapes than SMs
+  const long long base = (long long)p.ngroups * p.n_ctiles * p.n_ktiles;
+  const long long stage_count = (Mtot + p.KB - 1) / p.KB;
+  long long ns = base >= di.sms ? 1 : std::max(1ll, (long long)di.sms / base);
+  ns = std::min(ns, stage_count);
+  const size_t per_split = (size_t)p.RS * d.C * d.K * sizeof(float);
+  while (ns > 1 && per_split * (size_t)ns > kWorkspaceCap / 2) --ns;
+  p.split_len = (stage_count + ns - 1) / ns * p.KB;
+  p.nsplit = (int)((Mtot + p.split_len - 1) / p.split_len);
+  p.total_tiles = base * p.nsplit;
+  b.grid = (int)std::min<long long>(p.total_tiles, di.sms);
+  // workspace: packed x planes, packed dy, partials
+  const int C8 = (d.C + 7) / 8, K8 = (d.K + 7) / 8;
+  b.xq_bytes = (size_t)npl * C8 * (size_t)Mtot * 16;
+  b.dyq_bytes = (size_t)K8 * (size_t)Mtot * 16;
+  b.partial_bytes = per_split * (size_t)p.nsplit;
+  if (align_ws(b.xq_bytes) + align_ws(b.dyq_bytes) + b.partial_bytes > kWorkspaceCap) return CONV2D_ERR_UNSUPPORTED;
+  uint8_t* w8 = static_cast<uint8_t*>(ws);
+  void* xq = w8 ? w8 : nullptr;
+  void* dyq = w8 ? w8 + align_ws(b.xq_bytes) : nullptr;
+  p.partial = w8 ? reinterpret_cast<float*>(w8 + align_ws(b.xq_bytes) + align_ws(b.dyq_bytes)) : nullptr;
+  // packs
+  NhwcPackPlan& px = b.px;
+  std::memset(&px, 0, sizeof(px));
+  px.src = x;
+  px.dst = xq;
+  px.src_nstride = (long long)d.g * d.C * d.H * d.W;
+  px.N = d.N;
+  px.C = d.C;
+  px.H = d.H;
+  px.W = d.W;
+  px.nchunk = C8;
+  px.EX = EX;
+  px.WL = WL;
+  px.fd_WL = make_fastdiv((uint32_t)WL);
+  px.npl = npl;
+  px.step_h = d.sh;
+  px.step_w = d.sw;
+  for (size_t a = 0; a < rows.size(); ++a)
+    for (size_t c = 0; c < cols.size(); ++c) {
+      px.off_h[a * cols.size() + c] = rows[a].xoff;
+      px.off_w[a * cols.size() + c] = cols[c].xoff;
+    }
+  NhwcPackPlan& pd = b.pd;
+  std::memset(&pd, 0, sizeof(pd));
+  pd.src = dy;
+  pd.dst = dyq;
+  pd.src_nstride = (long long)d.g * d.K * d.P * d.Q;
+  pd.N = d.N;
+  pd.C = d.K;
+  pd.H = d.P;
+  pd.W = d.Q;
+  pd.nchunk = K8;
+  pd.EX = EX;
+  pd.WL = WL;
+  pd.fd_WL = make_fastdiv((uint32_t)WL);
+  pd.npl = 1;
+  pd.step_h = pd.step_w = 1;
+  // copy-engine packs when both sources allow them (whole rows of 16-byte multiples, aligned)
+  const bool tma_pack = setup_pack_tma(px, x, 1, d.g * d.C, d.N, d.H, d.W, 2) &&
+                        setup_pack_tma(pd, dy, 1, d.g * d.K, d.N, d.P, d.Q, 2);
+  if (!tma_pack) px.use_tma = pd.use_tma = 0;
+  for (NhwcPackPlan* q : {&px, &pd}) {
+    const long long upp = ((long long)q->EX * q->WL + kPackUnit - 1) / kPackUnit;
+    const long long units = upp * q->npl * q->nchunk * q->N;
+    if (units >= (1ll << 31) || (long long)q->EX * q->WL >= (1ll << 31)) return CONV2D_ERR_TOO_LARGE;
+    q->units = (unsigned)units;
+    q->fd_upp = make_fastdiv((uint32_t)upp);
+    q->fd_N = make_fastdiv((uint32_t)q->N);
+    q->fd_nchunk = make_fastdiv((uint32_t)q->nchunk);
+  }
+  // tensor maps over the packed planes (sizing calls pass no workspace)
+  if (w8 != nullptr) {
+    const uint64_t xd[3] = {2 * (uint64_t)Mtot, (uint64_t)C8, (uint64_t)npl};
+    const uint32_t xb[3] = {2 * (uint32_t)p.KBX, 16, 1};
+    const uint64_t yd[2] = {2 * (uint64_t)Mtot, (uint64_t)K8};
+    const uint32_t yb[2] = {2 * (uint32_t)p.KB, (uint32_t)(p.NK / 8)};
+    if (!encode_mn_map(&p.tm_x, xq, 3, xd, xb) || !encode_mn_map(&p.tm_dy, dyq, 2, yd, yb))
+      return CONV2D_ERR_UNSUPPORTED;
+  }
+  ReduceTPlan& rp = b.rp;
+  std::memset(&rp, 0, sizeof(rp));
+  rp.partial = p.partial;
+  rp.dw = dw;
+  rp.rows = d.C * d.R * d.S;
+  rp.K = d.K;
+  rp.RS = d.R * d.S;
+  rp.nsplit = p.nsplit;
+  return CONV2D_OK;
+}
+
+size_t mn_ws_bytes(const MnBuild& b) {
+  return align_ws(b.xq_bytes) + align_ws(b.dyq_bytes) + align_ws(b.partial_bytes);
+}
+
 int check_ptrs(const void* a, const void* b, const void* c, int dt) {
   if (!a || !b || !c) return CONV2D_ERR_NULLPTR;
   const uintptr_t m = dt == CONV2D_DTYPE_F32 ? 3 : 1;
@@ -1013,7 +1317,9 @@ struct PlanCache {
 
 PlanCache<TapSet> g_tap_plans;
 PlanCache<WgradBuild> g_wgrad_plans;
+PlanCache<MnBuild> g_mn_plans;
 PlanCache<size_t> g_ws_sizes;
+constexpr int kMnKey = 17;  // cache key tag of the channel-chunked backward-filter plans (not an op code)
 
 int workspace_size_uncached(int op, const Desc& d, size_t* bytes);
 
@@ -1145,9 +1451,16 @@ int workspace_size_uncached(int op, const Desc& d, size_t* bytes) {
     return CONV2D_OK;
   }
   if (op == CONV2D_OP_BWD_FILTER) {
+    // bf16: the channel-chunked path when it plans (size for it and for the others)
+    size_t mn = 0;
+    if (d.dt == CONV2D_DTYPE_BF16) {
+      MnBuild mb;
+      if (build_wgrad_mn(d, nullptr, nullptr, nullptr, nullptr, di, mb) == CONV2D_OK)
+        mn = mn_ws_bytes(mb) + chan_sum_bytes(d);
+    }
     // Strided filters run as stride phases when every phase plans (else as one problem);
     // size for either.
-    const size_t phased = phase_need(d, di);
+    const size_t phased = std::max(phase_need(d, di), mn);
     // The launch plans the copy-engine staging unless its tensor maps fail to encode for the
     // actual tensors; size for whichever of the two plans it ends up with.
     WgradBuild b;
@@ -1285,10 +1598,51 @@ int conv2d_bwd_filter_ex(int N, int C, int H, int W, int K, int R, int S, int pa
   const size_t esz = d.dt == CONV2D_DTYPE_F32 ? 4 : 2;
   size_t sum0 = 0;
   bool phases_run = false;
+  // bf16: x and dy packed into channel-chunked planes, then one tensor-copy-fed GEMM and the
+  // fixed-order reduce.  One plan serves every group (its tensor maps address the workspace);
+  // each group packs its own slices into the workspace in stream order.
+  if (d.dt == CONV2D_DTYPE_BF16 && workspace != nullptr) {
+    MnBuild mb;
+    const PlanKey key = make_key(kMnKey, dg, x, dy, nullptr, workspace);
+    bool have = g_mn_plans.get(key, mb);
+    if (!have) {
+      rc = build_wgrad_mn(dg, x, dy, dw, workspace, di, mb);
+      if (rc == CONV2D_OK) {
+        g_mn_plans.put(key, mb);
+        have = true;
+      } else if (rc != CONV2D_ERR_UNSUPPORTED) {
+        return rc;
+      }
+    }
+    if (have) {
+      rc = check_ws(workspace, workspace_bytes, mn_ws_bytes(mb) + (sums ? chan_sum_bytes(d) : 0));
+      if (rc) return rc;
+      for (int gi = 0; gi < groups; ++gi) {
+        // a group's channel slice: a channel offset in the copy-engine packs (their maps hold the
+        // whole tensors), a pointer offset in the plain ones
+        const bool ce = mb.px.use_tma != 0;
+        mb.px.src = ce ? x : byte_ptr(x) + gi * (size_t)dg.C * dg.H * dg.W * esz;
+        mb.pd.src = ce ? dy : byte_ptr(dy) + gi * (size_t)dg.K * dg.P * dg.Q * esz;
+        mb.px.c_base = ce ? gi * dg.C : 0;
+        mb.pd.c_base = ce ? gi * dg.K : 0;
+        mb.rp.dw = const_cast<uint8_t*>(byte_ptr(dw)) + gi * (size_t)dg.K * dg.C * dg.R * dg.S * esz;
+        mb.rp.beta = beta;  // per-call (not part of the cached plan)
+        mb.rp.flip = mode == CONV2D_MODE_CONVOLUTION ? 1 : 0;
+        rc = launch_err(launch_nhwc_pack(mb.px, mb.pd, d.dt, di.sms, st));
+        if (rc) return rc;
+        rc = launch_err(launch_wgrad_mn(mb.p, mb.grid, st));
+        if (rc) return rc;
+        rc = launch_err(launch_wgrad_reduce_t(mb.rp, d.dt, di.sms, st));
+        if (rc) return rc;
+      }
+      sum0 = mn_ws_bytes(mb);
+      phases_run = true;  // (the other paths below are skipped)
+    }
+  }
   // Strided filters: x into stride-phase planes once, then one stride-1 pass per phase and
   // group (all planned before anything is enqueued; one problem if a phase has no plan).
   const PhaseLayout L = phase_layout(dg);
-  if (L.on && workspace != nullptr && phase_need(dg, di) != 0) {
+  if (!phases_run && L.on && workspace != nullptr && phase_need(dg, di) != 0) {
     uint8_t* wsp = static_cast<uint8_t*>(workspace);
     std::vector<std::vector<WgradBuild>> gp((size_t)groups);
     size_t partial = 0;
@@ -1425,8 +1779,10 @@ int conv2d_device_status(void* stream) {
   }
   const int a = tap_gemm_take_error();
   const int b = wgrad_take_error();
-  if (a < 0 || b < 0) return CONV2D_ERR_LAUNCH;
-  if (a || b) return CONV2D_ERR_DEVICE_TIMEOUT;
+  const int c = wgrad_mn_take_error();
+  if (a < 0 || b < 0 || c < 0) return CONV2D_ERR_LAUNCH;
+  if (a == DEV_ERR_LAYOUT || b == DEV_ERR_LAYOUT || c == DEV_ERR_LAYOUT) return CONV2D_ERR_LAUNCH;
+  if (a || b || c) return CONV2D_ERR_DEVICE_TIMEOUT;
   return CONV2D_OK;
 }
 

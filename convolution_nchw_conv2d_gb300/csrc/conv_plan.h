@@ -17,6 +17,10 @@
 
 namespace cg3 {
 
+// Device-side error codes a kernel records in its error word (read back by conv2d_device_status):
+// a bounded pipeline wait that expired, or a shared-memory carve-up larger than the launch gave.
+enum : int { DEV_ERR_NONE = 0, DEV_ERR_TIMEOUT = 1, DEV_ERR_LAYOUT = 2 };
+
 // Unsigned 32-bit division by a divisor fixed at planning time, as a multiply-high and
 // shifts (Granlund and Montgomery, "Division by Invariant Integers using
 // Multiplication", PLDI 1994, unsigned case): with l = ceil(log2 d) and
@@ -192,6 +196,17 @@ struct WgradPlan {
   int vec_dy;            // 16-byte dy copies allowed (alignment / contiguity)
 };
 
+// Sum of the split partials [split][rows][K] of the channel-chunked backward-filter, transposed:
+// dw[k][row] = sum over splits of partial[split][row][k] (+ beta * dw), row = c*R*S + r*S + s
+// (convolution mode writes tap r*S + s at (R-1-r)*S + S-1-s).
+struct ReduceTPlan {
+  const float* partial;
+  void* dw;
+  int rows, K, RS, nsplit;
+  float beta;
+  int flip;
+};
+
 struct ReducePlan {
   const float* partial;
   void* dw;              // K x C x R_out x S_out, fp32 or bf16
@@ -202,6 +217,68 @@ struct ReducePlan {
   // Placement of partial tap (r', s') in dw: (r0 + rstep * r', s0 + sstep * s') of an
   // R_out x S_out filter (one stride phase of a strided filter; the identity otherwise).
   int R_out, S_out, r0, s0, rstep, sstep;
+};
+
+// Channel-chunked, zero-padded planes of an NCHW tensor ("NHWC within chunks"):
+//   dst[pl][cc][n][e][f][j] = src[n][CHUNK*cc + j][e*step_h + off_h[pl]][f*step_w + off_w[pl]]
+// for e < EX, f < WL, j < CHUNK (CHUNK = 16 bytes of elements), zero where the channel, row or
+// column lies outside the source.  Every 16-byte group holds CHUNK consecutive channels of one
+// position, so a tile of positions x channel chunks is one tensor copy into the MN-major operand
+// layout, and a shift of the position by one is a shift of one 16-byte row.
+constexpr int kPackUnit = 128;  // positions per warp work unit of the channel-chunk pack
+
+struct NhwcPackPlan {
+  const void* src;
+  void* dst;
+  long long src_nstride;  // elements from one source image to the next
+  int N, C, H, W;         // source extents (C channels per image)
+  int nchunk;             // ceil(C / CHUNK)
+  int EX, WL;             // padded plane extent
+  FastDiv fd_WL;          // division by WL
+  int npl;                // planes
+  int step_h, step_w;
+  int off_h[kMaxPlanes], off_w[kMaxPlanes];
+  // work units of kPackUnit positions: upp per slab, units = upp * npl * nchunk * N (< 2^31)
+  unsigned units;
+  FastDiv fd_upp, fd_N, fd_nchunk;
+  // Copy-engine variant (use_tma): the source as the 4-D tensor (W, H, channels, images) with a
+  // box of whole rows (W) x ER plane rows (traversal stride step_h) x CHUNK channels, so every
+  // ER padded rows of a slab are one tensor copy (rows and channels outside the tensor read as
+  // zero); threads then only transpose shared memory into the 16-byte groups.  c_base: first
+  // channel of the source slice (a group's channels within the tensor).
+  CUtensorMap tm_src;
+  int use_tma, ER, c_base;
+  unsigned tma_units;    // npl * nchunk * N * ceil(EX / ER)
+  FastDiv fd_gps;        // division by ceil(EX / ER)
+};
+
+// Backward-filter on channel-chunked planes (bf16): for every filter tap t of a stride phase,
+//   D_t[c, k] = sum over positions L of Xq_plane(t)[c, L + off_t] * DYq[k, L]
+// over the padded position space L = n*EX*WL + e*WL + f shared by all phases (DYq is zero past
+// the output rows and columns).  Both operands are MN-major tiles in shared memory (16 bytes =
+// 8 channels of one position), so every tap is a row offset of the staged x tile.  A tile is
+// (tap group, 128 channels, NK output channels, one range of positions); a tap group is up to T
+// taps of one phase, sorted by offset, staged as one x tile spanning their offsets.  Split
+// partials [split][C*R*S][K] (fp32, row c*R*S + r*S + s) are added by a fixed-order reduce that
+// transposes them into KCRS.  The tensor maps view the packed planes as 8-byte elements (two per
+// position), so that each copy row is a contiguous run of positions, not one 16-byte group.
+struct WgradMnPlan {
+  CUtensorMap tm_x;   // Xq as (2*positions, C/8, planes) of 8-byte elements, box (2*KBX, 16, 1)
+  CUtensorMap tm_dy;  // DYq as (2*positions, K/8), box (2*KB, NK/8)
+  float* partial;
+  int C, K, RS;
+  long long Mtot;     // positions N*EX*WL
+  int KB, KBX, stages, NK, T;
+  int n_ctiles, n_ktiles, ngroups, nsplit;
+  long long split_len;   // positions per split (multiple of KB)
+  long long total_tiles; // nsplit * ngroups * n_ctiles * n_ktiles
+  int a_stage_bytes, b_stage_bytes;  // stage strides (1024-byte multiples)
+  int tx_bytes;                      // bytes of one stage's two boxes
+  int tmem_cols;
+  // tap group g: plane, first tap index, tap count, position offset of the staged x tile
+  int grp_plane[kMaxTaps], grp_tap0[kMaxTaps], grp_ntaps[kMaxTaps], grp_off0[kMaxTaps];
+  // tap i: row offset in the staged x tile, and its filter tap r*S + s (the partial's slot)
+  int tap_delta[kMaxTaps], tap_out[kMaxTaps];
 };
 
 // Space-to-depth of x for strided backward-filter: xs[n][a*sw + b][c][i][j] =

@@ -1,0 +1,610 @@
+// conv_wgrad_mn.cu -- backward-filter of bf16 tensors on channel-chunked planes (sm_103a).
+//
+//   dw[k,c,r,s] = sum_{n,p,q} X(n, c, p*sh - ph + r*dh, q*sw - pw + s*dw) * dy[n,k,p,q]
+// (the filter gradient of the cuDNN backward-filter call in Apache SystemDS
+// LibMatrixCuDNNConvolutionAlgorithm.java; deconvolution's backward-weights in Apache MXNet
+// mkldnn_deconvolution.cc is the same product with the weight's roles swapped).
+//
+// Two kernels:
+//   nhwc_pack_kernel   copies an NCHW tensor into zero-padded planes whose 16-byte groups hold
+//                      consecutive channels of one position (see NhwcPackPlan); x goes in once
+//                      per stride phase plane, dy once.
+//   wgrad_mn_kernel    one implicit GEMM per tile over the padded position space (WgradMnPlan):
+//                      a single thread stages, per pipeline stage, one x tile (128 channels x
+//                      the stage's positions plus the tap group's span) and one dy tile (NK
+//                      output channels x the stage's positions) with tensor copies; both land
+//                      in the MN-major operand layout (16 bytes = 8 channels of one position,
+//                      8 positions per core matrix), so every tap of the group is the same x
+//                      tile started a few rows later.  One elected thread issues, per 16
+//                      positions and tap, one tcgen05.mma kind::f16 (bf16 operands, fp32
+//                      accumulators in TMEM, M = 128 channels, N = NK); four epilogue warps
+//                      move each tap's accumulator to the fp32 split partials, which the
+//                      fixed-order reduce of conv_wgrad.cu adds into dw.
+#include <algorithm>
+#include <atomic>
+#include <type_traits>
+
+#include <cuda_bf16.h>
+
+#include "conv_plan.h"
+#include "sm103_ptx.cuh"
+#include "launch_util.cuh"
+
+namespace cg3 {
+
+__device__ int g_wgmn_err;
+
+namespace {
+
+constexpr int kMnEpiWarps = 8;    // two per TMEM lane quarter, taking alternate 16-column chunks
+constexpr int kMnThreads = 32 * (2 + kMnEpiWarps);  // warp 0 producer, warp 1 TMEM + MMA, then epilogue
+constexpr int kMnRowPitch = 80;   // epilogue staging: 16 fp32 + 16 bytes per row (conflict-free)
+constexpr int kMnStageTile = 32 * kMnRowPitch;
+
+__device__ __forceinline__ uint32_t bar_at(uint32_t base, int i) { return base + 8u * (uint32_t)i; }
+
+struct MnTile {
+  int sp, g, mc, nk;
+};
+
+// Tiles run output-channel tile fastest, then channel tile, tap group and split, so that CTAs
+// running at the same time share their x tiles (same channel tile) and dy tiles (same split).
+__device__ __forceinline__ MnTile decode_mn(const WgradMnPlan& p, long long t) {
+  MnTile w;
+  w.nk = (int)(t % p.n_ktiles);
+  long long r = t / p.n_ktiles;
+  w.mc = (int)(r % p.n_ctiles);
+  r /= p.n_ctiles;
+  w.g = (int)(r % p.ngroups);
+  w.sp = (int)(r / p.ngroups);
+  return w;
+}
+
+// One stage's MMAs: for every tap j of the group, KS steps of 16 positions (unrolled; a single
+// issuing thread spends tens of cycles per tcgen05.mma in a runtime-bounded loop).
+template <int KS>
+__device__ __forceinline__ void issue_mn_stage(const WgradMnPlan& p, uint32_t tmem, uint32_t xlo, uint32_t ylo,
+                                               uint32_t a_hi, uint32_t b_hi, uint32_t id, int tap0, int ntaps,
+                                               bool first) {
+  for (int j = 0; j < ntaps; ++j) {
+    const uint32_t d = tmem + (uint32_t)(j * p.NK);
+    const uint32_t alo = xlo + (uint32_t)p.tap_delta[tap0 + j];  // 16-byte units
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks)
+      mma_ss_lh<1>(d, alo + 16u * ks, a_hi, ylo + 16u * ks, b_hi, id, (first && ks == 0) ? 0u : 1u);
+  }
+}
+
+}  // namespace
+
+// One 16-byte group per thread and item: CHUNK channels of one padded position, read from the
+// CHUNK channel planes of the source pixel (each read coalesced across the warp's consecutive
+// positions) and written as one 16-byte store (a warp writes 512 contiguous bytes).  Work units
+// are (slab = plane, chunk, image; kPackUnit consecutive positions of the slab), one per warp, the
+// units of plan `a` first, then those of plan `b` (b.src NULL: none), so the packs of x and dy
+// are one launch.
+template <int DT>
+__global__ void __launch_bounds__(256) nhwc_pack_kernel(const __grid_constant__ NhwcPackPlan a,
+                                                        const __grid_constant__ NhwcPackPlan b) {
+  constexpr int CHUNK = DT == 0 ? 4 : 8;
+  constexpr int UNIT = kPackUnit;
+  using E = typename std::conditional<DT == 0, uint32_t, uint16_t>::type;
+  const int warp = (int)(threadIdx.x >> 5), lane = (int)(threadIdx.x & 31);
+  const uint32_t na = a.units, nb = b.src != nullptr ? b.units : 0u;
+  for (uint32_t u = blockIdx.x * 8u + (uint32_t)warp; u < na + nb; u += gridDim.x * 8u) {
+    const bool first = u < na;
+    const NhwcPackPlan& p = first ? a : b;
+    const uint32_t v = first ? u : u - na;
+    const uint32_t sl = fdiv(v, p.fd_upp);          // slab: ((pl * nchunk + cc) * N + n)
+    const int i0 = (int)(v - sl * p.fd_upp.d) * UNIT;  // first position of the unit
+    const uint32_t r = fdiv(sl, p.fd_N);
+    const int n = (int)(sl - r * (uint32_t)p.N);
+    const uint32_t pl = fdiv(r, p.fd_nchunk);
+    const int cc = (int)(r - pl * (uint32_t)p.nchunk);
+    const long long HW = (long long)p.H * p.W;
+    const E* base = static_cast<const E*>(p.src) + (long long)n * p.src_nstride + (long long)(CHUNK * cc) * HW;
+    const int nch = p.C - CHUNK * cc < CHUNK ? p.C - CHUNK * cc : CHUNK;
+    const int slab = p.EX * p.WL;
+    uint4* dst = reinterpret_cast<uint4*>(p.dst) + sl * (long long)slab;
+    uint32_t q[UNIT / 32][4];
+#pragma unroll
+    for (int j = 0; j < UNIT / 32; ++j) {  // all loads of the lane's positions first
+      q[j][0] = q[j][1] = q[j][2] = q[j][3] = 0u;
+      const int i = i0 + 32 * j + lane;
+      if (i >= slab) continue;
+      const int e = (int)fdiv((uint32_t)i, p.fd_WL);
+      const int f = i - e * p.WL;
+      const int h = e * p.step_h + p.off_h[pl];
+      const int w = f * p.step_w + p.off_w[pl];
+      if (h >= 0 && h < p.H && w >= 0 && w < p.W) {
+        const E* s = base + (long long)h * p.W + w;
+#pragma unroll
+        for (int c = 0; c < CHUNK; ++c) {
+          if (c < nch) {
+            const uint32_t x = (uint32_t)__ldg(s + c * HW);
+            if constexpr (DT == 0) q[j][c] = x;
+            else q[j][c >> 1] |= x << (16 * (c & 1));
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < UNIT / 32; ++j) {
+      const int i = i0 + 32 * j + lane;
+      if (i < slab) dst[i] = make_uint4(q[j][0], q[j][1], q[j][2], q[j][3]);
+    }
+  }
+}
+
+// Copy-engine variant of the pack (NhwcPackPlan::use_tma): a work unit is ER padded rows of one
+// slab (plane, chunk, image); one thread copies the unit's source rows (whole image rows of the
+// chunk's channels, every step_h-th row, zeros outside the tensor) into shared memory as one
+// tensor copy, while the block transposes the previous unit (two buffers): thread i writes the
+// 16-byte groups of positions i, i + 256, ... of the unit (consecutive 16-byte stores).
+constexpr int kPackTmaThreads = 256;
+constexpr int kPackBufs = 4;  // copies of up to kPackBufs - 1 units in flight per block
+template <int DT>
+__global__ void __launch_bounds__(kPackTmaThreads) nhwc_pack_tma_kernel(const __grid_constant__ NhwcPackPlan a,
+                                                                        const __grid_constant__ NhwcPackPlan b) {
+  constexpr int CHUNK = DT == 0 ? 4 : 8;
+  constexpr int ESZ = DT == 0 ? 4 : 2;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  __shared__ uint64_t bars[kPackBufs];
+  __shared__ int abort_flag;
+  const uint32_t na = a.tma_units, nb = b.src != nullptr ? b.tma_units : 0u;
+  // a buffer holds one copy box: CHUNK channels x ER rows (the rows the traversal stride keeps) x W
+  const int rows_a = a.ER, rows_b = b.ER;
+  const uint32_t buf_bytes = (uint32_t)(((size_t)CHUNK * (rows_a > rows_b ? rows_a : rows_b) *
+                                         (a.W > b.W ? a.W : b.W) * ESZ + 1023) & ~size_t(1023));
+  if ((uint32_t)(sm - smem_raw) + kPackBufs * buf_bytes > dynamic_smem_bytes()) {
+    if (threadIdx.x == 0) atomicExch(&g_wgmn_err, DEV_ERR_LAYOUT);
+    return;
+  }
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kPackBufs; ++i) mbar_init(smem_u32(&bars[i]), 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  // unit u -> (plan, slab, first padded row), and its copy
+  auto locate = [&](uint32_t u, const NhwcPackPlan*& p, uint32_t& sl, int& e0) {
+    const bool first = u < na;
+    p = first ? &a : &b;
+    const uint32_t v = first ? u : u - na;
+    sl = fdiv(v, p->fd_gps);
+    e0 = (int)(v - sl * p->fd_gps.d) * p->ER;
+  };
+  auto issue = [&](uint32_t u, int buf) {
+    const NhwcPackPlan* p;
+    uint32_t sl;
+    int e0;
+    locate(u, p, sl, e0);
+    const uint32_t r = fdiv(sl, p->fd_N);
+    const int n = (int)(sl - r * (uint32_t)p->N);
+    const uint32_t pl = fdiv(r, p->fd_nchunk);
+    const int cc = (int)(r - pl * (uint32_t)p->nchunk);
+    const uint32_t bar = smem_u32(&bars[buf]);
+    mbar_arrive_expect_tx(bar, (uint32_t)(CHUNK * p->ER * p->W * ESZ));
+    tma_load_4d(smem_u32(sm) + (uint32_t)buf * buf_bytes, &p->tm_src, 0, e0 * p->step_h + p->off_h[pl],
+                p->c_base + CHUNK * cc, n, bar);
+  };
+  const uint32_t total = na + nb;
+  uint32_t u = blockIdx.x;
+  int fills[kPackBufs] = {};  // copies issued into each buffer (thread 0)
+  if (threadIdx.x == 0)
+    for (int i = 0; i < kPackBufs - 1; ++i)
+      if (u + (uint32_t)i * gridDim.x < total) {
+        issue(u + (uint32_t)i * gridDim.x, i);
+        ++fills[i];
+      }
+  for (int it = 0; u < total; ++it, u += gridDim.x) {
+    const int buf = it % kPackBufs;
+    // the buffer of iteration it - 1 was released by that iteration's barrier
+    const uint32_t ahead = u + (uint32_t)(kPackBufs - 1) * gridDim.x;
+    if (threadIdx.x == 0 && ahead < total) {
+      issue(ahead, (it + kPackBufs - 1) % kPackBufs);
+      ++fills[(it + kPackBufs - 1) % kPackBufs];
+    }
+    // every thread reaches the barrier below whether or not its wait succeeded, then all leave
+    // together if any wait expired
+    if (mbar_wait(smem_u32(&bars[buf]), (uint32_t)((it / kPackBufs) & 1), &abort_flag, &g_wgmn_err)) {
+    const NhwcPackPlan* p;
+    uint32_t sl;
+    int e0;
+    locate(u, p, sl, e0);
+    const uint32_t r = fdiv(sl, p->fd_N);
+    const uint32_t pl = fdiv(r, p->fd_nchunk);
+    const int cc = (int)(r - pl * (uint32_t)p->nchunk);
+    const int nch = p->C - CHUNK * cc < CHUNK ? p->C - CHUNK * cc : CHUNK;
+    const int rows = p->EX - e0 < p->ER ? p->EX - e0 : p->ER;
+    const uint8_t* src = sm + (size_t)buf * buf_bytes;  // [channel][row][W]
+    uint4* dst = reinterpret_cast<uint4*>(p->dst) + ((long long)sl * p->EX + e0) * p->WL;
+    const int W = p->W, ER = p->ER;
+    for (int i = threadIdx.x; i < rows * p->WL; i += kPackTmaThreads) {
+      const int er = (int)fdiv((uint32_t)i, p->fd_WL);
+      const int f = i - er * p->WL;
+      const int w = f * p->step_w + p->off_w[pl];
+      uint32_t q[4] = {0u, 0u, 0u, 0u};
+      if (w >= 0 && w < W) {
+#pragma unroll
+        for (int c = 0; c < CHUNK; ++c) {
+          if (c < nch) {
+            const size_t o = ((size_t)c * ER + er) * W + w;
+            if constexpr (DT == 0) q[c] = reinterpret_cast<const uint32_t*>(src)[o];
+            else q[c >> 1] |= (uint32_t)reinterpret_cast<const uint16_t*>(src)[o] << (16 * (c & 1));
+          }
+        }
+      }
+      dst[i] = make_uint4(q[0], q[1], q[2], q[3]);
+    }
+    }
+    __syncthreads();  // the buffer is read before it is refilled
+    if (abort_flag) break;
+  }
+  // leave no copy in flight into shared memory (after an abort); bounded
+  if (threadIdx.x == 0 && abort_flag) {
+    for (int bI = 0; bI < kPackBufs; ++bI)
+      if (fills[bI] > 0) mbar_wait_drain(smem_u32(&bars[bI]), (uint32_t)((fills[bI] - 1) & 1));
+  }
+}
+
+// Fixed-order sum of the split partials and transpose into KCRS (ReduceTPlan): a block of 8 warps
+// takes a tile of 32 partial rows (c, tap) x 128 output channels k; lane l of warp w adds, in
+// split order, the 4 consecutive k (one 16-byte read per split: a warp reads 512 contiguous
+// bytes of a row) of rows w, w + 8, w + 16, w + 24; the tile is transposed through shared memory
+// and each warp writes runs of 32 consecutive dw elements (rows) per k.  K % 4 == 0.
+template <int DT>
+__global__ void __launch_bounds__(256) wgrad_reduce_t_kernel(const __grid_constant__ ReduceTPlan rp) {
+  __shared__ float tile[32][129];
+  griddep_wait();  // the partials are written by the previous grid
+  const int tx = (int)(threadIdx.x & 31), ty = (int)(threadIdx.x >> 5);
+  const long long ntr = (rp.rows + 31) / 32, ntk = (rp.K + 127) / 128;
+  const long long split_stride = (long long)rp.rows * rp.K;
+  for (long long tid = blockIdx.x; tid < ntr * ntk; tid += gridDim.x) {
+    const int r0 = (int)(tid / ntk) * 32, k0 = (int)(tid % ntk) * 128;
+    float acc[4][4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+    const int k = k0 + 4 * tx;
+    if (k < rp.K) {
+      const float* src = rp.partial + k;
+      for (int sp = 0; sp < rp.nsplit; ++sp) {
+        float4 v[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int row = r0 + ty + 8 * i;
+          v[i] = row < rp.rows ? __ldg(reinterpret_cast<const float4*>(src + (long long)sp * split_stride +
+                                                                        (long long)row * rp.K))
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          acc[i][0] += v[i].x;
+          acc[i][1] += v[i].y;
+          acc[i][2] += v[i].z;
+          acc[i][3] += v[i].w;
+        }
+      }
+    }
+    __syncthreads();  // the previous tile's transposed values are read
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) tile[ty + 8 * i][4 * tx + j] = acc[i][j];
+    __syncthreads();
+    for (int kk = ty; kk < 128; kk += 8) {
+      const int kg = k0 + kk, row = r0 + tx;
+      if (kg >= rp.K || row >= rp.rows) continue;
+      float v = tile[tx][kk];
+      int orow = row;
+      if (rp.flip) {
+        const int c = row / rp.RS;
+        orow = c * rp.RS + (rp.RS - 1 - (row - c * rp.RS));
+      }
+      const long long o = (long long)kg * rp.rows + orow;
+      if constexpr (DT == 0) {
+        float* dwp = static_cast<float*>(rp.dw);
+        if (rp.beta != 0.f) v += rp.beta * dwp[o];
+        dwp[o] = v;
+      } else {
+        __nv_bfloat16* dwp = static_cast<__nv_bfloat16*>(rp.dw);
+        if (rp.beta != 0.f) v += rp.beta * __bfloat162float(dwp[o]);
+        dwp[o] = __float2bfloat16_rn(v);
+      }
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kMnThreads, 1) wgrad_mn_kernel(const __grid_constant__ WgradMnPlan p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const int S = p.stages;
+  const int KB = p.KB;
+
+  uint8_t* ptr = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t a0 = smem_u32(ptr);  // x tiles, one per stage (1024-byte multiples)
+  ptr += (size_t)S * p.a_stage_bytes;
+  const uint32_t b0 = smem_u32(ptr);  // dy tiles
+  ptr += (size_t)S * p.b_stage_bytes;
+  const uint32_t stg0 = smem_u32(ptr);  // epilogue: one 32 x 32 fp32 tile per warp, rows 144 bytes apart
+  ptr += kMnStageTile * kMnEpiWarps;
+  const uint32_t full = smem_u32(ptr);
+  const uint32_t empty = full + 8u * S;
+  const uint32_t accf = empty + 8u * S;
+  const uint32_t acce = accf + 8u;
+  const uint32_t drain = acce + 8u;
+  ptr += 8 * (2 * S + 3);
+  volatile uint32_t* tmem_holder = reinterpret_cast<volatile uint32_t*>(ptr);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(ptr + 4);
+  // The carve-up must lie inside the launch's dynamic shared memory; otherwise record the error
+  // and leave before touching any of it (every thread takes the same branch).
+  if ((uint32_t)(ptr + 8 - smem_raw) > dynamic_smem_bytes()) {
+    if (tid == 0) atomicExch(&g_wgmn_err, DEV_ERR_LAYOUT);
+    return;
+  }
+
+  if (tid == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(bar_at(full, s), 1);   // the producer's arrival + both copies' bytes
+      mbar_init(bar_at(empty, s), 1);  // the MMA commit
+    }
+    mbar_init(accf, 1);
+    mbar_init(acce, kMnEpiWarps);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32((const void*)tmem_holder), (uint32_t)p.tmem_cols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+  griddep_launch_dependents();  // the reduce may be scheduled; it waits for this grid to finish
+
+  if (warp == 0) {
+    // =============================================================== producer (one thread)
+    if (lane == 0) {
+      uint32_t last[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};  // 1 + parity of the last fill per slot
+      const uint32_t bytes = (uint32_t)p.tx_bytes;  // both boxes, out-of-bounds parts included
+      long long counter = 0;
+      bool ok = true;
+      for (long long t = blockIdx.x; t < p.total_tiles && ok; t += gridDim.x) {
+        const MnTile w = decode_mn(p, t);
+        const long long lbeg = (long long)w.sp * p.split_len;
+        const long long lend = lbeg + p.split_len < p.Mtot ? lbeg + p.split_len : p.Mtot;
+        const int xoff = p.grp_off0[w.g];
+        for (long long l0 = lbeg; l0 < lend; l0 += KB, ++counter) {
+          const int stage = (int)(counter % S);
+          const uint32_t ephase = (uint32_t)((counter / S) & 1);
+          if (!mbar_wait(bar_at(empty, stage), ephase ^ 1u, abort_flag, &g_wgmn_err)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = bar_at(full, stage);
+          mbar_arrive_expect_tx(fb, bytes);
+          // boxes past the position space or the channel extents read as zeros
+          tma_load_3d(a0 + (uint32_t)stage * (uint32_t)p.a_stage_bytes, &p.tm_x, (int)(2 * (l0 + xoff)), 16 * w.mc,
+                      p.grp_plane[w.g], fb);
+          tma_load_2d(b0 + (uint32_t)stage * (uint32_t)p.b_stage_bytes, &p.tm_dy, (int)(2 * l0), (p.NK / 8) * w.nk, fb);
+          if (stage < 8) last[stage] = 1u + ephase;
+        }
+      }
+      // After an abort, wait (bounded) for copies still in flight into shared memory.
+      if (*abort_flag)
+        for (int s = 0; s < S && s < 8; ++s)
+          if (last[s]) mbar_wait_drain(bar_at(full, s), last[s] - 1u);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // =============================================================== MMA issuer
+    const bool leader = elect_one();
+    const uint32_t id = idesc(1, 128, p.NK, 1, 1);  // bf16 x bf16 -> fp32, both operands MN-major
+    const uint32_t a_hi = (uint32_t)(sdesc(0u, 0u, (uint32_t)(p.KBX * 16)) >> 32);  // stride offset + version
+    const uint32_t b_hi = (uint32_t)(sdesc(0u, 0u, (uint32_t)(KB * 16)) >> 32);
+    long long counter = 0;
+    uint32_t aphase = 0;
+    bool ok = true, issued = false;
+    for (long long t = blockIdx.x; t < p.total_tiles && ok; t += gridDim.x) {
+      const MnTile w = decode_mn(p, t);
+      const long long lbeg = (long long)w.sp * p.split_len;
+      const long long lend = lbeg + p.split_len < p.Mtot ? lbeg + p.split_len : p.Mtot;
+      const int tap0 = p.grp_tap0[w.g], ntaps = p.grp_ntaps[w.g];
+      // the epilogue has moved the previous tile's accumulators out of TMEM
+      if (!mbar_wait(acce, aphase ^ 1u, abort_flag, &g_wgmn_err)) break;
+      tc_fence_after();
+      bool first = true;
+      for (long long l0 = lbeg; l0 < lend; l0 += KB, ++counter) {
+        const int stage = (int)(counter % S);
+        const uint32_t fphase = (uint32_t)((counter / S) & 1);
+        if (!mbar_wait(bar_at(full, stage), fphase, abort_flag, &g_wgmn_err)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        if (leader) {
+          // descriptor low halves (start address, leading offset 128 B) of the stage's tiles; a
+          // tap starts its x tile tap_delta rows later, a 16-position step is 16 rows
+          const uint32_t xlo = (uint32_t)sdesc(a0 + (uint32_t)stage * (uint32_t)p.a_stage_bytes, 128u, 0u);
+          const uint32_t ylo = (uint32_t)sdesc(b0 + (uint32_t)stage * (uint32_t)p.b_stage_bytes, 128u, 0u);
+          switch (KB / 16) {
+            case 2: issue_mn_stage<2>(p, tmem, xlo, ylo, a_hi, b_hi, id, tap0, ntaps, first); break;
+            case 4: issue_mn_stage<4>(p, tmem, xlo, ylo, a_hi, b_hi, id, tap0, ntaps, first); break;
+            default: issue_mn_stage<8>(p, tmem, xlo, ylo, a_hi, b_hi, id, tap0, ntaps, first); break;
+          }
+          tc_commit(bar_at(empty, stage));  // frees the stage once its MMAs are done
+        }
+        __syncwarp();
+        issued = true;
+        first = false;
+      }
+      if (!ok) break;
+      if (leader) tc_commit(accf);
+      __syncwarp();
+      aphase ^= 1u;
+    }
+    if (!ok && issued && leader) {
+      tc_commit(drain);
+      mbar_wait_drain(drain, 0);
+    }
+    __syncwarp();
+  } else {
+    // =============================================================== epilogue
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const bool vec = (p.K & 3) == 0;
+    uint32_t aphase = 0;
+    for (long long t = blockIdx.x; t < p.total_tiles; t += gridDim.x) {
+      const MnTile w = decode_mn(p, t);
+      if (!mbar_wait(accf, aphase, abort_flag, &g_wgmn_err)) break;
+      tc_fence_after();
+      // Each warp moves its 32 TMEM lanes (channels c) 16 columns at a time (the two warps of a
+      // lane quarter take alternate chunks): TMEM -> registers -> a padded shared tile (lane = row)
+      // -> registers (4 lanes per row) -> 64 contiguous bytes of each of 8 partial rows per store
+      // instruction.  The next chunk's TMEM load is in flight while a chunk is stored.
+      const int c_w = 128 * w.mc + 32 * q;  // first channel of this warp's rows
+      const int tap0 = p.grp_tap0[w.g], ntaps = p.grp_ntaps[w.g];
+      const uint32_t stg = stg0 + (uint32_t)((warp - 2) * kMnStageTile);
+      const int half = (warp - 2) >> 2;
+      const int rr = lane >> 2, ch = lane & 3;  // read-back: row within a group of 8, 16-byte chunk
+      const int nchunk = p.NK / 16;             // per tap
+      const int total = ntaps * nchunk;
+      uint32_t ra[16], rb[16];
+      int ci = half;
+      if (ci < total)
+        tmem_ld16(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)((ci / nchunk) * p.NK + 16 * (ci % nchunk)), ra);
+      while (ci < total) {
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 16; ++i) rb[i] = ra[i];
+        const int nx = ci + 2;
+        if (nx < total)
+          tmem_ld16(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)((nx / nchunk) * p.NK + 16 * (nx % nchunk)), ra);
+        const int j = ci / nchunk, c0 = 16 * (ci % nchunk);
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(stg + (uint32_t)(lane * kMnRowPitch + 16 * i)),
+                       "r"(rb[4 * i]), "r"(rb[4 * i + 1]), "r"(rb[4 * i + 2]), "r"(rb[4 * i + 3])
+                       : "memory");
+        __syncwarp();
+        const long long row0 = ((long long)w.sp * p.C + c_w) * p.RS + p.tap_out[tap0 + j];  // partial row of c_w
+        const int kk = w.nk * p.NK + c0 + 4 * ch;  // this lane's 4 output channels
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          const int row = 8 * g + rr;  // channel c_w + row
+          uint32_t v0, v1, v2, v3;
+          asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+                       : "=r"(v0), "=r"(v1), "=r"(v2), "=r"(v3)
+                       : "r"(stg + (uint32_t)(row * kMnRowPitch + 16 * ch)));
+          if (c_w + row < p.C && kk < p.K) {
+            float* d = p.partial + (row0 + (long long)row * p.RS) * p.K + kk;
+            if (vec) {
+              *reinterpret_cast<uint4*>(d) = make_uint4(v0, v1, v2, v3);
+            } else {
+              const uint32_t vv[4] = {v0, v1, v2, v3};
+#pragma unroll
+              for (int i = 0; i < 4; ++i)
+                if (kk + i < p.K) d[i] = __uint_as_float(vv[i]);
+            }
+          }
+        }
+        __syncwarp();
+        ci = nx;
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acce);
+      aphase ^= 1u;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, (uint32_t)p.tmem_cols);
+  }
+}
+
+// ---------------------------------------------------------------------------- launchers
+// A CTA that takes more than half of TMEM asks for more than half of the SM's shared memory,
+// so that a second CTA never waits on the SM for TMEM columns.
+size_t wgrad_mn_smem_bytes(const WgradMnPlan& p) {
+  const size_t b = (size_t)p.stages * (p.a_stage_bytes + p.b_stage_bytes) + (size_t)kMnEpiWarps * kMnStageTile +
+                   8 * (2 * p.stages + 3) + 16 + 1024;
+  return p.tmem_cols > 256 && b < (size_t)(120 << 10) ? (size_t)(120 << 10) : b;
+}
+
+static std::atomic<int> g_mn_smem_set[kMaxDevices];
+
+cudaError_t launch_wgrad_mn(const WgradMnPlan& p, int grid, cudaStream_t st) {
+  const size_t smem = wgrad_mn_smem_bytes(p);
+  const cudaError_t e = ensure_dyn_smem(wgrad_mn_kernel, smem, g_mn_smem_set);
+  if (e != cudaSuccess) return e;
+  wgrad_mn_kernel<<<grid, kMnThreads, smem, st>>>(p);
+  return cudaGetLastError();
+}
+
+size_t nhwc_pack_tma_smem(const NhwcPackPlan& a, const NhwcPackPlan& b, int dt) {
+  const size_t chunk = dt == 0 ? 4 : 8, esz = dt == 0 ? 4 : 2;
+  const int ra = a.ER, rb = b.src != nullptr ? b.ER : 0;
+  const int rows = ra > rb ? ra : rb, W = b.src != nullptr && b.W > a.W ? b.W : a.W;
+  return kPackBufs * ((chunk * rows * W * esz + 1023) & ~size_t(1023)) + 1024;
+}
+
+static std::atomic<int> g_pack_smem_set[2][kMaxDevices];
+
+// Packs a and (if b.src is not NULL) b in one launch; both copy-engine or both plain.
+cudaError_t launch_nhwc_pack(const NhwcPackPlan& a, const NhwcPackPlan& b, int dt, int num_sms, cudaStream_t st) {
+  if (a.use_tma && (b.src == nullptr || b.use_tma)) {
+    const long long units = (long long)a.tma_units + (b.src != nullptr ? (long long)b.tma_units : 0ll);
+    const size_t smem = nhwc_pack_tma_smem(a, b, dt);
+    const long long per_sm = std::max<long long>(1, std::min<long long>(8, (220ll << 10) / (long long)smem));
+    const unsigned blocks = (unsigned)std::max(1ll, std::min<long long>(units, (long long)num_sms * per_sm));
+    cudaError_t e = dt == 0 ? ensure_dyn_smem(nhwc_pack_tma_kernel<0>, smem, g_pack_smem_set[0])
+                            : ensure_dyn_smem(nhwc_pack_tma_kernel<1>, smem, g_pack_smem_set[1]);
+    if (e != cudaSuccess) return e;
+    if (dt == 0)
+      nhwc_pack_tma_kernel<0><<<blocks, kPackTmaThreads, smem, st>>>(a, b);
+    else
+      nhwc_pack_tma_kernel<1><<<blocks, kPackTmaThreads, smem, st>>>(a, b);
+    return cudaGetLastError();
+  }
+  const long long warps = (long long)a.units + (b.src != nullptr ? (long long)b.units : 0ll);
+  const long long blocks = std::max(1ll, std::min<long long>((warps + 7) / 8, (long long)num_sms * 16));
+  if (dt == 0)
+    nhwc_pack_kernel<0><<<(unsigned)blocks, 256, 0, st>>>(a, b);
+  else
+    nhwc_pack_kernel<1><<<(unsigned)blocks, 256, 0, st>>>(a, b);
+  return cudaGetLastError();
+}
+
+// Launched with programmatic stream serialization after the GEMM (it waits for the GEMM).
+cudaError_t launch_wgrad_reduce_t(const ReduceTPlan& rp, int dt, int num_sms, cudaStream_t st) {
+  const long long tiles = (long long)(rp.rows + 31) / 32 * ((rp.K + 127) / 128);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)std::max(1ll, std::min<long long>(tiles, (long long)num_sms * 8)));
+  cfg.blockDim = dim3(256);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = dt == 0 ? cudaLaunchKernelEx(&cfg, wgrad_reduce_t_kernel<0>, rp)
+                                : cudaLaunchKernelEx(&cfg, wgrad_reduce_t_kernel<1>, rp);
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+int wgrad_mn_take_error() {
+  int v = 0, zero = 0;
+  if (cudaMemcpyFromSymbol(&v, g_wgmn_err, sizeof(int)) != cudaSuccess) return -1;
+  if (v != 0) cudaMemcpyToSymbol(g_wgmn_err, &zero, sizeof(int));
+  return v;
+}
+
+}  // namespace cg3

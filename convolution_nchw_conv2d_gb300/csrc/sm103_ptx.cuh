@@ -16,10 +16,18 @@
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 
+#include "conv_plan.h"
+
 namespace cg3 {
 
-// Device-side error codes written to the per-library error word.
-enum : int { DEV_ERR_NONE = 0, DEV_ERR_TIMEOUT = 1 };
+// Device-side error codes written to the per-library error word: DEV_ERR_* in conv_plan.h.
+
+// Bytes of dynamic shared memory the launch provided.
+__device__ __forceinline__ uint32_t dynamic_smem_bytes() {
+  uint32_t v;
+  asm volatile("mov.u32 %0, %%dynamic_smem_size;" : "=r"(v));
+  return v;
+}
 
 // Bounded waits give up after this many nanoseconds of %globaltimer.
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s
@@ -184,6 +192,20 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
 // 4-D tiled tensor copy global -> shared (no swizzle, no multicast), completion counted in
 // bytes on an mbarrier.  Coordinates are element indices; the innermost one times the
 // element size must be a multiple of 16 bytes.  Elements outside the tensor read as zero.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int c0, int c1, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(tmap), "r"(c0), "r"(c1), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* tmap, int c0, int c1, int c2, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(tmap), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
+      : "memory");
+}
+
 __device__ __forceinline__ void tma_load_4d(uint32_t dst, const void* tmap, int c0, int c1, int c2, int c3,
                                             uint32_t bar) {
   asm volatile(
