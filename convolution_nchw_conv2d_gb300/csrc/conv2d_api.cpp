@@ -968,41 +968,21 @@ bool encode_mn_map(CUtensorMap* m, const void* base, int rank, const uint64_t* d
   return r == CUDA_SUCCESS;
 }
 
-// Copy-engine variant of a pack (NhwcPackPlan::use_tma): the source tensor (all Ctot channels,
-// whole rows) as a 4-D map with a box of W columns x ER plane rows (row traversal stride
-// step_h) x one chunk of channels.  Needs rows of whole 16-byte groups, W <= 256 and an
-// aligned base; false (plain pack) otherwise.  Sizing calls (no tensor) plan it as possible.
-bool setup_pack_tma(NhwcPackPlan& q, const void* base, int /*unused*/, int Ctot, int N, int H, int W, int esz) {
-  q.use_tma = 0;
+// Word variant of a pack (NhwcPackPlan::words): needs rows of whole 16-byte words, an aligned
+// tensor (sizing calls pass none: planned as aligned) and step_w 1 or 2; false (plain pack)
+// otherwise.
+bool setup_pack_words(NhwcPackPlan& q, const void* base, int esz) {
+  q.words = 0;
   const int CHUNK = 16 / esz;
-  if ((W * esz) % 16 != 0 || W > 256 || ((uintptr_t)base & 15) != 0) return false;
-  // rows per copy: at most 16 KB of source per buffer, then split the slab's rows evenly
-  int ER = std::max(1, std::min(q.EX, 20480 / (CHUNK * W * esz)));
-  while (ER > 1 && ER * q.step_h > 256) --ER;
-  if (ER * q.step_h > 256) return false;
-  const int ngrp = (q.EX + ER - 1) / ER;
-  ER = (q.EX + ngrp - 1) / ngrp;
-  if (base != nullptr) {
-    EncodeTiledFn fn = encode_tiled_fn();
-    if (!fn) return false;
-    const cuuint64_t dims[4] = {(cuuint64_t)W, (cuuint64_t)H, (cuuint64_t)Ctot, (cuuint64_t)N};
-    const cuuint64_t strides[3] = {(cuuint64_t)W * esz, (cuuint64_t)H * W * esz, (cuuint64_t)q.src_nstride * esz};
-    const cuuint32_t box[4] = {(cuuint32_t)W, (cuuint32_t)(ER * q.step_h), (cuuint32_t)CHUNK, 1u};
-    const cuuint32_t estr[4] = {1u, (cuuint32_t)q.step_h, 1u, 1u};
-    const CUresult r = fn(&q.tm_src, esz == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
-                          const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                          CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
-                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS) return false;
-  }
-  const long long gps = (q.EX + ER - 1) / ER;
-  const long long units = gps * q.npl * q.nchunk * N;
-  if (units >= (1ll << 31)) return false;
-  q.use_tma = 1;
-  q.ER = ER;
-  q.c_base = 0;
-  q.tma_units = (unsigned)units;
-  q.fd_gps = make_fastdiv((uint32_t)gps);
+  if ((q.W * esz) % 16 != 0 || ((uintptr_t)base & 15) != 0 || (q.step_w != 1 && q.step_w != 2)) return false;
+  const long long nblk = (q.WL + CHUNK - 1) / CHUNK;
+  const long long items = nblk * q.EX * q.npl * q.nchunk * q.N;
+  if (items >= (1ll << 31)) return false;
+  for (int pl = 0; pl < q.npl; ++pl) q.xs[pl] = floor_div(q.off_w[pl], CHUNK) * CHUNK;
+  q.words = 1;
+  q.witems = (unsigned)items;
+  q.fd_nblk = make_fastdiv((uint32_t)nblk);
+  q.fd_EX = make_fastdiv((uint32_t)q.EX);
   return true;
 }
 
@@ -1164,10 +1144,8 @@ int build_wgrad_mn(const Desc& d, const void* x, const void* dy, void* dw, void*
   pd.fd_WL = make_fastdiv((uint32_t)WL);
   pd.npl = 1;
   pd.step_h = pd.step_w = 1;
-  // copy-engine packs when both sources allow them (whole rows of 16-byte multiples, aligned)
-  const bool tma_pack = setup_pack_tma(px, x, 1, d.g * d.C, d.N, d.H, d.W, 2) &&
-                        setup_pack_tma(pd, dy, 1, d.g * d.K, d.N, d.P, d.Q, 2);
-  if (!tma_pack) px.use_tma = pd.use_tma = 0;
+  // word packs when both sources allow them (one launch runs both)
+  if (!(setup_pack_words(px, x, 2) && setup_pack_words(pd, dy, 2))) px.words = pd.words = 0;
   for (NhwcPackPlan* q : {&px, &pd}) {
     const long long upp = ((long long)q->EX * q->WL + kPackUnit - 1) / kPackUnit;
     const long long units = upp * q->npl * q->nchunk * q->N;
@@ -1603,7 +1581,7 @@ int conv2d_bwd_filter_ex(int N, int C, int H, int W, int K, int R, int S, int pa
   // each group packs its own slices into the workspace in stream order.
   if (d.dt == CONV2D_DTYPE_BF16 && workspace != nullptr) {
     MnBuild mb;
-    const PlanKey key = make_key(kMnKey, dg, x, dy, nullptr, workspace);
+    const PlanKey key = make_key(kMnKey, dg, nullptr, nullptr, nullptr, workspace);
     bool have = g_mn_plans.get(key, mb);
     if (!have) {
       rc = build_wgrad_mn(dg, x, dy, dw, workspace, di, mb);
@@ -1618,13 +1596,8 @@ int conv2d_bwd_filter_ex(int N, int C, int H, int W, int K, int R, int S, int pa
       rc = check_ws(workspace, workspace_bytes, mn_ws_bytes(mb) + (sums ? chan_sum_bytes(d) : 0));
       if (rc) return rc;
       for (int gi = 0; gi < groups; ++gi) {
-        // a group's channel slice: a channel offset in the copy-engine packs (their maps hold the
-        // whole tensors), a pointer offset in the plain ones
-        const bool ce = mb.px.use_tma != 0;
-        mb.px.src = ce ? x : byte_ptr(x) + gi * (size_t)dg.C * dg.H * dg.W * esz;
-        mb.pd.src = ce ? dy : byte_ptr(dy) + gi * (size_t)dg.K * dg.P * dg.Q * esz;
-        mb.px.c_base = ce ? gi * dg.C : 0;
-        mb.pd.c_base = ce ? gi * dg.K : 0;
+        mb.px.src = byte_ptr(x) + gi * (size_t)dg.C * dg.H * dg.W * esz;
+        mb.pd.src = byte_ptr(dy) + gi * (size_t)dg.K * dg.P * dg.Q * esz;
         mb.rp.dw = const_cast<uint8_t*>(byte_ptr(dw)) + gi * (size_t)dg.K * dg.C * dg.R * dg.S * esz;
         mb.rp.beta = beta;  // per-call (not part of the cached plan)
         mb.rp.flip = mode == CONV2D_MODE_CONVOLUTION ? 1 : 0;

@@ -241,15 +241,13 @@ struct NhwcPackPlan {
   // work units of kPackUnit positions: upp per slab, units = upp * npl * nchunk * N (< 2^31)
   unsigned units;
   FastDiv fd_upp, fd_N, fd_nchunk;
-  // Copy-engine variant (use_tma): the source as the 4-D tensor (W, H, channels, images) with a
-  // box of whole rows (W) x ER plane rows (traversal stride step_h) x CHUNK channels, so every
-  // ER padded rows of a slab are one tensor copy (rows and channels outside the tensor read as
-  // zero); threads then only transpose shared memory into the 16-byte groups.  c_base: first
-  // channel of the source slice (a group's channels within the tensor).
-  CUtensorMap tm_src;
-  int use_tma, ER, c_base;
-  unsigned tma_units;    // npl * nchunk * N * ceil(EX / ER)
-  FastDiv fd_gps;        // division by ceil(EX / ER)
+  // Word variant (words): rows of whole 16-byte words, an aligned tensor, step_w 1 or 2; items of
+  // CHUNK positions (witems = npl * nchunk * N * EX * nblk), xs[pl] = off_w[pl] rounded down to a
+  // multiple of CHUNK.
+  int words;
+  unsigned witems;
+  FastDiv fd_nblk, fd_EX;  // division by nblk = ceil(WL / CHUNK) and by EX
+  int xs[kMaxPlanes];
 };
 
 // Backward-filter on channel-chunked planes (bf16): for every filter tap t of a stride phase,

@@ -136,116 +136,104 @@ __global__ void __launch_bounds__(256) nhwc_pack_kernel(const __grid_constant__ 
   }
 }
 
-// Copy-engine variant of the pack (NhwcPackPlan::use_tma): a work unit is ER padded rows of one
-// slab (plane, chunk, image); one thread copies the unit's source rows (whole image rows of the
-// chunk's channels, every step_h-th row, zeros outside the tensor) into shared memory as one
-// tensor copy, while the block transposes the previous unit (two buffers): thread i writes the
-// 16-byte groups of positions i, i + 256, ... of the unit (consecutive 16-byte stores).
-constexpr int kPackTmaThreads = 256;
-constexpr int kPackBufs = 4;  // copies of up to kPackBufs - 1 units in flight per block
-template <int DT>
-__global__ void __launch_bounds__(kPackTmaThreads) nhwc_pack_tma_kernel(const __grid_constant__ NhwcPackPlan a,
-                                                                        const __grid_constant__ NhwcPackPlan b) {
+// Word variant of the pack (NhwcPackPlan::words: rows of whole 16-byte words, aligned tensor,
+// step_w 1 or 2): an item is CHUNK consecutive positions f0 .. f0 + CHUNK - 1 of one padded row
+// of one slab.  Their source columns f*SW + off_w lie in a window of NW aligned 16-byte words
+// starting at column wbase = f0*SW + xs (xs = off_w rounded down to a multiple of CHUNK,
+// R = off_w - xs); the thread loads those words of each of the CHUNK channels (words outside the
+// row, the tensor or the chunk's channel slice read as zero; all loads issued before any use),
+// transposes them in registers -- output f0 + i takes element R + SW*i of every channel -- and
+// writes the `nout` 16-byte groups (consecutive).
+template <int DT, int SW, int R>
+__device__ __forceinline__ void pack_words_item(const void* row0_v, long long HW, int W, int wbase, int nch, int nout,
+                                                uint4* dst) {
   constexpr int CHUNK = DT == 0 ? 4 : 8;
-  constexpr int ESZ = DT == 0 ? 4 : 2;
-  extern __shared__ __align__(1024) uint8_t smem_raw[];
-  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ uint64_t bars[kPackBufs];
-  __shared__ int abort_flag;
-  const uint32_t na = a.tma_units, nb = b.src != nullptr ? b.tma_units : 0u;
-  // a buffer holds one copy box: CHUNK channels x ER rows (the rows the traversal stride keeps) x W
-  const int rows_a = a.ER, rows_b = b.ER;
-  const uint32_t buf_bytes = (uint32_t)(((size_t)CHUNK * (rows_a > rows_b ? rows_a : rows_b) *
-                                         (a.W > b.W ? a.W : b.W) * ESZ + 1023) & ~size_t(1023));
-  if ((uint32_t)(sm - smem_raw) + kPackBufs * buf_bytes > dynamic_smem_bytes()) {
-    if (threadIdx.x == 0) atomicExch(&g_wgmn_err, DEV_ERR_LAYOUT);
-    return;
-  }
-  if (threadIdx.x == 0) {
-    for (int i = 0; i < kPackBufs; ++i) mbar_init(smem_u32(&bars[i]), 1);
-    abort_flag = 0;
-    fence_mbar_init();
-  }
-  __syncthreads();
-  // unit u -> (plan, slab, first padded row), and its copy
-  auto locate = [&](uint32_t u, const NhwcPackPlan*& p, uint32_t& sl, int& e0) {
-    const bool first = u < na;
-    p = first ? &a : &b;
-    const uint32_t v = first ? u : u - na;
-    sl = fdiv(v, p->fd_gps);
-    e0 = (int)(v - sl * p->fd_gps.d) * p->ER;
-  };
-  auto issue = [&](uint32_t u, int buf) {
-    const NhwcPackPlan* p;
-    uint32_t sl;
-    int e0;
-    locate(u, p, sl, e0);
-    const uint32_t r = fdiv(sl, p->fd_N);
-    const int n = (int)(sl - r * (uint32_t)p->N);
-    const uint32_t pl = fdiv(r, p->fd_nchunk);
-    const int cc = (int)(r - pl * (uint32_t)p->nchunk);
-    const uint32_t bar = smem_u32(&bars[buf]);
-    mbar_arrive_expect_tx(bar, (uint32_t)(CHUNK * p->ER * p->W * ESZ));
-    tma_load_4d(smem_u32(sm) + (uint32_t)buf * buf_bytes, &p->tm_src, 0, e0 * p->step_h + p->off_h[pl],
-                p->c_base + CHUNK * cc, n, bar);
-  };
-  const uint32_t total = na + nb;
-  uint32_t u = blockIdx.x;
-  int fills[kPackBufs] = {};  // copies issued into each buffer (thread 0)
-  if (threadIdx.x == 0)
-    for (int i = 0; i < kPackBufs - 1; ++i)
-      if (u + (uint32_t)i * gridDim.x < total) {
-        issue(u + (uint32_t)i * gridDim.x, i);
-        ++fills[i];
-      }
-  for (int it = 0; u < total; ++it, u += gridDim.x) {
-    const int buf = it % kPackBufs;
-    // the buffer of iteration it - 1 was released by that iteration's barrier
-    const uint32_t ahead = u + (uint32_t)(kPackBufs - 1) * gridDim.x;
-    if (threadIdx.x == 0 && ahead < total) {
-      issue(ahead, (it + kPackBufs - 1) % kPackBufs);
-      ++fills[(it + kPackBufs - 1) % kPackBufs];
-    }
-    // every thread reaches the barrier below whether or not its wait succeeded, then all leave
-    // together if any wait expired
-    if (mbar_wait(smem_u32(&bars[buf]), (uint32_t)((it / kPackBufs) & 1), &abort_flag, &g_wgmn_err)) {
-    const NhwcPackPlan* p;
-    uint32_t sl;
-    int e0;
-    locate(u, p, sl, e0);
-    const uint32_t r = fdiv(sl, p->fd_N);
-    const uint32_t pl = fdiv(r, p->fd_nchunk);
-    const int cc = (int)(r - pl * (uint32_t)p->nchunk);
-    const int nch = p->C - CHUNK * cc < CHUNK ? p->C - CHUNK * cc : CHUNK;
-    const int rows = p->EX - e0 < p->ER ? p->EX - e0 : p->ER;
-    const uint8_t* src = sm + (size_t)buf * buf_bytes;  // [channel][row][W]
-    uint4* dst = reinterpret_cast<uint4*>(p->dst) + ((long long)sl * p->EX + e0) * p->WL;
-    const int W = p->W, ER = p->ER;
-    for (int i = threadIdx.x; i < rows * p->WL; i += kPackTmaThreads) {
-      const int er = (int)fdiv((uint32_t)i, p->fd_WL);
-      const int f = i - er * p->WL;
-      const int w = f * p->step_w + p->off_w[pl];
-      uint32_t q[4] = {0u, 0u, 0u, 0u};
-      if (w >= 0 && w < W) {
+  constexpr int NW = (R + SW * (CHUNK - 1)) / CHUNK + 1;
+  using E = typename std::conditional<DT == 0, uint32_t, uint16_t>::type;
+  const E* row0 = static_cast<const E*>(row0_v);  // channel 0 of the source row (NULL: outside)
+  uint4 v[CHUNK][NW];
 #pragma unroll
-        for (int c = 0; c < CHUNK; ++c) {
-          if (c < nch) {
-            const size_t o = ((size_t)c * ER + er) * W + w;
-            if constexpr (DT == 0) q[c] = reinterpret_cast<const uint32_t*>(src)[o];
-            else q[c >> 1] |= (uint32_t)reinterpret_cast<const uint16_t*>(src)[o] << (16 * (c & 1));
-          }
-        }
+  for (int c = 0; c < CHUNK; ++c)
+#pragma unroll
+    for (int q = 0; q < NW; ++q) {
+      v[c][q] = make_uint4(0u, 0u, 0u, 0u);
+      const int col = wbase + q * CHUNK;
+      if (row0 != nullptr && c < nch && col >= 0 && col + CHUNK <= W)
+        v[c][q] = __ldg(reinterpret_cast<const uint4*>(row0 + (long long)c * HW + col));
+    }
+#pragma unroll
+  for (int i = 0; i < CHUNK; ++i) {
+    if (i >= nout) break;
+    const int j = R + SW * i;  // window element of output i
+    uint32_t o[4];
+    if constexpr (DT == 0) {
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const uint4 wv = v[c][j / 4];
+        o[c] = (j % 4) == 0 ? wv.x : (j % 4) == 1 ? wv.y : (j % 4) == 2 ? wv.z : wv.w;
       }
-      dst[i] = make_uint4(q[0], q[1], q[2], q[3]);
+    } else {
+#pragma unroll
+      for (int q2 = 0; q2 < 4; ++q2) {
+        const uint4 wa = v[2 * q2][j / 8], wb = v[2 * q2 + 1][j / 8];
+        const int e = (j % 8) / 2;
+        const uint32_t ra = e == 0 ? wa.x : e == 1 ? wa.y : e == 2 ? wa.z : wa.w;
+        const uint32_t rb = e == 0 ? wb.x : e == 1 ? wb.y : e == 2 ? wb.z : wb.w;
+        o[q2] = __byte_perm(ra, rb, (j & 1) ? 0x7632 : 0x5410);
+      }
     }
-    }
-    __syncthreads();  // the buffer is read before it is refilled
-    if (abort_flag) break;
+    dst[i] = make_uint4(o[0], o[1], o[2], o[3]);
   }
-  // leave no copy in flight into shared memory (after an abort); bounded
-  if (threadIdx.x == 0 && abort_flag) {
-    for (int bI = 0; bI < kPackBufs; ++bI)
-      if (fills[bI] > 0) mbar_wait_drain(smem_u32(&bars[bI]), (uint32_t)((fills[bI] - 1) & 1));
+}
+
+template <int DT, int SW, int Rn>
+__device__ __forceinline__ void pack_words_dispatch(int R, const void* row0, long long HW, int W, int wbase, int nch,
+                                                    int nout, uint4* dst) {
+  if constexpr (Rn > 0) {
+    if (R == Rn - 1) {
+      pack_words_item<DT, SW, Rn - 1>(row0, HW, W, wbase, nch, nout, dst);
+      return;
+    }
+    pack_words_dispatch<DT, SW, Rn - 1>(R, row0, HW, W, wbase, nch, nout, dst);
+  }
+}
+
+// Items run position block fastest, then padded row, then slab (plane, chunk, image), the items
+// of plan `a` first, then those of plan `b` (b.src NULL: none): packs of x and dy in one launch.
+template <int DT>
+__global__ void __launch_bounds__(256) nhwc_pack_words_kernel(const __grid_constant__ NhwcPackPlan a,
+                                                              const __grid_constant__ NhwcPackPlan b) {
+  constexpr int CHUNK = DT == 0 ? 4 : 8;
+  using E = typename std::conditional<DT == 0, uint32_t, uint16_t>::type;
+  const uint32_t na = a.witems, nb = b.src != nullptr ? b.witems : 0u;
+  for (uint32_t it = blockIdx.x * blockDim.x + threadIdx.x; it < na + nb; it += gridDim.x * blockDim.x) {
+    const bool first = it < na;
+    const NhwcPackPlan& p = first ? a : b;
+    const uint32_t v = first ? it : it - na;
+    const uint32_t rowi = fdiv(v, p.fd_nblk);        // (slab, padded row)
+    const int blk = (int)(v - rowi * p.fd_nblk.d);
+    const uint32_t sl = fdiv(rowi, p.fd_EX);
+    const int e = (int)(rowi - sl * (uint32_t)p.EX);
+    const uint32_t r = fdiv(sl, p.fd_N);
+    const int n = (int)(sl - r * (uint32_t)p.N);
+    const uint32_t pl = fdiv(r, p.fd_nchunk);
+    const int cc = (int)(r - pl * (uint32_t)p.nchunk);
+    const int nch = p.C - CHUNK * cc < CHUNK ? p.C - CHUNK * cc : CHUNK;
+    const int h = e * p.step_h + p.off_h[pl];
+    const long long HW = (long long)p.H * p.W;
+    const E* row0 = (h >= 0 && h < p.H)
+                        ? static_cast<const E*>(p.src) + (long long)n * p.src_nstride + (long long)(CHUNK * cc) * HW +
+                              (long long)h * p.W
+                        : nullptr;
+    const int f0 = blk * CHUNK;
+    const int nout = p.WL - f0 < CHUNK ? p.WL - f0 : CHUNK;
+    const int R = p.off_w[pl] - p.xs[pl];
+    const int wbase = f0 * p.step_w + p.xs[pl];
+    uint4* dst = reinterpret_cast<uint4*>(p.dst) + ((long long)sl * p.EX + e) * p.WL + f0;
+    if (p.step_w == 1)
+      pack_words_dispatch<DT, 1, CHUNK>(R, row0, HW, p.W, wbase, nch, nout, dst);
+    else
+      pack_words_dispatch<DT, 2, CHUNK>(R, row0, HW, p.W, wbase, nch, nout, dst);
   }
 }
 
@@ -549,29 +537,15 @@ cudaError_t launch_wgrad_mn(const WgradMnPlan& p, int grid, cudaStream_t st) {
   return cudaGetLastError();
 }
 
-size_t nhwc_pack_tma_smem(const NhwcPackPlan& a, const NhwcPackPlan& b, int dt) {
-  const size_t chunk = dt == 0 ? 4 : 8, esz = dt == 0 ? 4 : 2;
-  const int ra = a.ER, rb = b.src != nullptr ? b.ER : 0;
-  const int rows = ra > rb ? ra : rb, W = b.src != nullptr && b.W > a.W ? b.W : a.W;
-  return kPackBufs * ((chunk * rows * W * esz + 1023) & ~size_t(1023)) + 1024;
-}
-
-static std::atomic<int> g_pack_smem_set[2][kMaxDevices];
-
-// Packs a and (if b.src is not NULL) b in one launch; both copy-engine or both plain.
+// Packs a and (if b.src is not NULL) b in one launch; the word kernel when both allow it.
 cudaError_t launch_nhwc_pack(const NhwcPackPlan& a, const NhwcPackPlan& b, int dt, int num_sms, cudaStream_t st) {
-  if (a.use_tma && (b.src == nullptr || b.use_tma)) {
-    const long long units = (long long)a.tma_units + (b.src != nullptr ? (long long)b.tma_units : 0ll);
-    const size_t smem = nhwc_pack_tma_smem(a, b, dt);
-    const long long per_sm = std::max<long long>(1, std::min<long long>(8, (220ll << 10) / (long long)smem));
-    const unsigned blocks = (unsigned)std::max(1ll, std::min<long long>(units, (long long)num_sms * per_sm));
-    cudaError_t e = dt == 0 ? ensure_dyn_smem(nhwc_pack_tma_kernel<0>, smem, g_pack_smem_set[0])
-                            : ensure_dyn_smem(nhwc_pack_tma_kernel<1>, smem, g_pack_smem_set[1]);
-    if (e != cudaSuccess) return e;
+  if (a.words && (b.src == nullptr || b.words)) {
+    const long long items = (long long)a.witems + (b.src != nullptr ? (long long)b.witems : 0ll);
+    const unsigned blocks = (unsigned)std::max(1ll, std::min<long long>((items + 255) / 256, (long long)num_sms * 8));
     if (dt == 0)
-      nhwc_pack_tma_kernel<0><<<blocks, kPackTmaThreads, smem, st>>>(a, b);
+      nhwc_pack_words_kernel<0><<<blocks, 256, 0, st>>>(a, b);
     else
-      nhwc_pack_tma_kernel<1><<<blocks, kPackTmaThreads, smem, st>>>(a, b);
+      nhwc_pack_words_kernel<1><<<blocks, 256, 0, st>>>(a, b);
     return cudaGetLastError();
   }
   const long long warps = (long long)a.units + (b.src != nullptr ? (long long)b.units : 0ll);
