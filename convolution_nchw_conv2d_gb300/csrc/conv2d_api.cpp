@@ -152,11 +152,41 @@ struct TapBuild {
   PackPlan pp;
   size_t pack_bytes;
   int grid;
+  NhwcPackPlan px;        // channel-chunk pack of the source planes (when p.a_tma)
+  size_t src_pack_bytes;  // its size: planes * chunks * positions * 16 bytes
 };
+
+bool setup_pack_tiles(NhwcPackPlan& q, int esz);
+bool encode_mn_map(CUtensorMap* m, const void* base, int rank, const uint64_t* dims, const uint32_t* box);
+
+// MMA operand offsets of every tap within a pipeline stage, in 16-byte units, once the tile
+// shape (NCH channel chunks of `rows` rows per plane, NT filter rows per chunk) is fixed.  A
+// stage holds, per source plane, NCH chunk blocks of `rows` position rows, and per tap of the
+// phase NCH chunk blocks of NT filter rows.  In tap-pair mode (NCH == 1) the even tap of each
+// pair also carries the row distance to the odd tap in bits 16..29, the field the descriptor
+// reads as its K-direction (leading byte) offset, so that one K = 2-chunk MMA covers both.
+void fill_tap_offsets(TapPlan& p, int NCH) {
+  for (int ph = 0; ph < p.nph; ++ph)
+    for (int i = 0; i < p.ph_ntaps[ph]; ++i) {
+      const int t = p.ph_tap_begin[ph] + i;
+      const int oa = p.tap_plane[t] * NCH * p.rows + p.tap_off[t];
+      if (NCH >= 2) {
+        p.tap_a[t] = oa;
+        p.tap_b[t] = i * NCH * p.NT;
+      } else if ((i & 1) == 0) {
+        const int ob = p.tap_plane[t + 1] * p.rows + p.tap_off[t + 1];
+        p.tap_a[t] = (int)((uint32_t)oa | ((uint32_t)(ob - oa) << 16));
+        p.tap_b[t] = i * p.NT;
+      } else {
+        p.tap_a[t] = 0;
+        p.tap_b[t] = 0;
+      }
+    }
+}
 
 // Chooses MH, NT, CB, ACCB and the stage count for a TapPlan whose geometry (linear
 // space, planes, phases, taps) is already filled in.  Returns false if nothing fits.
-bool choose_tap_tiles(TapPlan& p, int max_off, int dt, const DevInfo& di, bool pair_taps) {
+bool choose_tap_tiles(TapPlan& p, int max_off, int dt, const DevInfo& di, bool pair_taps, bool a_tma) {
   const int CHUNK = dt == 0 ? 4 : 8;
   const size_t budget = di.smem_optin - 2048;
   int nt_cands[2];
@@ -189,20 +219,39 @@ bool choose_tap_tiles(TapPlan& p, int max_off, int dt, const DevInfo& di, bool p
       for (int ci = 0; ci < ncand; ++ci) {
         const int CB = cb_cands[ci];
         const int NCH = CB / CHUNK;
-        const int rows = round_up(128 * mh + max_off + (pair_taps ? 1 : 0), 8);
+        int rows = round_up(128 * mh + max_off + (pair_taps ? 1 : 0), 8);
+        // tensor-copied rows: equal boxes of at most 128 rows (256 8-byte elements), a multiple
+        // of 8 rows each; the box count that pads the rows least
+        int nbox = 1, box = rows;
+        if (a_tma) {
+          const int n0 = (rows + 127) / 128;
+          box = 1 << 30;
+          for (int nb = n0; nb < n0 + 4; ++nb) {
+            const int bx = round_up((rows + nb - 1) / nb, 8);
+            if (nb * bx < nbox * box) {
+              nbox = nb;
+              box = bx;
+            }
+          }
+        }
+        rows = nbox * box;
+        if (a_tma && 2 * (p.Mtot + rows) >= (1ll << 31)) return false;  // 32-bit copy coordinates
         const long long a_bytes = (long long)p.npl * NCH * rows * 16;
         const long long b_bytes = (long long)p.max_taps_ph * NCH * NT * 16;
-        const long long fixed = 8ll * p.ntaps_total + 8 * (3 * 4 + 6) + 24 + 4 * 4 + 1024;
+        const long long fixed = 8 * (3 * 4 + 6) + 24 + 4 * 4 + 1024;
         const long long per = a_bytes + b_bytes;
         long long stages = ((long long)budget - fixed) / per;
         if (stages < 2) continue;
         if (stages > 4) stages = 4;
-        if (b_bytes >= (1 << 20)) continue;  // mbarrier transaction-count limit
+        if (b_bytes + (a_tma ? a_bytes : 0) >= (1 << 20)) continue;  // mbarrier transaction-count limit
         p.NT = NT;
         p.n_ntiles = n_ntiles;
         p.MH = mh;
         p.CB = CB;
         p.rows = rows;
+        p.a_tma = a_tma ? 1 : 0;
+        p.a_box = box;
+        p.a_nbox = nbox;
         p.a_stage_bytes = (int)a_bytes;
         p.b_stage_bytes = (int)b_bytes;
         p.stages = (int)stages;
@@ -212,11 +261,55 @@ bool choose_tap_tiles(TapPlan& p, int max_off, int dt, const DevInfo& di, bool p
         p.nkb = (p.Cs + CB - 1) / CB;
         p.n_mtiles = (int)mtiles;
         p.total_tiles = (long long)p.nph * p.n_mtiles * p.n_ntiles;
-        if (tap_gemm_smem_bytes(p) <= di.smem_optin) return true;
+        if (tap_gemm_smem_bytes(p) <= di.smem_optin) {
+          fill_tap_offsets(p, NCH);
+          return true;
+        }
       }
     }
   }
   return false;
+}
+
+// The channel-chunk pack of a tap plan's source planes: plane pl at linear position
+// L = n*EL*WL + e*WL + f holds the source pixel (e*pl_step_h + pl_off_h[pl], f*pl_step_w +
+// pl_off_w[pl]) of image n, zero outside the tensor -- the pixel the producers' direct loads
+// read for staged row L.  The destination is set once the workspace is laid out.
+void fill_src_pack(TapBuild& b, int dt) {
+  const TapPlan& p = b.p;
+  NhwcPackPlan& q = b.px;
+  std::memset(&q, 0, sizeof(q));
+  const int CHUNK = dt == 0 ? 4 : 8;
+  q.src = p.src;
+  q.src_nstride = p.src_nstride;
+  q.N = p.N;
+  q.C = p.Cs;
+  q.H = p.Hs;
+  q.W = p.Ws;
+  q.nchunk = (p.Cs + CHUNK - 1) / CHUNK;
+  q.EX = p.EL;
+  q.WL = p.WL;
+  q.fd_WL = make_fastdiv((uint32_t)p.WL);
+  q.npl = p.npl;
+  q.step_h = p.pl_step_h;
+  q.step_w = p.pl_step_w;
+  for (int pl = 0; pl < p.npl; ++pl) {
+    q.off_h[pl] = p.pl_off_h[pl];
+    q.off_w[pl] = p.pl_off_w[pl];
+  }
+  b.src_pack_bytes = (size_t)q.npl * q.nchunk * (size_t)p.Mtot * 16;
+}
+
+// Packed-source staging is planned when the caller allows the workspace for it, the pack has a
+// work-unit tiling (fill_src_pack, then setup_pack_tiles), and the copy pays: bf16 sources, and
+// fp32 sources of one channel chunk (the direct loads then fill a quarter of each staged row
+// with 3 or fewer channels).  For fp32 sources of several chunks the extra pass over the
+// 4-byte tensor costs more than the staging it saves (measured on the 3x3, strided and 1x1
+// layers: the direct producers keep up with the MMAs there).
+bool packed_src_ok(TapBuild& b, int dt) {
+  if (dt == 0 && b.p.Cs > 4) return false;
+  fill_src_pack(b, dt);
+  return setup_pack_tiles(b.px, dt == 0 ? 4 : 2);
 }
 
 void fill_pack(TapBuild& b, const Desc& d, const void* w, void* wpack, int transpose,
@@ -281,11 +374,12 @@ void order_phase_taps(std::vector<int>& pl, std::vector<int>& off, std::vector<i
 // Taps u = r*S + s in [u_lo, u_hi) only (the whole filter by default).  A partial tap set
 // moves the staged window down by its smallest tap row (plane offsets up, tap offsets
 // down by the same rows), so that the window holds no rows that none of its taps reads.
-int build_fwd(const Desc& d0, const void* x, const void* w, void* y, void* ws, const DevInfo& di,
-              TapBuild& b, int u_lo = 0, int u_hi = 1 << 30) {
+int build_fwd_impl(const Desc& d0, const void* x, const void* w, void* y, void* ws, const DevInfo& di,
+                   TapBuild& b, int u_lo, int u_hi, bool packed_src, bool pair) {
   const Desc d = flatten_pointwise(d0);
   TapPlan& p = b.p;
   std::memset(&p, 0, sizeof(p));
+  b.src_pack_bytes = 0;
   p.src = x;
   p.dst = y;
   p.N = d.N;
@@ -316,7 +410,6 @@ int build_fwd(const Desc& d0, const void* x, const void* w, void* y, void* ws, c
   p.nph = 1;
   p.ph_step_h = 1;
   p.ph_step_w = 1;
-  const bool pair = d.C <= CHUNK;
   std::vector<int> tpl, toff, tr, ts;
   int min_row = 1 << 30;
   for (int r = 0; r < d.R; ++r)
@@ -346,7 +439,10 @@ int build_fwd(const Desc& d0, const void* x, const void* w, void* y, void* ws, c
     p.tap_plane[t] = tpl[t];
     p.tap_off[t] = toff[t];
   }
-  if (!choose_tap_tiles(p, max_off, d.dt, di, pair)) return CONV2D_ERR_UNSUPPORTED;
+  const bool a_tma = packed_src && packed_src_ok(b, d.dt);
+  if (!choose_tap_tiles(p, max_off, d.dt, di, pair, a_tma) && !(a_tma && choose_tap_tiles(p, max_off, d.dt, di, pair, false)))
+    return CONV2D_ERR_UNSUPPORTED;
+  if (!p.a_tma) b.src_pack_bytes = 0;
   p.wpack = ws;
   fill_pack(b, d, w, ws, 0, tr, ts);
   b.grid = (int)std::min<long long>(p.total_tiles, di.sms);
@@ -355,11 +451,12 @@ int build_fwd(const Desc& d0, const void* x, const void* w, void* y, void* ws, c
 
 // Taps u = r*S + s in [u_lo, u_hi) only, with the staged window moved down by the
 // smallest tap row as in build_fwd.
-int build_bwd_data(const Desc& d0, const void* dy, const void* w, void* dx, void* ws, const DevInfo& di,
-                   TapBuild& b, int u_lo = 0, int u_hi = 1 << 30) {
+int build_bwd_data_impl(const Desc& d0, const void* dy, const void* w, void* dx, void* ws, const DevInfo& di,
+                        TapBuild& b, int u_lo, int u_hi, bool packed_src, bool pair) {
   const Desc d = flatten_pointwise(d0);
   TapPlan& p = b.p;
   std::memset(&p, 0, sizeof(p));
+  b.src_pack_bytes = 0;
   p.src = dy;
   p.dst = dx;
   p.N = d.N;
@@ -425,7 +522,6 @@ int build_bwd_data(const Desc& d0, const void* dy, const void* w, void* dx, void
   p.nph = d.sh * d.sw;
   p.ph_step_h = d.sh;
   p.ph_step_w = d.sw;
-  const bool pair = d.K <= CHUNK;
   std::vector<int> tpl, toff, tr, ts;
   int max_taps = 0, min_row = 1 << 30, n_real = 0;
   for (int a = 0; a < d.sh; ++a)
@@ -472,12 +568,50 @@ int build_bwd_data(const Desc& d0, const void* dy, const void* w, void* dx, void
     p.tap_plane[t] = tpl[t];
     p.tap_off[t] = toff[t];
   }
-  if (!choose_tap_tiles(p, max_off, d.dt, di, pair)) return CONV2D_ERR_UNSUPPORTED;
+  const bool a_tma = packed_src && p.ntaps_total > 0 && packed_src_ok(b, d.dt);
+  if (!choose_tap_tiles(p, max_off, d.dt, di, pair, a_tma) && !(a_tma && choose_tap_tiles(p, max_off, d.dt, di, pair, false)))
+    return CONV2D_ERR_UNSUPPORTED;
+  if (!p.a_tma) b.src_pack_bytes = 0;
   p.wpack = ws;
   fill_pack(b, d, w, ws, 1, tr, ts);
   if (p.ntaps_total == 0) b.pack_bytes = 0;
   b.grid = (int)std::min<long long>(p.total_tiles, di.sms);
   return CONV2D_OK;
+}
+
+// Tap-pair mode (one MMA of K = two 16-byte chunks covers one chunk of two taps) is natural
+// when the source has at most one chunk of channels.  With more channels a stage normally holds
+// two or more chunks of every tap of the phase; when that caps the tile's N below what the
+// destination channels want, pair mode, whose stages hold one chunk (half the filter slice),
+// is planned as well and kept if it reaches a wider N.
+template <class Impl>
+int build_tap_pass(Impl impl, int Cs, int Cd, int dt, TapBuild& b) {
+  const int CHUNK = dt == 0 ? 4 : 8;
+  const bool natural = Cs <= CHUNK;
+  const int rc = impl(b, natural);
+  if (natural || (rc != CONV2D_OK && rc != CONV2D_ERR_UNSUPPORTED)) return rc;
+  if (rc == CONV2D_OK && b.p.NT >= std::min(256, round_up(Cd, 16))) return rc;
+  TapBuild b2;
+  const int rc2 = impl(b2, true);
+  if (rc2 == CONV2D_OK && (rc != CONV2D_OK || b2.p.NT > b.p.NT)) {
+    b = b2;
+    return CONV2D_OK;
+  }
+  return rc;
+}
+
+int build_fwd(const Desc& d, const void* x, const void* w, void* y, void* ws, const DevInfo& di, TapBuild& b,
+              int u_lo = 0, int u_hi = 1 << 30, bool packed_src = false) {
+  return build_tap_pass(
+      [&](TapBuild& bb, bool pair) { return build_fwd_impl(d, x, w, y, ws, di, bb, u_lo, u_hi, packed_src, pair); },
+      d.C, d.K, d.dt, b);
+}
+
+int build_bwd_data(const Desc& d, const void* dy, const void* w, void* dx, void* ws, const DevInfo& di, TapBuild& b,
+                   int u_lo = 0, int u_hi = 1 << 30, bool packed_src = false) {
+  return build_tap_pass(
+      [&](TapBuild& bb, bool pair) { return build_bwd_data_impl(d, dy, w, dx, ws, di, bb, u_lo, u_hi, packed_src, pair); },
+      d.K, d.C, d.dt, b);
 }
 
 // ------------------------------------------------------------------ tensor maps
@@ -968,21 +1102,33 @@ bool encode_mn_map(CUtensorMap* m, const void* base, int rank, const uint64_t* d
   return r == CUDA_SUCCESS;
 }
 
-// Word variant of a pack (NhwcPackPlan::words): needs rows of whole 16-byte words, an aligned
-// tensor (sizing calls pass none: planned as aligned) and step_w 1 or 2; false (plain pack)
-// otherwise.
-bool setup_pack_words(NhwcPackPlan& q, const void* base, int esz) {
-  q.words = 0;
+// Work-unit tiling of a pack (NhwcPackPlan): the most padded rows per unit whose staged channel
+// runs fit 32 KB of shared memory (at least one row, then up to 200 KB); false if none fits or
+// the unit count passes 32 bits.
+bool setup_pack_tiles(NhwcPackPlan& q, int esz) {
   const int CHUNK = 16 / esz;
-  if ((q.W * esz) % 16 != 0 || ((uintptr_t)base & 15) != 0 || (q.step_w != 1 && q.step_w != 2)) return false;
-  const long long nblk = (q.WL + CHUNK - 1) / CHUNK;
-  const long long items = nblk * q.EX * q.npl * q.nchunk * q.N;
-  if (items >= (1ll << 31)) return false;
-  for (int pl = 0; pl < q.npl; ++pl) q.xs[pl] = floor_div(q.off_w[pl], CHUNK) * CHUNK;
-  q.words = 1;
-  q.witems = (unsigned)items;
-  q.fd_nblk = make_fastdiv((uint32_t)nblk);
-  q.fd_EX = make_fastdiv((uint32_t)q.EX);
+  int lo = q.off_h[0], hi = q.off_h[0];
+  for (int pl = 1; pl < q.npl; ++pl) {
+    lo = std::min(lo, q.off_h[pl]);
+    hi = std::max(hi, q.off_h[pl]);
+  }
+  q.off_h_min = lo;
+  q.h_span = hi - lo;
+  auto pitch = [&](int te) {  // elements per staged channel run, rounded up to 16 bytes
+    const long long rows = std::min<long long>((long long)(te - 1) * q.step_h + q.h_span + 1, q.H);
+    return (rows * q.W * esz + 15) / 16 * 16 / esz;
+  };
+  int te = 1;
+  while (te < q.EX && (long long)CHUNK * pitch(te + 1) * esz <= 32 * 1024) ++te;
+  if ((long long)CHUNK * pitch(te) * esz > 200 * 1024) return false;
+  q.te = te;
+  q.ch_pitch = (int)pitch(te);
+  q.n_etiles = (q.EX + te - 1) / te;
+  const long long units = (long long)q.N * q.nchunk * q.n_etiles;
+  if (units >= (1ll << 31)) return false;
+  q.units = (unsigned)units;
+  q.fd_et = make_fastdiv((uint32_t)q.n_etiles);
+  q.fd_nchunk = make_fastdiv((uint32_t)q.nchunk);
   return true;
 }
 
@@ -1144,17 +1290,8 @@ int build_wgrad_mn(const Desc& d, const void* x, const void* dy, void* dw, void*
   pd.fd_WL = make_fastdiv((uint32_t)WL);
   pd.npl = 1;
   pd.step_h = pd.step_w = 1;
-  // word packs when both sources allow them (one launch runs both)
-  if (!(setup_pack_words(px, x, 2) && setup_pack_words(pd, dy, 2))) px.words = pd.words = 0;
-  for (NhwcPackPlan* q : {&px, &pd}) {
-    const long long upp = ((long long)q->EX * q->WL + kPackUnit - 1) / kPackUnit;
-    const long long units = upp * q->npl * q->nchunk * q->N;
-    if (units >= (1ll << 31) || (long long)q->EX * q->WL >= (1ll << 31)) return CONV2D_ERR_TOO_LARGE;
-    q->units = (unsigned)units;
-    q->fd_upp = make_fastdiv((uint32_t)upp);
-    q->fd_N = make_fastdiv((uint32_t)q->N);
-    q->fd_nchunk = make_fastdiv((uint32_t)q->nchunk);
-  }
+  if ((long long)EX * WL >= (1ll << 31)) return CONV2D_ERR_TOO_LARGE;
+  if (!setup_pack_tiles(px, 2) || !setup_pack_tiles(pd, 2)) return CONV2D_ERR_UNSUPPORTED;
   // tensor maps over the packed planes (sizing calls pass no workspace)
   if (w8 != nullptr) {
     const uint64_t xd[3] = {2 * (uint64_t)Mtot, (uint64_t)C8, (uint64_t)npl};
@@ -1238,11 +1375,14 @@ constexpr int kMaxTapPasses = 16;
 
 struct TapSet {
   std::vector<TapBuild> pass;
-  size_t pack_bytes = 0;  // workspace for all passes' repacked filters
+  size_t pack_bytes = 0;  // workspace for all passes' repacked filters (and the packed source)
 };
 
+// packed_src: a single-pass plan may stage its source rows from a channel-chunk packed copy
+// of the source, placed in the workspace after the repacked filter (the allocation-free entry
+// point passes false: its scratch holds the filter only).
 int build_tap_set(int op, const Desc& d, const void* src, const void* w, void* dst, void* ws, const DevInfo& di,
-                  TapSet& out) {
+                  TapSet& out, bool packed_src) {
   const int RS = d.R * d.S;
   for (int n = 1; n <= std::min(RS, kMaxTapPasses); ++n) {
     TapSet set;
@@ -1252,11 +1392,23 @@ int build_tap_set(int op, const Desc& d, const void* src, const void* w, void* d
       const int lo = (int)((long long)RS * i / n), hi = (int)((long long)RS * (i + 1) / n);
       void* wsi = ws != nullptr ? static_cast<void*>(static_cast<uint8_t*>(ws) + off) : nullptr;
       TapBuild b;
-      rc = op == CONV2D_OP_FWD ? build_fwd(d, src, w, dst, wsi, di, b, n == 1 ? 0 : lo, n == 1 ? 1 << 30 : hi)
-                               : build_bwd_data(d, src, w, dst, wsi, di, b, n == 1 ? 0 : lo, n == 1 ? 1 << 30 : hi);
+      const bool pk = packed_src && n == 1;
+      rc = op == CONV2D_OP_FWD ? build_fwd(d, src, w, dst, wsi, di, b, n == 1 ? 0 : lo, n == 1 ? 1 << 30 : hi, pk)
+                               : build_bwd_data(d, src, w, dst, wsi, di, b, n == 1 ? 0 : lo, n == 1 ? 1 << 30 : hi, pk);
       if (rc != CONV2D_OK) break;
       off += i + 1 < n ? align_ws(b.pack_bytes) : b.pack_bytes;
       set.pass.push_back(b);
+    }
+    if (rc == CONV2D_OK && n == 1 && set.pass[0].p.a_tma) {
+      TapBuild& b = set.pass[0];
+      const size_t xoff = align_ws(off);
+      off = xoff + b.src_pack_bytes;
+      b.px.dst = ws != nullptr ? static_cast<void*>(static_cast<uint8_t*>(ws) + xoff) : nullptr;
+      if (ws != nullptr) {  // sizing calls pass no workspace
+        const uint64_t dims[3] = {2 * (uint64_t)b.p.Mtot, (uint64_t)b.px.nchunk, (uint64_t)b.px.npl};
+        const uint32_t box[3] = {2 * (uint32_t)b.p.a_box, 1u, 1u};
+        if (!encode_mn_map(&b.p.tm_src, b.px.dst, 3, dims, box)) return CONV2D_ERR_UNSUPPORTED;
+      }
     }
     if (rc == CONV2D_OK) {
       set.pack_bytes = off;
@@ -1423,7 +1575,7 @@ int workspace_size_uncached(int op, const Desc& d, size_t* bytes) {
   const DevInfo di = device_info();
   if (op == CONV2D_OP_FWD || op == CONV2D_OP_BWD_DATA) {
     TapSet set;
-    rc = build_tap_set(op, d, nullptr, nullptr, nullptr, nullptr, di, set);
+    rc = build_tap_set(op, d, nullptr, nullptr, nullptr, nullptr, di, set, true);
     if (rc) return rc;
     *bytes = set.pack_bytes;
     return CONV2D_OK;
@@ -1479,7 +1631,7 @@ static int run_tap(int op, const Desc& d, int groups, const void* src, const voi
   TapSet set;
   const PlanKey key = make_key(op, dg, src, w, dst, ws);
   if (!g_tap_plans.get(key, set)) {
-    rc = build_tap_set(op, dg, src, w, dst, ws, di, set);
+    rc = build_tap_set(op, dg, src, w, dst, ws, di, set, true);
     if (rc) return rc;
     g_tap_plans.put(key, set);
   }
@@ -1504,6 +1656,13 @@ static int run_tap(int op, const Desc& d, int groups, const void* src, const voi
       b.p.dst = const_cast<uint8_t*>(byte_ptr(dst)) + gi * dst_g * esz;
       b.pp.w = byte_ptr(w) + gi * w_g * esz;
       b.p.bias = bias != nullptr && pi == 0 ? byte_ptr(bias) + gi * bias_g * esz : nullptr;
+      if (b.p.a_tma) {  // the group's source, packed channel-chunk-wise for the tensor copies
+        b.px.src = b.p.src;
+        NhwcPackPlan none;
+        std::memset(&none, 0, sizeof(none));
+        rc = launch_err(launch_nhwc_pack(b.px, none, d.dt, di.sms, st));
+        if (rc) return rc;
+      }
       if (b.pack_bytes) {
         rc = launch_err(launch_pack_filter(b.pp, d.dt, st));
         if (rc) return rc;
@@ -1721,7 +1880,7 @@ int conv2d_fwd_noalloc(int N, int C, int H, int W, int K, int R, int S, int pad_
   TapSet set;
   const PlanKey key = make_key(CONV2D_OP_FWD, d, x, w, y, scratch);
   if (!g_tap_plans.get(key, set)) {
-    rc = build_tap_set(CONV2D_OP_FWD, d, x, w, y, scratch, di, set);
+    rc = build_tap_set(CONV2D_OP_FWD, d, x, w, y, scratch, di, set, false);
     if (rc) return rc;
     g_tap_plans.put(key, set);
   }

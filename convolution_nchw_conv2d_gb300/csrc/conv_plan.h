@@ -55,6 +55,14 @@ constexpr int kMaxTaps = 256;    // R * S
 // Forward and backward-data: D[position, out_channel] = sum over taps and source
 // channels of S[channel, position + tap_off] * Wpacked[tap, out_channel, channel].
 struct TapPlan {
+  // Source planes packed channel-chunk-wise ([plane][chunk][position L][16 bytes]: CHUNK
+  // consecutive channels of the plane's pixel at L, zero outside the tensor) as a 3-D tensor
+  // of 8-byte elements (2*L, chunk, plane); valid when a_tma.  A stage's staged rows of one
+  // plane and chunk are then one contiguous run, loaded by tensor copies of a_box rows (the
+  // rows past the last position read as zero).
+  CUtensorMap tm_src;
+  int a_tma;             // 1: staged rows come from tm_src (rows = a_nbox * a_box)
+  int a_box, a_nbox;
   const void* src;       // x (forward) or dy (backward-data), NCHW
   void* dst;             // y or dx, NCHW
   const void* bias;      // optional, one value per destination channel (NULL: none)
@@ -81,6 +89,11 @@ struct TapPlan {
   int ntaps_total;
   int tap_plane[kMaxTaps];
   int tap_off[kMaxTaps];
+  // MMA operand offsets of tap t within a stage, in 16-byte units: tap_a = A rows (plane * NCH *
+  // rows + tap_off; in tap-pair mode, NCH = 1, the pair's first tap also carries the chunk stride
+  // to its second tap in bits 16..29, the descriptor's leading-byte-offset field), tap_b = B
+  // (index within the phase * NCH * NT).  Filled once the tile shape is chosen.
+  int tap_a[kMaxTaps], tap_b[kMaxTaps];
   int stages;
   int MH;                // 128-row halves per tile (1 or 2)
   int NT;                // GEMM N per tile (multiple of 16, <= 256)
@@ -225,8 +238,11 @@ struct ReducePlan {
 // column lies outside the source.  Every 16-byte group holds CHUNK consecutive channels of one
 // position, so a tile of positions x channel chunks is one tensor copy into the MN-major operand
 // layout, and a shift of the position by one is a shift of one 16-byte row.
-constexpr int kPackUnit = 128;  // positions per warp work unit of the channel-chunk pack
-
+//
+// Work unit = (image n, chunk cc, tile of te padded rows e): the CHUNK source channels' rows that
+// the tile's planes read, [h_lo, h_lo + span] with h_lo = e0*step_h + off_h_min, are one
+// contiguous run per channel, staged in shared memory by coalesced loads; the unit's output of
+// each plane is one contiguous run of te*WL 16-byte groups.
 struct NhwcPackPlan {
   const void* src;
   void* dst;
@@ -238,16 +254,12 @@ struct NhwcPackPlan {
   int npl;                // planes
   int step_h, step_w;
   int off_h[kMaxPlanes], off_w[kMaxPlanes];
-  // work units of kPackUnit positions: upp per slab, units = upp * npl * nchunk * N (< 2^31)
-  unsigned units;
-  FastDiv fd_upp, fd_N, fd_nchunk;
-  // Word variant (words): rows of whole 16-byte words, an aligned tensor, step_w 1 or 2; items of
-  // CHUNK positions (witems = npl * nchunk * N * EX * nblk), xs[pl] = off_w[pl] rounded down to a
-  // multiple of CHUNK.
-  int words;
-  unsigned witems;
-  FastDiv fd_nblk, fd_EX;  // division by nblk = ceil(WL / CHUNK) and by EX
-  int xs[kMaxPlanes];
+  int off_h_min, h_span;  // smallest plane row offset; largest minus smallest
+  int te, n_etiles;       // padded rows per unit; units per (image, chunk)
+  int ch_pitch;           // staged elements per channel: (te-1)*step_h + h_span + 1 rows of W,
+                          // rounded up to 16 bytes
+  unsigned units;         // N * nchunk * n_etiles (< 2^31)
+  FastDiv fd_et, fd_nchunk;  // division by n_etiles and by nchunk
 };
 
 // Backward-filter on channel-chunked planes (bf16): for every filter tap t of a stride phase,

@@ -27,12 +27,6 @@ __device__ __forceinline__ uint32_t comp(const uint4& v, int i) {
   return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
 }
 
-// 16-byte async copy global -> shared with zero fill beyond src_bytes (0..16).
-__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, int src_bytes) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
-               : "memory");
-}
-
 // ------------------------------------------------------------------ pixel rows
 // Source element offset of channel 0 of the pixel that plane `pl` of a TapPlan places at
 // linear position L (L = n*EL*WL + e*WL + f; plane pixel (e, f) is source pixel

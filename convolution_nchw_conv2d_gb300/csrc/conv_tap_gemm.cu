@@ -13,15 +13,20 @@
 //
 // CTA roles (448 threads, persistent over tiles):
 //   warps 0-7  two producer groups taking pipeline stages in turn: stage source rows
-//              for CB channels into shared memory in the core-matrix interleaved layout
-//              (one load per channel of each staged row, 16-byte shared stores), and
-//              bulk-copy the packed filter slice.
+//              for CB channels into shared memory in the core-matrix interleaved layout,
+//              and bulk-copy the packed filter slice.  The rows come either from a copy of
+//              the source packed channel-chunk-wise beforehand (nhwc pack kernel), by
+//              tensor copies of whole runs of rows, or straight from NCHW (one load per
+//              channel of each staged row, 16-byte shared stores) when the caller gives
+//              no room for that copy.
 //   warps 8-11 epilogue: TMEM -> registers -> NCHW global stores, coalesced along
 //              output positions, with the optional bias and add-to (beta) of the fused
 //              epilogue; bf16 outputs rounded to nearest even.
 //   warps 12-13 TMEM allocation (warp 12); each warp issues tcgen05.mma (kind::tf32
 //              for fp32, kind::f16 with bf16 operands) for one 128-row accumulator half,
 //              through one elected lane.
+#include <algorithm>
+#include <atomic>
 #include <mutex>
 #include <vector>
 
@@ -110,39 +115,35 @@ __device__ __forceinline__ void store16(const TapPlan& p, long long ob, long lon
   }
 }
 
-// Issues one pipeline stage's MMAs for one 128-row accumulator: for every tap of the
-// phase, KS MMAs (K = two 16-byte chunks each) over the stage's channel chunks; KS == 0
-// is tap-pair mode (one MMA covers two taps whose rows the A entry's chunk stride links).
-// The whole warp walks the taps; tap table entry j sits in lane j (blocks of 32) and is
-// broadcast by shuffles; only `leader` issues.  The inner sequence is unrolled: a single
-// issuing thread spends tens of cycles per tcgen05.mma, more with loop overhead.
+// Issues one pipeline stage's MMAs for one 128-row accumulator, by the elected lane alone: for
+// every tap of the phase (four at a time, straight-line), KS MMAs (K = two 16-byte chunks each)
+// over the stage's channel chunks; KS == 0 is tap-pair mode (one MMA covers two taps whose rows
+// the A entry's chunk stride links).  The taps' operand offsets are read from the kernel
+// parameters: a constant-cache read, which does not wait behind the MMAs this thread has issued
+// (a shared-memory load would).  A single issuing thread spends tens of cycles per tcgen05.mma,
+// more in a loop with shuffles or branches, so the sequence is kept short and unrolled.
 template <int KIND, int KS>
-__device__ __forceinline__ void issue_stage(const uint2* tapo, int tap0, int ntaps, uint2 tap_first, bool leader,
-                                            int lane, uint32_t dcol, uint32_t a_lo0, uint32_t b_lo0, uint32_t d_hi,
-                                            uint32_t id, uint32_t a_ks, uint32_t b_ks, bool first) {
+__device__ __forceinline__ void issue_stage(const TapPlan& p, int tap0, int ntaps, uint32_t dcol, uint32_t a_lo0,
+                                            uint32_t b_lo0, uint32_t d_hi, uint32_t id, uint32_t a_ks, uint32_t b_ks,
+                                            bool first) {
   constexpr int TSTEP = KS == 0 ? 2 : 1;
-  for (int tb = 0; tb < ntaps; tb += 32) {
-    const uint2 blk = tb == 0 ? tap_first : (tb + lane < ntaps ? tapo[tap0 + tb + lane] : make_uint2(0u, 0u));
-    const int nb = ntaps - tb < 32 ? ntaps - tb : 32;
-    for (int j = 0; j < nb; j += TSTEP) {
-      const uint32_t ox = __shfl_sync(0xffffffffu, blk.x, j);
-      const uint32_t oy = __shfl_sync(0xffffffffu, blk.y, j);
-      if (leader) {
-        const uint32_t acc_in = (first && tb == 0 && j == 0) ? 0u : 1u;
-        uint32_t alo = a_lo0 + ox, blo = b_lo0 + oy;
-        if constexpr (KS == 0) {
-          mma_ss_lh<KIND>(dcol, alo, d_hi, blo, d_hi, id, acc_in);
-        } else {
+  auto one = [&](int t, bool init) {
+    const uint32_t alo = a_lo0 + (uint32_t)p.tap_a[t], blo = b_lo0 + (uint32_t)p.tap_b[t];
+    if constexpr (KS == 0) {
+      mma_ss_lh<KIND>(dcol, alo, d_hi, blo, d_hi, id, init ? 0u : 1u);
+    } else {
 #pragma unroll
-          for (int ks = 0; ks < KS; ++ks) {
-            mma_ss_lh<KIND>(dcol, alo, d_hi, blo, d_hi, id, ks ? 1u : acc_in);
-            alo += a_ks;
-            blo += b_ks;
-          }
-        }
-      }
+      for (int ks = 0; ks < KS; ++ks)
+        mma_ss_lh<KIND>(dcol, alo + (uint32_t)ks * a_ks, d_hi, blo + (uint32_t)ks * b_ks, d_hi, id,
+                        (init && ks == 0) ? 0u : 1u);
     }
+  };
+  int j = 0;
+  for (; j + 4 * TSTEP <= ntaps; j += 4 * TSTEP) {
+#pragma unroll
+    for (int u = 0; u < 4; ++u) one(tap0 + j + u * TSTEP, first && j == 0 && u == 0);
   }
+  for (; j < ntaps; j += TSTEP) one(tap0 + j, first && j == 0);
 }
 
 }  // namespace
@@ -168,11 +169,6 @@ __global__ void __launch_bounds__(kThreads, 1) tap_gemm_kernel(const __grid_cons
   ptr += (size_t)S * p.a_stage_bytes;
   const uint32_t b0 = smem_u32(ptr);
   ptr += (size_t)S * p.b_stage_bytes;
-  // Per tap: {A operand offset, B operand offset} relative to the stage bases, in 16-byte
-  // units (in tap-pair mode the A entry of a pair's first tap also carries the chunk
-  // stride to the second tap in bits 16..29, the descriptor's leading-byte-offset field).
-  uint2* tapo = reinterpret_cast<uint2*>(ptr);
-  ptr += (size_t)p.ntaps_total * sizeof(uint2);
   ptr = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(ptr) + 15) & ~uintptr_t(15));
   const uint32_t full = smem_u32(ptr);
   const uint32_t empty = full + 8u * S;
@@ -205,17 +201,6 @@ __global__ void __launch_bounds__(kThreads, 1) tap_gemm_kernel(const __grid_cons
     tmem_alloc(smem_u32((const void*)tmem_holder), (uint32_t)p.tmem_cols);
     tmem_relinquish();
   }
-  for (int ph = 0; ph < p.nph; ++ph)
-    for (int i = tid; i < p.ph_ntaps[ph]; i += kThreads) {
-      const int t = p.ph_tap_begin[ph] + i;
-      const uint32_t oa = (uint32_t)(p.tap_plane[t] * NCH * rows + p.tap_off[t]);
-      if (NCH >= 2) {
-        tapo[t] = make_uint2(oa, (uint32_t)(i * NCH * p.NT));
-      } else if ((i & 1) == 0) {
-        const uint32_t ob = (uint32_t)(p.tap_plane[t + 1] * rows + p.tap_off[t + 1]);
-        tapo[t] = make_uint2(oa | ((ob - oa) << 16), (uint32_t)(i * p.NT));
-      }
-    }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -253,14 +238,24 @@ __global__ void __launch_bounds__(kThreads, 1) tap_gemm_kernel(const __grid_cons
           const uint32_t bytes = (uint32_t)(ntaps * b_tap_bytes);
           const long long img_off =
               ((long long)(tc.nt * p.nkb + kb) * p.ntaps_total + p.ph_tap_begin[tc.ph]) * b_tap_bytes;
-          // The copy completes on the stage's full barrier: its bytes are expected there
-          // before it is issued, and this thread arrives with the others after its fill.
-          mbar_expect_tx(bar_at(full, stage), bytes);
+          // The copies complete on the stage's full barrier: their bytes are expected there
+          // before they are issued, and this thread arrives with the others after its fill.
+          mbar_expect_tx(bar_at(full, stage), bytes + (p.a_tma ? (uint32_t)p.a_stage_bytes : 0u));
           bulk_g2s(b_st, static_cast<const uint8_t*>(p.wpack) + img_off, bytes, bar_at(full, stage));
+          if (p.a_tma) {
+            // one tensor copy per (plane, chunk, box of rows): [plane][chunk][row][16 bytes]
+            for (int pl = 0; pl < p.npl; ++pl)
+              for (int j = 0; j < NCH; ++j)
+                for (int bx = 0; bx < p.a_nbox; ++bx)
+                  tma_load_3d(a_st + (uint32_t)(((pl * NCH + j) * rows + bx * p.a_box) * 16), &p.tm_src,
+                              (int)(2 * (m0 + (long long)bx * p.a_box)), kb * NCH + j, pl, bar_at(full, stage));
+          }
           last_copy[stage] = 1 + (int)ephase;
         }
-        stage_pixel_rows<DT>(p, m0, a_st, kb * p.CB, NCH, gtid);
-        fence_proxy_async();
+        if (!p.a_tma) {
+          stage_pixel_rows<DT>(p, m0, a_st, kb * p.CB, NCH, gtid);
+          fence_proxy_async();
+        }
         mbar_arrive(bar_at(full, stage));
       }
     }
@@ -349,9 +344,8 @@ __global__ void __launch_bounds__(kThreads, 1) tap_gemm_kernel(const __grid_cons
   } else {
     // =============================================================== MMA issuers
     // The whole warp runs the loop (warp-uniform control flow and descriptor arithmetic);
-    // one elected lane issues the MMAs and commits.  The tap table is read into lane
-    // registers (entry j in lane j) and broadcast with shuffles: a shared-memory load that
-    // a descriptor depends on would wait behind the MMAs already issued by this thread.
+    // one elected lane issues the MMAs, with the taps' operand offsets read from the kernel
+    // parameters, and commits.
     const int issuer = warp - kMmaWarp;  // accumulator half this warp owns
     if (issuer < nissuers) {
       const bool leader = elect_one();
@@ -369,7 +363,6 @@ __global__ void __launch_bounds__(kThreads, 1) tap_gemm_kernel(const __grid_cons
         const int ntaps = p.ph_ntaps[tc.ph];
         if (ntaps == 0) continue;
         const int tap0 = p.ph_tap_begin[tc.ph];
-        const uint2 tap_first = lane < ntaps ? tapo[tap0 + lane] : make_uint2(0u, 0u);
         if (!mbar_wait(bar_at(acce, acc), aphase ^ 1u, abort_flag, &g_tap_err)) break;
         tc_fence_after();
         const uint32_t dcol = tmem + (uint32_t)((acc * p.MH + issuer) * p.NT);
@@ -387,22 +380,14 @@ __global__ void __launch_bounds__(kThreads, 1) tap_gemm_kernel(const __grid_cons
           // In tap-pair mode the A entry carries the chunk stride to the pair's second tap.
           const uint32_t a_lo0 = (uint32_t)sdesc(a_st, NCH >= 2 ? (uint32_t)rows * 16u : 0u, 0u);
           const bool first = kb == 0;
-          switch (NCH) {
-            case 1:
-              issue_stage<KIND, 0>(tapo, tap0, ntaps, tap_first, leader, lane, dcol, a_lo0, b_lo0, d_hi, id, a_ks, b_ks, first);
-              break;
-            case 2:
-              issue_stage<KIND, 1>(tapo, tap0, ntaps, tap_first, leader, lane, dcol, a_lo0, b_lo0, d_hi, id, a_ks, b_ks, first);
-              break;
-            case 4:
-              issue_stage<KIND, 2>(tapo, tap0, ntaps, tap_first, leader, lane, dcol, a_lo0, b_lo0, d_hi, id, a_ks, b_ks, first);
-              break;
-            case 8:
-              issue_stage<KIND, 4>(tapo, tap0, ntaps, tap_first, leader, lane, dcol, a_lo0, b_lo0, d_hi, id, a_ks, b_ks, first);
-              break;
-            default:
-              issue_stage<KIND, 8>(tapo, tap0, ntaps, tap_first, leader, lane, dcol, a_lo0, b_lo0, d_hi, id, a_ks, b_ks, first);
-              break;
+          if (leader) {
+            switch (NCH) {
+              case 1: issue_stage<KIND, 0>(p, tap0, ntaps, dcol, a_lo0, b_lo0, d_hi, id, a_ks, b_ks, first); break;
+              case 2: issue_stage<KIND, 1>(p, tap0, ntaps, dcol, a_lo0, b_lo0, d_hi, id, a_ks, b_ks, first); break;
+              case 4: issue_stage<KIND, 2>(p, tap0, ntaps, dcol, a_lo0, b_lo0, d_hi, id, a_ks, b_ks, first); break;
+              case 8: issue_stage<KIND, 4>(p, tap0, ntaps, dcol, a_lo0, b_lo0, d_hi, id, a_ks, b_ks, first); break;
+              default: issue_stage<KIND, 8>(p, tap0, ntaps, dcol, a_lo0, b_lo0, d_hi, id, a_ks, b_ks, first); break;
+            }
           }
           __syncwarp();
           if (leader) tc_commit(bar_at(empty, stage));
@@ -437,56 +422,127 @@ __global__ void __launch_bounds__(kThreads, 1) tap_gemm_kernel(const __grid_cons
 // CHUNK consecutive source channels cs = kb*CB + j*CHUNK + e of out channel nt*NT + n
 // for filter tap (tap_r[t], tap_s[t]); zero outside the tensor.  fp32 values are
 // rounded to tf32 (round to nearest, ties away) on the way.
+//
+// Work unit = (n tile, k block, UN consecutive out channels of the tile): the unit's filter
+// values for every tap are staged in shared memory with coalesced 16-byte reads where aligned
+// (for a fixed out channel the CB source channels x R*S taps are one contiguous run of the
+// KCRS filter; with `transpose`, for a fixed source channel the UN out channels x R*S are), at
+// a row pitch per out channel that spreads the UN rows over distinct banks; then each chunk is
+// gathered from shared memory and stored, consecutive threads storing consecutive out channels.
 template <int DT>
-__global__ void pack_filter_kernel(const __grid_constant__ PackPlan pp) {
+__global__ void __launch_bounds__(256) pack_filter_kernel(const __grid_constant__ PackPlan pp, int UN, int pitch) {
   constexpr int ESZ = DT == 0 ? 4 : 2;
   constexpr int CHUNK = 16 / ESZ;
+  using E = typename std::conditional<DT == 0, uint32_t, uint16_t>::type;
+  extern __shared__ __align__(16) uint8_t pf_smem[];
+  E* sm = reinterpret_cast<E*>(pf_smem);
   const int NCH = pp.CB / CHUNK;
+  const int RS = pp.R * pp.S;
   griddep_launch_dependents();  // the GEMM may start; it waits for this grid before reading wpack
-  const long long total = (long long)pp.n_ntiles * pp.nkb * pp.ntaps_total * NCH * pp.NT;
-  for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < total;
-       idx += (long long)gridDim.x * blockDim.x) {
-    long long rest = idx;
-    const int n = (int)(rest % pp.NT);
-    rest /= pp.NT;
-    const int j = (int)(rest % NCH);
-    rest /= NCH;
-    const int t = (int)(rest % pp.ntaps_total);
-    rest /= pp.ntaps_total;
+  const int nsub = (pp.NT + UN - 1) / UN;
+  const long long units = (long long)pp.n_ntiles * pp.nkb * nsub;
+  for (long long u = blockIdx.x; u < units; u += gridDim.x) {
+    const int sub = (int)(u % nsub);
+    const long long rest = u / nsub;
     const int kb = (int)(rest % pp.nkb);
     const int nt = (int)(rest / pp.nkb);
-    const int nn = nt * pp.NT + n;
-    int r = pp.tap_r[t], s = pp.tap_s[t];
-    if (pp.flip && r >= 0) {  // convolution mode: the filter rotated by 180 degrees
-      r = pp.R - 1 - r;
-      s = pp.S - 1 - s;
-    }
-    uint32_t out[4] = {0u, 0u, 0u, 0u};
+    const int nl0 = sub * UN;                       // first out channel of the unit within the tile
+    const int ncnt = min(UN, pp.NT - nl0);
+    const int n0 = nt * pp.NT + nl0, c0 = kb * pp.CB;
+    __syncthreads();  // the previous unit's reads of shared memory are done
+    // The staged values are NRUN contiguous runs of the filter, RLEN elements each (the first
+    // `valid` of them exist); a thread copies 16-byte groups of a run, four groups in flight.
+    const int RLEN = pp.transpose ? UN * RS : pp.CB * RS;
+    const int NRUN = pp.transpose ? pp.CB : UN;
+    const int NG = (RLEN + CHUNK - 1) / CHUNK;  // 16-byte groups per run
+    const int total_g = NRUN * NG;
+    for (int base = (int)threadIdx.x; base < total_g; base += 4 * (int)blockDim.x) {
+      E val[4][CHUNK];
 #pragma unroll
-    for (int e = 0; e < CHUNK; ++e) {
-      const int cs = kb * pp.CB + j * CHUNK + e;
-      if (nn < pp.Cd && cs < pp.Cs && r >= 0) {
-        const long long widx = pp.transpose ? (((long long)cs * pp.C + nn) * pp.R + r) * pp.S + s
-                                            : (((long long)nn * pp.C + cs) * pp.R + r) * pp.S + s;
-        if constexpr (DT == 0) {
-          const float v = static_cast<const float*>(pp.w)[widx];
-          uint32_t tf;
-          asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(tf) : "f"(v));
-          out[e] = tf;
+      for (int bq = 0; bq < 4; ++bq) {
+        const int gi = base + bq * (int)blockDim.x;
+#pragma unroll
+        for (int e = 0; e < CHUNK; ++e) val[bq][e] = 0;
+        if (gi >= total_g) continue;
+        const int k = gi / NG, q0 = (gi - k * NG) * CHUNK;
+        long long start;
+        int valid;
+        if (!pp.transpose) {  // run k = out channel n0 + k: source channels c0.. x taps
+          const int nn = n0 + k;
+          valid = (k < ncnt && nn < pp.Cd) ? min(pp.CB, pp.Cs - c0) * RS : 0;
+          start = ((long long)nn * pp.C + c0) * RS;
+        } else {  // run k = source channel c0 + k: out channels n0.. x taps
+          const int cs = c0 + k;
+          valid = cs < pp.Cs ? min(ncnt, pp.Cd - n0) * RS : 0;
+          start = ((long long)cs * pp.C + n0) * RS;
+        }
+        const E* g = static_cast<const E*>(pp.w) + start + q0;
+        if (q0 + CHUNK <= valid && (reinterpret_cast<uintptr_t>(g) & 15u) == 0) {
+          const uint4 t4 = __ldg(reinterpret_cast<const uint4*>(g));
+          const uint32_t wd[4] = {t4.x, t4.y, t4.z, t4.w};
+#pragma unroll
+          for (int e = 0; e < CHUNK; ++e) {
+            if constexpr (DT == 0) val[bq][e] = wd[e];
+            else val[bq][e] = (E)(wd[e >> 1] >> (16 * (e & 1)));
+          }
         } else {
-          const uint32_t v = static_cast<const uint16_t*>(pp.w)[widx];
-          out[e >> 1] |= v << (16 * (e & 1));
+#pragma unroll
+          for (int e = 0; e < CHUNK; ++e)
+            if (q0 + e < valid) val[bq][e] = g[e];
+        }
+      }
+#pragma unroll
+      for (int bq = 0; bq < 4; ++bq) {
+        const int gi = base + bq * (int)blockDim.x;
+        if (gi >= total_g) continue;
+        const int k = gi / NG, q0 = (gi - k * NG) * CHUNK;
+#pragma unroll
+        for (int e = 0; e < CHUNK; ++e) {
+          const int q = q0 + e;
+          if (q >= RLEN) break;
+          if (!pp.transpose) {
+            sm[k * pitch + q] = val[bq][e];
+          } else {
+            const int nl = q / RS;
+            sm[nl * pitch + k * RS + (q - nl * RS)] = val[bq][e];
+          }
         }
       }
     }
-    reinterpret_cast<uint4*>(pp.wpack)[idx] = make_uint4(out[0], out[1], out[2], out[3]);
+    __syncthreads();
+    const int outs = pp.ntaps_total * NCH * UN;
+    for (int i = (int)threadIdx.x; i < outs; i += (int)blockDim.x) {
+      const int tj = i / UN, nl = i - tj * UN;
+      const int t = tj / NCH, j = tj - t * NCH;
+      if (nl >= ncnt) continue;
+      int r = pp.tap_r[t], s = pp.tap_s[t];
+      if (pp.flip && r >= 0) {  // convolution mode: the filter rotated by 180 degrees
+        r = pp.R - 1 - r;
+        s = pp.S - 1 - s;
+      }
+      uint32_t out[4] = {0u, 0u, 0u, 0u};
+      if (r >= 0) {
+        const E* src = sm + nl * pitch + (j * CHUNK) * RS + r * pp.S + s;
+#pragma unroll
+        for (int e = 0; e < CHUNK; ++e) {
+          if constexpr (DT == 0) {
+            uint32_t tf;
+            asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(tf) : "f"(__uint_as_float(src[e * RS])));
+            out[e] = tf;
+          } else {
+            out[e >> 1] |= (uint32_t)src[e * RS] << (16 * (e & 1));
+          }
+        }
+      }
+      const long long oidx = (((long long)(nt * pp.nkb + kb) * pp.ntaps_total + t) * NCH + j) * pp.NT + nl0 + nl;
+      reinterpret_cast<uint4*>(pp.wpack)[oidx] = make_uint4(out[0], out[1], out[2], out[3]);
+    }
   }
 }
 
 // ---------------------------------------------------------------------------- launchers
 size_t tap_gemm_smem_bytes(const TapPlan& p) {
   size_t b = (size_t)p.stages * (p.a_stage_bytes + p.b_stage_bytes);
-  b += (size_t)p.ntaps_total * sizeof(uint2);
   b = (b + 15) & ~size_t(15);
   b += 8 * (2 * p.stages + 6) + 8 + 4 * p.stages + 16;
   return b + 1024;  // alignment slack for the dynamic base
@@ -524,16 +580,43 @@ cudaError_t launch_tap_gemm(const TapPlan& p, int dt, int grid, cudaStream_t st)
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
+// Out channels per filter-pack unit (32, or fewer when the staged values would pass 48 KB; at
+// least 1) and the staged row pitch in elements: CB * R * S rounded up so that consecutive rows
+// start in different 4-byte banks (an odd number of words apart).
+void pack_filter_shape(const PackPlan& pp, int dt, int* un, int* pitch) {
+  const int esz = dt == 0 ? 4 : 2;
+  int p = pp.CB * pp.R * pp.S;
+  if (dt == 0) p |= 1;
+  else p = (p + 1) / 2 * 2 + ((((p + 1) / 2) & 1) ? 0 : 2);
+  int u = 32;
+  while (u > 1 && (long long)u * p * esz > 48 * 1024) u >>= 1;
+  *un = u;
+  *pitch = p;
+}
+
+size_t pack_filter_smem_bytes(const PackPlan& pp, int dt) {
+  int un, pitch;
+  pack_filter_shape(pp, dt, &un, &pitch);
+  return (size_t)un * pitch * (dt == 0 ? 4 : 2);
+}
+
 cudaError_t launch_pack_filter(const PackPlan& pp, int dt, cudaStream_t st) {
-  const int CHUNK = dt == 0 ? 4 : 8;
-  const long long total = (long long)pp.n_ntiles * pp.nkb * pp.ntaps_total * (pp.CB / CHUNK) * pp.NT;
-  long long blocks = (total + 255) / 256;
-  if (blocks > 4096) blocks = 4096;
-  if (blocks < 1) blocks = 1;
-  if (dt == 0)
-    pack_filter_kernel<0><<<(int)blocks, 256, 0, st>>>(pp);
-  else
-    pack_filter_kernel<1><<<(int)blocks, 256, 0, st>>>(pp);
+  int un, pitch;
+  pack_filter_shape(pp, dt, &un, &pitch);
+  const size_t smem = (size_t)un * pitch * (dt == 0 ? 4 : 2);
+  const long long units = (long long)pp.n_ntiles * pp.nkb * ((pp.NT + un - 1) / un);
+  long long blocks = std::min<long long>(std::max(1ll, units), 4096);
+  static std::atomic<int> set_bytes[2][kMaxDevices];
+  cudaError_t e;
+  if (dt == 0) {
+    e = ensure_dyn_smem(pack_filter_kernel<0>, smem, set_bytes[0]);
+    if (e != cudaSuccess) return e;
+    pack_filter_kernel<0><<<(int)blocks, 256, smem, st>>>(pp, un, pitch);
+  } else {
+    e = ensure_dyn_smem(pack_filter_kernel<1>, smem, set_bytes[1]);
+    if (e != cudaSuccess) return e;
+    pack_filter_kernel<1><<<(int)blocks, 256, smem, st>>>(pp, un, pitch);
+  }
   return cudaGetLastError();
 }
 

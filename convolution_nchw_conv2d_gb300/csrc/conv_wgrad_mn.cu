@@ -77,163 +77,100 @@ __device__ __forceinline__ void issue_mn_stage(const WgradMnPlan& p, uint32_t tm
 
 }  // namespace
 
-// One 16-byte group per thread and item: CHUNK channels of one padded position, read from the
-// CHUNK channel planes of the source pixel (each read coalesced across the warp's consecutive
-// positions) and written as one 16-byte store (a warp writes 512 contiguous bytes).  Work units
-// are (slab = plane, chunk, image; kPackUnit consecutive positions of the slab), one per warp, the
-// units of plan `a` first, then those of plan `b` (b.src NULL: none), so the packs of x and dy
-// are one launch.
+// Channel-chunk pack (NhwcPackPlan), one work unit per block iteration: the unit's channel runs
+// are staged in shared memory (16-byte asynchronous copies when every run starts on a 16-byte
+// boundary and is whole 16-byte groups, batched element loads otherwise; channels past C are not
+// read), then each output
+// 16-byte group is assembled from CHUNK shared-memory reads of its position and stored, with
+// consecutive threads storing consecutive groups.  The units of plan `a` come first, then those of
+// plan `b` (b.src NULL: none), so the packs of x and dy are one launch.
 template <int DT>
 __global__ void __launch_bounds__(256) nhwc_pack_kernel(const __grid_constant__ NhwcPackPlan a,
                                                         const __grid_constant__ NhwcPackPlan b) {
   constexpr int CHUNK = DT == 0 ? 4 : 8;
-  constexpr int UNIT = kPackUnit;
+  constexpr int ESZ = DT == 0 ? 4 : 2;
   using E = typename std::conditional<DT == 0, uint32_t, uint16_t>::type;
-  const int warp = (int)(threadIdx.x >> 5), lane = (int)(threadIdx.x & 31);
+  extern __shared__ __align__(16) uint8_t pk_smem[];
+  E* sm = reinterpret_cast<E*>(pk_smem);
   const uint32_t na = a.units, nb = b.src != nullptr ? b.units : 0u;
-  for (uint32_t u = blockIdx.x * 8u + (uint32_t)warp; u < na + nb; u += gridDim.x * 8u) {
+  for (uint32_t u = blockIdx.x; u < na + nb; u += gridDim.x) {
     const bool first = u < na;
     const NhwcPackPlan& p = first ? a : b;
     const uint32_t v = first ? u : u - na;
-    const uint32_t sl = fdiv(v, p.fd_upp);          // slab: ((pl * nchunk + cc) * N + n)
-    const int i0 = (int)(v - sl * p.fd_upp.d) * UNIT;  // first position of the unit
-    const uint32_t r = fdiv(sl, p.fd_N);
-    const int n = (int)(sl - r * (uint32_t)p.N);
-    const uint32_t pl = fdiv(r, p.fd_nchunk);
-    const int cc = (int)(r - pl * (uint32_t)p.nchunk);
-    const long long HW = (long long)p.H * p.W;
-    const E* base = static_cast<const E*>(p.src) + (long long)n * p.src_nstride + (long long)(CHUNK * cc) * HW;
-    const int nch = p.C - CHUNK * cc < CHUNK ? p.C - CHUNK * cc : CHUNK;
-    const int slab = p.EX * p.WL;
-    uint4* dst = reinterpret_cast<uint4*>(p.dst) + sl * (long long)slab;
-    uint32_t q[UNIT / 32][4];
+    const uint32_t r = fdiv(v, p.fd_et);  // r = n * nchunk + cc
+    const int et = (int)(v - r * (uint32_t)p.n_etiles);
+    const uint32_t n = fdiv(r, p.fd_nchunk);
+    const int cc = (int)(r - n * (uint32_t)p.nchunk);
+    const int e0 = et * p.te, ne = min(p.te, p.EX - e0);
+    const int h_lo = e0 * p.step_h + p.off_h_min;
+    const int h_hi = (e0 + ne - 1) * p.step_h + p.off_h_min + p.h_span;
+    const int hl = max(h_lo, 0), hh = min(h_hi, p.H - 1);
+    const int nr = hh - hl + 1;  // staged rows (none when <= 0)
+    const int nch = min(CHUNK, p.C - CHUNK * cc);
+    __syncthreads();  // the previous unit's reads of shared memory are done
+    if (nr > 0) {
+      const long long HW = (long long)p.H * p.W;
+      const E* base = static_cast<const E*>(p.src) + (long long)n * p.src_nstride + (long long)(CHUNK * cc) * HW +
+                      (long long)hl * p.W;
+      const int len = nr * p.W;  // elements per channel run
+      const bool vec =
+          ((reinterpret_cast<uintptr_t>(base) | (uintptr_t)(HW * ESZ) | (uintptr_t)(len * ESZ)) & 15u) == 0;
+      if (vec) {  // asynchronous 16-byte copies: all of a thread's copies in flight at once
+        const int g = len * ESZ / 16;  // 16-byte groups per channel run
+        const uint32_t s0 = smem_u32(sm);
+        for (int i = (int)threadIdx.x; i < nch * g; i += (int)blockDim.x) {
+          const int c = i / g, k = i - c * g;
+          cp_async_16(s0 + (uint32_t)((c * p.ch_pitch) * ESZ + k * 16), base + c * HW + k * (16 / ESZ), 16);
+        }
+        cp_async_commit();
+        cp_async_wait<0>();
+      } else {  // element loads, eight in flight per thread before their stores
+        const int tot = nch * len;
+        for (int i0 = (int)threadIdx.x; i0 < tot; i0 += 8 * (int)blockDim.x) {
+          E v[8];
 #pragma unroll
-    for (int j = 0; j < UNIT / 32; ++j) {  // all loads of the lane's positions first
-      q[j][0] = q[j][1] = q[j][2] = q[j][3] = 0u;
-      const int i = i0 + 32 * j + lane;
-      if (i >= slab) continue;
-      const int e = (int)fdiv((uint32_t)i, p.fd_WL);
-      const int f = i - e * p.WL;
-      const int h = e * p.step_h + p.off_h[pl];
-      const int w = f * p.step_w + p.off_w[pl];
-      if (h >= 0 && h < p.H && w >= 0 && w < p.W) {
-        const E* s = base + (long long)h * p.W + w;
+          for (int u = 0; u < 8; ++u) {
+            const int i = i0 + u * (int)blockDim.x;
+            if (i < tot) {
+              const int c = i / len, k = i - c * len;
+              v[u] = base[c * HW + k];
+            }
+          }
 #pragma unroll
-        for (int c = 0; c < CHUNK; ++c) {
-          if (c < nch) {
-            const uint32_t x = (uint32_t)__ldg(s + c * HW);
-            if constexpr (DT == 0) q[j][c] = x;
-            else q[j][c >> 1] |= x << (16 * (c & 1));
+          for (int u = 0; u < 8; ++u) {
+            const int i = i0 + u * (int)blockDim.x;
+            if (i < tot) {
+              const int c = i / len, k = i - c * len;
+              sm[c * p.ch_pitch + k] = v[u];
+            }
           }
         }
       }
     }
+    __syncthreads();
+    const int groups = ne * p.WL;
+    for (int pl = 0; pl < p.npl; ++pl) {
+      uint4* dst = reinterpret_cast<uint4*>(p.dst) + ((((long long)pl * p.nchunk + cc) * p.N + n) * p.EX + e0) * p.WL;
+      for (int i = (int)threadIdx.x; i < groups; i += (int)blockDim.x) {
+        const int de = (int)fdiv((uint32_t)i, p.fd_WL);
+        const int f = i - de * p.WL;
+        const int h = (e0 + de) * p.step_h + p.off_h[pl];
+        const int w = f * p.step_w + p.off_w[pl];
+        uint32_t o[4] = {0u, 0u, 0u, 0u};
+        if (h >= hl && h <= hh && w >= 0 && w < p.W) {
+          const E* s0 = sm + (h - hl) * p.W + w;
 #pragma unroll
-    for (int j = 0; j < UNIT / 32; ++j) {
-      const int i = i0 + 32 * j + lane;
-      if (i < slab) dst[i] = make_uint4(q[j][0], q[j][1], q[j][2], q[j][3]);
-    }
-  }
-}
-
-// Word variant of the pack (NhwcPackPlan::words: rows of whole 16-byte words, aligned tensor,
-// step_w 1 or 2): an item is CHUNK consecutive positions f0 .. f0 + CHUNK - 1 of one padded row
-// of one slab.  Their source columns f*SW + off_w lie in a window of NW aligned 16-byte words
-// starting at column wbase = f0*SW + xs (xs = off_w rounded down to a multiple of CHUNK,
-// R = off_w - xs); the thread loads those words of each of the CHUNK channels (words outside the
-// row, the tensor or the chunk's channel slice read as zero; all loads issued before any use),
-// transposes them in registers -- output f0 + i takes element R + SW*i of every channel -- and
-// writes the `nout` 16-byte groups (consecutive).
-template <int DT, int SW, int R>
-__device__ __forceinline__ void pack_words_item(const void* row0_v, long long HW, int W, int wbase, int nch, int nout,
-                                                uint4* dst) {
-  constexpr int CHUNK = DT == 0 ? 4 : 8;
-  constexpr int NW = (R + SW * (CHUNK - 1)) / CHUNK + 1;
-  using E = typename std::conditional<DT == 0, uint32_t, uint16_t>::type;
-  const E* row0 = static_cast<const E*>(row0_v);  // channel 0 of the source row (NULL: outside)
-  uint4 v[CHUNK][NW];
-#pragma unroll
-  for (int c = 0; c < CHUNK; ++c)
-#pragma unroll
-    for (int q = 0; q < NW; ++q) {
-      v[c][q] = make_uint4(0u, 0u, 0u, 0u);
-      const int col = wbase + q * CHUNK;
-      if (row0 != nullptr && c < nch && col >= 0 && col + CHUNK <= W)
-        v[c][q] = __ldg(reinterpret_cast<const uint4*>(row0 + (long long)c * HW + col));
-    }
-#pragma unroll
-  for (int i = 0; i < CHUNK; ++i) {
-    if (i >= nout) break;
-    const int j = R + SW * i;  // window element of output i
-    uint32_t o[4];
-    if constexpr (DT == 0) {
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const uint4 wv = v[c][j / 4];
-        o[c] = (j % 4) == 0 ? wv.x : (j % 4) == 1 ? wv.y : (j % 4) == 2 ? wv.z : wv.w;
-      }
-    } else {
-#pragma unroll
-      for (int q2 = 0; q2 < 4; ++q2) {
-        const uint4 wa = v[2 * q2][j / 8], wb = v[2 * q2 + 1][j / 8];
-        const int e = (j % 8) / 2;
-        const uint32_t ra = e == 0 ? wa.x : e == 1 ? wa.y : e == 2 ? wa.z : wa.w;
-        const uint32_t rb = e == 0 ? wb.x : e == 1 ? wb.y : e == 2 ? wb.z : wb.w;
-        o[q2] = __byte_perm(ra, rb, (j & 1) ? 0x7632 : 0x5410);
+          for (int c = 0; c < CHUNK; ++c) {
+            if (c < nch) {
+              const uint32_t x = (uint32_t)s0[c * p.ch_pitch];
+              if constexpr (DT == 0) o[c] = x;
+              else o[c >> 1] |= x << (16 * (c & 1));
+            }
+          }
+        }
+        dst[i] = make_uint4(o[0], o[1], o[2], o[3]);
       }
     }
-    dst[i] = make_uint4(o[0], o[1], o[2], o[3]);
-  }
-}
-
-template <int DT, int SW, int Rn>
-__device__ __forceinline__ void pack_words_dispatch(int R, const void* row0, long long HW, int W, int wbase, int nch,
-                                                    int nout, uint4* dst) {
-  if constexpr (Rn > 0) {
-    if (R == Rn - 1) {
-      pack_words_item<DT, SW, Rn - 1>(row0, HW, W, wbase, nch, nout, dst);
-      return;
-    }
-    pack_words_dispatch<DT, SW, Rn - 1>(R, row0, HW, W, wbase, nch, nout, dst);
-  }
-}
-
-// Items run position block fastest, then padded row, then slab (plane, chunk, image), the items
-// of plan `a` first, then those of plan `b` (b.src NULL: none): packs of x and dy in one launch.
-template <int DT>
-__global__ void __launch_bounds__(256) nhwc_pack_words_kernel(const __grid_constant__ NhwcPackPlan a,
-                                                              const __grid_constant__ NhwcPackPlan b) {
-  constexpr int CHUNK = DT == 0 ? 4 : 8;
-  using E = typename std::conditional<DT == 0, uint32_t, uint16_t>::type;
-  const uint32_t na = a.witems, nb = b.src != nullptr ? b.witems : 0u;
-  for (uint32_t it = blockIdx.x * blockDim.x + threadIdx.x; it < na + nb; it += gridDim.x * blockDim.x) {
-    const bool first = it < na;
-    const NhwcPackPlan& p = first ? a : b;
-    const uint32_t v = first ? it : it - na;
-    const uint32_t rowi = fdiv(v, p.fd_nblk);        // (slab, padded row)
-    const int blk = (int)(v - rowi * p.fd_nblk.d);
-    const uint32_t sl = fdiv(rowi, p.fd_EX);
-    const int e = (int)(rowi - sl * (uint32_t)p.EX);
-    const uint32_t r = fdiv(sl, p.fd_N);
-    const int n = (int)(sl - r * (uint32_t)p.N);
-    const uint32_t pl = fdiv(r, p.fd_nchunk);
-    const int cc = (int)(r - pl * (uint32_t)p.nchunk);
-    const int nch = p.C - CHUNK * cc < CHUNK ? p.C - CHUNK * cc : CHUNK;
-    const int h = e * p.step_h + p.off_h[pl];
-    const long long HW = (long long)p.H * p.W;
-    const E* row0 = (h >= 0 && h < p.H)
-                        ? static_cast<const E*>(p.src) + (long long)n * p.src_nstride + (long long)(CHUNK * cc) * HW +
-                              (long long)h * p.W
-                        : nullptr;
-    const int f0 = blk * CHUNK;
-    const int nout = p.WL - f0 < CHUNK ? p.WL - f0 : CHUNK;
-    const int R = p.off_w[pl] - p.xs[pl];
-    const int wbase = f0 * p.step_w + p.xs[pl];
-    uint4* dst = reinterpret_cast<uint4*>(p.dst) + ((long long)sl * p.EX + e) * p.WL + f0;
-    if (p.step_w == 1)
-      pack_words_dispatch<DT, 1, CHUNK>(R, row0, HW, p.W, wbase, nch, nout, dst);
-    else
-      pack_words_dispatch<DT, 2, CHUNK>(R, row0, HW, p.W, wbase, nch, nout, dst);
   }
 }
 
@@ -537,23 +474,29 @@ cudaError_t launch_wgrad_mn(const WgradMnPlan& p, int grid, cudaStream_t st) {
   return cudaGetLastError();
 }
 
-// Packs a and (if b.src is not NULL) b in one launch; the word kernel when both allow it.
+// Shared memory of a pack unit: CHUNK staged channel runs of ch_pitch elements.
+size_t nhwc_pack_smem_bytes(const NhwcPackPlan& q, int dt) {
+  return (size_t)(dt == 0 ? 4 : 8) * q.ch_pitch * (dt == 0 ? 4 : 2);
+}
+
+// Packs a and (if b.src is not NULL) b in one launch.
 cudaError_t launch_nhwc_pack(const NhwcPackPlan& a, const NhwcPackPlan& b, int dt, int num_sms, cudaStream_t st) {
-  if (a.words && (b.src == nullptr || b.words)) {
-    const long long items = (long long)a.witems + (b.src != nullptr ? (long long)b.witems : 0ll);
-    const unsigned blocks = (unsigned)std::max(1ll, std::min<long long>((items + 255) / 256, (long long)num_sms * 8));
-    if (dt == 0)
-      nhwc_pack_words_kernel<0><<<blocks, 256, 0, st>>>(a, b);
-    else
-      nhwc_pack_words_kernel<1><<<blocks, 256, 0, st>>>(a, b);
-    return cudaGetLastError();
+  const bool two = b.src != nullptr;
+  const size_t smem = std::max(nhwc_pack_smem_bytes(a, dt), two ? nhwc_pack_smem_bytes(b, dt) : (size_t)0);
+  const long long units = (long long)a.units + (two ? (long long)b.units : 0ll);
+  const long long per_sm = std::max<long long>(1, std::min<long long>(8, (long long)(200 * 1024) / (long long)std::max<size_t>(smem, 1)));
+  const unsigned blocks = (unsigned)std::max(1ll, std::min<long long>(units, (long long)num_sms * per_sm));
+  static std::atomic<int> set_bytes[2][kMaxDevices];
+  cudaError_t e;
+  if (dt == 0) {
+    e = ensure_dyn_smem(nhwc_pack_kernel<0>, smem, set_bytes[0]);
+    if (e != cudaSuccess) return e;
+    nhwc_pack_kernel<0><<<blocks, 256, smem, st>>>(a, b);
+  } else {
+    e = ensure_dyn_smem(nhwc_pack_kernel<1>, smem, set_bytes[1]);
+    if (e != cudaSuccess) return e;
+    nhwc_pack_kernel<1><<<blocks, 256, smem, st>>>(a, b);
   }
-  const long long warps = (long long)a.units + (b.src != nullptr ? (long long)b.units : 0ll);
-  const long long blocks = std::max(1ll, std::min<long long>((warps + 7) / 8, (long long)num_sms * 16));
-  if (dt == 0)
-    nhwc_pack_kernel<0><<<(unsigned)blocks, 256, 0, st>>>(a, b);
-  else
-    nhwc_pack_kernel<1><<<(unsigned)blocks, 256, 0, st>>>(a, b);
   return cudaGetLastError();
 }
 

@@ -166,6 +166,12 @@ __device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src, bool v
                "r"(valid ? 4 : 0)
                : "memory");
 }
+// 16-byte async copy global -> shared with zero fill beyond src_bytes (0..16); both
+// addresses 16-byte aligned.
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, int src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
+               : "memory");
+}
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 // Waits until at most N committed groups of this thread are pending.  Copies issued
 // after the last cp_async_commit() are not covered: commit first.

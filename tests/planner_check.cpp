@@ -24,6 +24,7 @@ static cudaError_t entry_point_stand_in(const char*, void** f, unsigned int, uns
 #define cudaGetDriverEntryPointByVersion entry_point_stand_in
 #include "conv2d_api.cpp"
 
+#include <cmath>
 #include <cstdio>
 #include <vector>
 
@@ -53,6 +54,194 @@ void check_tap(const char* nm, const char* op, const TapBuild& b, const DevInfo&
       if (p.tap_off[t] < 0 || p.tap_off[t] + 128 * p.MH > p.rows) fail(nm, op, "tap offset beyond the staged rows");
   if (p.NT % 16 || p.NT > 256 || (p.MH != 1 && p.MH != 2)) fail(nm, op, "tile shape");
   if (p.Mtot >= (1ll << 31)) fail(nm, op, "position space too large");
+  if (p.a_tma) {
+    // staged rows as tensor copies of the packed source: equal boxes of at most 128 rows
+    // (256 8-byte elements) that tile the rows; one stage's bytes within the barrier's
+    // transaction count; copy coordinates (2 per position) within 32 bits
+    if (p.rows != p.a_nbox * p.a_box || p.a_box % 8 || p.a_box < 8 || p.a_box > 128)
+      fail(nm, op, "tensor-copy boxes do not tile the staged rows");
+    if ((long long)p.a_stage_bytes + p.b_stage_bytes >= (1 << 20)) fail(nm, op, "stage bytes over the barrier limit");
+    if (2 * (p.Mtot + p.rows) >= (1ll << 31)) fail(nm, op, "copy coordinates beyond 32 bits");
+    const NhwcPackPlan& q = b.px;
+    bool same = q.EX == p.EL && q.WL == p.WL && q.npl == p.npl && q.step_h == p.pl_step_h && q.step_w == p.pl_step_w &&
+                q.N == p.N && q.C == p.Cs && q.H == p.Hs && q.W == p.Ws && q.src_nstride == p.src_nstride;
+    for (int pl = 0; pl < p.npl; ++pl) same = same && q.off_h[pl] == p.pl_off_h[pl] && q.off_w[pl] == p.pl_off_w[pl];
+    if (!same) fail(nm, op, "source pack geometry differs from the tap plan's");
+    if (b.src_pack_bytes != (size_t)q.npl * q.nchunk * (size_t)p.Mtot * 16) fail(nm, op, "source pack size");
+  }
+}
+
+// The channel-chunk pack, run on the host exactly as the kernel walks it (units, staged rows
+// and channel runs, output groups), against the definition of the packed planes:
+//   dst[pl][cc][n][e][f][j] = src[n][CHUNK*cc + j][e*step_h + off_h[pl]][f*step_w + off_w[pl]]
+// (zero outside the source).  Every group must be written once with that value; the source
+// holds each element's own index, so a wrong row, column, channel or image shows.  Small
+// tensors only (the emulation touches every element).
+template <class E>
+void check_pack_as_kernel(const char* nm, const char* op, const NhwcPackPlan& q) {
+  constexpr int CHUNK = 16 / (int)sizeof(E);
+  const long long HW = (long long)q.H * q.W;
+  const long long src_elems = (long long)(q.N - 1) * q.src_nstride + (long long)q.C * HW;
+  const long long groups = (long long)q.npl * q.nchunk * q.N * q.EX * q.WL;
+  if (src_elems > (1ll << 22) || groups > (1ll << 22)) return;
+  if (q.units != (unsigned)((long long)q.N * q.nchunk * q.n_etiles) || q.te < 1 ||
+      (long long)q.te * q.n_etiles < q.EX || (long long)q.te * (q.n_etiles - 1) >= q.EX)
+    fail(nm, op, "pack units do not tile the padded rows");
+  std::vector<E> src((size_t)src_elems);
+  for (size_t i = 0; i < src.size(); ++i) src[i] = (E)(i * 2654435761u + 1u);
+  std::vector<E> dst((size_t)groups * CHUNK, (E)0);
+  std::vector<int> wrote((size_t)groups, 0);
+  std::vector<E> sm((size_t)CHUNK * q.ch_pitch);
+  for (unsigned v = 0; v < q.units; ++v) {
+    const int r = (int)(v / (unsigned)q.n_etiles), et = (int)(v % (unsigned)q.n_etiles);
+    const int n = r / q.nchunk, cc = r % q.nchunk;
+    const int e0 = et * q.te, ne = std::min(q.te, q.EX - e0);
+    const int h_lo = e0 * q.step_h + q.off_h_min, h_hi = (e0 + ne - 1) * q.step_h + q.off_h_min + q.h_span;
+    const int hl = std::max(h_lo, 0), hh = std::min(h_hi, q.H - 1), nr = hh - hl + 1;
+    const int nch = std::min(CHUNK, q.C - CHUNK * cc);
+    if (nr > 0) {
+      if ((long long)nr * q.W > q.ch_pitch) {
+        fail(nm, op, "pack unit stages more rows than its channel pitch holds");
+        return;
+      }
+      for (int c = 0; c < nch; ++c)
+        for (long long k = 0; k < (long long)nr * q.W; ++k)
+          sm[(size_t)c * q.ch_pitch + k] = src[(size_t)(n * q.src_nstride + (long long)(CHUNK * cc + c) * HW + (long long)hl * q.W + k)];
+    }
+    for (int pl = 0; pl < q.npl; ++pl)
+      for (int i = 0; i < ne * q.WL; ++i) {
+        const int de = i / q.WL, f = i % q.WL;
+        const int h = (e0 + de) * q.step_h + q.off_h[pl], w = f * q.step_w + q.off_w[pl];
+        const long long g = (((long long)pl * q.nchunk + cc) * q.N + n) * q.EX * q.WL + (long long)e0 * q.WL + i;
+        ++wrote[(size_t)g];
+        for (int c = 0; c < CHUNK; ++c)
+          dst[(size_t)g * CHUNK + c] =
+              (h >= hl && h <= hh && w >= 0 && w < q.W && c < nch) ? sm[(size_t)c * q.ch_pitch + (size_t)(h - hl) * q.W + w] : (E)0;
+      }
+  }
+  for (int pl = 0; pl < q.npl; ++pl)
+    for (int cc = 0; cc < q.nchunk; ++cc)
+      for (int n = 0; n < q.N; ++n)
+        for (int e = 0; e < q.EX; ++e)
+          for (int f = 0; f < q.WL; ++f) {
+            const long long g = ((((long long)pl * q.nchunk + cc) * q.N + n) * q.EX + e) * q.WL + f;
+            if (wrote[(size_t)g] != 1) {
+              fail(nm, op, "a packed group is not written exactly once");
+              return;
+            }
+            const int h = e * q.step_h + q.off_h[pl], w = f * q.step_w + q.off_w[pl];
+            for (int j = 0; j < CHUNK; ++j) {
+              const int c = CHUNK * cc + j;
+              const E want = (c < q.C && h >= 0 && h < q.H && w >= 0 && w < q.W)
+                                 ? src[(size_t)(n * q.src_nstride + (long long)c * HW + (long long)h * q.W + w)]
+                                 : (E)0;
+              if (dst[(size_t)g * CHUNK + j] != want) {
+                fail(nm, op, "a packed element differs from the plane definition");
+                return;
+              }
+            }
+          }
+}
+
+// bf16 backward-filter on channel-chunked planes: the shared-memory carve of the kernel fits the
+// request and the device limit; both packs, run as the kernel walks them, match the plane
+// definition; and the plan's tap groups, offsets and output taps, applied to the packed planes
+// in fp64, give the filter gradient of the definition (small problems: the emulation sums every
+// product).
+void check_wgrad_mn(const char* nm, const Desc& d, const DevInfo& di) {
+  const char* op = "bwd_filter(mn)";
+  MnBuild b;
+  alignas(256) static char ws[64];
+  const int rc = build_wgrad_mn(d, ws, ws, ws, ws, di, b);
+  if (rc == CONV2D_ERR_UNSUPPORTED || rc == CONV2D_ERR_TOO_LARGE) return;
+  if (rc != CONV2D_OK) {
+    fail(nm, op, "planner error");
+    return;
+  }
+  const WgradMnPlan& p = b.p;
+  // carve: 1 KB alignment slack, the stages, 8 epilogue staging tiles of 32 x 80 floats, barriers
+  const size_t carve = 1023 + (size_t)p.stages * (p.a_stage_bytes + p.b_stage_bytes) + 8 * 32 * 80 + 8 * (2 * p.stages + 3) + 8;
+  if (carve > wgrad_mn_smem_bytes(p)) fail(nm, op, "shared-memory carve beyond the request");
+  if (wgrad_mn_smem_bytes(p) > di.smem_optin) fail(nm, op, "shared memory over budget");
+  check_pack_as_kernel<uint16_t>(nm, op, b.px);
+  check_pack_as_kernel<uint16_t>(nm, op, b.pd);
+  const long long M = p.Mtot;
+  const long long macs = (long long)d.K * d.C * d.R * d.S * M;
+  if (macs > 40000000ll || (long long)d.N * d.C * d.H * d.W > 2000000ll) return;
+  std::vector<double> x((size_t)d.N * d.C * d.H * d.W), dy((size_t)d.N * d.K * d.P * d.Q);
+  unsigned long long st = 12345;
+  auto u = [&]() {  // uniform in [-1, 1), splitmix64
+    st += 0x9E3779B97F4A7C15ull;
+    unsigned long long z = st;
+    z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+    z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+    z ^= z >> 31;
+    return (double)(z >> 11) / (double)(1ull << 52) - 1.0;
+  };
+  for (double& v : x) v = u();
+  for (double& v : dy) v = u();
+  auto plane = [&](const NhwcPackPlan& q, const std::vector<double>& src, int pl, int c, long long L) {
+    if (L >= M || c >= q.C) return 0.0;
+    const long long n = L / ((long long)q.EX * q.WL), rem = L % ((long long)q.EX * q.WL);
+    const int h = (int)(rem / q.WL) * q.step_h + q.off_h[pl], w = (int)(rem % q.WL) * q.step_w + q.off_w[pl];
+    if (h < 0 || h >= q.H || w < 0 || w >= q.W) return 0.0;
+    return src[(((size_t)n * q.C + c) * q.H + h) * q.W + w];
+  };
+  std::vector<double> dw((size_t)d.K * d.C * d.R * d.S, NAN);
+  std::vector<int> seen((size_t)d.R * d.S, 0);
+  for (int gi = 0; gi < p.ngroups; ++gi)
+    for (int j = 0; j < p.grp_ntaps[gi]; ++j) {
+      const int t = p.grp_tap0[gi] + j;
+      const int off = p.grp_off0[gi] + p.tap_delta[t];
+      if (p.tap_delta[t] + p.KB > p.KBX) fail(nm, op, "tap offset beyond the staged box");
+      if (p.tap_out[t] < 0 || p.tap_out[t] >= d.R * d.S) {
+        fail(nm, op, "output tap outside the filter");
+        return;
+      }
+      ++seen[(size_t)p.tap_out[t]];
+      for (int k = 0; k < d.K; ++k)
+        for (int c = 0; c < d.C; ++c) {
+          double acc = 0;
+          for (long long L = 0; L < M; ++L)
+            acc += plane(b.px, x, p.grp_plane[gi], c, L + off) * plane(b.pd, dy, 0, k, L);
+          dw[((size_t)k * d.C + c) * d.R * d.S + p.tap_out[t]] = acc;
+        }
+    }
+  for (size_t i = 0; i < seen.size(); ++i)
+    if (seen[i] != 1) {
+      fail(nm, op, "a filter tap is not produced exactly once");
+      return;
+    }
+  for (int k = 0; k < d.K; ++k)
+    for (int c = 0; c < d.C; ++c)
+      for (int r = 0; r < d.R; ++r)
+        for (int s2 = 0; s2 < d.S; ++s2) {
+          double ref = 0;
+          for (int n = 0; n < d.N; ++n)
+            for (int pp = 0; pp < d.P; ++pp)
+              for (int q = 0; q < d.Q; ++q) {
+                const int h = pp * d.sh - d.ph + r * d.dh, w = q * d.sw - d.pw + s2 * d.dw;
+                if (h < 0 || h >= d.H || w < 0 || w >= d.W) continue;
+                ref += x[(((size_t)n * d.C + c) * d.H + h) * d.W + w] * dy[(((size_t)n * d.K + k) * d.P + pp) * d.Q + q];
+              }
+          const double got = dw[(((size_t)k * d.C + c) * d.R + r) * d.S + s2];
+          if (!(std::fabs(got - ref) <= 1e-9 * (1.0 + std::fabs(ref)))) {
+            fail(nm, op, "the planned GEMM on the packed planes differs from the definition");
+            return;
+          }
+        }
+}
+
+// The workspace of a tap set: the repacked filters of the passes, then (single pass) the packed
+// source, 256-byte aligned and inside the set's size.
+void check_tap_set(const char* nm, const char* op, const TapSet& set, const void* ws, int dt) {
+  if (set.pass.size() != 1 || !set.pass[0].p.a_tma) return;
+  const TapBuild& b = set.pass[0];
+  const size_t off = static_cast<const uint8_t*>(b.px.dst) - static_cast<const uint8_t*>(ws);
+  if (off % 256 || off < b.pack_bytes || off + b.src_pack_bytes != set.pack_bytes)
+    fail(nm, op, "packed source misplaced in the workspace");
+  if (dt == 1) check_pack_as_kernel<uint16_t>(nm, op, b.px);
+  else check_pack_as_kernel<uint32_t>(nm, op, b.px);
 }
 
 // Every real tap of every pass reads, for every output the plan writes, the source pixel the
@@ -288,11 +477,12 @@ void check_phase_choice(int& plans) {
 int main() {
   using namespace cg3;
   // The last field gives the tap passes expected for forward and backward-data.  The tap GEMM
-  // stages the filter slices of every tap of a phase for each k-block; with a stride-1 15x15
-  // filter and more than 4 fp32 (8 bf16) source channels that is 225 taps x 2 chunks x 16
-  // columns x 16 bytes = 115 KB a stage, so two stages do not fit in shared memory and the
-  // taps are split over passes.  With at most 4 (8) source channels two taps share one MMA
-  // and the slices halve.  The source channels are C forward and K backward-data.
+  // stages the filter slices of every tap of a phase for each k-block: in tap-pair mode one
+  // 16-byte chunk of source channels per tap (two taps share one MMA), otherwise two or more.
+  // A 16x16 stride-1 filter over N = 64 columns is 256 taps x 64 x 16 bytes = 256 KB a stage
+  // even in pair mode, so two stages do not fit in shared memory and the taps are split over
+  // passes; smaller N or fewer taps fit one pass.  The source channels are C forward and K
+  // backward-data; N follows the destination channels (K forward, C backward-data).
   std::vector<Shape> shapes = {
       {"tiny", 2, 3, 8, 8, 4, 3, 3, 1, 1, 1, 1, 0, 1, 1, 1, {1, 1}},
       {"resnet3x3", 32, 64, 56, 56, 64, 3, 3, 1, 1, 1, 1, 0, 1, 1, 1, {1, 1}},
@@ -305,11 +495,15 @@ int main() {
       {"k300", 1, 17, 6, 6, 300, 3, 3, 1, 1, 1, 1, 0, 1, 1, 1, {1, 1}},
       {"c300", 2, 300, 5, 5, 20, 3, 3, 1, 1, 1, 1, 1, 1, 1, 1, {1, 1}},
       {"c5k300", 2, 5, 17, 13, 300, 5, 3, 2, 1, 2, 1, 1, 1, 1, 1, {1, 1}},
-      {"r15", 1, 4, 40, 40, 8, 15, 15, 7, 7, 1, 1, 0, 1, 1, 1, {1, 2}},
-      {"r15_k4", 1, 8, 40, 40, 4, 15, 15, 7, 7, 1, 1, 0, 1, 1, 1, {2, 1}},
-      {"r16_c16", 1, 16, 40, 40, 16, 16, 16, 7, 7, 1, 1, 0, 1, 1, 1, {2, 2}},
-      {"r16_s2_bf16", 2, 24, 40, 40, 20, 16, 16, 7, 7, 2, 2, 1, 1, 1, 1, {4, 1}},
-      {"r1_s256", 1, 16, 4, 300, 16, 1, 256, 0, 3, 1, 1, 0, 1, 1, 1, {2, 2}},
+      {"r15", 1, 4, 40, 40, 8, 15, 15, 7, 7, 1, 1, 0, 1, 1, 1, {1, 1}},
+      {"r15_k4", 1, 8, 40, 40, 4, 15, 15, 7, 7, 1, 1, 0, 1, 1, 1, {1, 1}},
+      {"r16_c16", 1, 16, 40, 40, 16, 16, 16, 7, 7, 1, 1, 0, 1, 1, 1, {1, 1}},
+      {"r16_c32", 1, 32, 40, 40, 32, 16, 16, 7, 7, 1, 1, 0, 1, 1, 1, {2, 2}},
+      {"r13_c64", 1, 64, 30, 30, 64, 13, 13, 6, 6, 1, 1, 0, 1, 1, 1, {2, 2}},
+      {"r15_bf16_k96", 1, 40, 40, 40, 96, 15, 15, 7, 7, 1, 1, 1, 1, 1, 1, {4, 2}},
+      {"r16_s2_bf16", 2, 24, 40, 40, 20, 16, 16, 7, 7, 2, 2, 1, 1, 1, 1, {2, 1}},
+      {"r1_s256", 1, 16, 4, 300, 16, 1, 256, 0, 3, 1, 1, 0, 1, 1, 1, {1, 1}},
+      {"r1_s256_c64", 1, 64, 4, 300, 64, 1, 256, 0, 3, 1, 1, 0, 1, 1, 1, {3, 3}},
       {"s32", 2, 40, 23, 19, 24, 3, 3, 1, 1, 3, 2, 1, 1, 1, 1, {1, 1}},
       {"hr", 1, 2, 6, 13, 2, 6, 13, 0, 0, 1, 1, 0, 1, 1, 1, {1, 1}},
       {"rows5", 1, 40, 16, 16, 48, 5, 3, 2, 1, 1, 1, 0, 1, 1, 1, {1, 1}},
@@ -353,8 +547,8 @@ int main() {
     for (int op = 0; op < 2; ++op) {
       const char* opn = op == 0 ? "fwd" : "bwd_data";
       TapSet set;
-      const int rc = op == 0 ? build_tap_set(CONV2D_OP_FWD, d, px, pw, py, ws, di, set)
-                             : build_tap_set(CONV2D_OP_BWD_DATA, d, py, pw, px, ws, di, set);
+      const int rc = op == 0 ? build_tap_set(CONV2D_OP_FWD, d, px, pw, py, ws, di, set, true)
+                             : build_tap_set(CONV2D_OP_BWD_DATA, d, py, pw, px, ws, di, set, true);
       if (rc != CONV2D_OK) {
         fail(s.nm, opn, "no plan");
         continue;
@@ -368,6 +562,7 @@ int main() {
         ++plans;
       }
       check_tap_semantics(s.nm, opn, d, set, op == 0);
+      check_tap_set(s.nm, opn, set, ws, d.dt);
     }
     for (const auto& v : kWgradVariants) {  // every staging variant the planner may fall back to
       WgradBuild bw;
@@ -380,6 +575,9 @@ int main() {
     WgradBuild bw;
     if (build_bwd_filter(d, px, py, pw, ws, di, bw) != CONV2D_OK) fail(s.nm, "bwd_filter", "no plan");
     check_phases(s.nm, d, di, plans);
+    Desc d16 = d;  // the channel-chunked path plans bf16 only
+    d16.dt = 1;
+    check_wgrad_mn(s.nm, d16, di);
   }
   check_phase_choice(plans);
   int refused = 0;  // backward-filter problems refused with CONV2D_ERR_UNSUPPORTED
@@ -430,8 +628,8 @@ int main() {
       void* ws = (void*)0x400000;
       for (int op = 0; op < 2; ++op) {
         TapSet set;
-        const int rc = op == 0 ? build_tap_set(CONV2D_OP_FWD, d, px, pw, py, ws, di, set)
-                               : build_tap_set(CONV2D_OP_BWD_DATA, d, py, pw, px, ws, di, set);
+        const int rc = op == 0 ? build_tap_set(CONV2D_OP_FWD, d, px, pw, py, ws, di, set, true)
+                               : build_tap_set(CONV2D_OP_BWD_DATA, d, py, pw, px, ws, di, set, true);
         if (rc != CONV2D_OK) {
           fail(nm, op == 0 ? "fwd" : "bwd_data", "no plan");
           continue;
@@ -441,6 +639,7 @@ int main() {
           ++plans;
         }
         check_tap_semantics(nm, op == 0 ? "fwd" : "bwd_data", d, set, op == 0);
+        check_tap_set(nm, op == 0 ? "fwd" : "bwd_data", set, ws, d.dt);
       }
       WgradBuild bw;
       const int rcw = build_bwd_filter(d, px, py, pw, ws, di, bw);
@@ -454,6 +653,7 @@ int main() {
         ++refused;  // the documented refusal: no stage layout fits shared memory
       }
       check_phases(nm, d, di, plans);
+      if (d.dt == 1) check_wgrad_mn(nm, d, di);
     }
   }
   // Layer-scale strided or dilated filter gradients whose slot ring does not fit are refused

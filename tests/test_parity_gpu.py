@@ -488,11 +488,12 @@ def test_groups_parity(cg, case, groups, dil, flip, dtype):
 # taps run in contiguous ranges, the first pass with the caller's bias and beta, the later
 # ones adding on.  The comment gives the passes the planner makes (forward, backward-data).
 PASS_CASES = [
-    ((1, 4, 40, 40, 8, 15, 15, 7, 7, 1, 1), "f32"),     # 1, 2
-    ((1, 8, 40, 40, 4, 15, 15, 7, 7, 1, 1), "f32"),     # 2, 1
-    ((1, 16, 40, 40, 16, 16, 16, 7, 7, 1, 1), "f32"),   # 2, 2
-    ((2, 24, 40, 40, 20, 16, 16, 7, 7, 2, 2), "bf16"),  # 4, 1
-    ((1, 16, 4, 300, 16, 1, 256, 0, 3, 1, 1), "f32"),   # 2, 2
+    ((1, 16, 40, 40, 16, 16, 16, 7, 7, 1, 1), "f32"),   # 1, 1 (tap pairs: 256 taps in one pass)
+    ((1, 32, 40, 40, 32, 16, 16, 7, 7, 1, 1), "f32"),   # 2, 2
+    ((1, 64, 30, 30, 64, 13, 13, 6, 6, 1, 1), "f32"),   # 2, 2
+    ((2, 24, 40, 40, 20, 16, 16, 7, 7, 2, 2), "bf16"),  # 2, 1
+    ((1, 40, 40, 40, 96, 15, 15, 7, 7, 1, 1), "bf16"),  # 4, 2
+    ((1, 64, 4, 300, 64, 1, 256, 0, 3, 1, 1), "f32"),   # 3, 3
 ]
 
 
