@@ -26,6 +26,7 @@ cudaError_t launch_space_to_depth(const S2dPlan& sp, int dt, cudaStream_t st);
 size_t wgrad_smem_bytes(const WgradPlan& p, int dt);
 cudaError_t launch_wgrad_mn(const WgradMnPlan& p, int grid, cudaStream_t st);
 cudaError_t launch_nhwc_pack(const NhwcPackPlan& a, const NhwcPackPlan& b, int dt, int num_sms, cudaStream_t st);
+cudaError_t launch_tap_packs(const NhwcPackPlan& px, const PackPlan& pp, int dt, int num_sms, cudaStream_t st);
 cudaError_t launch_wgrad_reduce_t(const ReduceTPlan& rp, int dt, int num_sms, cudaStream_t st);
 size_t wgrad_mn_smem_bytes(const WgradMnPlan& p);
 int tap_gemm_take_error();
@@ -1103,8 +1104,8 @@ bool encode_mn_map(CUtensorMap* m, const void* base, int rank, const uint64_t* d
 }
 
 // Work-unit tiling of a pack (NhwcPackPlan): the most padded rows per unit whose staged channel
-// runs fit 32 KB of shared memory (at least one row, then up to 200 KB); false if none fits or
-// the unit count passes 32 bits.
+// runs of one chunk fit 32 KB of shared memory (at least one row, then up to 200 KB), then the
+// chunks per unit; false if none fits or the unit count passes 32 bits.
 bool setup_pack_tiles(NhwcPackPlan& q, int esz) {
   const int CHUNK = 16 / esz;
   int lo = q.off_h[0], hi = q.off_h[0];
@@ -1124,11 +1125,19 @@ bool setup_pack_tiles(NhwcPackPlan& q, int esz) {
   q.te = te;
   q.ch_pitch = (int)pitch(te);
   q.n_etiles = (q.EX + te - 1) / te;
-  const long long units = (long long)q.N * q.nchunk * q.n_etiles;
+  // chunks per unit: as many as fit the same 32 KB, while the units still number four per SM
+  // of a full GPU (small images: one unit per chunk leaves the work per block too small)
+  int cg = 1;
+  while (cg < q.nchunk && (long long)(cg + 1) * CHUNK * q.ch_pitch * esz <= 32 * 1024 &&
+         (long long)q.N * ((q.nchunk + cg) / (cg + 1)) * q.n_etiles >= 4 * 152)
+    ++cg;
+  q.cg = cg;
+  q.ngroups = (q.nchunk + cg - 1) / cg;
+  const long long units = (long long)q.N * q.ngroups * q.n_etiles;
   if (units >= (1ll << 31)) return false;
   q.units = (unsigned)units;
   q.fd_et = make_fastdiv((uint32_t)q.n_etiles);
-  q.fd_nchunk = make_fastdiv((uint32_t)q.nchunk);
+  q.fd_ng = make_fastdiv((uint32_t)q.ngroups);
   return true;
 }
 
@@ -1658,12 +1667,15 @@ static int run_tap(int op, const Desc& d, int groups, const void* src, const voi
       b.p.bias = bias != nullptr && pi == 0 ? byte_ptr(bias) + gi * bias_g * esz : nullptr;
       if (b.p.a_tma) {  // the group's source, packed channel-chunk-wise for the tensor copies
         b.px.src = b.p.src;
-        NhwcPackPlan none;
-        std::memset(&none, 0, sizeof(none));
-        rc = launch_err(launch_nhwc_pack(b.px, none, d.dt, di.sms, st));
+        if (b.pack_bytes) {  // with the filter pack in the same launch
+          rc = launch_err(launch_tap_packs(b.px, b.pp, d.dt, di.sms, st));
+        } else {
+          NhwcPackPlan none;
+          std::memset(&none, 0, sizeof(none));
+          rc = launch_err(launch_nhwc_pack(b.px, none, d.dt, di.sms, st));
+        }
         if (rc) return rc;
-      }
-      if (b.pack_bytes) {
+      } else if (b.pack_bytes) {
         rc = launch_err(launch_pack_filter(b.pp, d.dt, st));
         if (rc) return rc;
       }

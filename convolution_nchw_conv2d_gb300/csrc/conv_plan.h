@@ -239,10 +239,10 @@ struct ReducePlan {
 // position, so a tile of positions x channel chunks is one tensor copy into the MN-major operand
 // layout, and a shift of the position by one is a shift of one 16-byte row.
 //
-// Work unit = (image n, chunk cc, tile of te padded rows e): the CHUNK source channels' rows that
-// the tile's planes read, [h_lo, h_lo + span] with h_lo = e0*step_h + off_h_min, are one
-// contiguous run per channel, staged in shared memory by coalesced loads; the unit's output of
-// each plane is one contiguous run of te*WL 16-byte groups.
+// Work unit = (image n, group of cg chunks, tile of te padded rows e): the source rows that the
+// tile's planes read, [h_lo, h_lo + span] with h_lo = e0*step_h + off_h_min, are one contiguous
+// run per channel, staged in shared memory by coalesced copies; the unit's output of each chunk
+// and plane is one contiguous run of te*WL 16-byte groups.
 struct NhwcPackPlan {
   const void* src;
   void* dst;
@@ -255,11 +255,12 @@ struct NhwcPackPlan {
   int step_h, step_w;
   int off_h[kMaxPlanes], off_w[kMaxPlanes];
   int off_h_min, h_span;  // smallest plane row offset; largest minus smallest
-  int te, n_etiles;       // padded rows per unit; units per (image, chunk)
+  int te, n_etiles;       // padded rows per unit; row tiles per image
+  int cg, ngroups;        // chunks per unit; chunk groups per image
   int ch_pitch;           // staged elements per channel: (te-1)*step_h + h_span + 1 rows of W,
                           // rounded up to 16 bytes
-  unsigned units;         // N * nchunk * n_etiles (< 2^31)
-  FastDiv fd_et, fd_nchunk;  // division by n_etiles and by nchunk
+  unsigned units;         // N * ngroups * n_etiles (< 2^31)
+  FastDiv fd_et, fd_ng;   // division by n_etiles and by ngroups
 };
 
 // Backward-filter on channel-chunked planes (bf16): for every filter tap t of a stride phase,

@@ -30,6 +30,7 @@
 #include <mutex>
 #include <vector>
 
+#include "conv_pack.cuh"
 #include "conv_plan.h"
 #include "conv_stage.cuh"
 #include "sm103_ptx.cuh"
@@ -418,125 +419,33 @@ __global__ void __launch_bounds__(kThreads, 1) tap_gemm_kernel(const __grid_cons
 }
 
 // ---------------------------------------------------------------------------- packing
-// wpack chunk index = (((nt * nkb + kb) * ntaps + t) * NCH + j) * NT + n; the chunk holds
-// CHUNK consecutive source channels cs = kb*CB + j*CHUNK + e of out channel nt*NT + n
-// for filter tap (tap_r[t], tap_s[t]); zero outside the tensor.  fp32 values are
-// rounded to tf32 (round to nearest, ties away) on the way.
-//
-// Work unit = (n tile, k block, UN consecutive out channels of the tile): the unit's filter
-// values for every tap are staged in shared memory with coalesced 16-byte reads where aligned
-// (for a fixed out channel the CB source channels x R*S taps are one contiguous run of the
-// KCRS filter; with `transpose`, for a fixed source channel the UN out channels x R*S are), at
-// a row pitch per out channel that spreads the UN rows over distinct banks; then each chunk is
-// gathered from shared memory and stored, consecutive threads storing consecutive out channels.
+// Filter pack alone (pack_filter_one per chunk).
 template <int DT>
-__global__ void __launch_bounds__(256) pack_filter_kernel(const __grid_constant__ PackPlan pp, int UN, int pitch) {
-  constexpr int ESZ = DT == 0 ? 4 : 2;
-  constexpr int CHUNK = 16 / ESZ;
-  using E = typename std::conditional<DT == 0, uint32_t, uint16_t>::type;
-  extern __shared__ __align__(16) uint8_t pf_smem[];
-  E* sm = reinterpret_cast<E*>(pf_smem);
-  const int NCH = pp.CB / CHUNK;
-  const int RS = pp.R * pp.S;
+__global__ void __launch_bounds__(256) pack_filter_kernel(const __grid_constant__ PackPlan pp) {
   griddep_launch_dependents();  // the GEMM may start; it waits for this grid before reading wpack
-  const int nsub = (pp.NT + UN - 1) / UN;
-  const long long units = (long long)pp.n_ntiles * pp.nkb * nsub;
-  for (long long u = blockIdx.x; u < units; u += gridDim.x) {
-    const int sub = (int)(u % nsub);
-    const long long rest = u / nsub;
-    const int kb = (int)(rest % pp.nkb);
-    const int nt = (int)(rest / pp.nkb);
-    const int nl0 = sub * UN;                       // first out channel of the unit within the tile
-    const int ncnt = min(UN, pp.NT - nl0);
-    const int n0 = nt * pp.NT + nl0, c0 = kb * pp.CB;
-    __syncthreads();  // the previous unit's reads of shared memory are done
-    // The staged values are NRUN contiguous runs of the filter, RLEN elements each (the first
-    // `valid` of them exist); a thread copies 16-byte groups of a run, four groups in flight.
-    const int RLEN = pp.transpose ? UN * RS : pp.CB * RS;
-    const int NRUN = pp.transpose ? pp.CB : UN;
-    const int NG = (RLEN + CHUNK - 1) / CHUNK;  // 16-byte groups per run
-    const int total_g = NRUN * NG;
-    for (int base = (int)threadIdx.x; base < total_g; base += 4 * (int)blockDim.x) {
-      E val[4][CHUNK];
-#pragma unroll
-      for (int bq = 0; bq < 4; ++bq) {
-        const int gi = base + bq * (int)blockDim.x;
-#pragma unroll
-        for (int e = 0; e < CHUNK; ++e) val[bq][e] = 0;
-        if (gi >= total_g) continue;
-        const int k = gi / NG, q0 = (gi - k * NG) * CHUNK;
-        long long start;
-        int valid;
-        if (!pp.transpose) {  // run k = out channel n0 + k: source channels c0.. x taps
-          const int nn = n0 + k;
-          valid = (k < ncnt && nn < pp.Cd) ? min(pp.CB, pp.Cs - c0) * RS : 0;
-          start = ((long long)nn * pp.C + c0) * RS;
-        } else {  // run k = source channel c0 + k: out channels n0.. x taps
-          const int cs = c0 + k;
-          valid = cs < pp.Cs ? min(ncnt, pp.Cd - n0) * RS : 0;
-          start = ((long long)cs * pp.C + n0) * RS;
-        }
-        const E* g = static_cast<const E*>(pp.w) + start + q0;
-        if (q0 + CHUNK <= valid && (reinterpret_cast<uintptr_t>(g) & 15u) == 0) {
-          const uint4 t4 = __ldg(reinterpret_cast<const uint4*>(g));
-          const uint32_t wd[4] = {t4.x, t4.y, t4.z, t4.w};
-#pragma unroll
-          for (int e = 0; e < CHUNK; ++e) {
-            if constexpr (DT == 0) val[bq][e] = wd[e];
-            else val[bq][e] = (E)(wd[e >> 1] >> (16 * (e & 1)));
-          }
-        } else {
-#pragma unroll
-          for (int e = 0; e < CHUNK; ++e)
-            if (q0 + e < valid) val[bq][e] = g[e];
-        }
-      }
-#pragma unroll
-      for (int bq = 0; bq < 4; ++bq) {
-        const int gi = base + bq * (int)blockDim.x;
-        if (gi >= total_g) continue;
-        const int k = gi / NG, q0 = (gi - k * NG) * CHUNK;
-#pragma unroll
-        for (int e = 0; e < CHUNK; ++e) {
-          const int q = q0 + e;
-          if (q >= RLEN) break;
-          if (!pp.transpose) {
-            sm[k * pitch + q] = val[bq][e];
-          } else {
-            const int nl = q / RS;
-            sm[nl * pitch + k * RS + (q - nl * RS)] = val[bq][e];
-          }
-        }
-      }
-    }
-    __syncthreads();
-    const int outs = pp.ntaps_total * NCH * UN;
-    for (int i = (int)threadIdx.x; i < outs; i += (int)blockDim.x) {
-      const int tj = i / UN, nl = i - tj * UN;
-      const int t = tj / NCH, j = tj - t * NCH;
-      if (nl >= ncnt) continue;
-      int r = pp.tap_r[t], s = pp.tap_s[t];
-      if (pp.flip && r >= 0) {  // convolution mode: the filter rotated by 180 degrees
-        r = pp.R - 1 - r;
-        s = pp.S - 1 - s;
-      }
-      uint32_t out[4] = {0u, 0u, 0u, 0u};
-      if (r >= 0) {
-        const E* src = sm + nl * pitch + (j * CHUNK) * RS + r * pp.S + s;
-#pragma unroll
-        for (int e = 0; e < CHUNK; ++e) {
-          if constexpr (DT == 0) {
-            uint32_t tf;
-            asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(tf) : "f"(__uint_as_float(src[e * RS])));
-            out[e] = tf;
-          } else {
-            out[e >> 1] |= (uint32_t)src[e * RS] << (16 * (e & 1));
-          }
-        }
-      }
-      const long long oidx = (((long long)(nt * pp.nkb + kb) * pp.ntaps_total + t) * NCH + j) * pp.NT + nl0 + nl;
-      reinterpret_cast<uint4*>(pp.wpack)[oidx] = make_uint4(out[0], out[1], out[2], out[3]);
-    }
+  const int NCH = pp.CB / (DT == 0 ? 4 : 8);
+  const long long total = (long long)pp.n_ntiles * pp.nkb * NCH * pp.NT * pp.ntaps_total;
+  for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < total;
+       idx += (long long)gridDim.x * blockDim.x)
+    pack_filter_one<DT>(pp, idx);
+}
+
+// The two packs that precede a tap GEMM with packed-source staging, in one launch: blocks
+// [0, xblocks) run the source's channel-chunk pack units, the others the filter chunks, so
+// that neither waits for the other's tail.
+template <int DT>
+__global__ void __launch_bounds__(256) tap_packs_kernel(const __grid_constant__ NhwcPackPlan px,
+                                                        const __grid_constant__ PackPlan pp, unsigned xblocks) {
+  extern __shared__ __align__(16) uint8_t pk_smem[];
+  griddep_launch_dependents();  // the GEMM may start; it waits for this grid before its copies
+  if (blockIdx.x < xblocks) {
+    for (uint32_t u = blockIdx.x; u < px.units; u += xblocks) nhwc_pack_unit<DT>(px, u, pk_smem);
+  } else {
+    const int NCH = pp.CB / (DT == 0 ? 4 : 8);
+    const long long total = (long long)pp.n_ntiles * pp.nkb * NCH * pp.NT * pp.ntaps_total;
+    const long long nthr = (long long)(gridDim.x - xblocks) * blockDim.x;
+    for (long long idx = (blockIdx.x - xblocks) * (long long)blockDim.x + threadIdx.x; idx < total; idx += nthr)
+      pack_filter_one<DT>(pp, idx);
   }
 }
 
@@ -580,43 +489,37 @@ cudaError_t launch_tap_gemm(const TapPlan& p, int dt, int grid, cudaStream_t st)
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
-// Out channels per filter-pack unit (32, or fewer when the staged values would pass 48 KB; at
-// least 1) and the staged row pitch in elements: CB * R * S rounded up so that consecutive rows
-// start in different 4-byte banks (an odd number of words apart).
-void pack_filter_shape(const PackPlan& pp, int dt, int* un, int* pitch) {
-  const int esz = dt == 0 ? 4 : 2;
-  int p = pp.CB * pp.R * pp.S;
-  if (dt == 0) p |= 1;
-  else p = (p + 1) / 2 * 2 + ((((p + 1) / 2) & 1) ? 0 : 2);
-  int u = 32;
-  while (u > 1 && (long long)u * p * esz > 48 * 1024) u >>= 1;
-  *un = u;
-  *pitch = p;
-}
-
-size_t pack_filter_smem_bytes(const PackPlan& pp, int dt) {
-  int un, pitch;
-  pack_filter_shape(pp, dt, &un, &pitch);
-  return (size_t)un * pitch * (dt == 0 ? 4 : 2);
-}
-
-cudaError_t launch_pack_filter(const PackPlan& pp, int dt, cudaStream_t st) {
-  int un, pitch;
-  pack_filter_shape(pp, dt, &un, &pitch);
-  const size_t smem = (size_t)un * pitch * (dt == 0 ? 4 : 2);
-  const long long units = (long long)pp.n_ntiles * pp.nkb * ((pp.NT + un - 1) / un);
-  long long blocks = std::min<long long>(std::max(1ll, units), 4096);
+// Source pack px (units over at most 6 blocks per SM) and filter pack pp (one chunk per thread,
+// at most 2 blocks per SM of threads) in one launch.
+cudaError_t launch_tap_packs(const NhwcPackPlan& px, const PackPlan& pp, int dt, int num_sms, cudaStream_t st) {
+  const int CHUNK = dt == 0 ? 4 : 8;
+  const size_t smem = nhwc_pack_smem_bytes(px, dt);
+  const long long per_sm = std::max<long long>(1, std::min<long long>(6, (long long)(200 * 1024) / (long long)std::max<size_t>(smem, 1)));
+  const long long xb = std::max(1ll, std::min<long long>((long long)px.units, (long long)num_sms * per_sm));
+  const long long total = (long long)pp.n_ntiles * pp.nkb * pp.ntaps_total * (pp.CB / CHUNK) * pp.NT;
+  const long long fb = std::max(1ll, std::min<long long>((total + 255) / 256, (long long)num_sms * 2));
   static std::atomic<int> set_bytes[2][kMaxDevices];
   cudaError_t e;
   if (dt == 0) {
-    e = ensure_dyn_smem(pack_filter_kernel<0>, smem, set_bytes[0]);
+    e = ensure_dyn_smem(tap_packs_kernel<0>, smem, set_bytes[0]);
     if (e != cudaSuccess) return e;
-    pack_filter_kernel<0><<<(int)blocks, 256, smem, st>>>(pp, un, pitch);
+    tap_packs_kernel<0><<<(unsigned)(xb + fb), 256, smem, st>>>(px, pp, (unsigned)xb);
   } else {
-    e = ensure_dyn_smem(pack_filter_kernel<1>, smem, set_bytes[1]);
+    e = ensure_dyn_smem(tap_packs_kernel<1>, smem, set_bytes[1]);
     if (e != cudaSuccess) return e;
-    pack_filter_kernel<1><<<(int)blocks, 256, smem, st>>>(pp, un, pitch);
+    tap_packs_kernel<1><<<(unsigned)(xb + fb), 256, smem, st>>>(px, pp, (unsigned)xb);
   }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_pack_filter(const PackPlan& pp, int dt, cudaStream_t st) {
+  const int CHUNK = dt == 0 ? 4 : 8;
+  const long long total = (long long)pp.n_ntiles * pp.nkb * pp.ntaps_total * (pp.CB / CHUNK) * pp.NT;
+  const long long blocks = std::max(1ll, std::min<long long>((total + 255) / 256, 8192));
+  if (dt == 0)
+    pack_filter_kernel<0><<<(int)blocks, 256, 0, st>>>(pp);
+  else
+    pack_filter_kernel<1><<<(int)blocks, 256, 0, st>>>(pp);
   return cudaGetLastError();
 }
 

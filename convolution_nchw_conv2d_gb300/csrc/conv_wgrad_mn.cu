@@ -26,6 +26,7 @@
 
 #include <cuda_bf16.h>
 
+#include "conv_pack.cuh"
 #include "conv_plan.h"
 #include "sm103_ptx.cuh"
 #include "launch_util.cuh"
@@ -77,100 +78,18 @@ __device__ __forceinline__ void issue_mn_stage(const WgradMnPlan& p, uint32_t tm
 
 }  // namespace
 
-// Channel-chunk pack (NhwcPackPlan), one work unit per block iteration: the unit's channel runs
-// are staged in shared memory (16-byte asynchronous copies when every run starts on a 16-byte
-// boundary and is whole 16-byte groups, batched element loads otherwise; channels past C are not
-// read), then each output
-// 16-byte group is assembled from CHUNK shared-memory reads of its position and stored, with
-// consecutive threads storing consecutive groups.  The units of plan `a` come first, then those of
-// plan `b` (b.src NULL: none), so the packs of x and dy are one launch.
+// Channel-chunk packs of plan `a` and (b.src not NULL) plan `b` in one launch: the units of `a`,
+// then those of `b`, one per block iteration (nhwc_pack_unit).
 template <int DT>
 __global__ void __launch_bounds__(256) nhwc_pack_kernel(const __grid_constant__ NhwcPackPlan a,
                                                         const __grid_constant__ NhwcPackPlan b) {
-  constexpr int CHUNK = DT == 0 ? 4 : 8;
-  constexpr int ESZ = DT == 0 ? 4 : 2;
-  using E = typename std::conditional<DT == 0, uint32_t, uint16_t>::type;
   extern __shared__ __align__(16) uint8_t pk_smem[];
-  E* sm = reinterpret_cast<E*>(pk_smem);
   const uint32_t na = a.units, nb = b.src != nullptr ? b.units : 0u;
   for (uint32_t u = blockIdx.x; u < na + nb; u += gridDim.x) {
-    const bool first = u < na;
-    const NhwcPackPlan& p = first ? a : b;
-    const uint32_t v = first ? u : u - na;
-    const uint32_t r = fdiv(v, p.fd_et);  // r = n * nchunk + cc
-    const int et = (int)(v - r * (uint32_t)p.n_etiles);
-    const uint32_t n = fdiv(r, p.fd_nchunk);
-    const int cc = (int)(r - n * (uint32_t)p.nchunk);
-    const int e0 = et * p.te, ne = min(p.te, p.EX - e0);
-    const int h_lo = e0 * p.step_h + p.off_h_min;
-    const int h_hi = (e0 + ne - 1) * p.step_h + p.off_h_min + p.h_span;
-    const int hl = max(h_lo, 0), hh = min(h_hi, p.H - 1);
-    const int nr = hh - hl + 1;  // staged rows (none when <= 0)
-    const int nch = min(CHUNK, p.C - CHUNK * cc);
-    __syncthreads();  // the previous unit's reads of shared memory are done
-    if (nr > 0) {
-      const long long HW = (long long)p.H * p.W;
-      const E* base = static_cast<const E*>(p.src) + (long long)n * p.src_nstride + (long long)(CHUNK * cc) * HW +
-                      (long long)hl * p.W;
-      const int len = nr * p.W;  // elements per channel run
-      const bool vec =
-          ((reinterpret_cast<uintptr_t>(base) | (uintptr_t)(HW * ESZ) | (uintptr_t)(len * ESZ)) & 15u) == 0;
-      if (vec) {  // asynchronous 16-byte copies: all of a thread's copies in flight at once
-        const int g = len * ESZ / 16;  // 16-byte groups per channel run
-        const uint32_t s0 = smem_u32(sm);
-        for (int i = (int)threadIdx.x; i < nch * g; i += (int)blockDim.x) {
-          const int c = i / g, k = i - c * g;
-          cp_async_16(s0 + (uint32_t)((c * p.ch_pitch) * ESZ + k * 16), base + c * HW + k * (16 / ESZ), 16);
-        }
-        cp_async_commit();
-        cp_async_wait<0>();
-      } else {  // element loads, eight in flight per thread before their stores
-        const int tot = nch * len;
-        for (int i0 = (int)threadIdx.x; i0 < tot; i0 += 8 * (int)blockDim.x) {
-          E v[8];
-#pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            const int i = i0 + u * (int)blockDim.x;
-            if (i < tot) {
-              const int c = i / len, k = i - c * len;
-              v[u] = base[c * HW + k];
-            }
-          }
-#pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            const int i = i0 + u * (int)blockDim.x;
-            if (i < tot) {
-              const int c = i / len, k = i - c * len;
-              sm[c * p.ch_pitch + k] = v[u];
-            }
-          }
-        }
-      }
-    }
-    __syncthreads();
-    const int groups = ne * p.WL;
-    for (int pl = 0; pl < p.npl; ++pl) {
-      uint4* dst = reinterpret_cast<uint4*>(p.dst) + ((((long long)pl * p.nchunk + cc) * p.N + n) * p.EX + e0) * p.WL;
-      for (int i = (int)threadIdx.x; i < groups; i += (int)blockDim.x) {
-        const int de = (int)fdiv((uint32_t)i, p.fd_WL);
-        const int f = i - de * p.WL;
-        const int h = (e0 + de) * p.step_h + p.off_h[pl];
-        const int w = f * p.step_w + p.off_w[pl];
-        uint32_t o[4] = {0u, 0u, 0u, 0u};
-        if (h >= hl && h <= hh && w >= 0 && w < p.W) {
-          const E* s0 = sm + (h - hl) * p.W + w;
-#pragma unroll
-          for (int c = 0; c < CHUNK; ++c) {
-            if (c < nch) {
-              const uint32_t x = (uint32_t)s0[c * p.ch_pitch];
-              if constexpr (DT == 0) o[c] = x;
-              else o[c >> 1] |= x << (16 * (c & 1));
-            }
-          }
-        }
-        dst[i] = make_uint4(o[0], o[1], o[2], o[3]);
-      }
-    }
+    if (u < na)
+      nhwc_pack_unit<DT>(a, u, pk_smem);
+    else
+      nhwc_pack_unit<DT>(b, u - na, pk_smem);
   }
 }
 
@@ -472,11 +391,6 @@ cudaError_t launch_wgrad_mn(const WgradMnPlan& p, int grid, cudaStream_t st) {
   if (e != cudaSuccess) return e;
   wgrad_mn_kernel<<<grid, kMnThreads, smem, st>>>(p);
   return cudaGetLastError();
-}
-
-// Shared memory of a pack unit: CHUNK staged channel runs of ch_pitch elements.
-size_t nhwc_pack_smem_bytes(const NhwcPackPlan& q, int dt) {
-  return (size_t)(dt == 0 ? 4 : 8) * q.ch_pitch * (dt == 0 ? 4 : 2);
 }
 
 // Packs a and (if b.src is not NULL) b in one launch.

@@ -84,40 +84,45 @@ void check_pack_as_kernel(const char* nm, const char* op, const NhwcPackPlan& q)
   const long long src_elems = (long long)(q.N - 1) * q.src_nstride + (long long)q.C * HW;
   const long long groups = (long long)q.npl * q.nchunk * q.N * q.EX * q.WL;
   if (src_elems > (1ll << 22) || groups > (1ll << 22)) return;
-  if (q.units != (unsigned)((long long)q.N * q.nchunk * q.n_etiles) || q.te < 1 ||
-      (long long)q.te * q.n_etiles < q.EX || (long long)q.te * (q.n_etiles - 1) >= q.EX)
-    fail(nm, op, "pack units do not tile the padded rows");
+  if (q.units != (unsigned)((long long)q.N * q.ngroups * q.n_etiles) || q.te < 1 ||
+      (long long)q.te * q.n_etiles < q.EX || (long long)q.te * (q.n_etiles - 1) >= q.EX || q.cg < 1 ||
+      (long long)q.cg * q.ngroups < q.nchunk || (long long)q.cg * (q.ngroups - 1) >= q.nchunk)
+    fail(nm, op, "pack units do not tile the padded rows and chunks");
   std::vector<E> src((size_t)src_elems);
   for (size_t i = 0; i < src.size(); ++i) src[i] = (E)(i * 2654435761u + 1u);
   std::vector<E> dst((size_t)groups * CHUNK, (E)0);
   std::vector<int> wrote((size_t)groups, 0);
-  std::vector<E> sm((size_t)CHUNK * q.ch_pitch);
+  std::vector<E> sm((size_t)q.cg * CHUNK * q.ch_pitch);
   for (unsigned v = 0; v < q.units; ++v) {
     const int r = (int)(v / (unsigned)q.n_etiles), et = (int)(v % (unsigned)q.n_etiles);
-    const int n = r / q.nchunk, cc = r % q.nchunk;
+    const int n = r / q.ngroups, cc0 = (r % q.ngroups) * q.cg, ncc = std::min(q.cg, q.nchunk - cc0);
     const int e0 = et * q.te, ne = std::min(q.te, q.EX - e0);
     const int h_lo = e0 * q.step_h + q.off_h_min, h_hi = (e0 + ne - 1) * q.step_h + q.off_h_min + q.h_span;
     const int hl = std::max(h_lo, 0), hh = std::min(h_hi, q.H - 1), nr = hh - hl + 1;
-    const int nch = std::min(CHUNK, q.C - CHUNK * cc);
+    const int nchs = std::min(ncc * CHUNK, q.C - CHUNK * cc0);
     if (nr > 0) {
       if ((long long)nr * q.W > q.ch_pitch) {
         fail(nm, op, "pack unit stages more rows than its channel pitch holds");
         return;
       }
-      for (int c = 0; c < nch; ++c)
+      for (int c = 0; c < nchs; ++c)
         for (long long k = 0; k < (long long)nr * q.W; ++k)
-          sm[(size_t)c * q.ch_pitch + k] = src[(size_t)(n * q.src_nstride + (long long)(CHUNK * cc + c) * HW + (long long)hl * q.W + k)];
+          sm[(size_t)c * q.ch_pitch + k] =
+              src[(size_t)(n * q.src_nstride + (long long)(CHUNK * cc0 + c) * HW + (long long)hl * q.W + k)];
     }
-    for (int pl = 0; pl < q.npl; ++pl)
-      for (int i = 0; i < ne * q.WL; ++i) {
-        const int de = i / q.WL, f = i % q.WL;
-        const int h = (e0 + de) * q.step_h + q.off_h[pl], w = f * q.step_w + q.off_w[pl];
-        const long long g = (((long long)pl * q.nchunk + cc) * q.N + n) * q.EX * q.WL + (long long)e0 * q.WL + i;
-        ++wrote[(size_t)g];
-        for (int c = 0; c < CHUNK; ++c)
-          dst[(size_t)g * CHUNK + c] =
-              (h >= hl && h <= hh && w >= 0 && w < q.W && c < nch) ? sm[(size_t)c * q.ch_pitch + (size_t)(h - hl) * q.W + w] : (E)0;
-      }
+    for (int ccl = 0; ccl < ncc; ++ccl)
+      for (int pl = 0; pl < q.npl; ++pl)
+        for (int i = 0; i < ne * q.WL; ++i) {
+          const int de = i / q.WL, f = i % q.WL;
+          const int h = (e0 + de) * q.step_h + q.off_h[pl], w = f * q.step_w + q.off_w[pl];
+          const int nch = std::min(CHUNK, nchs - ccl * CHUNK);
+          const long long g = (((long long)pl * q.nchunk + cc0 + ccl) * q.N + n) * q.EX * q.WL + (long long)e0 * q.WL + i;
+          ++wrote[(size_t)g];
+          for (int c = 0; c < CHUNK; ++c)
+            dst[(size_t)g * CHUNK + c] = (h >= hl && h <= hh && w >= 0 && w < q.W && c < nch)
+                                             ? sm[(size_t)(ccl * CHUNK + c) * q.ch_pitch + (size_t)(h - hl) * q.W + w]
+                                             : (E)0;
+        }
   }
   for (int pl = 0; pl < q.npl; ++pl)
     for (int cc = 0; cc < q.nchunk; ++cc)
