@@ -21,7 +21,7 @@ cudaError_t launch_pack_filter(const PackPlan& pp, int dt, cudaStream_t st);
 size_t tap_gemm_smem_bytes(const TapPlan& p);
 cudaError_t launch_wgrad(const WgradPlan& p, int dt, int grid, cudaStream_t st);
 cudaError_t launch_wgrad_reduce(const ReducePlan& rp, int dt, int num_sms, cudaStream_t st);
-cudaError_t launch_chan_sum(const ChanSumPlan& cp, int dt, cudaStream_t st);
+cudaError_t launch_chan_sum(const ChanSumPlan& a, const ChanSumPlan& b, int dt, cudaStream_t st);
 cudaError_t launch_space_to_depth(const S2dPlan& sp, int dt, cudaStream_t st);
 size_t wgrad_smem_bytes(const WgradPlan& p, int dt);
 cudaError_t launch_wgrad_mn(const WgradMnPlan& p, int grid, cudaStream_t st);
@@ -446,6 +446,7 @@ int build_fwd_impl(const Desc& d0, const void* x, const void* w, void* y, void* 
   if (!p.a_tma) b.src_pack_bytes = 0;
   p.wpack = ws;
   fill_pack(b, d, w, ws, 0, tr, ts);
+  if (b.pack_bytes / 16 >= (size_t(1) << 31)) return CONV2D_ERR_TOO_LARGE;  // 32-bit chunk indices
   b.grid = (int)std::min<long long>(p.total_tiles, di.sms);
   return CONV2D_OK;
 }
@@ -576,6 +577,7 @@ int build_bwd_data_impl(const Desc& d0, const void* dy, const void* w, void* dx,
   p.wpack = ws;
   fill_pack(b, d, w, ws, 1, tr, ts);
   if (p.ntaps_total == 0) b.pack_bytes = 0;
+  if (b.pack_bytes / 16 >= (size_t(1) << 31)) return CONV2D_ERR_TOO_LARGE;  // 32-bit chunk indices
   b.grid = (int)std::min<long long>(p.total_tiles, di.sms);
   return CONV2D_OK;
 }
@@ -1335,6 +1337,20 @@ int check_ptrs(const void* a, const void* b, const void* c, int dt) {
 // Workspace of the bias-gradient sums of conv2d_bwd_filter_ex: fp32 partials per (channel,
 // image) for the K sums over dy and the C sums over x, each region 256-byte aligned.
 size_t align_ws(size_t b) { return (b + 255) & ~size_t(255); }
+
+// Images per block of a channel sum: enough that a block reads about 64 KB (at least one
+// image), fewer while the blocks would number under four per SM.  The partials (Ch * nblk
+// floats) fit the Ch * N floats the workspace holds for them; a block's 16-byte groups stay
+// within 32-bit counts.
+void chan_sum_blocks(ChanSumPlan& cp, int dt) {
+  const long long img = cp.HW * (dt == 0 ? 4 : 2);
+  int ipb = (int)std::max<long long>(1, std::min<long long>(cp.N, (64 * 1024) / std::max<long long>(img, 1)));
+  while (ipb > 1 && (long long)ipb * img / 16 >= (1ll << 31)) --ipb;
+  while (ipb > 1 && (long long)cp.Ch * ((cp.N + ipb - 1) / ipb) < 4 * 152) ipb = (ipb + 1) / 2;
+  cp.ipb = ipb;
+  cp.nblk = (cp.N + ipb - 1) / ipb;
+}
+
 size_t chan_sum_bytes(const Desc& d) {  // the sums cover all d.g groups' channels
   return align_ws((size_t)d.g * d.K * d.N * sizeof(float)) + align_ws((size_t)d.g * d.C * d.N * sizeof(float));
 }
@@ -1855,19 +1871,22 @@ int conv2d_bwd_filter_ex(int N, int C, int H, int W, int K, int R, int S, int pa
     rc = launch_err(launch_wgrad_reduce(b.rp, d.dt, di.sms, st));
     if (rc) return rc;
   }
+  // Bias gradients, both in one launch pair: the conv bias gradient db_k sums dy over images
+  // and output pixels per output channel k; the deconvolution bias gradient db_c sums x (the
+  // deconvolution's output gradient) over images and pixels per channel c.
   uint8_t* wsb = static_cast<uint8_t*>(workspace) + sum0;
+  ChanSumPlan sk{}, sc{};
   if (db_k != nullptr) {
-    // conv bias gradient: sum of dy over images and output pixels, per output channel k
-    const ChanSumPlan cp{dy, db_k, reinterpret_cast<float*>(wsb), d.N, d.K, (long long)d.P * d.Q, beta};
-    rc = launch_err(launch_chan_sum(cp, d.dt, st), 2);
-    if (rc) return rc;
+    sk = ChanSumPlan{dy, db_k, reinterpret_cast<float*>(wsb), d.N, d.K, (long long)d.P * d.Q, beta, 0, 0};
+    chan_sum_blocks(sk, d.dt);
   }
   if (db_c != nullptr) {
-    // deconvolution bias gradient: sum of x (the deconvolution's output gradient) over images
-    // and pixels, per channel c
-    const ChanSumPlan cp{x, db_c, reinterpret_cast<float*>(wsb + align_ws((size_t)d.K * d.N * sizeof(float))), d.N,
-                         d.C, (long long)d.H * d.W, beta};
-    rc = launch_err(launch_chan_sum(cp, d.dt, st), 2);
+    sc = ChanSumPlan{x, db_c, reinterpret_cast<float*>(wsb + align_ws((size_t)d.K * d.N * sizeof(float))), d.N, d.C,
+                     (long long)d.H * d.W, beta, 0, 0};
+    chan_sum_blocks(sc, d.dt);
+  }
+  if (sums) {
+    rc = launch_err(launch_chan_sum(db_k != nullptr ? sk : sc, db_k != nullptr ? sc : ChanSumPlan{}, d.dt, st), 2);
     if (rc) return rc;
   }
   return CONV2D_OK;

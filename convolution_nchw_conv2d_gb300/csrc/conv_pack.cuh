@@ -116,21 +116,23 @@ __device__ __forceinline__ void nhwc_pack_unit(const NhwcPackPlan& p, uint32_t v
 // filter row -- adjacent addresses of the KCRS filter -- and are coalesced; the 16-byte chunk
 // stores are spread (one per tap slice) and merge in L2.
 template <int DT>
-__device__ __forceinline__ void pack_filter_one(const PackPlan& pp, long long idx) {
+__device__ __forceinline__ void pack_filter_one(const PackPlan& pp, uint32_t idx) {
   constexpr int ESZ = DT == 0 ? 4 : 2;
   constexpr int CHUNK = 16 / ESZ;
   using E = typename std::conditional<DT == 0, uint32_t, uint16_t>::type;
-  const int NCH = pp.CB / CHUNK;
+  const uint32_t NCH = (uint32_t)(pp.CB / CHUNK);
   const int RS = pp.R * pp.S;
-  long long rest = idx;
-  const int t = (int)(rest % pp.ntaps_total);
-  rest /= pp.ntaps_total;
-  const int n = (int)(rest % pp.NT);
-  rest /= pp.NT;
+  // 32-bit index arithmetic: the packed filter has fewer than 2^31 chunks (the planner keeps
+  // it within its workspace cap)
+  uint32_t rest = idx;
+  const int t = (int)(rest % (uint32_t)pp.ntaps_total);
+  rest /= (uint32_t)pp.ntaps_total;
+  const int n = (int)(rest % (uint32_t)pp.NT);
+  rest /= (uint32_t)pp.NT;
   const int j = (int)(rest % NCH);
   rest /= NCH;
-  const int kb = (int)(rest % pp.nkb);
-  const int nt = (int)(rest / pp.nkb);
+  const int kb = (int)(rest % (uint32_t)pp.nkb);
+  const int nt = (int)(rest / (uint32_t)pp.nkb);
   const int nn = nt * pp.NT + n;
   int r = pp.tap_r[t], s = pp.tap_s[t];
   if (pp.flip && r >= 0) {  // convolution mode: the filter rotated by 180 degrees

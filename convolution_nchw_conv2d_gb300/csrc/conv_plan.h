@@ -305,10 +305,11 @@ struct S2dPlan {
 struct ChanSumPlan {
   const void* t;
   void* out;
-  float* part;           // Ch * N fp32 (workspace)
+  float* part;           // Ch * nblk fp32 (workspace)
   int N, Ch;
   long long HW;
   float beta;
+  int ipb, nblk;         // images per block; blocks per channel = ceil(N / ipb)
 };
 
 }  // namespace cg3

@@ -73,6 +73,25 @@ __device__ __forceinline__ float load_elem(const void* base, long long idx) {
     return __bfloat162float(static_cast<const __nv_bfloat16*>(base)[idx]);
 }
 
+// Fused epilogue of 16 output channels (the first `lim` of them exist) at one output position,
+// with the old values and the channels' bias values (zero without bias) already read:
+// D + bias (+ beta * old), in fp32, then stored (bf16: rounded to nearest even).
+template <int DT>
+__device__ __forceinline__ void store16_epi(const TapPlan& p, long long ob, long long ostep, int lim,
+                                            const uint32_t (&r)[16], const float (&old)[16], const float (&bv)[16]) {
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    if (j < lim) {
+      float v = __uint_as_float(r[j]) + bv[j];
+      if (p.beta != 0.f) v += p.beta * old[j];
+      if constexpr (DT == 0)
+        static_cast<float*>(p.dst)[ob + j * ostep] = v;
+      else
+        static_cast<__nv_bfloat16*>(p.dst)[ob + j * ostep] = __float2bfloat16_rn(v);
+    }
+  }
+}
+
 // Epilogue of 16 output channels ch0 .. ch0 + 15 (the first `lim` of them exist) at one output
 // position: D (+ bias of the channel) (+ beta * the old value), in fp32, then stored (bf16:
 // rounded to nearest even).  The old values are all read before the first store, so their
@@ -280,6 +299,28 @@ __global__ void __launch_bounds__(kThreads, 1) tap_gemm_kernel(const __grid_cons
       const TileCoord tc = decode_tile(p, t);
       const int ntaps = p.ph_ntaps[tc.ph];
       const long long m0 = (long long)tc.mt * MT;
+      if constexpr (EPI) {
+        // Add-to: while the tile's accumulator is computed, pull the old output values of
+        // this lane's rows into L2 (the epilogue's reads of them then wait on L2, not DRAM).
+        if (p.beta != 0.f) {
+          const int nb = tc.nt * p.NT;
+          const int nv = min(p.NT, p.Cd - nb);
+          for (int h = 0; h < p.MH; ++h) {
+            const long long L = m0 + h * 128 + q * 32 + lane;
+            if (L >= p.Mtot) continue;
+            const uint32_t n = fdiv((uint32_t)L, p.fd_img);
+            const uint32_t rem = (uint32_t)L - n * p.fd_img.d;
+            const int e = (int)fdiv(rem, p.fd_WL);
+            const int f = (int)rem - e * p.WL;
+            const int oh = e * p.ph_step_h + p.ph_off_h[tc.ph];
+            const int ow = f * p.ph_step_w + p.ph_off_w[tc.ph];
+            if (oh < 0 || oh >= p.Hd || ow < 0 || ow >= p.Wd) continue;
+            const char* o = static_cast<const char*>(p.dst) +
+                            ((long long)n * p.dst_nstride + (long long)nb * HdWd + (long long)oh * p.Wd + ow) * (DT == 0 ? 4 : 2);
+            for (int j = 0; j < nv; ++j) prefetch_l2(o + (long long)j * HdWd * (DT == 0 ? 4 : 2));
+          }
+        }
+      }
       if (ntaps != 0) {
         if (!mbar_wait(bar_at(accf, acc), aphase, abort_flag, &g_tap_err)) break;
         tc_fence_after();
@@ -313,6 +354,53 @@ __global__ void __launch_bounds__(kThreads, 1) tap_gemm_kernel(const __grid_cons
           for (int j = 0; j < 16; ++j) ra[j] = rb[j] = 0u;
         }
         const long long ostep = HdWd;
+        if constexpr (EPI) {
+          // Fused epilogue: the old values of up to EG = 2 16-channel chunks are all read before
+          // the first of them is used (32 loads in flight per lane: the reads of the old output
+          // are latency-bound otherwise), and so are the chunks' bias values, one per lane
+          // (lane j holds channel j of a chunk; the warp broadcasts them with shuffles, so no
+          // bias read waits behind an output store); then each chunk's accumulator columns are
+          // loaded from TMEM, combined and stored.
+          constexpr int EG = 2;
+          for (int c0 = 0; c0 < nchunk; c0 += EG) {
+            float old[EG][16], bsel[EG];
+#pragma unroll
+            for (int g = 0; g < EG; ++g) {
+              const int ch = nbase + 16 * (c0 + g) + (lane & 15);
+              bsel[g] = (p.bias != nullptr && 16 * (c0 + g) + (lane & 15) < nvalid) ? load_elem<DT>(p.bias, ch) : 0.f;
+#pragma unroll
+              for (int j = 0; j < 16; ++j) old[g][j] = 0.f;
+            }
+            if (valid && p.beta != 0.f) {
+#pragma unroll
+              for (int g = 0; g < EG; ++g) {
+                const int ci = c0 + g;
+                const long long ob = obase + (long long)(nbase + 16 * ci) * ostep;
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                  if (ci < nchunk && 16 * ci + j < nvalid) old[g][j] = load_elem<DT>(p.dst, ob + j * ostep);
+              }
+            }
+#pragma unroll
+            for (int g = 0; g < EG; ++g) {
+              const int ci = c0 + g;
+              if (ci >= nchunk) break;
+              if (ntaps != 0 && ci > 0) {
+                tmem_ld16(tcol + (uint32_t)(16 * ci), ra);
+                tmem_ld_wait();
+              }
+              float bv[16];  // the chunk's bias values in every lane (all lanes shuffle)
+#pragma unroll
+              for (int j = 0; j < 16; ++j) bv[j] = __shfl_sync(0xffffffffu, bsel[g], j);
+              if (valid) {
+                const long long ob = obase + (long long)(nbase + 16 * ci) * ostep;
+                const int lim = nvalid - 16 * ci;
+                store16_epi<DT>(p, ob, ostep, lim < 16 ? lim : 16, ra, old[g], bv);
+              }
+            }
+          }
+          continue;
+        }
         for (int ci = 0; ci < nchunk; ci += 2) {
           const bool two = ci + 1 < nchunk;
           if (ntaps != 0 && two) tmem_ld16(tcol + (uint32_t)(16 * (ci + 1)), rb);
@@ -424,9 +512,8 @@ template <int DT>
 __global__ void __launch_bounds__(256) pack_filter_kernel(const __grid_constant__ PackPlan pp) {
   griddep_launch_dependents();  // the GEMM may start; it waits for this grid before reading wpack
   const int NCH = pp.CB / (DT == 0 ? 4 : 8);
-  const long long total = (long long)pp.n_ntiles * pp.nkb * NCH * pp.NT * pp.ntaps_total;
-  for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < total;
-       idx += (long long)gridDim.x * blockDim.x)
+  const uint32_t total = (uint32_t)pp.n_ntiles * pp.nkb * NCH * pp.NT * pp.ntaps_total;
+  for (uint32_t idx = blockIdx.x * blockDim.x + threadIdx.x; idx < total; idx += gridDim.x * blockDim.x)
     pack_filter_one<DT>(pp, idx);
 }
 
@@ -442,9 +529,9 @@ __global__ void __launch_bounds__(256) tap_packs_kernel(const __grid_constant__ 
     for (uint32_t u = blockIdx.x; u < px.units; u += xblocks) nhwc_pack_unit<DT>(px, u, pk_smem);
   } else {
     const int NCH = pp.CB / (DT == 0 ? 4 : 8);
-    const long long total = (long long)pp.n_ntiles * pp.nkb * NCH * pp.NT * pp.ntaps_total;
-    const long long nthr = (long long)(gridDim.x - xblocks) * blockDim.x;
-    for (long long idx = (blockIdx.x - xblocks) * (long long)blockDim.x + threadIdx.x; idx < total; idx += nthr)
+    const uint32_t total = (uint32_t)pp.n_ntiles * pp.nkb * NCH * pp.NT * pp.ntaps_total;
+    const uint32_t nthr = (gridDim.x - xblocks) * blockDim.x;
+    for (uint32_t idx = (blockIdx.x - xblocks) * blockDim.x + threadIdx.x; idx < total; idx += nthr)
       pack_filter_one<DT>(pp, idx);
   }
 }

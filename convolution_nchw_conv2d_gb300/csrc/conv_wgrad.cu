@@ -1088,45 +1088,74 @@ __global__ void __launch_bounds__(32 * kReduceWarps) wgrad_reduce_kernel(const _
   }
 }
 
-// Per-channel sums (bias gradients).  Block (ch, n) adds t[n, ch, 0 .. HW) -- thread i takes
-// 16-byte groups i, i + 256, ... in order (elements i, i + 256, ... when HW is not a multiple
-// of a group), then the 256 thread sums are added by a fixed tree -- into part[ch * N + n];
-// the final pass adds the N partials of a channel in order.  (A bf16 value is the high half
-// of the fp32 with the same bits.)
+// Per-channel sums (bias gradients) of up to two tensors in one launch (plan `a`, then plan `b`
+// when b.t is not NULL).  Block (ch, j) of a plan adds t[n, ch, 0 .. HW) for the images
+// n = j*ipb .. j*ipb + ipb - 1: thread i takes the blocks' 16-byte groups i, i + 256, ... in
+// order, eight reads in flight (elements instead of groups when HW is not a multiple of a group
+// or the tensor is not 16-byte aligned); the 256 thread sums are added by a fixed tree into
+// part[ch * nblk + j].  The final pass adds a channel's nblk partials in order, so the sums are
+// the same on every run.  (A bf16 value is the high half of the fp32 with the same bits.)
 constexpr int kSumThreads = 256;
+
 template <int DT>
-__global__ void __launch_bounds__(kSumThreads) chan_sum_partial_kernel(const __grid_constant__ ChanSumPlan cp) {
+__device__ __forceinline__ float sum_group(const uint4& u) {
+  const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
+  float acc = 0.f;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    if constexpr (DT == 0) {
+      acc += __uint_as_float(wv[e]);
+    } else {
+      acc += __uint_as_float(wv[e] << 16);
+      acc += __uint_as_float(wv[e] & 0xffff0000u);
+    }
+  }
+  return acc;
+}
+
+template <int DT>
+__global__ void __launch_bounds__(kSumThreads) chan_sum_partial_kernel(const __grid_constant__ ChanSumPlan a,
+                                                                       const __grid_constant__ ChanSumPlan b) {
   __shared__ float red[kSumThreads];
-  const long long b = blockIdx.x;
-  const int n = (int)(b % cp.N);
-  const int ch = (int)(b / cp.N);
-  const long long base = ((long long)n * cp.Ch + ch) * cp.HW;
+  const long long na = (long long)a.Ch * a.nblk;
+  const bool first = blockIdx.x < na;
+  const ChanSumPlan& cp = first ? a : b;
+  const long long bi = first ? blockIdx.x : blockIdx.x - na;
+  const int j = (int)(bi % cp.nblk);
+  const int ch = (int)(bi / cp.nblk);
+  const int n0 = j * cp.ipb, n1 = min(cp.N, n0 + cp.ipb);
   float acc = 0.f;
   constexpr int VE = DT == 0 ? 4 : 8;  // elements per 16-byte read
   const bool vec = (cp.HW % VE) == 0 && (reinterpret_cast<uintptr_t>(cp.t) & 15) == 0;
   if (vec) {
-    // 16-byte reads: thread i adds groups i, i + 256, ... (each group's elements in order)
-    const uint4* src = reinterpret_cast<const uint4*>(static_cast<const char*>(cp.t) + base * (16 / VE));
-    const long long ng = cp.HW / VE;
-    for (long long gi = threadIdx.x; gi < ng; gi += kSumThreads) {
-      const uint4 u = __ldg(src + gi);
-      const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
+    // 32-bit group indices within the block (a block reads at most a few hundred KB)
+    const uint32_t ng = (uint32_t)(cp.HW / VE);  // groups per image
+    const uint32_t tot = ng * (uint32_t)(n1 - n0);
+    const uint4* src = reinterpret_cast<const uint4*>(cp.t) + (((long long)n0 * cp.Ch + ch) * cp.HW) / VE;
+    const long long istride = (long long)cp.Ch * cp.HW / VE;  // groups from one image to the next
+    for (uint32_t g0 = threadIdx.x; g0 < tot; g0 += 8 * kSumThreads) {
+      uint4 u[8];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        if constexpr (DT == 0) {
-          acc += __uint_as_float(wv[e]);
-        } else {
-          acc += __uint_as_float(wv[e] << 16);
-          acc += __uint_as_float(wv[e] & 0xffff0000u);
+      for (int q = 0; q < 8; ++q) {
+        const uint32_t g = g0 + (uint32_t)q * kSumThreads;
+        u[q] = make_uint4(0u, 0u, 0u, 0u);
+        if (g < tot) {
+          const uint32_t n = g / ng;
+          u[q] = __ldg(src + n * istride + (g - n * ng));
         }
       }
+#pragma unroll
+      for (int q = 0; q < 8; ++q) acc += sum_group<DT>(u[q]);
     }
   } else {
-    for (long long i = threadIdx.x; i < cp.HW; i += kSumThreads) {
+    const long long tot = cp.HW * (n1 - n0);
+    for (long long i = threadIdx.x; i < tot; i += kSumThreads) {
+      const long long n = n0 + i / cp.HW, k = i % cp.HW;
+      const long long o = (n * cp.Ch + ch) * cp.HW + k;
       if constexpr (DT == 0)
-        acc += static_cast<const float*>(cp.t)[base + i];
+        acc += static_cast<const float*>(cp.t)[o];
       else
-        acc += __bfloat162float(static_cast<const __nv_bfloat16*>(cp.t)[base + i]);
+        acc += __bfloat162float(static_cast<const __nv_bfloat16*>(cp.t)[o]);
     }
   }
   red[threadIdx.x] = acc;
@@ -1135,15 +1164,19 @@ __global__ void __launch_bounds__(kSumThreads) chan_sum_partial_kernel(const __g
     if ((int)threadIdx.x < h) red[threadIdx.x] += red[threadIdx.x + h];
     __syncthreads();
   }
-  if (threadIdx.x == 0) cp.part[(long long)ch * cp.N + n] = red[0];
+  if (threadIdx.x == 0) cp.part[(long long)ch * cp.nblk + j] = red[0];
 }
 
 template <int DT>
-__global__ void __launch_bounds__(kSumThreads) chan_sum_final_kernel(const __grid_constant__ ChanSumPlan cp) {
-  const int ch = blockIdx.x * kSumThreads + threadIdx.x;
-  if (ch >= cp.Ch) return;
+__global__ void __launch_bounds__(kSumThreads) chan_sum_final_kernel(const __grid_constant__ ChanSumPlan a,
+                                                                     const __grid_constant__ ChanSumPlan b) {
+  const int i = blockIdx.x * kSumThreads + threadIdx.x;
+  const bool first = i < a.Ch;
+  const ChanSumPlan& cp = first ? a : b;
+  const int ch = first ? i : i - a.Ch;
+  if (ch >= cp.Ch || cp.t == nullptr) return;
   float sum = 0.f;
-  for (int n = 0; n < cp.N; ++n) sum += cp.part[(long long)ch * cp.N + n];
+  for (int j = 0; j < cp.nblk; ++j) sum += cp.part[(long long)ch * cp.nblk + j];
   if constexpr (DT == 0) {
     float* o = static_cast<float*>(cp.out);
     if (cp.beta != 0.f) sum += cp.beta * o[ch];
@@ -1155,15 +1188,17 @@ __global__ void __launch_bounds__(kSumThreads) chan_sum_final_kernel(const __gri
   }
 }
 
-cudaError_t launch_chan_sum(const ChanSumPlan& cp, int dt, cudaStream_t st) {
-  const unsigned blocks = (unsigned)((long long)cp.Ch * cp.N);
-  const unsigned fblocks = (unsigned)((cp.Ch + kSumThreads - 1) / kSumThreads);
+// Sums of a and (b.t not NULL) b; ipb and nblk are set by chan_sum_blocks.
+cudaError_t launch_chan_sum(const ChanSumPlan& a, const ChanSumPlan& b, int dt, cudaStream_t st) {
+  const long long blocks = (long long)a.Ch * a.nblk + (b.t != nullptr ? (long long)b.Ch * b.nblk : 0ll);
+  const long long chs = (long long)a.Ch + (b.t != nullptr ? b.Ch : 0);
+  const unsigned fblocks = (unsigned)((chs + kSumThreads - 1) / kSumThreads);
   if (dt == 0) {
-    chan_sum_partial_kernel<0><<<blocks, kSumThreads, 0, st>>>(cp);
-    chan_sum_final_kernel<0><<<fblocks, kSumThreads, 0, st>>>(cp);
+    chan_sum_partial_kernel<0><<<(unsigned)blocks, kSumThreads, 0, st>>>(a, b);
+    chan_sum_final_kernel<0><<<fblocks, kSumThreads, 0, st>>>(a, b);
   } else {
-    chan_sum_partial_kernel<1><<<blocks, kSumThreads, 0, st>>>(cp);
-    chan_sum_final_kernel<1><<<fblocks, kSumThreads, 0, st>>>(cp);
+    chan_sum_partial_kernel<1><<<(unsigned)blocks, kSumThreads, 0, st>>>(a, b);
+    chan_sum_final_kernel<1><<<fblocks, kSumThreads, 0, st>>>(a, b);
   }
   return cudaGetLastError();
 }

@@ -166,6 +166,11 @@ __device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src, bool v
                "r"(valid ? 4 : 0)
                : "memory");
 }
+// Prefetch the line holding a global address into L2 (no register result, no wait).
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 // 16-byte async copy global -> shared with zero fill beyond src_bytes (0..16); both
 // addresses 16-byte aligned.
 __device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, int src_bytes) {
