@@ -170,12 +170,13 @@ void fill_tap_offsets(TapPlan& p, int NCH) {
   for (int ph = 0; ph < p.nph; ++ph)
     for (int i = 0; i < p.ph_ntaps[ph]; ++i) {
       const int t = p.ph_tap_begin[ph] + i;
-      const int oa = p.tap_plane[t] * NCH * p.rows + p.tap_off[t];
+      const int spl = p.plane_per_phase ? 0 : p.tap_plane[t];  // plane within the stage
+      const int oa = spl * NCH * p.rows + p.tap_off[t];
       if (NCH >= 2) {
         p.tap_a[t] = oa;
         p.tap_b[t] = i * NCH * p.NT;
       } else if ((i & 1) == 0) {
-        const int ob = p.tap_plane[t + 1] * p.rows + p.tap_off[t + 1];
+        const int ob = (p.plane_per_phase ? 0 : p.tap_plane[t + 1]) * p.rows + p.tap_off[t + 1];
         p.tap_a[t] = (int)((uint32_t)oa | ((uint32_t)(ob - oa) << 16));
         p.tap_b[t] = i * p.NT;
       } else {
@@ -237,7 +238,7 @@ bool choose_tap_tiles(TapPlan& p, int max_off, int dt, const DevInfo& di, bool p
         }
         rows = nbox * box;
         if (a_tma && 2 * (p.Mtot + rows) >= (1ll << 31)) return false;  // 32-bit copy coordinates
-        const long long a_bytes = (long long)p.npl * NCH * rows * 16;
+        const long long a_bytes = (long long)(p.plane_per_phase ? 1 : p.npl) * NCH * rows * 16;
         const long long b_bytes = (long long)p.max_taps_ph * NCH * NT * 16;
         const long long fixed = 8 * (3 * 4 + 6) + 24 + 4 * 4 + 1024;
         const long long per = a_bytes + b_bytes;
@@ -495,6 +496,74 @@ int build_bwd_data_impl(const Desc& d0, const void* dy, const void* w, void* dx,
   std::vector<std::vector<int>> tapsh, tapsw;
   phase_dims(d.H, d.ph, d.R, d.dh, d.sh, Th, uloh, Uh, tapsh);
   phase_dims(d.W, d.pw, d.S, d.dw, d.sw, Tw, ulow, Uw, tapsw);
+  const int CHUNK = d.dt == 0 ? 4 : 8;
+  // With the source packed for tensor copies (whole filter in one pass), every phase reads its
+  // own dy plane: phase (a, c) at linear (e, f) reads plane row e + Th[a]-1 - t_r, column
+  // f + Tw[c]-1 - t_s, its plane starting at dy row ulo_a - (Th[a]-1) and column
+  // ulo_c - (Tw[c]-1).  The linear space then needs only U + T - 1 rows (columns) per phase
+  // instead of the span of all phases' windows in one shared plane, so fewer position tiles;
+  // the pack writes one plane per phase.
+  if (packed_src && u_lo == 0 && u_hi >= d.R * d.S && d.sh * d.sw > 1) {
+    int EL = 1, WL = 1;
+    for (int a = 0; a < d.sh; ++a) EL = std::max(EL, Uh[a] + std::max(Th[a], 1) - 1);
+    for (int c = 0; c < d.sw; ++c) WL = std::max(WL, Uw[c] + std::max(Tw[c], 1) - 1);
+    TapPlan q = p;
+    q.WL = WL;
+    q.EL = EL;
+    q.Mtot = (long long)d.N * EL * WL;
+    if (q.Mtot < (1ll << 31)) {
+      q.fd_img = make_fastdiv((uint32_t)(EL * WL));
+      q.fd_WL = make_fastdiv((uint32_t)WL);
+      q.nph = q.npl = d.sh * d.sw;
+      q.plane_per_phase = 1;
+      q.pl_step_h = q.pl_step_w = 1;
+      q.ph_step_h = d.sh;
+      q.ph_step_w = d.sw;
+      std::vector<int> tpl, toff, tr, ts;
+      int max_taps = 0, max_off = 0;
+      for (int a = 0; a < d.sh; ++a)
+        for (int c = 0; c < d.sw; ++c) {
+          const int ph = a * d.sw + c;
+          q.pl_off_h[ph] = uloh[a] - (std::max(Th[a], 1) - 1);
+          q.pl_off_w[ph] = ulow[c] - (std::max(Tw[c], 1) - 1);
+          q.ph_off_h[ph] = d.sh * uloh[a] + a - d.ph;
+          q.ph_off_w[ph] = d.sw * ulow[c] + c - d.pw;
+          const int begin = (int)tpl.size();
+          q.ph_tap_begin[ph] = begin;
+          for (const int r : tapsh[a])
+            for (const int s2 : tapsw[c]) {
+              const int t = (r * d.dh - a) / d.sh, t2 = (s2 * d.dw - c) / d.sw;
+              tpl.push_back(ph);
+              toff.push_back((Th[a] - 1 - t) * WL + (Tw[c] - 1 - t2));
+              tr.push_back(r);
+              ts.push_back(s2);
+            }
+          if ((int)tpl.size() > begin) order_phase_taps(tpl, toff, tr, ts, begin, 1 << 20, pair);
+          q.ph_ntaps[ph] = (int)tpl.size() - begin;
+          max_taps = std::max(max_taps, q.ph_ntaps[ph]);
+        }
+      for (const int o : toff) max_off = std::max(max_off, o);
+      q.ntaps_total = (int)tpl.size();
+      q.max_taps_ph = std::max(1, max_taps);
+      if (q.ntaps_total > 0 && q.ntaps_total <= kMaxTaps) {
+        for (int t = 0; t < q.ntaps_total; ++t) {
+          q.tap_plane[t] = tpl[t];
+          q.tap_off[t] = toff[t];
+        }
+        TapBuild bq = b;
+        bq.p = q;
+        if (packed_src_ok(bq, d.dt) && choose_tap_tiles(bq.p, max_off, d.dt, di, pair, true)) {
+          bq.p.wpack = ws;
+          fill_pack(bq, d, w, ws, 1, tr, ts);
+          if (bq.pack_bytes / 16 < (size_t(1) << 31)) {
+            bq.grid = (int)std::min<long long>(bq.p.total_tiles, di.sms);
+            b = bq;
+            return CONV2D_OK;
+          }
+        }
+      }
+    }
+  }
   int T0h = 0, T0w = 0;
   for (int a = 0; a < d.sh; ++a)
     if (Th[a] > 0) T0h = std::max(T0h, Th[a] - 1 - uloh[a]);
@@ -509,7 +578,6 @@ int build_bwd_data_impl(const Desc& d0, const void* dy, const void* w, void* dx,
     WL = std::max(WL, Uw[c]);
     if (Tw[c] > 0) WL = std::max(WL, Uw[c] + ulow[c] + T0w);
   }
-  const int CHUNK = d.dt == 0 ? 4 : 8;
   p.WL = WL;
   p.EL = EL;
   p.Mtot = (long long)d.N * EL * WL;
