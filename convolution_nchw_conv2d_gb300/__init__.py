@@ -49,7 +49,8 @@ def lib_path() -> str:
 
 EXPORTS = ("conv2d_output_dim", "conv2d_workspace_size", "conv2d_workspace_size_ex", "conv2d_fwd", "conv2d_bwd_data",
            "conv2d_bwd_filter", "conv2d_fwd_ex", "conv2d_bwd_data_ex", "conv2d_bwd_filter_ex",
-           "conv2d_fwd_noalloc", "conv2d_device_status", "conv2d_strerror", "conv2d_kernel_launches")
+           "conv2d_fwd_noalloc", "conv2d_device_status", "conv2d_strerror", "conv2d_kernel_launches",
+           "conv3d_workspace_size", "conv3d_fwd", "conv3d_bwd_data", "conv3d_bwd_filter")
 
 
 def load_library():
@@ -88,6 +89,13 @@ def load_library():
         lib.conv2d_kernel_launches.restype = ctypes.c_ulonglong
         lib.conv2d_strerror.argtypes = [i]
         lib.conv2d_strerror.restype = ctypes.c_char_p
+        ip = ctypes.POINTER(i)
+        lib.conv3d_workspace_size.argtypes = [i, ip, i, i, ctypes.POINTER(sz)]
+        lib.conv3d_workspace_size.restype = i
+        for name in ("conv3d_fwd", "conv3d_bwd_data", "conv3d_bwd_filter"):
+            f = getattr(lib, name)
+            f.argtypes = [ip, i, i, vp, vp, vp, vp, sz, vp]
+            f.restype = i
         _lib = lib
         return lib
 
@@ -367,3 +375,83 @@ def conv2d_device_status(stream=None) -> int:
     if rc:
         raise Conv2dError(rc, "conv2d_device_status")
     return 0
+
+
+# ---------------------------------------------------------------------------- 3-D (NCDHW)
+def _triple(v):
+    return (int(v),) * 3 if isinstance(v, int) else tuple(int(a) for a in v)
+
+
+def _dims3(N, C, dhw, K, trs, pad, stride, dilation):
+    pads, strides, dils = _triple(pad), _triple(stride), _triple(dilation)
+    out = [conv2d_output_dim(i_, p_, d_ * (k_ - 1) + 1, s_) for i_, p_, k_, s_, d_ in zip(dhw, pads, trs, strides, dils)]
+    return [N, C, *dhw, K, *trs, *pads, *strides, *dils, *out], tuple(out)
+
+
+def _call3(name, dims, groups, dt, a, b, out, workspace, op, stream):
+    import torch
+    arr = (ctypes.c_int * 21)(*dims)
+    need = ctypes.c_size_t(0)
+    rc = load_library().conv3d_workspace_size(op, arr, int(groups), dt, ctypes.byref(need))
+    if rc:
+        raise Conv2dError(rc, "conv3d_workspace_size")
+    if workspace is None:
+        workspace = torch.empty(max(need.value, 1), dtype=torch.uint8, device=out.device)
+    if workspace.numel() * workspace.element_size() < need.value:
+        raise ValueError(f"workspace too small: need {need.value} bytes")
+    rc = getattr(load_library(), name)(arr, int(groups), dt, _ptr(a), _ptr(b), _ptr(out), _ptr(workspace),
+                                       ctypes.c_size_t(workspace.numel() * workspace.element_size()),
+                                       _stream_ptr(stream))
+    if rc:
+        raise Conv2dError(rc, name)
+    return out
+
+
+def conv3d_fwd(x, w, pad=0, stride=1, dilation=1, groups=1, out=None, workspace=None, stream=None):
+    """y (N,K,Z,P,Q) = 3-D cross-correlation of x (N,C,D,H,W) with w (K,C/groups,T,R,S)."""
+    import torch
+    _check_tensor(x, "x")
+    _check_tensor(w, "w")
+    N, C = x.shape[:2]
+    K, Cg = w.shape[:2]
+    if Cg * groups != C or K % groups != 0 or w.dtype != x.dtype:
+        raise ValueError("x / w channel count, groups or dtype mismatch")
+    dims, zpq = _dims3(N, C, tuple(x.shape[2:]), K, tuple(w.shape[2:]), pad, stride, dilation)
+    if out is None:
+        out = torch.empty((N, K, *zpq), dtype=x.dtype, device=x.device)
+    return _call3("conv3d_fwd", dims, groups, _dtype_code(x), x, w, out, workspace, OP_FWD, stream)
+
+
+def conv3d_bwd_data(dy, w, x_dhw, pad=0, stride=1, dilation=1, groups=1, out=None, workspace=None, stream=None):
+    """dx (N,C,D,H,W) from dy (N,K,Z,P,Q) and w (K,C/groups,T,R,S); x_dhw = (D, H, W)."""
+    import torch
+    _check_tensor(dy, "dy")
+    _check_tensor(w, "w")
+    N, K = dy.shape[:2]
+    K2, Cg = w.shape[:2]
+    if K2 != K or K % groups != 0 or w.dtype != dy.dtype:
+        raise ValueError("dy / w channel count, groups or dtype mismatch")
+    C = Cg * groups
+    dims, zpq = _dims3(N, C, tuple(x_dhw), K, tuple(w.shape[2:]), pad, stride, dilation)
+    if tuple(dy.shape[2:]) != zpq:
+        raise ValueError("dy spatial shape does not match the descriptor")
+    if out is None:
+        out = torch.empty((N, C, *x_dhw), dtype=dy.dtype, device=dy.device)
+    return _call3("conv3d_bwd_data", dims, groups, _dtype_code(dy), dy, w, out, workspace, OP_BWD_DATA, stream)
+
+
+def conv3d_bwd_filter(x, dy, trs, pad=0, stride=1, dilation=1, groups=1, out=None, workspace=None, stream=None):
+    """dw (K,C/groups,T,R,S) from x (N,C,D,H,W) and dy (N,K,Z,P,Q); trs = (T, R, S)."""
+    import torch
+    _check_tensor(x, "x")
+    _check_tensor(dy, "dy")
+    N, C = x.shape[:2]
+    K = dy.shape[1]
+    if C % groups != 0 or K % groups != 0 or dy.dtype != x.dtype:
+        raise ValueError("x / dy channel count, groups or dtype mismatch")
+    dims, zpq = _dims3(N, C, tuple(x.shape[2:]), K, tuple(trs), pad, stride, dilation)
+    if tuple(dy.shape[2:]) != zpq:
+        raise ValueError("dy spatial shape does not match the descriptor")
+    if out is None:
+        out = torch.empty((K, C // groups, *trs), dtype=x.dtype, device=x.device)
+    return _call3("conv3d_bwd_filter", dims, groups, _dtype_code(x), x, dy, out, workspace, OP_BWD_FILTER, stream)

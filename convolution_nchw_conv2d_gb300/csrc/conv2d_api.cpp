@@ -1627,6 +1627,12 @@ size_t phase_need(const Desc& dg, const DevInfo& di) {
 
 }  // namespace
 
+namespace cg3 {
+// Status of a launch made by another file of the library (the 3-D layout copies), counted
+// like this file's launches.
+int count_launch(cudaError_t e, int kernels) { return launch_err(e, kernels); }
+}  // namespace cg3
+
 extern "C" {
 
 int conv2d_output_dim(int in, int pad, int k, int stride, int* out) {

@@ -202,6 +202,33 @@ int conv2d_bwd_filter_ex(int N, int C, int H, int W, int K, int R, int S,
                          const void *x, const void *dy, float beta, void *dw, void *db_k, void *db_c,
                          void *workspace, size_t workspace_bytes, void *stream);
 
+/* 3-D (NCDHW) cross-correlation, the same three operations one dimension up (page
+ * "mkldnn_deconvolution.cc": SupportMKLDNNDeconv accepts kernels of 1 to 3 spatial dimensions,
+ * DeconvDescCreator strides, pads and dilations of the same rank):
+ *
+ *   x  : N x C x D x H x W,  w : K x C/groups x T x R x S,  y : N x K x Z x P x Q
+ *   y[n,k,z,p,q] = sum_{c,t,r,s} X(n, c, z*stride_d - pad_d + t*dil_d,
+ *                                        p*stride_h - pad_h + r*dil_h, q*stride_w - pad_w + s*dil_w) * w[k,c,t,r,s]
+ *   (X zero outside the tensor; c over the input channels of k's group); backward-data and
+ *   backward-filter are its two gradients, as in 2-D.
+ *
+ * `dims` points to 21 host ints: N, C, D, H, W, K, T, R, S, pad_d, pad_h, pad_w, stride_d,
+ * stride_h, stride_w, dil_d, dil_h, dil_w, Z, P, Q (Z, P, Q by the dilated floor formula, else
+ * CONV2D_ERR_SHAPE).  groups >= 1 divides C and K.  Outputs are overwritten (beta = 0),
+ * cross-correlation.  Each op runs as one 2-D operation per depth tap t on a batch of the N*Z
+ * depth slices that tap reads (gathered into the workspace), so the 2-D limits apply to
+ * (R, S, strides, dilations) and the workspace (256-byte aligned) must hold
+ * conv3d_workspace_size() bytes: the gathered batches, one filter slice, for backward-data an
+ * fp32 dx accumulator, and the 2-D call's workspace.  bf16 forward outputs are rounded once per
+ * depth tap (the passes add onto the output); backward-data accumulates in fp32. */
+int conv3d_workspace_size(int op, const int *dims, int groups, int dtype, size_t *bytes);
+int conv3d_fwd(const int *dims, int groups, int dtype, const void *x, const void *w, void *y,
+               void *workspace, size_t workspace_bytes, void *stream);
+int conv3d_bwd_data(const int *dims, int groups, int dtype, const void *dy, const void *w, void *dx,
+                    void *workspace, size_t workspace_bytes, void *stream);
+int conv3d_bwd_filter(const int *dims, int groups, int dtype, const void *x, const void *dy, void *dw,
+                      void *workspace, size_t workspace_bytes, void *stream);
+
 /* Forward without any workspace argument, for callers that cannot allocate device
  * memory: for example code whose device memory is entirely owned by another runtime's
  * pool, or a latency-critical path that must never call cudaMalloc (which can

@@ -25,7 +25,7 @@ def cg():
 
 def _declared():
     text = open(HEADER).read()
-    return sorted(set(re.findall(r"^\s*(?:const\s+char\s*\*|int|unsigned\s+long\s+long)\s*(conv2d_\w+)\s*\(", text,
+    return sorted(set(re.findall(r"^\s*(?:const\s+char\s*\*|int|unsigned\s+long\s+long)\s*(conv[23]d_\w+)\s*\(", text,
                                  re.M)))
 
 
@@ -33,7 +33,8 @@ def test_header_declares_the_abi():
     names = _declared()
     for n in ("conv2d_fwd", "conv2d_bwd_data", "conv2d_bwd_filter", "conv2d_workspace_size",
               "conv2d_output_dim", "conv2d_strerror", "conv2d_device_status", "conv2d_fwd_noalloc",
-              "conv2d_kernel_launches"):
+              "conv2d_kernel_launches", "conv3d_workspace_size", "conv3d_fwd", "conv3d_bwd_data",
+              "conv3d_bwd_filter"):
         assert n in names
 
 

@@ -21,6 +21,9 @@ def _host_calls():
     x1 = torch.ones(1, 2, 5)
     w1 = torch.ones(3, 2, 3)
     dy1 = torch.ones(1, 3, 3)
+    x3 = torch.ones(1, 2, 4, 5, 5)
+    w3 = torch.ones(3, 2, 2, 3, 3)
+    dy3 = torch.ones(1, 3, 3, 3, 3)
     return {
         "conv2d_fwd": lambda: cg.conv2d_fwd(x, w),
         "conv2d_fwd_noalloc": lambda: cg.conv2d_fwd_noalloc(x, w),
@@ -30,6 +33,9 @@ def _host_calls():
         "conv1d_fwd": lambda: cg.conv1d_fwd(x1, w1),
         "conv1d_bwd_data": lambda: cg.conv1d_bwd_data(dy1, w1, 5),
         "conv1d_bwd_filter": lambda: cg.conv1d_bwd_filter(x1, dy1, 3),
+        "conv3d_fwd": lambda: cg.conv3d_fwd(x3, w3),
+        "conv3d_bwd_data": lambda: cg.conv3d_bwd_data(dy3, w3, (4, 5, 5)),
+        "conv3d_bwd_filter": lambda: cg.conv3d_bwd_filter(x3, dy3, (2, 3, 3)),
     }
 
 

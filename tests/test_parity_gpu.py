@@ -564,3 +564,52 @@ def test_stride_phase_bwd_filter_parity(cg, case, groups, flip, dtype):
                  f"{case}/g{groups}/flip={flip}/{dtype}")
     _check_plain(pb, dbk.double().cpu().numpy(), oracle.channel_sum(dy, 0.5, dbk0), amax(dy), N * pb.P * pb.Q,
                  f"{case}/db_k/{dtype}")
+
+
+# 3-D (NCDHW): every element of the three ops against the fp64 3-D oracle.  Each case is
+# N, C, (D, H, W), K, (T, R, S), pads, strides, dilations, groups.
+CASES_3D = [
+    (2, 3, (5, 6, 7), 4, (3, 3, 3), (1, 1, 1), (1, 1, 1), (1, 1, 1), 1),
+    (1, 8, (7, 9, 8), 6, (3, 3, 2), (1, 1, 0), (2, 2, 1), (1, 1, 1), 1),     # depth and row stride 2
+    (2, 4, (6, 8, 8), 4, (2, 3, 3), (0, 2, 1), (1, 1, 2), (2, 2, 1), 2),     # depth dilation 2, groups 2
+    (1, 16, (4, 10, 10), 24, (3, 1, 1), (1, 0, 0), (1, 1, 1), (1, 1, 1), 1),  # depth-only filter
+    (1, 5, (9, 5, 6), 7, (4, 2, 3), (2, 1, 1), (3, 1, 1), (1, 1, 1), 1),     # depth stride 3, uncovered tail
+]
+
+
+def _red_len_3d(op, N, C, K, T, R, S, Z, P, Q, st, groups):
+    if op == "fwd":
+        return (C // groups) * T * R * S
+    if op == "bwd_data":
+        return (K // groups) * math.ceil(T / st[0]) * math.ceil(R / st[1]) * math.ceil(S / st[2])
+    return N * Z * P * Q
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("op", ["fwd", "bwd_data", "bwd_filter"])
+@pytest.mark.parametrize("case", CASES_3D)
+def test_conv3d_parity(cg, case, op, dtype):
+    N, C, dhw, K, trs, pad, st, dil, groups = case
+    tdt = torch.float32 if dtype == "f32" else torch.bfloat16
+    g = torch.Generator().manual_seed(9700 + CASES_3D.index(case))
+    x = (torch.rand((N, C, *dhw), generator=g) * 2 - 1).to(tdt)
+    w = (torch.rand((K, C // groups, *trs), generator=g) * 2 - 1).to(tdt)
+    zpq = tuple((i + 2 * p - (d * (k - 1) + 1)) // s + 1 for i, p, k, s, d in zip(dhw, pad, trs, st, dil))
+    dy = (torch.rand((N, K, *zpq), generator=g) * 2 - 1).to(tdt)
+    if op == "fwd":
+        out = cg.conv3d_fwd(x.to(DEV), w.to(DEV), pad, st, dil, groups)
+        ref = oracle.conv3d_fwd(x, w, pad, st, dil, groups)
+        a, b = x, w
+    elif op == "bwd_data":
+        out = cg.conv3d_bwd_data(dy.to(DEV), w.to(DEV), dhw, pad, st, dil, groups)
+        ref = oracle.conv3d_bwd_data(dy, w, dhw, pad, st, dil, groups)
+        a, b = dy, w
+    else:
+        out = cg.conv3d_bwd_filter(x.to(DEV), dy.to(DEV), trs, pad, st, dil, groups)
+        ref = oracle.conv3d_bwd_filter(x, dy, trs, pad, st, dil, groups)
+        a, b = x, dy
+    cg.conv2d_device_status()
+    pb = W.Conv2dProblem(1, 1, 1, 1, 1, 1, 1, dtype=dtype)  # carries the dtype for the check
+    length = _red_len_3d(op, N, C, K, *trs, *zpq, st, groups)
+    _check_plain(pb, out.double().cpu().numpy(), ref, float(a.abs().max()) * float(b.abs().max()), length,
+                 f"3-D {case}/{op}/{dtype}")
