@@ -41,6 +41,7 @@ using namespace cg3;
 namespace {
 
 constexpr size_t kWorkspaceCap = 1000000000ull;  // 1e9 bytes
+constexpr int kMaxTapPasses = 16;                // tap passes of one forward / backward-data call
 constexpr int kDefaultSMs = 152;                  // used when no device can be queried
 constexpr size_t kDefaultSmemOptin = 232448;      // 227 KB
 
@@ -78,7 +79,10 @@ int validate(const Desc& d) {
   if ((long long)d.N * d.C * d.H * d.W >= lim || (long long)d.N * d.K * d.P * d.Q >= lim ||
       (long long)d.K * d.C * d.R * d.S >= lim)
     return CONV2D_ERR_TOO_LARGE;
-  if (d.R * d.S > kMaxTaps || d.sh * d.sw > kMaxPlanes) return CONV2D_ERR_UNSUPPORTED;
+  // forward / backward-data run at most kMaxTapPasses passes of at most kMaxTaps taps;
+  // backward-filter plans refuse more than kMaxTaps taps per stride phase themselves
+  if ((long long)d.R * d.S > (long long)kMaxTapPasses * kMaxTaps || (long long)d.sh * d.sw > kMaxPlanes)
+    return CONV2D_ERR_UNSUPPORTED;
   return CONV2D_OK;
 }
 
@@ -1213,6 +1217,7 @@ bool setup_pack_tiles(NhwcPackPlan& q, int esz) {
 
 int build_wgrad_mn(const Desc& d, const void* x, const void* dy, void* dw, void* ws, const DevInfo& di, MnBuild& b) {
   if (d.dt != CONV2D_DTYPE_BF16) return CONV2D_ERR_UNSUPPORTED;
+  if (d.R * d.S > kMaxTaps) return CONV2D_ERR_UNSUPPORTED;  // the plan's tap tables
   if ((d.sh > 1 || d.sw > 1) && (d.dh != 1 || d.dw != 1)) return CONV2D_ERR_UNSUPPORTED;
   if (d.K % 4 != 0) return CONV2D_ERR_UNSUPPORTED;  // the reduce reads 4 output channels at a time
   const std::vector<MnPhase> rows = mn_phases(d.R, d.ph, d.sh, d.dh), cols = mn_phases(d.S, d.pw, d.sw, d.dw);
@@ -1464,7 +1469,6 @@ bool same_key(const PlanKey& a, const PlanKey& b) {
 // (large filters over many source channels) the taps u = r*S + s are split into contiguous
 // ranges, one pass each: the first pass applies the caller's bias and beta, the later ones
 // add onto the output (beta = 1).  Each pass has its own repacked filter in the workspace.
-constexpr int kMaxTapPasses = 16;
 
 struct TapSet {
   std::vector<TapBuild> pass;

@@ -48,9 +48,9 @@ __device__ __forceinline__ uint32_t fdiv(uint32_t n, const FastDiv& f) {
 }
 #endif
 
-constexpr int kMaxPlanes = 16;   // stride_h * stride_w
-constexpr int kMaxPhases = 16;
-constexpr int kMaxTaps = 256;    // R * S
+constexpr int kMaxPlanes = 64;   // stride_h * stride_w
+constexpr int kMaxPhases = 64;
+constexpr int kMaxTaps = 256;    // R * S of one pass (forward / backward-data split larger filters into passes)
 
 // Forward and backward-data: D[position, out_channel] = sum over taps and source
 // channels of S[channel, position + tap_off] * Wpacked[tap, out_channel, channel].

@@ -104,10 +104,12 @@ enum {
     CONV2D_ERR_LAUNCH = -8,         /* the CUDA runtime rejected a launch */
     CONV2D_ERR_DEVICE = -9,         /* no usable sm_100-family device */
     CONV2D_ERR_DEVICE_TIMEOUT = -10,/* a kernel's bounded internal wait expired */
-    CONV2D_ERR_UNSUPPORTED = -11,   /* R*S > 256, stride_h*stride_w > 16, or no tile fits
+    CONV2D_ERR_UNSUPPORTED = -11,   /* R*S > 4096, stride_h*stride_w > 64, or no tile fits
                                        shared memory: forward / backward-data even with the
-                                       taps split over 16 passes, backward-filter when the
-                                       dilated filter spans too many input rows */
+                                       taps split over 16 passes of at most 256 taps,
+                                       backward-filter with more than 256 taps in one stride
+                                       phase or when the dilated filter spans too many input
+                                       rows */
     CONV2D_ERR_BAD_OP = -12,        /* unknown op in conv2d_workspace_size() */
     CONV2D_ERR_NOALLOC_LIMIT = -13  /* conv2d_fwd_noalloc: problem exceeds its fixed scratch */
 };

@@ -509,6 +509,10 @@ int main() {
       {"r16_s2_bf16", 2, 24, 40, 40, 20, 16, 16, 7, 7, 2, 2, 1, 1, 1, 1, {2, 1}},
       {"r1_s256", 1, 16, 4, 300, 16, 1, 256, 0, 3, 1, 1, 0, 1, 1, 1, {1, 1}},
       {"r1_s256_c64", 1, 64, 4, 300, 64, 1, 256, 0, 3, 1, 1, 0, 1, 1, 1, {3, 3}},
+      {"r17", 1, 4, 40, 40, 8, 17, 17, 8, 8, 1, 1, 0, 1, 1, 1, {2, 2}},
+      {"r17_bf16", 1, 8, 36, 36, 16, 17, 17, 8, 8, 1, 1, 1, 1, 1, 1, {2, 2}},
+      {"s5_patch", 2, 3, 20, 20, 8, 5, 5, 0, 0, 5, 5, 0, 1, 1, 1, {1, 1}},
+      {"s6x5", 1, 6, 27, 26, 5, 3, 4, 1, 2, 6, 5, 0, 1, 1, 1, {1, 1}},
       {"s32", 2, 40, 23, 19, 24, 3, 3, 1, 1, 3, 2, 1, 1, 1, 1, {1, 1}},
       {"hr", 1, 2, 6, 13, 2, 6, 13, 0, 0, 1, 1, 0, 1, 1, 1, {1, 1}},
       {"rows5", 1, 40, 16, 16, 48, 5, 3, 2, 1, 1, 1, 0, 1, 1, 1, {1, 1}},
@@ -578,7 +582,11 @@ int main() {
       ++plans;
     }
     WgradBuild bw;
-    if (build_bwd_filter(d, px, py, pw, ws, di, bw) != CONV2D_OK) fail(s.nm, "bwd_filter", "no plan");
+    const int rcf = build_bwd_filter(d, px, py, pw, ws, di, bw);
+    // backward-filter refuses more than kMaxTaps filter taps (the documented limit)
+    if (rcf != CONV2D_OK && !(rcf == CONV2D_ERR_UNSUPPORTED && d.R * d.S > kMaxTaps))
+      fail(s.nm, "bwd_filter", "no plan");
+    if (rcf == CONV2D_OK && d.R * d.S > kMaxTaps) fail(s.nm, "bwd_filter", "planned past the tap tables");
     check_phases(s.nm, d, di, plans);
     Desc d16 = d;  // the channel-chunked path plans bf16 only
     d16.dt = 1;

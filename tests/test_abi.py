@@ -84,7 +84,8 @@ GOOD = (2, 3, 8, 8, 4, 3, 3, 1, 1, 1, 1, 8, 8)
     ((2, 3, 8, 8, 4, 3, 3, 1, 1, 1, 1, 7, 8), -2),    # P mismatch
     ((2, 3, 2, 8, 4, 5, 3, 0, 1, 1, 1, 0, 8), -2),    # no output rows
     ((65536, 256, 256, 256, 4, 3, 3, 1, 1, 1, 1, 256, 256), -7),  # too large
-    ((2, 3, 80, 80, 4, 17, 17, 1, 1, 1, 1, 66, 66), -11),  # R*S > 256
+    ((1, 1, 80, 80, 1, 65, 65, 0, 0, 1, 1, 16, 16), -11),  # R*S > 4096 (16 passes of 256 taps)
+    ((1, 1, 90, 90, 1, 9, 9, 0, 0, 9, 9, 10, 10), -11),    # stride_h*stride_w > 64
 ])
 def test_descriptor_errors(cg, bad, code):
     for op in (0, 1, 2):

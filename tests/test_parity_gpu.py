@@ -187,6 +187,8 @@ SMALL = [
     (1, 33, 9, 9, 40, 3, 3, 1, 1, 1, 1),     # channel counts off every chunk size
     (1, 17, 6, 6, 300, 3, 3, 1, 1, 1, 1),    # K > 256: several N tiles
     (2, 70, 11, 5, 130, 2, 2, 0, 1, 1, 2),
+    (2, 3, 20, 20, 8, 5, 5, 0, 0, 5, 5),     # stride 5 x 5: 25 phase planes, non-overlapping windows
+    (1, 6, 27, 26, 5, 3, 4, 1, 2, 6, 5),     # stride 6 x 5: 30 planes
     (1, 1, 4, 4, 1, 1, 1, 0, 0, 3, 3),       # 1x1 stride 3: backward-data phases without taps
     (4, 12, 20, 20, 24, 3, 3, 0, 0, 1, 1),   # no padding
     (1, 9, 31, 17, 11, 5, 5, 2, 2, 1, 1),
@@ -494,6 +496,8 @@ PASS_CASES = [
     ((2, 24, 40, 40, 20, 16, 16, 7, 7, 2, 2), "bf16"),  # 2, 1
     ((1, 40, 40, 40, 96, 15, 15, 7, 7, 1, 1), "bf16"),  # 4, 2
     ((1, 64, 4, 300, 64, 1, 256, 0, 3, 1, 1), "f32"),   # 3, 3
+    ((1, 4, 40, 40, 8, 17, 17, 8, 8, 1, 1), "f32"),     # 2, 2 (289 taps: more than one pass holds)
+    ((1, 8, 36, 36, 16, 17, 17, 8, 8, 1, 1), "bf16"),   # 2, 2
 ]
 
 
