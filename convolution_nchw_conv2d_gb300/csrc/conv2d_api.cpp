@@ -501,26 +501,38 @@ int build_bwd_data_impl(const Desc& d0, const void* dy, const void* w, void* dx,
   phase_dims(d.H, d.ph, d.R, d.dh, d.sh, Th, uloh, Uh, tapsh);
   phase_dims(d.W, d.pw, d.S, d.dw, d.sw, Tw, ulow, Uw, tapsw);
   const int CHUNK = d.dt == 0 ? 4 : 8;
-  // With the source packed for tensor copies (whole filter in one pass), every phase reads its
-  // own dy plane: phase (a, c) at linear (e, f) reads plane row e + Th[a]-1 - t_r, column
-  // f + Tw[c]-1 - t_s, its plane starting at dy row ulo_a - (Th[a]-1) and column
-  // ulo_c - (Tw[c]-1).  The linear space then needs only U + T - 1 rows (columns) per phase
-  // instead of the span of all phases' windows in one shared plane, so fewer position tiles;
-  // the pack writes one plane per phase.
+  // With the source packed for tensor copies (whole filter in one pass), every phase reads the
+  // one packed dy plane from its own origin: phase (a, c) at linear (e, f) reads dy row
+  // e + (Th[a]-1 - t_r) + dh_a and column f + (Tw[c]-1 - t_s) + dw_c with dh_a = ulo_a - (Th[a]-1),
+  // dw_c likewise, i.e. the plane at linear position L + tap offset + dh_a*WL + dw_c.  The grid
+  // (EL x WL per image) is large enough that every position a phase reads either lies in its
+  // own image's rows or falls on zero rows / columns of the grid (a read before row 0 lands on
+  // the previous image's last rows, which lie past P): EL >= U + T - 1, >= ulo + U and
+  // >= P + T - 1 - ulo for every phase, likewise WL.  Each phase's linear space then spans its
+  // own outputs, not the union of all phases' windows, so fewer position tiles, and the pack
+  // writes dy once.
   if (packed_src && u_lo == 0 && u_hi >= d.R * d.S && d.sh * d.sw > 1) {
-    int EL = 1, WL = 1;
-    for (int a = 0; a < d.sh; ++a) EL = std::max(EL, Uh[a] + std::max(Th[a], 1) - 1);
-    for (int c = 0; c < d.sw; ++c) WL = std::max(WL, Uw[c] + std::max(Tw[c], 1) - 1);
+    int EL = std::max(1, d.P), WL = std::max(1, d.Q);
+    for (int a = 0; a < d.sh; ++a) {
+      EL = std::max(EL, Uh[a]);
+      if (Th[a] > 0) EL = std::max({EL, Uh[a] + Th[a] - 1, Uh[a] + uloh[a], d.P + Th[a] - 1 - uloh[a]});
+    }
+    for (int c = 0; c < d.sw; ++c) {
+      WL = std::max(WL, Uw[c]);
+      if (Tw[c] > 0) WL = std::max({WL, Uw[c] + Tw[c] - 1, Uw[c] + ulow[c], d.Q + Tw[c] - 1 - ulow[c]});
+    }
     TapPlan q = p;
     q.WL = WL;
     q.EL = EL;
     q.Mtot = (long long)d.N * EL * WL;
-    if (q.Mtot < (1ll << 31)) {
+    if (q.Mtot < (1ll << 30)) {  // room for the phase shifts in the copies' 32-bit coordinates
       q.fd_img = make_fastdiv((uint32_t)(EL * WL));
       q.fd_WL = make_fastdiv((uint32_t)WL);
-      q.nph = q.npl = d.sh * d.sw;
+      q.npl = 1;
+      q.nph = d.sh * d.sw;
       q.plane_per_phase = 1;
       q.pl_step_h = q.pl_step_w = 1;
+      q.pl_off_h[0] = q.pl_off_w[0] = 0;
       q.ph_step_h = d.sh;
       q.ph_step_w = d.sw;
       std::vector<int> tpl, toff, tr, ts;
@@ -528,8 +540,7 @@ int build_bwd_data_impl(const Desc& d0, const void* dy, const void* w, void* dx,
       for (int a = 0; a < d.sh; ++a)
         for (int c = 0; c < d.sw; ++c) {
           const int ph = a * d.sw + c;
-          q.pl_off_h[ph] = uloh[a] - (std::max(Th[a], 1) - 1);
-          q.pl_off_w[ph] = ulow[c] - (std::max(Tw[c], 1) - 1);
+          q.ph_shift[ph] = (uloh[a] - (std::max(Th[a], 1) - 1)) * WL + (ulow[c] - (std::max(Tw[c], 1) - 1));
           q.ph_off_h[ph] = d.sh * uloh[a] + a - d.ph;
           q.ph_off_w[ph] = d.sw * ulow[c] + c - d.pw;
           const int begin = (int)tpl.size();
@@ -537,7 +548,7 @@ int build_bwd_data_impl(const Desc& d0, const void* dy, const void* w, void* dx,
           for (const int r : tapsh[a])
             for (const int s2 : tapsw[c]) {
               const int t = (r * d.dh - a) / d.sh, t2 = (s2 * d.dw - c) / d.sw;
-              tpl.push_back(ph);
+              tpl.push_back(0);
               toff.push_back((Th[a] - 1 - t) * WL + (Tw[c] - 1 - t2));
               tr.push_back(r);
               ts.push_back(s2);

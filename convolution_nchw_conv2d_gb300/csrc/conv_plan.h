@@ -63,8 +63,9 @@ struct TapPlan {
   CUtensorMap tm_src;
   int a_tma;             // 1: staged rows come from tm_src (rows = a_nbox * a_box)
   int a_box, a_nbox;
-  int plane_per_phase;   // 1 (with a_tma): phase ph reads only plane ph, and a stage holds the
-                         // tile's phase plane alone (tap_plane[t] is then t's phase)
+  int plane_per_phase;   // 1 (with a_tma, one plane): phase ph reads the plane shifted by
+                         // ph_shift[ph] positions, so a stage holds the tile's phase window alone
+  int ph_shift[kMaxPhases];
   const void* src;       // x (forward) or dy (backward-data), NCHW
   void* dst;             // y or dx, NCHW
   const void* bias;      // optional, one value per destination channel (NULL: none)

@@ -263,14 +263,15 @@ __global__ void __launch_bounds__(kThreads, 1) tap_gemm_kernel(const __grid_cons
           mbar_expect_tx(bar_at(full, stage), bytes + (p.a_tma ? (uint32_t)p.a_stage_bytes : 0u));
           bulk_g2s(b_st, static_cast<const uint8_t*>(p.wpack) + img_off, bytes, bar_at(full, stage));
           if (p.a_tma) {
-            // one tensor copy per (plane, chunk, box of rows): [plane][chunk][row][16 bytes]; with
-            // a plane per phase, the tile's phase plane alone
-            const int pl0 = p.plane_per_phase ? tc.ph : 0, pl1 = p.plane_per_phase ? tc.ph + 1 : p.npl;
-            for (int pl = pl0; pl < pl1; ++pl)
+            // one tensor copy per (plane, chunk, box of rows): [plane][chunk][row][16 bytes]; with a
+            // shift per phase, the plane's rows from the tile's phase origin (a negative start
+            // reads zeros)
+            const long long l0 = m0 + (p.plane_per_phase ? p.ph_shift[tc.ph] : 0);
+            for (int pl = 0; pl < p.npl; ++pl)
               for (int j = 0; j < NCH; ++j)
                 for (int bx = 0; bx < p.a_nbox; ++bx)
-                  tma_load_3d(a_st + (uint32_t)((((pl - pl0) * NCH + j) * rows + bx * p.a_box) * 16), &p.tm_src,
-                              (int)(2 * (m0 + (long long)bx * p.a_box)), kb * NCH + j, pl, bar_at(full, stage));
+                  tma_load_3d(a_st + (uint32_t)(((pl * NCH + j) * rows + bx * p.a_box) * 16), &p.tm_src,
+                              (int)(2 * (l0 + (long long)bx * p.a_box)), kb * NCH + j, pl, bar_at(full, stage));
           }
           last_copy[stage] = 1 + (int)ephase;
         }

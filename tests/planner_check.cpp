@@ -271,6 +271,45 @@ void check_tap_semantics(const char* nm, const char* op, const Desc& d, const Ta
           for (int f = 0; f < p.WL; ++f) {
             const int oh = e * p.ph_step_h + p.ph_off_h[ph], ow = f * p.ph_step_w + p.ph_off_w[ph];
             if (oh < 0 || oh >= p.Hd || ow < 0 || ow >= p.Wd) continue;  // not an output
+            if (p.plane_per_phase) {
+              // the phase reads the one plane at linear e*WL + f + tap offset + its shift, which may
+              // leave the image: there it must land on a zero row or column of the grid (past the
+              // source's rows / columns) of a neighbouring image, or before the first / past the
+              // last image (zero fill); inside, on the pixel the definition names
+              if (fwd || pl != 0) {
+                fail(nm, op, "phase shifts outside backward-data with one plane");
+                bad = true;
+                break;
+              }
+              const int nh = oh + d.ph - r * d.dh, nw = ow + d.pw - s * d.dw;
+              const bool inside = ((nh % d.sh) + d.sh) % d.sh == 0 && ((nw % d.sw) + d.sw) % d.sw == 0;
+              if (!inside) {
+                fail(nm, op, "a tap sits in a phase whose outputs it does not reach");
+                bad = true;
+                break;
+              }
+              const long long dh = floor_div(nh, d.sh), dwc = floor_div(nw, d.sw);
+              const bool def_zero = dh < 0 || dh >= p.Hs || dwc < 0 || dwc >= p.Ws;
+              const long long img = (long long)p.EL * p.WL;
+              for (int n = 0; n < std::min(p.N, 2); ++n) {  // the first image and one after it
+                const long long Lr = n * img + (long long)e * p.WL + f + p.tap_off[t] + p.ph_shift[ph];
+                bool got_zero = Lr < 0 || Lr >= p.Mtot;
+                long long gn = 0, ge = 0, gf = 0;
+                if (!got_zero) {
+                  gn = Lr / img;
+                  ge = (Lr % img) / p.WL;
+                  gf = Lr % p.WL;
+                  got_zero = ge >= p.Hs || gf >= p.Ws;
+                }
+                if (got_zero != def_zero || (!got_zero && (gn != n || ge != dh || gf != dwc))) {
+                  fail(nm, op, "a shifted phase reads the wrong dy pixel");
+                  bad = true;
+                  break;
+                }
+              }
+              if (bad) break;
+              continue;
+            }
             const long long L = (long long)e * p.WL + f + p.tap_off[t];
             const long long es = L / p.WL, fs = L % p.WL;
             if (es >= p.EL) {  // the kernel would read the next image's rows
