@@ -252,6 +252,24 @@ def _roofline_of(pb, op_ms, peaks):
     return per_op, roof
 
 
+def _fused_backward(c, flush, stream, reps, warmup, op_ms):
+    """Both gradients through the one-call backward (dy read once where the plans share it) beside
+    the two separate backward calls on the same workload."""
+    import torch
+    import convolution_nchw_conv2d_gb300 as cg
+    pb = c["pb"]
+    pad, st = (pb.pad_h, pb.pad_w), (pb.stride_h, pb.stride_w)
+    dt = 0 if pb.dtype == "f32" else 1
+    wsz = cg.conv2d_workspace_size(cg.OP_BWD, pb.dims(), dt)
+    ws = torch.empty(max(wsz, 16), dtype=torch.uint8, device=c["x"].device)
+    ms = _time_call(lambda: cg.conv2d_bwd(c["x"], c["w"], c["dy"], pad, st, dx=c["dx"], dw=c["dw"], workspace=ws,
+                                          stream=stream), flush, stream, reps, warmup)
+    sep = op_ms["bwd_data"] + op_ms["bwd_filter"]
+    return {"bwd_ms": round(ms, 5), "bwd_data_plus_bwd_filter_ms": round(sep, 5),
+            "tflops": round(2 * pb.flops() / (ms * 1e-3) / 1e12, 2), "saved_ms": round(sep - ms, 5),
+            "note": "conv2d_bwd (dx and dw in one call) against the two separate calls, same inputs"}
+
+
 def _extras_resnet(c, flush, stream, reps, warmup, op_ms):
     """Timings of the extended entry points on the ResNet 3x3 layer: the fused epilogues (bias +
     add-to on the forward op, both bias gradients on backward-filter), dilation 2, groups 2."""
@@ -453,13 +471,14 @@ def run_ours(args, rank, world):
                           "every call); tensor peak TF32 for fp32 workloads, BF16 for bf16; the dominant op against "
                           "its roof (tensor or HBM by arithmetic intensity)")
 
-    extras = {}
+    extras = {"fused_backward": _fused_backward(head, flush, stream, reps, args.warmup,
+                                                {op: per_config[wl.name]["per_op"][op]["ms"] for op in OPS})}
     if "resnet3x3" in W.WORKLOADS:
         rc = head if wl.name == "resnet3x3" else _device_case(W.WORKLOADS["resnet3x3"], dev)
         rms = per_config["resnet3x3"]["per_op"]
         fused, dilated, grouped = _extras_resnet(rc, flush, stream, reps, args.warmup,
                                                  {op: rms[op]["ms"] for op in OPS})
-        extras = {"fused_epilogue": fused, "dilation_2": dilated, "groups_2": grouped}
+        extras.update({"fused_epilogue": fused, "dilation_2": dilated, "groups_2": grouped})
 
     e2e_ms = _e2e(head, flush, stream, max(1, args.e2e_steps))
     esz = pb.elem_bytes()

@@ -22,12 +22,12 @@ __all__ = [
     "conv2d_fwd", "conv2d_bwd_data", "conv2d_bwd_filter", "deconv2d_fwd", "conv2d_fwd_noalloc",
     "conv1d_fwd", "conv1d_bwd_data", "conv1d_bwd_filter", "MODE_CROSS_CORRELATION", "MODE_CONVOLUTION",
     "conv2d_workspace_size", "conv2d_output_dim", "conv2d_device_status", "conv2d_strerror",
-    "conv2d_kernel_launches",
-    "Conv2dError", "lib_path", "load_library", "OP_FWD", "OP_BWD_DATA", "OP_BWD_FILTER",
+    "conv2d_kernel_launches", "conv2d_bwd", "conv3d_fwd", "conv3d_bwd_data", "conv3d_bwd_filter",
+    "Conv2dError", "lib_path", "load_library", "OP_FWD", "OP_BWD_DATA", "OP_BWD_FILTER", "OP_BWD",
     "DTYPE_F32", "DTYPE_BF16",
 ]
 
-OP_FWD, OP_BWD_DATA, OP_BWD_FILTER = 0, 1, 2
+OP_FWD, OP_BWD_DATA, OP_BWD_FILTER, OP_BWD = 0, 1, 2, 3
 MODE_CROSS_CORRELATION, MODE_CONVOLUTION = 0, 1
 DTYPE_F32, DTYPE_BF16 = 0, 1
 
@@ -50,7 +50,7 @@ def lib_path() -> str:
 EXPORTS = ("conv2d_output_dim", "conv2d_workspace_size", "conv2d_workspace_size_ex", "conv2d_fwd", "conv2d_bwd_data",
            "conv2d_bwd_filter", "conv2d_fwd_ex", "conv2d_bwd_data_ex", "conv2d_bwd_filter_ex",
            "conv2d_fwd_noalloc", "conv2d_device_status", "conv2d_strerror", "conv2d_kernel_launches",
-           "conv3d_workspace_size", "conv3d_fwd", "conv3d_bwd_data", "conv3d_bwd_filter")
+           "conv3d_workspace_size", "conv3d_fwd", "conv3d_bwd_data", "conv3d_bwd_filter", "conv2d_bwd")
 
 
 def load_library():
@@ -89,6 +89,8 @@ def load_library():
         lib.conv2d_kernel_launches.restype = ctypes.c_ulonglong
         lib.conv2d_strerror.argtypes = [i]
         lib.conv2d_strerror.restype = ctypes.c_char_p
+        lib.conv2d_bwd.argtypes = [i] * 13 + [i, vp, vp, vp, vp, vp, vp, sz, vp]
+        lib.conv2d_bwd.restype = i
         ip = ctypes.POINTER(i)
         lib.conv3d_workspace_size.argtypes = [i, ip, i, i, ctypes.POINTER(sz)]
         lib.conv3d_workspace_size.restype = i
@@ -375,6 +377,35 @@ def conv2d_device_status(stream=None) -> int:
     if rc:
         raise Conv2dError(rc, "conv2d_device_status")
     return 0
+
+
+def conv2d_bwd(x, w, dy, pad=0, stride=1, dx=None, dw=None, workspace=None, stream=None):
+    """(dx, dw) = (conv2d_bwd_data(dy, w), conv2d_bwd_filter(x, dy)) in one call; with bf16
+    tensors dy is read from memory once for both where the plans allow."""
+    import torch
+    for t, nm in ((x, "x"), (w, "w"), (dy, "dy")):
+        _check_tensor(t, nm)
+    N, C, H, W = x.shape
+    K, C2, R, S = w.shape
+    if C2 != C or w.dtype != x.dtype or dy.dtype != x.dtype:
+        raise ValueError("x / w channel count or dtype mismatch")
+    ph, pw = _pair(pad)
+    sh, sw = _pair(stride)
+    P, Q = conv2d_output_dim(H, ph, R, sh), conv2d_output_dim(W, pw, S, sw)
+    if tuple(dy.shape) != (N, K, P, Q):
+        raise ValueError("dy shape does not match the descriptor")
+    dims = (N, C, H, W, K, R, S, ph, pw, sh, sw, P, Q)
+    dt = _dtype_code(x)
+    if dx is None:
+        dx = torch.empty_like(x)
+    if dw is None:
+        dw = torch.empty_like(w)
+    ws, wsb = _workspace(OP_BWD, dims, dt, workspace, x.device)
+    rc = load_library().conv2d_bwd(*dims, dt, _ptr(x), _ptr(w), _ptr(dy), _ptr(dx), _ptr(dw), _ptr(ws),
+                                   ctypes.c_size_t(wsb), _stream_ptr(stream))
+    if rc:
+        raise Conv2dError(rc, "conv2d_bwd")
+    return dx, dw
 
 
 # ---------------------------------------------------------------------------- 3-D (NCDHW)

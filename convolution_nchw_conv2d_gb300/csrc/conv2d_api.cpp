@@ -1558,6 +1558,7 @@ PlanCache<WgradBuild> g_wgrad_plans;
 PlanCache<MnBuild> g_mn_plans;
 PlanCache<size_t> g_ws_sizes;
 constexpr int kMnKey = 17;  // cache key tag of the channel-chunked backward-filter plans (not an op code)
+constexpr int kFusedKey = 18;  // cache key tag of the both-gradients plans
 
 int workspace_size_uncached(int op, const Desc& d, size_t* bytes);
 
@@ -1684,9 +1685,64 @@ int conv2d_workspace_size_ex(int op, int N, int C, int H, int W, int K, int R, i
 }  // extern "C"
 
 namespace {
+// Both gradients in one call (conv2d_bwd).  bf16, one group: the backward-filter plan packs x
+// and dy into channel-chunk planes; when the backward-data plan stages dy from one packed plane
+// of the same grid (rows EX, row width WL, dy at its origin), it reads that same pack, so dy is
+// read from memory once for both gradients (the pages' backward pass schedules backward-data
+// and backward-weights together on the shared output gradient).  Workspace: the
+// backward-filter plan's, then the backward-data filter pack.  Otherwise the two ops run one
+// after the other in the same workspace.
+struct FusedBwd {
+  bool fused = false;
+  MnBuild mb;
+  TapSet set;
+  size_t tap_off = 0;  // offset of the backward-data part of the workspace
+  size_t need = 0;
+};
+
+int build_fused_bwd(const Desc& d, const void* x, const void* w, const void* dy, void* dx, void* dw, void* ws,
+                    const DevInfo& di, FusedBwd& f) {
+  f.fused = false;
+  if (d.dt == CONV2D_DTYPE_BF16 && d.g == 1 && build_wgrad_mn(d, x, dy, dw, ws, di, f.mb) == CONV2D_OK) {
+    f.tap_off = align_ws(mn_ws_bytes(f.mb));
+    void* wt = ws != nullptr ? static_cast<void*>(static_cast<uint8_t*>(ws) + f.tap_off) : nullptr;
+    const int rc = build_tap_set(CONV2D_OP_BWD_DATA, d, dy, w, dx, wt, di, f.set, true);
+    if (rc) return rc;
+    const TapBuild& b = f.set.pass[0];
+    const NhwcPackPlan& q = f.mb.pd;  // dy as the backward-filter plan packs it
+    if (f.set.pass.size() == 1 && b.p.a_tma && b.p.npl == 1 && b.p.pl_off_h[0] == 0 && b.p.pl_off_w[0] == 0 &&
+        b.p.pl_step_h == 1 && b.p.pl_step_w == 1 && b.p.EL == q.EX && b.p.WL == q.WL && b.px.nchunk == q.nchunk &&
+        b.p.Mtot == (long long)q.N * q.EX * q.WL) {
+      f.fused = true;
+      f.need = f.tap_off + b.pack_bytes;
+      if (ws != nullptr) {  // the backward-data copies read the backward-filter plan's dy pack
+        const uint64_t dims[3] = {2 * (uint64_t)b.p.Mtot, (uint64_t)q.nchunk, 1};
+        const uint32_t box[3] = {2 * (uint32_t)b.p.a_box, 1u, 1u};
+        if (!encode_mn_map(&f.set.pass[0].p.tm_src, q.dst, 3, dims, box)) return CONV2D_ERR_UNSUPPORTED;
+      }
+      return CONV2D_OK;
+    }
+  }
+  return CONV2D_OK;
+}
+
+PlanCache<FusedBwd> g_fused_plans;
+
 int workspace_size_uncached(int op, const Desc& d, size_t* bytes) {
   int rc;
   const DevInfo di = device_info();
+  if (op == CONV2D_OP_BWD) {
+    FusedBwd f;
+    rc = build_fused_bwd(d, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, di, f);
+    if (rc) return rc;
+    size_t a = 0, b = 0;
+    rc = workspace_size_uncached(CONV2D_OP_BWD_DATA, d, &a);
+    if (rc) return rc;
+    rc = workspace_size_uncached(CONV2D_OP_BWD_FILTER, d, &b);
+    if (rc) return rc;
+    *bytes = std::max({a, b, f.fused ? f.need : size_t(0)});
+    return CONV2D_OK;
+  }
   if (op == CONV2D_OP_FWD || op == CONV2D_OP_BWD_DATA) {
     TapSet set;
     rc = build_tap_set(op, d, nullptr, nullptr, nullptr, nullptr, di, set, true);
@@ -1820,6 +1876,62 @@ int conv2d_bwd_data_ex(int N, int C, int H, int W, int K, int R, int S, int pad_
                        size_t workspace_bytes, void* stream) {
   const Desc d{N, C, H, W, K, R, S, pad_h, pad_w, stride_h, stride_w, P, Q, dtype, dil_h, dil_w};
   return run_tap(CONV2D_OP_BWD_DATA, d, groups, dy, w, bias, beta, mode, dx, workspace, workspace_bytes, stream);
+}
+
+int conv2d_bwd(int N, int C, int H, int W, int K, int R, int S, int pad_h, int pad_w, int stride_h, int stride_w,
+               int P, int Q, int dtype, const void* x, const void* w, const void* dy, void* dx, void* dw,
+               void* workspace, size_t workspace_bytes, void* stream) {
+  const Desc d{N, C, H, W, K, R, S, pad_h, pad_w, stride_h, stride_w, P, Q, dtype};
+  int rc = validate(d);
+  if (rc) return rc;
+  rc = check_ptrs(x, w, dy, dtype);
+  if (rc) return rc;
+  rc = check_ptrs(dx, dw, dy, dtype);
+  if (rc) return rc;
+  const DevInfo di = device_info();
+  if (!di.ok) return CONV2D_ERR_DEVICE;
+  FusedBwd f;
+  const PlanKey key = make_key(kFusedKey, d, x, dy, dw, workspace);
+  if (!g_fused_plans.get(key, f)) {
+    rc = build_fused_bwd(d, x, w, dy, dx, dw, workspace, di, f);
+    if (rc) return rc;
+    if (workspace != nullptr) g_fused_plans.put(key, f);
+  }
+  if (!f.fused) {  // one op after the other, each planned on its own
+    rc = conv2d_bwd_data(N, C, H, W, K, R, S, pad_h, pad_w, stride_h, stride_w, P, Q, dtype, dy, w, dx, workspace,
+                         workspace_bytes, stream);
+    if (rc) return rc;
+    return conv2d_bwd_filter(N, C, H, W, K, R, S, pad_h, pad_w, stride_h, stride_w, P, Q, dtype, x, dy, dw,
+                             workspace, workspace_bytes, stream);
+  }
+  rc = check_ws(workspace, workspace_bytes, f.need);
+  if (rc) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  MnBuild& mb = f.mb;
+  mb.px.src = x;
+  mb.pd.src = dy;
+  mb.rp.dw = dw;
+  mb.rp.beta = 0.f;
+  mb.rp.flip = 0;
+  TapBuild& b = f.set.pass[0];
+  b.p.src = dy;  // per call: the plan is cached under x, dy, dw and the workspace only
+  b.p.dst = dx;
+  b.pp.w = w;
+  b.p.beta = 0.f;
+  b.p.bias = nullptr;
+  b.pp.flip = 0;
+  // x and dy packed once; the backward-data GEMM (after its filter pack) reads the dy pack
+  rc = launch_err(launch_nhwc_pack(mb.px, mb.pd, dtype, di.sms, st));
+  if (rc) return rc;
+  if (b.pack_bytes) {
+    rc = launch_err(launch_pack_filter(b.pp, dtype, st));
+    if (rc) return rc;
+  }
+  rc = launch_err(launch_tap_gemm(b.p, dtype, b.grid, st));
+  if (rc) return rc;
+  rc = launch_err(launch_wgrad_mn(mb.p, mb.grid, st));
+  if (rc) return rc;
+  return launch_err(launch_wgrad_reduce_t(mb.rp, dtype, di.sms, st));
 }
 
 int conv2d_bwd_filter(int N, int C, int H, int W, int K, int R, int S, int pad_h, int pad_w, int stride_h,

@@ -89,7 +89,8 @@ enum {
 enum {
     CONV2D_OP_FWD = 0,
     CONV2D_OP_BWD_DATA = 1,
-    CONV2D_OP_BWD_FILTER = 2
+    CONV2D_OP_BWD_FILTER = 2,
+    CONV2D_OP_BWD = 3           /* both gradients in one call (conv2d_bwd) */
 };
 
 enum {
@@ -203,6 +204,19 @@ int conv2d_bwd_filter_ex(int N, int C, int H, int W, int K, int R, int S,
                          int dil_h, int dil_w, int groups, int dtype, int mode,
                          const void *x, const void *dy, float beta, void *dw, void *db_k, void *db_c,
                          void *workspace, size_t workspace_bytes, void *stream);
+
+/* Both gradients of one convolution in one call: dx = conv2d_bwd_data(dy, w) and
+ * dw = conv2d_bwd_filter(x, dy), overwritten, cross-correlation (page "mkldnn_deconvolution.cc",
+ * MKLDNNDeconvBwd::Execute: backward-data and backward-weights scheduled together on the shared
+ * output gradient).  With bf16 tensors, where the backward-data plan stages dy from the same
+ * channel-chunk copy that the backward-filter plan makes, dy is read from memory once for both;
+ * otherwise the two operations run one after the other.  Same descriptor, pointer and error
+ * rules as the single operations; the workspace is sized by conv2d_workspace_size with
+ * CONV2D_OP_BWD. */
+int conv2d_bwd(int N, int C, int H, int W, int K, int R, int S,
+               int pad_h, int pad_w, int stride_h, int stride_w, int P, int Q,
+               int dtype, const void *x, const void *w, const void *dy, void *dx, void *dw,
+               void *workspace, size_t workspace_bytes, void *stream);
 
 /* 3-D (NCDHW) cross-correlation, the same three operations one dimension up (page
  * "mkldnn_deconvolution.cc": SupportMKLDNNDeconv accepts kernels of 1 to 3 spatial dimensions,

@@ -34,7 +34,7 @@ def test_header_declares_the_abi():
     for n in ("conv2d_fwd", "conv2d_bwd_data", "conv2d_bwd_filter", "conv2d_workspace_size",
               "conv2d_output_dim", "conv2d_strerror", "conv2d_device_status", "conv2d_fwd_noalloc",
               "conv2d_kernel_launches", "conv3d_workspace_size", "conv3d_fwd", "conv3d_bwd_data",
-              "conv3d_bwd_filter"):
+              "conv3d_bwd_filter", "conv2d_bwd"):
         assert n in names
 
 

@@ -33,6 +33,7 @@ def _host_calls():
         "conv1d_fwd": lambda: cg.conv1d_fwd(x1, w1),
         "conv1d_bwd_data": lambda: cg.conv1d_bwd_data(dy1, w1, 5),
         "conv1d_bwd_filter": lambda: cg.conv1d_bwd_filter(x1, dy1, 3),
+        "conv2d_bwd": lambda: cg.conv2d_bwd(x, w, dy),
         "conv3d_fwd": lambda: cg.conv3d_fwd(x3, w3),
         "conv3d_bwd_data": lambda: cg.conv3d_bwd_data(dy3, w3, (4, 5, 5)),
         "conv3d_bwd_filter": lambda: cg.conv3d_bwd_filter(x3, dy3, (2, 3, 3)),

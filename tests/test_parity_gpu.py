@@ -617,3 +617,38 @@ def test_conv3d_parity(cg, case, op, dtype):
     length = _red_len_3d(op, N, C, K, *trs, *zpq, st, groups)
     _check_plain(pb, out.double().cpu().numpy(), ref, float(a.abs().max()) * float(b.abs().max()), length,
                  f"3-D {case}/{op}/{dtype}")
+
+
+
+# Both gradients in one call (conv2d_bwd): every element of dx and dw against the full oracle,
+# and bit for bit equal to the two single operations (the same plans; with bf16 the
+# backward-data GEMM reads the backward-filter plan's dy pack).
+@pytest.mark.parametrize("name", ["deconv", "resnet3x3", "tiny"])
+def test_fused_backward_parity(cg, name):
+    wl = W.WORKLOADS[name]
+    pb = wl.problem
+    x, w, dy = W.make_inputs(wl)
+    xd, wd, dyd = x.to(DEV), w.to(DEV), dy.to(DEV)
+    pad, st = (pb.pad_h, pb.pad_w), (pb.stride_h, pb.stride_w)
+    dx, dw = cg.conv2d_bwd(xd, wd, dyd, pad, st)
+    dx1 = cg.conv2d_bwd_data(dyd, wd, (pb.H, pb.W), pad, st)
+    dw1 = cg.conv2d_bwd_filter(xd, dyd, (pb.R, pb.S), pad, st)
+    cg.conv2d_device_status()
+    assert torch.equal(dx, dx1) and torch.equal(dw, dw1), f"{name}: fused backward differs from the single ops"
+    for op, out in (("bwd_data", dx), ("bwd_filter", dw)):
+        ref = _oracle_cached(op, name, pb, x, w, dy)
+        a, b = _operands(op, x, w, dy)
+        _check(op, pb, out.double().cpu().numpy(), ref, a, b, f"{name}/fused {op}")
+
+
+@pytest.mark.parametrize("case", [(2, 16, 12, 10, 24, 4, 4, 1, 1, 2, 2), (1, 8, 9, 11, 16, 3, 3, 1, 1, 2, 2)])
+def test_fused_backward_small_bf16(cg, case):
+    N, C, H, Wd, K, R, S, ph, pw, sh, sw = case
+    pb = W.Conv2dProblem(N, C, H, Wd, K, R, S, ph, pw, sh, sw, "bf16")
+    x, w, dy = W.random_problem_inputs(pb, 9800)
+    dx, dw = cg.conv2d_bwd(x.to(DEV), w.to(DEV), dy.to(DEV), (ph, pw), (sh, sw))
+    cg.conv2d_device_status()
+    for op, out in (("bwd_data", dx), ("bwd_filter", dw)):
+        ref = _oracle_full(op, pb, x, w, dy)
+        a, b = _operands(op, x, w, dy)
+        _check(op, pb, out.double().cpu().numpy(), ref, a, b, f"{case}/fused {op}")
