@@ -22,7 +22,7 @@ size_t tap_gemm_smem_bytes(const TapPlan& p);
 cudaError_t launch_wgrad(const WgradPlan& p, int dt, int grid, cudaStream_t st);
 cudaError_t launch_wgrad_reduce(const ReducePlan& rp, int dt, int num_sms, cudaStream_t st);
 cudaError_t launch_chan_sum(const ChanSumPlan& a, const ChanSumPlan& b, int dt, cudaStream_t st);
-cudaError_t launch_space_to_depth(const S2dPlan& sp, int dt, cudaStream_t st);
+cudaError_t launch_space_to_depth(const S2dPlan& sp, int dt, int num_sms, cudaStream_t st);
 size_t wgrad_smem_bytes(const WgradPlan& p, int dt);
 cudaError_t launch_wgrad_mn(const WgradMnPlan& p, int grid, cudaStream_t st);
 cudaError_t launch_nhwc_pack(const NhwcPackPlan& a, const NhwcPackPlan& b, int dt, int num_sms, cudaStream_t st);
@@ -32,6 +32,9 @@ size_t wgrad_mn_smem_bytes(const WgradMnPlan& p);
 int tap_gemm_take_error();
 int wgrad_take_error();
 int wgrad_mn_take_error();
+cudaError_t launch_c2i(const C2iPlan& p, int num_sms, cudaStream_t st);
+size_t c2i_smem_bytes(const C2iPlan& p);
+int c2i_take_error();
 size_t noalloc_scratch_capacity();
 cudaError_t noalloc_scratch_ptr(void** ptr);
 }  // namespace cg3
@@ -1481,6 +1484,57 @@ bool same_key(const PlanKey& a, const PlanKey& b) {
 // ranges, one pass each: the first pass applies the caller's bias and beta, the later ones
 // add onto the output (beta = 1).  Each pass has its own repacked filter in the workspace.
 
+// Backward-data for few input channels (dgrad_c2i_kernel): fp32, C <= 8, C*R <= 32, S <= 8,
+// strides <= 8, the halo within a tile (dlt_h <= 5 of 8 dy rows, dlt_w <= 7 of 32 dy
+// columns), the resident filter operand <= 64 KB.  d is the per-group descriptor.
+int build_c2i(const Desc& d, const void* dy, const void* w, void* dx, const DevInfo& di, C2iPlan& p) {
+  if (d.dt != CONV2D_DTYPE_F32 || d.C > 8 || d.S > 8 || d.C * d.R > 32 || d.sh > 8 || d.sw > 8)
+    return CONV2D_ERR_UNSUPPORTED;
+  const int dlt_h = (d.R - 1) * d.dh / d.sh, dlt_w = (d.S - 1) * d.dw / d.sw;
+  if (dlt_h > 5 || dlt_w > 7) return CONV2D_ERR_UNSUPPORTED;
+  std::memset(&p, 0, sizeof(p));
+  p.dy = dy;
+  p.w = w;
+  p.dx = dx;
+  p.N = d.N;
+  p.C = d.C;
+  p.H = d.H;
+  p.W = d.W;
+  p.K = d.K;
+  p.R = d.R;
+  p.S = d.S;
+  p.P = d.P;
+  p.Q = d.Q;
+  p.sh = d.sh;
+  p.sw = d.sw;
+  p.ph = d.ph;
+  p.pw = d.pw;
+  p.dh = d.dh;
+  p.dw = d.dw;
+  p.dy_nstride = (long long)d.g * d.K * d.P * d.Q;
+  p.dx_nstride = (long long)d.g * d.C * d.H * d.W;
+  p.Npad = round_up(d.C * d.R * 8, 16);
+  p.nkb = (d.K + 31) / 32;
+  p.dlt_h = dlt_h;
+  p.dlt_w = dlt_w;
+  p.THp = 8 - dlt_h;
+  p.TWq = 32 - dlt_w;
+  p.p_start = d.ph / d.sh;
+  p.q_start = d.pw / d.sw;
+  p.ntp = ceil_div_i(d.H + d.ph - p.p_start * d.sh, p.THp * d.sh);
+  p.ntq = ceil_div_i(d.W + d.pw - p.q_start * d.sw, p.TWq * d.sw);
+  p.tiles = (long long)d.N * p.ntp * p.ntq;
+  const long long bb = (long long)p.nkb * 8 * p.Npad * 16;
+  if (bb > 64 * 1024) return CONV2D_ERR_UNSUPPORTED;
+  p.b_bytes = (int)bb;
+  p.g_floats = 8 * d.R * 32 * d.sw;
+  int tc = 32;
+  while (tc < 2 * p.Npad) tc <<= 1;
+  p.tmem_cols = tc;
+  if (c2i_smem_bytes(p) > di.smem_optin) return CONV2D_ERR_UNSUPPORTED;
+  return CONV2D_OK;
+}
+
 struct TapSet {
   std::vector<TapBuild> pass;
   size_t pack_bytes = 0;  // workspace for all passes' repacked filters (and the packed source)
@@ -1554,6 +1608,7 @@ struct PlanCache {
 };
 
 PlanCache<TapSet> g_tap_plans;
+PlanCache<C2iPlan> g_c2i_plans;
 PlanCache<WgradBuild> g_wgrad_plans;
 PlanCache<MnBuild> g_mn_plans;
 PlanCache<size_t> g_ws_sizes;
@@ -1743,6 +1798,13 @@ int workspace_size_uncached(int op, const Desc& d, size_t* bytes) {
     *bytes = std::max({a, b, f.fused ? f.need : size_t(0)});
     return CONV2D_OK;
   }
+  if (op == CONV2D_OP_BWD_DATA) {
+    C2iPlan cp;
+    if (build_c2i(d, nullptr, nullptr, nullptr, di, cp) == CONV2D_OK) {
+      *bytes = 0;
+      return CONV2D_OK;
+    }
+  }
   if (op == CONV2D_OP_FWD || op == CONV2D_OP_BWD_DATA) {
     TapSet set;
     rc = build_tap_set(op, d, nullptr, nullptr, nullptr, nullptr, di, set, true);
@@ -1798,15 +1860,6 @@ static int run_tap(int op, const Desc& d, int groups, const void* src, const voi
   if (rc) return rc;
   const DevInfo di = device_info();
   if (!di.ok) return CONV2D_ERR_DEVICE;
-  TapSet set;
-  const PlanKey key = make_key(op, dg, src, w, dst, ws);
-  if (!g_tap_plans.get(key, set)) {
-    rc = build_tap_set(op, dg, src, w, dst, ws, di, set, true);
-    if (rc) return rc;
-    g_tap_plans.put(key, set);
-  }
-  rc = check_ws(ws, wsb, set.pack_bytes);
-  if (rc) return rc;
   if (bias != nullptr && ((uintptr_t)bias & (d.dt == CONV2D_DTYPE_F32 ? 3 : 1))) return CONV2D_ERR_ALIGN;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const size_t esz = d.dt == CONV2D_DTYPE_F32 ? 4 : 2;
@@ -1816,6 +1869,37 @@ static int run_tap(int op, const Desc& d, int groups, const void* src, const voi
   const size_t dst_g = fwd ? (size_t)dg.K * dg.P * dg.Q : (size_t)dg.C * dg.H * dg.W;
   const size_t w_g = (size_t)dg.K * dg.C * dg.R * dg.S;
   const size_t bias_g = fwd ? (size_t)dg.K : (size_t)dg.C;
+  if (!fwd) {  // few input channels: the scatter-form kernel (no workspace)
+    C2iPlan cp;
+    const PlanKey ckey = make_key(op, dg, nullptr, nullptr, nullptr, nullptr);
+    bool have = g_c2i_plans.get(ckey, cp);
+    if (!have && build_c2i(dg, src, w, dst, di, cp) == CONV2D_OK) {
+      g_c2i_plans.put(ckey, cp);
+      have = true;
+    }
+    if (have) {
+      for (int gi = 0; gi < groups; ++gi) {
+        cp.dy = byte_ptr(src) + gi * src_g * esz;
+        cp.dx = const_cast<uint8_t*>(byte_ptr(dst)) + gi * dst_g * esz;
+        cp.w = byte_ptr(w) + gi * w_g * esz;
+        cp.bias = bias != nullptr ? byte_ptr(bias) + gi * bias_g * esz : nullptr;
+        cp.beta = beta;
+        cp.flip = mode == CONV2D_MODE_CONVOLUTION ? 1 : 0;
+        rc = launch_err(launch_c2i(cp, di.sms, st));
+        if (rc) return rc;
+      }
+      return CONV2D_OK;
+    }
+  }
+  TapSet set;
+  const PlanKey key = make_key(op, dg, src, w, dst, ws);
+  if (!g_tap_plans.get(key, set)) {
+    rc = build_tap_set(op, dg, src, w, dst, ws, di, set, true);
+    if (rc) return rc;
+    g_tap_plans.put(key, set);
+  }
+  rc = check_ws(ws, wsb, set.pack_bytes);
+  if (rc) return rc;
   for (int gi = 0; gi < groups; ++gi)
     for (size_t pi = 0; pi < set.pass.size(); ++pi) {
       TapBuild& b = set.pass[pi];
@@ -2033,7 +2117,7 @@ int conv2d_bwd_filter_ex(int N, int C, int H, int W, int K, int R, int S, int pa
                     L.xs_bytes + (sums ? align_ws(partial) + chan_sum_bytes(d) : partial));
       if (rc) return rc;
       const S2dPlan sp{x, wsp, d.N, d.C, d.H, d.W, d.sh, d.sw, L.Hp, L.Wp};
-      rc = launch_err(launch_space_to_depth(sp, d.dt, st));
+      rc = launch_err(launch_space_to_depth(sp, d.dt, di.sms, st));
       if (rc) return rc;
       for (auto& phases : gp)
         for (WgradBuild& wb : phases) {
@@ -2144,9 +2228,11 @@ int conv2d_device_status(void* stream) {
   const int a = tap_gemm_take_error();
   const int b = wgrad_take_error();
   const int c = wgrad_mn_take_error();
-  if (a < 0 || b < 0 || c < 0) return CONV2D_ERR_LAUNCH;
-  if (a == DEV_ERR_LAYOUT || b == DEV_ERR_LAYOUT || c == DEV_ERR_LAYOUT) return CONV2D_ERR_LAUNCH;
-  if (a || b || c) return CONV2D_ERR_DEVICE_TIMEOUT;
+  const int e = c2i_take_error();
+  if (a < 0 || b < 0 || c < 0 || e < 0) return CONV2D_ERR_LAUNCH;
+  if (a == DEV_ERR_LAYOUT || b == DEV_ERR_LAYOUT || c == DEV_ERR_LAYOUT || e == DEV_ERR_LAYOUT)
+    return CONV2D_ERR_LAUNCH;
+  if (a || b || c || e) return CONV2D_ERR_DEVICE_TIMEOUT;
   return CONV2D_OK;
 }
 

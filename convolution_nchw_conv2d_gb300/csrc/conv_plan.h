@@ -295,6 +295,38 @@ struct WgradMnPlan {
   int tap_delta[kMaxTaps], tap_out[kMaxTaps];
 };
 
+// Backward-data for few input channels (C <= 8): the scatter form of the sum.  Every dy
+// element (k, p, q) meets filter tap (c, r, s) once and lands on dx pixel
+// (c, p*sh - ph + r*dh, q*sw - pw + s*dw), so with
+//     Z[(p, q), (c, r, s)] = sum_k dy[k, p, q] * w[k, c, r, s]
+// dx[c, h, w] is the sum of Z over the (p, q, r, s) that land on (h, w).  A tile holds 8 dy
+// rows x 32 dy columns of positions (M = 256 rows of Z, two 128-row MMAs) and computes Z for
+// N = C*R*8 columns (s padded to 8) on the tensor cores, reduction over K.  The dy rows
+// dlt_h.. and columns dlt_w.. of the tile are the ones whose dx pixels receive all their
+// contributions from inside the tile; tiles step by THp = 8 - dlt_h rows and TWq = 32 - dlt_w
+// columns.  Layouts: dy NKPQ, w KCRS, dx NCHW.
+struct C2iPlan {
+  const void* dy;
+  const void* w;
+  const void* bias;   // per c, or NULL
+  void* dx;
+  float beta;         // dx = sum + bias + beta * dx
+  int flip;           // convolution mode: the filter rotated by 180 degrees
+  int N, C, H, W, K, R, S, P, Q;
+  int sh, sw, ph, pw, dh, dw;
+  long long dy_nstride, dx_nstride;  // elements from one image to the next
+  int Npad;           // MMA N: C*R*8 rounded up to 16
+  int nkb;            // blocks of 32 dy channels (K padded with zeros)
+  int dlt_h, dlt_w;   // floor((R-1)*dh/sh), floor((S-1)*dw/sw)
+  int THp, TWq;       // owned dy rows / columns per tile
+  int p_start, q_start;  // first owned dy row / column of tile 0: floor(ph/sh), floor(pw/sw)
+  int ntp, ntq;       // tiles per image along dy rows / columns
+  long long tiles;    // N * ntp * ntq
+  int b_bytes;        // resident filter operand: (nkb*8) chunks x Npad rows x 16 bytes
+  int g_floats;       // one fold buffer: 8 rows x R x 32*sw floats
+  int tmem_cols;
+};
+
 // Space-to-depth of x for strided backward-filter: xs[n][a*sw + b][c][i][j] =
 // x[n][c][i*sh + a][j*sw + b] (zero where that lies outside x), i < Hp, j < Wp.
 struct S2dPlan {

@@ -1208,37 +1208,64 @@ cudaError_t launch_chan_sum(const ChanSumPlan& a, const ChanSumPlan& b, int dt, 
 // channel) slab per block row; threads take consecutive j, so stores are contiguous and a
 // warp's loads touch sw times its width of one input row.
 template <int DT>
-__global__ void __launch_bounds__(256) space_to_depth_kernel(const __grid_constant__ S2dPlan sp) {
+__global__ void __launch_bounds__(256) space_to_depth_kernel(const __grid_constant__ S2dPlan sp, int band,
+                                                             int nbands) {
+  // A unit is one band of `band` rows of every phase plane of one (image, channel): the
+  // band's band*sh input rows are one contiguous run, read with coalesced loads into shared
+  // memory; each phase plane's rows of the band are then written as one contiguous run.
+  extern __shared__ __align__(16) uint8_t s2d_smem[];
   using E = typename std::conditional<DT == 0, uint32_t, uint16_t>::type;
+  E* tile = reinterpret_cast<E*>(s2d_smem);
   const E* x = static_cast<const E*>(sp.x);
   E* xs = static_cast<E*>(sp.xs);
   const int npl = sp.sh * sp.sw;
-  const long long slabs = (long long)sp.N * npl * sp.C;
-  const int plane = sp.Hp * sp.Wp;
-  for (long long sl = blockIdx.y; sl < slabs; sl += gridDim.y) {
-    const int c = (int)(sl % sp.C);
-    const long long t = sl / sp.C;  // n * npl + plane index
-    const int pl = (int)(t % npl);
-    const long long n = t / npl;
-    const int a = pl / sp.sw, b = pl - (pl / sp.sw) * sp.sw;
-    const E* src = x + (n * sp.C + c) * (long long)sp.H * sp.W;
-    E* dst = xs + sl * (long long)plane;
-    for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < plane; e += gridDim.x * blockDim.x) {
-      const int i = e / sp.Wp, j = e - (e / sp.Wp) * sp.Wp;
-      const int h = i * sp.sh + a, w = j * sp.sw + b;
-      dst[e] = (h < sp.H && w < sp.W) ? src[(long long)h * sp.W + w] : E(0);
+  const long long plane = (long long)sp.Hp * sp.Wp;
+  const long long units = (long long)sp.N * sp.C * nbands;
+  for (long long u = blockIdx.x; u < units; u += gridDim.x) {
+    const int bd = (int)(u % nbands);
+    const long long nc = u / nbands;  // n * C + c
+    const int c = (int)(nc % sp.C);
+    const long long n = nc / sp.C;
+    const int i0 = bd * band;
+    const int bi = min(band, sp.Hp - i0);
+    const int h0 = i0 * sp.sh;
+    const int nh = max(0, min(bi * sp.sh, sp.H - h0));
+    const E* src = x + nc * (long long)sp.H * sp.W + (long long)h0 * sp.W;
+    for (int e = threadIdx.x; e < nh * sp.W; e += blockDim.x) tile[e] = src[e];
+    __syncthreads();
+    const int per = bi * sp.Wp;
+    for (int e = threadIdx.x; e < npl * per; e += blockDim.x) {
+      const int pl = e / per;
+      const int r = e - pl * per;
+      const int ii = r / sp.Wp, j = r - ii * sp.Wp;
+      const int a = pl / sp.sw, b = pl - a * sp.sw;
+      const int hh = ii * sp.sh + a, w = j * sp.sw + b;
+      const E v = (hh < nh && w < sp.W) ? tile[hh * sp.W + w] : E(0);
+      xs[((n * npl + pl) * sp.C + c) * plane + (long long)(i0 + ii) * sp.Wp + j] = v;
     }
+    __syncthreads();
   }
 }
 
-cudaError_t launch_space_to_depth(const S2dPlan& sp, int dt, cudaStream_t st) {
-  const long long plane = (long long)sp.Hp * sp.Wp;
-  const long long slabs = (long long)sp.N * sp.sh * sp.sw * sp.C;
-  const dim3 grid((unsigned)std::min<long long>((plane + 255) / 256, 64), (unsigned)std::min<long long>(slabs, 65535));
-  if (dt == 0)
-    space_to_depth_kernel<0><<<grid, 256, 0, st>>>(sp);
-  else
-    space_to_depth_kernel<1><<<grid, 256, 0, st>>>(sp);
+cudaError_t launch_space_to_depth(const S2dPlan& sp, int dt, int num_sms, cudaStream_t st) {
+  const int esz = dt == 0 ? 4 : 2;
+  const long long row_bytes = (long long)sp.sh * sp.W * esz;  // input bytes per band row
+  const int band = (int)std::max(1ll, std::min<long long>(sp.Hp, (16 * 1024) / std::max(1ll, row_bytes)));
+  const int nbands = (sp.Hp + band - 1) / band;
+  const size_t smem = (size_t)band * row_bytes;
+  const long long units = (long long)sp.N * sp.C * nbands;
+  const unsigned grid = (unsigned)std::max(1ll, std::min<long long>(units, (long long)num_sms * 16));
+  static std::atomic<int> set_bytes[2][kMaxDevices];
+  cudaError_t e;
+  if (dt == 0) {
+    e = ensure_dyn_smem(space_to_depth_kernel<0>, smem, set_bytes[0]);
+    if (e != cudaSuccess) return e;
+    space_to_depth_kernel<0><<<grid, 256, smem, st>>>(sp, band, nbands);
+  } else {
+    e = ensure_dyn_smem(space_to_depth_kernel<1>, smem, set_bytes[1]);
+    if (e != cudaSuccess) return e;
+    space_to_depth_kernel<1><<<grid, 256, smem, st>>>(sp, band, nbands);
+  }
   return cudaGetLastError();
 }
 

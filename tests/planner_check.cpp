@@ -518,6 +518,145 @@ void check_phase_choice(int& plans) {
 
 }  // namespace
 
+// The few-channel backward-data kernel (dgrad_c2i_kernel), run on the host exactly as it walks
+// its tiles: Z for the tile's 8 x 32 staged positions (zero outside dy), the column fold with
+// the kernel's shift codes (a lane below the shift reads its own value, as the shuffle does),
+// the row fold with its table, and the owned pixels it writes.  Checked against the definition
+//   dx[n][c][h][w] = sum over k, r, s with h = p*sh - ph + r*dh, w = q*sw - pw + s*dw of
+//                    dy[n][k][p][q] * w[k][c][r][s]   (filter rotated in convolution mode)
+// in fp64: every pixel written exactly once, with that value.  Budgets as the launch sees them.
+void check_c2i(const char* nm, const Desc& d, const DevInfo& di, int flip, int& plans) {
+  C2iPlan p;
+  if (build_c2i(d, nullptr, nullptr, nullptr, di, p) != CONV2D_OK) return;
+  ++plans;
+  if (c2i_smem_bytes(p) > di.smem_optin) fail(nm, "c2i", "shared memory over budget");
+  if (p.Npad % 16 || p.Npad > 256 || p.Npad < d.C * d.R * 8) fail(nm, "c2i", "MMA N");
+  if (p.tmem_cols > 512 || p.tmem_cols < 2 * p.Npad) fail(nm, "c2i", "TMEM columns");
+  if (p.THp < 1 || p.TWq < 1 || p.dlt_w > 7 || d.S > 8 || d.sw > 8 || d.sh * d.R > 256) fail(nm, "c2i", "fold tables");
+  const double work = (double)p.tiles * 256.0 * d.C * d.R * d.S * d.K;
+  if (work > 3e8) return;  // the emulation below is for small problems
+  const int g = d.g;
+  const long long dyn = (long long)g * d.K * d.P * d.Q, dxn = (long long)g * d.C * d.H * d.W;
+  if (p.dy_nstride != dyn || p.dx_nstride != dxn) fail(nm, "c2i", "image strides");
+  std::vector<double> dy((size_t)d.N * dyn), w((size_t)d.K * d.C * d.R * d.S);
+  unsigned long long st = 12345;
+  auto rnd = [&]() {
+    st = st * 6364136223846793005ull + 1442695040888963407ull;
+    return (double)((st >> 11) & 0xFFFFF) / 1048576.0 - 0.5;
+  };
+  for (auto& v : dy) v = rnd();
+  for (auto& v : w) v = rnd();
+  auto W_ = [&](int k, int c, int r, int s) {
+    const int rr = flip ? d.R - 1 - r : r, ss = flip ? d.S - 1 - s : s;
+    return w[(((size_t)k * d.C + c) * d.R + rr) * d.S + ss];
+  };
+  // group 0 of the batch: dy channels 0..K-1, dx channels 0..C-1
+  std::vector<double> ref((size_t)d.N * d.C * d.H * d.W, 0.0);
+  for (int n = 0; n < d.N; ++n)
+    for (int c = 0; c < d.C; ++c)
+      for (int h = 0; h < d.H; ++h)
+        for (int x = 0; x < d.W; ++x) {
+          double acc = 0;
+          for (int r = 0; r < d.R; ++r) {
+            const int a = h + d.ph - r * d.dh;
+            if (a < 0 || a % d.sh) continue;
+            const int pp = a / d.sh;
+            if (pp >= d.P) continue;
+            for (int s = 0; s < d.S; ++s) {
+              const int b = x + d.pw - s * d.dw;
+              if (b < 0 || b % d.sw) continue;
+              const int q = b / d.sw;
+              if (q >= d.Q) continue;
+              for (int k = 0; k < d.K; ++k) acc += dy[(size_t)n * dyn + ((size_t)k * d.P + pp) * d.Q + q] * W_(k, c, r, s);
+            }
+          }
+          ref[(((size_t)n * d.C + c) * d.H + h) * d.W + x] = acc;
+        }
+  std::vector<double> out(ref.size(), 0.0);
+  std::vector<int> hits(ref.size(), 0);
+  // the kernel's tables
+  std::vector<int> rtab(d.sh * d.R);
+  for (int ph = 0; ph < d.sh; ++ph)
+    for (int r = 0; r < d.R; ++r) {
+      const int dd = r * d.dh - ph;
+      rtab[ph * d.R + r] = (dd >= 0 && dd % d.sh == 0) ? dd / d.sh : -1;
+    }
+  unsigned ctab[8];
+  for (int phi = 0; phi < 8; ++phi) {
+    unsigned code = 0;
+    for (int s = 0; s < d.S; ++s) {
+      const int dd = s * d.dw - phi;
+      if (phi < d.sw && dd >= 0 && dd % d.sw == 0) code |= (8u | (unsigned)(dd / d.sw)) << (4 * s);
+    }
+    ctab[phi] = code;
+  }
+  const int GW = 32 * d.sw, TH = p.THp * d.sh, TW = p.TWq * d.sw;
+  std::vector<double> Z(256 * 8), G((size_t)8 * d.R * GW);
+  for (long long t = 0; t < p.tiles; ++t) {
+    const long long per = (long long)p.ntp * p.ntq;
+    const int n = (int)(t / per), rem = (int)(t % per);
+    const int p_lo = p.p_start + (rem / p.ntq) * p.THp - p.dlt_h;
+    const int q_lo = p.q_start + (rem % p.ntq) * p.TWq - p.dlt_w;
+    for (int c = 0; c < d.C; ++c) {
+      for (int r = 0; r < d.R; ++r) {
+        // Z for (c, r, s < 8) at the 256 staged positions
+        for (int m = 0; m < 256; ++m)
+          for (int s = 0; s < 8; ++s) {
+            double acc = 0;
+            const int pp = p_lo + m / 32, q = q_lo + m % 32;
+            if (s < d.S && pp >= 0 && pp < d.P && q >= 0 && q < d.Q)
+              for (int k = 0; k < d.K; ++k) acc += dy[(size_t)n * dyn + ((size_t)k * d.P + pp) * d.Q + q] * W_(k, c, r, s);
+            Z[m * 8 + s] = acc;
+          }
+        for (int j = 0; j < 8; ++j)
+          for (int lane = 0; lane < 32; ++lane)
+            for (int phi = 0; phi < d.sw; ++phi) {
+              double acc = 0;
+              for (int s = 0; s < 8; ++s) {
+                const unsigned code = (ctab[phi] >> (4 * s)) & 15u;
+                if (!(code & 8u)) continue;
+                const int src = lane >= (int)(code & 7u) ? lane - (int)(code & 7u) : lane;
+                acc += Z[(j * 32 + src) * 8 + s];
+              }
+              G[((size_t)j * d.R + r) * GW + lane * d.sw + phi] = acc;
+            }
+      }
+      const int h_base = (p_lo + p.dlt_h) * d.sh - d.ph, w_base = (q_lo + p.dlt_w) * d.sw - d.pw;
+      for (int hr = 0; hr < TH; ++hr) {
+        const int h = h_base + hr;
+        if (h < 0 || h >= d.H) continue;
+        const int prow0 = p.dlt_h + hr / d.sh, phh = hr % d.sh;
+        for (int wc = 0; wc < TW; ++wc) {
+          const int x = w_base + wc;
+          if (x < 0 || x >= d.W) continue;
+          const int col = p.dlt_w * d.sw + wc;
+          double acc = 0;
+          for (int r = 0; r < d.R; ++r) {
+            const int dd = rtab[phh * d.R + r];
+            if (dd >= 0) acc += G[((size_t)(prow0 - dd) * d.R + r) * GW + col];
+          }
+          const size_t o = (((size_t)n * d.C + c) * d.H + h) * d.W + x;
+          out[o] = acc;
+          ++hits[o];
+        }
+      }
+    }
+  }
+  int bad_hits = 0, bad_val = 0;
+  for (size_t i = 0; i < ref.size(); ++i) {
+    if (hits[i] != 1) ++bad_hits;
+    else if (std::fabs(out[i] - ref[i]) > 1e-9 * (1.0 + std::fabs(ref[i]))) ++bad_val;
+  }
+  if (bad_hits) {
+    std::printf("  %s c2i: %d pixels not written exactly once\n", nm, bad_hits);
+    fail(nm, "c2i", "pixel coverage");
+  }
+  if (bad_val) {
+    std::printf("  %s c2i: %d pixels differ from the definition\n", nm, bad_val);
+    fail(nm, "c2i", "folded sums differ from the definition");
+  }
+}
+
 int main() {
   using namespace cg3;
   // The last field gives the tap passes expected for forward and backward-data.  The tap GEMM
@@ -573,6 +712,15 @@ int main() {
       {"s2_9x9", 2, 3, 9, 9, 4, 3, 3, 1, 1, 2, 2, 0, 1, 1, 1, {1, 1}},
       {"s2_grp", 2, 8, 14, 13, 6, 3, 3, 1, 1, 2, 2, 1, 1, 1, 2, {1, 1}},
       {"s32_r5", 1, 40, 20, 19, 24, 5, 3, 2, 0, 2, 3, 0, 1, 1, 1, {1, 1}},
+      // few input channels: backward-data runs the scatter-form kernel where it plans
+      {"c2i_stem", 1, 3, 37, 45, 16, 7, 7, 3, 3, 2, 2, 0, 1, 1, 1, {1, 1}},
+      {"c2i_s1", 2, 1, 19, 70, 40, 3, 3, 1, 1, 1, 1, 0, 1, 1, 1, {1, 1}},
+      {"c2i_dil", 1, 2, 23, 29, 8, 3, 3, 2, 2, 1, 1, 0, 2, 2, 1, {1, 1}},
+      {"c2i_s32", 1, 4, 25, 22, 12, 5, 4, 1, 2, 3, 2, 0, 1, 1, 1, {1, 1}},
+      {"c2i_k33", 1, 3, 12, 12, 33, 3, 3, 1, 1, 1, 1, 0, 1, 1, 1, {1, 1}},
+      {"c2i_r1s8", 1, 4, 9, 40, 20, 1, 8, 0, 3, 1, 1, 0, 1, 1, 1, {1, 1}},
+      {"c2i_s4", 1, 2, 18, 37, 7, 4, 4, 0, 1, 4, 4, 0, 1, 1, 1, {1, 1}},
+      {"c2i_grp", 2, 6, 11, 13, 10, 3, 3, 1, 1, 2, 1, 0, 1, 1, 2, {1, 1}},
   };
   DevInfo di;
   di.sms = 152;
@@ -627,6 +775,8 @@ int main() {
       fail(s.nm, "bwd_filter", "no plan");
     if (rcf == CONV2D_OK && d.R * d.S > kMaxTaps) fail(s.nm, "bwd_filter", "planned past the tap tables");
     check_phases(s.nm, d, di, plans);
+    check_c2i(s.nm, d, di, 0, plans);
+    check_c2i(s.nm, d, di, 1, plans);
     Desc d16 = d;  // the channel-chunked path plans bf16 only
     d16.dt = 1;
     check_wgrad_mn(s.nm, d16, di);

@@ -119,7 +119,10 @@ def test_workspace_sizes_are_bounded(cg):
         dt = 0 if pb.dtype == "f32" else 1
         for op in (0, 1, 2):
             rc, n = _ws(cg, op, pb.dims(), dt)
-            assert rc == 0 and 0 < n <= 1_000_000_000 and n % 16 == 0
+            assert rc == 0 and 0 <= n <= 1_000_000_000 and n % 16 == 0
+            # fp32 backward-data with few input channels runs without a workspace
+            few = op == 1 and pb.dtype == "f32" and pb.C <= 8
+            assert (n == 0) == few, (wl.name, op, n)
 
 
 def test_strided_filter_gradient_workspace_stays_under_the_cap(cg):
@@ -175,4 +178,6 @@ def test_grouped_and_dilated_workspace_bounded(cg):
                               ((8, 32, 28, 28, 32, 3, 3, 1, 1, 1, 1, 28, 28), (1, 1), 32)]:
         for op in (0, 1, 2):
             rc, n = _ws_ex(cg, op, dims, dil, groups)
-            assert rc == 0 and 0 < n <= 1_000_000_000 and n % 16 == 0
+            assert rc == 0 and 0 <= n <= 1_000_000_000 and n % 16 == 0
+            # backward-data with few input channels per group runs without a workspace
+            assert (n == 0) == (op == 1 and dims[1] // groups <= 8), (dims, op, n)

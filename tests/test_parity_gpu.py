@@ -652,3 +652,50 @@ def test_fused_backward_small_bf16(cg, case):
         ref = _oracle_full(op, pb, x, w, dy)
         a, b = _operands(op, x, w, dy)
         _check(op, pb, out.double().cpu().numpy(), ref, a, b, f"{case}/fused {op}")
+
+
+# Backward-data with few input channels (C <= 8) runs the scatter-form kernel: Z = dy^T w on
+# the tensor cores for 8 x 32 dy positions per tile, folded on chip into dx.  Cases: strides,
+# dilations, halos up to the tile limits (5 dy rows, 7 dy columns), K not a multiple of the
+# 32-channel block, groups, convolution mode, bias + add-to; image edges ragged in both axes.
+C2I_CASES = [
+    # (N, C, H, W, K, R, S, ph, pw, sh, sw), (dh, dw), groups, flip, epilogue
+    ((1, 3, 37, 45, 16, 7, 7, 3, 3, 2, 2), (1, 1), 1, False, False),   # the stem's shape, small
+    ((2, 1, 19, 70, 40, 3, 3, 1, 1, 1, 1), (1, 1), 1, True, False),
+    ((1, 2, 23, 29, 8, 3, 3, 2, 2, 1, 1), (2, 2), 1, False, True),
+    ((1, 4, 25, 22, 12, 5, 4, 1, 2, 3, 2), (1, 1), 1, True, True),
+    ((3, 3, 12, 12, 33, 3, 3, 1, 1, 1, 1), (1, 1), 1, False, False),
+    ((1, 4, 9, 40, 20, 1, 8, 0, 3, 1, 1), (1, 1), 1, False, True),
+    ((1, 2, 18, 37, 7, 4, 4, 0, 1, 4, 4), (1, 1), 1, True, False),
+    ((2, 6, 11, 13, 10, 3, 3, 1, 1, 2, 1), (1, 1), 2, False, True),
+    ((1, 8, 30, 33, 64, 4, 3, 1, 1, 1, 2), (1, 1), 1, False, False),
+    ((2, 3, 64, 96, 64, 6, 7, 0, 3, 1, 1), (1, 1), 1, False, False),   # 5-row, 6-column halo
+]
+
+
+@pytest.mark.parametrize("case", C2I_CASES, ids=[f"c2i{i}" for i in range(len(C2I_CASES))])
+def test_few_channel_bwd_data_parity(cg, case):
+    (N, C, H, Wd, K, R, S, ph, pw, sh, sw), dil, groups, flip, epi = case
+    dh, dw_ = dil
+    P = (H + 2 * ph - dh * (R - 1) - 1) // sh + 1
+    Q = (Wd + 2 * pw - dw_ * (S - 1) - 1) // sw + 1
+    g = torch.Generator().manual_seed(9700 + C2I_CASES.index(case))
+    dy = torch.randn(N, K, P, Q, generator=g)
+    w = torch.randn(K, C // groups, R, S, generator=g)
+    bc = torch.randn(C, generator=g) if epi else None
+    dx0 = torch.randn(N, C, H, Wd, generator=g)
+    pad, st = (ph, pw), (sh, sw)
+    dx = dx0.to(DEV) if epi else _poisoned((N, C, H, Wd), torch.float32)
+    cg.conv2d_bwd_data(dy.to(DEV), w.to(DEV), (H, Wd), pad, st, out=dx, bias=bc.to(DEV) if epi else None,
+                       beta=0.5 if epi else 0.0, flip=flip, dilation=dil, groups=groups)
+    cg.conv2d_device_status()
+    ref = oracle.conv2d_bwd_data_ex(dy, w, (H, Wd), bc, 0.5 if epi else 0.0, dx0 if epi else None, pad, st,
+                                    flip, dil, groups)
+    pb = W.Conv2dProblem(N, C, H, Wd, K, R, S, ph, pw, sh, sw, "f32")
+    scale = float(dy.abs().max()) * float(w.abs().max())
+    _check_plain(pb, dx.double().cpu().numpy(), ref, scale, (K // groups) * R * S, f"{case}")
+    # deterministic: a second call gives the same bits
+    dx2 = dx0.to(DEV) if epi else _poisoned((N, C, H, Wd), torch.float32)
+    cg.conv2d_bwd_data(dy.to(DEV), w.to(DEV), (H, Wd), pad, st, out=dx2, bias=bc.to(DEV) if epi else None,
+                       beta=0.5 if epi else 0.0, flip=flip, dilation=dil, groups=groups)
+    assert torch.equal(dx, dx2)
