@@ -1484,11 +1484,12 @@ bool same_key(const PlanKey& a, const PlanKey& b) {
 // ranges, one pass each: the first pass applies the caller's bias and beta, the later ones
 // add onto the output (beta = 1).  Each pass has its own repacked filter in the workspace.
 
-// Backward-data for few input channels (dgrad_c2i_kernel): fp32, C <= 8, C*R <= 32, S <= 8,
-// strides <= 8, the halo within a tile (dlt_h <= 5 of 8 dy rows, dlt_w <= 7 of 32 dy
-// columns), the resident filter operand <= 64 KB.  d is the per-group descriptor.
+// Backward-data for few input channels (dgrad_c2i_kernel): fp32, C <= 8, S <= 8, strides <= 8,
+// C*sh <= 16 (the accumulator N, double-buffered in TMEM), the column halo dlt_w <= 7 of 32 dy
+// columns, the row halo dlt_h <= 5, the resident filter operand <= 64 KB, everything within
+// shared memory.  d is the per-group descriptor.
 int build_c2i(const Desc& d, const void* dy, const void* w, void* dx, const DevInfo& di, C2iPlan& p) {
-  if (d.dt != CONV2D_DTYPE_F32 || d.C > 8 || d.S > 8 || d.C * d.R > 32 || d.sh > 8 || d.sw > 8)
+  if (d.dt != CONV2D_DTYPE_F32 || d.C > 8 || d.S > 8 || d.sh > 8 || d.sw > 8 || d.C * d.sh > 16)
     return CONV2D_ERR_UNSUPPORTED;
   const int dlt_h = (d.R - 1) * d.dh / d.sh, dlt_w = (d.S - 1) * d.dw / d.sw;
   if (dlt_h > 5 || dlt_w > 7) return CONV2D_ERR_UNSUPPORTED;
@@ -1513,26 +1514,54 @@ int build_c2i(const Desc& d, const void* dy, const void* w, void* dx, const DevI
   p.dw = d.dw;
   p.dy_nstride = (long long)d.g * d.K * d.P * d.Q;
   p.dx_nstride = (long long)d.g * d.C * d.H * d.W;
-  p.Npad = round_up(d.C * d.R * 8, 16);
-  p.nkb = (d.K + 31) / 32;
+  p.Nr = round_up(d.C * d.sh * 8, 16);
+  p.nkb = (d.K + 15) / 16;
   p.dlt_h = dlt_h;
   p.dlt_w = dlt_w;
-  p.THp = 8 - dlt_h;
+  p.EH = 8 + dlt_h;
   p.TWq = 32 - dlt_w;
   p.p_start = d.ph / d.sh;
   p.q_start = d.pw / d.sw;
-  p.ntp = ceil_div_i(d.H + d.ph - p.p_start * d.sh, p.THp * d.sh);
+  p.ntp = ceil_div_i(d.H + d.ph - p.p_start * d.sh, 8 * d.sh);
   p.ntq = ceil_div_i(d.W + d.pw - p.q_start * d.sw, p.TWq * d.sw);
   p.tiles = (long long)d.N * p.ntp * p.ntq;
-  const long long bb = (long long)p.nkb * 8 * p.Npad * 16;
+  const long long bb = (long long)(dlt_h + 1) * p.nkb * 4 * p.Nr * 16;
   if (bb > 64 * 1024) return CONV2D_ERR_UNSUPPORTED;
   p.b_bytes = (int)bb;
-  p.g_floats = 8 * d.R * 32 * d.sw;
+  p.a_bytes = 4 * p.EH * 32 * 16;
   int tc = 32;
-  while (tc < 2 * p.Npad) tc <<= 1;
+  while (tc < 4 * p.Nr) tc <<= 1;
   p.tmem_cols = tc;
+  // staged operand slots: three if they fit, else two; dy boxes by tensor copies where dy's
+  // row and channel strides are 16-byte multiples: three box slots if they fit, else two
+  p.nraw = 0;
+  p.nast = 3;
+  if (c2i_smem_bytes(p) > di.smem_optin) p.nast = 2;
   if (c2i_smem_bytes(p) > di.smem_optin) return CONV2D_ERR_UNSUPPORTED;
+  p.nraw_tma = 0;
+  if (d.Q % 4 == 0 && ((long long)d.P * d.Q) % 4 == 0)
+    for (int nr = 3; nr >= 2; --nr) {
+      p.nraw = nr;
+      if (c2i_smem_bytes(p) <= di.smem_optin) {
+        p.nraw_tma = nr;
+        break;
+      }
+    }
+  p.nraw = 0;
   return CONV2D_OK;
+}
+
+// dy of one group (Q, P, K, N), fp32, box (36, EH, 16, 1) for dgrad_c2i_kernel.
+bool encode_c2i_dy_map(CUtensorMap* m, const void* dy, const C2iPlan& p) {
+  EncodeTiledFn fn = encode_tiled_fn();
+  if (!fn || ((uintptr_t)dy & 15) != 0) return false;
+  const cuuint64_t dims[4] = {(cuuint64_t)p.Q, (cuuint64_t)p.P, (cuuint64_t)p.K, (cuuint64_t)p.N};
+  const cuuint64_t strides[3] = {(cuuint64_t)p.Q * 4, (cuuint64_t)p.P * p.Q * 4, (cuuint64_t)p.dy_nstride * 4};
+  const cuuint32_t box[4] = {36u, (cuuint32_t)p.EH, 16u, 1u};
+  const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<void*>(dy), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 struct TapSet {
@@ -1885,6 +1914,8 @@ static int run_tap(int op, const Desc& d, int groups, const void* src, const voi
         cp.bias = bias != nullptr ? byte_ptr(bias) + gi * bias_g * esz : nullptr;
         cp.beta = beta;
         cp.flip = mode == CONV2D_MODE_CONVOLUTION ? 1 : 0;
+        cp.use_tma = cp.nraw_tma > 0 && encode_c2i_dy_map(&cp.tm_dy, cp.dy, cp) ? 1 : 0;
+        cp.nraw = cp.use_tma ? cp.nraw_tma : 0;
         rc = launch_err(launch_c2i(cp, di.sms, st));
         if (rc) return rc;
       }

@@ -295,17 +295,21 @@ struct WgradMnPlan {
   int tap_delta[kMaxTaps], tap_out[kMaxTaps];
 };
 
-// Backward-data for few input channels (C <= 8): the scatter form of the sum.  Every dy
-// element (k, p, q) meets filter tap (c, r, s) once and lands on dx pixel
-// (c, p*sh - ph + r*dh, q*sw - pw + s*dw), so with
-//     Z[(p, q), (c, r, s)] = sum_k dy[k, p, q] * w[k, c, r, s]
-// dx[c, h, w] is the sum of Z over the (p, q, r, s) that land on (h, w).  A tile holds 8 dy
-// rows x 32 dy columns of positions (M = 256 rows of Z, two 128-row MMAs) and computes Z for
-// N = C*R*8 columns (s padded to 8) on the tensor cores, reduction over K.  The dy rows
-// dlt_h.. and columns dlt_w.. of the tile are the ones whose dx pixels receive all their
-// contributions from inside the tile; tiles step by THp = 8 - dlt_h rows and TWq = 32 - dlt_w
-// columns.  Layouts: dy NKPQ, w KCRS, dx NCHW.
+// Backward-data for few input channels (C <= 8).  With output row phase phi_h (h = p*sh - ph +
+// phi_h) the filter rows r that reach dx row h from dy row p - d are those with
+// r*dh = d*sh + phi_h, so
+//     T[(p, q), (c, phi_h, s)] = sum over d, k of dy[k, p - d, q] * w[k, c, (d*sh + phi_h)/dh, s]
+// is a GEMM over k for every row shift d (one MMA set per shift: the shift is a whole-row
+// offset of the staged dy operand), and dx[c, p*sh - ph + phi_h, q*sw - pw + phi_w] is the
+// sum of T over the taps s that land on column phase phi_w, from columns q - (s*dw - phi_w)/sw
+// (a warp-shuffle fold).  A tile owns 8 dy "anchor" rows x (32 - dlt_w) columns and stages
+// dy rows p_lo - dlt_h .. p_lo + 7 and columns q_lo .. q_lo + 31.  Layouts: dy NKPQ, w KCRS,
+// dx NCHW.
 struct C2iPlan {
+  CUtensorMap tm_dy;  // dy (Q, P, K, N) fp32, box (36, EH, 16, 1); valid when use_tma
+  int use_tma;        // dy boxes by tensor copies (else the builders read global memory)
+  int nraw;           // dy box slots in shared memory (0 without tensor copies)
+  int nraw_tma;       // the slots a launch with tensor copies uses
   const void* dy;
   const void* w;
   const void* bias;   // per c, or NULL
@@ -315,16 +319,18 @@ struct C2iPlan {
   int N, C, H, W, K, R, S, P, Q;
   int sh, sw, ph, pw, dh, dw;
   long long dy_nstride, dx_nstride;  // elements from one image to the next
-  int Npad;           // MMA N: C*R*8 rounded up to 16
-  int nkb;            // blocks of 32 dy channels (K padded with zeros)
-  int dlt_h, dlt_w;   // floor((R-1)*dh/sh), floor((S-1)*dw/sw)
-  int THp, TWq;       // owned dy rows / columns per tile
-  int p_start, q_start;  // first owned dy row / column of tile 0: floor(ph/sh), floor(pw/sw)
-  int ntp, ntq;       // tiles per image along dy rows / columns
+  int Nr;             // MMA N: C*sh*8 ((c, phi_h, s), s padded to 8) rounded up to 16
+  int nkb;            // blocks of 16 dy channels (K padded with zeros)
+  int dlt_h, dlt_w;   // largest row shift floor((R-1)*dh/sh), column shift floor((S-1)*dw/sw)
+  int EH;             // staged dy rows: 8 + dlt_h
+  int TWq;            // owned dy columns per tile: 32 - dlt_w
+  int p_start, q_start;  // first anchor dy row / owned column of tile 0: floor(ph/sh), floor(pw/sw)
+  int ntp, ntq;       // tiles per image along dy rows (8 anchors) / columns (TWq)
   long long tiles;    // N * ntp * ntq
-  int b_bytes;        // resident filter operand: (nkb*8) chunks x Npad rows x 16 bytes
-  int g_floats;       // one fold buffer: 8 rows x R x 32*sw floats
-  int tmem_cols;
+  int b_bytes;        // filter operand: (dlt_h+1) shifts x (nkb*4) chunks x Nr rows x 16 bytes
+  int a_bytes;        // one staged operand: 4 chunks x EH*32 rows x 16 bytes
+  int nast;           // staged operand slots
+  int tmem_cols;      // two accumulators of 2 x Nr columns
 };
 
 // Space-to-depth of x for strided backward-filter: xs[n][a*sw + b][c][i][j] =

@@ -519,9 +519,10 @@ void check_phase_choice(int& plans) {
 }  // namespace
 
 // The few-channel backward-data kernel (dgrad_c2i_kernel), run on the host exactly as it walks
-// its tiles: Z for the tile's 8 x 32 staged positions (zero outside dy), the column fold with
-// the kernel's shift codes (a lane below the shift reads its own value, as the shuffle does),
-// the row fold with its table, and the owned pixels it writes.  Checked against the definition
+// its tiles: for the 8 anchor rows x 32 staged columns of a tile, T summed over the row shifts d
+// with the kernel's filter operand (tap r with r*dh = d*sh + phi_h, zero outside dy), the column
+// fold with the kernel's shift codes (a lane below the shift reads its own value, as the shuffle
+// does) and the owned pixels it writes.  Checked against the definition
 //   dx[n][c][h][w] = sum over k, r, s with h = p*sh - ph + r*dh, w = q*sw - pw + s*dw of
 //                    dy[n][k][p][q] * w[k][c][r][s]   (filter rotated in convolution mode)
 // in fp64: every pixel written exactly once, with that value.  Budgets as the launch sees them.
@@ -530,10 +531,19 @@ void check_c2i(const char* nm, const Desc& d, const DevInfo& di, int flip, int& 
   if (build_c2i(d, nullptr, nullptr, nullptr, di, p) != CONV2D_OK) return;
   ++plans;
   if (c2i_smem_bytes(p) > di.smem_optin) fail(nm, "c2i", "shared memory over budget");
-  if (p.Npad % 16 || p.Npad > 256 || p.Npad < d.C * d.R * 8) fail(nm, "c2i", "MMA N");
-  if (p.tmem_cols > 512 || p.tmem_cols < 2 * p.Npad) fail(nm, "c2i", "TMEM columns");
-  if (p.THp < 1 || p.TWq < 1 || p.dlt_w > 7 || d.S > 8 || d.sw > 8 || d.sh * d.R > 256) fail(nm, "c2i", "fold tables");
-  const double work = (double)p.tiles * 256.0 * d.C * d.R * d.S * d.K;
+  {
+    C2iPlan q = p;  // the launch with tensor copies of dy
+    q.nraw = q.nraw_tma;
+    if (c2i_smem_bytes(q) > di.smem_optin) fail(nm, "c2i", "shared memory over budget (box slots)");
+    if (p.nraw_tma != 0 && (d.Q % 4 || (d.P * d.Q) % 4 || p.nraw_tma < 2 || p.nraw_tma > 4))
+      fail(nm, "c2i", "box slots");
+  }
+  if (p.nast < 2 || p.nast > 4) fail(nm, "c2i", "operand slots");
+  if (p.Nr % 16 || p.Nr > 128 || p.Nr < d.C * d.sh * 8) fail(nm, "c2i", "MMA N");
+  if (p.tmem_cols > 512 || p.tmem_cols < 4 * p.Nr) fail(nm, "c2i", "TMEM columns");
+  if (p.TWq < 1 || p.dlt_w > 7 || d.S > 8 || d.sw > 8 || d.sh > 8 || p.EH != 8 + p.dlt_h || p.EH * 32 * 16 >= (1 << 18))
+    fail(nm, "c2i", "tile geometry");
+  const double work = (double)p.tiles * 256.0 * d.C * d.sh * 8 * (p.dlt_h + 1) * d.K;
   if (work > 3e8) return;  // the emulation below is for small problems
   const int g = d.g;
   const long long dyn = (long long)g * d.K * d.P * d.Q, dxn = (long long)g * d.C * d.H * d.W;
@@ -574,13 +584,6 @@ void check_c2i(const char* nm, const Desc& d, const DevInfo& di, int flip, int& 
         }
   std::vector<double> out(ref.size(), 0.0);
   std::vector<int> hits(ref.size(), 0);
-  // the kernel's tables
-  std::vector<int> rtab(d.sh * d.R);
-  for (int ph = 0; ph < d.sh; ++ph)
-    for (int r = 0; r < d.R; ++r) {
-      const int dd = r * d.dh - ph;
-      rtab[ph * d.R + r] = (dd >= 0 && dd % d.sh == 0) ? dd / d.sh : -1;
-    }
   unsigned ctab[8];
   for (int phi = 0; phi < 8; ++phi) {
     unsigned code = 0;
@@ -590,57 +593,50 @@ void check_c2i(const char* nm, const Desc& d, const DevInfo& di, int flip, int& 
     }
     ctab[phi] = code;
   }
-  const int GW = 32 * d.sw, TH = p.THp * d.sh, TW = p.TWq * d.sw;
-  std::vector<double> Z(256 * 8), G((size_t)8 * d.R * GW);
+  const int ngrp = d.C * d.sh;
+  auto dyv = [&](int n, int k, int pp, int q) {
+    return (pp < 0 || pp >= d.P || q < 0 || q >= d.Q) ? 0.0 : dy[(size_t)n * dyn + ((size_t)k * d.P + pp) * d.Q + q];
+  };
+  // filter operand of shift dd, group gi = c*sh + phi_h, tap s (zero where the kernel's is)
+  auto Wd = [&](int dd, int k, int gi, int s) {
+    const int c = gi / d.sh, phh = gi % d.sh;
+    const int rd = dd * d.sh + phh, r = rd / d.dh;
+    if (s >= d.S || rd % d.dh || r >= d.R) return 0.0;
+    return W_(k, c, r, s);
+  };
+  std::vector<double> T(32 * 8);
   for (long long t = 0; t < p.tiles; ++t) {
     const long long per = (long long)p.ntp * p.ntq;
     const int n = (int)(t / per), rem = (int)(t % per);
-    const int p_lo = p.p_start + (rem / p.ntq) * p.THp - p.dlt_h;
+    const int p_lo = p.p_start + (rem / p.ntq) * 8;
     const int q_lo = p.q_start + (rem % p.ntq) * p.TWq - p.dlt_w;
-    for (int c = 0; c < d.C; ++c) {
-      for (int r = 0; r < d.R; ++r) {
-        // Z for (c, r, s < 8) at the 256 staged positions
-        for (int m = 0; m < 256; ++m)
+    for (int j = 0; j < 8; ++j)
+      for (int gi = 0; gi < ngrp; ++gi) {
+        for (int lane = 0; lane < 32; ++lane)
           for (int s = 0; s < 8; ++s) {
             double acc = 0;
-            const int pp = p_lo + m / 32, q = q_lo + m % 32;
-            if (s < d.S && pp >= 0 && pp < d.P && q >= 0 && q < d.Q)
-              for (int k = 0; k < d.K; ++k) acc += dy[(size_t)n * dyn + ((size_t)k * d.P + pp) * d.Q + q] * W_(k, c, r, s);
-            Z[m * 8 + s] = acc;
+            for (int dd = 0; dd <= p.dlt_h; ++dd)
+              for (int k = 0; k < d.K; ++k) acc += dyv(n, k, p_lo + j - dd, q_lo + lane) * Wd(dd, k, gi, s);
+            T[lane * 8 + s] = acc;
           }
-        for (int j = 0; j < 8; ++j)
-          for (int lane = 0; lane < 32; ++lane)
-            for (int phi = 0; phi < d.sw; ++phi) {
-              double acc = 0;
-              for (int s = 0; s < 8; ++s) {
-                const unsigned code = (ctab[phi] >> (4 * s)) & 15u;
-                if (!(code & 8u)) continue;
-                const int src = lane >= (int)(code & 7u) ? lane - (int)(code & 7u) : lane;
-                acc += Z[(j * 32 + src) * 8 + s];
-              }
-              G[((size_t)j * d.R + r) * GW + lane * d.sw + phi] = acc;
+        const int c = gi / d.sh, phh = gi % d.sh;
+        const int h = (p_lo + j) * d.sh - d.ph + phh;
+        for (int lane = p.dlt_w; lane < 32; ++lane)
+          for (int phi = 0; phi < d.sw; ++phi) {
+            double acc = 0;
+            for (int s = 0; s < 8; ++s) {
+              const unsigned code = (ctab[phi] >> (4 * s)) & 15u;
+              if (!(code & 8u)) continue;
+              const int src = lane >= (int)(code & 7u) ? lane - (int)(code & 7u) : lane;
+              acc += T[src * 8 + s];
             }
-      }
-      const int h_base = (p_lo + p.dlt_h) * d.sh - d.ph, w_base = (q_lo + p.dlt_w) * d.sw - d.pw;
-      for (int hr = 0; hr < TH; ++hr) {
-        const int h = h_base + hr;
-        if (h < 0 || h >= d.H) continue;
-        const int prow0 = p.dlt_h + hr / d.sh, phh = hr % d.sh;
-        for (int wc = 0; wc < TW; ++wc) {
-          const int x = w_base + wc;
-          if (x < 0 || x >= d.W) continue;
-          const int col = p.dlt_w * d.sw + wc;
-          double acc = 0;
-          for (int r = 0; r < d.R; ++r) {
-            const int dd = rtab[phh * d.R + r];
-            if (dd >= 0) acc += G[((size_t)(prow0 - dd) * d.R + r) * GW + col];
+            const int x = (q_lo + lane) * d.sw - d.pw + phi;
+            if (h < 0 || h >= d.H || x < 0 || x >= d.W) continue;
+            const size_t o = (((size_t)n * d.C + c) * d.H + h) * d.W + x;
+            out[o] = acc;
+            ++hits[o];
           }
-          const size_t o = (((size_t)n * d.C + c) * d.H + h) * d.W + x;
-          out[o] = acc;
-          ++hits[o];
-        }
       }
-    }
   }
   int bad_hits = 0, bad_val = 0;
   for (size_t i = 0; i < ref.size(); ++i) {
