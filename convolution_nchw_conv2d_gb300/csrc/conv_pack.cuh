@@ -11,17 +11,33 @@
 
 namespace cg3 {
 
+__device__ __forceinline__ uint32_t comp4(const uint4& v, int i) {
+  return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
+}
+
 // Shared memory of a channel-chunk pack unit: cg * CHUNK staged channel runs of ch_pitch elements.
 inline size_t nhwc_pack_smem_bytes(const NhwcPackPlan& q, int dt) {
   return (size_t)q.cg * (dt == 0 ? 4 : 8) * q.ch_pitch * (dt == 0 ? 4 : 2);
 }
 
-// Channel-chunk pack (NhwcPackPlan), work unit v, run by a whole block: the unit's channel runs
-// are staged in shared memory (16-byte asynchronous copies when every run starts on a 16-byte
-// boundary and is whole 16-byte groups, batched element loads otherwise; channels past C are not
-// read), then each output 16-byte group is assembled from CHUNK shared-memory reads of its
-// position and stored, with consecutive threads storing consecutive groups.  `pk_smem` holds
-// nhwc_pack_smem_bytes(p) bytes.
+// Staged position slot of position `pos` within a chunk's region of the transposed staging
+// (CHUNK-aligned groups of CHUNK positions, the slot's low bits XORed with the group index:
+// consecutive lanes storing the same position of consecutive groups hit different banks).
+template <int CHUNK>
+__device__ __forceinline__ int pack_slot(int pos) {
+  return pos ^ ((pos / CHUNK) & (CHUNK - 1));
+}
+
+// Channel-chunk pack (NhwcPackPlan), work unit v, run by a whole block.  The unit's rows of
+// its channel chunks are staged in shared memory, then every output 16-byte group (CHUNK
+// channels of one plane position) is written, consecutive threads storing consecutive groups.
+// Staging, when every channel row starts on a 16-byte boundary and W is a multiple of CHUNK:
+// a thread loads a CHUNK x CHUNK block (one 16-byte load per channel: CHUNK consecutive
+// positions), transposes it in registers (bf16: byte permutes of channel pairs) and stores
+// CHUNK position-major 16-byte groups, so each output group is one 16-byte shared-memory read.
+// Otherwise: channel runs by 16-byte asynchronous copies (or batched element loads) and each
+// output group assembled from CHUNK shared-memory reads.  Channels past C are zero.
+// `pk_smem` holds nhwc_pack_smem_bytes(p) bytes.
 template <int DT>
 __device__ __forceinline__ void nhwc_pack_unit(const NhwcPackPlan& p, uint32_t v, uint8_t* pk_smem) {
   constexpr int CHUNK = DT == 0 ? 4 : 8;
@@ -39,72 +55,126 @@ __device__ __forceinline__ void nhwc_pack_unit(const NhwcPackPlan& p, uint32_t v
   const int hl = max(h_lo, 0), hh = min(h_hi, p.H - 1);
   const int nr = hh - hl + 1;                          // staged rows (none when <= 0)
   const int nchs = min(ncc * CHUNK, p.C - cc0 * CHUNK);  // staged channels
+  const long long HW = (long long)p.H * p.W;
+  const E* base = static_cast<const E*>(p.src) + (long long)n * p.src_nstride + (long long)(cc0 * CHUNK) * HW +
+                  (long long)(hl > 0 ? hl : 0) * p.W;
+  const bool tr = (p.W % CHUNK) == 0 && ((reinterpret_cast<uintptr_t>(base) | (uintptr_t)(HW * ESZ)) & 15u) == 0;
   __syncthreads();  // the previous unit's reads of shared memory are done
   if (nr > 0) {
-    const long long HW = (long long)p.H * p.W;
-    const E* base = static_cast<const E*>(p.src) + (long long)n * p.src_nstride + (long long)(cc0 * CHUNK) * HW +
-                    (long long)hl * p.W;
-    const int len = nr * p.W;  // elements per channel run
-    const bool vec =
-        ((reinterpret_cast<uintptr_t>(base) | (uintptr_t)(HW * ESZ) | (uintptr_t)(len * ESZ)) & 15u) == 0;
-    if (vec) {  // asynchronous 16-byte copies: all of a thread's copies in flight at once
-      const int g = len * ESZ / 16;  // 16-byte groups per channel run
+    const int len = nr * p.W;  // positions (elements per channel run)
+    if (tr) {
+      // transposed staging: chunk ccl's region holds ch_pitch 16-byte position slots
+      const int nblk = len / CHUNK;
       const uint32_t s0 = smem_u32(sm);
-      for (int i = (int)threadIdx.x; i < nchs * g; i += (int)blockDim.x) {
-        const int c = i / g, k = i - c * g;
-        cp_async_16(s0 + (uint32_t)((c * p.ch_pitch) * ESZ + k * 16), base + c * HW + k * (16 / ESZ), 16);
-      }
-      cp_async_commit();
-      cp_async_wait<0>();
-    } else {  // element loads, eight in flight per thread before their stores
-      const int tot = nchs * len;
-      for (int i0 = (int)threadIdx.x; i0 < tot; i0 += 8 * (int)blockDim.x) {
-        E v8[8];
+      for (int i = (int)threadIdx.x; i < ncc * nblk; i += (int)blockDim.x) {
+        const int ccl = i / nblk, b = i - ccl * nblk;
+        uint4 x[CHUNK];
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const int i = i0 + q * (int)blockDim.x;
-          if (i < tot) {
-            const int c = i / len, k = i - c * len;
-            v8[q] = base[c * HW + k];
-          }
+        for (int e = 0; e < CHUNK; ++e) {
+          const int c = ccl * CHUNK + e;
+          x[e] = c < nchs ? *reinterpret_cast<const uint4*>(base + (long long)c * HW + b * CHUNK)
+                          : make_uint4(0u, 0u, 0u, 0u);
         }
+        const uint32_t rb = s0 + (uint32_t)(ccl * p.ch_pitch) * 16u;
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const int i = i0 + q * (int)blockDim.x;
-          if (i < tot) {
-            const int c = i / len, k = i - c * len;
-            sm[c * p.ch_pitch + k] = v8[q];
+        for (int q = 0; q < CHUNK; ++q) {  // position b*CHUNK + q: CHUNK channels
+          uint32_t o[4];
+          if constexpr (DT == 0) {
+            o[0] = comp4(x[0], q);
+            o[1] = comp4(x[1], q);
+            o[2] = comp4(x[2], q);
+            o[3] = comp4(x[3], q);
+          } else {
+            const uint32_t sel = (q & 1) ? 0x7632u : 0x5410u;  // high or low halves of the pair
+#pragma unroll
+            for (int m = 0; m < 4; ++m) o[m] = __byte_perm(comp4(x[2 * m], q >> 1), comp4(x[2 * m + 1], q >> 1), sel);
+          }
+          const int slot = pack_slot<CHUNK>(b * CHUNK + q);
+          asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(rb + (uint32_t)slot * 16u), "r"(o[0]),
+                       "r"(o[1]), "r"(o[2]), "r"(o[3])
+                       : "memory");
+        }
+      }
+    } else {
+      const bool vec = ((reinterpret_cast<uintptr_t>(base) | (uintptr_t)(HW * ESZ) | (uintptr_t)(len * ESZ)) & 15u) == 0;
+      if (vec) {  // asynchronous 16-byte copies: all of a thread's copies in flight at once
+        const int g = len * ESZ / 16;  // 16-byte groups per channel run
+        const uint32_t s0 = smem_u32(sm);
+        for (int i = (int)threadIdx.x; i < nchs * g; i += (int)blockDim.x) {
+          const int c = i / g, k = i - c * g;
+          cp_async_16(s0 + (uint32_t)((c * p.ch_pitch) * ESZ + k * 16), base + c * HW + k * (16 / ESZ), 16);
+        }
+        cp_async_commit();
+        cp_async_wait<0>();
+      } else {  // element loads, eight in flight per thread before their stores
+        const int tot = nchs * len;
+        for (int i0 = (int)threadIdx.x; i0 < tot; i0 += 8 * (int)blockDim.x) {
+          E v8[8];
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const int i = i0 + q * (int)blockDim.x;
+            if (i < tot) {
+              const int c = i / len, k = i - c * len;
+              v8[q] = base[c * HW + k];
+            }
+          }
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const int i = i0 + q * (int)blockDim.x;
+            if (i < tot) {
+              const int c = i / len, k = i - c * len;
+              sm[c * p.ch_pitch + k] = v8[q];
+            }
           }
         }
       }
     }
   }
   __syncthreads();
+  // outputs (chunk ccl, plane pl, position gi of the unit's rows), flat index i; the (q, gi)
+  // split advances incrementally (no division per output)
   const int groups = ne * p.WL;  // output groups per (chunk, plane)
   const int outs = ncc * p.npl * groups;
-  for (int i = (int)threadIdx.x; i < outs; i += (int)blockDim.x) {
-    const int q = i / groups, gi = i - q * groups;
+  int i = (int)threadIdx.x;
+  int q = i / max(groups, 1), gi = i - q * groups;
+  for (; i < outs; i += (int)blockDim.x) {
     const int ccl = q / p.npl, pl = q - ccl * p.npl;
     const int de = (int)fdiv((uint32_t)gi, p.fd_WL);
     const int f = gi - de * p.WL;
     const int h = (e0 + de) * p.step_h + p.off_h[pl];
     const int w = f * p.step_w + p.off_w[pl];
-    const int nch = min(CHUNK, nchs - ccl * CHUNK);
-    uint32_t o[4] = {0u, 0u, 0u, 0u};
-    if (h >= hl && h <= hh && w >= 0 && w < p.W) {
-      const E* s0 = sm + (ccl * CHUNK) * p.ch_pitch + (h - hl) * p.W + w;
+    uint4 o = make_uint4(0u, 0u, 0u, 0u);
+    if (nr > 0 && h >= hl && h <= hh && w >= 0 && w < p.W) {
+      const int pos = (h - hl) * p.W + w;
+      if (tr) {
+        uint32_t a, b2, c2, d2;
+        const uint32_t addr =
+            smem_u32(sm) + (uint32_t)(ccl * p.ch_pitch + pack_slot<CHUNK>(pos)) * 16u;
+        asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];" : "=r"(a), "=r"(b2), "=r"(c2), "=r"(d2) : "r"(addr));
+        o = make_uint4(a, b2, c2, d2);
+      } else {
+        const int nch = min(CHUNK, nchs - ccl * CHUNK);
+        const E* s0 = sm + (ccl * CHUNK) * p.ch_pitch + pos;
+        uint32_t t[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
-      for (int c = 0; c < CHUNK; ++c) {
-        if (c < nch) {
-          const uint32_t x = (uint32_t)s0[c * p.ch_pitch];
-          if constexpr (DT == 0) o[c] = x;
-          else o[c >> 1] |= x << (16 * (c & 1));
+        for (int c = 0; c < CHUNK; ++c) {
+          if (c < nch) {
+            const uint32_t x = (uint32_t)s0[c * p.ch_pitch];
+            if constexpr (DT == 0) t[c] = x;
+            else t[c >> 1] |= x << (16 * (c & 1));
+          }
         }
+        o = make_uint4(t[0], t[1], t[2], t[3]);
       }
     }
     uint4* dst = reinterpret_cast<uint4*>(p.dst) +
                  ((((long long)pl * p.nchunk + cc0 + ccl) * p.N + n) * p.EX + e0) * p.WL + gi;
-    *dst = make_uint4(o[0], o[1], o[2], o[3]);
+    *dst = o;
+    gi += (int)blockDim.x;
+    while (gi >= groups) {
+      gi -= groups;
+      ++q;
+    }
   }
 }
 

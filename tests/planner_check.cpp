@@ -100,15 +100,35 @@ void check_pack_as_kernel(const char* nm, const char* op, const NhwcPackPlan& q)
     const int h_lo = e0 * q.step_h + q.off_h_min, h_hi = (e0 + ne - 1) * q.step_h + q.off_h_min + q.h_span;
     const int hl = std::max(h_lo, 0), hh = std::min(h_hi, q.H - 1), nr = hh - hl + 1;
     const int nchs = std::min(ncc * CHUNK, q.C - CHUNK * cc0);
+    // the kernel's transposed staging applies when every channel row starts on a 16-byte
+    // boundary (a 16-byte aligned tensor here) and W is a multiple of CHUNK
+    const long long row0 = (long long)n * q.src_nstride + (long long)(CHUNK * cc0) * HW + (long long)hl * q.W;
+    const bool tr = q.W % CHUNK == 0 && (row0 * (long long)sizeof(E)) % 16 == 0 && (HW * (long long)sizeof(E)) % 16 == 0;
+    auto slot = [&](long long pos) { return pos ^ ((pos / CHUNK) & (CHUNK - 1)); };
     if (nr > 0) {
       if ((long long)nr * q.W > q.ch_pitch) {
         fail(nm, op, "pack unit stages more rows than its channel pitch holds");
         return;
       }
-      for (int c = 0; c < nchs; ++c)
-        for (long long k = 0; k < (long long)nr * q.W; ++k)
-          sm[(size_t)c * q.ch_pitch + k] =
-              src[(size_t)(n * q.src_nstride + (long long)(CHUNK * cc0 + c) * HW + (long long)hl * q.W + k)];
+      if (tr) {  // region of chunk ccl: ch_pitch position slots of CHUNK channels
+        for (int ccl = 0; ccl < ncc; ++ccl)
+          for (long long k = 0; k < (long long)nr * q.W; ++k) {
+            const long long sl = slot(k);
+            if (sl < 0 || sl >= q.ch_pitch) {
+              fail(nm, op, "a transposed staging slot leaves its chunk's region");
+              return;
+            }
+            for (int e = 0; e < CHUNK; ++e) {
+              const int c = ccl * CHUNK + e;
+              sm[((size_t)ccl * q.ch_pitch + (size_t)sl) * CHUNK + e] =
+                  c < nchs ? src[(size_t)(row0 + (long long)c * HW + k)] : (E)0;
+            }
+          }
+      } else {
+        for (int c = 0; c < nchs; ++c)
+          for (long long k = 0; k < (long long)nr * q.W; ++k)
+            sm[(size_t)c * q.ch_pitch + k] = src[(size_t)(row0 + (long long)c * HW + k)];
+      }
     }
     for (int ccl = 0; ccl < ncc; ++ccl)
       for (int pl = 0; pl < q.npl; ++pl)
@@ -118,10 +138,15 @@ void check_pack_as_kernel(const char* nm, const char* op, const NhwcPackPlan& q)
           const int nch = std::min(CHUNK, nchs - ccl * CHUNK);
           const long long g = (((long long)pl * q.nchunk + cc0 + ccl) * q.N + n) * q.EX * q.WL + (long long)e0 * q.WL + i;
           ++wrote[(size_t)g];
-          for (int c = 0; c < CHUNK; ++c)
-            dst[(size_t)g * CHUNK + c] = (h >= hl && h <= hh && w >= 0 && w < q.W && c < nch)
-                                             ? sm[(size_t)(ccl * CHUNK + c) * q.ch_pitch + (size_t)(h - hl) * q.W + w]
-                                             : (E)0;
+          const bool in = nr > 0 && h >= hl && h <= hh && w >= 0 && w < q.W;
+          for (int c = 0; c < CHUNK; ++c) {
+            E val = (E)0;
+            if (in && tr)
+              val = sm[((size_t)ccl * q.ch_pitch + (size_t)slot((long long)(h - hl) * q.W + w)) * CHUNK + c];
+            else if (in && c < nch)
+              val = sm[(size_t)(ccl * CHUNK + c) * q.ch_pitch + (size_t)(h - hl) * q.W + w];
+            dst[(size_t)g * CHUNK + c] = val;
+          }
         }
   }
   for (int pl = 0; pl < q.npl; ++pl)
