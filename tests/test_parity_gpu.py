@@ -699,3 +699,51 @@ def test_few_channel_bwd_data_parity(cg, case):
     cg.conv2d_bwd_data(dy.to(DEV), w.to(DEV), (H, Wd), pad, st, out=dx2, bias=bc.to(DEV) if epi else None,
                        beta=0.5 if epi else 0.0, flip=flip, dilation=dil, groups=groups)
     assert torch.equal(dx, dx2)
+
+
+# Backward-filter with few input channels (fp32): the TMEM-built filter-gradient path on
+# stem-like shapes.  Cases: strides, dilation, K up to 128, groups, convolution mode, add-to
+# (beta) and both bias gradients, ragged rows; fixed-order split sums (bitwise repeatable).
+FC_CASES = [
+    # (N, C, H, W, K, R, S, ph, pw, sh, sw), (dh, dw), groups, flip, epilogue
+    ((2, 3, 32, 40, 16, 7, 7, 3, 3, 2, 2), (1, 1), 1, False, False),   # the stem's shape, small
+    ((1, 4, 20, 24, 40, 3, 3, 1, 1, 1, 1), (1, 1), 1, True, True),
+    ((1, 2, 16, 36, 9, 3, 3, 2, 2, 1, 1), (2, 2), 1, False, True),
+    ((1, 2, 12, 16, 128, 3, 3, 1, 1, 1, 1), (1, 1), 1, False, False),
+    ((2, 8, 12, 16, 12, 3, 3, 1, 1, 1, 1), (1, 1), 2, True, False),
+    ((1, 1, 9, 140, 5, 1, 5, 0, 2, 1, 1), (1, 1), 1, False, True),
+    ((3, 3, 64, 64, 64, 7, 7, 3, 3, 2, 2), (1, 1), 1, False, False),
+]
+
+
+@pytest.mark.parametrize("case", FC_CASES, ids=[f"fc{i}" for i in range(len(FC_CASES))])
+def test_few_channel_bwd_filter_parity(cg, case):
+    (N, C, H, Wd, K, R, S, ph, pw, sh, sw), dil, groups, flip, epi = case
+    dh, dw_ = dil
+    P = (H + 2 * ph - dh * (R - 1) - 1) // sh + 1
+    Q = (Wd + 2 * pw - dw_ * (S - 1) - 1) // sw + 1
+    g = torch.Generator().manual_seed(9800 + FC_CASES.index(case))
+    x = torch.randn(N, C, H, Wd, generator=g)
+    dy = torch.randn(N, K, P, Q, generator=g)
+    dw0 = torch.randn(K, C // groups, R, S, generator=g)
+    pad, st = (ph, pw), (sh, sw)
+    beta = 0.5 if epi else 0.0
+    dw = dw0.to(DEV) if epi else _poisoned((K, C // groups, R, S), torch.float32)
+    dbk = torch.zeros(K, device=DEV) if epi else None
+    dbc = torch.zeros(C, device=DEV) if epi else None
+    cg.conv2d_bwd_filter(x.to(DEV), dy.to(DEV), (R, S), pad, st, out=dw, beta=beta, flip=flip, dilation=dil,
+                         groups=groups, db_k=dbk, db_c=dbc)
+    cg.conv2d_device_status()
+    ref = oracle.conv2d_bwd_filter_ex(x, dy, (R, S), beta, dw0 if epi else None, pad, st, flip, dil, groups)
+    pb = W.Conv2dProblem(N, C, H, Wd, K, R, S, ph, pw, sh, sw, "f32")
+    scale = float(x.abs().max()) * float(dy.abs().max())
+    _check_plain(pb, dw.double().cpu().numpy(), ref, scale, N * P * Q, f"{case}")
+    if epi:
+        _check_plain(pb, dbk.double().cpu().numpy(), oracle.channel_sum(dy), float(dy.abs().max()), N * P * Q,
+                     f"{case}/db_k")
+        _check_plain(pb, dbc.double().cpu().numpy(), oracle.channel_sum(x), float(x.abs().max()), N * H * Wd,
+                     f"{case}/db_c")
+    dw2 = dw0.to(DEV) if epi else _poisoned((K, C // groups, R, S), torch.float32)
+    cg.conv2d_bwd_filter(x.to(DEV), dy.to(DEV), (R, S), pad, st, out=dw2, beta=beta, flip=flip, dilation=dil,
+                         groups=groups)
+    assert torch.equal(dw, dw2)  # deterministic (fixed-order split sums)
