@@ -1525,6 +1525,7 @@ int build_c2i(const Desc& d, const void* dy, const void* w, void* dx, const DevI
   p.ntp = ceil_div_i(d.H + d.ph - p.p_start * d.sh, 8 * d.sh);
   p.ntq = ceil_div_i(d.W + d.pw - p.q_start * d.sw, p.TWq * d.sw);
   p.tiles = (long long)d.N * p.ntp * p.ntq;
+  if ((long long)p.ntp * p.ntq >= (1ll << 31)) return CONV2D_ERR_UNSUPPORTED;  // per-image tile index in 32 bits
   const long long bb = (long long)(dlt_h + 1) * p.nkb * 4 * p.Nr * 16;
   if (bb > 64 * 1024) return CONV2D_ERR_UNSUPPORTED;
   p.b_bytes = (int)bb;
