@@ -166,6 +166,7 @@ struct TapBuild {
 
 bool setup_pack_tiles(NhwcPackPlan& q, int esz);
 bool encode_mn_map(CUtensorMap* m, const void* base, int rank, const uint64_t* dims, const uint32_t* box);
+bool encode_tap_src_map(TapPlan& p, const void* base, int nchunk, int npl, int dt);
 
 // MMA operand offsets of every tap within a pipeline stage, in 16-byte units, once the tile
 // shape (NCH channel chunks of `rows` rows per plane, NT filter rows per chunk) is fixed.  A
@@ -261,6 +262,11 @@ bool choose_tap_tiles(TapPlan& p, int max_off, int dt, const DevInfo& di, bool p
         p.a_tma = a_tma ? 1 : 0;
         p.a_box = box;
         p.a_nbox = nbox;
+        // One copy per stage for stages of several planes (stride-phase planes of the forward
+        // op), where it replaced 8 copies and measured faster; single-plane stages keep the
+        // copies of a_box rows (one copy measured no faster there).  A box is at most 256 in
+        // every dimension.
+        p.a_one = a_tma && !p.plane_per_phase && p.npl > 1 && rows <= 256 ? 1 : 0;
         p.a_stage_bytes = (int)a_bytes;
         p.b_stage_bytes = (int)b_bytes;
         p.stages = (int)stages;
@@ -1171,13 +1177,15 @@ std::vector<MnPhase> mn_phases(int R, int pad, int st, int dil) {
   return v;
 }
 
-// Packed planes as tensors of 8-byte elements, two per position: dims[0] = 2 * positions
-// (contiguous), then chunks (and planes); the box's first dim is a run of positions.
+// Packed planes as dense tensors of 8-byte elements (rank 1 to 4, dims[0] contiguous), two per
+// position: either dims[0] = 2 * positions, then chunks (and planes), the box's first dim a run
+// of positions; or dims = (2, positions, chunks, planes), the box a run of whole positions.
 bool encode_mn_map(CUtensorMap* m, const void* base, int rank, const uint64_t* dims, const uint32_t* box) {
   EncodeTiledFn fn = encode_tiled_fn();
   if (!fn) return false;
-  cuuint64_t gd[3], gs[2];
-  cuuint32_t bx[3], es[3] = {1u, 1u, 1u};
+  if (rank < 1 || rank > 4) return false;
+  cuuint64_t gd[4], gs[3];
+  cuuint32_t bx[4], es[4] = {1u, 1u, 1u, 1u};
   uint64_t stride = 8;  // bytes per element
   for (int i = 0; i < rank; ++i) {
     gd[i] = dims[i];
@@ -1189,6 +1197,23 @@ bool encode_mn_map(CUtensorMap* m, const void* base, int rank, const uint64_t* d
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
+}
+
+// The tap GEMM's view of packed source planes at `base` (nchunk chunks, npl planes, p.Mtot
+// positions each), in the form the plan's producers copy it: with a_one, (2, positions, chunks,
+// planes) and a box of every row, chunk and plane of a stage; else (2 * positions, chunks,
+// planes) and a box of a_box rows.  Every encode of p.tm_src goes through here, so the map and
+// the copies the kernel issues always agree.
+bool encode_tap_src_map(TapPlan& p, const void* base, int nchunk, int npl, int dt) {
+  if (p.a_one) {
+    const uint64_t dims[4] = {2, (uint64_t)p.Mtot, (uint64_t)nchunk, (uint64_t)npl};
+    const uint32_t box[4] = {2u, (uint32_t)p.rows, (uint32_t)(p.CB / (dt == 0 ? 4 : 8)),
+                             p.plane_per_phase ? 1u : (uint32_t)npl};
+    return encode_mn_map(&p.tm_src, base, 4, dims, box);
+  }
+  const uint64_t dims[3] = {2 * (uint64_t)p.Mtot, (uint64_t)nchunk, (uint64_t)npl};
+  const uint32_t box[3] = {2 * (uint32_t)p.a_box, 1u, 1u};
+  return encode_mn_map(&p.tm_src, base, 3, dims, box);
 }
 
 // Work-unit tiling of a pack (NhwcPackPlan): the most padded rows per unit whose staged channel
@@ -1597,9 +1622,7 @@ int build_tap_set(int op, const Desc& d, const void* src, const void* w, void* d
       off = xoff + b.src_pack_bytes;
       b.px.dst = ws != nullptr ? static_cast<void*>(static_cast<uint8_t*>(ws) + xoff) : nullptr;
       if (ws != nullptr) {  // sizing calls pass no workspace
-        const uint64_t dims[3] = {2 * (uint64_t)b.p.Mtot, (uint64_t)b.px.nchunk, (uint64_t)b.px.npl};
-        const uint32_t box[3] = {2 * (uint32_t)b.p.a_box, 1u, 1u};
-        if (!encode_mn_map(&b.p.tm_src, b.px.dst, 3, dims, box)) return CONV2D_ERR_UNSUPPORTED;
+        if (!encode_tap_src_map(b.p, b.px.dst, b.px.nchunk, b.px.npl, d.dt)) return CONV2D_ERR_UNSUPPORTED;
       }
     }
     if (rc == CONV2D_OK) {
@@ -1801,9 +1824,7 @@ int build_fused_bwd(const Desc& d, const void* x, const void* w, const void* dy,
       f.fused = true;
       f.need = f.tap_off + b.pack_bytes;
       if (ws != nullptr) {  // the backward-data copies read the backward-filter plan's dy pack
-        const uint64_t dims[3] = {2 * (uint64_t)b.p.Mtot, (uint64_t)q.nchunk, 1};
-        const uint32_t box[3] = {2 * (uint32_t)b.p.a_box, 1u, 1u};
-        if (!encode_mn_map(&f.set.pass[0].p.tm_src, q.dst, 3, dims, box)) return CONV2D_ERR_UNSUPPORTED;
+        if (!encode_tap_src_map(f.set.pass[0].p, q.dst, q.nchunk, 1, d.dt)) return CONV2D_ERR_UNSUPPORTED;
       }
       return CONV2D_OK;
     }

@@ -63,6 +63,9 @@ struct TapPlan {
   CUtensorMap tm_src;
   int a_tma;             // 1: staged rows come from tm_src (rows = a_nbox * a_box)
   int a_box, a_nbox;
+  int a_one;             // 1 (rows <= 256): tm_src views the planes as (2, L, chunk, plane) and
+                         // one copy of box (2, rows, NCH, planes of the stage) stages them all;
+                         // 0: one copy per (plane, chunk, box of a_box rows) of the view above
   int plane_per_phase;   // 1 (with a_tma, one plane): phase ph reads the plane shifted by
                          // ph_shift[ph] positions, so a stage holds the tile's phase window alone
   int ph_shift[kMaxPhases];

@@ -267,11 +267,15 @@ __global__ void __launch_bounds__(kThreads, 1) tap_gemm_kernel(const __grid_cons
             // shift per phase, the plane's rows from the tile's phase origin (a negative start
             // reads zeros)
             const long long l0 = m0 + (p.plane_per_phase ? p.ph_shift[tc.ph] : 0);
-            for (int pl = 0; pl < p.npl; ++pl)
-              for (int j = 0; j < NCH; ++j)
-                for (int bx = 0; bx < p.a_nbox; ++bx)
-                  tma_load_3d(a_st + (uint32_t)(((pl * NCH + j) * rows + bx * p.a_box) * 16), &p.tm_src,
-                              (int)(2 * (l0 + (long long)bx * p.a_box)), kb * NCH + j, pl, bar_at(full, stage));
+            if (p.a_one) {  // every plane and chunk of the stage in one copy, [plane][chunk][row]
+              tma_load_4d(a_st, &p.tm_src, 0, (int)l0, kb * NCH, 0, bar_at(full, stage));
+            } else {
+              for (int pl = 0; pl < p.npl; ++pl)
+                for (int j = 0; j < NCH; ++j)
+                  for (int bx = 0; bx < p.a_nbox; ++bx)
+                    tma_load_3d(a_st + (uint32_t)(((pl * NCH + j) * rows + bx * p.a_box) * 16), &p.tm_src,
+                                (int)(2 * (l0 + (long long)bx * p.a_box)), kb * NCH + j, pl, bar_at(full, stage));
+            }
           }
           last_copy[stage] = 1 + (int)ephase;
         }

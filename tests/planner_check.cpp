@@ -60,6 +60,13 @@ void check_tap(const char* nm, const char* op, const TapBuild& b, const DevInfo&
     // transaction count; copy coordinates (2 per position) within 32 bits
     if (p.rows != p.a_nbox * p.a_box || p.a_box % 8 || p.a_box < 8 || p.a_box > 128)
       fail(nm, op, "tensor-copy boxes do not tile the staged rows");
+    // one copy per stage: box (2, rows, NCH, planes of the stage), every dimension at most 256,
+    // exactly the stage's A bytes
+    const long long planes = p.plane_per_phase ? 1 : p.npl;
+    if (p.a_one != (!p.plane_per_phase && p.npl > 1 && p.rows <= 256 ? 1 : 0)) fail(nm, op, "one-copy staging choice");
+    if (p.a_one && (planes > 256 || (long long)p.a_stage_bytes % (16ll * p.rows * planes) != 0 ||
+                    (long long)p.a_stage_bytes / (16ll * p.rows * planes) > 256))
+      fail(nm, op, "one-copy box beyond the copy limits or the stage");
     if ((long long)p.a_stage_bytes + p.b_stage_bytes >= (1 << 20)) fail(nm, op, "stage bytes over the barrier limit");
     if (2 * (p.Mtot + p.rows) >= (1ll << 31)) fail(nm, op, "copy coordinates beyond 32 bits");
     const NhwcPackPlan& q = b.px;

@@ -216,6 +216,56 @@ def test_small_parity(cg, case, op, dtype):
     _check(op, pb, out.double().cpu().numpy(), ref, a, b, f"{case}/{op}/{dtype}")
 
 
+# ------------------------------------------------------------------ wide bf16 layers
+# bf16 layers with 256 or more destination channels, whose filter slice is most of a stage (tiles
+# of 256 destination channels, tap-pair stages): an odd m-tile count, a ragged second
+# destination-channel tile, stride phases on both ops.
+WIDE_CASES = [
+    # N, C, H, W, K, R, S, ph, pw, sh, sw
+    (4, 16, 16, 16, 256, 4, 4, 1, 1, 2, 2),   # forward, 3 m-tiles
+    (4, 256, 16, 16, 16, 4, 4, 1, 1, 2, 2),   # backward-data, 4 output phases
+    (3, 8, 20, 18, 272, 3, 3, 1, 1, 1, 1),    # forward, K = 272: a ragged second tile
+    (6, 272, 14, 14, 8, 4, 4, 1, 1, 2, 2),    # backward-data, C = 272
+]
+
+
+@pytest.mark.parametrize("case", WIDE_CASES)
+@pytest.mark.parametrize("op", ["fwd", "bwd_data"])
+def test_wide_bf16_parity(cg, case, op):
+    N, C, H, Wd, K, R, S, ph, pw, sh, sw = case
+    pb = W.Conv2dProblem(N, C, H, Wd, K, R, S, ph, pw, sh, sw, "bf16")
+    x, w, dy = W.random_problem_inputs(pb, 7600 + WIDE_CASES.index(case))
+    out = _run(cg, op, pb, x.to(DEV), w.to(DEV), dy.to(DEV))
+    assert not torch.isnan(out).any().item()
+    ref = _oracle_full(op, pb, x, w, dy)
+    a, b = _operands(op, x, w, dy)
+    _check(op, pb, out.double().cpu().numpy(), ref, a, b, f"wide {case}/{op}")
+
+
+@pytest.mark.parametrize("case", WIDE_CASES[:2])
+def test_wide_bf16_fused_epilogue(cg, case):
+    """The fused epilogue (bias and add-to) on the wide bf16 layers, both ops."""
+    N, C, H, Wd, K, R, S, ph, pw, sh, sw = case
+    pb = W.Conv2dProblem(N, C, H, Wd, K, R, S, ph, pw, sh, sw, "bf16")
+    x, w, dy = W.random_problem_inputs(pb, 7700 + WIDE_CASES.index(case))
+    g = torch.Generator().manual_seed(7800 + WIDE_CASES.index(case))
+    bk = torch.randn(K, generator=g).to(torch.bfloat16)
+    bc = torch.randn(C, generator=g).to(torch.bfloat16)
+    y0 = torch.randn(pb.y_shape, generator=g).to(torch.bfloat16)
+    dx0 = torch.randn(pb.x_shape, generator=g).to(torch.bfloat16)
+    pad, st = (ph, pw), (sh, sw)
+    amax = lambda t: float(t.abs().max())
+    y = y0.to(DEV)
+    cg.conv2d_fwd(x.to(DEV), w.to(DEV), pad, st, out=y, bias=bk.to(DEV), beta=1.0)
+    dx = dx0.to(DEV)
+    cg.conv2d_bwd_data(dy.to(DEV), w.to(DEV), (H, Wd), pad, st, out=dx, bias=bc.to(DEV), beta=0.5)
+    cg.conv2d_device_status()
+    _check_plain(pb, y.double().cpu().numpy(), oracle.conv2d_fwd_ex(x, w, bk, 1.0, y0, pad, st),
+                 amax(x) * amax(w), C * R * S, f"wide {case}/fwd_ex")
+    _check_plain(pb, dx.double().cpu().numpy(), oracle.conv2d_bwd_data_ex(dy, w, (H, Wd), bc, 0.5, dx0, pad, st),
+                 amax(dy) * amax(w), K * R * S, f"wide {case}/bwd_data_ex")
+
+
 def test_deconv_alias_matches_oracle_scatter(cg):
     """deconv2d_fwd (= backward-data with the weight read as (in, out, R, S)) against
     the oracle's independent scatter-form transposed convolution."""
