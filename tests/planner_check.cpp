@@ -890,6 +890,26 @@ int main() {
   // today (a smaller m-tile group and dilated stride phases would plan them); pin the count so
   // that a change shows here.
   if (refused > 21) fail("random sweep", "bwd_filter", "more refusals than expected");
+  // The GPU parity test's two-half-tile bf16 layer (64 x 16 x 64 x 64, K = 64, 3x3 / 2) plans
+  // 256-row tiles over four stride-phase planes whose 312 staged rows take one copy per plane and
+  // box; the deconvolution forward stages its four planes with one copy.
+  {
+    auto fwd_plan = [&](int N, int C, int H, int W, int K, int R, int S, int pd, int sd, TapSet& set) {
+      Desc d{};
+      d.N = N; d.C = C; d.H = H; d.W = W; d.K = K; d.R = R; d.S = S;
+      d.ph = pd; d.pw = pd; d.sh = sd; d.sw = sd; d.dt = 1;
+      d.P = out_dim(d.H, d.ph, d.R, d.sh);
+      d.Q = out_dim(d.W, d.pw, d.S, d.sw);
+      return build_tap_set(CONV2D_OP_FWD, d, (void*)0x100000, (void*)0x200000, (void*)0x300000, (void*)0x400000,
+                           di, set, true);
+    };
+    TapSet a, b;
+    if (fwd_plan(64, 16, 64, 64, 64, 3, 3, 1, 2, a) != CONV2D_OK || a.pass.size() != 1 || a.pass[0].p.MH != 2 ||
+        a.pass[0].p.npl != 4 || a.pass[0].p.a_one != 0 || !a.pass[0].p.a_tma)
+      fail("two-half", "fwd", "expected 256-row tiles staged by one copy per plane and box");
+    if (fwd_plan(32, 256, 32, 32, 512, 4, 4, 1, 2, b) != CONV2D_OK || b.pass.size() != 1 || b.pass[0].p.a_one != 1)
+      fail("deconv", "fwd", "expected one copy per stage");
+  }
   std::printf("checked %d plans, %d backward-filter refusals, %d violations\n", plans, refused, g_fail);
   return g_fail > 100 ? 100 : g_fail;
 }

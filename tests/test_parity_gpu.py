@@ -242,6 +242,19 @@ def test_wide_bf16_parity(cg, case, op):
     _check(op, pb, out.double().cpu().numpy(), ref, a, b, f"wide {case}/{op}")
 
 
+@pytest.mark.parametrize("op", ["fwd", "bwd_data"])
+def test_bf16_strided_two_half_tiles(cg, op):
+    """A bf16 stride-2 layer large enough for 256-row tiles (two accumulator halves), whose
+    staged rows (312 per plane) exceed one copy's box: the forward stages its four stride-phase
+    planes with one copy per plane and box of rows."""
+    pb = W.Conv2dProblem(64, 16, 64, 64, 64, 3, 3, 1, 1, 2, 2, "bf16")
+    x, w, dy = W.random_problem_inputs(pb, 7900)
+    out = _run(cg, op, pb, x.to(DEV), w.to(DEV), dy.to(DEV))
+    assert not torch.isnan(out).any().item()
+    a, b = _operands(op, x, w, dy)
+    _check(op, pb, out.double().cpu().numpy(), _oracle_full(op, pb, x, w, dy), a, b, f"two-half {op}")
+
+
 @pytest.mark.parametrize("case", WIDE_CASES[:2])
 def test_wide_bf16_fused_epilogue(cg, case):
     """The fused epilogue (bias and add-to) on the wide bf16 layers, both ops."""
