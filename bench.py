@@ -328,8 +328,29 @@ def _extras_resnet(c, flush, stream, reps, warmup, op_ms):
         ms = _time_call(gcalls[op], flush, stream, reps, warmup)
         grouped[op] = {"ms": round(ms, 5), "tflops": round(pb.flops() / 2 / (ms * 1e-3) / 1e12, 2)}
     grouped["note"] = "same layer with groups 2 (C/2 -> K/2 per group, half the FLOP)"
+    # depthwise on the same layer (groups = C = K = 64: one 3x3 filter per channel; memory
+    # bound, so the rate is the op's algorithmic bytes against the HBM peak)
+    wdw = w[:, :1].contiguous()
+    wsz_w = max(cg.conv2d_workspace_size(op, pb.dims(), dt, (1, 1), pb.C) for op in range(3))
+    ws_w = torch.empty(max(wsz_w, 16), dtype=torch.uint8, device=dev)
+    dww = torch.empty_like(wdw)
+    wcalls = {"fwd": lambda: cg.conv2d_fwd(x, wdw, pad, st, out=y, workspace=ws_w, stream=stream, groups=pb.C),
+              "bwd_data": lambda: cg.conv2d_bwd_data(dy, wdw, (pb.H, pb.W), pad, st, out=dx, workspace=ws_w,
+                                                     stream=stream, groups=pb.C),
+              "bwd_filter": lambda: cg.conv2d_bwd_filter(x, dy, (pb.R, pb.S), pad, st, out=dww, workspace=ws_w,
+                                                         stream=stream, groups=pb.C)}
+    eb = pb.elem_bytes()
+    io = {"fwd": math.prod(pb.x_shape) + math.prod(pb.y_shape), "bwd_data": math.prod(pb.y_shape) + math.prod(pb.x_shape),
+          "bwd_filter": math.prod(pb.x_shape) + math.prod(pb.y_shape)}
+    depthwise = {}
+    for op in OPS:
+        ms = _time_call(wcalls[op], flush, stream, reps, warmup)
+        gbs = io[op] * eb / (ms * 1e-3) / 1e9
+        depthwise[op] = {"ms": round(ms, 5), "alg_gbs": round(gbs, 1)}
+    depthwise["note"] = ("same layer depthwise (groups = C = 64, filter 64 x 1 x 3 x 3); alg bytes = the two "
+                         "activation tensors of the op (the filter is 2.3 KB)")
     cg.conv2d_device_status(stream)
-    return fused, dilated, grouped
+    return fused, dilated, grouped, depthwise
 
 
 def _e2e(c, flush, stream, nsteps):
@@ -476,9 +497,9 @@ def run_ours(args, rank, world):
     if "resnet3x3" in W.WORKLOADS:
         rc = head if wl.name == "resnet3x3" else _device_case(W.WORKLOADS["resnet3x3"], dev)
         rms = per_config["resnet3x3"]["per_op"]
-        fused, dilated, grouped = _extras_resnet(rc, flush, stream, reps, args.warmup,
+        fused, dilated, grouped, depthwise = _extras_resnet(rc, flush, stream, reps, args.warmup,
                                                  {op: rms[op]["ms"] for op in OPS})
-        extras.update({"fused_epilogue": fused, "dilation_2": dilated, "groups_2": grouped})
+        extras.update({"fused_epilogue": fused, "dilation_2": dilated, "groups_2": grouped, "depthwise": depthwise})
 
     e2e_ms = _e2e(head, flush, stream, max(1, args.e2e_steps))
     esz = pb.elem_bytes()

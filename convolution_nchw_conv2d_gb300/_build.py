@@ -17,7 +17,7 @@ INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libconv2d_gb300.so")
 
-SOURCES = ["conv_tap_gemm.cu", "conv_wgrad.cu", "conv_wgrad_mn.cu", "conv_dgrad_c2i.cu", "conv3d_copy.cu", "conv2d_api.cpp",
+SOURCES = ["conv_tap_gemm.cu", "conv_wgrad.cu", "conv_wgrad_mn.cu", "conv_dgrad_c2i.cu", "conv_depthwise.cu", "conv3d_copy.cu", "conv2d_api.cpp",
            "conv3d_api.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

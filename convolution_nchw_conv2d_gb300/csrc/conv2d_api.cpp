@@ -18,6 +18,9 @@
 namespace cg3 {
 cudaError_t launch_tap_gemm(const TapPlan& p, int dt, int grid, cudaStream_t st);
 cudaError_t launch_pack_filter(const PackPlan& pp, int dt, cudaStream_t st);
+cudaError_t launch_dw_fwd(const DwPlan& p, int dt, int num_sms, cudaStream_t st);
+cudaError_t launch_dw_bwd_data(const DwPlan& p, int dt, int num_sms, cudaStream_t st);
+cudaError_t launch_dw_bwd_filter(const DwPlan& p, int dt, int num_sms, cudaStream_t st);
 size_t tap_gemm_smem_bytes(const TapPlan& p);
 cudaError_t launch_wgrad(const WgradPlan& p, int dt, int grid, cudaStream_t st);
 cudaError_t launch_wgrad_reduce(const ReducePlan& rp, int dt, int num_sms, cudaStream_t st);
@@ -101,6 +104,27 @@ int group_desc(const Desc& d, int groups, Desc& dg) {
 }
 
 const uint8_t* byte_ptr(const void* p) { return static_cast<const uint8_t*>(p); }
+
+// Depthwise layers (groups > 1 with one input channel per group) run the direct kernels of
+// conv_depthwise.cu (DwPlan) instead of one tap-GEMM pass per group.
+bool is_depthwise(const Desc& dg) { return dg.g > 1 && dg.C == 1; }
+
+// The depthwise plan of a whole grouped problem (d: the totals; dg: its per-group descriptor);
+// pointers, bias, beta and mode are set by the caller.  The filter gradient's splits are ranges
+// of images, enough (K * splits blocks) to fill two waves of the SMs.
+DwPlan dw_plan(const Desc& d, const Desc& dg, int sms) {
+  DwPlan p;
+  std::memset(&p, 0, sizeof(p));
+  p.N = d.N; p.C = d.C; p.H = d.H; p.W = d.W; p.K = d.K; p.R = d.R; p.S = d.S; p.P = d.P; p.Q = d.Q;
+  p.ph = d.ph; p.pw = d.pw; p.sh = d.sh; p.sw = d.sw; p.dh = d.dh; p.dw = d.dw;
+  p.M = dg.K;
+  const int want = std::max(1, (2 * sms + d.K - 1) / d.K);
+  p.n_per_split = std::max(1, (d.N + want - 1) / want);
+  p.nsplit = (d.N + p.n_per_split - 1) / p.n_per_split;
+  return p;
+}
+
+size_t dw_partial_bytes(const DwPlan& p) { return (size_t)p.nsplit * p.K * p.R * p.S * sizeof(float); }
 
 struct DevInfo {
   int sms = kDefaultSMs;
@@ -1837,6 +1861,13 @@ PlanCache<FusedBwd> g_fused_plans;
 int workspace_size_uncached(int op, const Desc& d, size_t* bytes) {
   int rc;
   const DevInfo di = device_info();
+  if (is_depthwise(d) && op != CONV2D_OP_BWD) {  // d: the per-group descriptor (d.g groups)
+    Desc t = d;
+    t.C = d.C * d.g;
+    t.K = d.K * d.g;
+    *bytes = op == CONV2D_OP_BWD_FILTER ? align_ws(dw_partial_bytes(dw_plan(t, d, di.sms))) + chan_sum_bytes(d) : 0;
+    return CONV2D_OK;
+  }
   if (op == CONV2D_OP_BWD) {
     FusedBwd f;
     rc = build_fused_bwd(d, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, di, f);
@@ -1920,6 +1951,16 @@ static int run_tap(int op, const Desc& d, int groups, const void* src, const voi
   const size_t dst_g = fwd ? (size_t)dg.K * dg.P * dg.Q : (size_t)dg.C * dg.H * dg.W;
   const size_t w_g = (size_t)dg.K * dg.C * dg.R * dg.S;
   const size_t bias_g = fwd ? (size_t)dg.K : (size_t)dg.C;
+  if (is_depthwise(dg)) {  // direct kernels, every group in one launch, no workspace
+    DwPlan dp = dw_plan(d, dg, di.sms);
+    (fwd ? dp.x : dp.dy) = src;
+    dp.w = w;
+    dp.out = dst;
+    dp.bias = bias;
+    dp.beta = beta;
+    dp.flip = mode == CONV2D_MODE_CONVOLUTION ? 1 : 0;
+    return launch_err(fwd ? launch_dw_fwd(dp, d.dt, di.sms, st) : launch_dw_bwd_data(dp, d.dt, di.sms, st));
+  }
   if (!fwd) {  // few input channels: the scatter-form kernel (no workspace)
     C2iPlan cp;
     const PlanKey ckey = make_key(op, dg, nullptr, nullptr, nullptr, nullptr);
@@ -2101,10 +2142,27 @@ int conv2d_bwd_filter_ex(int N, int C, int H, int W, int K, int R, int S, int pa
   const size_t esz = d.dt == CONV2D_DTYPE_F32 ? 4 : 2;
   size_t sum0 = 0;
   bool phases_run = false;
+  // Depthwise: the direct partial sums over image ranges and their fixed-order reduce.
+  if (is_depthwise(dg)) {
+    DwPlan dp = dw_plan(d, dg, di.sms);
+    dp.x = x;
+    dp.dy = dy;
+    dp.out = dw;
+    dp.beta = beta;
+    dp.flip = mode == CONV2D_MODE_CONVOLUTION ? 1 : 0;
+    const size_t part = align_ws(dw_partial_bytes(dp));
+    rc = check_ws(workspace, workspace_bytes, part + (sums ? chan_sum_bytes(d) : 0));
+    if (rc) return rc;
+    dp.partial = static_cast<float*>(workspace);
+    rc = launch_err(launch_dw_bwd_filter(dp, d.dt, di.sms, st));
+    if (rc) return rc;
+    sum0 = part;
+    phases_run = true;  // (the other paths below are skipped)
+  }
   // bf16: x and dy packed into channel-chunked planes, then one tensor-copy-fed GEMM and the
   // fixed-order reduce.  One plan serves every group (its tensor maps address the workspace);
   // each group packs its own slices into the workspace in stream order.
-  if (d.dt == CONV2D_DTYPE_BF16 && workspace != nullptr) {
+  if (!phases_run && d.dt == CONV2D_DTYPE_BF16 && workspace != nullptr) {
     MnBuild mb;
     const PlanKey key = make_key(kMnKey, dg, nullptr, nullptr, nullptr, workspace);
     bool have = g_mn_plans.get(key, mb);

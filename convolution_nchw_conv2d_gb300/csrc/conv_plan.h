@@ -356,4 +356,29 @@ struct ChanSumPlan {
   int ipb, nblk;         // images per block; blocks per channel = ceil(N / ipb)
 };
 
+// Depthwise layers (one input channel per group: groups == C, M = K / C output channels per
+// input channel), all three ops on CUDA cores, direct form:
+//   forward        y[n, k, p, q]  = sum_{r,s} x[n, k / M, p*sh - ph + r*dh, q*sw - pw + s*dw] * w[k, r', s']
+//   backward-data  dx[n, c, h, w] = sum_{m < M} sum_{r,s} dy[n, c*M + m, p, q] * w[c*M + m, r', s']
+//                                   over the (r, s) with h + ph - r*dh = p*sh, w + pw - s*dw = q*sw
+//   backward-filter dw[k, r', s'] = sum_{n,p,q} x[n, k / M, p*sh - ph + r*dh, ...] * dy[n, k, p, q]
+// with (r', s') = (r, s), or (R-1-r, S-1-s) in convolution mode; fp32 sums in a fixed order.  The
+// filter gradient sums split partials [split][K][R*S] (a split: a range of images) in split
+// order.
+struct DwPlan {
+  const void* x;
+  const void* w;
+  const void* dy;
+  void* out;             // y, dx or dw
+  const void* bias;      // per k (forward) or per c (backward-data), or NULL
+  float beta;            // out = sum + bias + beta * out (beta 0: out is not read)
+  int flip;
+  int N, C, H, W, K, R, S, P, Q;
+  int ph, pw, sh, sw, dh, dw;
+  int M;                 // K / C
+  float* partial;        // filter gradient: nsplit * K * R * S fp32 (workspace)
+  int nsplit;            // filter gradient: image ranges of n_per_split images
+  int n_per_split;
+};
+
 }  // namespace cg3

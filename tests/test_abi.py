@@ -179,5 +179,7 @@ def test_grouped_and_dilated_workspace_bounded(cg):
         for op in (0, 1, 2):
             rc, n = _ws_ex(cg, op, dims, dil, groups)
             assert rc == 0 and 0 <= n <= 1_000_000_000 and n % 16 == 0
-            # backward-data with few input channels per group runs without a workspace
-            assert (n == 0) == (op == 1 and dims[1] // groups <= 8), (dims, op, n)
+            # backward-data with few input channels per group, and the forward and backward-data
+            # of depthwise layers (one input channel per group), run without a workspace
+            depthwise = groups > 1 and dims[1] // groups == 1
+            assert (n == 0) == ((op == 1 and dims[1] // groups <= 8) or (op == 0 and depthwise)), (dims, op, n)

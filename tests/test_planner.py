@@ -24,7 +24,7 @@ def test_planner_invariants(tmp_path):
     import __graft_entry__
     __graft_entry__.build()  # leaves the kernel objects in _build/
     cuda = _cuda_home()
-    objs = [os.path.join(OBJS, n) for n in ("conv_tap_gemm.cu.o", "conv_wgrad.cu.o", "conv_wgrad_mn.cu.o", "conv_dgrad_c2i.cu.o")]
+    objs = [os.path.join(OBJS, n) for n in ("conv_tap_gemm.cu.o", "conv_wgrad.cu.o", "conv_wgrad_mn.cu.o", "conv_dgrad_c2i.cu.o", "conv_depthwise.cu.o")]
     if not all(os.path.exists(o) for o in objs):
         pytest.skip("kernel objects not found next to the built library")
     exe = str(tmp_path / "planner_check")
