@@ -7,6 +7,7 @@
 #include <cuda_bf16.h>
 
 #include <algorithm>
+#include <atomic>
 #include <type_traits>
 
 #include "conv_plan.h"
@@ -49,15 +50,104 @@ __device__ __forceinline__ long long wtap(const DwPlan& p, int k, int r, int s) 
   return ((long long)k * p.R + r) * p.S + s;
 }
 
+// Stages the window of nrows x wt elements into dst (row-major): element (row, col) is the
+// global element at index at(row, col), or 0 where at() returns a negative index.  Each thread
+// takes elements tid, tid + blockDim, ... and keeps kDwLoads of its loads in flight before
+// storing them; the (row, col) of its next element advances by blockDim without a division.
+constexpr int kDwLoads = 8;
+template <int DT, class At>
+__device__ __forceinline__ void stage_window(float* dst, const void* src, int nrows, int wt, At at) {
+  const int total = nrows * wt;
+  const int step = (int)blockDim.x;
+  const int dq = step / wt, dr = step - dq * wt;
+  int row = (int)threadIdx.x / wt, col = (int)threadIdx.x - row * wt;
+  for (int e0 = (int)threadIdx.x; e0 < total; e0 += kDwLoads * step) {
+    float v[kDwLoads];
+#pragma unroll
+    for (int u = 0; u < kDwLoads; ++u) {
+      const long long gi = e0 + u * step < total ? at(row, col) : -1;
+      v[u] = gi >= 0 ? ld<DT>(src, gi) : 0.f;
+      row += dq;
+      col += dr;
+      if (col >= wt) {
+        col -= wt;
+        ++row;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kDwLoads; ++u)
+      if (e0 + u * step < total) dst[e0 + u * step] = v[u];
+  }
+}
+
 }  // namespace
 
 constexpr int kDwTile = 1024;  // output positions of one plane per work unit (4 per thread)
+constexpr int kDwSmem = 16 * 1024;  // bytes of one staged input band (fp32)
 
-// Forward: work units of kDwTile positions of one output plane (n, k); thread t takes positions
+// Rows of a forward unit's band (band_rows(p) output rows of one plane) and the staged input
+// band's row width: columns iw = col - pw for col < wt, so that output column q, tap s reads col
+// q*sw + s*dw.
+__host__ __device__ inline int dw_fwd_wt(const DwPlan& p) { return (p.Q - 1) * p.sw + (p.S - 1) * p.dw + 1; }
+__host__ __device__ inline int dw_fwd_in_rows(const DwPlan& p, int bp) { return (bp - 1) * p.sh + (p.R - 1) * p.dh + 1; }
+__host__ inline int dw_fwd_band(const DwPlan& p) {
+  int bp = p.P;
+  while (bp > 1 && (long long)dw_fwd_in_rows(p, bp) * dw_fwd_wt(p) * 4 > kDwSmem) bp = (bp + 1) / 2;
+  return bp;
+}
+
+// Forward: a unit is a band of bp output rows of one plane (n, k).  The block stages the band's
+// input rows of channel k / M (zero outside x, so the sums need no bounds checks) and the
+// filter's taps in shared memory, then each thread sums the taps of its outputs (consecutive
+// threads on consecutive q: conflict-free shared reads at unit stride, coalesced y writes).
+// Falls back to global reads when the band does not fit (bp = 1 and still too wide).
+template <int DT>
+__global__ void __launch_bounds__(256) dw_fwd_kernel(const __grid_constant__ DwPlan p, int bp) {
+  extern __shared__ float dw_smem[];
+  const int PQ = p.P * p.Q;
+  const int wt = dw_fwd_wt(p), nrows = dw_fwd_in_rows(p, bp);
+  const int RS = p.R * p.S;
+  float* taps = dw_smem;                  // R*S filter taps (in the order the sums read them)
+  float* band = dw_smem + ((RS + 3) & ~3);  // nrows x wt staged input
+  const int nb = (p.P + bp - 1) / bp;     // bands per plane
+  const long long units = (long long)p.N * p.K * nb;
+  for (long long u = blockIdx.x; u < units; u += gridDim.x) {
+    const long long nk = u / nb;
+    const int b = (int)(u - nk * nb);
+    const int k = (int)(nk % p.K);
+    const long long n = nk / p.K;
+    const int c = k / p.M;
+    const int p0 = b * bp, np = min(bp, p.P - p0);
+    const int ih0 = p0 * p.sh - p.ph;
+    const long long xb = (n * p.C + c) * (long long)p.H * p.W;
+    __syncthreads();  // the previous unit's reads of the band are done
+    for (int t = (int)threadIdx.x; t < RS; t += (int)blockDim.x) taps[t] = ld<DT>(p.w, wtap(p, k, t / p.S, t % p.S));
+    const int rows_used = (np - 1) * p.sh + (p.R - 1) * p.dh + 1;
+    stage_window<DT>(band, p.x, rows_used, wt, [&](int row, int col) -> long long {
+      const int ih = ih0 + row, iw = col - p.pw;
+      return (ih >= 0 && ih < p.H && iw >= 0 && iw < p.W) ? xb + (long long)ih * p.W + iw : -1;
+    });
+    __syncthreads();
+    const long long yb = nk * PQ + (long long)p0 * p.Q;
+    for (int o = (int)threadIdx.x; o < np * p.Q; o += (int)blockDim.x) {
+      const int pp = o / p.Q, q = o - pp * p.Q;
+      const float* src = band + pp * p.sh * wt + q * p.sw;
+      float acc = 0.f;
+      for (int r = 0; r < p.R; ++r)
+        for (int s = 0; s < p.S; ++s) acc = fmaf(src[r * p.dh * wt + s * p.dw], taps[r * p.S + s], acc);
+      if (p.bias != nullptr) acc += ld<DT>(p.bias, k);
+      if (p.beta != 0.f) acc += p.beta * ld_rw<DT>(p.out, yb + o);
+      st<DT>(p.out, yb + o, acc);
+    }
+  }
+}
+
+// Forward without staging (a band row wider than the staging limit): work units of kDwTile
+// positions of one output plane (n, k); thread t takes positions
 // t, t + 256, ... of the unit (consecutive threads on consecutive q: coalesced x reads and y
 // writes); the plane's indices are computed once per unit, positions in 32 bits.
 template <int DT>
-__global__ void __launch_bounds__(256) dw_fwd_kernel(const __grid_constant__ DwPlan p) {
+__global__ void __launch_bounds__(256) dw_fwd_direct_kernel(const __grid_constant__ DwPlan p) {
   const int PQ = p.P * p.Q;
   const int tpp = (PQ + kDwTile - 1) / kDwTile;  // units per plane
   const long long units = (long long)p.N * p.K * tpp;
@@ -135,6 +225,70 @@ __global__ void __launch_bounds__(256) dw_bwd_data_kernel(const __grid_constant_
   }
 }
 
+// Backward-data at unit stride: a unit is a band of bh rows of one dx plane (n, c).  The block
+// stages, for each of the channel's M output channels, the dy rows the band reads (dy row
+// h + ph - r*dh, zero outside dy) with columns w + pw - s*dw for col = w + (S-1)*dw - s*dw, and
+// the filter taps; each thread then sums, for each of its dx elements, the taps in the order
+// (m, r, s).
+__host__ __device__ inline int dw_bd_wt(const DwPlan& p) { return p.W + (p.S - 1) * p.dw; }
+__host__ __device__ inline int dw_bd_rows(const DwPlan& p, int bh) { return bh + (p.R - 1) * p.dh; }
+__host__ inline int dw_bd_band(const DwPlan& p) {
+  int bh = p.H;
+  while (bh > 1 && (long long)p.M * dw_bd_rows(p, bh) * dw_bd_wt(p) * 4 > kDwSmem) bh = (bh + 1) / 2;
+  return bh;
+}
+
+template <int DT>
+__global__ void __launch_bounds__(256) dw_bwd_data_s1_kernel(const __grid_constant__ DwPlan p, int bh) {
+  extern __shared__ float dw_smem[];
+  const int HW = p.H * p.W;
+  const long long PQ = (long long)p.P * p.Q;
+  const int wt = dw_bd_wt(p), nrows = dw_bd_rows(p, bh);
+  const int RS = p.R * p.S;
+  float* taps = dw_smem;                        // M x R*S
+  float* band = dw_smem + ((p.M * RS + 3) & ~3);  // M x nrows x wt
+  const int nb = (p.H + bh - 1) / bh;
+  const long long units = (long long)p.N * p.C * nb;
+  for (long long u = blockIdx.x; u < units; u += gridDim.x) {
+    const long long nc = u / nb;
+    const int b = (int)(u - nc * nb);
+    const int c = (int)(nc % p.C);
+    const long long n = nc / p.C;
+    const int h0 = b * bh, nh = min(bh, p.H - h0);
+    const int rows_used = nh + (p.R - 1) * p.dh;
+    const int pr0 = h0 + p.ph - (p.R - 1) * p.dh;  // dy row of staged row 0
+    const int qc0 = p.pw - (p.S - 1) * p.dw;       // dy column of staged column 0
+    __syncthreads();
+    for (int t = (int)threadIdx.x; t < p.M * RS; t += (int)blockDim.x) {
+      const int m = t / RS, rs = t - m * RS;
+      taps[t] = ld<DT>(p.w, wtap(p, c * p.M + m, rs / p.S, rs % p.S));
+    }
+    for (int m = 0; m < p.M; ++m) {
+      const long long db = (n * p.K + c * p.M + m) * PQ;
+      float* bm = band + m * nrows * wt;
+      stage_window<DT>(bm, p.dy, rows_used, wt, [&](int row, int col) -> long long {
+        const int pp = pr0 + row, q = qc0 + col;
+        return (pp >= 0 && pp < p.P && q >= 0 && q < p.Q) ? db + (long long)pp * p.Q + q : -1;
+      });
+    }
+    __syncthreads();
+    const long long ob = nc * HW + (long long)h0 * p.W;
+    for (int o = (int)threadIdx.x; o < nh * p.W; o += (int)blockDim.x) {
+      const int hh = o / p.W, w = o - hh * p.W;
+      float acc = 0.f;
+      for (int m = 0; m < p.M; ++m) {
+        const float* bm = band + m * nrows * wt + (hh + (p.R - 1) * p.dh) * wt + w + (p.S - 1) * p.dw;
+        const float* tm = taps + m * RS;
+        for (int r = 0; r < p.R; ++r)
+          for (int s = 0; s < p.S; ++s) acc = fmaf(bm[-(r * p.dh) * wt - s * p.dw], tm[r * p.S + s], acc);
+      }
+      if (p.bias != nullptr) acc += ld<DT>(p.bias, c);
+      if (p.beta != 0.f) acc += p.beta * ld_rw<DT>(p.out, ob + o);
+      st<DT>(p.out, ob + o, acc);
+    }
+  }
+}
+
 // Backward-filter partials: block (k, split) sums, for every tap (r, s) in turn, x * dy over the
 // positions (p, q) of its split's images, each thread a strided subset in increasing order, then
 // a fixed-order tree over the block: partial[(split * K + k) * R*S + r*S + s].
@@ -170,6 +324,74 @@ __global__ void __launch_bounds__(256) dw_wgrad_kernel(const __grid_constant__ D
     }
 }
 
+// Backward-filter partials, staged: block (k, split) walks its images' output-row bands (the
+// forward's bands): the block stages the band's x rows (zero outside x, as the forward does) and
+// dy rows in shared memory, then each thread adds, for each of its outputs o in increasing
+// order, dy[o] times the band's input under every tap into its RSM register accumulators (R*S
+// <= RSM); a fixed-order tree over the block per tap gives the split's partials.
+template <int DT, int RSM>
+__global__ void __launch_bounds__(256) dw_wgrad_band_kernel(const __grid_constant__ DwPlan p, int bp) {
+  extern __shared__ float dw_smem[];
+  const int k = (int)(blockIdx.x % p.K);
+  const int sp = (int)(blockIdx.x / p.K);
+  const int c = k / p.M;
+  const int PQ = p.P * p.Q;
+  const int wt = dw_fwd_wt(p), nrows = dw_fwd_in_rows(p, bp);
+  const int RS = p.R * p.S;
+  float* band = dw_smem;                 // nrows x wt staged x
+  float* dyb = dw_smem + nrows * wt;     // bp x Q staged dy
+  float acc[RSM];
+#pragma unroll
+  for (int t = 0; t < RSM; ++t) acc[t] = 0.f;
+  const int n0 = sp * p.n_per_split, n1 = min(p.N, n0 + p.n_per_split);
+  for (int n = n0; n < n1; ++n) {
+    const long long xb = ((long long)n * p.C + c) * p.H * p.W;
+    const long long db = ((long long)n * p.K + k) * PQ;
+    for (int p0 = 0; p0 < p.P; p0 += bp) {
+      const int np = min(bp, p.P - p0);
+      const int ih0 = p0 * p.sh - p.ph;
+      const int rows_used = (np - 1) * p.sh + (p.R - 1) * p.dh + 1;
+      __syncthreads();  // the previous band's reads are done
+      stage_window<DT>(band, p.x, rows_used, wt, [&](int row, int col) -> long long {
+        const int ih = ih0 + row, iw = col - p.pw;
+        return (ih >= 0 && ih < p.H && iw >= 0 && iw < p.W) ? xb + (long long)ih * p.W + iw : -1;
+      });
+      stage_window<DT>(dyb, p.dy, np, p.Q, [&](int row, int col) -> long long {
+        return db + (long long)(p0 + row) * p.Q + col;
+      });
+      __syncthreads();
+      for (int o = (int)threadIdx.x; o < np * p.Q; o += (int)blockDim.x) {
+        const int pp = o / p.Q, q = o - pp * p.Q;
+        const float g = dyb[o];
+        const float* src = band + pp * p.sh * wt + q * p.sw;
+#pragma unroll
+        for (int t = 0; t < RSM; ++t) {
+          if (t < RS) {
+            const int r = t / p.S, s = t - r * p.S;
+            acc[t] = fmaf(src[r * p.dh * wt + s * p.dw], g, acc[t]);
+          }
+        }
+      }
+    }
+  }
+  // per tap: a fixed-order tree over the block's threads (the band area is free now)
+  float* red = dw_smem;
+  for (int t = 0; t < RS && t < RSM; ++t) {
+    __syncthreads();
+    float v = 0.f;
+#pragma unroll
+    for (int u = 0; u < RSM; ++u)
+      if (u == t) v = acc[u];
+    red[threadIdx.x] = v;
+    __syncthreads();
+    for (int h = 128; h > 0; h >>= 1) {
+      if ((int)threadIdx.x < h) red[threadIdx.x] += red[threadIdx.x + h];
+      __syncthreads();
+    }
+    if (threadIdx.x == 0) p.partial[((long long)sp * p.K + k) * RS + t] = red[0];
+  }
+}
+
 // dw[k, 0, r', s'] = sum over splits, in split order, of the tap's partials (+ beta * dw).
 template <int DT>
 __global__ void __launch_bounds__(256) dw_wgrad_reduce_kernel(const __grid_constant__ DwPlan p) {
@@ -190,17 +412,63 @@ static unsigned dw_grid(long long total, int num_sms) {
   return (unsigned)std::max(1ll, std::min<long long>((total + 255) / 256, (long long)num_sms * 16));
 }
 
+size_t dw_fwd_smem_bytes(const DwPlan& p) {
+  const int bp = dw_fwd_band(p);
+  return ((size_t)((p.R * p.S + 3) & ~3) + (size_t)dw_fwd_in_rows(p, bp) * dw_fwd_wt(p)) * sizeof(float);
+}
+
 cudaError_t launch_dw_fwd(const DwPlan& p, int dt, int num_sms, cudaStream_t st) {
-  const long long tpp = ((long long)p.P * p.Q + kDwTile - 1) / kDwTile;
-  const unsigned g = (unsigned)std::max(1ll, std::min<long long>((long long)p.N * p.K * tpp, (long long)num_sms * 8));
-  if (dt == 0)
-    dw_fwd_kernel<0><<<g, 256, 0, st>>>(p);
-  else
-    dw_fwd_kernel<1><<<g, 256, 0, st>>>(p);
+  const int bp = dw_fwd_band(p);
+  const size_t smem = dw_fwd_smem_bytes(p);
+  if (smem > 4 * (size_t)kDwSmem) {  // one band row past the staging limit: unstaged reads
+    const long long tpp = ((long long)p.P * p.Q + kDwTile - 1) / kDwTile;
+    const unsigned g = (unsigned)std::max(1ll, std::min<long long>((long long)p.N * p.K * tpp, (long long)num_sms * 8));
+    if (dt == 0)
+      dw_fwd_direct_kernel<0><<<g, 256, 0, st>>>(p);
+    else
+      dw_fwd_direct_kernel<1><<<g, 256, 0, st>>>(p);
+    return cudaGetLastError();
+  }
+  const long long units = (long long)p.N * p.K * ((p.P + bp - 1) / bp);
+  const unsigned g = (unsigned)std::max(1ll, std::min<long long>(units, (long long)num_sms * 8));
+  static std::atomic<int> set_bytes[2][kMaxDevices];
+  cudaError_t e;
+  if (dt == 0) {
+    e = ensure_dyn_smem(dw_fwd_kernel<0>, smem, set_bytes[0]);
+    if (e != cudaSuccess) return e;
+    dw_fwd_kernel<0><<<g, 256, smem, st>>>(p, bp);
+  } else {
+    e = ensure_dyn_smem(dw_fwd_kernel<1>, smem, set_bytes[1]);
+    if (e != cudaSuccess) return e;
+    dw_fwd_kernel<1><<<g, 256, smem, st>>>(p, bp);
+  }
   return cudaGetLastError();
 }
 
+size_t dw_bd_smem_bytes(const DwPlan& p) {
+  const int bh = dw_bd_band(p);
+  return ((size_t)((p.M * p.R * p.S + 3) & ~3) + (size_t)p.M * dw_bd_rows(p, bh) * dw_bd_wt(p)) * sizeof(float);
+}
+
 cudaError_t launch_dw_bwd_data(const DwPlan& p, int dt, int num_sms, cudaStream_t st) {
+  if (p.sh == 1 && p.sw == 1 && dw_bd_smem_bytes(p) <= 4 * (size_t)kDwSmem) {  // staged bands
+    const int bh = dw_bd_band(p);
+    const size_t smem = dw_bd_smem_bytes(p);
+    const long long units = (long long)p.N * p.C * ((p.H + bh - 1) / bh);
+    const unsigned g = (unsigned)std::max(1ll, std::min<long long>(units, (long long)num_sms * 8));
+    static std::atomic<int> set_bytes[2][kMaxDevices];
+    cudaError_t e;
+    if (dt == 0) {
+      e = ensure_dyn_smem(dw_bwd_data_s1_kernel<0>, smem, set_bytes[0]);
+      if (e != cudaSuccess) return e;
+      dw_bwd_data_s1_kernel<0><<<g, 256, smem, st>>>(p, bh);
+    } else {
+      e = ensure_dyn_smem(dw_bwd_data_s1_kernel<1>, smem, set_bytes[1]);
+      if (e != cudaSuccess) return e;
+      dw_bwd_data_s1_kernel<1><<<g, 256, smem, st>>>(p, bh);
+    }
+    return cudaGetLastError();
+  }
   const long long tpp = ((long long)p.H * p.W + kDwTile - 1) / kDwTile;
   const unsigned g = (unsigned)std::max(1ll, std::min<long long>((long long)p.N * p.C * tpp, (long long)num_sms * 8));
   if (dt == 0)
@@ -210,16 +478,44 @@ cudaError_t launch_dw_bwd_data(const DwPlan& p, int dt, int num_sms, cudaStream_
   return cudaGetLastError();
 }
 
+template <int DT, int RSM>
+static cudaError_t launch_dw_wgrad_band(const DwPlan& p, unsigned blocks, int bp, size_t smem, cudaStream_t st) {
+  static std::atomic<int> set_bytes[kMaxDevices];
+  const cudaError_t e = ensure_dyn_smem(dw_wgrad_band_kernel<DT, RSM>, smem, set_bytes);
+  if (e != cudaSuccess) return e;
+  dw_wgrad_band_kernel<DT, RSM><<<blocks, 256, smem, st>>>(p, bp);
+  return cudaGetLastError();
+}
+
+// Staged bands with register accumulators for filters of up to 49 taps whose bands fit the
+// staging limit; per-tap passes over global memory otherwise.
 cudaError_t launch_dw_bwd_filter(const DwPlan& p, int dt, int num_sms, cudaStream_t st) {
   const unsigned blocks = (unsigned)((long long)p.K * p.nsplit);
   const unsigned g = dw_grid((long long)p.K * p.R * p.S, num_sms);
-  if (dt == 0) {
+  const int RS = p.R * p.S;
+  const int bp = dw_fwd_band(p);
+  const size_t smem = std::max<size_t>(256 * sizeof(float),
+                                       ((size_t)dw_fwd_in_rows(p, bp) * dw_fwd_wt(p) + (size_t)bp * p.Q) * sizeof(float));
+  cudaError_t e = cudaSuccess;
+  if (RS <= 49 && smem <= 6 * (size_t)kDwSmem) {
+    if (dt == 0)
+      e = RS <= 9 ? launch_dw_wgrad_band<0, 9>(p, blocks, bp, smem, st)
+                  : RS <= 25 ? launch_dw_wgrad_band<0, 25>(p, blocks, bp, smem, st)
+                             : launch_dw_wgrad_band<0, 49>(p, blocks, bp, smem, st);
+    else
+      e = RS <= 9 ? launch_dw_wgrad_band<1, 9>(p, blocks, bp, smem, st)
+                  : RS <= 25 ? launch_dw_wgrad_band<1, 25>(p, blocks, bp, smem, st)
+                             : launch_dw_wgrad_band<1, 49>(p, blocks, bp, smem, st);
+  } else if (dt == 0) {
     dw_wgrad_kernel<0><<<blocks, 256, 0, st>>>(p);
-    dw_wgrad_reduce_kernel<0><<<g, 256, 0, st>>>(p);
   } else {
     dw_wgrad_kernel<1><<<blocks, 256, 0, st>>>(p);
-    dw_wgrad_reduce_kernel<1><<<g, 256, 0, st>>>(p);
   }
+  if (e != cudaSuccess) return e;
+  if (dt == 0)
+    dw_wgrad_reduce_kernel<0><<<g, 256, 0, st>>>(p);
+  else
+    dw_wgrad_reduce_kernel<1><<<g, 256, 0, st>>>(p);
   return cudaGetLastError();
 }
 

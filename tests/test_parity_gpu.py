@@ -504,6 +504,7 @@ GROUP_GPU_CASES = [
     ((2, 24, 15, 13, 24, 5, 5, 2, 2, 2, 2), 24, (1, 1), False),  # depthwise 5x5, stride 2
     ((2, 8, 12, 12, 16, 3, 3, 2, 2, 1, 1), 8, (2, 2), False),    # depthwise, 2 outputs per channel, dilation 2
     ((1, 5, 7, 9, 10, 3, 2, 1, 0, 2, 1), 5, (1, 1), True),       # depthwise x2, R != S, stride 2 x 1
+    ((2, 4, 1, 20000, 4, 1, 5, 0, 2, 1, 1), 4, (1, 1), False),   # depthwise 1-D, rows too wide to stage
 ]
 
 
