@@ -111,14 +111,14 @@ bool is_depthwise(const Desc& dg) { return dg.g > 1 && dg.C == 1; }
 
 // The depthwise plan of a whole grouped problem (d: the totals; dg: its per-group descriptor);
 // pointers, bias, beta and mode are set by the caller.  The filter gradient's splits are ranges
-// of images, enough (K * splits blocks) to fill two waves of the SMs.
+// of images, enough (K * splits blocks) for about eight blocks per SM.
 DwPlan dw_plan(const Desc& d, const Desc& dg, int sms) {
   DwPlan p;
   std::memset(&p, 0, sizeof(p));
   p.N = d.N; p.C = d.C; p.H = d.H; p.W = d.W; p.K = d.K; p.R = d.R; p.S = d.S; p.P = d.P; p.Q = d.Q;
   p.ph = d.ph; p.pw = d.pw; p.sh = d.sh; p.sw = d.sw; p.dh = d.dh; p.dw = d.dw;
   p.M = dg.K;
-  const int want = std::max(1, (2 * sms + d.K - 1) / d.K);
+  const int want = std::max(1, (8 * sms + d.K - 1) / d.K);
   p.n_per_split = std::max(1, (d.N + want - 1) / want);
   p.nsplit = (d.N + p.n_per_split - 1) / p.n_per_split;
   return p;
