@@ -52,6 +52,8 @@ def parse_args():
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--profile", choices=OPS, default=None,
                     help="run only this op of the workload (warmup + steps calls) for a profiler; prints its mean ms")
+    ap.add_argument("--groups", type=int, default=1,
+                    help="with --profile: the workload's layer with this many groups (filter K x C/groups)")
     return ap.parse_args()
 
 
@@ -66,9 +68,25 @@ def run_profile(args):
     stream = torch.cuda.current_stream()
     flush = torch.empty(2 * torch.cuda.get_device_properties(dev).L2_cache_size, dtype=torch.uint8, device=dev)
     c = _device_case(W.WORKLOADS[args.workload], dev)
-    ms = _time_call(lambda: _op_call(c, args.profile, stream), flush, stream, max(1, args.steps), args.warmup)
+    call = lambda: _op_call(c, args.profile, stream)
+    if args.groups > 1:  # the same layer grouped: filter K x C/groups, each op's grouped call
+        pb, g = c["pb"], args.groups
+        pad, st = (pb.pad_h, pb.pad_w), (pb.stride_h, pb.stride_w)
+        dt = 0 if pb.dtype == "f32" else 1
+        wg = c["w"][:, : pb.C // g].contiguous()
+        dwg = torch.empty_like(wg)
+        wsz = max(cg.conv2d_workspace_size(op, pb.dims(), dt, (1, 1), g) for op in range(3))
+        wsg = torch.empty(max(wsz, 16), dtype=torch.uint8, device=dev)
+        calls = {"fwd": lambda: cg.conv2d_fwd(c["x"], wg, pad, st, out=c["y"], workspace=wsg, stream=stream, groups=g),
+                 "bwd_data": lambda: cg.conv2d_bwd_data(c["dy"], wg, (pb.H, pb.W), pad, st, out=c["dx"], workspace=wsg,
+                                                        stream=stream, groups=g),
+                 "bwd_filter": lambda: cg.conv2d_bwd_filter(c["x"], c["dy"], (pb.R, pb.S), pad, st, out=dwg,
+                                                            workspace=wsg, stream=stream, groups=g)}
+        call = calls[args.profile]
+    ms = _time_call(call, flush, stream, max(1, args.steps), args.warmup)
     cg.conv2d_device_status(stream)
-    print(json.dumps({"profile": args.profile, "workload": args.workload, "ms": round(ms, 5)}), flush=True)
+    print(json.dumps({"profile": args.profile, "workload": args.workload, "groups": args.groups, "ms": round(ms, 5)}),
+          flush=True)
     return 0
 
 

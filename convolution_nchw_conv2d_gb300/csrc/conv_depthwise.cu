@@ -100,8 +100,9 @@ __host__ inline int dw_fwd_band(const DwPlan& p) {
 // input rows of channel k / M (zero outside x, so the sums need no bounds checks) and the
 // filter's taps in shared memory, then each thread sums the taps of its outputs (consecutive
 // threads on consecutive q: conflict-free shared reads at unit stride, coalesced y writes).
-// Falls back to global reads when the band does not fit (bp = 1 and still too wide).
-template <int DT>
+// RT x ST > 0: the filter size at compile time (taps and their band offsets in registers,
+// the tap loop unrolled); 0 x 0: any size.
+template <int DT, int RT, int ST>
 __global__ void __launch_bounds__(256) dw_fwd_kernel(const __grid_constant__ DwPlan p, int bp) {
   extern __shared__ float dw_smem[];
   const int PQ = p.P * p.Q;
@@ -129,6 +130,29 @@ __global__ void __launch_bounds__(256) dw_fwd_kernel(const __grid_constant__ DwP
     });
     __syncthreads();
     const long long yb = nk * PQ + (long long)p0 * p.Q;
+    if constexpr (RT > 0 && ST > 0) {
+      float tv[RT * ST];
+      int toff[RT * ST];
+#pragma unroll
+      for (int r = 0; r < RT; ++r)
+#pragma unroll
+        for (int s = 0; s < ST; ++s) {
+          tv[r * ST + s] = taps[r * ST + s];
+          toff[r * ST + s] = r * p.dh * wt + s * p.dw;
+        }
+      const float bv = p.bias != nullptr ? ld<DT>(p.bias, k) : 0.f;
+      for (int o = (int)threadIdx.x; o < np * p.Q; o += (int)blockDim.x) {
+        const int pp = o / p.Q, q = o - pp * p.Q;
+        const float* src = band + pp * p.sh * wt + q * p.sw;
+        float acc = 0.f;
+#pragma unroll
+        for (int t = 0; t < RT * ST; ++t) acc = fmaf(src[toff[t]], tv[t], acc);
+        acc += bv;
+        if (p.beta != 0.f) acc += p.beta * ld_rw<DT>(p.out, yb + o);
+        st<DT>(p.out, yb + o, acc);
+      }
+      continue;
+    }
     for (int o = (int)threadIdx.x; o < np * p.Q; o += (int)blockDim.x) {
       const int pp = o / p.Q, q = o - pp * p.Q;
       const float* src = band + pp * p.sh * wt + q * p.sw;
@@ -238,7 +262,7 @@ __host__ inline int dw_bd_band(const DwPlan& p) {
   return bh;
 }
 
-template <int DT>
+template <int DT, int RT, int ST>
 __global__ void __launch_bounds__(256) dw_bwd_data_s1_kernel(const __grid_constant__ DwPlan p, int bh) {
   extern __shared__ float dw_smem[];
   const int HW = p.H * p.W;
@@ -273,6 +297,31 @@ __global__ void __launch_bounds__(256) dw_bwd_data_s1_kernel(const __grid_consta
     }
     __syncthreads();
     const long long ob = nc * HW + (long long)h0 * p.W;
+    if constexpr (RT > 0 && ST > 0) {
+      if (p.M == 1) {  // one output channel per input channel: taps and offsets in registers
+        float tv[RT * ST];
+        int toff[RT * ST];
+#pragma unroll
+        for (int r = 0; r < RT; ++r)
+#pragma unroll
+          for (int s = 0; s < ST; ++s) {
+            tv[r * ST + s] = taps[r * ST + s];
+            toff[r * ST + s] = -(r * p.dh) * wt - s * p.dw;
+          }
+        const float bv = p.bias != nullptr ? ld<DT>(p.bias, c) : 0.f;
+        for (int o = (int)threadIdx.x; o < nh * p.W; o += (int)blockDim.x) {
+          const int hh = o / p.W, w = o - hh * p.W;
+          const float* bm = band + (hh + (RT - 1) * p.dh) * wt + w + (ST - 1) * p.dw;
+          float acc = 0.f;
+#pragma unroll
+          for (int t = 0; t < RT * ST; ++t) acc = fmaf(bm[toff[t]], tv[t], acc);
+          acc += bv;
+          if (p.beta != 0.f) acc += p.beta * ld_rw<DT>(p.out, ob + o);
+          st<DT>(p.out, ob + o, acc);
+        }
+        continue;
+      }
+    }
     for (int o = (int)threadIdx.x; o < nh * p.W; o += (int)blockDim.x) {
       const int hh = o / p.W, w = o - hh * p.W;
       float acc = 0.f;
@@ -329,7 +378,7 @@ __global__ void __launch_bounds__(256) dw_wgrad_kernel(const __grid_constant__ D
 // dy rows in shared memory, then each thread adds, for each of its outputs o in increasing
 // order, dy[o] times the band's input under every tap into its RSM register accumulators (R*S
 // <= RSM); a fixed-order tree over the block per tap gives the split's partials.
-template <int DT, int RSM>
+template <int DT, int RSM, int RT, int ST>
 __global__ void __launch_bounds__(256) dw_wgrad_band_kernel(const __grid_constant__ DwPlan p, int bp) {
   extern __shared__ float dw_smem[];
   const int k = (int)(blockIdx.x % p.K);
@@ -360,15 +409,30 @@ __global__ void __launch_bounds__(256) dw_wgrad_band_kernel(const __grid_constan
         return db + (long long)(p0 + row) * p.Q + col;
       });
       __syncthreads();
-      for (int o = (int)threadIdx.x; o < np * p.Q; o += (int)blockDim.x) {
-        const int pp = o / p.Q, q = o - pp * p.Q;
-        const float g = dyb[o];
-        const float* src = band + pp * p.sh * wt + q * p.sw;
+      if constexpr (RT > 0 && ST > 0) {  // RSM == RT * ST: every tap's offset in a register
+        int toff[RT * ST];
 #pragma unroll
-        for (int t = 0; t < RSM; ++t) {
-          if (t < RS) {
-            const int r = t / p.S, s = t - r * p.S;
-            acc[t] = fmaf(src[r * p.dh * wt + s * p.dw], g, acc[t]);
+        for (int r = 0; r < RT; ++r)
+#pragma unroll
+          for (int s = 0; s < ST; ++s) toff[r * ST + s] = r * p.dh * wt + s * p.dw;
+        for (int o = (int)threadIdx.x; o < np * p.Q; o += (int)blockDim.x) {
+          const int pp = o / p.Q, q = o - pp * p.Q;
+          const float g = dyb[o];
+          const float* src = band + pp * p.sh * wt + q * p.sw;
+#pragma unroll
+          for (int t = 0; t < RT * ST; ++t) acc[t] = fmaf(src[toff[t]], g, acc[t]);
+        }
+      } else {
+        for (int o = (int)threadIdx.x; o < np * p.Q; o += (int)blockDim.x) {
+          const int pp = o / p.Q, q = o - pp * p.Q;
+          const float g = dyb[o];
+          const float* src = band + pp * p.sh * wt + q * p.sw;
+#pragma unroll
+          for (int t = 0; t < RSM; ++t) {
+            if (t < RS) {
+              const int r = t / p.S, s = t - r * p.S;
+              acc[t] = fmaf(src[r * p.dh * wt + s * p.dw], g, acc[t]);
+            }
           }
         }
       }
@@ -408,6 +472,34 @@ __global__ void __launch_bounds__(256) dw_wgrad_reduce_kernel(const __grid_const
 }
 
 // ---------------------------------------------------------------------------- launchers
+// The staged forward and unit-stride backward-data kernels for 3x3, 5x5 and 7x7 filters
+// (compile-time sizes) and any other size.
+struct KernelFwd {
+  template <int DT, int RT, int ST>
+  static auto get() { return dw_fwd_kernel<DT, RT, ST>; }
+};
+struct KernelBwdData {
+  template <int DT, int RT, int ST>
+  static auto get() { return dw_bwd_data_s1_kernel<DT, RT, ST>; }
+};
+
+template <int DT, int RT, int ST, class K>
+static cudaError_t launch_sized(const DwPlan& p, unsigned g, int band, size_t smem, cudaStream_t st) {
+  static std::atomic<int> set_bytes[kMaxDevices];
+  auto kern = K::template get<DT, RT, ST>();
+  const cudaError_t e = ensure_dyn_smem(kern, smem, set_bytes);
+  if (e != cudaSuccess) return e;
+  kern<<<g, 256, smem, st>>>(p, band);
+  return cudaGetLastError();
+}
+
+template <int DT, class K>
+static cudaError_t launch_by_size(const DwPlan& p, K, unsigned g, int band, size_t smem, cudaStream_t st) {
+  if (p.R == 3 && p.S == 3) return launch_sized<DT, 3, 3, K>(p, g, band, smem, st);
+  if (p.R == 5 && p.S == 5) return launch_sized<DT, 5, 5, K>(p, g, band, smem, st);
+  if (p.R == 7 && p.S == 7) return launch_sized<DT, 7, 7, K>(p, g, band, smem, st);
+  return launch_sized<DT, 0, 0, K>(p, g, band, smem, st);
+}
 static unsigned dw_grid(long long total, int num_sms) {
   return (unsigned)std::max(1ll, std::min<long long>((total + 255) / 256, (long long)num_sms * 16));
 }
@@ -431,18 +523,7 @@ cudaError_t launch_dw_fwd(const DwPlan& p, int dt, int num_sms, cudaStream_t st)
   }
   const long long units = (long long)p.N * p.K * ((p.P + bp - 1) / bp);
   const unsigned g = (unsigned)std::max(1ll, std::min<long long>(units, (long long)num_sms * 8));
-  static std::atomic<int> set_bytes[2][kMaxDevices];
-  cudaError_t e;
-  if (dt == 0) {
-    e = ensure_dyn_smem(dw_fwd_kernel<0>, smem, set_bytes[0]);
-    if (e != cudaSuccess) return e;
-    dw_fwd_kernel<0><<<g, 256, smem, st>>>(p, bp);
-  } else {
-    e = ensure_dyn_smem(dw_fwd_kernel<1>, smem, set_bytes[1]);
-    if (e != cudaSuccess) return e;
-    dw_fwd_kernel<1><<<g, 256, smem, st>>>(p, bp);
-  }
-  return cudaGetLastError();
+  return dt == 0 ? launch_by_size<0>(p, KernelFwd(), g, bp, smem, st) : launch_by_size<1>(p, KernelFwd(), g, bp, smem, st);
 }
 
 size_t dw_bd_smem_bytes(const DwPlan& p) {
@@ -456,18 +537,8 @@ cudaError_t launch_dw_bwd_data(const DwPlan& p, int dt, int num_sms, cudaStream_
     const size_t smem = dw_bd_smem_bytes(p);
     const long long units = (long long)p.N * p.C * ((p.H + bh - 1) / bh);
     const unsigned g = (unsigned)std::max(1ll, std::min<long long>(units, (long long)num_sms * 8));
-    static std::atomic<int> set_bytes[2][kMaxDevices];
-    cudaError_t e;
-    if (dt == 0) {
-      e = ensure_dyn_smem(dw_bwd_data_s1_kernel<0>, smem, set_bytes[0]);
-      if (e != cudaSuccess) return e;
-      dw_bwd_data_s1_kernel<0><<<g, 256, smem, st>>>(p, bh);
-    } else {
-      e = ensure_dyn_smem(dw_bwd_data_s1_kernel<1>, smem, set_bytes[1]);
-      if (e != cudaSuccess) return e;
-      dw_bwd_data_s1_kernel<1><<<g, 256, smem, st>>>(p, bh);
-    }
-    return cudaGetLastError();
+    return dt == 0 ? launch_by_size<0>(p, KernelBwdData(), g, bh, smem, st)
+                   : launch_by_size<1>(p, KernelBwdData(), g, bh, smem, st);
   }
   const long long tpp = ((long long)p.H * p.W + kDwTile - 1) / kDwTile;
   const unsigned g = (unsigned)std::max(1ll, std::min<long long>((long long)p.N * p.C * tpp, (long long)num_sms * 8));
@@ -478,13 +549,24 @@ cudaError_t launch_dw_bwd_data(const DwPlan& p, int dt, int num_sms, cudaStream_
   return cudaGetLastError();
 }
 
-template <int DT, int RSM>
+template <int DT, int RSM, int RT, int ST>
 static cudaError_t launch_dw_wgrad_band(const DwPlan& p, unsigned blocks, int bp, size_t smem, cudaStream_t st) {
   static std::atomic<int> set_bytes[kMaxDevices];
-  const cudaError_t e = ensure_dyn_smem(dw_wgrad_band_kernel<DT, RSM>, smem, set_bytes);
+  const cudaError_t e = ensure_dyn_smem(dw_wgrad_band_kernel<DT, RSM, RT, ST>, smem, set_bytes);
   if (e != cudaSuccess) return e;
-  dw_wgrad_band_kernel<DT, RSM><<<blocks, 256, smem, st>>>(p, bp);
+  dw_wgrad_band_kernel<DT, RSM, RT, ST><<<blocks, 256, smem, st>>>(p, bp);
   return cudaGetLastError();
+}
+
+template <int DT>
+static cudaError_t launch_dw_wgrad_band_any(const DwPlan& p, unsigned blocks, int bp, size_t smem, cudaStream_t st) {
+  const int RS = p.R * p.S;
+  if (p.R == 3 && p.S == 3) return launch_dw_wgrad_band<DT, 9, 3, 3>(p, blocks, bp, smem, st);
+  if (p.R == 5 && p.S == 5) return launch_dw_wgrad_band<DT, 25, 5, 5>(p, blocks, bp, smem, st);
+  if (p.R == 7 && p.S == 7) return launch_dw_wgrad_band<DT, 49, 7, 7>(p, blocks, bp, smem, st);
+  return RS <= 9 ? launch_dw_wgrad_band<DT, 9, 0, 0>(p, blocks, bp, smem, st)
+                 : RS <= 25 ? launch_dw_wgrad_band<DT, 25, 0, 0>(p, blocks, bp, smem, st)
+                            : launch_dw_wgrad_band<DT, 49, 0, 0>(p, blocks, bp, smem, st);
 }
 
 // Staged bands with register accumulators for filters of up to 49 taps whose bands fit the
@@ -498,14 +580,8 @@ cudaError_t launch_dw_bwd_filter(const DwPlan& p, int dt, int num_sms, cudaStrea
                                        ((size_t)dw_fwd_in_rows(p, bp) * dw_fwd_wt(p) + (size_t)bp * p.Q) * sizeof(float));
   cudaError_t e = cudaSuccess;
   if (RS <= 49 && smem <= 6 * (size_t)kDwSmem) {
-    if (dt == 0)
-      e = RS <= 9 ? launch_dw_wgrad_band<0, 9>(p, blocks, bp, smem, st)
-                  : RS <= 25 ? launch_dw_wgrad_band<0, 25>(p, blocks, bp, smem, st)
-                             : launch_dw_wgrad_band<0, 49>(p, blocks, bp, smem, st);
-    else
-      e = RS <= 9 ? launch_dw_wgrad_band<1, 9>(p, blocks, bp, smem, st)
-                  : RS <= 25 ? launch_dw_wgrad_band<1, 25>(p, blocks, bp, smem, st)
-                             : launch_dw_wgrad_band<1, 49>(p, blocks, bp, smem, st);
+    e = dt == 0 ? launch_dw_wgrad_band_any<0>(p, blocks, bp, smem, st)
+                : launch_dw_wgrad_band_any<1>(p, blocks, bp, smem, st);
   } else if (dt == 0) {
     dw_wgrad_kernel<0><<<blocks, 256, 0, st>>>(p);
   } else {

@@ -505,6 +505,7 @@ GROUP_GPU_CASES = [
     ((2, 8, 12, 12, 16, 3, 3, 2, 2, 1, 1), 8, (2, 2), False),    # depthwise, 2 outputs per channel, dilation 2
     ((1, 5, 7, 9, 10, 3, 2, 1, 0, 2, 1), 5, (1, 1), True),       # depthwise x2, R != S, stride 2 x 1
     ((2, 4, 1, 20000, 4, 1, 5, 0, 2, 1, 1), 4, (1, 1), False),   # depthwise 1-D, rows too wide to stage
+    ((2, 6, 20, 18, 6, 7, 7, 3, 3, 1, 1), 6, (1, 1), True),      # depthwise 7x7
 ]
 
 
