@@ -3,7 +3,13 @@
 // convolution whose groups each have one input channel (Apache MXNet mkldnn_deconvolution.cc,
 // DeconvDescCreator: num_group; the grouped filter is K x C/groups x R x S); its GEMM view has
 // N = K / C columns per group, far too narrow for the tensor cores, and the layer is memory
-// bound, so each output element is one thread's fixed-order sum over its taps.
+// bound.  A block takes units of one plane's band of rows: it stages the band's zero-padded
+// input window in shared memory (eight loads in flight per thread), then each output element is
+// one thread's fixed-order fp32 sum over its taps (forward, backward-data at unit stride), or
+// each thread keeps every tap's running sum of x * dy in registers (filter gradient, reduced per
+// block and then over image splits in a fixed order).  3x3, 5x5 and 7x7 filters are compiled
+// with their taps and band offsets in registers; rows too wide to stage and strided
+// backward-data read global memory directly.
 #include <cuda_bf16.h>
 
 #include <algorithm>
@@ -83,6 +89,7 @@ __device__ __forceinline__ void stage_window(float* dst, const void* src, int nr
 }  // namespace
 
 constexpr int kDwTile = 1024;  // output positions of one plane per work unit (4 per thread)
+constexpr int kDwRun = 4;      // consecutive outputs of a row per thread (staged 3x3 / 5x5 / 7x7)
 constexpr int kDwSmem = 16 * 1024;  // bytes of one staged input band (fp32)
 
 // Rows of a forward unit's band (band_rows(p) output rows of one plane) and the staged input
@@ -141,6 +148,39 @@ __global__ void __launch_bounds__(256) dw_fwd_kernel(const __grid_constant__ DwP
           toff[r * ST + s] = r * p.dh * wt + s * p.dw;
         }
       const float bv = p.bias != nullptr ? ld<DT>(p.bias, k) : 0.f;
+      if (p.sw == 1 && p.dw == 1) {
+        // kDwRun consecutive outputs of a row per thread: each band row's kDwRun + ST - 1 inputs
+        // are read once for all of them (the reads past a row's end, at most kDwRun - 1 into the
+        // next row or the band's padding, only feed outputs past Q, which are not stored)
+        const int nq = (p.Q + kDwRun - 1) / kDwRun;
+        for (int it = (int)threadIdx.x; it < np * nq; it += (int)blockDim.x) {
+          const int pp = it / nq, q0 = (it - pp * nq) * kDwRun;
+          float acc[kDwRun];
+#pragma unroll
+          for (int j = 0; j < kDwRun; ++j) acc[j] = 0.f;
+#pragma unroll
+          for (int r = 0; r < RT; ++r) {
+            const float* row = band + (pp * p.sh + r * p.dh) * wt + q0;
+            float v[kDwRun + ST - 1];
+#pragma unroll
+            for (int i = 0; i < kDwRun + ST - 1; ++i) v[i] = row[i];
+#pragma unroll
+            for (int ss = 0; ss < ST; ++ss)
+#pragma unroll
+              for (int j = 0; j < kDwRun; ++j) acc[j] = fmaf(v[j + ss], tv[r * ST + ss], acc[j]);
+          }
+#pragma unroll
+          for (int j = 0; j < kDwRun; ++j) {
+            if (q0 + j < p.Q) {
+              const long long o = yb + (long long)pp * p.Q + q0 + j;
+              float a = acc[j] + bv;
+              if (p.beta != 0.f) a += p.beta * ld_rw<DT>(p.out, o);
+              st<DT>(p.out, o, a);
+            }
+          }
+        }
+        continue;
+      }
       for (int o = (int)threadIdx.x; o < np * p.Q; o += (int)blockDim.x) {
         const int pp = o / p.Q, q = o - pp * p.Q;
         const float* src = band + pp * p.sh * wt + q * p.sw;
@@ -309,6 +349,38 @@ __global__ void __launch_bounds__(256) dw_bwd_data_s1_kernel(const __grid_consta
             toff[r * ST + s] = -(r * p.dh) * wt - s * p.dw;
           }
         const float bv = p.bias != nullptr ? ld<DT>(p.bias, c) : 0.f;
+        if (p.dw == 1) {
+          // kDwRun consecutive dx elements of a row per thread (as the forward does): output
+          // w0 + j, tap s reads staged column w0 + j + ST - 1 - s
+          const int nw = (p.W + kDwRun - 1) / kDwRun;
+          for (int it = (int)threadIdx.x; it < nh * nw; it += (int)blockDim.x) {
+            const int hh = it / nw, w0 = (it - hh * nw) * kDwRun;
+            float acc[kDwRun];
+#pragma unroll
+            for (int j = 0; j < kDwRun; ++j) acc[j] = 0.f;
+#pragma unroll
+            for (int r = 0; r < RT; ++r) {
+              const float* row = band + (hh + (RT - 1 - r) * p.dh) * wt + w0;
+              float v[kDwRun + ST - 1];
+#pragma unroll
+              for (int i = 0; i < kDwRun + ST - 1; ++i) v[i] = row[i];
+#pragma unroll
+              for (int ss = 0; ss < ST; ++ss)
+#pragma unroll
+                for (int j = 0; j < kDwRun; ++j) acc[j] = fmaf(v[j + ST - 1 - ss], tv[r * ST + ss], acc[j]);
+            }
+#pragma unroll
+            for (int j = 0; j < kDwRun; ++j) {
+              if (w0 + j < p.W) {
+                const long long o = ob + (long long)hh * p.W + w0 + j;
+                float a = acc[j] + bv;
+                if (p.beta != 0.f) a += p.beta * ld_rw<DT>(p.out, o);
+                st<DT>(p.out, o, a);
+              }
+            }
+          }
+          continue;
+        }
         for (int o = (int)threadIdx.x; o < nh * p.W; o += (int)blockDim.x) {
           const int hh = o / p.W, w = o - hh * p.W;
           const float* bm = band + (hh + (RT - 1) * p.dh) * wt + w + (ST - 1) * p.dw;
@@ -410,6 +482,29 @@ __global__ void __launch_bounds__(256) dw_wgrad_band_kernel(const __grid_constan
       });
       __syncthreads();
       if constexpr (RT > 0 && ST > 0) {  // RSM == RT * ST: every tap's offset in a register
+        if (p.sw == 1 && p.dw == 1) {
+          // kDwRun consecutive outputs of a row per thread: each band row's kDwRun + ST - 1 inputs
+          // read once (columns past the row's end read as 0; outputs past Q carry dy = 0)
+          const int nq = (p.Q + kDwRun - 1) / kDwRun;
+          for (int it = (int)threadIdx.x; it < np * nq; it += (int)blockDim.x) {
+            const int pp = it / nq, q0 = (it - pp * nq) * kDwRun;
+            float g[kDwRun];
+#pragma unroll
+            for (int j = 0; j < kDwRun; ++j) g[j] = q0 + j < p.Q ? dyb[pp * p.Q + q0 + j] : 0.f;
+#pragma unroll
+            for (int r = 0; r < RT; ++r) {
+              const float* row = band + (pp * p.sh + r * p.dh) * wt + q0;
+              float v[kDwRun + ST - 1];
+#pragma unroll
+              for (int i = 0; i < kDwRun + ST - 1; ++i) v[i] = q0 + i < wt ? row[i] : 0.f;
+#pragma unroll
+              for (int ss = 0; ss < ST; ++ss)
+#pragma unroll
+                for (int j = 0; j < kDwRun; ++j) acc[r * ST + ss] = fmaf(v[j + ss], g[j], acc[r * ST + ss]);
+            }
+          }
+          continue;
+        }
         int toff[RT * ST];
 #pragma unroll
         for (int r = 0; r < RT; ++r)
@@ -506,7 +601,8 @@ static unsigned dw_grid(long long total, int num_sms) {
 
 size_t dw_fwd_smem_bytes(const DwPlan& p) {
   const int bp = dw_fwd_band(p);
-  return ((size_t)((p.R * p.S + 3) & ~3) + (size_t)dw_fwd_in_rows(p, bp) * dw_fwd_wt(p)) * sizeof(float);
+  // + kDwRun: the reads of a row's last run past the band's end
+  return ((size_t)((p.R * p.S + 3) & ~3) + (size_t)dw_fwd_in_rows(p, bp) * dw_fwd_wt(p) + kDwRun) * sizeof(float);
 }
 
 cudaError_t launch_dw_fwd(const DwPlan& p, int dt, int num_sms, cudaStream_t st) {
@@ -528,7 +624,8 @@ cudaError_t launch_dw_fwd(const DwPlan& p, int dt, int num_sms, cudaStream_t st)
 
 size_t dw_bd_smem_bytes(const DwPlan& p) {
   const int bh = dw_bd_band(p);
-  return ((size_t)((p.M * p.R * p.S + 3) & ~3) + (size_t)p.M * dw_bd_rows(p, bh) * dw_bd_wt(p)) * sizeof(float);
+  return ((size_t)((p.M * p.R * p.S + 3) & ~3) + (size_t)p.M * dw_bd_rows(p, bh) * dw_bd_wt(p) + kDwRun) *
+         sizeof(float);
 }
 
 cudaError_t launch_dw_bwd_data(const DwPlan& p, int dt, int num_sms, cudaStream_t st) {
