@@ -211,7 +211,27 @@ __device__ __forceinline__ void pack_filter_one(const PackPlan& pp, uint32_t idx
   }
   uint32_t out[4] = {0u, 0u, 0u, 0u};
   const int cs0 = kb * pp.CB + j * CHUNK;
-  if (nn < pp.Cd && r >= 0) {
+  if (nn < pp.Cd && r >= 0 && pp.gd != 0) {  // block-diagonal: the group's slice of the filter
+    const int g = nn / pp.gd, nl = nn - g * pp.gd;
+    E v[CHUNK];
+#pragma unroll
+    for (int e = 0; e < CHUNK; ++e) {
+      const int cs = cs0 + e;
+      const bool in = cs < pp.Cs && cs / pp.gs == g;
+      const long long idx = pp.transpose ? ((long long)cs * pp.C + nl) * RS : ((long long)nn * pp.C + (cs - g * pp.gs)) * RS;
+      v[e] = in ? static_cast<const E*>(pp.w)[idx + r * pp.S + s] : (E)0;
+    }
+#pragma unroll
+    for (int e = 0; e < CHUNK; ++e) {
+      if constexpr (DT == 0) {
+        uint32_t tf;
+        asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(tf) : "f"(__uint_as_float(v[e])));
+        out[e] = tf;
+      } else {
+        out[e >> 1] |= (uint32_t)v[e] << (16 * (e & 1));
+      }
+    }
+  } else if (nn < pp.Cd && r >= 0) {
     const E* src = static_cast<const E*>(pp.w) +
                    (pp.transpose ? ((long long)cs0 * pp.C + nn) * RS : ((long long)nn * pp.C + cs0) * RS) + r * pp.S + s;
     const long long estep = pp.transpose ? (long long)pp.C * RS : RS;  // next source channel

@@ -121,6 +121,10 @@ struct PackPlan {
   int NT, CB;
   int tap_r[kMaxTaps], tap_s[kMaxTaps];
   int flip;               // convolution mode: tap (r, s) reads w[.., R-1-r, S-1-s]
+  // Grouped filter packed block-diagonally (gd != 0): gs source and gd out channels per group;
+  // an element whose source and out channel lie in different groups is zero, and C is the
+  // filter's channels per group.
+  int gs, gd;
 };
 
 // Backward-filter as one implicit GEMM per tile:
