@@ -108,6 +108,12 @@ const uint8_t* byte_ptr(const void* p) { return static_cast<const uint8_t*>(p); 
 // Depthwise layers (groups > 1 with one input channel per group) run the direct kernels of
 // conv_depthwise.cu (DwPlan) instead of one tap-GEMM pass per group.
 bool is_depthwise(const Desc& dg) { return dg.g > 1 && dg.C == 1; }
+// Grouped layers (other than depthwise) whose forward and backward-data run as one pass over the
+// whole tensors with a block-diagonally packed filter (run_tap); fp32 backward-data over 8 or
+// fewer channels in all keeps the few-channel kernel per group.
+bool blockdiag_groups(int op, const Desc& whole, int groups) {
+  return groups >= 2 && (op == CONV2D_OP_FWD || whole.C > 8 || whole.dt != CONV2D_DTYPE_F32);
+}
 
 // The depthwise plan of a whole grouped problem (d: the totals; dg: its per-group descriptor);
 // pointers, bias, beta and mode are set by the caller.  The filter gradient's splits are ranges
@@ -1880,27 +1886,29 @@ int workspace_size_uncached(int op, const Desc& d, size_t* bytes) {
     *bytes = std::max({a, b, f.fused ? f.need : size_t(0)});
     return CONV2D_OK;
   }
-  if (op == CONV2D_OP_BWD_DATA) {
+  if (op == CONV2D_OP_FWD || op == CONV2D_OP_BWD_DATA) {  // the choices of run_tap, in its order
+    Desc t = d;
+    t.C = d.g * d.C;
+    t.K = d.g * d.K;
+    t.g = 1;
+    if (blockdiag_groups(op, t, d.g)) {  // the block-diagonal single pass over the whole tensors
+      TapSet whole, per;
+      if (build_tap_set(op, t, nullptr, nullptr, nullptr, nullptr, di, whole, true) == CONV2D_OK) {
+        // (and room for the per-group passes, should the call's pointers not plan whole)
+        const bool per_ok = build_tap_set(op, d, nullptr, nullptr, nullptr, nullptr, di, per, true) == CONV2D_OK;
+        *bytes = std::max(whole.pack_bytes, per_ok ? per.pack_bytes : size_t(0));
+        return CONV2D_OK;
+      }
+    }
     C2iPlan cp;
-    if (build_c2i(d, nullptr, nullptr, nullptr, di, cp) == CONV2D_OK) {
+    if (op == CONV2D_OP_BWD_DATA && build_c2i(d, nullptr, nullptr, nullptr, di, cp) == CONV2D_OK) {
       *bytes = 0;
       return CONV2D_OK;
     }
-  }
-  if (op == CONV2D_OP_FWD || op == CONV2D_OP_BWD_DATA) {
     TapSet set;
     rc = build_tap_set(op, d, nullptr, nullptr, nullptr, nullptr, di, set, true);
     if (rc) return rc;
     *bytes = set.pack_bytes;
-    if (d.g == 2) {  // the block-diagonal single pass over the whole tensors (run_tap)
-      Desc t = d;
-      t.C = 2 * d.C;
-      t.K = 2 * d.K;
-      t.g = 1;
-      TapSet whole;
-      if (build_tap_set(op, t, nullptr, nullptr, nullptr, nullptr, di, whole, true) == CONV2D_OK)
-        *bytes = std::max(*bytes, whole.pack_bytes);
-    }
     return CONV2D_OK;
   }
   if (op == CONV2D_OP_BWD_FILTER) {
@@ -1970,7 +1978,25 @@ static int run_tap(int op, const Desc& d, int groups, const void* src, const voi
     dp.flip = mode == CONV2D_MODE_CONVOLUTION ? 1 : 0;
     return launch_err(fwd ? launch_dw_fwd(dp, d.dt, di.sms, st) : launch_dw_bwd_data(dp, d.dt, di.sms, st));
   }
-  if (!fwd) {  // few input channels: the scatter-form kernel (no workspace)
+  TapSet set;
+  // Grouped layers: one pass over the whole tensors with the filter packed block-diagonally (zero
+  // between channels of different groups) when that plans.  It costs the ungrouped op whatever
+  // the group count (groups times the grouped multiply-adds, at the ungrouped tile width, one set
+  // of packs, fills and epilogues); one pass per group costs groups times a pass whose tile is
+  // only K/groups wide.  Measured on the ResNet 3x3 layer (ungrouped 30 us): one pass per group
+  // 41 / 55 / 113 / 236 us forward at 2 / 4 / 8 / 16 groups, block-diagonal 29-30 us; the
+  // deconvolution layer at 4 groups 69 -> 52 us forward, 69 -> 55 us backward-data (at 2 groups
+  // 57 -> 52 forward, 55 -> 57 backward-data).
+  bool blockdiag = false;
+  if (blockdiag_groups(op, d, groups)) {
+    const PlanKey bkey = make_key(op, d, src, w, dst, ws);
+    blockdiag = g_tap_plans.get(bkey, set);
+    if (!blockdiag && build_tap_set(op, d, src, w, dst, ws, di, set, true) == CONV2D_OK) {
+      g_tap_plans.put(bkey, set);
+      blockdiag = true;
+    }
+  }
+  if (!fwd && !blockdiag) {  // few input channels: the scatter-form kernel (no workspace)
     C2iPlan cp;
     const PlanKey ckey = make_key(op, dg, nullptr, nullptr, nullptr, nullptr);
     bool have = g_c2i_plans.get(ckey, cp);
@@ -1992,22 +2018,6 @@ static int run_tap(int op, const Desc& d, int groups, const void* src, const voi
         if (rc) return rc;
       }
       return CONV2D_OK;
-    }
-  }
-  TapSet set;
-  // Two groups: one pass over the whole tensors with the filter packed block-diagonally (zero
-  // between channels of different groups) when that plans: twice the groups' multiply-adds, at
-  // the ungrouped tile width and without a second set of packs, fills and epilogues.  Measured:
-  // the ResNet 3x3 layer 41 -> 29 us per op (a group alone sets an N = 32 tile whose MMAs the
-  // single issuing thread paces); the deconvolution layer's forward 57 -> 53 us, its
-  // backward-data 55 -> 57 us.
-  bool blockdiag = false;
-  if (groups == 2) {
-    const PlanKey bkey = make_key(op, d, src, w, dst, ws);
-    blockdiag = g_tap_plans.get(bkey, set);
-    if (!blockdiag && build_tap_set(op, d, src, w, dst, ws, di, set, true) == CONV2D_OK) {
-      g_tap_plans.put(bkey, set);
-      blockdiag = true;
     }
   }
   if (!blockdiag) {

@@ -502,6 +502,7 @@ GROUP_GPU_CASES = [
     ((2, 64, 16, 16, 64, 3, 3, 1, 1, 1, 1), 2, (1, 1), False),    # copy-engine staging per group
     ((2, 8, 13, 11, 6, 3, 3, 2, 2, 1, 2), 2, (2, 1), True),
     ((2, 36, 14, 15, 20, 3, 3, 1, 1, 2, 2), 2, (1, 1), False),  # two groups of 18: chunks straddle the groups
+    ((2, 32, 12, 13, 48, 3, 3, 1, 1, 1, 1), 4, (1, 1), True),   # four groups of 8 -> 12
     ((2, 24, 15, 13, 24, 5, 5, 2, 2, 2, 2), 24, (1, 1), False),  # depthwise 5x5, stride 2
     ((2, 8, 12, 12, 16, 3, 3, 2, 2, 1, 1), 8, (2, 2), False),    # depthwise, 2 outputs per channel, dilation 2
     ((1, 5, 7, 9, 10, 3, 2, 1, 0, 2, 1), 5, (1, 1), True),       # depthwise x2, R != S, stride 2 x 1
