@@ -1041,6 +1041,7 @@ int build_bwd_filter_impl(const Desc& d0, const void* x, const void* dy, void* d
   rp.S_out = d.S;
   rp.r0 = rp.s0 = 0;
   rp.rstep = rp.sstep = 1;
+  rp.gk = rp.gc = 0;
   b.grid = (int)std::min<long long>(p.total_tiles, di.sms);
   return CONV2D_OK;
 }
@@ -1933,6 +1934,21 @@ int workspace_size_uncached(int op, const Desc& d, size_t* bytes) {
       if (build_bwd_filter_impl(d, nullptr, nullptr, nullptr, nullptr, di, b2, v[0], v[1]) == CONV2D_OK)
         need = std::max(need, b2.partial_bytes);
     }
+    if (d.g > 1) {  // grouped: the one pass over the whole tensors (conv2d_bwd_filter_ex)
+      Desc t = d;
+      t.C = d.g * d.C;
+      t.K = d.g * d.K;
+      t.g = 1;
+      WgradBuild w1;
+      if (build_bwd_filter(t, nullptr, nullptr, nullptr, nullptr, di, w1) == CONV2D_OK) {
+        need = std::max(need, w1.partial_bytes);
+        for (const auto& v : kWgradVariants) {
+          WgradBuild b2;
+          if (build_bwd_filter_impl(t, nullptr, nullptr, nullptr, nullptr, di, b2, v[0], v[1]) == CONV2D_OK)
+            need = std::max(need, b2.partial_bytes);
+        }
+      }
+    }
     *bytes = std::max(phased, align_ws(need) + chan_sum_bytes(d));
     return CONV2D_OK;
   }
@@ -2279,6 +2295,32 @@ int conv2d_bwd_filter_ex(int N, int C, int H, int W, int K, int R, int S, int pa
           if (rc) return rc;
         }
       sum0 = L.xs_bytes + align_ws(partial);
+      phases_run = true;
+    }
+  }
+  // Grouped layers: one split-K pass over the whole tensors whose reduce keeps only the diagonal
+  // blocks of the full K x C gradient (the ungrouped op's cost whatever the group count, against
+  // groups passes whose GEMMs are only K/groups wide).
+  if (!phases_run && groups > 1) {
+    WgradBuild b;
+    const PlanKey key = make_key(CONV2D_OP_BWD_FILTER, d, x, dy, dw, workspace);
+    bool have = g_wgrad_plans.get(key, b);
+    if (!have && build_bwd_filter(d, x, dy, dw, workspace, di, b) == CONV2D_OK) {
+      g_wgrad_plans.put(key, b);
+      have = true;
+    }
+    if (have) {
+      rc = check_ws(workspace, workspace_bytes, sums ? align_ws(b.partial_bytes) + chan_sum_bytes(d) : b.partial_bytes);
+      if (rc) return rc;
+      b.rp.beta = beta;  // per-call (not part of the cached plan)
+      b.rp.flip = mode == CONV2D_MODE_CONVOLUTION ? 1 : 0;
+      b.rp.gk = dg.K;
+      b.rp.gc = dg.C;
+      rc = launch_err(launch_wgrad(b.p, d.dt, b.grid, st));
+      if (rc) return rc;
+      rc = launch_err(launch_wgrad_reduce(b.rp, d.dt, di.sms, st));
+      if (rc) return rc;
+      sum0 = align_ws(b.partial_bytes);
       phases_run = true;
     }
   }

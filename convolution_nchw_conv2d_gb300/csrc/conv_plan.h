@@ -240,6 +240,9 @@ struct ReducePlan {
   // Placement of partial tap (r', s') in dw: (r0 + rstep * r', s0 + sstep * s') of an
   // R_out x S_out filter (one stride phase of a strided filter; the identity otherwise).
   int R_out, S_out, r0, s0, rstep, sstep;
+  // Grouped filter from the whole problem's partials (gk != 0): gk output and gc input channels
+  // per group; only the diagonal blocks (c / gc == k / gk) are kept, dw is K x gc x R_out x S_out.
+  int gk, gc;
 };
 
 // Channel-chunked, zero-padded planes of an NCHW tensor ("NHWC within chunks"):

@@ -1072,7 +1072,14 @@ __global__ void __launch_bounds__(32 * kReduceWarps) wgrad_reduce_kernel(const _
           rr = rp.R_out - 1 - rr;
           ss = rp.S_out - 1 - ss;
         }
-        const long long o = (((long long)k * rp.C + c) * rp.R_out + rr) * rp.S_out + ss;
+        int cw = c, cn = rp.C;
+        if (rp.gk != 0) {  // grouped: keep the diagonal block of k's group
+          const int g = k / rp.gk;
+          if (c / rp.gc != g) continue;
+          cw = c - g * rp.gc;
+          cn = rp.gc;
+        }
+        const long long o = (((long long)k * cn + cw) * rp.R_out + rr) * rp.S_out + ss;
         if constexpr (DT == 0) {
           float* dwp = static_cast<float*>(rp.dw);
           if (rp.beta != 0.f) sum += rp.beta * dwp[o];
