@@ -1919,6 +1919,15 @@ int workspace_size_uncached(int op, const Desc& d, size_t* bytes) {
       MnBuild mb;
       if (build_wgrad_mn(d, nullptr, nullptr, nullptr, nullptr, di, mb) == CONV2D_OK)
         mn = mn_ws_bytes(mb) + chan_sum_bytes(d);
+      if (d.g > 1) {  // grouped: the one pass over the whole tensors (conv2d_bwd_filter_ex)
+        Desc t = d;
+        t.C = d.g * d.C;
+        t.K = d.g * d.K;
+        t.g = 1;
+        MnBuild mw;
+        if (build_wgrad_mn(t, nullptr, nullptr, nullptr, nullptr, di, mw) == CONV2D_OK)
+          mn = std::max(mn, mn_ws_bytes(mw) + chan_sum_bytes(d));
+      }
     }
     // Strided filters run as stride phases when every phase plans (else as one problem);
     // size for either.
@@ -2219,8 +2228,19 @@ int conv2d_bwd_filter_ex(int N, int C, int H, int W, int K, int R, int S, int pa
   // each group packs its own slices into the workspace in stream order.
   if (!phases_run && d.dt == CONV2D_DTYPE_BF16 && workspace != nullptr) {
     MnBuild mb;
+    // Grouped: first the whole tensors in one pass (the full K x C gradient; the reduce keeps
+    // the diagonal blocks), else one pass per group.
+    bool whole = false;
+    if (groups > 1) {
+      const PlanKey wkey = make_key(kMnKey, d, nullptr, nullptr, nullptr, workspace);
+      whole = g_mn_plans.get(wkey, mb);
+      if (!whole && build_wgrad_mn(d, x, dy, dw, workspace, di, mb) == CONV2D_OK) {
+        g_mn_plans.put(wkey, mb);
+        whole = true;
+      }
+    }
     const PlanKey key = make_key(kMnKey, dg, nullptr, nullptr, nullptr, workspace);
-    bool have = g_mn_plans.get(key, mb);
+    bool have = whole || g_mn_plans.get(key, mb);
     if (!have) {
       rc = build_wgrad_mn(dg, x, dy, dw, workspace, di, mb);
       if (rc == CONV2D_OK) {
@@ -2233,7 +2253,9 @@ int conv2d_bwd_filter_ex(int N, int C, int H, int W, int K, int R, int S, int pa
     if (have) {
       rc = check_ws(workspace, workspace_bytes, mn_ws_bytes(mb) + (sums ? chan_sum_bytes(d) : 0));
       if (rc) return rc;
-      for (int gi = 0; gi < groups; ++gi) {
+      mb.rp.gk = whole ? dg.K : 0;
+      mb.rp.gc = whole ? dg.C : 0;
+      for (int gi = 0; gi < (whole ? 1 : groups); ++gi) {
         mb.px.src = byte_ptr(x) + gi * (size_t)dg.C * dg.H * dg.W * esz;
         mb.pd.src = byte_ptr(dy) + gi * (size_t)dg.K * dg.P * dg.Q * esz;
         mb.rp.dw = const_cast<uint8_t*>(byte_ptr(dw)) + gi * (size_t)dg.K * dg.C * dg.R * dg.S * esz;

@@ -228,6 +228,9 @@ struct ReduceTPlan {
   int rows, K, RS, nsplit;
   float beta;
   int flip;
+  // Grouped filter from the whole problem's partials (gk != 0): gk output and gc input channels
+  // per group; only the diagonal blocks (c / gc == k / gk) are kept, dw is K x gc x R x S.
+  int gk, gc;
 };
 
 struct ReducePlan {

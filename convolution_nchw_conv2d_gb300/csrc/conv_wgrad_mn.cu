@@ -146,7 +146,12 @@ __global__ void __launch_bounds__(256) wgrad_reduce_t_kernel(const __grid_consta
         const int c = row / rp.RS;
         orow = c * rp.RS + (rp.RS - 1 - (row - c * rp.RS));
       }
-      const long long o = (long long)kg * rp.rows + orow;
+      long long o = (long long)kg * rp.rows + orow;
+      if (rp.gk != 0) {  // grouped: keep the diagonal block of k's group
+        const int g = kg / rp.gk;
+        if (row / rp.RS / rp.gc != g) continue;
+        o = ((long long)kg * rp.gc - (long long)g * rp.gc) * rp.RS + orow;
+      }
       if constexpr (DT == 0) {
         float* dwp = static_cast<float*>(rp.dw);
         if (rp.beta != 0.f) v += rp.beta * dwp[o];
