@@ -98,7 +98,7 @@ __global__ void __launch_bounds__(256) nhwc_pack_kernel(const __grid_constant__ 
 // split order, the 4 consecutive k (one 16-byte read per split: a warp reads 512 contiguous
 // bytes of a row) of rows w, w + 8, w + 16, w + 24; the tile is transposed through shared memory
 // and each warp writes runs of 32 consecutive dw elements (rows) per k.  K % 4 == 0.
-template <int DT>
+template <int DT, bool GRP>  // GRP: rp.gk != 0 (grouped: diagonal blocks only)
 __global__ void __launch_bounds__(256) wgrad_reduce_t_kernel(const __grid_constant__ ReduceTPlan rp) {
   __shared__ float tile[32][129];
   griddep_wait();  // the partials are written by the previous grid
@@ -147,7 +147,7 @@ __global__ void __launch_bounds__(256) wgrad_reduce_t_kernel(const __grid_consta
         orow = c * rp.RS + (rp.RS - 1 - (row - c * rp.RS));
       }
       long long o = (long long)kg * rp.rows + orow;
-      if (rp.gk != 0) {  // grouped: keep the diagonal block of k's group
+      if constexpr (GRP) {  // grouped: keep the diagonal block of k's group
         const int g = kg / rp.gk;
         if (row / rp.RS / rp.gc != g) continue;
         o = ((long long)kg * rp.gc - (long long)g * rp.gc) * rp.RS + orow;
@@ -431,8 +431,11 @@ cudaError_t launch_wgrad_reduce_t(const ReduceTPlan& rp, int dt, int num_sms, cu
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  const cudaError_t e = dt == 0 ? cudaLaunchKernelEx(&cfg, wgrad_reduce_t_kernel<0>, rp)
-                                : cudaLaunchKernelEx(&cfg, wgrad_reduce_t_kernel<1>, rp);
+  const bool grp = rp.gk != 0;
+  const cudaError_t e = dt == 0 ? (grp ? cudaLaunchKernelEx(&cfg, wgrad_reduce_t_kernel<0, true>, rp)
+                                       : cudaLaunchKernelEx(&cfg, wgrad_reduce_t_kernel<0, false>, rp))
+                                : (grp ? cudaLaunchKernelEx(&cfg, wgrad_reduce_t_kernel<1, true>, rp)
+                                       : cudaLaunchKernelEx(&cfg, wgrad_reduce_t_kernel<1, false>, rp));
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 

@@ -781,6 +781,7 @@ FC_CASES = [
     ((1, 2, 16, 36, 9, 3, 3, 2, 2, 1, 1), (2, 2), 1, False, True),
     ((1, 2, 12, 16, 128, 3, 3, 1, 1, 1, 1), (1, 1), 1, False, False),
     ((2, 8, 12, 16, 12, 3, 3, 1, 1, 1, 1), (1, 1), 2, True, False),
+    ((1, 16, 14, 18, 24, 3, 3, 1, 1, 1, 1), (1, 1), 4, True, True),   # four groups, add-to: diagonal blocks only
     ((1, 1, 9, 140, 5, 1, 5, 0, 2, 1, 1), (1, 1), 1, False, True),
     ((3, 3, 64, 64, 64, 7, 7, 3, 3, 2, 2), (1, 1), 1, False, False),
 ]
